@@ -1,0 +1,378 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each test checks the oracle against one of: the tables and identities the pages
+print (golden files under tests/golden/, each citing its passage), exact closed
+forms evaluated with rational arithmetic, mathematical invariants, brute force
+on tiny inputs written independently in numpy / plain Python, or special cases
+that reduce to a textbook SwiGLU FFN.  They are chosen so that a plausible slip
+in the oracle (nibble order, sign bit, magnitude order, exponent bias, block
+index, tie-break, renormalisation, permutation stability, gate/up swap, a
+dropped shared expert, a dropped slice) fails at least one of them.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from mxfp4_routed_expert_router_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def load_e2m1_table():
+    table = {}
+    with open(os.path.join(GOLDEN, "e2m1_table.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            c, v = line.split()
+            table[int(c)] = float(v)
+    assert sorted(table) == list(range(16))
+    return table
+
+
+E2M1 = load_e2m1_table()
+
+
+def exact_decode(code, e):
+    """v(c) * 2^(e-127) from the golden table with exact rational arithmetic."""
+    v = Fraction(E2M1[code])
+    val = float(v * Fraction(2) ** (e - 127))
+    return math.copysign(val, E2M1[code]) if val == 0 else val
+
+
+def np_decode_golden(codes, scales):
+    """Independent numpy decode of an MXFP4 matrix via the golden table."""
+    tab = np.array([E2M1[c] for c in range(16)], np.float64)
+    lo = codes & 0xF
+    hi = codes >> 4
+    c = np.stack([lo, hi], axis=-1).reshape(codes.shape[0], -1)
+    v = tab[c]
+    s = np.repeat(scales.astype(np.int64), 32, axis=1)
+    return np.ldexp(v, s - 127)
+
+
+# ------------------------------------------------------------------ decode pins
+
+@pytest.mark.parametrize("e", [0, 1, 2, 120, 126, 127, 128, 130, 200, 252])
+def test_e2m1_table_all_codes(e):
+    for code in range(16):
+        got = oracle.mx_value(code, e)
+        want = exact_decode(code, e)
+        assert got == want and math.copysign(1, got) == math.copysign(1, want), (code, e, got, want)
+
+
+def test_e2m1_value_table():
+    for code in range(16):
+        got = oracle.e2m1_value(code)
+        assert got == E2M1[code] and math.copysign(1, got) == math.copysign(1, E2M1[code])
+
+
+def test_e8m0_zero_is_subnormal_not_zero():
+    # 0.5 * 2^-127 = 2^-128 is a float32 subnormal; it must not flush to zero.
+    assert oracle.mx_value(1, 0) == 2.0 ** -128
+    assert oracle.mx_value(7, 0) == 6 * 2.0 ** -127
+
+
+def test_nibble_order_low_is_even():
+    codes = np.zeros((1, 16), np.uint8)
+    codes[0, 0] = 0x21          # element 0 = code 1 (0.5), element 1 = code 2 (1.0)
+    codes[0, 5] = 0xF0          # element 10 = code 0, element 11 = code 15 (-6)
+    out = oracle.mx_decode(codes, np.full((1, 1), 127, np.uint8))
+    assert out[0, 0] == 0.5 and out[0, 1] == 1.0
+    assert out[0, 10] == 0.0 and out[0, 11] == -6.0
+    assert np.count_nonzero(out) == 3
+
+
+def test_block_index_is_floor_k_over_32():
+    codes = np.full((1, 48), 0x22, np.uint8)  # every element code 2 = 1.0
+    scales = np.array([[127, 128, 125]], np.uint8)
+    out = oracle.mx_decode(codes, scales)
+    assert np.all(out[0, :32] == 1.0)
+    assert np.all(out[0, 32:64] == 2.0)
+    assert np.all(out[0, 64:] == 0.25)
+
+
+def test_decode_matches_independent_numpy_random():
+    rng = np.random.default_rng(5)
+    codes = rng.integers(0, 256, (7, 64), dtype=np.uint8)
+    scales = rng.integers(0, 255, (7, 4), dtype=np.uint8)
+    got = oracle.mx_decode(codes, scales).astype(np.float64)
+    want = np_decode_golden(codes, scales).astype(np.float32).astype(np.float64)
+    np.testing.assert_array_equal(got, want)
+
+
+def test_scale_255_rejected():
+    with pytest.raises(ValueError):
+        oracle.mx_decode(np.zeros((1, 16), np.uint8), np.array([[255]], np.uint8))
+
+
+def test_size_identity_4_25_bits():
+    with open(os.path.join(GOLDEN, "mxfp4_sizes.txt")) as f:
+        rows = [l.split() for l in f if l.strip() and not l.startswith("#")]
+    for r, c, b in rows:
+        r, c, b = int(r), int(c), int(b)
+        assert oracle.mx_bytes(r, c) == b
+        assert Fraction(8 * b, r * c) == Fraction(17, 4)
+    # one expert at H=7168, I=2048 and the decode working set of 9 experts
+    per_expert = oracle.mx_bytes(4096, 7168) + oracle.mx_bytes(7168, 2048)
+    assert per_expert == 23_396_352
+    assert 9 * per_expert == 210_567_168
+
+
+# ------------------------------------------------------------------ routing pins
+
+def brute_route(l, k):
+    """Plain-Python selection: larger first, equal (incl. +-0) by lower index, NaN last."""
+    E = len(l)
+    order = sorted(range(E), key=lambda e: (math.isnan(l[e]), 0.0 if math.isnan(l[e]) else -l[e], e))
+    return order[:k]
+
+
+def test_route_ties_and_signed_zero_brute_force():
+    rng = np.random.default_rng(11)
+    vals = np.array([0.0, -0.0, 1.0, -1.0, 0.5, 2.0, 2.0, -3.0], np.float32)
+    for trial in range(200):
+        E = int(rng.integers(1, 40))
+        k = int(rng.integers(1, E + 1))
+        l = rng.choice(vals, size=(1, E)).astype(np.float32)
+        ids, w = oracle.route(l, k)
+        assert ids[0].tolist() == brute_route(l[0].tolist(), k)
+
+
+def test_route_nan_ranks_last():
+    l = np.array([[np.nan, -np.inf, 0.0, np.nan, 1.0, -5.0]], np.float32)
+    ids, _ = oracle.route(l, 6)
+    assert ids[0].tolist() == [4, 2, 5, 1, 0, 3]
+
+
+def test_route_weights_invariants():
+    rng = np.random.default_rng(12)
+    l = rng.standard_normal((64, 256)).astype(np.float32)
+    ids, w = oracle.route(l, 8)
+    assert np.all(np.abs(w.sum(1) - 1.0) <= 1e-12)
+    assert np.all(np.diff(w, axis=1) <= 0)
+    # the ratio of two kept weights is exp of their logit difference
+    for t in range(64):
+        lt = l[t, ids[t]].astype(np.float64)
+        for j in range(1, 8):
+            assert math.isclose(w[t, 0] / w[t, j], math.exp(lt[0] - lt[j]), rel_tol=1e-12)
+    # k = 1 gives weight exactly 1
+    _, w1 = oracle.route(l, 1)
+    assert np.all(w1 == 1.0)
+
+
+def test_route_metamorphic_unselected_logits_do_not_matter():
+    rng = np.random.default_rng(13)
+    l = rng.standard_normal((32, 64)).astype(np.float32)
+    ids, w = oracle.route(l, 6)
+    l2 = l.copy()
+    for t in range(32):
+        kth = l[t, ids[t, -1]]
+        mask = np.ones(64, bool)
+        mask[ids[t]] = False
+        l2[t, mask] = np.minimum(l[t, mask], kth) - rng.uniform(0.01, 5.0, mask.sum()).astype(np.float32)
+    ids2, w2 = oracle.route(l2, 6)
+    np.testing.assert_array_equal(ids, ids2)
+    np.testing.assert_array_equal(w, w2)
+
+
+# ------------------------------------------------------------------ permutation pins
+
+def test_permute_against_python_stable_sort():
+    rng = np.random.default_rng(14)
+    for trial in range(20):
+        T, E = int(rng.integers(0, 50)), int(rng.integers(1, 20))
+        k = int(rng.integers(1, E + 1))
+        ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32).reshape(T, k)
+        off, ss, sp = oracle.permute(ids, E)
+        flat = ids.ravel().tolist()
+        want_ss = sorted(range(T * k), key=lambda s: flat[s])  # Python sort is stable
+        assert ss.tolist() == want_ss
+        counts = np.bincount(ids.ravel(), minlength=E)
+        assert off.tolist() == [0] + np.cumsum(counts).tolist()
+        assert np.all(sp[ss] == np.arange(T * k))
+
+
+# ------------------------------------------------------------------ expert / layer pins
+
+def silu(z):
+    return z / (1.0 + math.exp(-z))
+
+
+def onehot_mx(rows, cols, positions, code, e=127):
+    """MXFP4 matrix with a single nonzero code per row at positions[r]."""
+    codes = np.zeros((rows, cols // 2), np.uint8)
+    for r, c in enumerate(positions):
+        codes[r, c // 2] |= (code << 4) if c % 2 else code
+    return codes, np.full((rows, cols // 32), e, np.uint8)
+
+
+def test_onehot_expert_closed_form():
+    H, I = 64, 32
+    rng = np.random.default_rng(15)
+    a = rng.integers(0, H, I)
+    b = rng.integers(0, H, I)
+    dn = rng.integers(0, I, H)
+    gc, gs = onehot_mx(I, H, a, 2)          # gate row n = e_{a_n} (1.0)
+    uc, us = onehot_mx(I, H, b, 5, 128)     # up row n = 3 * 2 * e_{b_n}
+    gu_c = np.concatenate([gc, uc])
+    gu_s = np.concatenate([gs, us])
+    dc, ds = onehot_mx(H, I, dn, 12, 126)   # down row m = -2 * 0.5 * e_{dn_m}
+    W = oracle.OracleWeights(H, I, 1, 0)
+    W.set_expert(0, gu_c, gu_s, dc, ds)
+    x = wl.f32_to_bf16_bits(rng.standard_normal((3, H)).astype(np.float32))
+    xf = wl.bf16_bits_to_f32(x).astype(np.float64)
+    out, ids, w = oracle.moe_layer(W, x, np.zeros((3, 1), np.float32), 1)
+    assert np.all(ids == 0) and np.all(w == 1.0)
+    for t in range(3):
+        h = [silu(xf[t, a[n]]) * 6.0 * xf[t, b[n]] for n in range(I)]
+        want = [-1.0 * h[dn[m]] for m in range(H)]
+        np.testing.assert_allclose(out[t], want, rtol=1e-15, atol=0)
+
+
+def test_silu_known_values():
+    # x = e_0 with value 1 through a one-hot gate/up/down: out = silu(1) * 1
+    H, I = 32, 32
+    gc, gs = onehot_mx(I, H, [0] * I, 2)
+    dc, ds = onehot_mx(H, I, [0] * H, 2)
+    W = oracle.OracleWeights(H, I, 1, 0)
+    W.set_expert(0, np.concatenate([gc, gc]), np.concatenate([gs, gs]), dc, ds)
+    for xv, want in ((1.0, 0.7310585786300049), (0.0, 0.0), (-1.0, 0.2689414213699951)):
+        x = np.zeros((1, H), np.float32)
+        x[0, 0] = xv
+        out, _, _ = oracle.moe_layer(W, wl.f32_to_bf16_bits(x), np.zeros((1, 1), np.float32), 1)
+        # h = silu(x0) * x0; for x0 = -1 this is -silu(-1) = 0.2689...
+        assert math.isclose(out[0, 0], want, rel_tol=1e-15, abs_tol=1e-300)
+
+
+def numpy_layer(cfg, x_bits, logits, experts):
+    """Independent brute force: every expert on every token (numpy FP64), then select."""
+    H, I, E, S, k = cfg.hidden, cfg.inter, cfg.n_experts, cfg.n_shared, cfg.k
+    x = wl.bf16_bits_to_f32(x_bits).astype(np.float64)
+    Y = []
+    for e in range(E + S):
+        gc, gs, dc, ds = experts[e]
+        Wgu = np_decode_golden(gc, gs)
+        Wd = np_decode_golden(dc, ds)
+        g = x @ Wgu[:I].T
+        u = x @ Wgu[I:].T
+        h = g / (1.0 + np.exp(-g)) * u
+        Y.append(h @ Wd.T)
+    out = np.zeros((x.shape[0], H))
+    for t in range(x.shape[0]):
+        sel = brute_route(logits[t].tolist(), k)
+        lv = np.array([float(logits[t, e]) for e in sel])
+        p = np.exp(lv - lv.max())
+        p /= p.sum()
+        for j, e in enumerate(sel):
+            out[t] += p[j] * Y[e][t]
+        for s in range(S):
+            out[t] += Y[E + s][t]
+    return out
+
+
+@pytest.mark.parametrize("cfg", [wl.tiny(), wl.custom("tiny_shared", 12, 96, 64, 5, 1, 3, seed=7)],
+                         ids=lambda c: c.name)
+def test_layer_brute_force_tiny(cfg):
+    x = wl.tokens(cfg)
+    l = wl.router_logits(cfg)
+    experts = [wl.expert_weights(cfg, e) for e in range(cfg.n_groups)]
+    W = oracle.OracleWeights(cfg.hidden, cfg.inter, cfg.n_experts, cfg.n_shared)
+    for e, ws in enumerate(experts):
+        W.set_expert(e, *ws)
+    out, ids, w = oracle.moe_layer(W, x, l, cfg.k, nthreads=2)
+    want = numpy_layer(cfg, x, l, experts)
+    scale = np.sqrt(np.mean(want ** 2))
+    assert np.max(np.abs(out - want)) / scale <= 1e-12
+
+
+def test_layer_single_expert_is_textbook_swiglu():
+    cfg = wl.custom("e1", 5, 128, 96, 1, 0, 1, seed=8)
+    x = wl.tokens(cfg)
+    gc, gs, dc, ds = wl.expert_weights(cfg, 0)
+    W = oracle.OracleWeights(cfg.hidden, cfg.inter, 1, 0)
+    W.set_expert(0, gc, gs, dc, ds)
+    out, _, _ = oracle.moe_layer(W, x, wl.router_logits(cfg), 1)
+    Wgu = np_decode_golden(gc, gs)
+    Wd = np_decode_golden(dc, ds)
+    xf = wl.bf16_bits_to_f32(x).astype(np.float64)
+    g, u = xf @ Wgu[:96].T, xf @ Wgu[96:].T
+    want = (g / (1 + np.exp(-g)) * u) @ Wd.T
+    assert np.max(np.abs(out - want)) / np.sqrt(np.mean(want ** 2)) <= 1e-12
+    # the dense path on the same weights gives the same result
+    dense = oracle.dense_ffn(((gc[:96], gs[:96]), (gc[96:], gs[96:]), (dc, ds)), x, 0)
+    assert np.max(np.abs(dense - want)) / np.sqrt(np.mean(want ** 2)) <= 1e-12
+
+
+def test_layer_down_exponent_plus_one_doubles_exactly():
+    # Powers of two change exponents exactly ("Cascadia" §3.3): +1 on every
+    # down-projection E8M0 exponent doubles the output bit for bit.
+    cfg = wl.custom("dbl", 6, 64, 64, 4, 1, 2, seed=9)
+    x, l = wl.tokens(cfg), wl.router_logits(cfg)
+    W1 = oracle.OracleWeights(64, 64, 4, 1)
+    W2 = oracle.OracleWeights(64, 64, 4, 1)
+    for e in range(5):
+        gc, gs, dc, ds = wl.expert_weights(cfg, e)
+        W1.set_expert(e, gc, gs, dc, ds)
+        W2.set_expert(e, gc, gs, dc, ds + 1)
+    o1, _, _ = oracle.moe_layer(W1, x, l, 2)
+    o2, _, _ = oracle.moe_layer(W2, x, l, 2)
+    np.testing.assert_array_equal(o2, 2 * o1)
+
+
+def test_layer_shared_expert_is_added_with_unit_weight():
+    cfg = wl.custom("sh", 4, 64, 32, 3, 1, 1, seed=10)
+    x, l = wl.tokens(cfg), wl.router_logits(cfg)
+    ws = [wl.expert_weights(cfg, e) for e in range(4)]
+    with_s = oracle.OracleWeights(64, 32, 3, 1)
+    without = oracle.OracleWeights(64, 32, 3, 0)
+    only_s = oracle.OracleWeights(64, 32, 1, 0)
+    for e in range(3):
+        with_s.set_expert(e, *ws[e])
+        without.set_expert(e, *ws[e])
+    with_s.set_expert(3, *ws[3])
+    only_s.set_expert(0, *ws[3])
+    a, _, _ = oracle.moe_layer(with_s, x, l, 1)
+    b, _, _ = oracle.moe_layer(without, x, l, 1)
+    c, _, _ = oracle.moe_layer(only_s, x, np.zeros((4, 1), np.float32), 1)
+    np.testing.assert_allclose(a, b + c, rtol=1e-14, atol=1e-14 * np.abs(a).max())
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "bf16"])
+def test_dense_slices_equal_unsliced(fmt):
+    # Eq. (2) of "Cascadia" §3.4 with 4 slices of 32 over I = 128.
+    H, I = 64, 128
+    rng = np.random.default_rng(16)
+    if fmt == "bf16":
+        w = tuple(wl.f32_to_bf16_bits(rng.standard_normal(s).astype(np.float32) * 0.1)
+                  for s in ((I, H), (I, H), (H, I)))
+    else:
+        w = (wl.mx_matrix(rng, I, H, 120, 130), wl.mx_matrix(rng, I, H, 120, 130), wl.mx_matrix(rng, H, I, 120, 130))
+    x = wl.f32_to_bf16_bits(rng.standard_normal((3, H)).astype(np.float32))
+    full = oracle.dense_ffn(w, x, 0, fmt)
+    sliced = oracle.dense_ffn(w, x, 4, fmt)
+    assert np.max(np.abs(full - sliced)) / np.sqrt(np.mean(full ** 2)) <= 1e-12
+    # and against the textbook FFN in numpy
+    if fmt == "bf16":
+        Wg, Wu, Wd = (wl.bf16_bits_to_f32(a).astype(np.float64) for a in w)
+    else:
+        Wg, Wu, Wd = (np_decode_golden(c, s) for c, s in w)
+    xf = wl.bf16_bits_to_f32(x).astype(np.float64)
+    g, u = xf @ Wg.T, xf @ Wu.T
+    want = (g / (1 + np.exp(-g)) * u) @ Wd.T
+    assert np.max(np.abs(full - want)) / np.sqrt(np.mean(want ** 2)) <= 1e-12
+
+
+def test_dense_rejects_slice_cutting_a_block():
+    # A slice width that is not a multiple of 32 would cut an MX block.
+    H, I = 64, 96
+    rng = np.random.default_rng(17)
+    w = (wl.mx_matrix(rng, I, H, 127, 127), wl.mx_matrix(rng, I, H, 127, 127), wl.mx_matrix(rng, H, I, 127, 127))
+    x = wl.f32_to_bf16_bits(np.ones((1, H), np.float32))
+    with pytest.raises(ValueError):
+        oracle.dense_ffn(w, x, 2)   # 48-wide slices
