@@ -1,0 +1,179 @@
+/*
+ * moe.h -- C ABI of libmoe_gb300.so, a GB300 (sm_103a) Mixture-of-Experts
+ * feed-forward layer with MXFP4 expert weights.
+ *
+ * What one forward call computes, step by step (sources are named by page
+ * title and section):
+ *
+ *  1. Routing.  For each token t, softmax over the E router logits, keep the
+ *     k largest and renormalise over them, so that w_tj = exp(l_tj - l_max) /
+ *     sum_{j' < k} exp(l_tj' - l_max).  Larger logits come first; equal logits
+ *     (+0 equals -0) go to the lower expert index; NaN ranks below every
+ *     number.  Routing enters the expert computation as expert IDs plus
+ *     weights ("Cascadia: Resident 975B MoE Inference on Eleven AI PCs" §3.1).
+ *  2. Grouping.  Slots s = t*k + j are grouped by expert with a stable counting
+ *     sort (ascending slot order within an expert) -- the expert-major
+ *     arrangement of the same paper's §3.1.
+ *  3. Experts.  Every routed expert, and every shared expert (always included,
+ *     weight 1.0, same paper §3.1), is a SwiGLU FFN
+ *        h = SiLU(x W_g^T) * (x W_u^T),   y = h W_d^T,   SiLU(z) = z / (1 + e^-z)
+ *     whose weights are OCP MXFP4: 4-bit E2M1 codes c with one unsigned E8M0
+ *     exponent e per 32 consecutive values of a row, decoding to
+ *     v(c) * 2^(e-127), v over {0, 0.5, 1, 1.5, 2, 3, 4, 6} plus a sign bit
+ *     (4.25 bits per weight) -- "DeepSeek-V4-Flash on a four-GPU Ampere
+ *     workstation", section "MXFP4 is not NVFP4, and the difference matters on
+ *     Ampere".  Weights are decoded on chip inside the reduction; no BF16 copy
+ *     of an expert is ever written to device memory.  Products accumulate in
+ *     FP32; h is rounded to BF16.
+ *  4. Combine.  out_t = sum_{j<k} w_tj y_{e_tj}(x_t) + sum_shared y_s(x_t) in
+ *     FP32 ("Cascadia" §3.3, Eq. 1), written to (or, with accumulate, added
+ *     to) the caller's FP32 buffer.
+ *
+ *  A dense SwiGLU FFN is run as n_slices all-active slices of its intermediate
+ *  dimension, each with unit weight ("Cascadia" §3.4, Eq. 2).
+ *
+ * Layouts (all row-major, C order):
+ *  - pack4 (MXFP4 codes): byte j of a row holds element 2j in its low nibble
+ *    and element 2j+1 in its high nibble.  Code bit 3 is the sign; bits 0..2
+ *    index the magnitude list above in the printed order.
+ *  - scales: one E8M0 byte per 32 consecutive elements of a row.
+ *  - BF16 tensors are 16-bit BF16 bit patterns.
+ *
+ * Conventions:
+ *  - Tensor pointers are DEVICE pointers owned by the caller unless a comment
+ *    says otherwise.  The library owns only the handle and its own repacked
+ *    copy of the weights (made at load; the caller's weight buffers can be
+ *    freed as soon as moe_load_weights returns).
+ *  - moe_forward and moe_dense_sliced_forward enqueue work on `cuda_stream`
+ *    (a cudaStream_t, NULL = legacy default stream) and return without waiting
+ *    for it.  They allocate nothing and never synchronise.
+ *  - Every argument is checked on the host before anything is enqueued; a bad
+ *    argument returns a status, never aborts, and leaves the outputs untouched.
+ *    moe_last_error() then describes the problem.
+ *  - A device-side failure of an earlier call (a kernel's own bounds or wait
+ *    check) is reported as MOE_EDEVICE by the next call on the same handle,
+ *    or by moe_sync_status().
+ *  - One handle may be used from several host threads only if the caller
+ *    serialises the calls; separate handles are independent.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct MoeHandle MoeHandle;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_EINVAL = 1,     /* a NULL or misaligned pointer, a negative size, k out of range, wrong handle kind */
+    MOE_EDIMS = 2,      /* hidden / inter / slice width not a multiple of 32, or too large */
+    MOE_ESCALE = 3,     /* an E8M0 scale byte is 255 (NaN in the OCP format) */
+    MOE_ENOMEM = 4,     /* the library could not allocate its weight copy */
+    MOE_ECUDA = 5,      /* a CUDA runtime call failed (message in moe_last_error) */
+    MOE_EWORKSPACE = 6, /* workspace smaller than moe_workspace_bytes() or not 256-byte aligned */
+    MOE_EDEVICE = 7     /* a kernel of an earlier call reported a device-side error */
+} MoeStatus;
+
+typedef enum { MOE_W_MXFP4 = 0, MOE_W_BF16 = 1 } MoeWeightFormat;
+
+typedef struct {
+    int hidden;            /* H, multiple of 32, 32 .. 65536 */
+    int inter;             /* I per expert, or the dense FFN's total I; multiple of 32 */
+    int n_experts;         /* E routed experts (1 .. 1024); for a dense layer: n_slices */
+    int n_shared;          /* S always-on shared experts (0 .. 64); 0 for a dense layer */
+    int k_max;             /* largest k a forward call may ask for, 1 .. min(E, 32); ignored when dense */
+    int n_slices;          /* 0: routed MoE layer.  > 0: dense FFN cut into this many slices */
+    MoeWeightFormat fmt;   /* MXFP4 or BF16 weights */
+} MoeConfig;
+
+/* One weight matrix.  MXFP4: codes = pack4 bytes [rows][cols/2], scales =
+ * E8M0 bytes [rows][cols/32].  BF16: codes = BF16 [rows][cols], scales NULL.
+ * Device pointers, any alignment. */
+typedef struct {
+    const void *codes;
+    const void *scales;
+} MoeMx;
+
+/* Copy the weights into the library's own storage and return a handle.
+ *
+ * Routed layer (n_slices == 0): gate_up[g] and down[g] for g in [0, E+S);
+ *   g < E are the routed experts, g >= E the shared ones.
+ *   gate_up[g] is the [2I][H] matrix whose rows 0..I-1 are W_g and rows
+ *   I..2I-1 are W_u; down[g] is W_d [H][I].
+ * Dense layer (n_slices > 0, n_experts == n_slices, n_shared == 0):
+ *   gate_up[0] = W_g [I][H], gate_up[1] = W_u [I][H], down[0] = W_d [H][I],
+ *   all unsliced.  The library cuts I into n_slices equal slices; each width
+ *   must be a multiple of 32 so that no MX block is cut (a requested split
+ *   that would cut a 32-value block is rejected, as the loader rule in
+ *   "DeepSeek-V4-Flash on a four-GPU Ampere workstation", section "Why it
+ *   would not run", requires; weights and their scales are sliced together).
+ *
+ * The library repacks into its own buffers (a copy, never a view of the
+ * caller's memory, per the same section's note on narrow() views).  The call
+ * is synchronous: it waits for `cuda_stream` before returning.
+ * Errors: MOE_EINVAL (NULL pointers, bad counts), MOE_EDIMS, MOE_ESCALE,
+ * MOE_ENOMEM, MOE_ECUDA.  *out is set only on MOE_OK. */
+MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const MoeMx *down, void *cuda_stream,
+                           MoeHandle **out);
+
+/* Bytes of device workspace a forward call with T tokens and top-k needs
+ * (for a dense handle pass k = 0).  0 for a NULL handle or T <= 0. */
+size_t moe_workspace_bytes(const MoeHandle *h, int T, int k);
+
+/* Optional routing outputs of moe_forward; each pointer may be NULL.
+ *  topk_ids [T][k] int32, topk_w [T][k] float (j = 0 has the largest weight),
+ *  expert_offsets [E+1] int32 (first sorted position of each expert,
+ *  expert_offsets[E] = T*k), sorted_slot [T*k] int32 (slot s = t*k + j at
+ *  sorted position p), slot_pos [T*k] int32 (inverse of sorted_slot). */
+typedef struct {
+    int *topk_ids;
+    float *topk_w;
+    int *expert_offsets;
+    int *sorted_slot;
+    int *slot_pos;
+} MoeRoutingOut;
+
+/* One routed MoE layer on T tokens.
+ *  x_bf16        [T][H] BF16, 16-byte aligned
+ *  router_logits [T][E] float, 4-byte aligned
+ *  out_fp32      [T][H] float, 16-byte aligned; overwritten, or added to when
+ *                accumulate != 0 (e.g. a residual stream)
+ *  workspace     >= moe_workspace_bytes(h, T, k) bytes, 256-byte aligned;
+ *                contents on entry do not matter
+ *  routing       NULL or device pointers that receive the routing
+ * T == 0 enqueues nothing and returns MOE_OK.
+ * Errors: MOE_EINVAL (NULL/misaligned pointers, T < 0, k outside
+ * [1, k_max], a dense handle), MOE_EWORKSPACE, MOE_EDEVICE, MOE_ECUDA. */
+MoeStatus moe_forward(MoeHandle *h, const void *x_bf16, const float *router_logits, int T, int k, float *out_fp32,
+                      int accumulate, void *workspace, size_t ws_bytes, const MoeRoutingOut *routing,
+                      void *cuda_stream);
+
+/* The dense FFN of a dense handle on T tokens, as the sum of its all-active
+ * slices ("Cascadia" §3.4, Eq. 2).  Arguments as for moe_forward; the
+ * workspace size is moe_workspace_bytes(h, T, 0).
+ * Errors: MOE_EINVAL (also for a routed handle), MOE_EWORKSPACE, MOE_EDEVICE,
+ * MOE_ECUDA. */
+MoeStatus moe_dense_sliced_forward(MoeHandle *h, const void *x_bf16, int T, float *out_fp32, int accumulate,
+                                   void *workspace, size_t ws_bytes, void *cuda_stream);
+
+/* Wait for `cuda_stream`, then report MOE_EDEVICE if any kernel of this handle
+ * has flagged a device-side error, MOE_ECUDA if the CUDA runtime reports an
+ * error, else MOE_OK.  The flag is sticky until moe_free. */
+MoeStatus moe_sync_status(MoeHandle *h, void *cuda_stream);
+
+/* Human-readable description of the last non-OK status returned on the
+ * calling thread (thread-local, never NULL). */
+const char *moe_last_error(void);
+
+/* Release the handle and the library's weight copy (waits for the device). */
+void moe_free(MoeHandle *h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

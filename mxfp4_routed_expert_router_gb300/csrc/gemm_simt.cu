@@ -1,0 +1,147 @@
+// gemm_simt.cu -- straightforward CUDA-core grouped expert GEMMs (gate|up with
+// fused SwiGLU, and down), decoding MXFP4 inside the reduction.
+//
+// The decode is the one of "DeepSeek-V4-Flash on a four-GPU Ampere
+// workstation", section "MXFP4 is not NVFP4, and the difference matters on
+// Ampere": z_n = sum_k a_k v(c_nk) 2^(e_{n, k/32} - 127), FP32 accumulation, no
+// decoded copy of the expert written anywhere.  The SwiGLU expert is the one of
+// "Cascadia: Resident 975B MoE Inference on Eleven AI PCs" §3.1.
+//
+// One CTA of 128 threads per (row tile, expert group); thread r owns tile row
+// r and walks the group's tokens 8 at a time.
+#include <cuda_bf16.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+struct SimtArgs {
+    const uint8_t *wbase;
+    size_t group_bytes;
+    int kchunks, chunk_bytes, K;
+    const int *grp_start, *grp_count, *row_token;
+    const uint16_t *in;
+    int in_ld;
+    uint16_t *h_out;
+    float *y_out;
+    int I, H, gate_up, fmt;
+};
+
+// v(c) of an E2M1 code: magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6, bit 3 = sign.
+__device__ __forceinline__ float e2m1_to_float(uint32_t c)
+{
+    uint32_t m = c & 7u;
+    // exponent field E = m >> 1, mantissa bit M = m & 1: value 2^(E-1) * (1 + M/2) for E > 0, M/2 for E = 0
+    float v = (m < 2u) ? 0.5f * (float)m : __int_as_float((int)((126u + (m >> 1)) << 23 | (m & 1u) << 22));
+    return (c & 8u) ? -v : v;
+}
+
+__device__ __forceinline__ float e8m0_to_float(uint32_t e)
+{
+    return e == 0 ? __int_as_float(0x00400000) : __int_as_float((int)(e << 23));
+}
+
+__device__ __forceinline__ float bf16_to_float(uint16_t b) { return __int_as_float((int)((uint32_t)b << 16)); }
+
+constexpr int TOK = 8;
+constexpr int TOK_PER_CTA = 64;  // tokens of a group handled by one CTA (blockIdx.z)
+
+__global__ void __launch_bounds__(TILE_ROWS) gemm_simt_kernel(SimtArgs a)
+{
+    const int g = blockIdx.y, tile = blockIdx.x, r = threadIdx.x, lane = r & 31, q = r >> 5;
+    const int cnt = a.grp_count[g];
+    if ((int)blockIdx.z * TOK_PER_CTA >= cnt)
+        return;
+    const int start = a.grp_start[g];
+    const uint8_t *wtile = a.wbase + (size_t)g * a.group_bytes + (size_t)tile * a.kchunks * a.chunk_bytes;
+
+    const int c_end = min(cnt, (int)(blockIdx.z + 1) * TOK_PER_CTA);
+    for (int c0 = blockIdx.z * TOK_PER_CTA; c0 < c_end; c0 += TOK) {
+        float acc[TOK];
+        const uint16_t *xrow[TOK];
+#pragma unroll
+        for (int tt = 0; tt < TOK; ++tt) {
+            acc[tt] = 0.f;
+            int pos = start + min(c0 + tt, c_end - 1);
+            int src = a.gate_up ? a.row_token[pos] : pos;
+            xrow[tt] = a.in + (size_t)src * a.in_ld;
+        }
+        for (int kc = 0; kc < a.kchunks; ++kc) {
+            const uint8_t *chunk = wtile + (size_t)kc * a.chunk_bytes;
+            for (int b = 0; b < CHUNK_K / 32; ++b) {
+                const int k0 = kc * CHUNK_K + 32 * b;
+                if (k0 >= a.K)
+                    break;
+                float w[32];
+                if (a.fmt == FMT_MXFP4) {
+                    const uint8_t *codes = chunk + r * (CHUNK_K / 2) + b * 16;
+                    const float s = e8m0_to_float(chunk[CHUNK_MX_CODE_BYTES + r * (CHUNK_K / 32) + b]);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        uint32_t byte = codes[j];
+                        w[2 * j] = e2m1_to_float(byte & 0xFu) * s;
+                        w[2 * j + 1] = e2m1_to_float(byte >> 4) * s;
+                    }
+                } else {
+                    const uint16_t *vals = reinterpret_cast<const uint16_t *>(chunk) + r * CHUNK_K + b * 32;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        w[j] = bf16_to_float(vals[j]);
+                }
+#pragma unroll
+                for (int tt = 0; tt < TOK; ++tt) {
+                    float s = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        s = fmaf(bf16_to_float(xrow[tt][k0 + j]), w[j], s);
+                    acc[tt] += s;
+                }
+            }
+        }
+        if (a.gate_up) {
+            const int n = tile * GU_FEATURES_PER_TILE + q * 16 + (lane & 15);
+#pragma unroll
+            for (int tt = 0; tt < TOK; ++tt) {
+                float u = __shfl_sync(0xffffffffu, acc[tt], lane | 16);
+                if (lane < 16 && n < a.I && c0 + tt < c_end) {
+                    float gt = acc[tt];
+                    float hv = gt / (1.0f + expf(-gt)) * u;
+                    __nv_bfloat16 hb = __float2bfloat16_rn(hv);
+                    a.h_out[(size_t)(start + c0 + tt) * a.I + n] = *reinterpret_cast<uint16_t *>(&hb);
+                }
+            }
+        } else {
+            const int m = tile * TILE_ROWS + r;
+            if (m < a.H) {
+#pragma unroll
+                for (int tt = 0; tt < TOK; ++tt)
+                    if (c0 + tt < c_end)
+                        a.y_out[(size_t)(start + c0 + tt) * a.H + m] = acc[tt];
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_gate_up(const Plan &p, const WeightStore &w, int fmt, const uint16_t *x, cudaStream_t st)
+{
+    SimtArgs a{w.base, w.group_bytes, w.kchunks, w.chunk_bytes, w.cols, p.grp_start, p.grp_count, p.row_token,
+               x, p.H, p.h, nullptr, p.I, p.H, 1, fmt};
+    dim3 grid(w.row_tiles, p.G, (p.T + TOK_PER_CTA - 1) / TOK_PER_CTA);
+    gemm_simt_kernel<<<grid, TILE_ROWS, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_down(const Plan &p, const WeightStore &w, int fmt, cudaStream_t st)
+{
+    SimtArgs a{w.base, w.group_bytes, w.kchunks, w.chunk_bytes, w.cols, p.grp_start, p.grp_count, p.row_token,
+               p.h, p.I, nullptr, p.y, p.I, p.H, 0, fmt};
+    dim3 grid(w.row_tiles, p.G, (p.T + TOK_PER_CTA - 1) / TOK_PER_CTA);
+    gemm_simt_kernel<<<grid, TILE_ROWS, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

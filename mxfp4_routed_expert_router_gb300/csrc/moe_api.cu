@@ -1,0 +1,370 @@
+// moe_api.cu -- the C ABI of libmoe_gb300.so (declared in include/moe.h):
+// argument checks, the library's weight copy, workspace layout and the launch
+// sequence of one forward pass.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+#include <vector>
+
+#include "../../include/moe.h"
+#include "moe_internal.cuh"
+
+using namespace moe;
+
+struct MoeHandle {
+    MoeConfig cfg;
+    int E = 0, S = 0, G = 0;   // routed groups, shared groups (a dense layer: E = 0, S = n_slices)
+    int H = 0, I = 0;          // hidden, per-group intermediate
+    int fmt = 0;
+    int k_max = 0;
+    int device = 0;
+    WeightStore gu, dn;
+    int *err_host = nullptr;   // mapped pinned host memory, written by kernels on device-side errors
+    int *err_dev = nullptr;    // device alias of err_host
+};
+
+namespace {
+
+thread_local char g_msg[512] = "no error";
+
+MoeStatus fail(MoeStatus s, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+MoeStatus cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(MOE_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+void init_store(WeightStore &w, int rows_per_group_tiles_basis, bool gate_up, int K, int fmt)
+{
+    // gate|up: a row tile covers 64 intermediate features (128 rows); down: 128 output features.
+    w.rows = rows_per_group_tiles_basis;
+    w.cols = K;
+    w.row_tiles = gate_up ? (rows_per_group_tiles_basis + GU_FEATURES_PER_TILE - 1) / GU_FEATURES_PER_TILE
+                          : (rows_per_group_tiles_basis + TILE_ROWS - 1) / TILE_ROWS;
+    w.kchunks = (K + CHUNK_K - 1) / CHUNK_K;
+    w.chunk_bytes = fmt == FMT_MXFP4 ? CHUNK_MX_BYTES : CHUNK_BF16_BYTES;
+    w.group_bytes = (size_t)w.row_tiles * w.kchunks * w.chunk_bytes;
+}
+
+// Workspace carve-up for T tokens and top-k (see Plan in moe_internal.cuh).
+size_t plan_layout(const MoeHandle *h, int T, int k, char *base, Plan *p)
+{
+    const int E = h->E, S = h->S, G = h->G, H = h->H, I = h->I;
+    const long long n = (long long)T * k;
+    const long long P = n + (long long)S * T;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        char *ptr = base ? base + off : nullptr;
+        off = align_up(off + bytes, 256);
+        return ptr;
+    };
+    Plan q{};
+    q.T = T;
+    q.k = k;
+    q.E = E;
+    q.S = S;
+    q.G = G;
+    q.H = H;
+    q.I = I;
+    q.P = (int)P;
+    q.topk_ids = (int *)take(sizeof(int) * (n > 0 ? n : 1));
+    q.topk_w = (float *)take(sizeof(float) * (n > 0 ? n : 1));
+    q.counts = (int *)take(sizeof(int) * (E > 0 ? E : 1));
+    q.expert_offsets = (int *)take(sizeof(int) * (E + 1));
+    q.sorted_slot = (int *)take(sizeof(int) * (n > 0 ? n : 1));
+    q.slot_pos = (int *)take(sizeof(int) * (n > 0 ? n : 1));
+    q.grp_start = (int *)take(sizeof(int) * G);
+    q.grp_count = (int *)take(sizeof(int) * G);
+    q.row_token = (int *)take(sizeof(int) * P);
+    q.h = (uint16_t *)take(sizeof(uint16_t) * (size_t)P * I);
+    q.y = (float *)take(sizeof(float) * (size_t)P * H);
+    q.err = h->err_dev;
+    if (p)
+        *p = q;
+    return off;
+}
+
+MoeStatus check_pending(const MoeHandle *h)
+{
+    int e = *(volatile int *)h->err_host;
+    if (e != DEV_ERR_NONE)
+        return fail(MOE_EDEVICE, "a kernel of an earlier call reported device error %d", e);
+    return MOE_OK;
+}
+
+MoeStatus run_layer(MoeHandle *h, const void *x, const float *logits, int T, int k, float *out, int accumulate,
+                    void *ws, size_t ws_bytes, const MoeRoutingOut *routing, cudaStream_t st)
+{
+    Plan p;
+    size_t need = plan_layout(h, T, k, (char *)ws, &p);
+    if (ws_bytes < need)
+        return fail(MOE_EWORKSPACE, "workspace has %zu bytes, this call needs %zu", ws_bytes, need);
+    if (routing) {
+        if (routing->topk_ids) p.topk_ids = routing->topk_ids;
+        if (routing->topk_w) p.topk_w = routing->topk_w;
+        if (routing->expert_offsets) p.expert_offsets = routing->expert_offsets;
+        if (routing->sorted_slot) p.sorted_slot = routing->sorted_slot;
+        if (routing->slot_pos) p.slot_pos = routing->slot_pos;
+    }
+    cudaError_t e;
+    if (h->E > 0) {
+        if ((e = launch_router(logits, T, h->E, k, p.topk_ids, p.topk_w, p.counts, h->E, st)) != cudaSuccess)
+            return cuda_fail(e, "router launch");
+        if ((e = launch_permute(p, st)) != cudaSuccess)
+            return cuda_fail(e, "permute launch");
+    } else {
+        if ((e = launch_dense_plan(p, st)) != cudaSuccess)
+            return cuda_fail(e, "dense plan launch");
+    }
+    if ((e = launch_gemm_gate_up(p, h->gu, h->fmt, (const uint16_t *)x, st)) != cudaSuccess)
+        return cuda_fail(e, "gate/up launch");
+    if ((e = launch_gemm_down(p, h->dn, h->fmt, st)) != cudaSuccess)
+        return cuda_fail(e, "down launch");
+    if ((e = launch_combine(p, out, accumulate, st)) != cudaSuccess)
+        return cuda_fail(e, "combine launch");
+    return MOE_OK;
+}
+
+void destroy(MoeHandle *h)
+{
+    if (!h)
+        return;
+    if (h->gu.base)
+        cudaFree(h->gu.base);
+    if (h->dn.base)
+        cudaFree(h->dn.base);
+    if (h->err_host)
+        cudaFreeHost(h->err_host);
+    delete h;
+}
+
+}  // namespace
+
+extern "C" {
+
+MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const MoeMx *down, void *cuda_stream,
+                           MoeHandle **out)
+{
+    if (!cfg || !gate_up || !down || !out)
+        return fail(MOE_EINVAL, "moe_load_weights: NULL argument");
+    const MoeConfig c = *cfg;
+    if (c.fmt != MOE_W_MXFP4 && c.fmt != MOE_W_BF16)
+        return fail(MOE_EINVAL, "unknown weight format %d", (int)c.fmt);
+    if (c.hidden <= 0 || c.inter <= 0 || c.hidden % 32 || c.inter % 32 || c.hidden > 65536 || c.inter > 262144)
+        return fail(MOE_EDIMS, "hidden (%d) and inter (%d) must be positive multiples of 32 (hidden <= 65536)",
+                    c.hidden, c.inter);
+    const bool dense = c.n_slices > 0;
+    int E, S, I, G, k_max;
+    if (dense) {
+        if (c.n_experts != c.n_slices || c.n_shared != 0)
+            return fail(MOE_EINVAL, "dense layer: n_experts must equal n_slices and n_shared must be 0");
+        if (c.n_slices > 1024 || c.inter % c.n_slices || (c.inter / c.n_slices) % 32)
+            return fail(MOE_EDIMS, "dense layer: inter %d cannot be cut into %d slices of a multiple of 32",
+                        c.inter, c.n_slices);
+        E = 0;
+        S = c.n_slices;
+        I = c.inter / c.n_slices;
+        k_max = 0;
+    } else {
+        if (c.n_slices < 0)
+            return fail(MOE_EINVAL, "n_slices must be >= 0");
+        if (c.n_experts < 1 || c.n_experts > 1024 || c.n_shared < 0 || c.n_shared > 64)
+            return fail(MOE_EINVAL, "n_experts must be in [1, 1024] and n_shared in [0, 64]");
+        if (c.k_max < 1 || c.k_max > 32 || c.k_max > c.n_experts)
+            return fail(MOE_EINVAL, "k_max must be in [1, min(n_experts, 32)]");
+        E = c.n_experts;
+        S = c.n_shared;
+        I = c.inter;
+        k_max = c.k_max;
+    }
+    G = E + S;
+    const int fmt = c.fmt == MOE_W_MXFP4 ? FMT_MXFP4 : FMT_BF16;
+    const int n_gu = dense ? 2 : G, n_dn = dense ? 1 : G;
+    for (int i = 0; i < n_gu; ++i)
+        if (!gate_up[i].codes || (fmt == FMT_MXFP4 && !gate_up[i].scales))
+            return fail(MOE_EINVAL, "gate_up[%d] has a NULL pointer", i);
+    for (int i = 0; i < n_dn; ++i)
+        if (!down[i].codes || (fmt == FMT_MXFP4 && !down[i].scales))
+            return fail(MOE_EINVAL, "down[%d] has a NULL pointer", i);
+
+    MoeHandle *h = new (std::nothrow) MoeHandle();
+    if (!h)
+        return fail(MOE_ENOMEM, "host allocation failed");
+    h->cfg = c;
+    h->E = E;
+    h->S = S;
+    h->G = G;
+    h->H = c.hidden;
+    h->I = I;
+    h->fmt = fmt;
+    h->k_max = k_max;
+    cudaStream_t st = (cudaStream_t)cuda_stream;
+    cudaError_t e = cudaGetDevice(&h->device);
+    if (e != cudaSuccess) {
+        destroy(h);
+        return cuda_fail(e, "cudaGetDevice");
+    }
+    init_store(h->gu, I, true, c.hidden, fmt);
+    init_store(h->dn, c.hidden, false, I, fmt);
+    if ((e = cudaHostAlloc((void **)&h->err_host, 2 * sizeof(int), cudaHostAllocMapped)) != cudaSuccess) {
+        destroy(h);
+        return cuda_fail(e, "cudaHostAlloc");
+    }
+    h->err_host[0] = 0;
+    h->err_host[1] = 0;
+    if ((e = cudaHostGetDevicePointer((void **)&h->err_dev, h->err_host, 0)) != cudaSuccess) {
+        destroy(h);
+        return cuda_fail(e, "cudaHostGetDevicePointer");
+    }
+    if (cudaMalloc(&h->gu.base, h->gu.group_bytes * G) != cudaSuccess ||
+        cudaMalloc(&h->dn.base, h->dn.group_bytes * G) != cudaSuccess) {
+        cudaGetLastError();
+        destroy(h);
+        return fail(MOE_ENOMEM, "device allocation of %zu bytes of weights failed",
+                    (h->gu.group_bytes + h->dn.group_bytes) * (size_t)G);
+    }
+    int *bad_scale = &h->err_dev[1];
+    const long long esz = fmt == FMT_MXFP4 ? 1 : 2;  // bytes per code unit of a row (MXFP4: per 2 elements)
+    for (int g = 0; g < G; ++g) {
+        SrcMat gate{}, up{}, dn{};
+        if (dense) {
+            // slice g: gate/up rows [g*I, (g+1)*I) of the unsliced W_g / W_u; down columns likewise
+            const long long gs = fmt == FMT_MXFP4 ? c.hidden / 2 : (long long)c.hidden * 2;
+            const long long ss = c.hidden / 32;
+            gate = {(const uint8_t *)gate_up[0].codes + (long long)g * I * gs,
+                    fmt == FMT_MXFP4 ? (const uint8_t *)gate_up[0].scales + (long long)g * I * ss : nullptr, gs, ss};
+            up = {(const uint8_t *)gate_up[1].codes + (long long)g * I * gs,
+                  fmt == FMT_MXFP4 ? (const uint8_t *)gate_up[1].scales + (long long)g * I * ss : nullptr, gs, ss};
+            const long long dstride = fmt == FMT_MXFP4 ? c.inter / 2 : (long long)c.inter * 2;
+            const long long dss = c.inter / 32;
+            const long long col_off = fmt == FMT_MXFP4 ? (long long)g * I / 2 : (long long)g * I * 2;
+            dn = {(const uint8_t *)down[0].codes + col_off,
+                  fmt == FMT_MXFP4 ? (const uint8_t *)down[0].scales + (long long)g * I / 32 : nullptr, dstride, dss};
+        } else {
+            const long long gs = fmt == FMT_MXFP4 ? c.hidden / 2 : (long long)c.hidden * 2;
+            const long long ss = c.hidden / 32;
+            gate = {(const uint8_t *)gate_up[g].codes, (const uint8_t *)gate_up[g].scales, gs, ss};
+            up = {(const uint8_t *)gate_up[g].codes + (long long)I * gs,
+                  fmt == FMT_MXFP4 ? (const uint8_t *)gate_up[g].scales + (long long)I * ss : nullptr, gs, ss};
+            const long long dstride = fmt == FMT_MXFP4 ? I / 2 : (long long)I * 2;
+            dn = {(const uint8_t *)down[g].codes, (const uint8_t *)down[g].scales, dstride, I / 32};
+        }
+        (void)esz;
+        if ((e = launch_repack(fmt, true, gate, up, h->gu, g, I, c.hidden, bad_scale, st)) != cudaSuccess ||
+            (e = launch_repack(fmt, false, dn, dn, h->dn, g, I, c.hidden, bad_scale, st)) != cudaSuccess) {
+            destroy(h);
+            return cuda_fail(e, "repack launch");
+        }
+    }
+    if ((e = cudaStreamSynchronize(st)) != cudaSuccess) {
+        destroy(h);
+        return cuda_fail(e, "repack");
+    }
+    if (*(volatile int *)bad_scale) {
+        destroy(h);
+        return fail(MOE_ESCALE, "an E8M0 scale byte is 255 (NaN)");
+    }
+    *out = h;
+    return MOE_OK;
+}
+
+size_t moe_workspace_bytes(const MoeHandle *h, int T, int k)
+{
+    if (!h || T <= 0 || k < 0)
+        return 0;
+    return plan_layout(h, T, h->E > 0 ? k : 0, nullptr, nullptr);
+}
+
+MoeStatus moe_forward(MoeHandle *h, const void *x_bf16, const float *router_logits, int T, int k, float *out_fp32,
+                      int accumulate, void *workspace, size_t ws_bytes, const MoeRoutingOut *routing,
+                      void *cuda_stream)
+{
+    if (!h)
+        return fail(MOE_EINVAL, "moe_forward: NULL handle");
+    if (h->E == 0)
+        return fail(MOE_EINVAL, "moe_forward on a dense handle; use moe_dense_sliced_forward");
+    if (T < 0 || T > (1 << 24))
+        return fail(MOE_EINVAL, "T = %d out of range [0, 2^24]", T);
+    if (k < 1 || k > h->k_max)
+        return fail(MOE_EINVAL, "k = %d out of range [1, %d]", k, h->k_max);
+    if (T == 0)
+        return check_pending(h);
+    if (!x_bf16 || !router_logits || !out_fp32 || !workspace)
+        return fail(MOE_EINVAL, "moe_forward: NULL pointer");
+    if (!aligned(x_bf16, 16) || !aligned(out_fp32, 16) || !aligned(router_logits, 4))
+        return fail(MOE_EINVAL, "x and out must be 16-byte aligned, logits 4-byte aligned");
+    if (!aligned(workspace, 256))
+        return fail(MOE_EWORKSPACE, "workspace must be 256-byte aligned");
+    MoeStatus s = check_pending(h);
+    if (s != MOE_OK)
+        return s;
+    return run_layer(h, x_bf16, router_logits, T, k, out_fp32, accumulate, workspace, ws_bytes, routing,
+                     (cudaStream_t)cuda_stream);
+}
+
+MoeStatus moe_dense_sliced_forward(MoeHandle *h, const void *x_bf16, int T, float *out_fp32, int accumulate,
+                                   void *workspace, size_t ws_bytes, void *cuda_stream)
+{
+    if (!h)
+        return fail(MOE_EINVAL, "moe_dense_sliced_forward: NULL handle");
+    if (h->E != 0)
+        return fail(MOE_EINVAL, "moe_dense_sliced_forward on a routed handle; use moe_forward");
+    if (T < 0 || T > (1 << 24))
+        return fail(MOE_EINVAL, "T = %d out of range [0, 2^24]", T);
+    if (T == 0)
+        return check_pending(h);
+    if (!x_bf16 || !out_fp32 || !workspace)
+        return fail(MOE_EINVAL, "moe_dense_sliced_forward: NULL pointer");
+    if (!aligned(x_bf16, 16) || !aligned(out_fp32, 16))
+        return fail(MOE_EINVAL, "x and out must be 16-byte aligned");
+    if (!aligned(workspace, 256))
+        return fail(MOE_EWORKSPACE, "workspace must be 256-byte aligned");
+    MoeStatus s = check_pending(h);
+    if (s != MOE_OK)
+        return s;
+    return run_layer(h, x_bf16, nullptr, T, 0, out_fp32, accumulate, workspace, ws_bytes, nullptr,
+                     (cudaStream_t)cuda_stream);
+}
+
+MoeStatus moe_sync_status(MoeHandle *h, void *cuda_stream)
+{
+    if (!h)
+        return fail(MOE_EINVAL, "moe_sync_status: NULL handle");
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)cuda_stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaStreamSynchronize");
+    MoeStatus s = check_pending(h);
+    if (s != MOE_OK)
+        return s;
+    e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "CUDA runtime");
+    return MOE_OK;
+}
+
+const char *moe_last_error(void) { return g_msg; }
+
+void moe_free(MoeHandle *h)
+{
+    if (!h)
+        return;
+    cudaDeviceSynchronize();
+    destroy(h);
+}
+
+}  // extern "C"

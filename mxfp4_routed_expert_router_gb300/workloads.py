@@ -15,6 +15,7 @@ is not NVFP4, and the difference matters on Ampere"):
 * ``sweep``    same layer, T in {1, 15, 88, 176}, logits N(0,1) + b_e with a
                per-expert bias b_e ~ N(0, 0.5), seed 2
 * ``prefill``  same layer, T=8192, Zipf(1.1) expert popularity, seed 3
+  (decode, sweep and prefill share the expert weights, seeded by 1)
 * ``dense``    dense SwiGLU FFN H=7168, I=18432 as 9 slices of 2048, T in
                {1, 88, 4096}; BF16 weights N(0, 0.02) and an MXFP4 variant, seed 4
 
@@ -63,8 +64,9 @@ class LayerConfig:
     n_experts: int
     n_shared: int
     k: int
-    seed: int
+    seed: int                       # seeds x and the router logits
     logits: str = "normal"          # "normal" | "biased" | "zipf"
+    weight_seed: int = -1           # seeds the expert weights (-1: same as seed)
     e8m0_lo: int = 120              # E8M0 exponents are uniform in [lo, hi]
     e8m0_hi: int = 130
     # dense layer only
@@ -76,24 +78,34 @@ class LayerConfig:
     def n_groups(self) -> int:
         return self.n_experts + self.n_shared
 
+    @property
+    def wseed(self) -> int:
+        return self.seed if self.weight_seed < 0 else self.weight_seed
+
 
 def tiny() -> LayerConfig:
     return LayerConfig("tiny", T=16, hidden=256, inter=128, n_experts=8, n_shared=0, k=2, seed=0)
 
 
+# The decode, sweep and prefill workloads run on one and the same layer (expert
+# weights seeded by 1); each workload seeds its own tokens and logits.
+LAYER_WEIGHT_SEED = 1
+
+
 def decode(T: int = 1) -> LayerConfig:
-    return LayerConfig(f"decode_T{T}", T=T, hidden=7168, inter=2048, n_experts=256, n_shared=1, k=8, seed=1)
+    return LayerConfig(f"decode_T{T}", T=T, hidden=7168, inter=2048, n_experts=256, n_shared=1, k=8, seed=1,
+                       weight_seed=LAYER_WEIGHT_SEED)
 
 
 def sweep(T: int) -> LayerConfig:
     assert T in (1, 15, 88, 176)
     return LayerConfig(f"sweep_T{T}", T=T, hidden=7168, inter=2048, n_experts=256, n_shared=1, k=8, seed=2,
-                       logits="biased")
+                       logits="biased", weight_seed=LAYER_WEIGHT_SEED)
 
 
 def prefill(T: int = 8192) -> LayerConfig:
     return LayerConfig(f"prefill_T{T}", T=T, hidden=7168, inter=2048, n_experts=256, n_shared=1, k=8, seed=3,
-                       logits="zipf")
+                       logits="zipf", weight_seed=LAYER_WEIGHT_SEED)
 
 
 def dense(T: int, weight_format: str = "bf16") -> LayerConfig:
@@ -178,8 +190,8 @@ def expert_weights(cfg: LayerConfig, e: int):
              down_codes [H, I/2], down_scales [H, I/32]), all uint8.
     """
     H, I = cfg.hidden, cfg.inter
-    gc, gs = mx_matrix(_rng(cfg.seed, _TAG_GATE_UP, e), 2 * I, H, cfg.e8m0_lo, cfg.e8m0_hi)
-    dc, ds = mx_matrix(_rng(cfg.seed, _TAG_DOWN, e), H, I, cfg.e8m0_lo, cfg.e8m0_hi)
+    gc, gs = mx_matrix(_rng(cfg.wseed, _TAG_GATE_UP, e), 2 * I, H, cfg.e8m0_lo, cfg.e8m0_hi)
+    dc, ds = mx_matrix(_rng(cfg.wseed, _TAG_DOWN, e), H, I, cfg.e8m0_lo, cfg.e8m0_hi)
     return gc, gs, dc, ds
 
 
@@ -193,12 +205,12 @@ def dense_weights(cfg: LayerConfig):
     if cfg.weight_format == "bf16":
         out = []
         for tag, shape in ((_TAG_DENSE_G, (I, H)), (_TAG_DENSE_U, (I, H)), (_TAG_DENSE_D, (H, I))):
-            w = _rng(cfg.seed, tag).standard_normal(shape, dtype=np.float32) * np.float32(0.02)
+            w = _rng(cfg.wseed, tag).standard_normal(shape, dtype=np.float32) * np.float32(0.02)
             out.append(f32_to_bf16_bits(w))
         return tuple(out)
-    g = mx_matrix(_rng(cfg.seed, _TAG_DENSE_G), I, H, cfg.e8m0_lo, cfg.e8m0_hi)
-    u = mx_matrix(_rng(cfg.seed, _TAG_DENSE_U), I, H, cfg.e8m0_lo, cfg.e8m0_hi)
-    d = mx_matrix(_rng(cfg.seed, _TAG_DENSE_D), H, I, cfg.e8m0_lo, cfg.e8m0_hi)
+    g = mx_matrix(_rng(cfg.wseed, _TAG_DENSE_G), I, H, cfg.e8m0_lo, cfg.e8m0_hi)
+    u = mx_matrix(_rng(cfg.wseed, _TAG_DENSE_U), I, H, cfg.e8m0_lo, cfg.e8m0_hi)
+    d = mx_matrix(_rng(cfg.wseed, _TAG_DENSE_D), H, I, cfg.e8m0_lo, cfg.e8m0_hi)
     return g, u, d
 
 
