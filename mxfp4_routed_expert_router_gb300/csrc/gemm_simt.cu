@@ -23,8 +23,10 @@ struct SimtArgs {
     int kchunks, chunk_bytes, K;
     const int *grp_start, *grp_count, *row_token;
     const uint16_t *in;
+    const uint16_t *in_lo;  // down: low BF16 plane of h (h = hi + lo), else nullptr
     int in_ld;
-    uint16_t *h_out;
+    uint16_t *h_out;        // gate|up: hi plane; the lo plane follows at h_out + h_plane
+    long long h_plane;
     float *y_out;
     int I, H, gate_up, fmt;
 };
@@ -61,12 +63,14 @@ __global__ void __launch_bounds__(TILE_ROWS) gemm_simt_kernel(SimtArgs a)
     for (int c0 = blockIdx.z * TOK_PER_CTA; c0 < c_end; c0 += TOK) {
         float acc[TOK];
         const uint16_t *xrow[TOK];
+        const uint16_t *xlo[TOK];
 #pragma unroll
         for (int tt = 0; tt < TOK; ++tt) {
             acc[tt] = 0.f;
             int pos = start + min(c0 + tt, c_end - 1);
             int src = a.gate_up ? a.row_token[pos] : pos;
             xrow[tt] = a.in + (size_t)src * a.in_ld;
+            xlo[tt] = a.in_lo ? a.in_lo + (size_t)src * a.in_ld : nullptr;
         }
         for (int kc = 0; kc < a.kchunks; ++kc) {
             const uint8_t *chunk = wtile + (size_t)kc * a.chunk_bytes;
@@ -93,9 +97,15 @@ __global__ void __launch_bounds__(TILE_ROWS) gemm_simt_kernel(SimtArgs a)
 #pragma unroll
                 for (int tt = 0; tt < TOK; ++tt) {
                     float s = 0.f;
+                    if (xlo[tt]) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        s = fmaf(bf16_to_float(xrow[tt][k0 + j]), w[j], s);
+                        for (int j = 0; j < 32; ++j)
+                            s = fmaf(bf16_to_float(xrow[tt][k0 + j]) + bf16_to_float(xlo[tt][k0 + j]), w[j], s);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            s = fmaf(bf16_to_float(xrow[tt][k0 + j]), w[j], s);
+                    }
                     acc[tt] += s;
                 }
             }
@@ -108,8 +118,12 @@ __global__ void __launch_bounds__(TILE_ROWS) gemm_simt_kernel(SimtArgs a)
                 if (lane < 16 && n < a.I && c0 + tt < c_end) {
                     float gt = acc[tt];
                     float hv = gt / (1.0f + expf(-gt)) * u;
+                    // h is kept as hi + lo, two BF16 values: hi = bf16(h), lo = bf16(h - hi)
                     __nv_bfloat16 hb = __float2bfloat16_rn(hv);
-                    a.h_out[(size_t)(start + c0 + tt) * a.I + n] = *reinterpret_cast<uint16_t *>(&hb);
+                    __nv_bfloat16 lb = __float2bfloat16_rn(hv - __bfloat162float(hb));
+                    size_t o = (size_t)(start + c0 + tt) * a.I + n;
+                    a.h_out[o] = *reinterpret_cast<uint16_t *>(&hb);
+                    a.h_out[o + a.h_plane] = *reinterpret_cast<uint16_t *>(&lb);
                 }
             }
         } else {
@@ -129,7 +143,7 @@ __global__ void __launch_bounds__(TILE_ROWS) gemm_simt_kernel(SimtArgs a)
 cudaError_t launch_gemm_gate_up(const Plan &p, const WeightStore &w, int fmt, const uint16_t *x, cudaStream_t st)
 {
     SimtArgs a{w.base, w.group_bytes, w.kchunks, w.chunk_bytes, w.cols, p.grp_start, p.grp_count, p.row_token,
-               x, p.H, p.h, nullptr, p.I, p.H, 1, fmt};
+               x, nullptr, p.H, p.h, (long long)p.P * p.I, nullptr, p.I, p.H, 1, fmt};
     dim3 grid(w.row_tiles, p.G, (p.T + TOK_PER_CTA - 1) / TOK_PER_CTA);
     gemm_simt_kernel<<<grid, TILE_ROWS, 0, st>>>(a);
     return cudaGetLastError();
@@ -138,7 +152,7 @@ cudaError_t launch_gemm_gate_up(const Plan &p, const WeightStore &w, int fmt, co
 cudaError_t launch_gemm_down(const Plan &p, const WeightStore &w, int fmt, cudaStream_t st)
 {
     SimtArgs a{w.base, w.group_bytes, w.kchunks, w.chunk_bytes, w.cols, p.grp_start, p.grp_count, p.row_token,
-               p.h, p.I, nullptr, p.y, p.I, p.H, 0, fmt};
+               p.h, p.h + (size_t)p.P * p.I, p.I, nullptr, 0, p.y, p.I, p.H, 0, fmt};
     dim3 grid(w.row_tiles, p.G, (p.T + TOK_PER_CTA - 1) / TOK_PER_CTA);
     gemm_simt_kernel<<<grid, TILE_ROWS, 0, st>>>(a);
     return cudaGetLastError();

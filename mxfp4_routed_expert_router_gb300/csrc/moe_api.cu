@@ -91,7 +91,7 @@ size_t plan_layout(const MoeHandle *h, int T, int k, char *base, Plan *p)
     q.grp_start = (int *)take(sizeof(int) * G);
     q.grp_count = (int *)take(sizeof(int) * G);
     q.row_token = (int *)take(sizeof(int) * P);
-    q.h = (uint16_t *)take(sizeof(uint16_t) * (size_t)P * I);
+    q.h = (uint16_t *)take(2 * sizeof(uint16_t) * (size_t)P * I);
     q.y = (float *)take(sizeof(float) * (size_t)P * H);
     q.err = h->err_dev;
     if (p)

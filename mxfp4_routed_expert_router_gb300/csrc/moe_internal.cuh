@@ -79,7 +79,7 @@ struct Plan {
     int *grp_start;           // [G]
     int *grp_count;           // [G]
     int *row_token;           // [P] token index of each position
-    uint16_t *h;              // [P][I] BF16
+    uint16_t *h;              // [2][P][I] BF16: h = hi plane + lo plane (lo = bf16(h - hi))
     float *y;                 // [P][H] FP32
     int *err;                 // device-visible error flag (mapped host memory)
 };
