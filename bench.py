@@ -1,0 +1,429 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 MXFP4 routed-expert MoE layer.
+
+One step = one full forward pass of the layer (routing, grouping, gate|up GEMM
+with SwiGLU, down GEMM, combine) on one batch of seeded synthetic input, with
+inputs resident in HBM.  Default workload: the decode layer, T=1 token,
+H=7168, I=2048, 256 routed MXFP4 experts + 1 shared, top-8.
+
+Timing: W warm-up steps, then K steps, each timed with CUDA events on the
+launching stream; the L2 cache (129 MB) is flushed between steps by writing a
+512 MB buffer outside the timed events.  Per-stage CUDA events recorded by the
+library on the same stream give the dominant kernel's duration for the roofline.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload decode_T1|sweep_T15|...|prefill_T8192|dense_bf16_T4096|...]
+Under torchrun each rank runs an independent replica of the layer on its own
+GPU (the layer is not sharded); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from mxfp4_routed_expert_router_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "MoE-layer tokens/s; decode weight-stream HBM GB/s; prefill tensor TFLOPS vs peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20
+MX_BYTES_PER_WEIGHT = 17 / 32   # 4 bits of code + 8 bits of scale per 32 weights
+
+
+def workload(name: str) -> wl.LayerConfig:
+    if name == "tiny":
+        return wl.tiny()
+    kind, _, rest = name.rpartition("_T")
+    T = int(rest)
+    if kind == "decode":
+        return wl.decode(T)
+    if kind == "sweep":
+        return wl.sweep(T)
+    if kind == "prefill":
+        return wl.prefill(T)
+    if kind in ("dense_bf16", "dense_mxfp4"):
+        return wl.dense(T, kind.split("_")[1])
+    raise SystemExit(f"unknown workload {name}")
+
+
+def describe(cfg: wl.LayerConfig) -> str:
+    if cfg.dense:
+        return (f"{cfg.name}: dense SwiGLU FFN T={cfg.T}, H={cfg.hidden}, I={cfg.inter} as {cfg.n_slices} "
+                f"all-active slices of {cfg.inter // cfg.n_slices}, {cfg.weight_format.upper()} weights")
+    return (f"{cfg.name}: MoE layer T={cfg.T}, H={cfg.hidden}, I={cfg.inter}, E={cfg.n_experts} routed + "
+            f"{cfg.n_shared} shared MXFP4 experts, top-{cfg.k}, logits {cfg.logits}")
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ algorithmic work
+
+def work_model(cfg: wl.LayerConfig, groups_active: int):
+    """Algorithmic bytes and flops of the two GEMM kernels for one call.
+
+    groups_active: expert groups with at least one token (routed experts hit by
+    the batch, plus shared experts / dense slices).  Weight bytes are counted
+    once per active group in their stored format (MXFP4: 17/32 byte per weight);
+    flops are 2 per multiply-add over every (position, weight) pair.
+    """
+    H, T = cfg.hidden, cfg.T
+    if cfg.dense:
+        I = cfg.inter // cfg.n_slices
+        P = T * cfg.n_slices
+        wb = 2.0 if cfg.weight_format == "bf16" else MX_BYTES_PER_WEIGHT
+    else:
+        I = cfg.inter
+        P = T * cfg.k + T * cfg.n_shared
+        wb = MX_BYTES_PER_WEIGHT
+    gu_w = groups_active * 2 * I * H * wb
+    dn_w = groups_active * H * I * wb
+    gate_up = {"bytes": gu_w + T * H * 2 + P * I * 4, "flops": 2.0 * P * 2 * I * H,
+               "weight_bytes": gu_w, "per_unit": 2 * I * H * wb}
+    down = {"bytes": dn_w + P * I * 4 + P * H * 4, "flops": 2.0 * P * H * I, "weight_bytes": dn_w,
+            "per_unit": H * I * wb}
+    return gate_up, down
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.proc or not self.path or not os.path.exists(self.path):
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ traffic (ncu)
+
+def ncu_traffic(kernel_key: str):
+    """Per-launch DRAM traffic of a kernel from the committed ncu summary, or
+    None when the kernel's source changed since that capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get(kernel_key)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, ent["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != ent["source_sha256"]:
+        return None
+    return float(ent["bytes_per_launch"]) * float(ent.get("scale_to_workload", 1.0))
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, cfg, rank, world):
+    import torch
+
+    from mxfp4_routed_expert_router_gb300 import binding as B
+    from mxfp4_routed_expert_router_gb300.layer import MoeLayer, bf16_tensor
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    L = MoeLayer(cfg, device=str(dev))
+    x_bits = wl.tokens(cfg)
+    x = bf16_tensor(x_bits, str(dev))
+    logits = None if cfg.dense else torch.from_numpy(wl.router_logits(cfg)).to(dev)
+    out = torch.empty((cfg.T, cfg.hidden), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ids = None
+    if not cfg.dense:
+        ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
+
+    def step(routing=None):
+        L.forward(x, logits, cfg.k, out=out, routing=routing)
+
+    for _ in range(args.warmup):
+        step()
+    L.sync()
+    # distinct active expert groups of this batch (the unit of the weight stream)
+    if cfg.dense:
+        groups = cfg.n_slices
+    else:
+        step(B.routing_out(topk_ids=ids))
+        L.sync()
+        groups = int(torch.unique(ids).numel()) + cfg.n_shared
+
+    B.moe_profile_enable(L.handle, True)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stages = []
+    with ClockSampler(dev.index) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+            stages.append(B.moe_profile_read(L.handle))
+        torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    B.moe_profile_enable(L.handle, False)
+    L.sync()
+    times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(times) / len(times)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    stage_ms = {k: sum(s[k] for s in stages) / len(stages) for k in stages[0]}
+
+    # end to end through the public API with host buffers: pinned x/logits in,
+    # out back to pinned host memory, copies inside the timed region
+    hx = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hl = None if cfg.dense else torch.from_numpy(wl.router_logits(cfg)).pin_memory()
+    hout = torch.empty((cfg.T, cfg.hidden), dtype=torch.float32).pin_memory()
+    e2e_times = []
+    for i in range(max(3, min(args.steps, 20))):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        x.copy_(hx, non_blocking=True)
+        if hl is not None:
+            logits.copy_(hl, non_blocking=True)
+        L.forward(x, logits, cfg.k, out=out)
+        hout.copy_(out, non_blocking=True)
+        e.record(stream)
+        e.synchronize()
+        e2e_times.append(s.elapsed_time(e))
+    e2e_ms = sum(e2e_times) / len(e2e_times)
+    h2d = x_bits.nbytes + (0 if cfg.dense else cfg.T * cfg.n_experts * 4)
+    d2h = cfg.T * cfg.hidden * 4
+
+    gate_up, down = work_model(cfg, groups)
+    peaks, peak_src = read_peaks()
+    # the dominant GEMM stage of this workload
+    dom_name = "gate_up" if stage_ms["gate_up"] >= stage_ms["down"] else "down"
+    dom = gate_up if dom_name == "gate_up" else down
+    dom_ms = stage_ms[dom_name]
+    tokens_per_expert = (cfg.T * cfg.k) / max(1, groups - cfg.n_shared) if not cfg.dense else cfg.T
+    # roofline: the bound is whichever minimum time is longer at the measured peaks
+    tensor_bound = dom["flops"] / (peaks["bf16_tflops"] * 1e12) > dom["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    if tensor_bound:
+        achieved = dom["flops"] / (dom_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "peak_source": f"bf16 burst, of {peak_src}"}
+    else:
+        achieved = dom["bytes"] / (dom_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "peak_source": f"copy bandwidth, of {peak_src}"}
+    roof["kernel"] = f"{dom_name} GEMM"
+    roof["traffic"] = ncu_traffic(f"{dom_name}:{cfg.name}")
+    roof["algorithmic_bytes"] = dom["bytes"]
+    roof["algorithmic_flops"] = dom["flops"]
+    roof["kernel_ms"] = dom_ms
+    launches_per_step = (4 if cfg.dense else 6)
+    weight_bytes = gate_up["weight_bytes"] + down["weight_bytes"]
+    value = world * cfg.T / (ms * 1e-3)
+    res = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; random MXFP4 codes and E8M0 scales)",
+        "config": {"workload": describe(cfg), "T": cfg.T, "hidden": cfg.hidden, "inter": cfg.inter,
+                   "experts": cfg.n_experts, "shared": cfg.n_shared, "top_k": cfg.k,
+                   "active_groups": groups, "tokens_per_routed_expert": tokens_per_expert,
+                   "l2": "flushed between steps (512 MB write outside the timed events)",
+                   "parallelism": f"replicas x{world}"},
+        "weight_stream_GBps": weight_bytes / (ms * 1e-3) / 1e9,
+        "layer_TFLOPs": (gate_up["flops"] + down["flops"]) / (ms * 1e-3) / 1e12,
+        "stages_ms": stage_ms,
+        "roofline": roof,
+        "e2e": {"value": world * cfg.T / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    L.free()
+    return res
+
+
+# ------------------------------------------------------------------ the oracle (CPU)
+
+_DENSE_CACHE = {}
+
+
+def oracle_sample(cfg: wl.LayerConfig, budget_s: float, max_tokens: int = None):
+    """Time the CPU oracle, as it stands, on a bounded token sample of the workload.
+
+    Returns (tokens processed, seconds, threads used, description)."""
+    import oracle
+
+    oracle.build()
+    x_bits = wl.tokens(cfg)
+    nthreads = os.cpu_count() or 1
+    sample = wl.sample_tokens(cfg.T, max_tokens or cfg.T)
+    done, secs, rounds = 0, 0.0, 0
+    if cfg.dense:
+        if cfg.name not in _DENSE_CACHE:
+            _DENSE_CACHE.clear()
+            _DENSE_CACHE[cfg.name] = wl.dense_weights(cfg)
+        weights = _DENSE_CACHE[cfg.name]
+    else:
+        lg = wl.router_logits(cfg)
+    while secs < budget_s or rounds == 0:
+        t0 = time.perf_counter()
+        if cfg.dense:
+            oracle.dense_ffn(weights, x_bits[sample], cfg.n_slices, cfg.weight_format)
+        else:
+            ids, _ = oracle.route(lg[sample], cfg.k)
+            needed = sorted(set(ids.ravel().tolist()) | set(range(cfg.n_experts, cfg.n_groups)))
+            W = oracle.OracleWeights(cfg.hidden, cfg.inter, cfg.n_experts, cfg.n_shared)
+            for e in needed:
+                W.set_expert(e, *wl.expert_weights(cfg, e))
+            t0 = time.perf_counter()  # weight generation is input synthesis, not oracle work
+            oracle.moe_layer(W, x_bits[sample], lg[sample], cfg.k, nthreads=nthreads)
+        secs += time.perf_counter() - t0
+        done += len(sample)
+        rounds += 1
+    used = 1 if cfg.dense else min(nthreads, len(sample) * (cfg.k + cfg.n_shared))
+    desc = (f"{len(sample)} of {cfg.T} tokens per round x {rounds} rounds "
+            f"({'dense FFN' if cfg.dense else 'full routing + every selected and shared expert'}, "
+            f"weights decoded per round)")
+    return done, secs, used, desc
+
+
+def oracle_budget_tokens(cfg):
+    if cfg.dense:
+        return 1 if cfg.T == 1 else 2
+    return min(cfg.T, 2)
+
+
+def run_reference(args, cfg, rank, world):
+    if rank != 0:
+        return None
+    times = []
+    sample_desc = ""
+    used = 1
+    ntok = oracle_budget_tokens(cfg)
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        oracle_sample(cfg, 0.0, ntok)
+    for _ in range(args.steps):
+        done, secs, used, sample_desc = oracle_sample(cfg, 0.0, ntok)
+        times.append(secs / done)   # seconds per token
+    per_tok = sum(times) / len(times)
+    value = 1.0 / per_tok
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_tok * 1e3 * cfg.T,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "config": {"workload": describe(cfg), "T": cfg.T},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
+                         "sample": sample_desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode_T1")
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    cfg = workload(args.workload)
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+
+    if args.impl == "reference":
+        res = run_reference(args, cfg, rank, world)
+        if res is not None:
+            print(json.dumps(res))
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    res = run_ours(args, cfg, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            done, secs, used, desc = oracle_sample(cfg, args.cpu_baseline_seconds, oracle_budget_tokens(cfg))
+            res["cpu_baseline"] = {"value": done / secs, "unit": "tokens/s", "cores": used, "kind": "oracle",
+                                   "sample": desc + f"; {secs:.1f} s of CPU work"}
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

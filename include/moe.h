@@ -24,7 +24,8 @@
  *     workstation", section "MXFP4 is not NVFP4, and the difference matters on
  *     Ampere".  Weights are decoded on chip inside the reduction; no BF16 copy
  *     of an expert is ever written to device memory.  Products accumulate in
- *     FP32; h is rounded to BF16.
+ *     FP32; h is kept between the two projections as a pair of BF16 values
+ *     (hi = bf16(h), lo = bf16(h - hi)), about 16 significant bits.
  *  4. Combine.  out_t = sum_{j<k} w_tj y_{e_tj}(x_t) + sum_shared y_s(x_t) in
  *     FP32 ("Cascadia" §3.3, Eq. 1), written to (or, with accumulate, added
  *     to) the caller's FP32 buffer.
@@ -164,6 +165,19 @@ MoeStatus moe_dense_sliced_forward(MoeHandle *h, const void *x_bf16, int T, floa
  * has flagged a device-side error, MOE_ECUDA if the CUDA runtime reports an
  * error, else MOE_OK.  The flag is sticky until moe_free. */
 MoeStatus moe_sync_status(MoeHandle *h, void *cuda_stream);
+
+/* Per-stage timing for benchmarking.  While enabled, every forward call on
+ * this handle records a CUDA event on its stream before its first stage and
+ * after each stage.  Stages: [0] routing (router kernel), [1] grouping
+ * (histogram + permutation, or the dense plan), [2] gate|up GEMM with SwiGLU,
+ * [3] down GEMM, [4] combine.  A stage a call does not run reads 0.
+ * Errors: MOE_EINVAL (NULL handle), MOE_ECUDA (event creation failed). */
+MoeStatus moe_profile_enable(MoeHandle *h, int enable);
+
+/* Wait for the events of the most recent profiled call and write up to n
+ * stage durations in milliseconds to the HOST array ms.  Returns the number of
+ * stages written (5), or -1 if profiling is off or no call was profiled. */
+int moe_profile_read(MoeHandle *h, float *ms, int n);
 
 /* Human-readable description of the last non-OK status returned on the
  * calling thread (thread-local, never NULL). */

@@ -22,7 +22,8 @@ MOE_W_MXFP4, MOE_W_BF16 = 0, 1
 
 # every symbol include/moe.h declares
 EXPORTED = ("moe_load_weights", "moe_workspace_bytes", "moe_forward", "moe_dense_sliced_forward",
-            "moe_sync_status", "moe_last_error", "moe_free")
+            "moe_sync_status", "moe_profile_enable", "moe_profile_read", "moe_last_error", "moe_free")
+STAGES = ("routing", "grouping", "gate_up", "down", "combine")
 
 
 class MoeError(RuntimeError):
@@ -63,6 +64,10 @@ def _load():
     L.moe_dense_sliced_forward.restype = ci
     L.moe_sync_status.argtypes = [vp, vp]
     L.moe_sync_status.restype = ci
+    L.moe_profile_enable.argtypes = [vp, ci]
+    L.moe_profile_enable.restype = ci
+    L.moe_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ci]
+    L.moe_profile_read.restype = ci
     L.moe_last_error.argtypes = []
     L.moe_last_error.restype = ctypes.c_char_p
     L.moe_free.argtypes = [vp]
@@ -127,6 +132,19 @@ def moe_dense_sliced_forward(handle: int, x_bf16, T: int, out_fp32, accumulate: 
 
 def moe_sync_status(handle: int, stream=None) -> None:
     _check(lib.moe_sync_status(handle, _stream(stream)))
+
+
+def moe_profile_enable(handle: int, enable: bool = True) -> None:
+    _check(lib.moe_profile_enable(handle, int(bool(enable))))
+
+
+def moe_profile_read(handle: int) -> dict:
+    """Stage durations (ms) of the most recent profiled forward call."""
+    buf = (ctypes.c_float * len(STAGES))()
+    n = lib.moe_profile_read(handle, buf, len(STAGES))
+    if n < 0:
+        raise MoeError(MOE_EINVAL, "no profiled call")
+    return {STAGES[i]: float(buf[i]) for i in range(n)}
 
 
 def moe_free(handle: int) -> None:

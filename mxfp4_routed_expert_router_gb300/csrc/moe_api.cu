@@ -25,7 +25,12 @@ struct MoeHandle {
     WeightStore gu, dn;
     int *err_host = nullptr;   // mapped pinned host memory, written by kernels on device-side errors
     int *err_dev = nullptr;    // device alias of err_host
+    bool profile = false;      // record stage events (moe_profile_enable)
+    bool profiled = false;     // a call has recorded its events
+    cudaEvent_t ev[6] = {};
 };
+
+constexpr int N_STAGES = 5;
 
 namespace {
 
@@ -122,21 +127,34 @@ MoeStatus run_layer(MoeHandle *h, const void *x, const float *logits, int T, int
         if (routing->slot_pos) p.slot_pos = routing->slot_pos;
     }
     cudaError_t e;
+    auto mark = [&](int i) {
+        if (h->profile)
+            cudaEventRecord(h->ev[i], st);
+    };
+    mark(0);
     if (h->E > 0) {
         if ((e = launch_router(logits, T, h->E, k, p.topk_ids, p.topk_w, p.counts, h->E, st)) != cudaSuccess)
             return cuda_fail(e, "router launch");
+        mark(1);
         if ((e = launch_permute(p, st)) != cudaSuccess)
             return cuda_fail(e, "permute launch");
     } else {
+        mark(1);
         if ((e = launch_dense_plan(p, st)) != cudaSuccess)
             return cuda_fail(e, "dense plan launch");
     }
+    mark(2);
     if ((e = launch_gemm_gate_up(p, h->gu, h->fmt, (const uint16_t *)x, st)) != cudaSuccess)
         return cuda_fail(e, "gate/up launch");
+    mark(3);
     if ((e = launch_gemm_down(p, h->dn, h->fmt, st)) != cudaSuccess)
         return cuda_fail(e, "down launch");
+    mark(4);
     if ((e = launch_combine(p, out, accumulate, st)) != cudaSuccess)
         return cuda_fail(e, "combine launch");
+    mark(5);
+    if (h->profile)
+        h->profiled = true;
     return MOE_OK;
 }
 
@@ -150,6 +168,9 @@ void destroy(MoeHandle *h)
         cudaFree(h->dn.base);
     if (h->err_host)
         cudaFreeHost(h->err_host);
+    for (cudaEvent_t &ev : h->ev)
+        if (ev)
+            cudaEventDestroy(ev);
     delete h;
 }
 
@@ -355,6 +376,37 @@ MoeStatus moe_sync_status(MoeHandle *h, void *cuda_stream)
     if (e != cudaSuccess)
         return cuda_fail(e, "CUDA runtime");
     return MOE_OK;
+}
+
+MoeStatus moe_profile_enable(MoeHandle *h, int enable)
+{
+    if (!h)
+        return fail(MOE_EINVAL, "moe_profile_enable: NULL handle");
+    if (enable && !h->ev[0]) {
+        for (cudaEvent_t &ev : h->ev) {
+            cudaError_t e = cudaEventCreate(&ev);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "cudaEventCreate");
+        }
+    }
+    h->profile = enable != 0;
+    h->profiled = false;
+    return MOE_OK;
+}
+
+int moe_profile_read(MoeHandle *h, float *ms, int n)
+{
+    if (!h || !ms || !h->profile || !h->profiled)
+        return -1;
+    if (cudaEventSynchronize(h->ev[N_STAGES]) != cudaSuccess)
+        return -1;
+    int m = n < N_STAGES ? n : N_STAGES;
+    for (int i = 0; i < m; ++i) {
+        float t = 0.f;
+        cudaEventElapsedTime(&t, h->ev[i], h->ev[i + 1]);
+        ms[i] = t;
+    }
+    return m;
 }
 
 const char *moe_last_error(void) { return g_msg; }
