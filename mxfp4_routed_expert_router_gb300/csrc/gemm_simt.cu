@@ -12,6 +12,7 @@
 #include <cuda_bf16.h>
 
 #include "moe_internal.cuh"
+#include "mx_decode.cuh"
 
 namespace moe {
 
@@ -30,20 +31,6 @@ struct SimtArgs {
     float *y_out;
     int I, H, gate_up, fmt;
 };
-
-// v(c) of an E2M1 code: magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6, bit 3 = sign.
-__device__ __forceinline__ float e2m1_to_float(uint32_t c)
-{
-    uint32_t m = c & 7u;
-    // exponent field E = m >> 1, mantissa bit M = m & 1: value 2^(E-1) * (1 + M/2) for E > 0, M/2 for E = 0
-    float v = (m < 2u) ? 0.5f * (float)m : __int_as_float((int)((126u + (m >> 1)) << 23 | (m & 1u) << 22));
-    return (c & 8u) ? -v : v;
-}
-
-__device__ __forceinline__ float e8m0_to_float(uint32_t e)
-{
-    return e == 0 ? __int_as_float(0x00400000) : __int_as_float((int)(e << 23));
-}
 
 __device__ __forceinline__ float bf16_to_float(uint16_t b) { return __int_as_float((int)((uint32_t)b << 16)); }
 
@@ -80,16 +67,22 @@ __global__ void __launch_bounds__(TILE_ROWS) gemm_simt_kernel(SimtArgs a)
                     break;
                 float w[32];
                 if (a.fmt == FMT_MXFP4) {
-                    const uint8_t *codes = chunk + r * (CHUNK_K / 2) + b * 16;
-                    const float s = e8m0_to_float(chunk[CHUNK_MX_CODE_BYTES + r * (CHUNK_K / 32) + b]);
+                    const uint32_t *words = reinterpret_cast<const uint32_t *>(
+                        chunk + (b / 2) * (CHUNK_MX_CODE_BYTES / 2) + r * 32 + (b % 2) * 16);
+                    const uint32_t s2 = e8m0_to_bf16x2(chunk[CHUNK_MX_CODE_BYTES + r * (CHUNK_K / 32) + b]);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        uint32_t byte = codes[j];
-                        w[2 * j] = e2m1_to_float(byte & 0xFu) * s;
-                        w[2 * j + 1] = e2m1_to_float(byte >> 4) * s;
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t o[4];
+                        decode_word(words[c], s2, o);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            w[8 * c + 2 * j] = bf16_to_float((uint16_t)(o[j] & 0xFFFFu));
+                            w[8 * c + 2 * j + 1] = bf16_to_float((uint16_t)(o[j] >> 16));
+                        }
                     }
                 } else {
-                    const uint16_t *vals = reinterpret_cast<const uint16_t *>(chunk) + r * CHUNK_K + b * 32;
+                    const uint16_t *vals = reinterpret_cast<const uint16_t *>(
+                        chunk + (b / 2) * (CHUNK_BF16_BYTES / 2) + r * HALF_K * 2) + (b % 2) * 32;
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         w[j] = bf16_to_float(vals[j]);

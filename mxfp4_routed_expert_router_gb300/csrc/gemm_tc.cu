@@ -1,0 +1,736 @@
+// gemm_tc.cu -- grouped expert GEMMs on the 5th-generation tensor cores
+// (tcgen05, sm_103a): gate|up with fused SwiGLU, and down.
+//
+// Operation (per expert group g and token position p of the group):
+//   gate|up:  g_n = x_p . W_g[n],  u_n = x_p . W_u[n],  h_pn = SiLU(g_n) * u_n
+//   down:     y_pm = h_p . W_d[m]
+// with the SwiGLU expert of "Cascadia: Resident 975B MoE Inference on Eleven
+// AI PCs" §3.1 and MXFP4 weights decoded inside the reduction as in
+// "DeepSeek-V4-Flash on a four-GPU Ampere workstation", section "MXFP4 is not
+// NVFP4, and the difference matters on Ampere" (scale loaded once per 32-value
+// block, FP32 accumulation, no decoded copy of an expert in device memory).
+//
+// Mapping to the hardware ("swap-AB": weights are the M side):
+//   D[128 weight rows, N tokens] (FP32, TMEM)  +=  A[128 rows, K] . B[N tokens, K]^T
+//   A = 128 weight rows decoded to BF16 in shared memory by CUDA-core warps,
+//       from MXFP4 chunks streamed out of HBM by bulk async copies;
+//   B = token rows (BF16; for down the hi and lo BF16 planes of h, two MMAs per
+//       K step), loaded by TMA into the 128-byte-swizzled K-major layout;
+//   MMA = tcgen05.mma kind::f16, M=128, N = 16..NMAX, K=16, issued by one thread.
+// One CTA per SM walks a static schedule of (group, row tile, token tile)
+// work items.  Warp roles:
+//   warp 0      bulk-copies weight chunks into a ring of raw buffers
+//   warp 1      TMA-loads token tiles (B) into the stage ring
+//   warp 2      allocates TMEM, issues the MMAs, commits to mbarriers
+//   warps 3-10  decode raw MXFP4 (or copy BF16) into the swizzled A stage
+//   warps 11-14 epilogue: TMEM -> registers, SwiGLU (gate|up) or FP32 y (down)
+// Two TMEM accumulators let the epilogue of one work item overlap the MMAs of
+// the next.  Every mbarrier wait is bounded: on a timeout the kernel records
+// DEV_ERR_WAIT_TIMEOUT, stops issuing work, waits (bounded) for the copies and
+// MMAs it has in flight, frees its TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include "moe_internal.cuh"
+#include "mx_decode.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int NUM_THREADS = 480;
+constexpr int WARP_WLOAD = 0, WARP_BLOAD = 1, WARP_MMA = 2, WARP_DEC0 = 3, N_DEC_WARPS = 8, WARP_EPI0 = 11;
+constexpr int A_STAGE_BYTES = TILE_ROWS * HALF_K * 2;  // 16 KB: 128 rows x 64 BF16
+constexpr int B_BOX_ROWS = 16;
+constexpr int B_BOX_BYTES = B_BOX_ROWS * HALF_K * 2;   // 2 KB
+constexpr int MAX_GROUPS = 1088;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
+
+struct TcArgs {
+    const uint8_t *wbase;
+    size_t group_bytes;
+    int kchunks, chunk_bytes, row_tiles;
+    const int *grp_start, *grp_count;
+    int E, G, I, H;
+    uint16_t *h_out;
+    long long h_plane;
+    float *y_out;
+    int *err;
+};
+
+// ------------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait (one thread) for the phase with the given parity.  Gives up
+// after WAIT_LIMIT_NS, recording DEV_ERR_WAIT_TIMEOUT and raising the CTA's
+// abort flag, or as soon as another role has raised it.  Returns true when
+// the phase completed.
+__device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *err)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((i & 63u) == 0) {
+            if (*abort_flag)
+                return false;
+            if (global_ns() - t0 > WAIT_LIMIT_NS) {
+                atomicCAS(err, 0, DEV_ERR_WAIT_TIMEOUT);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// The same, taken by a whole warp: every lane observes the phase, and the
+// outcome is uniform across the warp (so warp-collective instructions that
+// follow never run with a partial warp).
+__device__ __noinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *err)
+{
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity)))
+            return true;
+        if ((i & 63u) == 63u) {
+            if (i == 63u)
+                t0 = global_ns();
+            bool stop = *abort_flag != 0;
+            if (!stop && global_ns() - t0 > WAIT_LIMIT_NS) {
+                atomicCAS(err, 0, DEV_ERR_WAIT_TIMEOUT);
+                *abort_flag = 1;
+                stop = true;
+            }
+            if (__any_sync(0xffffffffu, stop))
+                return false;
+        }
+    }
+}
+
+// Bounded wait used while tearing down: true when the phase completed.
+__device__ __noinline__ bool mbar_drain(uint64_t *bar, uint32_t parity)
+{
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (global_ns() - t0 > WAIT_LIMIT_NS)
+            return false;
+    }
+}
+
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate)
+{
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16])
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
+// core groups 1024 bytes apart (SBO), leading offset unused for this layout.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+{
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
+           (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: BF16 A and B, FP32 D, both K-major,
+// M = 128, N given.
+__device__ __forceinline__ uint32_t idesc_bf16(int n)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(TILE_ROWS >> 4) << 24);
+}
+
+// Byte offset of 16-byte chunk c (0..7) of row r inside a 128-byte-swizzled
+// K-major tile whose rows are 128 bytes: 8-row groups are 1024 bytes apart
+// and the chunk index is XORed with the row's position in its group.
+__device__ __forceinline__ uint32_t sw128_offset(int r, int c)
+{
+    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// ------------------------------------------------------------------ schedule
+
+struct WorkItem {
+    int g, rt, tok0, nvalid, n_mma;
+};
+
+// prefix[g] = first work item of group g; work items of a group are ordered
+// row tile major, token tile minor, so that CTAs running neighbouring items
+// share the weight chunk through L2.
+__device__ __forceinline__ WorkItem decompose(int t, const int *prefix, const int *counts, int G, int row_tiles,
+                                              int nmax)
+{
+    int lo = 0, hi = G;  // find g with prefix[g] <= t < prefix[g+1]
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= t)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    WorkItem w;
+    w.g = lo;
+    const int cnt = counts[lo];
+    const int ntiles = (cnt + nmax - 1) / nmax;
+    const int local = t - prefix[lo];
+    w.rt = local / ntiles;
+    const int nt = local % ntiles;
+    const int per = (((cnt + ntiles - 1) / ntiles) + 15) & ~15;
+    w.tok0 = nt * per;
+    w.nvalid = min(per, cnt - w.tok0);
+    w.n_mma = (w.nvalid + 15) & ~15;
+    return w;
+}
+
+template <int NMAX, int NB, int S, int R, int RAW_BYTES>
+struct Smem {
+    static constexpr int B_STAGE = NMAX * HALF_K * 2 * NB;
+    static constexpr int A_OFF = 0;
+    static constexpr int B_OFF = A_OFF + S * A_STAGE_BYTES;
+    static constexpr int RAW_OFF = B_OFF + S * B_STAGE;
+    static constexpr int BAR_OFF = RAW_OFF + R * RAW_BYTES;
+    static constexpr int N_BARS = 2 * R + 2 * S + 4;
+    static constexpr int SCHED_OFF = BAR_OFF + N_BARS * 8;
+    static constexpr int MISC_OFF = SCHED_OFF + (MAX_GROUPS + 1) * 4;
+    static constexpr int TOTAL = MISC_OFF + 16 + 1024;  // + alignment slack
+};
+
+// ------------------------------------------------------------------ kernel
+
+template <bool GU, int WFMT, int NMAX, int S, int R>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_b2)
+{
+    constexpr int NB = GU ? 1 : 2;
+    constexpr int RAW_BYTES = WFMT == FMT_MXFP4 ? CHUNK_MX_BYTES : CHUNK_BF16_BYTES;
+    using L = Smem<NMAX, NB, S, R, RAW_BYTES>;
+    constexpr int TMEM_COLS = 2 * NMAX < 32 ? 32 : 2 * NMAX;
+    static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM columns");
+    static_assert(L::TOTAL <= 232448, "shared memory");
+
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);
+    uint64_t *raw_full = bars, *raw_empty = bars + R, *ab_full = bars + 2 * R, *ab_empty = bars + 2 * R + S;
+    uint64_t *acc_full = bars + 2 * R + 2 * S, *acc_empty = acc_full + 2;
+    int *prefix = reinterpret_cast<int *>(smem + L::SCHED_OFF);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::MISC_OFF + 4);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        for (int i = 0; i < R; ++i) {
+            mbar_init(&raw_full[i], 1);
+            mbar_init(&raw_empty[i], N_DEC_WARPS);
+        }
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&ab_full[i], 1 + N_DEC_WARPS);
+            mbar_init(&ab_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 4);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_proxy_async();
+    }
+    if (warp == WARP_MMA) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (warp == WARP_WLOAD) {
+        // work-item prefix over groups (one warp scan, 32 groups per step)
+        int run = 0;
+        for (int base = 0; base < a.G; base += 32) {
+            int g = base + lane;
+            int cnt = g < a.G ? a.grp_count[g] : 0;
+            int v = ((cnt + NMAX - 1) / NMAX) * a.row_tiles;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o)
+                    incl += n;
+            }
+            if (g < a.G)
+                prefix[g] = run + incl - v;
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0)
+            prefix[a.G] = run;
+    }
+    if (warp == WARP_BLOAD && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b2)) : "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total = prefix[a.G];
+    const int nstages = 2 * a.kchunks;
+
+    if (warp == WARP_WLOAD) {
+        if (lane == 0) {
+            uint32_t rc = 0, armed = 0, armed_par = 0;
+            for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+                WorkItem w = decompose(t, prefix, a.grp_count, a.G, a.row_tiles, NMAX);
+                const uint8_t *src =
+                    a.wbase + (size_t)w.g * a.group_bytes + (size_t)w.rt * a.kchunks * (size_t)a.chunk_bytes;
+                bool ok = true;
+                for (int kc = 0; kc < a.kchunks; ++kc, ++rc) {
+                    const int slot = rc % R;
+                    const uint32_t ph = (rc / R) & 1;
+                    if (!(ok = mbar_wait(&raw_empty[slot], ph ^ 1, abort_flag, a.err)))
+                        break;
+                    mbar_arrive_expect_tx(&raw_full[slot], RAW_BYTES);
+                    bulk_g2s(smem + L::RAW_OFF + slot * RAW_BYTES, src + (size_t)kc * a.chunk_bytes, RAW_BYTES,
+                             &raw_full[slot]);
+                    armed |= 1u << slot;
+                    armed_par = (armed_par & ~(1u << slot)) | (ph << slot);
+                }
+                if (!ok)
+                    break;
+            }
+            // drain: every armed raw buffer's last copy has landed
+            for (int s = 0; s < R; ++s)
+                if (armed & (1u << s))
+                    mbar_drain(&raw_full[s], (armed_par >> s) & 1);
+        }
+        __syncwarp();
+    } else if (warp == WARP_BLOAD) {
+        if (lane == 0) {
+            uint32_t sc = 0, armed = 0, armed_par = 0;
+            for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+                WorkItem w = decompose(t, prefix, a.grp_count, a.G, a.row_tiles, NMAX);
+                int row0;
+                const CUtensorMap *m0 = &map_b;
+                if (GU) {
+                    // routed groups read gathered rows by position, shared groups x by token
+                    if (w.g < a.E) {
+                        row0 = a.grp_start[w.g] + w.tok0;
+                    } else {
+                        row0 = w.tok0;
+                        m0 = &map_b2;
+                    }
+                } else {
+                    row0 = a.grp_start[w.g] + w.tok0;
+                }
+                const int nbox = w.n_mma / B_BOX_ROWS;
+                const uint32_t bytes = (uint32_t)(nbox * B_BOX_BYTES * NB);
+                bool ok = true;
+                for (int st = 0; st < nstages; ++st, ++sc) {
+                    const int slot = sc % S;
+                    const uint32_t ph = (sc / S) & 1;
+                    if (!(ok = mbar_wait(&ab_empty[slot], ph ^ 1, abort_flag, a.err)))
+                        break;
+                    mbar_arrive_expect_tx(&ab_full[slot], bytes);
+                    uint8_t *bdst = smem + L::B_OFF + slot * L::B_STAGE;
+                    for (int b = 0; b < nbox; ++b) {
+                        tma_2d(bdst + b * B_BOX_BYTES, m0, st * HALF_K, row0 + b * B_BOX_ROWS, &ab_full[slot]);
+                        if (!GU)
+                            tma_2d(bdst + NMAX * HALF_K * 2 + b * B_BOX_BYTES, &map_b2, st * HALF_K,
+                                   row0 + b * B_BOX_ROWS, &ab_full[slot]);
+                    }
+                    armed |= 1u << slot;
+                    armed_par = (armed_par & ~(1u << slot)) | (ph << slot);
+                }
+                if (!ok)
+                    break;
+            }
+            // drain: every armed stage's B tiles have landed and been consumed (returns at
+            // once on the normal path; bounded after an abort)
+            for (int s = 0; s < S; ++s)
+                if (armed & (1u << s))
+                    mbar_drain(&ab_full[s], (armed_par >> s) & 1);
+        }
+        __syncwarp();
+    } else if (warp == WARP_MMA) {
+        if (lane == 0) {
+            uint32_t sc = 0, tc = 0;
+            bool issued = false;
+            uint32_t last_acc = 0, last_par = 0;
+            for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x, ++tc) {
+                WorkItem w = decompose(t, prefix, a.grp_count, a.G, a.row_tiles, NMAX);
+                const int buf = tc & 1;
+                const uint32_t aph = (tc >> 1) & 1;
+                if (!mbar_wait(&acc_empty[buf], aph ^ 1, abort_flag, a.err))
+                    break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(buf * NMAX);
+                const uint32_t idesc = idesc_bf16(w.n_mma);
+                bool ok = true;
+                for (int st = 0; st < nstages; ++st, ++sc) {
+                    const int slot = sc % S;
+                    if (!(ok = mbar_wait(&ab_full[slot], (sc / S) & 1, abort_flag, a.err)))
+                        break;
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_addr(smem + L::A_OFF + slot * A_STAGE_BYTES);
+                    const uint32_t b_addr = smem_addr(smem + L::B_OFF + slot * L::B_STAGE);
+#pragma unroll
+                    for (int j = 0; j < HALF_K / 16; ++j) {
+                        const uint64_t ad = sw128_desc(a_addr + j * 32);
+                        tc_mma(d_tmem, ad, sw128_desc(b_addr + j * 32), idesc, (st | j) ? 1u : 0u);
+                        if (!GU)
+                            tc_mma(d_tmem, ad, sw128_desc(b_addr + NMAX * HALF_K * 2 + j * 32), idesc, 1u);
+                    }
+                    tc_commit(&ab_empty[slot]);
+                    issued = true;
+                }
+                if (!ok)
+                    break;
+                tc_commit(&acc_full[buf]);
+                last_acc = buf;
+                last_par = aph;
+            }
+            // drain: the MMAs of the last committed item have completed
+            if (issued)
+                mbar_drain(&acc_full[last_acc], last_par);
+        }
+        __syncwarp();
+    } else if (warp < WARP_EPI0) {
+        // ---------------------------------------------------------- decoders
+        const int dt = tid - WARP_DEC0 * 32;   // 0..255
+        const int r = dt >> 1, blk = dt & 1;   // tile row, 32-element block of the 64-wide stage
+        uint32_t rc = 0, sc = 0;
+        for (int t = blockIdx.x; t < total && !__any_sync(0xffffffffu, *abort_flag); t += gridDim.x) {
+            bool ok = true;
+            for (int kc = 0; kc < a.kchunks && ok; ++kc, ++rc) {
+                const int rslot = rc % R;
+                if (!(ok = mbar_wait_warp(&raw_full[rslot], (rc / R) & 1, abort_flag, a.err)))
+                    break;
+                const uint8_t *raw = smem + L::RAW_OFF + rslot * RAW_BYTES;
+                for (int h = 0; h < 2; ++h, ++sc) {
+                    const int slot = sc % S;
+                    if (!(ok = mbar_wait_warp(&ab_empty[slot], ((sc / S) & 1) ^ 1, abort_flag, a.err)))
+                        break;
+                    uint8_t *adst = smem + L::A_OFF + slot * A_STAGE_BYTES;
+                    if (WFMT == FMT_MXFP4) {
+                        const uint4 cw = *reinterpret_cast<const uint4 *>(raw + h * (CHUNK_MX_CODE_BYTES / 2) + r * 32 +
+                                                                          blk * 16);
+                        const uint32_t s2 = e8m0_to_bf16x2(raw[CHUNK_MX_CODE_BYTES + r * 4 + h * 2 + blk]);
+                        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t o[4];
+                            decode_word(words[c], s2, o);
+                            *reinterpret_cast<uint4 *>(adst + sw128_offset(r, blk * 4 + c)) =
+                                make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                    } else {
+                        const uint4 *src = reinterpret_cast<const uint4 *>(raw + h * (CHUNK_BF16_BYTES / 2) + r * 128 +
+                                                                           blk * 64);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            *reinterpret_cast<uint4 *>(adst + sw128_offset(r, blk * 4 + c)) = src[c];
+                    }
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&ab_full[slot]);
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&raw_empty[rslot]);
+            }
+            if (!ok)
+                break;
+        }
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int q = warp & 3;                 // TMEM lane quadrant of this warp
+        uint32_t tc = 0;
+        for (int t = blockIdx.x; t < total && !__any_sync(0xffffffffu, *abort_flag); t += gridDim.x, ++tc) {
+            WorkItem w = decompose(t, prefix, a.grp_count, a.G, a.row_tiles, NMAX);
+            const int buf = tc & 1;
+            if (!mbar_wait_warp(&acc_full[buf], (tc >> 1) & 1, abort_flag, a.err))
+                break;
+            tc_fence_after();
+            const int pos0 = a.grp_start[w.g] + w.tok0;
+            const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * NMAX);
+            for (int c0 = 0; c0 < w.n_mma; c0 += 16) {
+                float v[16];
+                tmem_ld16(taddr + c0, v);
+                if (GU) {
+                    const int n = w.rt * GU_FEATURES_PER_TILE + 16 * q + (lane & 15);
+                    const bool up_lane = lane >= 16;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float send = up_lane ? v[j] : v[8 + j];
+                        const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+                        const float gv = up_lane ? recv : v[j];
+                        const float uv = up_lane ? v[8 + j] : recv;
+                        const int tok = c0 + (up_lane ? 8 : 0) + j;
+                        if (tok < w.nvalid && n < a.I) {
+                            const float hv = gv / (1.0f + __expf(-gv)) * uv;
+                            const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
+                            const __nv_bfloat16 lb = __float2bfloat16_rn(hv - __bfloat162float(hb));
+                            const size_t o = (size_t)(pos0 + tok) * a.I + n;
+                            a.h_out[o] = __bfloat16_as_ushort(hb);
+                            a.h_out[o + a.h_plane] = __bfloat16_as_ushort(lb);
+                        }
+                    }
+                } else {
+                    const int m = w.rt * TILE_ROWS + 32 * q + lane;
+                    if (m < a.H) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (c0 + j < w.nvalid)
+                                a.y_out[(size_t)(pos0 + c0 + j) * a.H + m] = v[j];
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&acc_empty[buf]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == WARP_MMA) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2-D BF16 tensor [rows][cols] (row stride cols*2 bytes), box 64 x 16, 128B swizzle.
+cudaError_t make_map(CUtensorMap *m, const void *base, long long rows, int cols)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc)
+        return cudaErrorNotSupported;
+    if (rows < 1)
+        rows = 1;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {HALF_K, B_BOX_ROWS};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+int sm_count()
+{
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0)
+            n = 1;
+    }
+    return n;
+}
+
+template <bool GU, int WFMT, int NMAX, int S, int R>
+cudaError_t launch_cfg(const TcArgs &a, const CUtensorMap &m1, const CUtensorMap &m2, cudaStream_t st)
+{
+    constexpr int NB = GU ? 1 : 2;
+    constexpr int RAW_BYTES = WFMT == FMT_MXFP4 ? CHUNK_MX_BYTES : CHUNK_BF16_BYTES;
+    constexpr int SMEM = Smem<NMAX, NB, S, R, RAW_BYTES>::TOTAL;
+    auto kern = gemm_tc_kernel<GU, WFMT, NMAX, S, R>;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        if (e != cudaSuccess)
+            return e;
+        attr = true;
+    }
+    kern<<<sm_count(), NUM_THREADS, SMEM, st>>>(a, m1, m2);
+    return cudaGetLastError();
+}
+
+// token tile sizes: decode-sized batches use a small tile (more pipeline
+// stages and raw buffers in flight), larger batches the full tile.
+constexpr int SMALL_T = 64;
+
+template <bool GU>
+cudaError_t launch_any(const TcArgs &a, int fmt, int T, const CUtensorMap &m1, const CUtensorMap &m2,
+                       cudaStream_t st)
+{
+    const bool small = T <= SMALL_T;
+    if constexpr (GU) {
+        if (fmt == FMT_MXFP4)
+            return small ? launch_cfg<true, FMT_MXFP4, 64, 6, 8>(a, m1, m2, st)
+                         : launch_cfg<true, FMT_MXFP4, 256, 3, 4>(a, m1, m2, st);
+        return small ? launch_cfg<true, FMT_BF16, 64, 4, 2>(a, m1, m2, st)
+                     : launch_cfg<true, FMT_BF16, 256, 3, 2>(a, m1, m2, st);
+    } else {
+        if (fmt == FMT_MXFP4)
+            return small ? launch_cfg<false, FMT_MXFP4, 64, 5, 6>(a, m1, m2, st)
+                         : launch_cfg<false, FMT_MXFP4, 128, 3, 4>(a, m1, m2, st);
+        return small ? launch_cfg<false, FMT_BF16, 64, 4, 2>(a, m1, m2, st)
+                     : launch_cfg<false, FMT_BF16, 128, 3, 2>(a, m1, m2, st);
+    }
+}
+
+}  // namespace
+
+// x_perm[p] = x[row_token[p]] for the routed positions p < T*k (16-byte copies).
+__global__ void gather_rows_kernel(const uint4 *__restrict__ x, const int *__restrict__ row_token, int n_rows,
+                                   int row_vecs, uint4 *__restrict__ out)
+{
+    long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    long long total = (long long)n_rows * row_vecs;
+    for (; i < total; i += (long long)gridDim.x * blockDim.x) {
+        const long long p = i / row_vecs, c = i % row_vecs;
+        out[i] = x[(long long)row_token[p] * row_vecs + c];
+    }
+}
+
+cudaError_t launch_gather_rows(const Plan &p, const uint16_t *x, cudaStream_t st)
+{
+    const int n = p.T * p.k;
+    if (n == 0)
+        return cudaSuccess;
+    const int row_vecs = p.H / 8;
+    long long total = (long long)n * row_vecs;
+    long long blocks = (total + 255) / 256;
+    if (blocks > 4 * 152 * 8)
+        blocks = 4 * 152 * 8;
+    gather_rows_kernel<<<(unsigned)blocks, 256, 0, st>>>(reinterpret_cast<const uint4 *>(x), p.row_token, n, row_vecs,
+                                                         reinterpret_cast<uint4 *>(p.x_perm));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_gate_up_tc(const Plan &p, const WeightStore &w, int fmt, const uint16_t *x, cudaStream_t st)
+{
+    TcArgs a{w.base, w.group_bytes, w.kchunks, w.chunk_bytes, w.row_tiles, p.grp_start, p.grp_count, p.E, p.G,
+             p.I, p.H, p.h, (long long)p.P * p.I, nullptr, p.err};
+    CUtensorMap m1, m2;
+    cudaError_t e = make_map(&m2, x, p.T, p.H);
+    if (e != cudaSuccess)
+        return e;
+    if (p.T * p.k > 0) {
+        if ((e = make_map(&m1, p.x_perm, (long long)p.T * p.k, p.H)) != cudaSuccess)
+            return e;
+    } else {
+        m1 = m2;
+    }
+    return launch_any<true>(a, fmt, p.T, m1, m2, st);
+}
+
+cudaError_t launch_gemm_down_tc(const Plan &p, const WeightStore &w, int fmt, cudaStream_t st)
+{
+    TcArgs a{w.base, w.group_bytes, w.kchunks, w.chunk_bytes, w.row_tiles, p.grp_start, p.grp_count, p.E, p.G,
+             p.I, p.H, nullptr, 0, p.y, p.err};
+    CUtensorMap m1, m2;
+    cudaError_t e = make_map(&m1, p.h, p.P, p.I);
+    if (e != cudaSuccess)
+        return e;
+    if ((e = make_map(&m2, p.h + (size_t)p.P * p.I, p.P, p.I)) != cudaSuccess)
+        return e;
+    return launch_any<false>(a, fmt, p.T, m1, m2, st);
+}
+
+}  // namespace moe

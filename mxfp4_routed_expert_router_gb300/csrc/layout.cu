@@ -1,6 +1,7 @@
 // layout.cu -- load-time weight repack, dense-layer plan, and the weighted
 // unpermute-combine of expert outputs into the FP32 result.
 #include "moe_internal.cuh"
+#include "mx_decode.cuh"
 
 namespace moe {
 
@@ -40,16 +41,24 @@ __global__ void repack_kernel(int fmt, int gate_up, SrcMat gate, SrcMat up, uint
     uint8_t *chunk = dst + ((long long)tile * kchunks + kc) * chunk_bytes;
     int k0 = kc * CHUNK_K;
     if (fmt == FMT_MXFP4) {
-        uint8_t *codes = chunk + r * (CHUNK_K / 2);
-        uint8_t *scales = chunk + CHUNK_MX_CODE_BYTES + r * (CHUNK_K / 32);
-        for (int j = 0; j < CHUNK_K / 2; ++j) {
-            int k = k0 + 2 * j;
-            uint8_t b = 0;
-            if (srow >= 0 && k < K)
-                b = src->codes[srow * src->code_stride + k / 2];
-            codes[j] = b;
-        }
+        // 4 blocks of 32 elements; block b lives in half b/2 at 16*(b%2)
         for (int b = 0; b < CHUNK_K / 32; ++b) {
+            uint32_t *words = reinterpret_cast<uint32_t *>(chunk + (b / 2) * (CHUNK_MX_CODE_BYTES / 2) + r * 32 +
+                                                           (b % 2) * 16);
+            for (int c = 0; c < 4; ++c) {
+                uint32_t w = 0;
+                for (int i = 0; i < 8; ++i) {
+                    int k = k0 + 32 * b + 8 * c + i;
+                    uint32_t code = 0;
+                    if (srow >= 0 && k < K) {
+                        uint8_t byte = src->codes[srow * src->code_stride + k / 2];
+                        code = (k & 1) ? (byte >> 4) : (byte & 0xF);
+                    }
+                    w |= (code & 7u) << (4 * i);
+                    w |= (code >> 3) << repacked_sign_bit(i);
+                }
+                words[c] = w;
+            }
             int k = k0 + 32 * b;
             uint8_t e = 127;
             if (srow >= 0 && k < K) {
@@ -57,16 +66,18 @@ __global__ void repack_kernel(int fmt, int gate_up, SrcMat gate, SrcMat up, uint
                 if (e == 255)
                     atomicOr(bad_scale, 1);
             }
-            scales[b] = e;
+            chunk[CHUNK_MX_CODE_BYTES + r * (CHUNK_K / 32) + b] = e;
         }
     } else {
-        uint16_t *vals = reinterpret_cast<uint16_t *>(chunk) + r * CHUNK_K;
-        for (int j = 0; j < CHUNK_K; ++j) {
-            int k = k0 + j;
-            uint16_t v = 0;
-            if (srow >= 0 && k < K)
-                v = reinterpret_cast<const uint16_t *>(src->codes + srow * src->code_stride)[k];
-            vals[j] = v;
+        for (int h = 0; h < 2; ++h) {
+            uint16_t *vals = reinterpret_cast<uint16_t *>(chunk + h * (CHUNK_BF16_BYTES / 2) + r * HALF_K * 2);
+            for (int j = 0; j < HALF_K; ++j) {
+                int k = k0 + h * HALF_K + j;
+                uint16_t v = 0;
+                if (srow >= 0 && k < K)
+                    v = reinterpret_cast<const uint16_t *>(src->codes + srow * src->code_stride)[k];
+                vals[j] = v;
+            }
         }
     }
 }

@@ -5,6 +5,7 @@
 #include <stdarg.h>
 #include <stdint.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <new>
@@ -22,6 +23,7 @@ struct MoeHandle {
     int fmt = 0;
     int k_max = 0;
     int device = 0;
+    bool simt = false;         // MOE_GEMM_ENGINE=simt selects the CUDA-core GEMMs (validation aid)
     WeightStore gu, dn;
     int *err_host = nullptr;   // mapped pinned host memory, written by kernels on device-side errors
     int *err_dev = nullptr;    // device alias of err_host
@@ -96,6 +98,7 @@ size_t plan_layout(const MoeHandle *h, int T, int k, char *base, Plan *p)
     q.grp_start = (int *)take(sizeof(int) * G);
     q.grp_count = (int *)take(sizeof(int) * G);
     q.row_token = (int *)take(sizeof(int) * P);
+    q.x_perm = (uint16_t *)take(sizeof(uint16_t) * (size_t)(n > 0 ? n : 1) * H);
     q.h = (uint16_t *)take(2 * sizeof(uint16_t) * (size_t)P * I);
     q.y = (float *)take(sizeof(float) * (size_t)P * H);
     q.err = h->err_dev;
@@ -144,10 +147,18 @@ MoeStatus run_layer(MoeHandle *h, const void *x, const float *logits, int T, int
             return cuda_fail(e, "dense plan launch");
     }
     mark(2);
-    if ((e = launch_gemm_gate_up(p, h->gu, h->fmt, (const uint16_t *)x, st)) != cudaSuccess)
-        return cuda_fail(e, "gate/up launch");
+    if (h->simt) {
+        if ((e = launch_gemm_gate_up(p, h->gu, h->fmt, (const uint16_t *)x, st)) != cudaSuccess)
+            return cuda_fail(e, "gate/up launch");
+    } else {
+        if ((e = launch_gather_rows(p, (const uint16_t *)x, st)) != cudaSuccess)
+            return cuda_fail(e, "gather launch");
+        if ((e = launch_gemm_gate_up_tc(p, h->gu, h->fmt, (const uint16_t *)x, st)) != cudaSuccess)
+            return cuda_fail(e, "gate/up launch");
+    }
     mark(3);
-    if ((e = launch_gemm_down(p, h->dn, h->fmt, st)) != cudaSuccess)
+    if ((e = h->simt ? launch_gemm_down(p, h->dn, h->fmt, st) : launch_gemm_down_tc(p, h->dn, h->fmt, st)) !=
+        cudaSuccess)
         return cuda_fail(e, "down launch");
     mark(4);
     if ((e = launch_combine(p, out, accumulate, st)) != cudaSuccess)
@@ -239,6 +250,10 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
     if (e != cudaSuccess) {
         destroy(h);
         return cuda_fail(e, "cudaGetDevice");
+    }
+    {
+        const char *eng = getenv("MOE_GEMM_ENGINE");
+        h->simt = eng && strcmp(eng, "simt") == 0;
     }
     init_store(h->gu, I, true, c.hidden, fmt);
     init_store(h->dn, c.hidden, false, I, fmt);

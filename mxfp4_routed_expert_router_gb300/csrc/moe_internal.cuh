@@ -16,10 +16,12 @@ namespace moe {
 // consecutive along K; row tiles of one group are consecutive; groups are
 // consecutive.
 //
-// MXFP4 chunk (CHUNK_MX_BYTES):
-//   [0, 8192)     codes: 128 rows x 64 bytes (128 elements of a row)
-//   [8192, 8704)  scales: 128 rows x 4 E8M0 bytes (one per 32 elements)
-// BF16 chunk (CHUNK_BF16_BYTES): 128 rows x 128 BF16 values, row-major.
+// MXFP4 chunk (CHUNK_MX_BYTES), K = 128 elements split into two halves of 64:
+//   [h*4096 + r*32, +32)  half h (h = 0, 1) of row r: two 16-byte blocks of 32
+//                         elements, each block 4 repacked words (mx_decode.cuh)
+//   [8192 + r*4, +4)      E8M0 scales of row r, one per 32 elements
+// BF16 chunk (CHUNK_BF16_BYTES): [h*16384 + r*128, +128) = 64 BF16 values of
+//   half h of row r.
 //
 // Row order inside a row tile:
 //   gate|up matrices: tile row r = 32*q + l (q = r / 32, l = r % 32) holds
@@ -28,9 +30,6 @@ namespace moe {
 //     the same warp of the epilogue.  A tile covers 64 intermediate features.
 //   down matrices: tile row r holds output feature 128*tile + r.
 // Rows past the logical end, and K past the logical end, are zero codes.
-//
-// Code order inside a 64-byte row segment: see moe::code_byte_index() in
-// layout.cu (the decode kernels read exactly that order).
 constexpr int TILE_ROWS = 128;
 constexpr int CHUNK_K = 128;
 constexpr int GU_FEATURES_PER_TILE = 64;
@@ -38,6 +37,7 @@ constexpr int CHUNK_MX_CODE_BYTES = TILE_ROWS * CHUNK_K / 2;        // 8192
 constexpr int CHUNK_MX_SCALE_BYTES = TILE_ROWS * CHUNK_K / 32;      // 512
 constexpr int CHUNK_MX_BYTES = CHUNK_MX_CODE_BYTES + CHUNK_MX_SCALE_BYTES;  // 8704
 constexpr int CHUNK_BF16_BYTES = TILE_ROWS * CHUNK_K * 2;           // 32768
+constexpr int HALF_K = CHUNK_K / 2;                                 // K of one pipeline stage
 
 enum WeightFormat { FMT_MXFP4 = 0, FMT_BF16 = 1 };
 
@@ -79,6 +79,7 @@ struct Plan {
     int *grp_start;           // [G]
     int *grp_count;           // [G]
     int *row_token;           // [P] token index of each position
+    uint16_t *x_perm;         // [T*k][H] BF16 rows of x gathered in routed position order
     uint16_t *h;              // [2][P][I] BF16: h = hi plane + lo plane (lo = bf16(h - hi))
     float *y;                 // [P][H] FP32
     int *err;                 // device-visible error flag (mapped host memory)
@@ -110,5 +111,11 @@ cudaError_t launch_gemm_gate_up(const Plan &p, const WeightStore &w, int fmt, co
 cudaError_t launch_gemm_down(const Plan &p, const WeightStore &w, int fmt, cudaStream_t st);
 
 cudaError_t launch_combine(const Plan &p, float *out, int accumulate, cudaStream_t st);
+
+cudaError_t launch_gather_rows(const Plan &p, const uint16_t *x, cudaStream_t st);
+
+cudaError_t launch_gemm_gate_up_tc(const Plan &p, const WeightStore &w, int fmt, const uint16_t *x, cudaStream_t st);
+
+cudaError_t launch_gemm_down_tc(const Plan &p, const WeightStore &w, int fmt, cudaStream_t st);
 
 }  // namespace moe

@@ -1,0 +1,123 @@
+"""CPU emulation of the GPU's in-register MXFP4 -> BF16 decode.
+
+The CUDA kernels decode repacked 32-bit words with byte permutes (PRMT) and a
+BF16 multiply (mx_decode.cuh).  This test emulates those exact bit operations
+in Python for every code and sign pattern and compares the result with the
+E2M1 table printed on the page (tests/golden/e2m1_table.txt) times 2^(e-127).
+The repack bit layout it emulates is the one documented in mx_decode.cuh.
+"""
+import math
+import os
+import struct
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "e2m1_table.txt")
+
+MAG_HI_0, MAG_HI_1 = 0x3F3F3F00, 0x40404040
+MAG_LO_0, MAG_LO_1 = 0xC0800000, 0xC0804000
+
+
+def table():
+    t = {}
+    for line in open(GOLDEN):
+        line = line.split("#")[0].strip()
+        if line:
+            c, v = line.split()
+            t[int(c)] = float(v)
+    return t
+
+
+def prmt(a, b, sel):
+    src = [(a >> (8 * i)) & 0xFF for i in range(4)] + [(b >> (8 * i)) & 0xFF for i in range(4)]
+    d = 0
+    for i in range(4):
+        n = (sel >> (4 * i)) & 0xF
+        byte = src[n & 7]
+        if n & 8:
+            byte = 0xFF if byte & 0x80 else 0x00
+        d |= byte << (8 * i)
+    return d
+
+
+def sign_bit(i):
+    return 8 * i + 7 if i < 4 else 8 * (i - 4) + 3
+
+
+def repack_word(codes8):
+    w = 0
+    for i, c in enumerate(codes8):
+        w |= (c & 7) << (4 * i)
+        w |= (c >> 3) << sign_bit(i)
+    return w
+
+
+def bf16_bits_value(b):
+    return struct.unpack("<f", struct.pack("<I", (b & 0xFFFF) << 16))[0]
+
+
+def to_bf16_exact(x):
+    """x must be exactly representable in BF16 (possibly subnormal)."""
+    f = np.float32(x)
+    assert float(f) == x or (x != 0 and math.isinf(float(f)))
+    b = int(f.view(np.uint32))
+    assert b & 0xFFFF == 0, x
+    return b >> 16
+
+
+def bf16x2_mul(a, b):
+    out = 0
+    for half in range(2):
+        x = bf16_bits_value(a >> (16 * half))
+        y = bf16_bits_value(b >> (16 * half))
+        p = x * y
+        out |= to_bf16_exact(p) << (16 * half)
+    return out
+
+
+def e8m0_to_bf16x2(e):
+    b = (e << 7) if e else 0x0040
+    return b | (b << 16)
+
+
+def decode_word(w, s2):
+    m = w & 0x77777777
+    mh = m >> 16
+    h0 = prmt(MAG_HI_0, MAG_HI_1, m)
+    l0 = prmt(MAG_LO_0, MAG_LO_1, m)
+    h1 = prmt(MAG_HI_0, MAG_HI_1, mh)
+    l1 = prmt(MAG_LO_0, MAG_LO_1, mh)
+    h0 |= w & 0x80808080
+    h1 |= ((w << 4) & 0xFFFFFFFF) & 0x80808080
+    return [bf16x2_mul(prmt(l0, h0, 0x5140), s2), bf16x2_mul(prmt(l0, h0, 0x7362), s2),
+            bf16x2_mul(prmt(l1, h1, 0x5140), s2), bf16x2_mul(prmt(l1, h1, 0x7362), s2)]
+
+
+def unpack(outs):
+    vals = []
+    for r in outs:
+        vals.append(bf16_bits_value(r))
+        vals.append(bf16_bits_value(r >> 16))
+    return vals
+
+
+def expect(code, e, tab):
+    v = Fraction(tab[code]) * Fraction(2) ** (e - 127)
+    return math.copysign(float(v), tab[code]) if v == 0 else float(v)
+
+
+@pytest.mark.parametrize("e", [0, 1, 2, 64, 120, 126, 127, 128, 130, 200, 252])
+def test_every_code_in_every_position(e):
+    tab = table()
+    s2 = e8m0_to_bf16x2(e)
+    rng = np.random.default_rng(e)
+    words = [list(range(i, i + 8)) for i in (0, 8)]          # all 16 codes, each position
+    words += [[(c + s) % 16 for c in range(8)] for s in range(16)]
+    words += [rng.integers(0, 16, 8).tolist() for _ in range(50)]
+    for codes in words:
+        got = unpack(decode_word(repack_word(codes), s2))
+        for i, c in enumerate(codes):
+            want = expect(c, e, tab)
+            assert got[i] == want and math.copysign(1, got[i]) == math.copysign(1, want), (e, codes, i)
