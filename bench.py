@@ -395,9 +395,14 @@ def main():
     ap.add_argument("--workload", default="decode_T1")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="profiling aid: routed experts of a smaller layer with the same shapes per expert")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     cfg = workload(args.workload)
+    if args.experts:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, name=f"{cfg.name}_E{args.experts}", n_experts=args.experts)
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
 

@@ -32,149 +32,22 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
-#include "moe_internal.cuh"
+#include "gemm_common.cuh"
 #include "mx_decode.cuh"
 
 namespace moe {
 
 namespace {
 
+using namespace gemm;
+
 constexpr int NUM_THREADS = 480;
 constexpr int WARP_WLOAD = 0, WARP_BLOAD = 1, WARP_MMA = 2, WARP_DEC0 = 3, N_DEC_WARPS = 8, WARP_EPI0 = 11;
 constexpr int A_STAGE_BYTES = TILE_ROWS * HALF_K * 2;  // 16 KB: 128 rows x 64 BF16
 constexpr int B_BOX_ROWS = 16;
 constexpr int B_BOX_BYTES = B_BOX_ROWS * HALF_K * 2;   // 2 KB
-constexpr int MAX_GROUPS = 1088;
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 
-struct TcArgs {
-    const uint8_t *wbase;
-    size_t group_bytes;
-    int kchunks, chunk_bytes, row_tiles;
-    const int *grp_start, *grp_count;
-    int E, G, I, H;
-    uint16_t *h_out;
-    long long h_plane;
-    float *y_out;
-    int *err;
-};
-
-// ------------------------------------------------------------------ PTX helpers
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ uint64_t global_ns()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Bounded wait (one thread) for the phase with the given parity.  Gives up
-// after WAIT_LIMIT_NS, recording DEV_ERR_WAIT_TIMEOUT and raising the CTA's
-// abort flag, or as soon as another role has raised it.  Returns true when
-// the phase completed.
-__device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *err)
-{
-    if (mbar_try_wait(bar, parity))
-        return true;
-    const uint64_t t0 = global_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity))
-            return true;
-        if ((i & 63u) == 0) {
-            if (*abort_flag)
-                return false;
-            if (global_ns() - t0 > WAIT_LIMIT_NS) {
-                atomicCAS(err, 0, DEV_ERR_WAIT_TIMEOUT);
-                *abort_flag = 1;
-                return false;
-            }
-        }
-    }
-}
-
-// The same, taken by a whole warp: every lane observes the phase, and the
-// outcome is uniform across the warp (so warp-collective instructions that
-// follow never run with a partial warp).
-__device__ __noinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *err)
-{
-    uint64_t t0 = 0;
-    for (uint32_t i = 0;; ++i) {
-        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity)))
-            return true;
-        if ((i & 63u) == 63u) {
-            if (i == 63u)
-                t0 = global_ns();
-            bool stop = *abort_flag != 0;
-            if (!stop && global_ns() - t0 > WAIT_LIMIT_NS) {
-                atomicCAS(err, 0, DEV_ERR_WAIT_TIMEOUT);
-                *abort_flag = 1;
-                stop = true;
-            }
-            if (__any_sync(0xffffffffu, stop))
-                return false;
-        }
-    }
-}
-
-// Bounded wait used while tearing down: true when the phase completed.
-__device__ __noinline__ bool mbar_drain(uint64_t *bar, uint32_t parity)
-{
-    const uint64_t t0 = global_ns();
-    for (;;) {
-        if (mbar_try_wait(bar, parity))
-            return true;
-        if (global_ns() - t0 > WAIT_LIMIT_NS)
-            return false;
-    }
-}
-
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_addr(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-        "[%4];" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
-        : "memory");
-}
+using TcArgs = GemmArgs;
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -233,40 +106,6 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int c)
     return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
-// ------------------------------------------------------------------ schedule
-
-struct WorkItem {
-    int g, rt, tok0, nvalid, n_mma;
-};
-
-// prefix[g] = first work item of group g; work items of a group are ordered
-// row tile major, token tile minor, so that CTAs running neighbouring items
-// share the weight chunk through L2.
-__device__ __forceinline__ WorkItem decompose(int t, const int *prefix, const int *counts, int G, int row_tiles,
-                                              int nmax)
-{
-    int lo = 0, hi = G;  // find g with prefix[g] <= t < prefix[g+1]
-    while (hi - lo > 1) {
-        int mid = (lo + hi) >> 1;
-        if (prefix[mid] <= t)
-            lo = mid;
-        else
-            hi = mid;
-    }
-    WorkItem w;
-    w.g = lo;
-    const int cnt = counts[lo];
-    const int ntiles = (cnt + nmax - 1) / nmax;
-    const int local = t - prefix[lo];
-    w.rt = local / ntiles;
-    const int nt = local % ntiles;
-    const int per = (((cnt + ntiles - 1) / ntiles) + 15) & ~15;
-    w.tok0 = nt * per;
-    w.nvalid = min(per, cnt - w.tok0);
-    w.n_mma = (w.nvalid + 15) & ~15;
-    return w;
-}
-
 template <int NMAX, int NB, int S, int R, int RAW_BYTES>
 struct Smem {
     static constexpr int B_STAGE = NMAX * HALF_K * 2 * NB;
@@ -277,7 +116,7 @@ struct Smem {
     static constexpr int N_BARS = 2 * R + 2 * S + 4;
     static constexpr int SCHED_OFF = BAR_OFF + N_BARS * 8;
     static constexpr int MISC_OFF = SCHED_OFF + (MAX_GROUPS + 1) * 4;
-    static constexpr int TOTAL = MISC_OFF + 16 + 1024;  // + alignment slack
+    static constexpr int TOTAL = MISC_OFF + 32 + 1024;  // + alignment slack
 };
 
 // ------------------------------------------------------------------ kernel
@@ -327,27 +166,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    if (warp == WARP_WLOAD) {
-        // work-item prefix over groups (one warp scan, 32 groups per step)
-        int run = 0;
-        for (int base = 0; base < a.G; base += 32) {
-            int g = base + lane;
-            int cnt = g < a.G ? a.grp_count[g] : 0;
-            int v = ((cnt + NMAX - 1) / NMAX) * a.row_tiles;
-            int incl = v;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                int n = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o)
-                    incl += n;
-            }
-            if (g < a.G)
-                prefix[g] = run + incl - v;
-            run += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        if (lane == 0)
-            prefix[a.G] = run;
-    }
+    if (warp == WARP_WLOAD)
+        schedule_prefix(a.grp_count, a.G, a.row_tiles, NMAX, prefix, lane);
     if (warp == WARP_BLOAD && lane == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b2)) : "memory");
@@ -359,60 +179,64 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int total = prefix[a.G];
     const int nstages = 2 * a.kchunks;
 
+    // Every role walks the same static schedule t = blockIdx.x, +gridDim.x, ...
+    // Single-thread roles keep the whole warp in the loop (lane 0 issues) so
+    // that no lanes sit parked at a warp barrier while lane 0 works.
     if (warp == WARP_WLOAD) {
-        if (lane == 0) {
-            uint32_t rc = 0, armed = 0, armed_par = 0;
-            for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
-                WorkItem w = decompose(t, prefix, a.grp_count, a.G, a.row_tiles, NMAX);
-                const uint8_t *src =
-                    a.wbase + (size_t)w.g * a.group_bytes + (size_t)w.rt * a.kchunks * (size_t)a.chunk_bytes;
-                bool ok = true;
-                for (int kc = 0; kc < a.kchunks; ++kc, ++rc) {
-                    const int slot = rc % R;
-                    const uint32_t ph = (rc / R) & 1;
-                    if (!(ok = mbar_wait(&raw_empty[slot], ph ^ 1, abort_flag, a.err)))
-                        break;
+        // ---------------------------------------------------------- weight chunks -> raw ring
+        uint32_t rc = 0, armed = 0, armed_par = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const WorkItem w = decompose(t, prefix, a.grp_count, a.G, a.row_tiles, NMAX);
+            const uint8_t *src =
+                a.wbase + (size_t)w.g * a.group_bytes + (size_t)w.rt * a.kchunks * (size_t)a.chunk_bytes;
+            for (int kc = 0; kc < a.kchunks; ++kc, ++rc) {
+                const int slot = rc % R;
+                const uint32_t ph = (rc / R) & 1;
+                if (!(ok = mbar_wait_warp(&raw_empty[slot], ph ^ 1, abort_flag, a.err, lane)))
+                    break;
+                if (lane == 0) {
                     mbar_arrive_expect_tx(&raw_full[slot], RAW_BYTES);
                     bulk_g2s(smem + L::RAW_OFF + slot * RAW_BYTES, src + (size_t)kc * a.chunk_bytes, RAW_BYTES,
                              &raw_full[slot]);
-                    armed |= 1u << slot;
-                    armed_par = (armed_par & ~(1u << slot)) | (ph << slot);
                 }
-                if (!ok)
-                    break;
+                armed |= 1u << slot;
+                armed_par = (armed_par & ~(1u << slot)) | (ph << slot);
             }
-            // drain: every armed raw buffer's last copy has landed
+        }
+        // drain: every armed raw buffer's last copy has landed
+        if (lane == 0)
             for (int s = 0; s < R; ++s)
                 if (armed & (1u << s))
                     mbar_drain(&raw_full[s], (armed_par >> s) & 1);
-        }
         __syncwarp();
     } else if (warp == WARP_BLOAD) {
-        if (lane == 0) {
-            uint32_t sc = 0, armed = 0, armed_par = 0;
-            for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
-                WorkItem w = decompose(t, prefix, a.grp_count, a.G, a.row_tiles, NMAX);
-                int row0;
-                const CUtensorMap *m0 = &map_b;
-                if (GU) {
-                    // routed groups read gathered rows by position, shared groups x by token
-                    if (w.g < a.E) {
-                        row0 = a.grp_start[w.g] + w.tok0;
-                    } else {
-                        row0 = w.tok0;
-                        m0 = &map_b2;
-                    }
-                } else {
+        // ---------------------------------------------------------- token tiles (B) -> stage ring
+        uint32_t sc = 0, armed = 0, armed_par = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const WorkItem w = decompose(t, prefix, a.grp_count, a.G, a.row_tiles, NMAX);
+            int row0;
+            const CUtensorMap *m0 = &map_b;
+            if (GU) {
+                // routed groups read gathered rows by position, shared groups x by token
+                if (w.g < a.E) {
                     row0 = a.grp_start[w.g] + w.tok0;
+                } else {
+                    row0 = w.tok0;
+                    m0 = &map_b2;
                 }
-                const int nbox = w.n_mma / B_BOX_ROWS;
-                const uint32_t bytes = (uint32_t)(nbox * B_BOX_BYTES * NB);
-                bool ok = true;
-                for (int st = 0; st < nstages; ++st, ++sc) {
-                    const int slot = sc % S;
-                    const uint32_t ph = (sc / S) & 1;
-                    if (!(ok = mbar_wait(&ab_empty[slot], ph ^ 1, abort_flag, a.err)))
-                        break;
+            } else {
+                row0 = a.grp_start[w.g] + w.tok0;
+            }
+            const int nbox = w.n_mma / B_BOX_ROWS;
+            const uint32_t bytes = (uint32_t)(nbox * B_BOX_BYTES * NB);
+            for (int st = 0; st < nstages; ++st, ++sc) {
+                const int slot = sc % S;
+                const uint32_t ph = (sc / S) & 1;
+                if (!(ok = mbar_wait_warp(&ab_empty[slot], ph ^ 1, abort_flag, a.err, lane)))
+                    break;
+                if (lane == 0) {
                     mbar_arrive_expect_tx(&ab_full[slot], bytes);
                     uint8_t *bdst = smem + L::B_OFF + slot * L::B_STAGE;
                     for (int b = 0; b < nbox; ++b) {
@@ -421,39 +245,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             tma_2d(bdst + NMAX * HALF_K * 2 + b * B_BOX_BYTES, &map_b2, st * HALF_K,
                                    row0 + b * B_BOX_ROWS, &ab_full[slot]);
                     }
-                    armed |= 1u << slot;
-                    armed_par = (armed_par & ~(1u << slot)) | (ph << slot);
                 }
-                if (!ok)
-                    break;
+                armed |= 1u << slot;
+                armed_par = (armed_par & ~(1u << slot)) | (ph << slot);
             }
-            // drain: every armed stage's B tiles have landed and been consumed (returns at
-            // once on the normal path; bounded after an abort)
+        }
+        // drain: every armed stage's B tiles have landed (returns at once on the
+        // normal path, where the MMA has consumed them; bounded after an abort)
+        if (lane == 0)
             for (int s = 0; s < S; ++s)
                 if (armed & (1u << s))
                     mbar_drain(&ab_full[s], (armed_par >> s) & 1);
-        }
         __syncwarp();
     } else if (warp == WARP_MMA) {
-        if (lane == 0) {
-            uint32_t sc = 0, tc = 0;
-            bool issued = false;
-            uint32_t last_acc = 0, last_par = 0;
-            for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x, ++tc) {
-                WorkItem w = decompose(t, prefix, a.grp_count, a.G, a.row_tiles, NMAX);
-                const int buf = tc & 1;
-                const uint32_t aph = (tc >> 1) & 1;
-                if (!mbar_wait(&acc_empty[buf], aph ^ 1, abort_flag, a.err))
+        // ---------------------------------------------------------- MMA issue (lane 0)
+        uint32_t sc = 0, tc = 0, last_acc = 0, last_par = 0;
+        bool issued = false, ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
+            const WorkItem w = decompose(t, prefix, a.grp_count, a.G, a.row_tiles, NMAX);
+            const int buf = tc & 1;
+            const uint32_t aph = (tc >> 1) & 1;
+            if (!(ok = mbar_wait_warp(&acc_empty[buf], aph ^ 1, abort_flag, a.err, lane)))
+                break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(buf * NMAX);
+            const uint32_t idesc = idesc_bf16(w.n_mma);
+            for (int st = 0; st < nstages; ++st, ++sc) {
+                const int slot = sc % S;
+                if (!(ok = mbar_wait_warp(&ab_full[slot], (sc / S) & 1, abort_flag, a.err, lane)))
                     break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(buf * NMAX);
-                const uint32_t idesc = idesc_bf16(w.n_mma);
-                bool ok = true;
-                for (int st = 0; st < nstages; ++st, ++sc) {
-                    const int slot = sc % S;
-                    if (!(ok = mbar_wait(&ab_full[slot], (sc / S) & 1, abort_flag, a.err)))
-                        break;
-                    tc_fence_after();
+                if (lane == 0) {
                     const uint32_t a_addr = smem_addr(smem + L::A_OFF + slot * A_STAGE_BYTES);
                     const uint32_t b_addr = smem_addr(smem + L::B_OFF + slot * L::B_STAGE);
 #pragma unroll
@@ -464,34 +286,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             tc_mma(d_tmem, ad, sw128_desc(b_addr + NMAX * HALF_K * 2 + j * 32), idesc, 1u);
                     }
                     tc_commit(&ab_empty[slot]);
-                    issued = true;
                 }
-                if (!ok)
-                    break;
-                tc_commit(&acc_full[buf]);
-                last_acc = buf;
-                last_par = aph;
+                __syncwarp();
+                issued = true;
             }
-            // drain: the MMAs of the last committed item have completed
-            if (issued)
-                mbar_drain(&acc_full[last_acc], last_par);
+            if (!ok)
+                break;
+            if (lane == 0)
+                tc_commit(&acc_full[buf]);
+            __syncwarp();
+            last_acc = buf;
+            last_par = aph;
         }
+        // drain: the MMAs of the last committed item have completed
+        if (lane == 0 && issued)
+            mbar_drain(&acc_full[last_acc], last_par);
         __syncwarp();
     } else if (warp < WARP_EPI0) {
         // ---------------------------------------------------------- decoders
+        // Each warp waits for itself (lane 0 polls) and arrives on ab_full
+        // once, so the 8 decoder warps never stall behind one another.
         const int dt = tid - WARP_DEC0 * 32;   // 0..255
         const int r = dt >> 1, blk = dt & 1;   // tile row, 32-element block of the 64-wide stage
         uint32_t rc = 0, sc = 0;
-        for (int t = blockIdx.x; t < total && !__any_sync(0xffffffffu, *abort_flag); t += gridDim.x) {
-            bool ok = true;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
             for (int kc = 0; kc < a.kchunks && ok; ++kc, ++rc) {
                 const int rslot = rc % R;
-                if (!(ok = mbar_wait_warp(&raw_full[rslot], (rc / R) & 1, abort_flag, a.err)))
+                if (!(ok = mbar_wait_warp(&raw_full[rslot], (rc / R) & 1, abort_flag, a.err, lane)))
                     break;
                 const uint8_t *raw = smem + L::RAW_OFF + rslot * RAW_BYTES;
                 for (int h = 0; h < 2; ++h, ++sc) {
                     const int slot = sc % S;
-                    if (!(ok = mbar_wait_warp(&ab_empty[slot], ((sc / S) & 1) ^ 1, abort_flag, a.err)))
+                    if (!(ok = mbar_wait_warp(&ab_empty[slot], ((sc / S) & 1) ^ 1, abort_flag, a.err, lane)))
                         break;
                     uint8_t *adst = smem + L::A_OFF + slot * A_STAGE_BYTES;
                     if (WFMT == FMT_MXFP4) {
@@ -518,21 +345,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (lane == 0)
                         mbar_arrive(&ab_full[slot]);
                 }
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&raw_empty[rslot]);
+                if (ok) {
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&raw_empty[rslot]);
+                }
             }
-            if (!ok)
-                break;
         }
     } else {
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;                 // TMEM lane quadrant of this warp
         uint32_t tc = 0;
-        for (int t = blockIdx.x; t < total && !__any_sync(0xffffffffu, *abort_flag); t += gridDim.x, ++tc) {
-            WorkItem w = decompose(t, prefix, a.grp_count, a.G, a.row_tiles, NMAX);
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
+            const WorkItem w = decompose(t, prefix, a.grp_count, a.G, a.row_tiles, NMAX);
             const int buf = tc & 1;
-            if (!mbar_wait_warp(&acc_full[buf], (tc >> 1) & 1, abort_flag, a.err))
+            if (!mbar_wait_warp(&acc_full[buf], (tc >> 1) & 1, abort_flag, a.err, lane))
                 break;
             tc_fence_after();
             const int pos0 = a.grp_start[w.g] + w.tok0;
@@ -541,12 +368,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 float v[16];
                 tmem_ld16(taddr + c0, v);
                 if (GU) {
-                    const int n = w.rt * GU_FEATURES_PER_TILE + 16 * q + (lane & 15);
-                    const bool up_lane = lane >= 16;
+                    // rows 16*gr + i: gate of feature 8*gr + i%8 when i < 8, up when i >= 8;
+                    // the gate lane finishes tokens c0..c0+7, its up partner (lane ^ 8) c0+8..c0+15
+                    const int n = gu_row_feature(w.rt, 32 * q + lane);
+                    const bool up_lane = gu_row_is_up(lane);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const float send = up_lane ? v[j] : v[8 + j];
-                        const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+                        const float recv = __shfl_xor_sync(0xffffffffu, send, 8);
                         const float gv = up_lane ? recv : v[j];
                         const float uv = up_lane ? v[8 + j] : recv;
                         const int tok = c0 + (up_lane ? 8 : 0) + j;
@@ -586,51 +415,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // ------------------------------------------------------------------ host side
-
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-// 2-D BF16 tensor [rows][cols] (row stride cols*2 bytes), box 64 x 16, 128B swizzle.
-cudaError_t make_map(CUtensorMap *m, const void *base, long long rows, int cols)
-{
-    auto enc = tensor_map_encoder();
-    if (!enc)
-        return cudaErrorNotSupported;
-    if (rows < 1)
-        rows = 1;
-    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {HALF_K, B_BOX_ROWS};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
-int sm_count()
-{
-    static int n = 0;
-    if (!n) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0)
-            n = 1;
-    }
-    return n;
-}
 
 template <bool GU, int WFMT, int NMAX, int S, int R>
 cudaError_t launch_cfg(const TcArgs &a, const CUtensorMap &m1, const CUtensorMap &m2, cudaStream_t st)
@@ -706,13 +490,13 @@ cudaError_t launch_gather_rows(const Plan &p, const uint16_t *x, cudaStream_t st
 cudaError_t launch_gemm_gate_up_tc(const Plan &p, const WeightStore &w, int fmt, const uint16_t *x, cudaStream_t st)
 {
     TcArgs a{w.base, w.group_bytes, w.kchunks, w.chunk_bytes, w.row_tiles, p.grp_start, p.grp_count, p.E, p.G,
-             p.I, p.H, p.h, (long long)p.P * p.I, nullptr, p.err};
+             p.I, p.H, p.h, (long long)p.P * p.I, nullptr, p.err, nullptr, nullptr, nullptr, nullptr, 0};
     CUtensorMap m1, m2;
-    cudaError_t e = make_map(&m2, x, p.T, p.H);
+    cudaError_t e = make_map(&m2, x, p.T, p.H, B_BOX_ROWS);
     if (e != cudaSuccess)
         return e;
     if (p.T * p.k > 0) {
-        if ((e = make_map(&m1, p.x_perm, (long long)p.T * p.k, p.H)) != cudaSuccess)
+        if ((e = make_map(&m1, p.x_perm, (long long)p.T * p.k, p.H, B_BOX_ROWS)) != cudaSuccess)
             return e;
     } else {
         m1 = m2;
@@ -723,12 +507,12 @@ cudaError_t launch_gemm_gate_up_tc(const Plan &p, const WeightStore &w, int fmt,
 cudaError_t launch_gemm_down_tc(const Plan &p, const WeightStore &w, int fmt, cudaStream_t st)
 {
     TcArgs a{w.base, w.group_bytes, w.kchunks, w.chunk_bytes, w.row_tiles, p.grp_start, p.grp_count, p.E, p.G,
-             p.I, p.H, nullptr, 0, p.y, p.err};
+             p.I, p.H, nullptr, 0, p.y, p.err, nullptr, nullptr, nullptr, nullptr, 0};
     CUtensorMap m1, m2;
-    cudaError_t e = make_map(&m1, p.h, p.P, p.I);
+    cudaError_t e = make_map(&m1, p.h, p.P, p.I, B_BOX_ROWS);
     if (e != cudaSuccess)
         return e;
-    if ((e = make_map(&m2, p.h + (size_t)p.P * p.I, p.P, p.I)) != cudaSuccess)
+    if ((e = make_map(&m2, p.h + (size_t)p.P * p.I, p.P, p.I, B_BOX_ROWS)) != cudaSuccess)
         return e;
     return launch_any<false>(a, fmt, p.T, m1, m2, st);
 }

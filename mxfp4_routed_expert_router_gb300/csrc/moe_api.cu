@@ -23,8 +23,8 @@ struct MoeHandle {
     int fmt = 0;
     int k_max = 0;
     int device = 0;
-    bool simt = false;         // MOE_GEMM_ENGINE=simt selects the CUDA-core GEMMs (validation aid)
-    WeightStore gu, dn;
+    WeightStore gu, dn;        // TILE layout (tensor-memory GEMMs, large batches)
+    WeightStore gu_f, dn_f;    // FRAG layout (register-streaming GEMMs, decode-sized batches)
     int *err_host = nullptr;   // mapped pinned host memory, written by kernels on device-side errors
     int *err_dev = nullptr;    // device alias of err_host
     bool profile = false;      // record stage events (moe_profile_enable)
@@ -99,6 +99,9 @@ size_t plan_layout(const MoeHandle *h, int T, int k, char *base, Plan *p)
     q.grp_count = (int *)take(sizeof(int) * G);
     q.row_token = (int *)take(sizeof(int) * P);
     q.x_perm = (uint16_t *)take(sizeof(uint16_t) * (size_t)(n > 0 ? n : 1) * H);
+    q.x16 = (uint16_t *)take(sizeof(uint16_t) * (size_t)T * H);
+    q.xs = (int *)take(sizeof(int) * (size_t)T);
+    q.hs = (int *)take(sizeof(int) * (size_t)P * ((I + 63) / 64));
     q.h = (uint16_t *)take(2 * sizeof(uint16_t) * (size_t)P * I);
     q.y = (float *)take(sizeof(float) * (size_t)P * H);
     q.err = h->err_dev;
@@ -147,18 +150,24 @@ MoeStatus run_layer(MoeHandle *h, const void *x, const float *logits, int T, int
             return cuda_fail(e, "dense plan launch");
     }
     mark(2);
-    if (h->simt) {
-        if ((e = launch_gemm_gate_up(p, h->gu, h->fmt, (const uint16_t *)x, st)) != cudaSuccess)
-            return cuda_fail(e, "gate/up launch");
-    } else {
-        if ((e = launch_gather_rows(p, (const uint16_t *)x, st)) != cudaSuccess)
-            return cuda_fail(e, "gather launch");
-        if ((e = launch_gemm_gate_up_tc(p, h->gu, h->fmt, (const uint16_t *)x, st)) != cudaSuccess)
-            return cuda_fail(e, "gate/up launch");
-    }
+    // Decode-sized batches (few tokens per expert) stream the weights through
+    // registers; larger batches use the tensor-memory GEMMs.
+    const bool stream = h->E > 0 ? (long long)T * k <= 16LL * h->E : T <= STREAM_MAX_T;
+    // token rows for the gate|up GEMM: FP16 (scaled per token) for the FP16
+    // streaming path, BF16 otherwise
+    if (stream && h->fmt == FMT_MXFP4)
+        e = launch_prep_x16(p, (const uint16_t *)x, st);
+    else
+        e = launch_gather_rows(p, (const uint16_t *)x, st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "gather launch");
+    e = stream ? launch_gemm_gate_up_stream(p, h->gu_f, h->fmt, (const uint16_t *)x, st)
+               : launch_gemm_gate_up_tc(p, h->gu, h->fmt, (const uint16_t *)x, st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "gate/up launch");
     mark(3);
-    if ((e = h->simt ? launch_gemm_down(p, h->dn, h->fmt, st) : launch_gemm_down_tc(p, h->dn, h->fmt, st)) !=
-        cudaSuccess)
+    e = stream ? launch_gemm_down_stream(p, h->dn_f, h->fmt, st) : launch_gemm_down_tc(p, h->dn, h->fmt, st);
+    if (e != cudaSuccess)
         return cuda_fail(e, "down launch");
     mark(4);
     if ((e = launch_combine(p, out, accumulate, st)) != cudaSuccess)
@@ -177,6 +186,14 @@ void destroy(MoeHandle *h)
         cudaFree(h->gu.base);
     if (h->dn.base)
         cudaFree(h->dn.base);
+    if (h->gu_f.base)
+        cudaFree(h->gu_f.base);
+    if (h->gu_f.rfac)
+        cudaFree(h->gu_f.rfac);
+    if (h->dn_f.rfac)
+        cudaFree(h->dn_f.rfac);
+    if (h->dn_f.base)
+        cudaFree(h->dn_f.base);
     if (h->err_host)
         cudaFreeHost(h->err_host);
     for (cudaEvent_t &ev : h->ev)
@@ -251,12 +268,11 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
         destroy(h);
         return cuda_fail(e, "cudaGetDevice");
     }
-    {
-        const char *eng = getenv("MOE_GEMM_ENGINE");
-        h->simt = eng && strcmp(eng, "simt") == 0;
-    }
     init_store(h->gu, I, true, c.hidden, fmt);
     init_store(h->dn, c.hidden, false, I, fmt);
+    h->gu_f = h->gu;
+    h->dn_f = h->dn;
+    const int f_layout = fmt == FMT_MXFP4 ? LAYOUT_FRAG_F16 : LAYOUT_FRAG;
     if ((e = cudaHostAlloc((void **)&h->err_host, 2 * sizeof(int), cudaHostAllocMapped)) != cudaSuccess) {
         destroy(h);
         return cuda_fail(e, "cudaHostAlloc");
@@ -268,11 +284,15 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
         return cuda_fail(e, "cudaHostGetDevicePointer");
     }
     if (cudaMalloc(&h->gu.base, h->gu.group_bytes * G) != cudaSuccess ||
-        cudaMalloc(&h->dn.base, h->dn.group_bytes * G) != cudaSuccess) {
+        cudaMalloc(&h->dn.base, h->dn.group_bytes * G) != cudaSuccess ||
+        cudaMalloc(&h->gu_f.base, h->gu_f.group_bytes * G) != cudaSuccess ||
+        cudaMalloc(&h->dn_f.base, h->dn_f.group_bytes * G) != cudaSuccess ||
+        cudaMalloc(&h->gu_f.rfac, sizeof(int16_t) * TILE_ROWS * h->gu_f.row_tiles * (size_t)G) != cudaSuccess ||
+        cudaMalloc(&h->dn_f.rfac, sizeof(int16_t) * TILE_ROWS * h->dn_f.row_tiles * (size_t)G) != cudaSuccess) {
         cudaGetLastError();
         destroy(h);
         return fail(MOE_ENOMEM, "device allocation of %zu bytes of weights failed",
-                    (h->gu.group_bytes + h->dn.group_bytes) * (size_t)G);
+                    2 * (h->gu.group_bytes + h->dn.group_bytes) * (size_t)G);
     }
     int *bad_scale = &h->err_dev[1];
     const long long esz = fmt == FMT_MXFP4 ? 1 : 2;  // bytes per code unit of a row (MXFP4: per 2 elements)
@@ -301,8 +321,14 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
             dn = {(const uint8_t *)down[g].codes, (const uint8_t *)down[g].scales, dstride, I / 32};
         }
         (void)esz;
-        if ((e = launch_repack(fmt, true, gate, up, h->gu, g, I, c.hidden, bad_scale, st)) != cudaSuccess ||
-            (e = launch_repack(fmt, false, dn, dn, h->dn, g, I, c.hidden, bad_scale, st)) != cudaSuccess) {
+        if ((e = launch_repack(fmt, LAYOUT_TILE, true, gate, up, h->gu, g, I, c.hidden, bad_scale, st)) !=
+                cudaSuccess ||
+            (e = launch_repack(fmt, LAYOUT_TILE, false, dn, dn, h->dn, g, I, c.hidden, bad_scale, st)) !=
+                cudaSuccess ||
+            (e = launch_repack(fmt, f_layout, true, gate, up, h->gu_f, g, I, c.hidden, bad_scale, st)) !=
+                cudaSuccess ||
+            (e = launch_repack(fmt, f_layout, false, dn, dn, h->dn_f, g, I, c.hidden, bad_scale, st)) !=
+                cudaSuccess) {
             destroy(h);
             return cuda_fail(e, "repack launch");
         }

@@ -16,18 +16,30 @@ namespace moe {
 // consecutive along K; row tiles of one group are consecutive; groups are
 // consecutive.
 //
-// MXFP4 chunk (CHUNK_MX_BYTES), K = 128 elements split into two halves of 64:
-//   [h*4096 + r*32, +32)  half h (h = 0, 1) of row r: two 16-byte blocks of 32
-//                         elements, each block 4 repacked words (mx_decode.cuh)
-//   [8192 + r*4, +4)      E8M0 scales of row r, one per 32 elements
-// BF16 chunk (CHUNK_BF16_BYTES): [h*16384 + r*128, +128) = 64 BF16 values of
-//   half h of row r.
+// Two chunk layouts are kept (two copies of every matrix; each kernel reads
+// only its own, so HBM traffic per call is that of one copy):
 //
-// Row order inside a row tile:
-//   gate|up matrices: tile row r = 32*q + l (q = r / 32, l = r % 32) holds
-//     feature n = 64*tile + 16*q + (l % 16) of W_g when l < 16 and of W_u
-//     when l >= 16, so that gate and up of one feature sit 16 lanes apart in
-//     the same warp of the epilogue.  A tile covers 64 intermediate features.
+// TILE layout (tcgen05 kernel), K = 128 split into two halves of 64:
+//   MXFP4: [h*4096 + r*32, +32)  half h of row r: two 16-byte blocks of 32
+//                                elements, each 4 repacked words (mx_decode.cuh)
+//          [8192 + r*4, +4)      E8M0 scales of row r, one per 32 elements
+//   BF16:  [h*16384 + r*128, +128)  64 BF16 values of half h of row r
+//
+// FRAG layout (register-streaming kernel): rows grouped by 16 (group w =
+// r / 16), K by 16 (step j = 0..7).  Thread t (g = t / 4, q = t % 4) of the
+// warp owning group w needs, per step j, the elements of the warp-level MMA
+// A fragment: (row g, k 2q..2q+1), (row g+8, k 2q..2q+1), (row g, k 2q+8..9),
+// (row g+8, k 2q+8..9) with k relative to 16j.
+//   MXFP4: word ((w*2 + j/4)*32 + t)*4 + j%4 holds those 8 elements in that
+//          order (repacked word format, mx_decode.cuh);
+//          [8192 + (w*8 + g)*8, +8)  scales: row 16w+g blocks 0..3, then row
+//                                    16w+g+8 blocks 0..3
+//   BF16:  [((w*8 + j)*32 + t)*16, +16)  the 8 BF16 values in that order
+//
+// Row order inside a row tile (both layouts): r = 16*w + i.
+//   gate|up matrices: feature n = 64*tile + 8*w + (i % 8), of W_g when i < 8
+//     and of W_u when i >= 8, so that gate and up of one feature are rows g
+//     and g+8 of the same 16-row group.  A tile covers 64 intermediate features.
 //   down matrices: tile row r holds output feature 128*tile + r.
 // Rows past the logical end, and K past the logical end, are zero codes.
 constexpr int TILE_ROWS = 128;
@@ -39,6 +51,34 @@ constexpr int CHUNK_MX_BYTES = CHUNK_MX_CODE_BYTES + CHUNK_MX_SCALE_BYTES;  // 8
 constexpr int CHUNK_BF16_BYTES = TILE_ROWS * CHUNK_K * 2;           // 32768
 constexpr int HALF_K = CHUNK_K / 2;                                 // K of one pipeline stage
 
+enum ChunkLayout { LAYOUT_TILE = 0, LAYOUT_FRAG = 1, LAYOUT_FRAG_F16 = 2 };
+
+// FRAG_F16 layout (register-streaming gate|up with FP16 operands): the same
+// fragment order as FRAG, but each word holds the 8 codes as 4 plain OCP E2M1
+// byte pairs (first element in the low nibble) so that the hardware
+// e2m1x2 -> f16x2 conversion decodes a byte per instruction:
+//   byte 0: (row g, k 2q, 2q+1), byte 1: (row g+8, k 2q, 2q+1),
+//   byte 2: (row g, k 2q+8, 2q+9), byte 3: (row g+8, k 2q+8, 2q+9).
+// Scale bytes hold 4*f with f = e - R_row - 112 clamped to [0, 30]: f is the
+// FP16 exponent field of the block multiplier 2^(e - 127 - R_row) (0 = block
+// flushed; only blocks 2^36 below the row's largest are), and 4*f placed in
+// the high byte of an FP16 is exactly that multiplier (one byte permute).  R_row = (max E8M0 of the row) -
+// 140 puts the row's largest block at 2^13 (6 * 2^13 < 65504); the epilogue
+// multiplies the row's result by 2^R_row, exactly.  R_row is kept per tile
+// row in WeightStore::rfac.
+constexpr int F16_ROW_HEADROOM = 140;
+
+// FP16 token rows (x16 and its gathered copies) store K in a permuted order
+// inside every 16-element group so that a lane's two MMA B registers are
+// adjacent: physical element 4q + c (q, c in 0..3) holds logical element
+// 2q + (c & 1) + 8 * (c >> 1).
+__host__ __device__ constexpr int x16_logical_k(int phys) { return 2 * (phys / 4) + (phys & 1) + 8 * ((phys & 3) >> 1); }
+__host__ __device__ constexpr int x16_phys_k(int k) { return 4 * ((k & 7) >> 1) + (k & 1) + 2 * (k >> 3); }
+
+// gate|up row order (see above)
+__host__ __device__ constexpr int gu_row_feature(int tile, int r) { return tile * 64 + 8 * (r >> 4) + (r & 7); }
+__host__ __device__ constexpr bool gu_row_is_up(int r) { return (r & 8) != 0; }
+
 enum WeightFormat { FMT_MXFP4 = 0, FMT_BF16 = 1 };
 
 struct WeightStore {
@@ -49,6 +89,7 @@ struct WeightStore {
     int kchunks = 0;
     int chunk_bytes = 0;
     size_t group_bytes = 0;   // bytes of one expert group's matrix
+    int16_t *rfac = nullptr;  // FRAG_F16 only: R_row per (group, row tile, tile row)
 };
 
 // A caller-side source matrix for the repack: row r starts at
@@ -79,8 +120,14 @@ struct Plan {
     int *grp_start;           // [G]
     int *grp_count;           // [G]
     int *row_token;           // [P] token index of each position
-    uint16_t *x_perm;         // [T*k][H] BF16 rows of x gathered in routed position order
-    uint16_t *h;              // [2][P][I] BF16: h = hi plane + lo plane (lo = bf16(h - hi))
+    uint16_t *x_perm;         // [T*k][H] rows of x gathered in routed position order (BF16, or FP16 for
+                              // the FP16 streaming path)
+    uint16_t *x16;            // [T][H] FP16: x_t * 2^-xs[t] (FP16 streaming path)
+    int *xs;                  // [T] per-token power-of-two scale exponent of x16
+    uint16_t *h;              // [2][P][I] h = hi plane + lo plane: BF16 (lo = bf16(h - hi)); on the FP16
+                              // streaming path FP16 (h * 2^-hs = hi + lo) in x16 K order
+    int *hs;                  // [P][ceil(I/64)] FP16 streaming path: power-of-two scale of each position's
+                              // 64-feature block of h
     float *y;                 // [P][H] FP32
     int *err;                 // device-visible error flag (mapped host memory)
 };
@@ -96,8 +143,12 @@ enum DeviceError {
 // ---------------------------------------------------------------- launchers
 // Each returns the cudaError_t of its launch.
 
-cudaError_t launch_repack(int fmt, bool gate_up, const SrcMat &gate, const SrcMat &up, const WeightStore &ws,
-                          int group, int I, int H, int *bad_scale, cudaStream_t st);
+cudaError_t launch_repack(int fmt, int layout, bool gate_up, const SrcMat &gate, const SrcMat &up,
+                          const WeightStore &ws, int group, int I, int H, int *bad_scale, cudaStream_t st);
+
+// x16[t] = fp16(x[t] * 2^-xs[t]) with xs[t] putting max|x[t]| in [2^14, 2^15),
+// also written to every routed position of the token in x_perm.
+cudaError_t launch_prep_x16(const Plan &p, const uint16_t *x, cudaStream_t st);
 
 cudaError_t launch_router(const float *logits, int T, int E, int k, int *ids, float *w, int *counts, int n_counts,
                           cudaStream_t st);
@@ -106,10 +157,6 @@ cudaError_t launch_permute(const Plan &p, cudaStream_t st);
 
 cudaError_t launch_dense_plan(const Plan &p, cudaStream_t st);
 
-cudaError_t launch_gemm_gate_up(const Plan &p, const WeightStore &w, int fmt, const uint16_t *x, cudaStream_t st);
-
-cudaError_t launch_gemm_down(const Plan &p, const WeightStore &w, int fmt, cudaStream_t st);
-
 cudaError_t launch_combine(const Plan &p, float *out, int accumulate, cudaStream_t st);
 
 cudaError_t launch_gather_rows(const Plan &p, const uint16_t *x, cudaStream_t st);
@@ -117,5 +164,14 @@ cudaError_t launch_gather_rows(const Plan &p, const uint16_t *x, cudaStream_t st
 cudaError_t launch_gemm_gate_up_tc(const Plan &p, const WeightStore &w, int fmt, const uint16_t *x, cudaStream_t st);
 
 cudaError_t launch_gemm_down_tc(const Plan &p, const WeightStore &w, int fmt, cudaStream_t st);
+
+// register-streaming GEMMs for decode-sized batches (every group has at most
+// STREAM_MAX_T tokens per work item; larger groups are split into items)
+constexpr int STREAM_MAX_T = 64;
+
+cudaError_t launch_gemm_gate_up_stream(const Plan &p, const WeightStore &w, int fmt, const uint16_t *x,
+                                       cudaStream_t st);
+
+cudaError_t launch_gemm_down_stream(const Plan &p, const WeightStore &w, int fmt, cudaStream_t st);
 
 }  // namespace moe

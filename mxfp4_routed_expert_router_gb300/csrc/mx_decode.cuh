@@ -76,4 +76,22 @@ __device__ __forceinline__ void decode_word(uint32_t w, uint32_t s2, uint32_t ou
     out[3] = bf16x2_mul(prmt(l1, h1, 0x7362u), s2);
 }
 
+// The same for a warp-level MMA A fragment word (FRAG layout): pairs 0 and 2
+// belong to row g and take scale sa, pairs 1 and 3 to row g+8 and take sb.
+__device__ __forceinline__ void decode_word_frag(uint32_t w, uint32_t sa, uint32_t sb, uint32_t out[4])
+{
+    const uint32_t m = w & 0x77777777u;
+    const uint32_t mh = m >> 16;
+    uint32_t h0 = prmt(MAG_HI_0, MAG_HI_1, m);
+    uint32_t l0 = prmt(MAG_LO_0, MAG_LO_1, m);
+    uint32_t h1 = prmt(MAG_HI_0, MAG_HI_1, mh);
+    uint32_t l1 = prmt(MAG_LO_0, MAG_LO_1, mh);
+    h0 |= w & 0x80808080u;
+    h1 |= (w << 4) & 0x80808080u;
+    out[0] = bf16x2_mul(prmt(l0, h0, 0x5140u), sa);
+    out[1] = bf16x2_mul(prmt(l0, h0, 0x7362u), sb);
+    out[2] = bf16x2_mul(prmt(l1, h1, 0x5140u), sa);
+    out[3] = bf16x2_mul(prmt(l1, h1, 0x7362u), sb);
+}
+
 }  // namespace moe

@@ -121,3 +121,38 @@ def test_every_code_in_every_position(e):
         for i, c in enumerate(codes):
             want = expect(c, e, tab)
             assert got[i] == want and math.copysign(1, got[i]) == math.copysign(1, want), (e, codes, i)
+
+
+def decode_word_frag(w, sa, sb):
+    m = w & 0x77777777
+    mh = m >> 16
+    h0 = prmt(MAG_HI_0, MAG_HI_1, m)
+    l0 = prmt(MAG_LO_0, MAG_LO_1, m)
+    h1 = prmt(MAG_HI_0, MAG_HI_1, mh)
+    l1 = prmt(MAG_LO_0, MAG_LO_1, mh)
+    h0 |= w & 0x80808080
+    h1 |= ((w << 4) & 0xFFFFFFFF) & 0x80808080
+    return [bf16x2_mul(prmt(l0, h0, 0x5140), sa), bf16x2_mul(prmt(l0, h0, 0x7362), sb),
+            bf16x2_mul(prmt(l1, h1, 0x5140), sa), bf16x2_mul(prmt(l1, h1, 0x7362), sb)]
+
+
+def test_fragment_word_maps_to_mma_a_registers():
+    """A FRAG-layout word holds, for lane (g, q) and K step j, the elements
+    (g, 2q), (g, 2q+1), (g+8, 2q), (g+8, 2q+1), (g, 2q+8), (g, 2q+9), (g+8, 2q+8),
+    (g+8, 2q+9) of the 16x16 A tile; the decode must yield the m16n8k16 A
+    registers a0 = rows g / k 2q..2q+1, a1 = rows g+8, a2 = rows g / k+8, a3 =
+    rows g+8 / k+8, each row with its own block scale."""
+    tab = table()
+    rng = np.random.default_rng(7)
+    for trial in range(200):
+        tile = rng.integers(0, 16, (16, 16))
+        ea, eb = int(rng.integers(100, 150)), int(rng.integers(100, 150))
+        g, q = int(rng.integers(0, 8)), int(rng.integers(0, 4))
+        codes = [tile[g, 2 * q], tile[g, 2 * q + 1], tile[g + 8, 2 * q], tile[g + 8, 2 * q + 1],
+                 tile[g, 2 * q + 8], tile[g, 2 * q + 9], tile[g + 8, 2 * q + 8], tile[g + 8, 2 * q + 9]]
+        regs = decode_word_frag(repack_word([int(c) for c in codes]), e8m0_to_bf16x2(ea), e8m0_to_bf16x2(eb))
+        want = [(g, 2 * q, ea), (g + 8, 2 * q, eb), (g, 2 * q + 8, ea), (g + 8, 2 * q + 8, eb)]
+        for reg, (row, col, e) in zip(regs, want):
+            lo, hi = bf16_bits_value(reg), bf16_bits_value(reg >> 16)
+            assert lo == expect(int(tile[row, col]), e, tab)
+            assert hi == expect(int(tile[row, col + 1]), e, tab)

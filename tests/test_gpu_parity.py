@@ -64,6 +64,10 @@ SMALL = [
     wl.custom("single_expert_T7_H96_I64", 7, 96, 64, 1, 0, 1, seed=23),
     wl.custom("wide_T300_H512_I256_E32_S2_k6", 300, 512, 256, 32, 2, 6, seed=24),
     wl.custom("T1_H7168_I2048_E4_S1_k2", 1, 7168, 2048, 4, 1, 2, seed=25),
+    # decode-sized batch (register-streaming path) with K not a multiple of 64
+    wl.custom("stream_ragged_T3_H288_I160_E16_S1_k4", 3, 288, 160, 16, 1, 4, seed=31),
+    # streaming path, largest token tile (64 tokens per group tile)
+    wl.custom("stream_T60_H256_I128_E64_S1_k4", 60, 256, 128, 64, 1, 4, seed=32),
 ]
 
 
