@@ -179,6 +179,50 @@ MoeStatus moe_profile_enable(MoeHandle *h, int enable);
  * stages written (5), or -1 if profiling is off or no call was profiled. */
 int moe_profile_read(MoeHandle *h, float *ms, int n);
 
+/* Limits of moe_route_static's fixed scratch. */
+#define MOE_ROUTE_STATIC_MAX_EXPERTS 1024
+#define MOE_ROUTE_STATIC_MAX_SLOTS 65536 /* T * k */
+
+/* Routing and grouping without any device allocation.  No counterpart in the
+ * paper: this is a deployment variant of the routing step of moe_forward.
+ *
+ * It is for callers that cannot allocate device memory or hand the library a
+ * workspace: for example code that runs while another allocator owns all
+ * free device memory, or a latency-bound loop where cudaMalloc/cudaFree
+ * would synchronise the device and stall other streams.  The call runs the
+ * same router, histogram and permutation kernels as moe_forward and writes
+ * the same routing results.  Their scratch (expert counts, group table,
+ * position -> token map; 274,436 bytes) is a fixed array in the library's
+ * device memory, one per device, that exists from module load to process
+ * exit.  No cudaMalloc, cudaFree or other allocating routine is called.
+ *
+ *  router_logits  [T][E] float, device
+ *  topk_ids       [T][k] int32, device; j = 0 has the largest weight
+ *  topk_w         [T][k] float, device; softmax over the k kept logits
+ *  expert_offsets [E+1] int32, device
+ *  sorted_slot    [T*k] int32, device (slot s = t*k + j at sorted position p)
+ *  slot_pos       [T*k] int32, device (inverse of sorted_slot)
+ *  cuda_stream    cudaStream_t or NULL; all work is enqueued on it
+ * Outputs are as in MoeRoutingOut.  T == 0 enqueues nothing.
+ *
+ * Set-up: the first call made with a given device current looks up the
+ * array's device address (cudaGetSymbolAddress) and keeps it for later calls
+ * on that device.  Make that first call before any stream capture starts.
+ *
+ * Shared scratch: every call on a device uses the same array.  The expert
+ * counts in it must start at zero; the router kernel of each call zeroes
+ * them itself, so the caller clears nothing.  Two calls whose work overlaps
+ * on the GPU (on different streams, or from several threads without an
+ * ordering between their streams) race on the array and give wrong results:
+ * order them on one stream, or with events.
+ *
+ * Errors: MOE_EINVAL (E outside [1, MOE_ROUTE_STATIC_MAX_EXPERTS], k outside
+ * [1, min(E, 32)], T < 0, T * k > MOE_ROUTE_STATIC_MAX_SLOTS, NULL pointer),
+ * MOE_EDEVICE (device ordinal >= 64), MOE_ECUDA (symbol lookup or launch
+ * failed).  The message is available from moe_last_error(). */
+MoeStatus moe_route_static(const float *router_logits, int T, int E, int k, int *topk_ids, float *topk_w,
+                           int *expert_offsets, int *sorted_slot, int *slot_pos, void *cuda_stream);
+
 /* Human-readable description of the last non-OK status returned on the
  * calling thread (thread-local, never NULL). */
 const char *moe_last_error(void);

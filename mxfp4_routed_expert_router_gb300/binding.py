@@ -22,7 +22,8 @@ MOE_W_MXFP4, MOE_W_BF16 = 0, 1
 
 # every symbol include/moe.h declares
 EXPORTED = ("moe_load_weights", "moe_workspace_bytes", "moe_forward", "moe_dense_sliced_forward",
-            "moe_sync_status", "moe_profile_enable", "moe_profile_read", "moe_last_error", "moe_free")
+            "moe_sync_status", "moe_profile_enable", "moe_profile_read", "moe_route_static", "moe_last_error",
+            "moe_free")
 STAGES = ("routing", "grouping", "gate_up", "down", "combine")
 
 
@@ -68,6 +69,8 @@ def _load():
     L.moe_profile_enable.restype = ci
     L.moe_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ci]
     L.moe_profile_read.restype = ci
+    L.moe_route_static.argtypes = [vp, ci, ci, ci, vp, vp, vp, vp, vp, vp]
+    L.moe_route_static.restype = ci
     L.moe_last_error.argtypes = []
     L.moe_last_error.restype = ctypes.c_char_p
     L.moe_free.argtypes = [vp]
@@ -145,6 +148,13 @@ def moe_profile_read(handle: int) -> dict:
     if n < 0:
         raise MoeError(MOE_EINVAL, "no profiled call")
     return {STAGES[i]: float(buf[i]) for i in range(n)}
+
+
+def moe_route_static(router_logits, T: int, E: int, k: int, topk_ids, topk_w, expert_offsets, sorted_slot,
+                     slot_pos, stream=None) -> None:
+    """Routing and grouping with the library's fixed scratch; allocates nothing (see include/moe.h)."""
+    _check(lib.moe_route_static(_ptr(router_logits), T, E, k, _ptr(topk_ids), _ptr(topk_w), _ptr(expert_offsets),
+                                _ptr(sorted_slot), _ptr(slot_pos), _stream(stream)))
 
 
 def moe_free(handle: int) -> None:

@@ -204,6 +204,12 @@ void destroy(MoeHandle *h)
 
 }  // namespace
 
+// Lets entry points defined in other files report through moe_last_error().
+int moe::set_last_error(int status, const char *msg)
+{
+    return (int)fail((MoeStatus)status, "%s", msg);
+}
+
 extern "C" {
 
 MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const MoeMx *down, void *cuda_stream,

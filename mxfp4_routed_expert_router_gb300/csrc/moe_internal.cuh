@@ -174,4 +174,7 @@ cudaError_t launch_gemm_gate_up_stream(const Plan &p, const WeightStore &w, int 
 
 cudaError_t launch_gemm_down_stream(const Plan &p, const WeightStore &w, int fmt, cudaStream_t st);
 
+// Record msg as the calling thread's moe_last_error() text; returns status.
+int set_last_error(int status, const char *msg);
+
 }  // namespace moe
