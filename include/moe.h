@@ -24,8 +24,9 @@
  *     workstation", section "MXFP4 is not NVFP4, and the difference matters on
  *     Ampere".  Weights are decoded on chip inside the reduction; no BF16 copy
  *     of an expert is ever written to device memory.  Products accumulate in
- *     FP32; h is kept between the two projections as a pair of BF16 values
- *     (hi = bf16(h), lo = bf16(h - hi)), about 16 significant bits.
+ *     FP32; h is kept between the two projections as a hi + lo pair, about
+ *     16 significant bits or more: BF16 pairs on the tensor-core path, FP16
+ *     pairs with a power-of-two scale per 64 features on the decode path.
  *  4. Combine.  out_t = sum_{j<k} w_tj y_{e_tj}(x_t) + sum_shared y_s(x_t) in
  *     FP32 ("Cascadia" §3.3, Eq. 1), written to (or, with accumulate, added
  *     to) the caller's FP32 buffer.
@@ -167,16 +168,17 @@ MoeStatus moe_dense_sliced_forward(MoeHandle *h, const void *x_bf16, int T, floa
 MoeStatus moe_sync_status(MoeHandle *h, void *cuda_stream);
 
 /* Per-stage timing for benchmarking.  While enabled, every forward call on
- * this handle records a CUDA event on its stream before its first stage and
- * after each stage.  Stages: [0] routing (router kernel), [1] grouping
- * (histogram + permutation, or the dense plan), [2] gate|up GEMM with SwiGLU,
- * [3] down GEMM, [4] combine.  A stage a call does not run reads 0.
+ * this handle records CUDA events on its stream around its stages.  Stages:
+ * [0] routing (router kernel), [1] grouping (histogram + permutation, or the
+ * dense plan), [2] gate|up GEMM with SwiGLU, [3] down GEMM, [4] combine,
+ * [5] the single-kernel layer that decode-sized batches run instead of
+ * [0]..[4].  A stage a call does not run reads 0.
  * Errors: MOE_EINVAL (NULL handle), MOE_ECUDA (event creation failed). */
 MoeStatus moe_profile_enable(MoeHandle *h, int enable);
 
 /* Wait for the events of the most recent profiled call and write up to n
  * stage durations in milliseconds to the HOST array ms.  Returns the number of
- * stages written (5), or -1 if profiling is off or no call was profiled. */
+ * stages written (at most 6), or -1 if profiling is off or no call was profiled. */
 int moe_profile_read(MoeHandle *h, float *ms, int n);
 
 /* Limits of moe_route_static's fixed scratch. */

@@ -24,7 +24,7 @@ MOE_W_MXFP4, MOE_W_BF16 = 0, 1
 EXPORTED = ("moe_load_weights", "moe_workspace_bytes", "moe_forward", "moe_dense_sliced_forward",
             "moe_sync_status", "moe_profile_enable", "moe_profile_read", "moe_route_static", "moe_last_error",
             "moe_free")
-STAGES = ("routing", "grouping", "gate_up", "down", "combine")
+STAGES = ("routing", "grouping", "gate_up", "down", "combine", "layer")
 
 
 class MoeError(RuntimeError):

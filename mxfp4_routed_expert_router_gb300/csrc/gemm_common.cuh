@@ -26,12 +26,6 @@ struct GemmArgs {
     long long h_plane;
     float *y_out;
     int *err;
-    // FP16 streaming gate|up only
-    const int16_t *rfac;   // R_row per (group, row tile, tile row)
-    const int *xs;         // per-token power-of-two scale of x16
-    const int *row_token;  // token of each position
-    int *hs;               // FP16 streaming path: per-(position, 64-feature block) scale of h
-    int row_tiles_h;       // 64-feature blocks per position in hs (down GEMM)
 };
 
 // ------------------------------------------------------------------ PTX helpers

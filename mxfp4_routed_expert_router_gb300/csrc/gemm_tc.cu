@@ -490,7 +490,7 @@ cudaError_t launch_gather_rows(const Plan &p, const uint16_t *x, cudaStream_t st
 cudaError_t launch_gemm_gate_up_tc(const Plan &p, const WeightStore &w, int fmt, const uint16_t *x, cudaStream_t st)
 {
     TcArgs a{w.base, w.group_bytes, w.kchunks, w.chunk_bytes, w.row_tiles, p.grp_start, p.grp_count, p.E, p.G,
-             p.I, p.H, p.h, (long long)p.P * p.I, nullptr, p.err, nullptr, nullptr, nullptr, nullptr, 0};
+             p.I, p.H, p.h, (long long)p.P * p.I, nullptr, p.err};
     CUtensorMap m1, m2;
     cudaError_t e = make_map(&m2, x, p.T, p.H, B_BOX_ROWS);
     if (e != cudaSuccess)
@@ -507,7 +507,7 @@ cudaError_t launch_gemm_gate_up_tc(const Plan &p, const WeightStore &w, int fmt,
 cudaError_t launch_gemm_down_tc(const Plan &p, const WeightStore &w, int fmt, cudaStream_t st)
 {
     TcArgs a{w.base, w.group_bytes, w.kchunks, w.chunk_bytes, w.row_tiles, p.grp_start, p.grp_count, p.E, p.G,
-             p.I, p.H, nullptr, 0, p.y, p.err, nullptr, nullptr, nullptr, nullptr, 0};
+             p.I, p.H, nullptr, 0, p.y, p.err};
     CUtensorMap m1, m2;
     cudaError_t e = make_map(&m1, p.h, p.P, p.I, B_BOX_ROWS);
     if (e != cudaSuccess)

@@ -1,0 +1,1304 @@
+// layer_stream.cu -- the whole MoE layer (routed or dense-as-slices) for
+// decode-sized batches in one persistent kernel: routing, grouping, gate|up
+// with SwiGLU, down and the weighted combine.  At a handful of tokens per
+// expert the layer is bound by reading each active expert's weights once from
+// HBM, so the kernel is built around one uninterrupted weight stream per SM.
+//
+// Operations (SwiGLU experts, shared experts with unit weight and the weighted
+// reduction of "Cascadia: Resident 975B MoE Inference on Eleven AI PCs" §3.1
+// and §3.3 Eq. 1; dense FFN as all-active slices, §3.4 Eq. 2; MXFP4 decoded
+// inside the reduction as in "DeepSeek-V4-Flash on a four-GPU Ampere
+// workstation", section "MXFP4 is not NVFP4, and the difference matters on
+// Ampere"):
+//
+//  phase 0a  each CTA routes its tokens (softmax top-k, renormalised) and
+//            writes their FP16 rows x16 (per-token power-of-two scale);
+//            a grid-wide counter tells every CTA when all tokens are done.
+//  phase 0b  every CTA builds the expert histogram, positions and the stable
+//            permutation in shared memory (CTA 0 also publishes them), then
+//            the work list: (gate|up, group, 128-row tile, token tile) items
+//            followed by (down, ...) items.
+//  stream    warp 0 takes items from a grid-wide counter and streams each
+//            item's weight chunks (one bulk copy per stage) plus its token
+//            rows (one bulk copy per row) into a ring of shared-memory stages;
+//            16 compute warps decode MXFP4 in registers straight into
+//            warp-level MMA fragments (FP16 operands, FP32 accumulation).
+//            gate|up epilogues write h (FP16 hi + lo, scaled per 64-feature
+//            block) and count finished warps per group; a down item's token
+//            rows are copied only once its group's h is complete, while its
+//            weights are already streaming.
+//  combine   down epilogues write y and count finished warps per (token,
+//            128-feature block); the warp that completes a block sums it into
+//            out in a fixed order (j ascending, then shared groups), so the
+//            result does not depend on which CTA did what.
+//
+// The grid is one CTA per SM, launched cooperatively so that all CTAs are
+// resident: CTAs wait on each other only through counters in the caller's
+// workspace, and every such wait -- like every mbarrier wait -- is bounded in
+// time; on expiry the kernel records DEV_ERR_WAIT_TIMEOUT and leaves.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "gemm_common.cuh"
+#include "mx_decode.cuh"
+
+namespace moe {
+
+namespace {
+
+using namespace gemm;
+
+constexpr int LS_WARPS = 17;
+constexpr int LS_THREADS = LS_WARPS * 32;
+constexpr int LS_COMPUTE_WARPS = 16;
+constexpr int LS_SMEM_LIMIT = 232448;
+constexpr int LS_STAGE_TARGET = 52224;
+constexpr int LS_R_MAX = 8;
+constexpr int LS_HS_ROW = 16;  // ints of h block scales kept per token row and stage
+
+// ------------------------------------------------------------------ stage geometry
+//
+// A stage holds, in this order: NB token operands of ROWS rows each, row r at
+// r * rowb(CH) bytes (CH*2 64-wide K slices of 128 bytes, then 32 bytes of
+// padding so that the 8 rows an MMA fragment reads fall on distinct banks);
+// for the FP16 down GEMM the rows' h block scales (LS_HS_ROW ints per row);
+// then CH weight chunks.
+__host__ __device__ constexpr int ls_rowb(int ch) { return ch * 256 + 32; }
+__host__ __device__ constexpr int ls_stage_bytes(int nb, int rows, int hsb, int ch, int wchunk)
+{
+    return nb * rows * ls_rowb(ch) + hsb + ch * wchunk;
+}
+__host__ __device__ constexpr int ls_pick_ch(int nb, int rows, int hsb, int wchunk)
+{
+    return ls_stage_bytes(nb, rows, hsb, 4, wchunk) <= LS_STAGE_TARGET   ? 4
+           : ls_stage_bytes(nb, rows, hsb, 2, wchunk) <= LS_STAGE_TARGET ? 2
+                                                                         : 1;
+}
+__host__ __device__ constexpr int ls_max(int a, int b) { return a > b ? a : b; }
+
+template <int WFMT, int NT>
+struct LsCfg {
+    static constexpr bool F16 = WFMT == FMT_MXFP4;
+    static constexpr int W_CHUNK = F16 ? CHUNK_MX_BYTES : CHUNK_BF16_BYTES;
+    static constexpr int ROWS = 8 * NT;
+    static constexpr int HSB_DN = F16 ? ROWS * LS_HS_ROW * 4 : 0;
+    static constexpr int CH_GU = ls_pick_ch(1, ROWS, 0, W_CHUNK);
+    static constexpr int CH_DN = ls_pick_ch(2, ROWS, HSB_DN, W_CHUNK);
+    static constexpr int STAGE = (ls_max(ls_stage_bytes(1, ROWS, 0, CH_GU, W_CHUNK),
+                                         ls_stage_bytes(2, ROWS, HSB_DN, CH_DN, W_CHUNK)) +
+                                  127) / 128 * 128;
+    static constexpr int RED_BYTES = 8 * NT * 4 * 32 * 4;  // kh = 1 partial sums, per 16-row group
+    static constexpr int HMAX_BYTES = 2 * 8 * ROWS * 4;    // block maxima of h, double-buffered
+};
+
+// Shared-memory carve-up (bytes from the 1024-aligned base).  The ring comes
+// first; phase 0 uses it as scratch before the first copy is issued.
+struct LsSmem {
+    int hdr, bars, pbars, misc, red, hmax, gcnt, gstart, tpre, sorted, xs, total;
+};
+
+__host__ __device__ inline LsSmem ls_smem(int R, int G, int n, int T, int stage, int red_bytes, int hmax_bytes)
+{
+    LsSmem s;
+    int o = R * stage;
+    s.hdr = o;
+    o += LS_R_MAX * 8;
+    s.bars = o;
+    o += 2 * LS_R_MAX * 8;
+    s.pbars = o;
+    o += 24 * 8;
+    s.misc = o;
+    o += 64;
+    s.red = o;
+    o += red_bytes;
+    s.hmax = o;
+    o += hmax_bytes;
+    s.gcnt = o;
+    o += G * 4;
+    s.gstart = o;
+    o += G * 4;
+    s.tpre = o;
+    o += (G + 1) * 4;
+    s.sorted = o;
+    o += (n > 0 ? n : 1) * 4;
+    s.xs = o;
+    o += T * 4;
+    s.total = o + 1024;  // room to align the dynamic base to 1024
+    return s;
+}
+
+// sync block (ints of the caller's workspace, zeroed before every launch)
+constexpr int SY_ROUTED = 0;  // tokens routed and prepared
+constexpr int SY_PERM = 1;    // 1 once CTA 0 has published the permutation
+constexpr int SY_WORK = 2;    // next work item
+constexpr int SY_DONE = 3;    // CTAs whose items are all finished
+constexpr int SY_GRP = 16;    // [G] gate|up warps finished per group
+
+struct LayerArgs {
+    const uint8_t *wgu, *wdn;
+    size_t gu_group_bytes, dn_group_bytes;
+    int gu_kchunks, dn_kchunks, gu_row_tiles, dn_row_tiles, chunk_bytes;
+    int T, k, E, S, G, H, I, n;
+    const uint16_t *x;
+    const float *logits;
+    int *topk_ids;
+    float *topk_w;
+    int *expert_offsets, *sorted_slot, *slot_pos;
+    uint16_t *x16;
+    int *xs;
+    uint16_t *h;
+    long long h_plane;
+    int *hs;
+    int hs_pitch;
+    float *y, *out;
+    int accumulate;
+    int *sync;
+    int *err;
+    int R;
+};
+
+// ------------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ void mma_bf16(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_f16(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// m16n8k16 FP16 MMA with a zero C operand: d = A * B
+__device__ __forceinline__ void mma_f16_z(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// FRAG_F16 word -> A fragment: each byte (two OCP E2M1 codes) converts to an
+// FP16 pair in hardware; values are the unscaled v(c) (exact in FP16).
+__device__ __forceinline__ void decode_e2m1(uint32_t w, uint32_t out[4])
+{
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+        : "=r"(out[0]), "=r"(out[1]), "=r"(out[2]), "=r"(out[3])
+        : "r"(w));
+}
+
+// 2^(e-127) as a float, exact for every E8M0 byte e in [0, 254] (e = 0 is the
+// subnormal 2^-127)
+__device__ __forceinline__ float e8m0_f32(uint32_t e) { return __int_as_float(e ? (int)(e << 23) : 0x00400000); }
+
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ int atom_add_release(int *p, int v)
+{
+    int old;
+    asm volatile("atom.add.release.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// B fragment: token rows hold K in the x16 order, so a lane's two registers
+// (logical k 2q..2q+1 and 2q+8..2q+9 of a 16-wide K step) are 8 adjacent bytes
+__device__ __forceinline__ void load_b(const uint8_t *p, uint32_t &b0, uint32_t &b1)
+{
+    const uint2 v = *reinterpret_cast<const uint2 *>(p);
+    b0 = v.x;
+    b1 = v.y;
+}
+
+// 2^k as a float for |k| <= 126
+__device__ __forceinline__ float pow2i(int k) { return __int_as_float((127 + k) << 23); }
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+__device__ __forceinline__ int ld_acquire(const int *p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(int *p, int v)
+{
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void red_release_add(int *p, int v)
+{
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait (one thread) until *p >= target, with acquire semantics.
+// Gives up after WAIT_LIMIT_NS (recording DEV_ERR_WAIT_TIMEOUT) or when the
+// CTA's abort flag is raised.
+__device__ __noinline__ bool wait_geq(const int *p, int target, volatile int *abort_flag, int *err)
+{
+    if (ld_acquire(p) >= target)
+        return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        __nanosleep(64);
+        if (ld_acquire(p) >= target)
+            return true;
+        if ((i & 15u) == 0) {
+            if (abort_flag && *abort_flag)
+                return false;
+            if (global_ns() - t0 > WAIT_LIMIT_NS) {
+                atomicCAS(err, 0, DEV_ERR_WAIT_TIMEOUT);
+                if (abort_flag)
+                    *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ phase 0a
+//
+// Warps 0..7 route (LS_ROUTE_THREADS threads, named barrier 1) while warps
+// 8..16 prepare token rows (LS_PREP_THREADS threads, named barrier 2); both
+// walk the same tokens t = blockIdx.x + i * gridDim.x.
+constexpr int LS_ROUTE_THREADS = 256;
+constexpr int LS_PREP_THREADS = LS_THREADS - LS_ROUTE_THREADS;
+constexpr int LS_SCRATCH_PREP = 9216;  // byte offset of the prep scratch (after 1024 keys + selection)
+
+// Order key of a logit: larger float -> larger key; +0 and -0 equal; NaN
+// below every number.
+__device__ __forceinline__ uint32_t ls_logit_key(float f)
+{
+    if (isnan(f))
+        return 0u;
+    if (f == 0.0f)
+        f = 0.0f;
+    const uint32_t b = __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// Route token t (threads 0..LS_ROUTE_THREADS-1).  Every expert gets the
+// 64-bit key (order key << 32 | ~e), so keys are distinct and "larger logit,
+// then lower index" is one unsigned compare; the rank of expert e is the
+// number of larger keys, and the experts of rank < k are the selection, in
+// order.  Weights: w_j = exp(l_j - l_0) / sum_{j' < k} exp(l_j' - l_0), l_0
+// the largest kept logit.
+__device__ void ls_route_token(const LayerArgs &a, int t, uint8_t *scratch)
+{
+    unsigned long long *keys = reinterpret_cast<unsigned long long *>(scratch);
+    int *sel_e = reinterpret_cast<int *>(scratch + 8192);
+    float *sel_v = reinterpret_cast<float *>(sel_e + 32);
+    const float *row = a.logits + (size_t)t * a.E;
+    const int tid = threadIdx.x;
+    for (int e = tid; e < a.E; e += LS_ROUTE_THREADS)
+        keys[e] = ((unsigned long long)ls_logit_key(row[e]) << 32) | (unsigned long long)(0xFFFFFFFFu - e);
+    named_bar_sync(1, LS_ROUTE_THREADS);
+    for (int e = tid; e < a.E; e += LS_ROUTE_THREADS) {
+        const unsigned long long my = keys[e];
+        int r = 0;
+        int i = 0;
+        for (; i + 4 <= a.E; i += 4)
+            r += (keys[i] > my) + (keys[i + 1] > my) + (keys[i + 2] > my) + (keys[i + 3] > my);
+        for (; i < a.E; ++i)
+            r += keys[i] > my;
+        if (r < a.k) {
+            sel_e[r] = e;
+            sel_v[r] = row[e];
+        }
+    }
+    named_bar_sync(1, LS_ROUTE_THREADS);
+    if (tid < 32) {
+        const int lane = tid;
+        const float my_v = lane < a.k ? sel_v[lane] : 0.f;
+        const float l0 = __shfl_sync(0xffffffffu, my_v, 0);
+        const float ex = lane < a.k ? expf(my_v - l0) : 0.f;
+        float sum = ex;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (lane < a.k) {
+            a.topk_ids[(size_t)t * a.k + lane] = sel_e[lane];
+            a.topk_w[(size_t)t * a.k + lane] = ex / sum;
+        }
+    }
+    named_bar_sync(1, LS_ROUTE_THREADS);
+}
+
+// Token row t for the GEMMs, in the x16 K order (physical element 4q + c of
+// every 16-element group holds logical element 2q + (c & 1) + 8 * (c >> 1)),
+// by threads LS_ROUTE_THREADS.. of the CTA.
+// MXFP4 weights: FP16 x_t * 2^-xs[t] with xs[t] = floor(log2 max|x_t|) - 14
+// (0 for an all-zero row, clamped to [-100, 100]); a BF16 value has 8
+// significant bits and FP16 11, so the conversion is exact for every element
+// within 2^17 of the row's largest.  BF16 weights: the BF16 row unchanged.
+template <bool F16>
+__device__ void ls_prep_token(const LayerArgs &a, int t, uint8_t *scratch)
+{
+    const int pt = threadIdx.x - LS_ROUTE_THREADS;
+    const uint4 *row = reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.H);
+    const int ngr = a.H / 16;  // 16-element groups (H is a multiple of 32)
+    float mul = 1.f;
+    if (F16) {
+        uint32_t *red = reinterpret_cast<uint32_t *>(scratch);
+        uint32_t mx = 0;  // max |x| as BF16 bits without sign (monotonic for finite values)
+        for (int i = pt; i < 2 * ngr; i += LS_PREP_THREADS) {
+            const uint4 v = row[i];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                mx = max(mx, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
+        }
+        for (int o = 16; o > 0; o >>= 1)
+            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if ((pt & 31) == 0)
+            red[pt >> 5] = mx;
+        named_bar_sync(2, LS_PREP_THREADS);
+        mx = 0;
+        for (int i = 0; i < LS_PREP_THREADS / 32; ++i)
+            mx = max(mx, red[i]);
+        int sc = mx == 0 ? 0 : (int)(mx >> 7) - 127 - 14;
+        sc = sc < -100 ? -100 : (sc > 100 ? 100 : sc);
+        if (pt == 0)
+            a.xs[t] = sc;
+        mul = ldexpf(1.0f, -sc);
+        named_bar_sync(2, LS_PREP_THREADS);  // red is reused by the next token
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(a.x16 + (size_t)t * a.H);
+    for (int gi = pt; gi < ngr; gi += LS_PREP_THREADS) {
+        const uint4 v0 = row[2 * gi], v1 = row[2 * gi + 1];
+        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        uint16_t hv[16];
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+            const uint32_t b = (w[kk >> 1] >> (16 * (kk & 1))) & 0xFFFFu;
+            hv[kk] = F16 ? __half_as_ushort(__float2half_rn(__uint_as_float(b << 16) * mul)) : (uint16_t)b;
+        }
+        uint32_t o[8];
+#pragma unroll
+        for (int p2 = 0; p2 < 8; ++p2)
+            o[p2] = (uint32_t)hv[x16_logical_k(2 * p2)] | (uint32_t)hv[x16_logical_k(2 * p2 + 1)] << 16;
+        dst[2 * gi] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[2 * gi + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+// ------------------------------------------------------------------ phase 0b
+
+// Groups, positions, token tiles and (routed) the stable permutation, in
+// shared memory.  Positions: routed slots 0..n-1 in expert-major order (slots
+// of one expert in ascending slot order s = t*k + j), then shared group s at
+// n + s*T + t.  gcnt[g] / gstart[g]: tokens and first position of group g;
+// tpre[g]: first token tile of group g (a group of c tokens has ceil(c/ROWS)
+// tiles); sorted[p]: slot at routed position p; xs_s[t]: the x16 scales.
+template <int ROWS, bool F16>
+__device__ void ls_schedule(const LayerArgs &a, uint8_t *scratch, int *gcnt, int *gstart, int *tpre, int *sorted,
+                            int *xs_s)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n = a.n, E = a.E, G = a.G;
+    int *sid = reinterpret_cast<int *>(scratch);
+    int *wtot = sid + ((n + 3) & ~3);     // [LS_WARPS][2] warp totals of the group scan
+    int *wc = wtot + 2 * LS_WARPS;        // [LS_WARPS][E] per-warp running positions
+    for (int g = tid; g < G; g += LS_THREADS)
+        gcnt[g] = g < E ? 0 : a.T;
+    for (int s = tid; s < n; s += LS_THREADS)
+        sid[s] = __ldcg(a.topk_ids + s);
+    if (F16)
+        for (int t = tid; t < a.T; t += LS_THREADS)
+            xs_s[t] = __ldcg(a.xs + t);
+    __syncthreads();
+    for (int s = tid; s < n; s += LS_THREADS)
+        atomicAdd(&gcnt[sid[s]], 1);
+    __syncthreads();
+    // group scan: positions (routed groups only) and token tiles, 32 groups per
+    // warp, LS_WARPS * 32 groups per round
+    int base_pos = 0, base_tiles = 0;
+    for (int g0 = 0; g0 < G; g0 += LS_WARPS * 32) {
+        const int g = g0 + warp * 32 + lane;
+        const int c = g < G ? gcnt[g] : 0;
+        const int cp = g < E ? c : 0;
+        const int tl = (c + ROWS - 1) / ROWS;
+        int ip = cp, it = tl;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int vp = __shfl_up_sync(0xffffffffu, ip, o), vt = __shfl_up_sync(0xffffffffu, it, o);
+            if (lane >= o) {
+                ip += vp;
+                it += vt;
+            }
+        }
+        if (lane == 31) {
+            wtot[2 * warp] = ip;
+            wtot[2 * warp + 1] = it;
+        }
+        __syncthreads();
+        int op = base_pos, ot = base_tiles, tp = 0, tt = 0;
+        for (int w = 0; w < LS_WARPS; ++w) {
+            if (w < warp) {
+                op += wtot[2 * w];
+                ot += wtot[2 * w + 1];
+            }
+            tp += wtot[2 * w];
+            tt += wtot[2 * w + 1];
+        }
+        if (g < G) {
+            gstart[g] = g < E ? op + ip - cp : n + (g - E) * a.T;
+            tpre[g] = ot + it - tl;
+        }
+        base_pos += tp;
+        base_tiles += tt;
+        __syncthreads();
+    }
+    if (tid == 0)
+        tpre[G] = base_tiles;
+    if (E == 0 || n == 0) {
+        __syncthreads();
+        return;
+    }
+    // stable permutation
+    if (n <= 2048) {
+        // one warp, 32 slots per step, a running position per expert
+        for (int e = tid; e < E; e += LS_THREADS)
+            wc[e] = gstart[e];
+        __syncthreads();
+        if (warp == 0) {
+            for (int base = 0; base < n; base += 32) {
+                const int s = base + lane;
+                const bool act = s < n;
+                const int e = act ? sid[s] : -1;
+                const unsigned m = __match_any_sync(0xffffffffu, e);
+                if (act)
+                    sorted[wc[e] + __popc(m & ((1u << lane) - 1u))] = s;
+                __syncwarp();
+                if (act && lane == 31 - __clz(m))
+                    wc[e] += __popc(m);
+                __syncwarp();
+            }
+        }
+    } else {
+        // every warp owns slots [lo, hi): per-warp counts per expert, turned
+        // into each warp's first position per expert, then every warp places
+        // its slots in order
+        const int lo = (int)((long long)warp * n / LS_WARPS), hi = (int)((long long)(warp + 1) * n / LS_WARPS);
+        int *my = wc + warp * E;
+        for (int e = lane; e < E; e += 32)
+            my[e] = 0;
+        __syncwarp();
+        for (int s = lo + lane; s < hi; s += 32)
+            atomicAdd(&my[sid[s]], 1);
+        __syncthreads();
+        for (int e = tid; e < E; e += LS_THREADS) {
+            int run = gstart[e];
+            for (int w = 0; w < LS_WARPS; ++w) {
+                const int c = wc[w * E + e];
+                wc[w * E + e] = run;
+                run += c;
+            }
+        }
+        __syncthreads();
+        for (int base = lo; base < hi; base += 32) {
+            const int s = base + lane;
+            const bool act = s < hi;
+            const int e = act ? sid[s] : -1;
+            const unsigned m = __match_any_sync(0xffffffffu, e);
+            if (act)
+                sorted[my[e] + __popc(m & ((1u << lane) - 1u))] = s;
+            __syncwarp();
+            if (act && lane == 31 - __clz(m))
+                my[e] += __popc(m);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    if (blockIdx.x == 0) {
+        for (int e = tid; e <= E; e += LS_THREADS)
+            a.expert_offsets[e] = e < E ? gstart[e] : n;
+        for (int p = tid; p < n; p += LS_THREADS) {
+            const int s = sorted[p];
+            a.sorted_slot[p] = s;
+            a.slot_pos[s] = p;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            __threadfence();
+            st_release(&a.sync[SY_PERM], 1);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ work items
+
+struct LsItem {
+    bool gu;
+    int g, rt, tok0, nvalid, pos0;
+};
+
+// Item u: gate|up items u < total_gu, then down items.  Items of one group are
+// ordered row tile major, token tile minor; a group of c tokens in ntiles
+// tiles gives each tile ceil(c / ntiles) tokens rounded up to 8.
+template <int ROWS>
+__device__ __forceinline__ LsItem ls_item(int u, int total_gu, int rt_gu, int rt_dn, int G, const int *gcnt,
+                                          const int *gstart, const int *tpre)
+{
+    LsItem it;
+    it.gu = u < total_gu;
+    if (!it.gu)
+        u -= total_gu;
+    const int rtn = it.gu ? rt_gu : rt_dn;
+    const int v = u / rtn;
+    int lo = 0, hi = G;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (tpre[mid] <= v)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    it.g = lo;
+    const int ntiles = tpre[lo + 1] - tpre[lo];
+    const int local = u - tpre[lo] * rtn;
+    it.rt = local / ntiles;
+    const int tt = local % ntiles;
+    const int cnt = gcnt[lo];
+    const int per = ((cnt + ntiles - 1) / ntiles + 7) & ~7;
+    it.tok0 = tt * per;
+    it.nvalid = min(per, cnt - it.tok0);
+    it.pos0 = gstart[lo] + it.tok0;
+    return it;
+}
+
+__device__ __forceinline__ int ls_token_of(const LayerArgs &a, const int *sorted, int pos)
+{
+    return pos < a.n ? sorted[pos] / a.k : (pos - a.n) % a.T;
+}
+
+// out[t][f..f+3] (+)= sum_{j<k} w_tj y[slot_pos[t*k+j]][f..] + sum_s y[n+s*T+t][f..],
+// in that order; loads in batches of 8 so that their latencies overlap.
+__device__ __forceinline__ void ls_combine(const LayerArgs &a, int tt, int f, int lane)
+{
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 *po = reinterpret_cast<float4 *>(a.out + (size_t)tt * a.H + f);
+    const bool on = f < a.H;
+    if (on && a.accumulate)
+        acc = *po;
+    for (int j0 = 0; j0 < a.k; j0 += 8) {
+        const int jn = min(8, a.k - j0);
+        float wl = 0.f;
+        int pl = 0;
+        if (lane < jn) {
+            wl = __ldcg(a.topk_w + (size_t)tt * a.k + j0 + lane);
+            pl = __ldcg(a.slot_pos + (size_t)tt * a.k + j0 + lane);
+        }
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int p = __shfl_sync(0xffffffffu, pl, u);
+            if (u < jn && on)
+                v[u] = __ldcg(reinterpret_cast<const float4 *>(a.y + (size_t)p * a.H + f));
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float wj = __shfl_sync(0xffffffffu, wl, u);
+            if (u < jn && on) {
+                acc.x = fmaf(wj, v[u].x, acc.x);
+                acc.y = fmaf(wj, v[u].y, acc.y);
+                acc.z = fmaf(wj, v[u].z, acc.z);
+                acc.w = fmaf(wj, v[u].w, acc.w);
+            }
+        }
+    }
+    const int S = a.G - a.E;
+    for (int s0 = 0; s0 < S; s0 += 8) {
+        const int sn = min(8, S - s0);
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (u < sn && on)
+                v[u] = __ldcg(reinterpret_cast<const float4 *>(
+                    a.y + ((size_t)a.n + (size_t)(s0 + u) * a.T + tt) * a.H + f));
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (u < sn && on) {
+                acc.x += v[u].x;
+                acc.y += v[u].y;
+                acc.z += v[u].z;
+                acc.w += v[u].w;
+            }
+    }
+    if (on)
+        *po = acc;
+}
+
+// ------------------------------------------------------------------ one item's stages
+//
+// The compute warps' work on one item: every stage of the item, from the
+// ring.  Warp (wg, kh) owns weight rows 16*wg .. 16*wg+15 of the 128-row tile
+// and the kh-th 64-wide half of every 128-wide chunk.  acc[nt]: [0],[1] = row
+// g, token columns 8nt+2q, +1; [2],[3] = row g+8, same columns.  Returns false
+// when a wait gave up.
+template <int WFMT, int NT, bool GU>
+__device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem &it, uint8_t *smem,
+                                               uint64_t *full, uint64_t *empty, const int2 *hdr, uint32_t &rc,
+                                               volatile int *abort_flag, float (&acc)[NT][4])
+{
+    using C = LsCfg<WFMT, NT>;
+    constexpr bool F16 = C::F16;
+    constexpr int ROWS = C::ROWS;
+    constexpr int CH = GU ? C::CH_GU : C::CH_DN;
+    constexpr int ROWB = ls_rowb(CH);
+    constexpr int HS_OFF = (GU ? 1 : 2) * ROWS * ROWB;
+    constexpr int W_OFF = HS_OFF + (GU ? 0 : C::HSB_DN);
+    const int R = a.R;
+    const int lane = threadIdx.x & 31, cw = (threadIdx.x >> 5) - 1;
+    const int wg = cw & 7, kh = cw >> 3, g = lane >> 2, q = lane & 3;
+    const int kch = GU ? a.gu_kchunks : a.dn_kchunks;
+    const int nst = (kch + CH - 1) / CH;
+    const int K = GU ? a.H : a.I;
+    // scale bytes of this warp's two 32-wide blocks: byte 2kh + b of the row's word
+    const int sh = 16 * kh;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+        acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    for (int s = 0; s < nst; ++s, ++rc) {
+        const int slot = rc % R;
+        if (s > 0 && !mbar_wait_warp(&full[slot], (rc / R) & 1, abort_flag, a.err, lane))
+            return false;
+        const uint8_t *st = smem + (size_t)slot * C::STAGE;
+        const uint8_t *brow = st + g * ROWB + q * 8;  // row g of token tile 0, this lane's 8 bytes
+        const int ch_n = min(CH, kch - s * CH);
+        const int sl0 = (s * 2 * CH) & ~3;
+#pragma unroll 1
+        for (int c = 0; c < ch_n; ++c) {
+            const uint8_t *wch = st + W_OFF + c * C::W_CHUNK;
+            const int ks = 2 * c + kh;                 // 64-wide K slice inside the stage
+            const int slice = s * 2 * CH + ks;         // 64-wide K slice of the matrix
+            const int kleft = K - slice * 64;          // K left from this slice on (a multiple of 32)
+            if (kleft <= 0)
+                continue;
+            const int nblk = kleft >= 64 ? 2 : 1;      // 32-wide blocks of the slice inside K
+            const uint8_t *bk = brow + ks * 128;
+            if (F16) {
+                // weights decode unscaled; each 32-wide block's partial sum takes the
+                // row's block scale 2^(e-127) in FP32 (bits max(e << 23, 0x400000))
+                const uint2 sc = *reinterpret_cast<const uint2 *>(wch + CHUNK_MX_CODE_BYTES + (wg * 8 + g) * 8);
+                const uint4 wv = *reinterpret_cast<const uint4 *>(wch + ((wg * 2 + kh) * 32 + lane) * 16);
+                const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+                float sg[2], sg8[2];
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    sg[b] = __int_as_float(max((int)(((sc.x >> (sh + 8 * b)) & 0xFFu) << 23), 0x00400000));
+                    sg8[b] = __int_as_float(max((int)(((sc.y >> (sh + 8 * b)) & 0xFFu) << 23), 0x00400000));
+                }
+                float part[NT][4];  // down: this slice's sum before the h block scale
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    if (b == 1 && nblk < 2)
+                        break;
+                    float t[NT][4];
+#pragma unroll
+                    for (int j2 = 0; j2 < 2; ++j2) {
+                        const int jj = 2 * b + j2;
+                        uint32_t af[4];
+                        decode_e2m1(words[jj], af);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const uint8_t *pb = bk + nt * 8 * ROWB + jj * 32;
+                            uint32_t b0, b1;
+                            load_b(pb, b0, b1);
+                            if (j2 == 0)
+                                mma_f16_z(t[nt], af, b0, b1);
+                            else
+                                mma_f16(t[nt], af, b0, b1);
+                            if (!GU) {
+                                load_b(pb + ROWS * ROWB, b0, b1);
+                                mma_f16(t[nt], af, b0, b1);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        if (GU) {
+                            acc[nt][0] = fmaf(t[nt][0], sg[b], acc[nt][0]);
+                            acc[nt][1] = fmaf(t[nt][1], sg[b], acc[nt][1]);
+                            acc[nt][2] = fmaf(t[nt][2], sg8[b], acc[nt][2]);
+                            acc[nt][3] = fmaf(t[nt][3], sg8[b], acc[nt][3]);
+                        } else if (b == 0) {
+                            part[nt][0] = t[nt][0] * sg[0];
+                            part[nt][1] = t[nt][1] * sg[0];
+                            part[nt][2] = t[nt][2] * sg8[0];
+                            part[nt][3] = t[nt][3] * sg8[0];
+                        } else {
+                            part[nt][0] = fmaf(t[nt][0], sg[1], part[nt][0]);
+                            part[nt][1] = fmaf(t[nt][1], sg[1], part[nt][1]);
+                            part[nt][2] = fmaf(t[nt][2], sg8[1], part[nt][2]);
+                            part[nt][3] = fmaf(t[nt][3], sg8[1], part[nt][3]);
+                        }
+                    }
+                }
+                if (!GU) {
+                    // fold in the scale of this 64-feature block of h for each token column
+                    // (columns past the item's tokens hold stale data and are discarded)
+                    const int *hs_st = reinterpret_cast<const int *>(st + HS_OFF) + (slice - sl0);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const int r0 = 8 * nt + 2 * q;
+                        const float f0 = r0 < it.nvalid ? pow2i(hs_st[r0 * LS_HS_ROW]) : 0.f;
+                        const float f1 = r0 + 1 < it.nvalid ? pow2i(hs_st[(r0 + 1) * LS_HS_ROW]) : 0.f;
+                        acc[nt][0] = fmaf(part[nt][0], f0, acc[nt][0]);
+                        acc[nt][1] = fmaf(part[nt][1], f1, acc[nt][1]);
+                        acc[nt][2] = fmaf(part[nt][2], f0, acc[nt][2]);
+                        acc[nt][3] = fmaf(part[nt][3], f1, acc[nt][3]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    if (jj >= 2 * nblk)
+                        break;
+                    const uint4 av = *reinterpret_cast<const uint4 *>(wch + ((wg * 8 + 4 * kh + jj) * 32 + lane) * 16);
+                    const uint32_t af[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const uint8_t *pb = bk + nt * 8 * ROWB + jj * 32;
+                        uint32_t b0, b1;
+                        load_b(pb, b0, b1);
+                        mma_bf16(acc[nt], af, b0, b1);
+                        if (!GU) {
+                            load_b(pb + ROWS * ROWB, b0, b1);
+                            mma_bf16(acc[nt], af, b0, b1);
+                        }
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&empty[slot]);
+    }
+    (void)hdr;
+    return true;
+}
+
+// ------------------------------------------------------------------ the kernel
+
+template <int WFMT, int NT>
+__global__ void __launch_bounds__(LS_THREADS, 1) layer_stream_kernel(const LayerArgs a)
+{
+    using C = LsCfg<WFMT, NT>;
+    constexpr bool F16 = C::F16;
+    constexpr int ROWS = C::ROWS;
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+    const LsSmem L = ls_smem(a.R, a.G, a.n, a.T, C::STAGE, C::RED_BYTES, C::HMAX_BYTES);
+    int2 *hdr = reinterpret_cast<int2 *>(smem + L.hdr);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars), *empty = full + LS_R_MAX;
+    uint64_t *red_full = reinterpret_cast<uint64_t *>(smem + L.pbars), *red_free = red_full + 8,
+             *hmax_bar = red_full + 16;
+    int *misc = reinterpret_cast<int *>(smem + L.misc);
+    volatile int *abort_flag = misc;
+    float *red = reinterpret_cast<float *>(smem + L.red);
+    float *hmaxb = reinterpret_cast<float *>(smem + L.hmax);
+    int *gcnt = reinterpret_cast<int *>(smem + L.gcnt), *gstart = reinterpret_cast<int *>(smem + L.gstart);
+    int *tpre = reinterpret_cast<int *>(smem + L.tpre), *sorted = reinterpret_cast<int *>(smem + L.sorted);
+    int *xs_s = reinterpret_cast<int *>(smem + L.xs);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int R = a.R;
+
+    if (tid == 0) {
+        for (int i = 0; i < R; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], LS_COMPUTE_WARPS);
+        }
+        for (int i = 0; i < 8; ++i) {
+            mbar_init(&red_full[i], 1);
+            mbar_init(&red_free[i], 1);
+        }
+        mbar_init(hmax_bar, 8);
+        misc[0] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_proxy_async();
+    }
+
+    // ---------------------------------------------------------- phase 0a
+    int mine = 0;
+    for (int t = blockIdx.x; t < a.T; t += gridDim.x, ++mine) {
+        if (tid < LS_ROUTE_THREADS) {
+            if (a.E > 0)
+                ls_route_token(a, t, smem);
+        } else {
+            ls_prep_token<F16>(a, t, smem + LS_SCRATCH_PREP);
+        }
+    }
+    fence_proxy_async_global();  // x16 is read by other CTAs' bulk copies
+    __syncthreads();
+    if (tid == 0) {
+        if (mine > 0) {
+            __threadfence();
+            red_release_add(&a.sync[SY_ROUTED], mine);
+        }
+        misc[1] = wait_geq(&a.sync[SY_ROUTED], a.T, nullptr, a.err) ? 1 : 0;
+    }
+    __syncthreads();
+    if (!misc[1])
+        return;
+
+    // ---------------------------------------------------------- phase 0b
+    ls_schedule<ROWS, F16>(a, smem, gcnt, gstart, tpre, sorted, xs_s);
+    __syncthreads();
+
+    const int rt_gu = a.gu_row_tiles, rt_dn = a.dn_row_tiles;
+    const int tiles = tpre[a.G];
+    const int total_gu = tiles * rt_gu, total = total_gu + tiles * rt_dn;
+    int *grp_done = a.sync + SY_GRP;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ loader
+        uint32_t rc = 0, armed = 0, armed_par = 0;
+        bool ok = true;
+        fence_proxy_async_global();  // x16 of other CTAs, acquired above, is read by bulk copies
+        // first item: blockIdx.x; the shared counter hands out the rest from gridDim.x on
+        int u = blockIdx.x;
+        while (ok && u < total) {
+            int nxt = 0;
+            if (lane == 0)
+                nxt = (int)gridDim.x + atomicAdd(&a.sync[SY_WORK], 1);
+            const LsItem it = ls_item<ROWS>(u, total_gu, rt_gu, rt_dn, a.G, gcnt, gstart, tpre);
+            const int CH = it.gu ? C::CH_GU : C::CH_DN;
+            const int kch = it.gu ? a.gu_kchunks : a.dn_kchunks;
+            const int nst = (kch + CH - 1) / CH;
+            const int K = it.gu ? a.H : a.I;
+            const int nb = it.gu ? 1 : 2;
+            const int rowb = ls_rowb(CH);
+            const int hsb = it.gu ? 0 : C::HSB_DN;
+            const int w_off = nb * ROWS * rowb + hsb;
+            const uint8_t *wsrc = (it.gu ? a.wgu + (size_t)it.g * a.gu_group_bytes
+                                         : a.wdn + (size_t)it.g * a.dn_group_bytes) +
+                                  (size_t)it.rt * kch * (size_t)a.chunk_bytes;
+            // this lane's token rows (r = lane, lane + 32): source row starts
+            const uint16_t *src[2] = {nullptr, nullptr};
+            int pos_r[2] = {0, 0};
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int r = lane + 32 * i;
+                if (r < it.nvalid) {
+                    pos_r[i] = it.pos0 + r;
+                    src[i] = it.gu ? a.x16 + (size_t)ls_token_of(a, sorted, pos_r[i]) * a.H
+                                   : a.h + (size_t)pos_r[i] * a.I;
+                }
+            }
+            for (int s = 0; s < nst; ++s, ++rc) {
+                const int slot = rc % R;
+                const uint32_t ph = (rc / R) & 1;
+                if (!(ok = mbar_wait_warp(&empty[slot], ph ^ 1, abort_flag, a.err, lane)))
+                    break;
+                uint8_t *st = smem + (size_t)slot * C::STAGE;
+                const int ch_n = min(CH, kch - s * CH);
+                const uint32_t wbytes = (uint32_t)(ch_n * a.chunk_bytes);
+                const int k0 = s * CH * 128;
+                const uint32_t vb = (uint32_t)min(CH * 128, K - k0) * 2;  // valid bytes of a token row
+                int sl0 = 0, nh = 0;
+                if (F16 && !it.gu) {
+                    const int ks2 = 2 * CH;
+                    sl0 = (s * ks2) & ~3;
+                    nh = min(((s * ks2 + ks2 + 3) & ~3) - sl0, a.hs_pitch - sl0);
+                }
+                const uint32_t tbytes = (uint32_t)it.nvalid * (nb * vb + (uint32_t)nh * 4);
+                const bool wait_h = !it.gu && s == 0;
+                if (lane == 0) {
+                    hdr[slot] = make_int2(u, s);
+                    if (wait_h)
+                        mbar_expect_tx(&full[slot], wbytes);
+                    else
+                        mbar_arrive_expect_tx(&full[slot], wbytes + tbytes);
+                    bulk_g2s(st + w_off, wsrc + (size_t)s * CH * a.chunk_bytes, wbytes, &full[slot]);
+                }
+                armed |= 1u << slot;
+                armed_par = (armed_par & ~(1u << slot)) | (ph << slot);
+                if (wait_h) {
+                    // the group's h must be complete: 8 epilogue warps per gate|up item
+                    int hok = 1;
+                    if (lane == 0) {
+                        const int ntl = tpre[it.g + 1] - tpre[it.g];
+                        hok = wait_geq(&grp_done[it.g], ntl * rt_gu * 8, abort_flag, a.err) ? 1 : 0;
+                        if (hok)
+                            fence_proxy_async_global();
+                        // arrive in any case so that the weight copy can still complete the phase
+                        mbar_arrive_expect_tx(&full[slot], hok ? tbytes : 0u);
+                    }
+                    if (!(ok = __shfl_sync(0xffffffffu, hok, 0) != 0))
+                        break;
+                }
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int r = lane + 32 * i;
+                    if (r < it.nvalid) {
+                        uint8_t *drow = st + r * rowb;
+                        bulk_g2s(drow, src[i] + k0, vb, &full[slot]);
+                        if (!it.gu) {
+                            bulk_g2s(drow + ROWS * rowb, src[i] + a.h_plane + k0, vb, &full[slot]);
+                            if (F16)
+                                bulk_g2s(st + nb * ROWS * rowb + r * LS_HS_ROW * 4,
+                                         a.hs + (size_t)pos_r[i] * a.hs_pitch + sl0, (uint32_t)nh * 4, &full[slot]);
+                        }
+                    }
+                }
+            }
+            u = __shfl_sync(0xffffffffu, nxt, 0);
+        }
+        if (ok) {
+            // terminal stage: tells the compute warps that the list is exhausted
+            const int slot = rc % R;
+            const uint32_t ph = (rc / R) & 1;
+            if (mbar_wait_warp(&empty[slot], ph ^ 1, abort_flag, a.err, lane)) {
+                // the slot's previous phase has been consumed, so its copies have landed;
+                // the terminal phase carries no copy
+                armed &= ~(1u << slot);
+                if (lane == 0) {
+                    hdr[slot] = make_int2(-1, 0);
+                    mbar_arrive(&full[slot]);
+                }
+            }
+        }
+        if (lane == 0)
+            for (int s = 0; s < R; ++s)
+                if (armed & (1u << s))
+                    mbar_drain(&full[s], (armed_par >> s) & 1);
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------ compute warps
+        const int cw = warp - 1;
+        const int wg = cw & 7, kh = cw >> 3;  // 16-row group, 64-wide half of each chunk
+        const int g = lane >> 2, q = lane & 3;
+        float *rbuf = red + (size_t)wg * NT * 4 * 32;
+        uint32_t rc = 0;
+        int item_i = 0, gu_i = 0;
+        bool ok = true;
+        for (;;) {
+            int slot = rc % R;
+            if (!(ok = mbar_wait_warp(&full[slot], (rc / R) & 1, abort_flag, a.err, lane)))
+                break;
+            const int2 h0 = hdr[slot];
+            if (h0.x < 0)
+                break;
+            const LsItem it = ls_item<ROWS>(h0.x, total_gu, rt_gu, rt_dn, a.G, gcnt, gstart, tpre);
+            const bool gu = it.gu;
+            float acc[NT][4];
+            ok = gu ? ls_item_stages<WFMT, NT, true>(a, it, smem, full, empty, hdr, rc, abort_flag, acc)
+                    : ls_item_stages<WFMT, NT, false>(a, it, smem, full, empty, hdr, rc, abort_flag, acc);
+            if (!ok)
+                break;
+            // ------------------------------------------------------ pair reduction (second half -> first)
+            if (kh == 1) {
+                if (item_i > 0 && !(ok = mbar_wait_warp(&red_free[wg], (item_i - 1) & 1, abort_flag, a.err, lane)))
+                    break;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        rbuf[(nt * 4 + i) * 32 + lane] = acc[nt][i];
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&red_full[wg]);
+                ++item_i;
+                continue;
+            }
+            if (!(ok = mbar_wait_warp(&red_full[wg], item_i & 1, abort_flag, a.err, lane)))
+                break;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    acc[nt][i] += rbuf[(nt * 4 + i) * 32 + lane];
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&red_free[wg]);
+            ++item_i;
+
+            // ------------------------------------------------------ epilogue
+            // acc[nt]: [0],[1] = row g, tokens 8nt+2q, +1; [2],[3] = row g+8, same tokens.
+            if (gu) {
+                const int n = gu_row_feature(it.rt, 16 * wg + g);  // row g: gate, row g+8: up of feature n
+                float hv[NT][2];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int tok = 8 * nt + 2 * q + e;
+                        float gv = acc[nt][e], uv = acc[nt][2 + e];
+                        if (F16) {  // undo the per-token scaling of x16
+                            const float fx = tok < it.nvalid ? pow2i(xs_s[ls_token_of(a, sorted, it.pos0 + tok)]) : 0.f;
+                            gv *= fx;
+                            uv *= fx;
+                        }
+                        hv[nt][e] = (tok < it.nvalid && n < a.I) ? gv / (1.0f + __expf(-gv)) * uv : 0.f;
+                    }
+                if (F16) {
+                    // h leaves as FP16 hi + lo scaled by 2^-hs, hs per (position, 64-feature block):
+                    // block maximum over the 8 features of each warp, then over the 8 warps
+                    float *hm = hmaxb + (gu_i & 1) * 8 * ROWS;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            float m = fabsf(hv[nt][e]);
+                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                            if (g == 0)
+                                hm[wg * ROWS + 8 * nt + 2 * q + e] = m;
+                        }
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(hmax_bar);
+                    if (!(ok = mbar_wait_warp(hmax_bar, gu_i & 1, abort_flag, a.err, lane)))
+                        break;
+                    ++gu_i;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int tok = 8 * nt + 2 * q + e;
+                            float m = 0.f;
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                m = fmaxf(m, hm[i * ROWS + tok]);
+                            const int mb = (int)((__float_as_uint(m) >> 23) & 0xFFu);
+                            int hsc = m > 0.f ? mb - 127 - 14 : 0;
+                            hsc = hsc < -100 ? -100 : (hsc > 100 ? 100 : hsc);
+                            if (tok < it.nvalid) {
+                                const float v = hv[nt][e] * pow2i(-hsc);
+                                const __half hb = __float2half_rn(v);
+                                const __half lb = __float2half_rn(v - __half2float(hb));
+                                if (n < a.I) {
+                                    const size_t o =
+                                        (size_t)(it.pos0 + tok) * a.I + (n & ~15) + x16_phys_k(n & 15);
+                                    a.h[o] = __half_as_ushort(hb);
+                                    a.h[o + a.h_plane] = __half_as_ushort(lb);
+                                }
+                                if (wg == 0 && g == 0)
+                                    a.hs[(size_t)(it.pos0 + tok) * a.hs_pitch + it.rt] = hsc;
+                            }
+                        }
+                } else {
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int tok = 8 * nt + 2 * q + e;
+                            if (tok < it.nvalid && n < a.I) {
+                                const float v = hv[nt][e];
+                                const __nv_bfloat16 hb = __float2bfloat16_rn(v);
+                                const __nv_bfloat16 lb = __float2bfloat16_rn(v - __bfloat162float(hb));
+                                const size_t o = (size_t)(it.pos0 + tok) * a.I + (n & ~15) + x16_phys_k(n & 15);
+                                a.h[o] = __bfloat16_as_ushort(hb);
+                                a.h[o + a.h_plane] = __bfloat16_as_ushort(lb);
+                            }
+                        }
+                }
+                // publish: this warp's part of the group's h is written
+                __threadfence();
+                __syncwarp();
+                if (lane == 0)
+                    red_release_add(&grp_done[it.g], 1);
+            } else {
+                const int m = it.rt * TILE_ROWS + 16 * wg + g;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int tok = 8 * nt + 2 * q + e;
+                        if (tok < it.nvalid) {
+                            float *yrow = a.y + (size_t)(it.pos0 + tok) * a.H;
+                            if (m < a.H)
+                                yrow[m] = acc[nt][e];
+                            if (m + 8 < a.H)
+                                yrow[m + 8] = acc[nt][2 + e];
+                        }
+                    }
+            }
+        }
+        __threadfence();  // y and h of this warp, before the CTA reports that it is done
+    }
+    __syncthreads();
+
+    // ---------------------------------------------------------- combine
+    // once every CTA has finished its items: warp w of CTA b combines the
+    // (token, 128-feature block)s w * gridDim.x + b, w * gridDim.x + b + 17 * gridDim.x, ...
+    if (tid == 0) {
+        red_release_add(&a.sync[SY_DONE], 1);
+        bool okc = wait_geq(&a.sync[SY_DONE], (int)gridDim.x, abort_flag, a.err);
+        if (okc && a.E > 0 && a.n > 0)
+            okc = wait_geq(&a.sync[SY_PERM], 1, abort_flag, a.err);
+        misc[2] = okc ? 1 : 0;
+    }
+    __syncthreads();
+    if (misc[2]) {
+        const int nblk = a.T * rt_dn;
+        for (int bk = warp * (int)gridDim.x + (int)blockIdx.x; bk < nblk; bk += LS_WARPS * (int)gridDim.x)
+            ls_combine(a, bk / rt_dn, (bk % rt_dn) * TILE_ROWS + 4 * lane, lane);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+template <int WFMT, int NT>
+int ls_ring_depth(int G, int n, int E, int T)
+{
+    using C = LsCfg<WFMT, NT>;
+    const LsSmem base = ls_smem(0, G, n, T, C::STAGE, C::RED_BYTES, C::HMAX_BYTES);
+    int R = (LS_SMEM_LIMIT - base.total) / C::STAGE;
+    if (R > LS_R_MAX)
+        R = LS_R_MAX;
+    // phase-0 scratch lives in the ring: routing keys and selection, prep
+    // reduction; then the slot ids, group-scan totals and permutation counters
+    const long long scratch0 = LS_SCRATCH_PREP + 128;
+    const long long scratch1 = ((long long)((n + 3) & ~3) + 2 * LS_WARPS + (long long)LS_WARPS * E) * 4;
+    const long long ring = (long long)R * C::STAGE;
+    if (ring < scratch0 || ring < scratch1)
+        return 0;
+    return R >= 2 ? R : 0;
+}
+
+template <int WFMT, int NT>
+cudaError_t ls_launch(LayerArgs a, cudaStream_t st)
+{
+    using C = LsCfg<WFMT, NT>;
+    a.R = ls_ring_depth<WFMT, NT>(a.G, a.n, a.E, a.T);
+    if (a.R < 2)
+        return cudaErrorNotSupported;
+    const LsSmem L = ls_smem(a.R, a.G, a.n, a.T, C::STAGE, C::RED_BYTES, C::HMAX_BYTES);
+    auto kern = layer_stream_kernel<WFMT, NT>;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LS_SMEM_LIMIT);
+        if (e != cudaSuccess)
+            return e;
+        attr = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)sm_count());
+    cfg.blockDim = dim3(LS_THREADS);
+    cfg.dynamicSmemBytes = (size_t)L.total;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeCooperative;
+    at[0].val.cooperative = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+int ls_nt(int T)
+{
+    const int t = T < STREAM_MAX_T ? T : STREAM_MAX_T;
+    return t <= 8 ? 1 : t <= 16 ? 2 : t <= 32 ? 4 : 8;
+}
+
+template <int WFMT>
+int ls_depth_fmt(int nt, int G, int n, int E, int T)
+{
+    switch (nt) {
+    case 1: return ls_ring_depth<WFMT, 1>(G, n, E, T);
+    case 2: return ls_ring_depth<WFMT, 2>(G, n, E, T);
+    case 4: return ls_ring_depth<WFMT, 4>(G, n, E, T);
+    default: return ls_ring_depth<WFMT, 8>(G, n, E, T);
+    }
+}
+
+template <int WFMT>
+cudaError_t ls_launch_fmt(int nt, const LayerArgs &a, cudaStream_t st)
+{
+    switch (nt) {
+    case 1: return ls_launch<WFMT, 1>(a, st);
+    case 2: return ls_launch<WFMT, 2>(a, st);
+    case 4: return ls_launch<WFMT, 4>(a, st);
+    default: return ls_launch<WFMT, 8>(a, st);
+    }
+}
+
+}  // namespace
+
+size_t layer_stream_sync_bytes(int G)
+{
+    return (size_t)(SY_GRP + G) * sizeof(int);
+}
+
+bool layer_stream_fits(const Plan &p, int fmt)
+{
+    if (p.T < 1 || p.G < 1 || p.G > MAX_GROUPS || p.E > LS_MAX_EXPERTS || (long long)p.T * p.k > LS_MAX_SLOTS)
+        return false;
+    const int nt = ls_nt(p.T);
+    const int n = p.T * p.k;
+    const int R = fmt == FMT_MXFP4 ? ls_depth_fmt<FMT_MXFP4>(nt, p.G, n, p.E, p.T)
+                                   : ls_depth_fmt<FMT_BF16>(nt, p.G, n, p.E, p.T);
+    return R >= 2;
+}
+
+cudaError_t launch_layer_stream(const Plan &p, const WeightStore &gu, const WeightStore &dn, int fmt,
+                                const uint16_t *x, const float *logits, float *out, int accumulate, cudaStream_t st)
+{
+    cudaError_t e = cudaMemsetAsync(p.sync, 0, layer_stream_sync_bytes(p.G), st);
+    if (e != cudaSuccess)
+        return e;
+    LayerArgs a{};
+    a.wgu = gu.base;
+    a.wdn = dn.base;
+    a.gu_group_bytes = gu.group_bytes;
+    a.dn_group_bytes = dn.group_bytes;
+    a.gu_kchunks = gu.kchunks;
+    a.dn_kchunks = dn.kchunks;
+    a.gu_row_tiles = gu.row_tiles;
+    a.dn_row_tiles = dn.row_tiles;
+    a.chunk_bytes = gu.chunk_bytes;
+    a.T = p.T;
+    a.k = p.E > 0 ? p.k : 0;
+    a.E = p.E;
+    a.S = p.S;
+    a.G = p.G;
+    a.H = p.H;
+    a.I = p.I;
+    a.n = p.E > 0 ? p.T * p.k : 0;
+    a.x = x;
+    a.logits = logits;
+    a.topk_ids = p.topk_ids;
+    a.topk_w = p.topk_w;
+    a.expert_offsets = p.expert_offsets;
+    a.sorted_slot = p.sorted_slot;
+    a.slot_pos = p.slot_pos;
+    a.x16 = p.x16;
+    a.xs = p.xs;
+    a.h = p.h;
+    a.h_plane = (long long)p.P * p.I;
+    a.hs = p.hs;
+    a.hs_pitch = p.hs_pitch;
+    a.y = p.y;
+    a.out = out;
+    a.accumulate = accumulate;
+    a.sync = p.sync;
+    a.err = p.err;
+    const int nt = ls_nt(p.T);
+    return fmt == FMT_MXFP4 ? ls_launch_fmt<FMT_MXFP4>(nt, a, st) : ls_launch_fmt<FMT_BF16>(nt, a, st);
+}
+
+}  // namespace moe

@@ -145,29 +145,9 @@ __global__ void repack_frag_kernel(int fmt, int gate_up, SrcMat gate, SrcMat up,
     }
 }
 
-// R_row of every tile row of one group: (largest E8M0 of the row) - 140, 0
-// for padding rows.
-__global__ void row_rfac_kernel(int gate_up, SrcMat gate, SrcMat up, int16_t *rfac, int row_tiles, int logical_rows,
-                                int K)
-{
-    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= row_tiles * TILE_ROWS)
-        return;
-    int srow;
-    const SrcMat *src = tile_row_source(gate_up, &gate, &up, idx / TILE_ROWS, idx % TILE_ROWS, logical_rows, &srow);
-    int emax = -1;
-    if (srow >= 0)
-        for (int b = 0; b < K / 32; ++b) {
-            const int e = src->scales[srow * src->scale_stride + b];
-            emax = e > emax ? e : emax;
-        }
-    rfac[idx] = (int16_t)(emax < 0 ? 0 : emax - F16_ROW_HEADROOM);
-}
-
-// FRAG_F16 layout (see moe_internal.cuh); rfac of the group filled beforehand.
-__global__ void repack_frag_f16_kernel(int gate_up, SrcMat gate, SrcMat up, uint8_t *dst, const int16_t *rfac,
-                                       int row_tiles, int kchunks, int chunk_bytes, int logical_rows, int K,
-                                       int *bad_scale)
+// FRAG_F16 layout (see moe_internal.cuh).
+__global__ void repack_frag_f16_kernel(int gate_up, SrcMat gate, SrcMat up, uint8_t *dst, int row_tiles, int kchunks,
+                                       int chunk_bytes, int logical_rows, int K, int *bad_scale)
 {
     long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (long long)row_tiles * kchunks * 256)
@@ -190,13 +170,10 @@ __global__ void repack_frag_f16_kernel(int gate_up, SrcMat gate, SrcMat up, uint
         reinterpret_cast<uint32_t *>(chunk)[((w * 2 + j / 4) * 32 + t) * 4 + j % 4] = b0 | b1 << 8 | b2 << 16 | b3 << 24;
     }
     if (q == 0) {
-        const int r0 = rfac[tile * TILE_ROWS + 16 * w + g], r1 = rfac[tile * TILE_ROWS + 16 * w + g + 8];
         uint8_t *sc = chunk + CHUNK_MX_CODE_BYTES + (w * 8 + g) * 8;
         for (int b = 0; b < 4; ++b) {
-            const int e0 = src_scale(src0, srow0, k0 + 32 * b, K, bad_scale) - r0 - 112;
-            const int e1 = src_scale(src1, srow1, k0 + 32 * b, K, bad_scale) - r1 - 112;
-            sc[b] = (uint8_t)(4 * (e0 < 0 ? 0 : (e0 > 30 ? 30 : e0)));
-            sc[4 + b] = (uint8_t)(4 * (e1 < 0 ? 0 : (e1 > 30 ? 30 : e1)));
+            sc[b] = src_scale(src0, srow0, k0 + 32 * b, K, bad_scale);
+            sc[4 + b] = src_scale(src1, srow1, k0 + 32 * b, K, bad_scale);
         }
     }
 }
@@ -206,12 +183,9 @@ cudaError_t launch_repack(int fmt, int layout, bool gate_up, const SrcMat &gate,
 {
     if (layout == LAYOUT_FRAG_F16) {
         const int logical_rows = gate_up ? I : H;
-        int16_t *rf = ws.rfac + (size_t)group * ws.row_tiles * TILE_ROWS;
-        row_rfac_kernel<<<(ws.row_tiles * TILE_ROWS + 127) / 128, 128, 0, st>>>(gate_up ? 1 : 0, gate, up, rf,
-                                                                              ws.row_tiles, logical_rows, ws.cols);
         const long long total = (long long)ws.row_tiles * ws.kchunks * 256;
         repack_frag_f16_kernel<<<(unsigned)((total + 127) / 128), 128, 0, st>>>(
-            gate_up ? 1 : 0, gate, up, ws.base + (size_t)group * ws.group_bytes, rf, ws.row_tiles, ws.kchunks,
+            gate_up ? 1 : 0, gate, up, ws.base + (size_t)group * ws.group_bytes, ws.row_tiles, ws.kchunks,
             ws.chunk_bytes, logical_rows, ws.cols, bad_scale);
         return cudaGetLastError();
     }
@@ -255,78 +229,6 @@ cudaError_t launch_dense_plan(const Plan &p, cudaStream_t st)
         n = p.G;
     dense_plan_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(p.T, p.G, p.grp_start, p.grp_count,
                                                                   p.row_token);
-    return cudaGetLastError();
-}
-
-// ---------------------------------------------------------------- FP16 token prep
-//
-// One CTA per token: xs[t] = floor(log2(max|x_t|)) - 14 (0 for an all-zero
-// row, clamped to [-100, 100]), and the FP16 row fp16(x[t][k] * 2^-xs[t]) is
-// written to x16[t] and to every routed position of the token
-// (x_perm[slot_pos[t*k + j]], j < k).  A BF16 value has 8 significant bits and
-// FP16 11, so the conversion is exact for every element within 2^17 of the
-// row's largest (and off by at most 2^-25 * 2^xs[t] below that).
-constexpr int PREP_THREADS = 256;
-
-__global__ void __launch_bounds__(PREP_THREADS) prep_x16_kernel(const uint16_t *__restrict__ x, int H, int k,
-                                                                const int *__restrict__ slot_pos,
-                                                                uint16_t *__restrict__ x16, uint16_t *__restrict__ x_perm,
-                                                                int *__restrict__ xs)
-{
-    __shared__ uint32_t red[PREP_THREADS / 32];
-    const int t = blockIdx.x, tid = threadIdx.x;
-    const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
-    const int nvec = H / 8;  // 8 BF16 per 16-byte vector (H is a multiple of 32)
-    uint32_t mx = 0;         // max |x| as BF16 bits without sign (monotonic for finite values)
-    for (int i = tid; i < nvec; i += PREP_THREADS) {
-        const uint4 v = row[i];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            mx = max(mx, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
-    }
-    for (int o = 16; o > 0; o >>= 1)
-        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if ((tid & 31) == 0)
-        red[tid >> 5] = mx;
-    __syncthreads();
-    mx = 0;
-    for (int i = 0; i < PREP_THREADS / 32; ++i)
-        mx = max(mx, red[i]);
-    int sc = mx == 0 ? 0 : (int)(mx >> 7) - 127 - 14;
-    sc = sc < -100 ? -100 : (sc > 100 ? 100 : sc);  // keep 2^-sc a finite float
-    if (tid == 0)
-        xs[t] = sc;
-    const float mul = ldexpf(1.0f, -sc);
-    // 16-element groups (two 16-byte vectors), written in the x16 K order
-    for (int gi = tid; gi < nvec / 2; gi += PREP_THREADS) {
-        const uint4 v0 = row[2 * gi], v1 = row[2 * gi + 1];
-        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-        uint16_t hv[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const uint32_t b = (w[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
-            hv[k] = __half_as_ushort(__float2half_rn(__uint_as_float(b << 16) * mul));
-        }
-        uint32_t o[8];
-#pragma unroll
-        for (int p2 = 0; p2 < 8; ++p2)
-            o[p2] = (uint32_t)hv[x16_logical_k(2 * p2)] | (uint32_t)hv[x16_logical_k(2 * p2 + 1)] << 16;
-        const uint4 o0 = make_uint4(o[0], o[1], o[2], o[3]), o1 = make_uint4(o[4], o[5], o[6], o[7]);
-        uint4 *dst = reinterpret_cast<uint4 *>(x16 + (size_t)t * H);
-        dst[2 * gi] = o0;
-        dst[2 * gi + 1] = o1;
-        for (int j = 0; j < k; ++j) {
-            uint4 *pd = reinterpret_cast<uint4 *>(x_perm + (size_t)slot_pos[t * k + j] * H);
-            pd[2 * gi] = o0;
-            pd[2 * gi + 1] = o1;
-        }
-    }
-}
-
-cudaError_t launch_prep_x16(const Plan &p, const uint16_t *x, cudaStream_t st)
-{
-    prep_x16_kernel<<<p.T, PREP_THREADS, 0, st>>>(x, p.H, p.k, p.slot_pos, p.x16, p.x_perm, p.xs);
     return cudaGetLastError();
 }
 

@@ -29,10 +29,10 @@ struct MoeHandle {
     int *err_dev = nullptr;    // device alias of err_host
     bool profile = false;      // record stage events (moe_profile_enable)
     bool profiled = false;     // a call has recorded its events
-    cudaEvent_t ev[6] = {};
+    cudaEvent_t ev[7] = {};
 };
 
-constexpr int N_STAGES = 5;
+constexpr int N_STAGES = 6;
 
 namespace {
 
@@ -101,9 +101,11 @@ size_t plan_layout(const MoeHandle *h, int T, int k, char *base, Plan *p)
     q.x_perm = (uint16_t *)take(sizeof(uint16_t) * (size_t)(n > 0 ? n : 1) * H);
     q.x16 = (uint16_t *)take(sizeof(uint16_t) * (size_t)T * H);
     q.xs = (int *)take(sizeof(int) * (size_t)T);
-    q.hs = (int *)take(sizeof(int) * (size_t)P * ((I + 63) / 64));
+    q.hs_pitch = ((I + 63) / 64 + 3) & ~3;
+    q.hs = (int *)take(sizeof(int) * (size_t)P * q.hs_pitch);
     q.h = (uint16_t *)take(2 * sizeof(uint16_t) * (size_t)P * I);
     q.y = (float *)take(sizeof(float) * (size_t)P * H);
+    q.sync = (int *)take(layer_stream_sync_bytes(G));
     q.err = h->err_dev;
     if (p)
         *p = q;
@@ -137,6 +139,21 @@ MoeStatus run_layer(MoeHandle *h, const void *x, const float *logits, int T, int
         if (h->profile)
             cudaEventRecord(h->ev[i], st);
     };
+    // Decode-sized batches (few tokens per expert) run the whole layer in one
+    // persistent weight-streaming kernel; larger batches use the tensor-memory
+    // GEMMs between the routing, permutation and combine kernels.
+    const bool stream = h->E > 0 ? (long long)T * k <= 16LL * h->E : T <= STREAM_MAX_T;
+    if (stream && layer_stream_fits(p, h->fmt)) {
+        for (int i = 0; i <= 5; ++i)
+            mark(i);
+        if ((e = launch_layer_stream(p, h->gu_f, h->dn_f, h->fmt, (const uint16_t *)x, logits, out, accumulate,
+                                     st)) != cudaSuccess)
+            return cuda_fail(e, "layer launch");
+        mark(6);
+        if (h->profile)
+            h->profiled = true;
+        return MOE_OK;
+    }
     mark(0);
     if (h->E > 0) {
         if ((e = launch_router(logits, T, h->E, k, p.topk_ids, p.topk_w, p.counts, h->E, st)) != cudaSuccess)
@@ -150,29 +167,18 @@ MoeStatus run_layer(MoeHandle *h, const void *x, const float *logits, int T, int
             return cuda_fail(e, "dense plan launch");
     }
     mark(2);
-    // Decode-sized batches (few tokens per expert) stream the weights through
-    // registers; larger batches use the tensor-memory GEMMs.
-    const bool stream = h->E > 0 ? (long long)T * k <= 16LL * h->E : T <= STREAM_MAX_T;
-    // token rows for the gate|up GEMM: FP16 (scaled per token) for the FP16
-    // streaming path, BF16 otherwise
-    if (stream && h->fmt == FMT_MXFP4)
-        e = launch_prep_x16(p, (const uint16_t *)x, st);
-    else
-        e = launch_gather_rows(p, (const uint16_t *)x, st);
-    if (e != cudaSuccess)
+    if ((e = launch_gather_rows(p, (const uint16_t *)x, st)) != cudaSuccess)
         return cuda_fail(e, "gather launch");
-    e = stream ? launch_gemm_gate_up_stream(p, h->gu_f, h->fmt, (const uint16_t *)x, st)
-               : launch_gemm_gate_up_tc(p, h->gu, h->fmt, (const uint16_t *)x, st);
-    if (e != cudaSuccess)
+    if ((e = launch_gemm_gate_up_tc(p, h->gu, h->fmt, (const uint16_t *)x, st)) != cudaSuccess)
         return cuda_fail(e, "gate/up launch");
     mark(3);
-    e = stream ? launch_gemm_down_stream(p, h->dn_f, h->fmt, st) : launch_gemm_down_tc(p, h->dn, h->fmt, st);
-    if (e != cudaSuccess)
+    if ((e = launch_gemm_down_tc(p, h->dn, h->fmt, st)) != cudaSuccess)
         return cuda_fail(e, "down launch");
     mark(4);
     if ((e = launch_combine(p, out, accumulate, st)) != cudaSuccess)
         return cuda_fail(e, "combine launch");
     mark(5);
+    mark(6);
     if (h->profile)
         h->profiled = true;
     return MOE_OK;
@@ -188,10 +194,6 @@ void destroy(MoeHandle *h)
         cudaFree(h->dn.base);
     if (h->gu_f.base)
         cudaFree(h->gu_f.base);
-    if (h->gu_f.rfac)
-        cudaFree(h->gu_f.rfac);
-    if (h->dn_f.rfac)
-        cudaFree(h->dn_f.rfac);
     if (h->dn_f.base)
         cudaFree(h->dn_f.base);
     if (h->err_host)
@@ -292,9 +294,7 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
     if (cudaMalloc(&h->gu.base, h->gu.group_bytes * G) != cudaSuccess ||
         cudaMalloc(&h->dn.base, h->dn.group_bytes * G) != cudaSuccess ||
         cudaMalloc(&h->gu_f.base, h->gu_f.group_bytes * G) != cudaSuccess ||
-        cudaMalloc(&h->dn_f.base, h->dn_f.group_bytes * G) != cudaSuccess ||
-        cudaMalloc(&h->gu_f.rfac, sizeof(int16_t) * TILE_ROWS * h->gu_f.row_tiles * (size_t)G) != cudaSuccess ||
-        cudaMalloc(&h->dn_f.rfac, sizeof(int16_t) * TILE_ROWS * h->dn_f.row_tiles * (size_t)G) != cudaSuccess) {
+        cudaMalloc(&h->dn_f.base, h->dn_f.group_bytes * G) != cudaSuccess) {
         cudaGetLastError();
         destroy(h);
         return fail(MOE_ENOMEM, "device allocation of %zu bytes of weights failed",

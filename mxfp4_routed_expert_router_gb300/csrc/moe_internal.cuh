@@ -53,21 +53,15 @@ constexpr int HALF_K = CHUNK_K / 2;                                 // K of one 
 
 enum ChunkLayout { LAYOUT_TILE = 0, LAYOUT_FRAG = 1, LAYOUT_FRAG_F16 = 2 };
 
-// FRAG_F16 layout (register-streaming gate|up with FP16 operands): the same
-// fragment order as FRAG, but each word holds the 8 codes as 4 plain OCP E2M1
-// byte pairs (first element in the low nibble) so that the hardware
-// e2m1x2 -> f16x2 conversion decodes a byte per instruction:
+// FRAG_F16 layout (streaming layer with FP16 operands): the same fragment
+// order as FRAG, but each word holds the 8 codes as 4 plain OCP E2M1 byte
+// pairs (first element in the low nibble) so that the hardware e2m1x2 -> f16x2
+// conversion decodes a byte per instruction:
 //   byte 0: (row g, k 2q, 2q+1), byte 1: (row g+8, k 2q, 2q+1),
 //   byte 2: (row g, k 2q+8, 2q+9), byte 3: (row g+8, k 2q+8, 2q+9).
-// Scale bytes hold 4*f with f = e - R_row - 112 clamped to [0, 30]: f is the
-// FP16 exponent field of the block multiplier 2^(e - 127 - R_row) (0 = block
-// flushed; only blocks 2^36 below the row's largest are), and 4*f placed in
-// the high byte of an FP16 is exactly that multiplier (one byte permute).  R_row = (max E8M0 of the row) -
-// 140 puts the row's largest block at 2^13 (6 * 2^13 < 65504); the epilogue
-// multiplies the row's result by 2^R_row, exactly.  R_row is kept per tile
-// row in WeightStore::rfac.
-constexpr int F16_ROW_HEADROOM = 140;
-
+// The codes decode to FP16 unscaled (exactly: |v| <= 6); the raw E8M0 bytes
+// (same positions as in FRAG) scale each 32-wide block's MMA partial sum in
+// FP32, where every power of two 2^(e-127), e in [0, 254], is exact.
 // FP16 token rows (x16 and its gathered copies) store K in a permuted order
 // inside every 16-element group so that a lane's two MMA B registers are
 // adjacent: physical element 4q + c (q, c in 0..3) holds logical element
@@ -89,7 +83,6 @@ struct WeightStore {
     int kchunks = 0;
     int chunk_bytes = 0;
     size_t group_bytes = 0;   // bytes of one expert group's matrix
-    int16_t *rfac = nullptr;  // FRAG_F16 only: R_row per (group, row tile, tile row)
 };
 
 // A caller-side source matrix for the repack: row r starts at
@@ -122,13 +115,16 @@ struct Plan {
     int *row_token;           // [P] token index of each position
     uint16_t *x_perm;         // [T*k][H] rows of x gathered in routed position order (BF16, or FP16 for
                               // the FP16 streaming path)
-    uint16_t *x16;            // [T][H] FP16: x_t * 2^-xs[t] (FP16 streaming path)
+    uint16_t *x16;            // [T][H] token rows of the streaming path in x16 K order: FP16
+                              // x_t * 2^-xs[t] for MXFP4 weights, BF16 x_t for BF16 weights
     int *xs;                  // [T] per-token power-of-two scale exponent of x16
     uint16_t *h;              // [2][P][I] h = hi plane + lo plane: BF16 (lo = bf16(h - hi)); on the FP16
-                              // streaming path FP16 (h * 2^-hs = hi + lo) in x16 K order
-    int *hs;                  // [P][ceil(I/64)] FP16 streaming path: power-of-two scale of each position's
+                              // streaming path FP16 (h * 2^-hs = hi + lo); x16 K order on the streaming path
+    int *hs;                  // [P][hs_pitch] FP16 streaming path: power-of-two scale of each position's
                               // 64-feature block of h
+    int hs_pitch;             // ceil(I/64) rounded up to a multiple of 4 (16-byte rows)
     float *y;                 // [P][H] FP32
+    int *sync;                // streaming path: grid-wide counters, zeroed before each launch
     int *err;                 // device-visible error flag (mapped host memory)
 };
 
@@ -146,10 +142,6 @@ enum DeviceError {
 cudaError_t launch_repack(int fmt, int layout, bool gate_up, const SrcMat &gate, const SrcMat &up,
                           const WeightStore &ws, int group, int I, int H, int *bad_scale, cudaStream_t st);
 
-// x16[t] = fp16(x[t] * 2^-xs[t]) with xs[t] putting max|x[t]| in [2^14, 2^15),
-// also written to every routed position of the token in x_perm.
-cudaError_t launch_prep_x16(const Plan &p, const uint16_t *x, cudaStream_t st);
-
 cudaError_t launch_router(const float *logits, int T, int E, int k, int *ids, float *w, int *counts, int n_counts,
                           cudaStream_t st);
 
@@ -165,14 +157,23 @@ cudaError_t launch_gemm_gate_up_tc(const Plan &p, const WeightStore &w, int fmt,
 
 cudaError_t launch_gemm_down_tc(const Plan &p, const WeightStore &w, int fmt, cudaStream_t st);
 
-// register-streaming GEMMs for decode-sized batches (every group has at most
-// STREAM_MAX_T tokens per work item; larger groups are split into items)
+// The whole layer in one persistent kernel for decode-sized batches
+// (layer_stream.cu): token tiles of at most STREAM_MAX_T tokens; larger
+// groups are split into several items.
 constexpr int STREAM_MAX_T = 64;
+constexpr int LS_MAX_EXPERTS = 512;
+constexpr int LS_MAX_SLOTS = 4096;  // T * k
 
-cudaError_t launch_gemm_gate_up_stream(const Plan &p, const WeightStore &w, int fmt, const uint16_t *x,
-                                       cudaStream_t st);
+// bytes of the grid-wide counters the streaming layer needs (Plan::sync)
+size_t layer_stream_sync_bytes(int G);
 
-cudaError_t launch_gemm_down_stream(const Plan &p, const WeightStore &w, int fmt, cudaStream_t st);
+// true when the streaming layer kernel can run this plan (sizes within its
+// shared-memory and scheduling limits)
+bool layer_stream_fits(const Plan &p, int fmt);
+
+// zeroes p.sync, then launches the layer kernel cooperatively (one CTA per SM)
+cudaError_t launch_layer_stream(const Plan &p, const WeightStore &gu, const WeightStore &dn, int fmt,
+                                const uint16_t *x, const float *logits, float *out, int accumulate, cudaStream_t st);
 
 // Record msg as the calling thread's moe_last_error() text; returns status.
 int set_last_error(int status, const char *msg);
