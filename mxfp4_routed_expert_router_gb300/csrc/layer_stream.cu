@@ -39,6 +39,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "gemm_common.cuh"
 #include "mx_decode.cuh"
 
@@ -48,9 +50,9 @@ namespace {
 
 using namespace gemm;
 
-constexpr int LS_WARPS = 17;
+constexpr int LS_WARPS = 9;  // warp 0 streams, warps 1..8 compute (one 16-row group each)
 constexpr int LS_THREADS = LS_WARPS * 32;
-constexpr int LS_COMPUTE_WARPS = 16;
+constexpr int LS_COMPUTE_WARPS = 8;
 constexpr int LS_SMEM_LIMIT = 232448;
 constexpr int LS_STAGE_TARGET = 52224;
 constexpr int LS_R_MAX = 8;
@@ -87,14 +89,14 @@ struct LsCfg {
     static constexpr int STAGE = (ls_max(ls_stage_bytes(1, ROWS, 0, CH_GU, W_CHUNK),
                                          ls_stage_bytes(2, ROWS, HSB_DN, CH_DN, W_CHUNK)) +
                                   127) / 128 * 128;
-    static constexpr int RED_BYTES = 8 * NT * 4 * 32 * 4;  // kh = 1 partial sums, per 16-row group
+    static constexpr int RED_BYTES = 0;
     static constexpr int HMAX_BYTES = 2 * 8 * ROWS * 4;    // block maxima of h, double-buffered
 };
 
 // Shared-memory carve-up (bytes from the 1024-aligned base).  The ring comes
 // first; phase 0 uses it as scratch before the first copy is issued.
 struct LsSmem {
-    int hdr, bars, pbars, misc, red, hmax, gcnt, gstart, tpre, sorted, xs, total;
+    int hdr, bars, pbars, misc, red, hmax, gcnt, gstart, tpre, sorted, xs, gdone, total;
 };
 
 __host__ __device__ inline LsSmem ls_smem(int R, int G, int n, int T, int stage, int red_bytes, int hmax_bytes)
@@ -123,6 +125,8 @@ __host__ __device__ inline LsSmem ls_smem(int R, int G, int n, int T, int stage,
     o += (n > 0 ? n : 1) * 4;
     s.xs = o;
     o += T * 4;
+    s.gdone = o;
+    o += ((G + 31) / 32) * 4;
     s.total = o + 1024;  // room to align the dynamic base to 1024
     return s;
 }
@@ -198,10 +202,6 @@ __device__ __forceinline__ void decode_e2m1(uint32_t w, uint32_t out[4])
         : "r"(w));
 }
 
-// 2^(e-127) as a float, exact for every E8M0 byte e in [0, 254] (e = 0 is the
-// subnormal 2^-127)
-__device__ __forceinline__ float e8m0_f32(uint32_t e) { return __int_as_float(e ? (int)(e << 23) : 0x00400000); }
-
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -241,6 +241,15 @@ __device__ __forceinline__ int ld_acquire(const int *p)
     return v;
 }
 
+__device__ __forceinline__ int ld_relaxed(const int *p)
+{
+    int v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 __device__ __forceinline__ void st_release(int *p, int v)
 {
     asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -278,10 +287,10 @@ __device__ __noinline__ bool wait_geq(const int *p, int target, volatile int *ab
 
 // ------------------------------------------------------------------ phase 0a
 //
-// Warps 0..7 route (LS_ROUTE_THREADS threads, named barrier 1) while warps
-// 8..16 prepare token rows (LS_PREP_THREADS threads, named barrier 2); both
+// Warps 0..3 route (LS_ROUTE_THREADS threads, named barrier 1) while warps
+// 4..8 prepare token rows (LS_PREP_THREADS threads, named barrier 2); both
 // walk the same tokens t = blockIdx.x + i * gridDim.x.
-constexpr int LS_ROUTE_THREADS = 256;
+constexpr int LS_ROUTE_THREADS = 128;
 constexpr int LS_PREP_THREADS = LS_THREADS - LS_ROUTE_THREADS;
 constexpr int LS_SCRATCH_PREP = 9216;  // byte offset of the prep scratch (after 1024 keys + selection)
 
@@ -409,7 +418,8 @@ __device__ void ls_prep_token(const LayerArgs &a, int t, uint8_t *scratch)
 // of one expert in ascending slot order s = t*k + j), then shared group s at
 // n + s*T + t.  gcnt[g] / gstart[g]: tokens and first position of group g;
 // tpre[g]: first token tile of group g (a group of c tokens has ceil(c/ROWS)
-// tiles); sorted[p]: slot at routed position p; xs_s[t]: the x16 scales.
+// tiles); sorted[p]: slot at routed position p, replaced by its token once
+// CTA 0 has published the permutation; xs_s[t]: the x16 scales.
 template <int ROWS, bool F16>
 __device__ void ls_schedule(const LayerArgs &a, uint8_t *scratch, int *gcnt, int *gstart, int *tpre, int *sorted,
                             int *xs_s)
@@ -544,6 +554,10 @@ __device__ void ls_schedule(const LayerArgs &a, uint8_t *scratch, int *gcnt, int
             st_release(&a.sync[SY_PERM], 1);
         }
     }
+    // from here on the GEMMs need only each routed position's token
+    __syncthreads();
+    for (int p = tid; p < n; p += LS_THREADS)
+        sorted[p] /= a.k;
 }
 
 // ------------------------------------------------------------------ work items
@@ -587,9 +601,11 @@ __device__ __forceinline__ LsItem ls_item(int u, int total_gu, int rt_gu, int rt
     return it;
 }
 
-__device__ __forceinline__ int ls_token_of(const LayerArgs &a, const int *sorted, int pos)
+// token of row r of an item: routed positions look it up (tokp: token of each
+// routed position); a shared group or dense slice holds every token in order
+__device__ __forceinline__ int ls_row_token(const LayerArgs &a, const int *tokp, const LsItem &it, int r)
 {
-    return pos < a.n ? sorted[pos] / a.k : (pos - a.n) % a.T;
+    return it.g < a.E ? tokp[it.pos0 + r] : it.tok0 + r;
 }
 
 // out[t][f..f+3] (+)= sum_{j<k} w_tj y[slot_pos[t*k+j]][f..] + sum_s y[n+s*T+t][f..],
@@ -652,10 +668,9 @@ __device__ __forceinline__ void ls_combine(const LayerArgs &a, int tt, int f, in
 // ------------------------------------------------------------------ one item's stages
 //
 // The compute warps' work on one item: every stage of the item, from the
-// ring.  Warp (wg, kh) owns weight rows 16*wg .. 16*wg+15 of the 128-row tile
-// and the kh-th 64-wide half of every 128-wide chunk.  acc[nt]: [0],[1] = row
-// g, token columns 8nt+2q, +1; [2],[3] = row g+8, same columns.  Returns false
-// when a wait gave up.
+// ring.  Compute warp wg owns weight rows 16*wg .. 16*wg+15 of the 128-row
+// tile over the whole K.  acc[nt]: [0],[1] = row g, token columns 8nt+2q, +1;
+// [2],[3] = row g+8, same columns.  Returns false when a wait gave up.
 template <int WFMT, int NT, bool GU>
 __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem &it, uint8_t *smem,
                                                uint64_t *full, uint64_t *empty, const int2 *hdr, uint32_t &rc,
@@ -670,12 +685,11 @@ __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem 
     constexpr int W_OFF = HS_OFF + (GU ? 0 : C::HSB_DN);
     const int R = a.R;
     const int lane = threadIdx.x & 31, cw = (threadIdx.x >> 5) - 1;
-    const int wg = cw & 7, kh = cw >> 3, g = lane >> 2, q = lane & 3;
+    const int wg = cw, g = lane >> 2, q = lane & 3;
     const int kch = GU ? a.gu_kchunks : a.dn_kchunks;
     const int nst = (kch + CH - 1) / CH;
     const int K = GU ? a.H : a.I;
-    // scale bytes of this warp's two 32-wide blocks: byte 2kh + b of the row's word
-    const int sh = 16 * kh;
+    const int nt_used = (it.nvalid + 7) >> 3;  // 8-token tiles holding the item's tokens
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
         acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
@@ -687,15 +701,17 @@ __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem 
         const uint8_t *brow = st + g * ROWB + q * 8;  // row g of token tile 0, this lane's 8 bytes
         const int ch_n = min(CH, kch - s * CH);
         const int sl0 = (s * 2 * CH) & ~3;
-#pragma unroll 1
-        for (int c = 0; c < ch_n; ++c) {
+        // 64-wide half kh of chunk c; FULL: the whole chunk lies inside K
+        auto half_chunk = [&](const int c, const int kh, auto full_tag) {
+            const int sh = 16 * kh;  // scale bytes of the half's two 32-wide blocks: 2kh, 2kh+1
+            constexpr bool FULL = decltype(full_tag)::value;
             const uint8_t *wch = st + W_OFF + c * C::W_CHUNK;
             const int ks = 2 * c + kh;                 // 64-wide K slice inside the stage
             const int slice = s * 2 * CH + ks;         // 64-wide K slice of the matrix
             const int kleft = K - slice * 64;          // K left from this slice on (a multiple of 32)
-            if (kleft <= 0)
-                continue;
-            const int nblk = kleft >= 64 ? 2 : 1;      // 32-wide blocks of the slice inside K
+            if (!FULL && kleft <= 0)
+                return;
+            const int nblk = FULL || kleft >= 64 ? 2 : 1;  // 32-wide blocks of the slice inside K
             const uint8_t *bk = brow + ks * 128;
             if (F16) {
                 // weights decode unscaled; each 32-wide block's partial sum takes the
@@ -709,65 +725,62 @@ __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem 
                     sg[b] = __int_as_float(max((int)(((sc.x >> (sh + 8 * b)) & 0xFFu) << 23), 0x00400000));
                     sg8[b] = __int_as_float(max((int)(((sc.y >> (sh + 8 * b)) & 0xFFu) << 23), 0x00400000));
                 }
-                float part[NT][4];  // down: this slice's sum before the h block scale
+                // the four A fragments of this half-chunk, decoded once for every token tile
+                uint32_t af[4][4];
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    if (b == 1 && nblk < 2)
-                        break;
-                    float t[NT][4];
+                for (int jj = 0; jj < 4; ++jj)
+                    if (jj < 2 * nblk)
+                        decode_e2m1(words[jj], af[jj]);
+                const int *hs_st = reinterpret_cast<const int *>(st + HS_OFF) + (slice - sl0);
 #pragma unroll
-                    for (int j2 = 0; j2 < 2; ++j2) {
-                        const int jj = 2 * b + j2;
-                        uint32_t af[4];
-                        decode_e2m1(words[jj], af);
+                for (int nt = 0; nt < NT; ++nt) {
+                    if (NT == 1 || nt < nt_used) {
+                        const uint8_t *pb = bk + nt * 8 * ROWB;
+                        float part[4];  // down: this slice's sum before the h block scale
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            const uint8_t *pb = bk + nt * 8 * ROWB + jj * 32;
-                            uint32_t b0, b1;
-                            load_b(pb, b0, b1);
-                            if (j2 == 0)
-                                mma_f16_z(t[nt], af, b0, b1);
-                            else
-                                mma_f16(t[nt], af, b0, b1);
-                            if (!GU) {
-                                load_b(pb + ROWS * ROWB, b0, b1);
-                                mma_f16(t[nt], af, b0, b1);
+                        for (int b = 0; b < 2; ++b) {
+                            if (b < nblk) {
+                                float t[4];  // one 32-wide block, before its weight scale
+                                uint32_t b0, b1;
+                                load_b(pb + (2 * b) * 32, b0, b1);
+                                mma_f16_z(t, af[2 * b], b0, b1);
+                                load_b(pb + (2 * b + 1) * 32, b0, b1);
+                                mma_f16(t, af[2 * b + 1], b0, b1);
+                                if (!GU) {
+                                    load_b(pb + ROWS * ROWB + (2 * b) * 32, b0, b1);
+                                    mma_f16(t, af[2 * b], b0, b1);
+                                    load_b(pb + ROWS * ROWB + (2 * b + 1) * 32, b0, b1);
+                                    mma_f16(t, af[2 * b + 1], b0, b1);
+                                }
+                                if (GU) {
+                                    acc[nt][0] = fmaf(t[0], sg[b], acc[nt][0]);
+                                    acc[nt][1] = fmaf(t[1], sg[b], acc[nt][1]);
+                                    acc[nt][2] = fmaf(t[2], sg8[b], acc[nt][2]);
+                                    acc[nt][3] = fmaf(t[3], sg8[b], acc[nt][3]);
+                                } else if (b == 0) {
+                                    part[0] = t[0] * sg[0];
+                                    part[1] = t[1] * sg[0];
+                                    part[2] = t[2] * sg8[0];
+                                    part[3] = t[3] * sg8[0];
+                                } else {
+                                    part[0] = fmaf(t[0], sg[1], part[0]);
+                                    part[1] = fmaf(t[1], sg[1], part[1]);
+                                    part[2] = fmaf(t[2], sg8[1], part[2]);
+                                    part[3] = fmaf(t[3], sg8[1], part[3]);
+                                }
                             }
                         }
-                    }
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        if (GU) {
-                            acc[nt][0] = fmaf(t[nt][0], sg[b], acc[nt][0]);
-                            acc[nt][1] = fmaf(t[nt][1], sg[b], acc[nt][1]);
-                            acc[nt][2] = fmaf(t[nt][2], sg8[b], acc[nt][2]);
-                            acc[nt][3] = fmaf(t[nt][3], sg8[b], acc[nt][3]);
-                        } else if (b == 0) {
-                            part[nt][0] = t[nt][0] * sg[0];
-                            part[nt][1] = t[nt][1] * sg[0];
-                            part[nt][2] = t[nt][2] * sg8[0];
-                            part[nt][3] = t[nt][3] * sg8[0];
-                        } else {
-                            part[nt][0] = fmaf(t[nt][0], sg[1], part[nt][0]);
-                            part[nt][1] = fmaf(t[nt][1], sg[1], part[nt][1]);
-                            part[nt][2] = fmaf(t[nt][2], sg8[1], part[nt][2]);
-                            part[nt][3] = fmaf(t[nt][3], sg8[1], part[nt][3]);
+                        if (!GU) {
+                            // fold in the scale of this 64-feature block of h for each token
+                            // column (columns past the item's tokens hold stale data, discarded)
+                            const int r0 = 8 * nt + 2 * q;
+                            const float f0 = r0 < it.nvalid ? pow2i(hs_st[r0 * LS_HS_ROW]) : 0.f;
+                            const float f1 = r0 + 1 < it.nvalid ? pow2i(hs_st[(r0 + 1) * LS_HS_ROW]) : 0.f;
+                            acc[nt][0] = fmaf(part[0], f0, acc[nt][0]);
+                            acc[nt][1] = fmaf(part[1], f1, acc[nt][1]);
+                            acc[nt][2] = fmaf(part[2], f0, acc[nt][2]);
+                            acc[nt][3] = fmaf(part[3], f1, acc[nt][3]);
                         }
-                    }
-                }
-                if (!GU) {
-                    // fold in the scale of this 64-feature block of h for each token column
-                    // (columns past the item's tokens hold stale data and are discarded)
-                    const int *hs_st = reinterpret_cast<const int *>(st + HS_OFF) + (slice - sl0);
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const int r0 = 8 * nt + 2 * q;
-                        const float f0 = r0 < it.nvalid ? pow2i(hs_st[r0 * LS_HS_ROW]) : 0.f;
-                        const float f1 = r0 + 1 < it.nvalid ? pow2i(hs_st[(r0 + 1) * LS_HS_ROW]) : 0.f;
-                        acc[nt][0] = fmaf(part[nt][0], f0, acc[nt][0]);
-                        acc[nt][1] = fmaf(part[nt][1], f1, acc[nt][1]);
-                        acc[nt][2] = fmaf(part[nt][2], f0, acc[nt][2]);
-                        acc[nt][3] = fmaf(part[nt][3], f1, acc[nt][3]);
                     }
                 }
             } else {
@@ -779,16 +792,31 @@ __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem 
                     const uint32_t af[4] = {av.x, av.y, av.z, av.w};
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
-                        const uint8_t *pb = bk + nt * 8 * ROWB + jj * 32;
-                        uint32_t b0, b1;
-                        load_b(pb, b0, b1);
-                        mma_bf16(acc[nt], af, b0, b1);
-                        if (!GU) {
-                            load_b(pb + ROWS * ROWB, b0, b1);
+                        if (NT == 1 || nt < nt_used) {
+                            const uint8_t *pb = bk + nt * 8 * ROWB + jj * 32;
+                            uint32_t b0, b1;
+                            load_b(pb, b0, b1);
                             mma_bf16(acc[nt], af, b0, b1);
+                            if (!GU) {
+                                load_b(pb + ROWS * ROWB, b0, b1);
+                                mma_bf16(acc[nt], af, b0, b1);
+                            }
                         }
                     }
                 }
+            }
+                };
+        if (ch_n == CH && (s + 1) * CH * 128 <= K) {
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+                half_chunk(c, 0, std::true_type{});
+                half_chunk(c, 1, std::true_type{});
+            }
+        } else {
+#pragma unroll 1
+            for (int c = 0; c < ch_n; ++c) {
+                half_chunk(c, 0, std::false_type{});
+                half_chunk(c, 1, std::false_type{});
             }
         }
         __syncwarp();
@@ -812,15 +840,14 @@ __global__ void __launch_bounds__(LS_THREADS, 1) layer_stream_kernel(const Layer
     const LsSmem L = ls_smem(a.R, a.G, a.n, a.T, C::STAGE, C::RED_BYTES, C::HMAX_BYTES);
     int2 *hdr = reinterpret_cast<int2 *>(smem + L.hdr);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars), *empty = full + LS_R_MAX;
-    uint64_t *red_full = reinterpret_cast<uint64_t *>(smem + L.pbars), *red_free = red_full + 8,
-             *hmax_bar = red_full + 16;
+    uint64_t *hmax_bar = reinterpret_cast<uint64_t *>(smem + L.pbars);
     int *misc = reinterpret_cast<int *>(smem + L.misc);
     volatile int *abort_flag = misc;
-    float *red = reinterpret_cast<float *>(smem + L.red);
     float *hmaxb = reinterpret_cast<float *>(smem + L.hmax);
     int *gcnt = reinterpret_cast<int *>(smem + L.gcnt), *gstart = reinterpret_cast<int *>(smem + L.gstart);
     int *tpre = reinterpret_cast<int *>(smem + L.tpre), *sorted = reinterpret_cast<int *>(smem + L.sorted);
     int *xs_s = reinterpret_cast<int *>(smem + L.xs);
+    uint32_t *gdone = reinterpret_cast<uint32_t *>(smem + L.gdone);  // loader: groups whose h is complete
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int R = a.R;
 
@@ -829,12 +856,10 @@ __global__ void __launch_bounds__(LS_THREADS, 1) layer_stream_kernel(const Layer
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], LS_COMPUTE_WARPS);
         }
-        for (int i = 0; i < 8; ++i) {
-            mbar_init(&red_full[i], 1);
-            mbar_init(&red_free[i], 1);
-        }
-        mbar_init(hmax_bar, 8);
+        mbar_init(hmax_bar, LS_COMPUTE_WARPS);
         misc[0] = 0;
+        for (int i = 0; i < (a.G + 31) / 32; ++i)
+            gdone[i] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async();
     }
@@ -854,7 +879,7 @@ __global__ void __launch_bounds__(LS_THREADS, 1) layer_stream_kernel(const Layer
     if (tid == 0) {
         if (mine > 0) {
             __threadfence();
-            red_release_add(&a.sync[SY_ROUTED], mine);
+            atomicAdd(&a.sync[SY_ROUTED], mine);
         }
         misc[1] = wait_geq(&a.sync[SY_ROUTED], a.T, nullptr, a.err) ? 1 : 0;
     }
@@ -878,6 +903,9 @@ __global__ void __launch_bounds__(LS_THREADS, 1) layer_stream_kernel(const Layer
         fence_proxy_async_global();  // x16 of other CTAs, acquired above, is read by bulk copies
         // first item: blockIdx.x; the shared counter hands out the rest from gridDim.x on
         int u = blockIdx.x;
+        // lane 0: completion count of the next item's group, read half-way through the
+        // current item so that a down item rarely waits for the round trip
+        int probe_g = -1, probe_v = 0;
         while (ok && u < total) {
             int nxt = 0;
             if (lane == 0)
@@ -902,7 +930,7 @@ __global__ void __launch_bounds__(LS_THREADS, 1) layer_stream_kernel(const Layer
                 const int r = lane + 32 * i;
                 if (r < it.nvalid) {
                     pos_r[i] = it.pos0 + r;
-                    src[i] = it.gu ? a.x16 + (size_t)ls_token_of(a, sorted, pos_r[i]) * a.H
+                    src[i] = it.gu ? a.x16 + (size_t)ls_row_token(a, sorted, it, r) * a.H
                                    : a.h + (size_t)pos_r[i] * a.I;
                 }
             }
@@ -938,8 +966,17 @@ __global__ void __launch_bounds__(LS_THREADS, 1) layer_stream_kernel(const Layer
                     // the group's h must be complete: 8 epilogue warps per gate|up item
                     int hok = 1;
                     if (lane == 0) {
-                        const int ntl = tpre[it.g + 1] - tpre[it.g];
-                        hok = wait_geq(&grp_done[it.g], ntl * rt_gu * 8, abort_flag, a.err) ? 1 : 0;
+                        const uint32_t bit = 1u << (it.g & 31);
+                        if (!(gdone[it.g >> 5] & bit)) {
+                            const int ntl = tpre[it.g + 1] - tpre[it.g];
+                            const int target = ntl * rt_gu * 8;
+                            if (probe_g == it.g && probe_v >= target)
+                                fence_acq_rel_gpu();
+                            else
+                                hok = wait_geq(&grp_done[it.g], target, abort_flag, a.err) ? 1 : 0;
+                            if (hok)
+                                gdone[it.g >> 5] |= bit;
+                        }
                         if (hok)
                             fence_proxy_async_global();
                         // arrive in any case so that the weight copy can still complete the phase
@@ -960,6 +997,16 @@ __global__ void __launch_bounds__(LS_THREADS, 1) layer_stream_kernel(const Layer
                             if (F16)
                                 bulk_g2s(st + nb * ROWS * rowb + r * LS_HS_ROW * 4,
                                          a.hs + (size_t)pos_r[i] * a.hs_pitch + sl0, (uint32_t)nh * 4, &full[slot]);
+                        }
+                    }
+                }
+                if (s == nst / 2 && lane == 0) {
+                    probe_g = -1;
+                    if (nxt < total) {
+                        const LsItem nx = ls_item<ROWS>(nxt, total_gu, rt_gu, rt_dn, a.G, gcnt, gstart, tpre);
+                        if (!nx.gu && !(gdone[nx.g >> 5] & (1u << (nx.g & 31)))) {
+                            probe_g = nx.g;
+                            probe_v = ld_relaxed(&grp_done[nx.g]);
                         }
                     }
                 }
@@ -988,11 +1035,10 @@ __global__ void __launch_bounds__(LS_THREADS, 1) layer_stream_kernel(const Layer
     } else {
         // ------------------------------------------------------ compute warps
         const int cw = warp - 1;
-        const int wg = cw & 7, kh = cw >> 3;  // 16-row group, 64-wide half of each chunk
+        const int wg = cw;  // 16-row group of the 128-row tile
         const int g = lane >> 2, q = lane & 3;
-        float *rbuf = red + (size_t)wg * NT * 4 * 32;
         uint32_t rc = 0;
-        int item_i = 0, gu_i = 0;
+        int gu_i = 0;
         bool ok = true;
         for (;;) {
             int slot = rc % R;
@@ -1008,32 +1054,7 @@ __global__ void __launch_bounds__(LS_THREADS, 1) layer_stream_kernel(const Layer
                     : ls_item_stages<WFMT, NT, false>(a, it, smem, full, empty, hdr, rc, abort_flag, acc);
             if (!ok)
                 break;
-            // ------------------------------------------------------ pair reduction (second half -> first)
-            if (kh == 1) {
-                if (item_i > 0 && !(ok = mbar_wait_warp(&red_free[wg], (item_i - 1) & 1, abort_flag, a.err, lane)))
-                    break;
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        rbuf[(nt * 4 + i) * 32 + lane] = acc[nt][i];
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&red_full[wg]);
-                ++item_i;
-                continue;
-            }
-            if (!(ok = mbar_wait_warp(&red_full[wg], item_i & 1, abort_flag, a.err, lane)))
-                break;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    acc[nt][i] += rbuf[(nt * 4 + i) * 32 + lane];
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&red_free[wg]);
-            ++item_i;
+            const int gu_idx = gu ? gu_i++ : 0;
 
             // ------------------------------------------------------ epilogue
             // acc[nt]: [0],[1] = row g, tokens 8nt+2q, +1; [2],[3] = row g+8, same tokens.
@@ -1047,16 +1068,16 @@ __global__ void __launch_bounds__(LS_THREADS, 1) layer_stream_kernel(const Layer
                         const int tok = 8 * nt + 2 * q + e;
                         float gv = acc[nt][e], uv = acc[nt][2 + e];
                         if (F16) {  // undo the per-token scaling of x16
-                            const float fx = tok < it.nvalid ? pow2i(xs_s[ls_token_of(a, sorted, it.pos0 + tok)]) : 0.f;
+                            const float fx = tok < it.nvalid ? pow2i(xs_s[ls_row_token(a, sorted, it, tok)]) : 0.f;
                             gv *= fx;
                             uv *= fx;
                         }
-                        hv[nt][e] = (tok < it.nvalid && n < a.I) ? gv / (1.0f + __expf(-gv)) * uv : 0.f;
+                        hv[nt][e] = (tok < it.nvalid && n < a.I) ? __fdividef(gv, 1.0f + __expf(-gv)) * uv : 0.f;
                     }
                 if (F16) {
                     // h leaves as FP16 hi + lo scaled by 2^-hs, hs per (position, 64-feature block):
                     // block maximum over the 8 features of each warp, then over the 8 warps
-                    float *hm = hmaxb + (gu_i & 1) * 8 * ROWS;
+                    float *hm = hmaxb + (gu_idx & 1) * 8 * ROWS;
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -1071,9 +1092,8 @@ __global__ void __launch_bounds__(LS_THREADS, 1) layer_stream_kernel(const Layer
                     __syncwarp();
                     if (lane == 0)
                         mbar_arrive(hmax_bar);
-                    if (!(ok = mbar_wait_warp(hmax_bar, gu_i & 1, abort_flag, a.err, lane)))
+                    if (!(ok = mbar_wait_warp(hmax_bar, gu_idx & 1, abort_flag, a.err, lane)))
                         break;
-                    ++gu_i;
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -1116,11 +1136,12 @@ __global__ void __launch_bounds__(LS_THREADS, 1) layer_stream_kernel(const Layer
                             }
                         }
                 }
-                // publish: this warp's part of the group's h is written
+                // publish: this warp's part of the group's h is written (the fence makes
+                // the count a release)
                 __threadfence();
                 __syncwarp();
                 if (lane == 0)
-                    red_release_add(&grp_done[it.g], 1);
+                    atomicAdd(&grp_done[it.g], 1);
             } else {
                 const int m = it.rt * TILE_ROWS + 16 * wg + g;
 #pragma unroll
