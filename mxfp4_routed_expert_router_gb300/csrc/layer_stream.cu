@@ -53,8 +53,12 @@ using namespace gemm;
 constexpr int LS_WARPS = 9;  // warp 0 streams, warps 1..8 compute (one 16-row group each)
 constexpr int LS_THREADS = LS_WARPS * 32;
 constexpr int LS_COMPUTE_WARPS = 8;
-constexpr int LS_SMEM_LIMIT = 232448;
-constexpr int LS_STAGE_TARGET = 52224;
+// CTAs per SM.  Two CTAs (two independent streams, four compute warps per
+// sub-partition, 112 registers, half the ring each) measured slower than one
+// CTA with 168 registers for every token tile, so all tiles run one.
+__host__ __device__ constexpr int ls_ctas_per_sm(int nt) { return nt > 0 ? 1 : 1; }
+__host__ __device__ constexpr int ls_smem_limit(int ctas) { return ctas == 1 ? 232448 : 114688; }
+__host__ __device__ constexpr int ls_stage_target(int ctas) { return ctas == 1 ? 52224 : 26624; }
 constexpr int LS_R_MAX = 8;
 constexpr int LS_HS_ROW = 16;  // ints of h block scales kept per token row and stage
 
@@ -70,11 +74,11 @@ __host__ __device__ constexpr int ls_stage_bytes(int nb, int rows, int hsb, int 
 {
     return nb * rows * ls_rowb(ch) + hsb + ch * wchunk;
 }
-__host__ __device__ constexpr int ls_pick_ch(int nb, int rows, int hsb, int wchunk)
+__host__ __device__ constexpr int ls_pick_ch(int nb, int rows, int hsb, int wchunk, int target)
 {
-    return ls_stage_bytes(nb, rows, hsb, 4, wchunk) <= LS_STAGE_TARGET   ? 4
-           : ls_stage_bytes(nb, rows, hsb, 2, wchunk) <= LS_STAGE_TARGET ? 2
-                                                                         : 1;
+    return ls_stage_bytes(nb, rows, hsb, 4, wchunk) <= target   ? 4
+           : ls_stage_bytes(nb, rows, hsb, 2, wchunk) <= target ? 2
+                                                                : 1;
 }
 __host__ __device__ constexpr int ls_max(int a, int b) { return a > b ? a : b; }
 
@@ -84,8 +88,10 @@ struct LsCfg {
     static constexpr int W_CHUNK = F16 ? CHUNK_MX_BYTES : CHUNK_BF16_BYTES;
     static constexpr int ROWS = 8 * NT;
     static constexpr int HSB_DN = F16 ? ROWS * LS_HS_ROW * 4 : 0;
-    static constexpr int CH_GU = ls_pick_ch(1, ROWS, 0, W_CHUNK);
-    static constexpr int CH_DN = ls_pick_ch(2, ROWS, HSB_DN, W_CHUNK);
+    static constexpr int CTAS = ls_ctas_per_sm(NT);
+    static constexpr int SMEM_LIMIT = ls_smem_limit(CTAS);
+    static constexpr int CH_GU = ls_pick_ch(1, ROWS, 0, W_CHUNK, ls_stage_target(CTAS));
+    static constexpr int CH_DN = ls_pick_ch(2, ROWS, HSB_DN, W_CHUNK, ls_stage_target(CTAS));
     static constexpr int STAGE = (ls_max(ls_stage_bytes(1, ROWS, 0, CH_GU, W_CHUNK),
                                          ls_stage_bytes(2, ROWS, HSB_DN, CH_DN, W_CHUNK)) +
                                   127) / 128 * 128;
@@ -807,7 +813,7 @@ __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem 
             }
                 };
         if (ch_n == CH && (s + 1) * CH * 128 <= K) {
-#pragma unroll
+#pragma unroll(C::CTAS == 1 ? CH : 1)
             for (int c = 0; c < CH; ++c) {
                 half_chunk(c, 0, std::true_type{});
                 half_chunk(c, 1, std::true_type{});
@@ -830,7 +836,7 @@ __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem 
 // ------------------------------------------------------------------ the kernel
 
 template <int WFMT, int NT>
-__global__ void __launch_bounds__(LS_THREADS, 1) layer_stream_kernel(const LayerArgs a)
+__global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_kernel(const LayerArgs a)
 {
     using C = LsCfg<WFMT, NT>;
     constexpr bool F16 = C::F16;
@@ -1188,7 +1194,7 @@ int ls_ring_depth(int G, int n, int E, int T)
 {
     using C = LsCfg<WFMT, NT>;
     const LsSmem base = ls_smem(0, G, n, T, C::STAGE, C::RED_BYTES, C::HMAX_BYTES);
-    int R = (LS_SMEM_LIMIT - base.total) / C::STAGE;
+    int R = (C::SMEM_LIMIT - base.total) / C::STAGE;
     if (R > LS_R_MAX)
         R = LS_R_MAX;
     // phase-0 scratch lives in the ring: routing keys and selection, prep
@@ -1212,13 +1218,13 @@ cudaError_t ls_launch(LayerArgs a, cudaStream_t st)
     auto kern = layer_stream_kernel<WFMT, NT>;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LS_SMEM_LIMIT);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_LIMIT);
         if (e != cudaSuccess)
             return e;
         attr = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)sm_count());
+    cfg.gridDim = dim3((unsigned)(sm_count() * C::CTAS));
     cfg.blockDim = dim3(LS_THREADS);
     cfg.dynamicSmemBytes = (size_t)L.total;
     cfg.stream = st;
