@@ -107,6 +107,47 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, v
     return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps (up to ns nanoseconds)
+// until the phase completes instead of spinning, leaving issue slots to the
+// warps that have work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded warp-wide wait for a role that waits long and has nothing else to
+// do meanwhile (epilogue, copy issuers): sleeps in the barrier between polls.
+__device__ __noinline__ bool mbar_wait_sleep_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *err)
+{
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 20000))
+            return true;
+        if (*abort_flag)
+            return false;
+        if (global_ns() - t0 > WAIT_LIMIT_NS) {
+            atomicCAS(err, 0, DEV_ERR_WAIT_TIMEOUT);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool mbar_wait_sleep_warp(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *err,
+                                                     int lane)
+{
+    bool ok = true;
+    if (lane == 0)
+        ok = mbar_try_wait(bar, parity) || mbar_wait_sleep_slow(bar, parity, abort_flag, err);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
 // Bounded wait used while tearing down: true when the phase completed.
 __device__ __noinline__ bool mbar_drain(uint64_t *bar, uint32_t parity)
 {

@@ -13,21 +13,23 @@
 // Mapping to the hardware ("swap-AB": weights are the M side):
 //   D[128 weight rows, N tokens] (FP32, TMEM)  +=  A[128 rows, K] . B[N tokens, K]^T
 //   A = 128 weight rows decoded to BF16 in shared memory by CUDA-core warps,
-//       from MXFP4 chunks streamed out of HBM by bulk async copies;
+//       straight from the MXFP4 chunks in global memory (each decoder thread
+//       keeps its next stages' raw bytes in flight in registers);
 //   B = token rows (BF16; for down the hi and lo BF16 planes of h, two MMAs per
 //       K step), loaded by TMA into the 128-byte-swizzled K-major layout;
 //   MMA = tcgen05.mma kind::f16, M=128, N = 16..NMAX, K=16, issued by one thread.
-// One CTA per SM walks a static schedule of (group, row tile, token tile)
-// work items.  Warp roles:
-//   warp 0      bulk-copies weight chunks into a ring of raw buffers
-//   warp 1      TMA-loads token tiles (B) into the stage ring
-//   warp 2      allocates TMEM, issues the MMAs, commits to mbarriers
-//   warps 3-10  decode raw MXFP4 (or copy BF16) into the swizzled A stage
-//   warps 11-14 epilogue: TMEM -> registers, SwiGLU (gate|up) or FP32 y (down)
-// Two TMEM accumulators let the epilogue of one work item overlap the MMAs of
-// the next.  Every mbarrier wait is bounded: on a timeout the kernel records
-// DEV_ERR_WAIT_TIMEOUT, stops issuing work, waits (bounded) for the copies and
-// MMAs it has in flight, frees its TMEM and exits.
+// A work item is (group, pair of 128-row tiles, token tile): both row tiles
+// share every staged token tile, so a 64 KB stage feeds 2 x 128 x N x 64
+// multiply-adds -- twice as many per staged byte as one row tile.
+// One CTA per SM walks a static schedule of work items.  Warp roles:
+//   warp 0      TMA-loads token tiles (B) into the stage ring
+//   warp 1      allocates TMEM, issues the MMAs, commits to mbarriers
+//   warps 2-9   decode MXFP4 (or copy BF16) into the swizzled A stages
+//   warps 10-13 epilogue: TMEM -> registers, SwiGLU (gate|up) or FP32 y (down)
+// Two TMEM accumulator sets (when N allows) let the epilogue of one work item
+// overlap the MMAs of the next.  Every mbarrier wait is bounded: on a timeout
+// the kernel records DEV_ERR_WAIT_TIMEOUT, stops issuing work, waits (bounded)
+// for the copies and MMAs it has in flight, frees its TMEM and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -41,8 +43,9 @@ namespace {
 
 using namespace gemm;
 
-constexpr int NUM_THREADS = 480;
-constexpr int WARP_WLOAD = 0, WARP_BLOAD = 1, WARP_MMA = 2, WARP_DEC0 = 3, N_DEC_WARPS = 8, WARP_EPI0 = 11;
+constexpr int N_DEC_WARPS = 16;
+constexpr int NUM_THREADS = (2 + N_DEC_WARPS + 4) * 32;
+constexpr int WARP_BLOAD = 0, WARP_MMA = 1, WARP_DEC0 = 2, WARP_EPI0 = WARP_DEC0 + N_DEC_WARPS;
 constexpr int A_STAGE_BYTES = TILE_ROWS * HALF_K * 2;  // 16 KB: 128 rows x 64 BF16
 constexpr int B_BOX_ROWS = 16;
 constexpr int B_BOX_BYTES = B_BOX_ROWS * HALF_K * 2;   // 2 KB
@@ -106,48 +109,60 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int c)
     return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
-template <int NMAX, int NB, int S, int R, int RAW_BYTES>
+// Work item: (expert group, pair of 128-row weight tiles, token tile).  The two
+// row tiles share every token (B) stage, which halves the token bytes staged
+// per multiply-add against one row tile per item.
+__device__ __forceinline__ int tile_pairs(int row_tiles) { return (row_tiles + 1) / 2; }
+
+template <int NMAX, int NB, int S>
 struct Smem {
-    static constexpr int B_STAGE = NMAX * HALF_K * 2 * NB;
-    static constexpr int A_OFF = 0;
-    static constexpr int B_OFF = A_OFF + S * A_STAGE_BYTES;
-    static constexpr int RAW_OFF = B_OFF + S * B_STAGE;
-    static constexpr int BAR_OFF = RAW_OFF + R * RAW_BYTES;
-    static constexpr int N_BARS = 2 * R + 2 * S + 4;
+    static constexpr int A_STAGE = 2 * A_STAGE_BYTES;        // two row tiles x 128 rows x 64 BF16
+    static constexpr int B_STAGE = NMAX * HALF_K * 2 * NB;   // NB token planes
+    static constexpr int STAGE = A_STAGE + B_STAGE;
+    static constexpr int BAR_OFF = S * STAGE;
+    static constexpr int N_BARS = 2 * S + 4;
     static constexpr int SCHED_OFF = BAR_OFF + N_BARS * 8;
     static constexpr int MISC_OFF = SCHED_OFF + (MAX_GROUPS + 1) * 4;
     static constexpr int TOTAL = MISC_OFF + 32 + 1024;  // + alignment slack
 };
 
+// Stages of raw weights a decoder thread keeps in flight in registers (its own
+// global loads, so no shared-memory staging of the raw chunks is needed).
+template <int WFMT>
+struct DecPipe {
+    static constexpr int PD = WFMT == FMT_MXFP4 ? 4 : 2;
+    static constexpr int V = WFMT == FMT_MXFP4 ? 1 : 2;  // vectors per thread, tile and stage (MXFP4: 8 bytes)
+};
+
 // ------------------------------------------------------------------ kernel
 
-template <bool GU, int WFMT, int NMAX, int S, int R>
+template <bool GU, int WFMT, int NMAX, int S>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_b2)
 {
     constexpr int NB = GU ? 1 : 2;
-    constexpr int RAW_BYTES = WFMT == FMT_MXFP4 ? CHUNK_MX_BYTES : CHUNK_BF16_BYTES;
-    using L = Smem<NMAX, NB, S, R, RAW_BYTES>;
-    constexpr int TMEM_COLS = 2 * NMAX < 32 ? 32 : 2 * NMAX;
+    using L = Smem<NMAX, NB, S>;
+    constexpr int NBUF = 4 * NMAX <= 512 ? 2 : 1;      // accumulator sets (two row tiles each)
+    constexpr int TMEM_COLS_RAW = 2 * NMAX * NBUF;
+    constexpr int TMEM_COLS = TMEM_COLS_RAW < 32 ? 32 : TMEM_COLS_RAW;
     static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM columns");
     static_assert(L::TOTAL <= 232448, "shared memory");
+    using DP = DecPipe<WFMT>;
+    constexpr int PD = DP::PD, V = DP::V;
 
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);
-    uint64_t *raw_full = bars, *raw_empty = bars + R, *ab_full = bars + 2 * R, *ab_empty = bars + 2 * R + S;
-    uint64_t *acc_full = bars + 2 * R + 2 * S, *acc_empty = acc_full + 2;
+    uint64_t *ab_full = bars, *ab_empty = bars + S;
+    uint64_t *acc_full = bars + 2 * S, *acc_empty = acc_full + 2;
     int *prefix = reinterpret_cast<int *>(smem + L::SCHED_OFF);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::MISC_OFF + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int pairs = tile_pairs(a.row_tiles);
 
     if (tid == 0) {
-        for (int i = 0; i < R; ++i) {
-            mbar_init(&raw_full[i], 1);
-            mbar_init(&raw_empty[i], N_DEC_WARPS);
-        }
         for (int i = 0; i < S; ++i) {
             mbar_init(&ab_full[i], 1 + N_DEC_WARPS);
             mbar_init(&ab_empty[i], 1);
@@ -166,8 +181,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    if (warp == WARP_WLOAD)
-        schedule_prefix(a.grp_count, a.G, a.row_tiles, NMAX, prefix, lane);
+    if (warp == WARP_BLOAD)
+        schedule_prefix(a.grp_count, a.G, pairs, NMAX, prefix, lane);
     if (warp == WARP_BLOAD && lane == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b2)) : "memory");
@@ -180,52 +195,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int nstages = 2 * a.kchunks;
 
     // Every role walks the same static schedule t = blockIdx.x, +gridDim.x, ...
-    // Single-thread roles keep the whole warp in the loop (lane 0 issues) so
-    // that no lanes sit parked at a warp barrier while lane 0 works.
-    if (warp == WARP_WLOAD) {
-        // ---------------------------------------------------------- weight chunks -> raw ring
-        uint32_t rc = 0, armed = 0, armed_par = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const WorkItem w = decompose(t, prefix, a.grp_count, a.G, a.row_tiles, NMAX);
-            const uint8_t *src =
-                a.wbase + (size_t)w.g * a.group_bytes + (size_t)w.rt * a.kchunks * (size_t)a.chunk_bytes;
-            for (int kc = 0; kc < a.kchunks; ++kc, ++rc) {
-                const int slot = rc % R;
-                const uint32_t ph = (rc / R) & 1;
-                if (!(ok = mbar_wait_warp(&raw_empty[slot], ph ^ 1, abort_flag, a.err, lane)))
-                    break;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&raw_full[slot], RAW_BYTES);
-                    bulk_g2s(smem + L::RAW_OFF + slot * RAW_BYTES, src + (size_t)kc * a.chunk_bytes, RAW_BYTES,
-                             &raw_full[slot]);
-                }
-                armed |= 1u << slot;
-                armed_par = (armed_par & ~(1u << slot)) | (ph << slot);
-            }
-        }
-        // drain: every armed raw buffer's last copy has landed
-        if (lane == 0)
-            for (int s = 0; s < R; ++s)
-                if (armed & (1u << s))
-                    mbar_drain(&raw_full[s], (armed_par >> s) & 1);
-        __syncwarp();
-    } else if (warp == WARP_BLOAD) {
+    // (decompose() over row-tile pairs: w.rt is the pair index).  Single-thread
+    // roles keep the whole warp in the loop (lane 0 issues).
+    if (warp == WARP_BLOAD) {
         // ---------------------------------------------------------- token tiles (B) -> stage ring
         uint32_t sc = 0, armed = 0, armed_par = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const WorkItem w = decompose(t, prefix, a.grp_count, a.G, a.row_tiles, NMAX);
+            const WorkItem w = decompose(t, prefix, a.grp_count, a.G, pairs, NMAX);
             int row0;
             const CUtensorMap *m0 = &map_b;
-            if (GU) {
-                // routed groups read gathered rows by position, shared groups x by token
-                if (w.g < a.E) {
-                    row0 = a.grp_start[w.g] + w.tok0;
-                } else {
-                    row0 = w.tok0;
-                    m0 = &map_b2;
-                }
+            if (GU && w.g >= a.E) {  // shared groups read x by token, routed groups gathered rows
+                row0 = w.tok0;
+                m0 = &map_b2;
             } else {
                 row0 = a.grp_start[w.g] + w.tok0;
             }
@@ -234,11 +216,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int st = 0; st < nstages; ++st, ++sc) {
                 const int slot = sc % S;
                 const uint32_t ph = (sc / S) & 1;
-                if (!(ok = mbar_wait_warp(&ab_empty[slot], ph ^ 1, abort_flag, a.err, lane)))
+                if (!(ok = mbar_wait_sleep_warp(&ab_empty[slot], ph ^ 1, abort_flag, a.err, lane)))
                     break;
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&ab_full[slot], bytes);
-                    uint8_t *bdst = smem + L::B_OFF + slot * L::B_STAGE;
+                    uint8_t *bdst = smem + slot * L::STAGE + L::A_STAGE;
                     for (int b = 0; b < nbox; ++b) {
                         tma_2d(bdst + b * B_BOX_BYTES, m0, st * HALF_K, row0 + b * B_BOX_ROWS, &ab_full[slot]);
                         if (!GU)
@@ -262,13 +244,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t sc = 0, tc = 0, last_acc = 0, last_par = 0;
         bool issued = false, ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
-            const WorkItem w = decompose(t, prefix, a.grp_count, a.G, a.row_tiles, NMAX);
-            const int buf = tc & 1;
-            const uint32_t aph = (tc >> 1) & 1;
-            if (!(ok = mbar_wait_warp(&acc_empty[buf], aph ^ 1, abort_flag, a.err, lane)))
+            const WorkItem w = decompose(t, prefix, a.grp_count, a.G, pairs, NMAX);
+            const bool two = 2 * w.rt + 1 < a.row_tiles;
+            const int buf = NBUF == 2 ? (tc & 1) : 0;
+            const uint32_t aph = (NBUF == 2 ? (tc >> 1) : tc) & 1;
+            if (!(ok = mbar_wait_sleep_warp(&acc_empty[buf], aph ^ 1, abort_flag, a.err, lane)))
                 break;
             tc_fence_after();
-            const uint32_t d_tmem = tmem_base + (uint32_t)(buf * NMAX);
+            const uint32_t d_tmem = tmem_base + (uint32_t)(buf * 2 * NMAX);
             const uint32_t idesc = idesc_bf16(w.n_mma);
             for (int st = 0; st < nstages; ++st, ++sc) {
                 const int slot = sc % S;
@@ -276,14 +259,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t a_addr = smem_addr(smem + L::A_OFF + slot * A_STAGE_BYTES);
-                    const uint32_t b_addr = smem_addr(smem + L::B_OFF + slot * L::B_STAGE);
+                    const uint32_t a_addr = smem_addr(smem + slot * L::STAGE);
+                    const uint32_t b_addr = a_addr + L::A_STAGE;
 #pragma unroll
-                    for (int j = 0; j < HALF_K / 16; ++j) {
-                        const uint64_t ad = sw128_desc(a_addr + j * 32);
-                        tc_mma(d_tmem, ad, sw128_desc(b_addr + j * 32), idesc, (st | j) ? 1u : 0u);
-                        if (!GU)
-                            tc_mma(d_tmem, ad, sw128_desc(b_addr + NMAX * HALF_K * 2 + j * 32), idesc, 1u);
+                    for (int j = 0; j < 2; ++j) {
+                        if (j == 1 && !two)
+                            break;
+#pragma unroll
+                        for (int kk = 0; kk < HALF_K / 16; ++kk) {
+                            const uint64_t ad = sw128_desc(a_addr + j * A_STAGE_BYTES + kk * 32);
+                            tc_mma(d_tmem + j * NMAX, ad, sw128_desc(b_addr + kk * 32), idesc, (st | kk) ? 1u : 0u);
+                            if (!GU)
+                                tc_mma(d_tmem + j * NMAX, ad, sw128_desc(b_addr + NMAX * HALF_K * 2 + kk * 32), idesc,
+                                       1u);
+                        }
                     }
                     tc_commit(&ab_empty[slot]);
                 }
@@ -304,52 +293,109 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
     } else if (warp < WARP_EPI0) {
         // ---------------------------------------------------------- decoders
-        // Each warp waits for itself (lane 0 polls) and arrives on ab_full
-        // once, so the 8 decoder warps never stall behind one another.
-        const int dt = tid - WARP_DEC0 * 32;   // 0..255
-        const int r = dt >> 1, blk = dt & 1;   // tile row, 32-element block of the 64-wide stage
-        uint32_t rc = 0, sc = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            for (int kc = 0; kc < a.kchunks && ok; ++kc, ++rc) {
-                const int rslot = rc % R;
-                if (!(ok = mbar_wait_warp(&raw_full[rslot], (rc / R) & 1, abort_flag, a.err, lane)))
-                    break;
-                const uint8_t *raw = smem + L::RAW_OFF + rslot * RAW_BYTES;
-                for (int h = 0; h < 2; ++h, ++sc) {
-                    const int slot = sc % S;
-                    if (!(ok = mbar_wait_warp(&ab_empty[slot], ((sc / S) & 1) ^ 1, abort_flag, a.err, lane)))
-                        break;
-                    uint8_t *adst = smem + L::A_OFF + slot * A_STAGE_BYTES;
-                    if (WFMT == FMT_MXFP4) {
-                        const uint4 cw = *reinterpret_cast<const uint4 *>(raw + h * (CHUNK_MX_CODE_BYTES / 2) + r * 32 +
-                                                                          blk * 16);
-                        const uint32_t s2 = e8m0_to_bf16x2(raw[CHUNK_MX_CODE_BYTES + r * 4 + h * 2 + blk]);
-                        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+        // Thread (r, blk, hf) owns row r of both row tiles and the 16 elements
+        // hf of the 32-wide block blk of every 64-wide stage.  It loads its raw
+        // codes and scale straight from global memory PD stages ahead (into
+        // registers), decodes the current stage into the swizzled A stage and
+        // arrives on ab_full once per warp.
+        const int dt = tid - WARP_DEC0 * 32;                     // 0..511
+        const int r = dt >> 2, blk = (dt >> 1) & 1, hf = dt & 1;  // tile row, block, half of the block
+        uint32_t soff[2];                                         // swizzled offsets of this thread's 2 x 16 bytes
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c)
+            soff[c] = sw128_offset(r, blk * 4 + hf * 2 + c);
+        uint2 qc[PD][2][V];                    // raw codes (MXFP4: 8 bytes; BF16: 2 x 8... see V) per tile
+        uint4 qb[PD][2][V];                    // BF16 weights: 2 x 16 bytes per tile
+        uint32_t qs[PD][2];                    // E8M0 scale bytes (MXFP4)
+        (void)qc;
+        (void)qb;
+        // stage gs of this CTA's item sequence -> raw source of tile j
+        int f_item = -1;                       // item whose addresses are cached below
+        const uint8_t *f_src[2] = {nullptr, nullptr};
+        auto fetch = [&](int gs, int k) {
+            const int ii = gs / nstages, st = gs % nstages;
+            const int t = blockIdx.x + ii * gridDim.x;
+            if (t >= total)
+                return;
+            if (ii != f_item) {
+                f_item = ii;
+                const WorkItem w = decompose(t, prefix, a.grp_count, a.G, pairs, NMAX);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int rt = 2 * w.rt + j;
+                    f_src[j] = rt < a.row_tiles
+                                   ? a.wbase + (size_t)w.g * a.group_bytes + (size_t)rt * a.kchunks * (size_t)a.chunk_bytes
+                                   : nullptr;
+                }
+            }
+            const int kc = st >> 1, h = st & 1;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                if (!f_src[j])
+                    continue;
+                const uint8_t *ch = f_src[j] + (size_t)kc * a.chunk_bytes;
+                if (WFMT == FMT_MXFP4) {
+                    qc[k][j][0] = __ldg(reinterpret_cast<const uint2 *>(ch + h * (CHUNK_MX_CODE_BYTES / 2) + r * 32 +
+                                                                        blk * 16 + hf * 8));
+                    qs[k][j] = __ldg(ch + CHUNK_MX_CODE_BYTES + r * 4 + h * 2 + blk);
+                } else {
+                    const uint4 *src =
+                        reinterpret_cast<const uint4 *>(ch + h * (CHUNK_BF16_BYTES / 2) + r * 128 + blk * 64 + hf * 32);
+#pragma unroll
+                    for (int v = 0; v < V; ++v)
+                        qb[k][j][v] = __ldg(src + v);
+                }
+            }
+        };
+        const int n_items = total > (int)blockIdx.x ? (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+        const int total_st = n_items * nstages;
+#pragma unroll
+        for (int k = 0; k < PD; ++k)
+            fetch(k, k);
+        bool ok = true;
+        int c_item = -1;   // item of the stage being decoded, and whether it has a second row tile
+        bool two = false;
+        for (int gs0 = 0; gs0 < total_st && ok; gs0 += PD) {
+#pragma unroll
+            for (int k = 0; k < PD; ++k) {
+                const int gs = gs0 + k;
+                if (gs >= total_st)
+                    break;
+                const int slot = gs % S;
+                if (!(ok = mbar_wait_warp(&ab_empty[slot], ((gs / S) & 1) ^ 1, abort_flag, a.err, lane)))
+                    break;
+                const int ii = gs / nstages;
+                if (ii != c_item) {
+                    c_item = ii;
+                    const WorkItem w = decompose(blockIdx.x + ii * gridDim.x, prefix, a.grp_count, a.G, pairs, NMAX);
+                    two = 2 * w.rt + 1 < a.row_tiles;
+                }
+                uint8_t *adst = smem + slot * L::STAGE;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    if (j == 1 && !two)
+                        break;
+                    uint8_t *aj = adst + j * A_STAGE_BYTES;
+                    if (WFMT == FMT_MXFP4) {
+                        const uint32_t s2 = e8m0_to_bf16x2(qs[k][j]);
+                        const uint32_t words[2] = {qc[k][j][0].x, qc[k][j][0].y};
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
                             uint32_t o[4];
                             decode_word(words[c], s2, o);
-                            *reinterpret_cast<uint4 *>(adst + sw128_offset(r, blk * 4 + c)) =
-                                make_uint4(o[0], o[1], o[2], o[3]);
+                            *reinterpret_cast<uint4 *>(aj + soff[c]) = make_uint4(o[0], o[1], o[2], o[3]);
                         }
                     } else {
-                        const uint4 *src = reinterpret_cast<const uint4 *>(raw + h * (CHUNK_BF16_BYTES / 2) + r * 128 +
-                                                                           blk * 64);
 #pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            *reinterpret_cast<uint4 *>(adst + sw128_offset(r, blk * 4 + c)) = src[c];
+                        for (int c = 0; c < 2; ++c)
+                            *reinterpret_cast<uint4 *>(aj + soff[c]) = qb[k][j][c];
                     }
-                    fence_proxy_async();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(&ab_full[slot]);
                 }
-                if (ok) {
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(&raw_empty[rslot]);
-                }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&ab_full[slot]);
+                fetch(gs + PD, k);
             }
         }
     } else {
@@ -357,44 +403,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int q = warp & 3;                 // TMEM lane quadrant of this warp
         uint32_t tc = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
-            const WorkItem w = decompose(t, prefix, a.grp_count, a.G, a.row_tiles, NMAX);
-            const int buf = tc & 1;
-            if (!mbar_wait_warp(&acc_full[buf], (tc >> 1) & 1, abort_flag, a.err, lane))
+            const WorkItem w = decompose(t, prefix, a.grp_count, a.G, pairs, NMAX);
+            const int buf = NBUF == 2 ? (tc & 1) : 0;
+            const uint32_t aph = (NBUF == 2 ? (tc >> 1) : tc) & 1;
+            if (!mbar_wait_sleep_warp(&acc_full[buf], aph, abort_flag, a.err, lane))
                 break;
             tc_fence_after();
             const int pos0 = a.grp_start[w.g] + w.tok0;
-            const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * NMAX);
-            for (int c0 = 0; c0 < w.n_mma; c0 += 16) {
-                float v[16];
-                tmem_ld16(taddr + c0, v);
-                if (GU) {
-                    // rows 16*gr + i: gate of feature 8*gr + i%8 when i < 8, up when i >= 8;
-                    // the gate lane finishes tokens c0..c0+7, its up partner (lane ^ 8) c0+8..c0+15
-                    const int n = gu_row_feature(w.rt, 32 * q + lane);
-                    const bool up_lane = gu_row_is_up(lane);
+#pragma unroll 1
+            for (int j = 0; j < 2; ++j) {
+                const int rt = 2 * w.rt + j;
+                if (rt >= a.row_tiles)
+                    break;
+                const uint32_t taddr =
+                    tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 2 * NMAX + j * NMAX);
+                for (int c0 = 0; c0 < w.n_mma; c0 += 16) {
+                    float v[16];
+                    tmem_ld16(taddr + c0, v);
+                    if (GU) {
+                        // rows 16*gr + i: gate of feature 8*gr + i%8 when i < 8, up when i >= 8;
+                        // the gate lane finishes tokens c0..c0+7, its up partner (lane ^ 8) c0+8..c0+15
+                        const int n = gu_row_feature(rt, 32 * q + lane);
+                        const bool up_lane = gu_row_is_up(lane);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float send = up_lane ? v[j] : v[8 + j];
-                        const float recv = __shfl_xor_sync(0xffffffffu, send, 8);
-                        const float gv = up_lane ? recv : v[j];
-                        const float uv = up_lane ? v[8 + j] : recv;
-                        const int tok = c0 + (up_lane ? 8 : 0) + j;
-                        if (tok < w.nvalid && n < a.I) {
-                            const float hv = gv / (1.0f + __expf(-gv)) * uv;
-                            const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
-                            const __nv_bfloat16 lb = __float2bfloat16_rn(hv - __bfloat162float(hb));
-                            const size_t o = (size_t)(pos0 + tok) * a.I + n;
-                            a.h_out[o] = __bfloat16_as_ushort(hb);
-                            a.h_out[o + a.h_plane] = __bfloat16_as_ushort(lb);
+                        for (int jj = 0; jj < 8; ++jj) {
+                            const float send = up_lane ? v[jj] : v[8 + jj];
+                            const float recv = __shfl_xor_sync(0xffffffffu, send, 8);
+                            const float gv = up_lane ? recv : v[jj];
+                            const float uv = up_lane ? v[8 + jj] : recv;
+                            const int tok = c0 + (up_lane ? 8 : 0) + jj;
+                            if (tok < w.nvalid && n < a.I) {
+                                const float hv = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+                                const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
+                                const __nv_bfloat16 lb = __float2bfloat16_rn(hv - __bfloat162float(hb));
+                                const size_t o = (size_t)(pos0 + tok) * a.I + n;
+                                a.h_out[o] = __bfloat16_as_ushort(hb);
+                                a.h_out[o + a.h_plane] = __bfloat16_as_ushort(lb);
+                            }
                         }
-                    }
-                } else {
-                    const int m = w.rt * TILE_ROWS + 32 * q + lane;
-                    if (m < a.H) {
+                    } else {
+                        const int m = rt * TILE_ROWS + 32 * q + lane;
+                        if (m < a.H) {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            if (c0 + j < w.nvalid)
-                                a.y_out[(size_t)(pos0 + c0 + j) * a.H + m] = v[j];
+                            for (int jj = 0; jj < 16; ++jj)
+                                if (c0 + jj < w.nvalid)
+                                    a.y_out[(size_t)(pos0 + c0 + jj) * a.H + m] = v[jj];
+                        }
                     }
                 }
             }
@@ -416,13 +470,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // ------------------------------------------------------------------ host side
 
-template <bool GU, int WFMT, int NMAX, int S, int R>
+template <bool GU, int WFMT, int NMAX, int S>
 cudaError_t launch_cfg(const TcArgs &a, const CUtensorMap &m1, const CUtensorMap &m2, cudaStream_t st)
 {
     constexpr int NB = GU ? 1 : 2;
-    constexpr int RAW_BYTES = WFMT == FMT_MXFP4 ? CHUNK_MX_BYTES : CHUNK_BF16_BYTES;
-    constexpr int SMEM = Smem<NMAX, NB, S, R, RAW_BYTES>::TOTAL;
-    auto kern = gemm_tc_kernel<GU, WFMT, NMAX, S, R>;
+    constexpr int SMEM = Smem<NMAX, NB, S>::TOTAL;
+    auto kern = gemm_tc_kernel<GU, WFMT, NMAX, S>;
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
@@ -434,8 +487,8 @@ cudaError_t launch_cfg(const TcArgs &a, const CUtensorMap &m1, const CUtensorMap
     return cudaGetLastError();
 }
 
-// token tile sizes: decode-sized batches use a small tile (more pipeline
-// stages and raw buffers in flight), larger batches the full tile.
+// token tile sizes: small batches use a small tile (more stages in flight),
+// larger batches the full tile.
 constexpr int SMALL_T = 64;
 
 template <bool GU>
@@ -445,16 +498,16 @@ cudaError_t launch_any(const TcArgs &a, int fmt, int T, const CUtensorMap &m1, c
     const bool small = T <= SMALL_T;
     if constexpr (GU) {
         if (fmt == FMT_MXFP4)
-            return small ? launch_cfg<true, FMT_MXFP4, 64, 6, 8>(a, m1, m2, st)
-                         : launch_cfg<true, FMT_MXFP4, 256, 3, 4>(a, m1, m2, st);
-        return small ? launch_cfg<true, FMT_BF16, 64, 4, 2>(a, m1, m2, st)
-                     : launch_cfg<true, FMT_BF16, 256, 3, 2>(a, m1, m2, st);
+            return small ? launch_cfg<true, FMT_MXFP4, 64, 4>(a, m1, m2, st)
+                         : launch_cfg<true, FMT_MXFP4, 256, 3>(a, m1, m2, st);
+        return small ? launch_cfg<true, FMT_BF16, 64, 4>(a, m1, m2, st)
+                     : launch_cfg<true, FMT_BF16, 256, 3>(a, m1, m2, st);
     } else {
         if (fmt == FMT_MXFP4)
-            return small ? launch_cfg<false, FMT_MXFP4, 64, 5, 6>(a, m1, m2, st)
-                         : launch_cfg<false, FMT_MXFP4, 128, 3, 4>(a, m1, m2, st);
-        return small ? launch_cfg<false, FMT_BF16, 64, 4, 2>(a, m1, m2, st)
-                     : launch_cfg<false, FMT_BF16, 128, 3, 2>(a, m1, m2, st);
+            return small ? launch_cfg<false, FMT_MXFP4, 64, 4>(a, m1, m2, st)
+                         : launch_cfg<false, FMT_MXFP4, 128, 3>(a, m1, m2, st);
+        return small ? launch_cfg<false, FMT_BF16, 64, 4>(a, m1, m2, st)
+                     : launch_cfg<false, FMT_BF16, 128, 3>(a, m1, m2, st);
     }
 }
 
