@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t idesc = idesc_bf16(w.n_mma);
             for (int st = 0; st < nstages; ++st, ++sc) {
                 const int slot = sc % S;
-                if (!(ok = mbar_wait_warp(&ab_full[slot], (sc / S) & 1, abort_flag, a.err, lane)))
+                if (!(ok = mbar_wait_sleep_warp(&ab_full[slot], (sc / S) & 1, abort_flag, a.err, lane)))
                     break;
                 tc_fence_after();
                 if (lane == 0) {
@@ -309,31 +309,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t qs[PD][2];                    // E8M0 scale bytes (MXFP4)
         (void)qc;
         (void)qb;
-        // stage gs of this CTA's item sequence -> raw source of tile j
-        int f_item = -1;                       // item whose addresses are cached below
+        // raw source of the stage PD ahead of the one being decoded; walked with
+        // counters (item, stage in item, chunk pointers) so that no division or
+        // schedule search runs per stage
+        int f_ii = 0, f_st = 0;                // next stage to fetch: item index, stage in item
         const uint8_t *f_src[2] = {nullptr, nullptr};
-        auto fetch = [&](int gs, int k) {
-            const int ii = gs / nstages, st = gs % nstages;
-            const int t = blockIdx.x + ii * gridDim.x;
-            if (t >= total)
-                return;
-            if (ii != f_item) {
-                f_item = ii;
-                const WorkItem w = decompose(t, prefix, a.grp_count, a.G, pairs, NMAX);
+        const int n_items = total > (int)blockIdx.x ? (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+        auto set_item = [&](int ii) {
+            const WorkItem w = decompose(blockIdx.x + ii * gridDim.x, prefix, a.grp_count, a.G, pairs, NMAX);
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int rt = 2 * w.rt + j;
-                    f_src[j] = rt < a.row_tiles
-                                   ? a.wbase + (size_t)w.g * a.group_bytes + (size_t)rt * a.kchunks * (size_t)a.chunk_bytes
-                                   : nullptr;
-                }
+            for (int j = 0; j < 2; ++j) {
+                const int rt = 2 * w.rt + j;
+                f_src[j] = rt < a.row_tiles
+                               ? a.wbase + (size_t)w.g * a.group_bytes + (size_t)rt * a.kchunks * (size_t)a.chunk_bytes
+                               : nullptr;
             }
-            const int kc = st >> 1, h = st & 1;
+        };
+        if (n_items > 0)
+            set_item(0);
+        auto fetch = [&](int k) {
+            if (f_ii >= n_items)
+                return;
+            const int h = f_st & 1;
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 if (!f_src[j])
                     continue;
-                const uint8_t *ch = f_src[j] + (size_t)kc * a.chunk_bytes;
+                const uint8_t *ch = f_src[j];
                 if (WFMT == FMT_MXFP4) {
                     qc[k][j][0] = __ldg(reinterpret_cast<const uint2 *>(ch + h * (CHUNK_MX_CODE_BYTES / 2) + r * 32 +
                                                                         blk * 16 + hf * 8));
@@ -346,15 +348,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         qb[k][j][v] = __ldg(src + v);
                 }
             }
+            // advance: next half of the chunk, next chunk, or the next item
+            if (h == 1) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    if (f_src[j])
+                        f_src[j] += a.chunk_bytes;
+            }
+            if (++f_st == nstages) {
+                f_st = 0;
+                if (++f_ii < n_items)
+                    set_item(f_ii);
+            }
         };
-        const int n_items = total > (int)blockIdx.x ? (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
         const int total_st = n_items * nstages;
 #pragma unroll
         for (int k = 0; k < PD; ++k)
-            fetch(k, k);
+            fetch(k);
         bool ok = true;
-        int c_item = -1;   // item of the stage being decoded, and whether it has a second row tile
+        int c_st = 0, c_ii = 0;   // stage being decoded: stage in item, item
         bool two = false;
+        if (n_items > 0) {
+            const WorkItem w = decompose(blockIdx.x, prefix, a.grp_count, a.G, pairs, NMAX);
+            two = 2 * w.rt + 1 < a.row_tiles;
+        }
         for (int gs0 = 0; gs0 < total_st && ok; gs0 += PD) {
 #pragma unroll
             for (int k = 0; k < PD; ++k) {
@@ -362,14 +379,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (gs >= total_st)
                     break;
                 const int slot = gs % S;
-                if (!(ok = mbar_wait_warp(&ab_empty[slot], ((gs / S) & 1) ^ 1, abort_flag, a.err, lane)))
+                if (!(ok = mbar_wait_sleep_warp(&ab_empty[slot], ((gs / S) & 1) ^ 1, abort_flag, a.err, lane)))
                     break;
-                const int ii = gs / nstages;
-                if (ii != c_item) {
-                    c_item = ii;
-                    const WorkItem w = decompose(blockIdx.x + ii * gridDim.x, prefix, a.grp_count, a.G, pairs, NMAX);
-                    two = 2 * w.rt + 1 < a.row_tiles;
-                }
                 uint8_t *adst = smem + slot * L::STAGE;
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
@@ -395,7 +406,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&ab_full[slot]);
-                fetch(gs + PD, k);
+                fetch(k);
+                if (++c_st == nstages) {
+                    c_st = 0;
+                    if (++c_ii < n_items) {
+                        const WorkItem w =
+                            decompose(blockIdx.x + c_ii * gridDim.x, prefix, a.grp_count, a.G, pairs, NMAX);
+                        two = 2 * w.rt + 1 < a.row_tiles;
+                    }
+                }
             }
         }
     } else {
