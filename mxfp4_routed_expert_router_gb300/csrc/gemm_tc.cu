@@ -44,7 +44,8 @@ namespace {
 using namespace gemm;
 
 constexpr int N_DEC_WARPS = 16;
-constexpr int NUM_THREADS = (2 + N_DEC_WARPS + 4) * 32;
+constexpr int N_EPI_WARPS = 8;  // two per TMEM lane quadrant, splitting the columns
+constexpr int NUM_THREADS = (2 + N_DEC_WARPS + N_EPI_WARPS) * 32;
 constexpr int WARP_BLOAD = 0, WARP_MMA = 1, WARP_DEC0 = 2, WARP_EPI0 = WARP_DEC0 + N_DEC_WARPS;
 constexpr int A_STAGE_BYTES = TILE_ROWS * HALF_K * 2;  // 16 KB: 128 rows x 64 BF16
 constexpr int B_BOX_ROWS = 16;
@@ -61,14 +62,40 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar)
                  : "memory");
 }
 
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate)
+// The four K=16 MMAs of one 64-wide stage: descriptors advance by 32 bytes
+// (2 in the address field) per K step; the first MMA accumulates only when
+// acc0 != 0, the other three always.
+__device__ __forceinline__ void tc_mma4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t acc0)
 {
     asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        "{\n .reg .pred p0, p1;\n setp.ne.b32 p0, %4, 0;\n setp.eq.b32 p1, %4, %4;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %3, p1;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %3, p1;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %10, %3, p1;\n}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc0), "l"(a_desc + 2), "l"(b_desc + 2), "l"(a_desc + 4),
+        "l"(b_desc + 4), "l"(a_desc + 6), "l"(b_desc + 6)
         : "memory");
+}
+
+// 32 consecutive TMEM columns of this warp's 32 lanes, one wait
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32])
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr), "r"(taddr + 16)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16])
@@ -169,7 +196,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&acc_full[i], 1);
-            mbar_init(&acc_empty[i], 4);
+            mbar_init(&acc_empty[i], N_EPI_WARPS);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -242,6 +269,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == WARP_MMA) {
         // ---------------------------------------------------------- MMA issue (lane 0)
         uint32_t sc = 0, tc = 0, last_acc = 0, last_par = 0;
+        const uint64_t desc0 = sw128_desc(smem_addr(smem));  // K-major SW128 descriptor of stage 0
         bool issued = false, ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
             const WorkItem w = decompose(t, prefix, a.grp_count, a.G, pairs, NMAX);
@@ -259,20 +287,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t a_addr = smem_addr(smem + slot * L::STAGE);
-                    const uint32_t b_addr = a_addr + L::A_STAGE;
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        if (j == 1 && !two)
-                            break;
-#pragma unroll
-                        for (int kk = 0; kk < HALF_K / 16; ++kk) {
-                            const uint64_t ad = sw128_desc(a_addr + j * A_STAGE_BYTES + kk * 32);
-                            tc_mma(d_tmem + j * NMAX, ad, sw128_desc(b_addr + kk * 32), idesc, (st | kk) ? 1u : 0u);
-                            if (!GU)
-                                tc_mma(d_tmem + j * NMAX, ad, sw128_desc(b_addr + NMAX * HALF_K * 2 + kk * 32), idesc,
-                                       1u);
-                        }
+                    // descriptors of this slot: base plus the slot's offset (address field = bytes >> 4)
+                    const uint64_t ad0 = desc0 + (uint64_t)((slot * L::STAGE) >> 4);
+                    const uint64_t bd0 = ad0 + (uint64_t)(L::A_STAGE >> 4);
+                    tc_mma4(d_tmem, ad0, bd0, idesc, st);
+                    if (!GU)
+                        tc_mma4(d_tmem, ad0, bd0 + (uint64_t)((NMAX * HALF_K * 2) >> 4), idesc, 1u);
+                    if (two) {
+                        const uint64_t ad1 = ad0 + (uint64_t)(A_STAGE_BYTES >> 4);
+                        tc_mma4(d_tmem + NMAX, ad1, bd0, idesc, st);
+                        if (!GU)
+                            tc_mma4(d_tmem + NMAX, ad1, bd0 + (uint64_t)((NMAX * HALF_K * 2) >> 4), idesc, 1u);
                     }
                     tc_commit(&ab_empty[slot]);
                 }
@@ -419,7 +444,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else {
         // ---------------------------------------------------------- epilogue
-        const int q = warp & 3;                 // TMEM lane quadrant of this warp
+        const int q = warp & 3;                        // TMEM lane quadrant of this warp
+        const int eh = (warp - WARP_EPI0) >> 2;         // which column chunks of the quadrant it takes
+        // columns per TMEM wait: gate|up (whose epilogue the MMAs wait for) 32, down 16
+        constexpr int EC = GU ? 32 : 16;
         uint32_t tc = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
             const WorkItem w = decompose(t, prefix, a.grp_count, a.G, pairs, NMAX);
@@ -436,9 +464,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 const uint32_t taddr =
                     tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 2 * NMAX + j * NMAX);
-                for (int c0 = 0; c0 < w.n_mma; c0 += 16) {
-                    float v[16];
-                    tmem_ld16(taddr + c0, v);
+                for (int c0 = EC * eh; c0 < w.n_mma; c0 += 2 * EC) {
+                    // EC columns per wait (a second load may lie past n_mma, inside the
+                    // accumulator, and is then ignored)
+                    float v2[EC];
+                    if constexpr (EC == 32)
+                        tmem_ld32(taddr + c0, v2);
+                    else
+                        tmem_ld16(taddr + c0, v2);
+#pragma unroll
+                    for (int half = 0; half < EC / 16; ++half) {
+                    const int c1 = c0 + 16 * half;
+                    if (c1 >= w.n_mma)
+                        break;
+                    const float *v = v2 + 16 * half;
                     if (GU) {
                         // rows 16*gr + i: gate of feature 8*gr + i%8 when i < 8, up when i >= 8;
                         // the gate lane finishes tokens c0..c0+7, its up partner (lane ^ 8) c0+8..c0+15
@@ -450,7 +489,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             const float recv = __shfl_xor_sync(0xffffffffu, send, 8);
                             const float gv = up_lane ? recv : v[jj];
                             const float uv = up_lane ? v[8 + jj] : recv;
-                            const int tok = c0 + (up_lane ? 8 : 0) + jj;
+                            const int tok = c1 + (up_lane ? 8 : 0) + jj;
                             if (tok < w.nvalid && n < a.I) {
                                 const float hv = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
                                 const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
@@ -465,9 +504,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (m < a.H) {
 #pragma unroll
                             for (int jj = 0; jj < 16; ++jj)
-                                if (c0 + jj < w.nvalid)
-                                    a.y_out[(size_t)(pos0 + c0 + jj) * a.H + m] = v[jj];
+                                if (c1 + jj < w.nvalid)
+                                    a.y_out[(size_t)(pos0 + c1 + jj) * a.H + m] = v[jj];
                         }
+                    }
                     }
                 }
             }
