@@ -24,8 +24,9 @@
 // One CTA per SM walks a static schedule of work items.  Warp roles:
 //   warp 0      TMA-loads token tiles (B) into the stage ring
 //   warp 1      allocates TMEM, issues the MMAs, commits to mbarriers
-//   warps 2-9   decode MXFP4 (or copy BF16) into the swizzled A stages
-//   warps 10-13 epilogue: TMEM -> registers, SwiGLU (gate|up) or FP32 y (down)
+//   warps 2-17  decode MXFP4 (or copy BF16) into the swizzled A stages
+//   warps 18-25 epilogue, two warps per TMEM lane quadrant splitting the
+//               columns: TMEM -> registers, SwiGLU (gate|up) or FP32 y (down)
 // Two TMEM accumulator sets (when N allows) let the epilogue of one work item
 // overlap the MMAs of the next.  Every mbarrier wait is bounded: on a timeout
 // the kernel records DEV_ERR_WAIT_TIMEOUT, stops issuing work, waits (bounded)

@@ -21,16 +21,18 @@
 //  stream    warp 0 takes items from a grid-wide counter and streams each
 //            item's weight chunks (one bulk copy per stage) plus its token
 //            rows (one bulk copy per row) into a ring of shared-memory stages;
-//            16 compute warps decode MXFP4 in registers straight into
-//            warp-level MMA fragments (FP16 operands, FP32 accumulation).
-//            gate|up epilogues write h (FP16 hi + lo, scaled per 64-feature
-//            block) and count finished warps per group; a down item's token
-//            rows are copied only once its group's h is complete, while its
-//            weights are already streaming.
-//  combine   down epilogues write y and count finished warps per (token,
-//            128-feature block); the warp that completes a block sums it into
-//            out in a fixed order (j ascending, then shared groups), so the
-//            result does not depend on which CTA did what.
+//            8 compute warps (16 weight rows each, the full K) decode MXFP4
+//            in registers straight into warp-level MMA fragments (FP16
+//            operands, FP32 accumulation, the E8M0 block scales applied in
+//            FP32 to each 32-wide block's partial sum).  gate|up epilogues
+//            write h (FP16 hi + lo, scaled per 64-feature block) and count
+//            finished warps per group; a down item's token rows are copied
+//            only once its group's h is complete, while its weights are
+//            already streaming.
+//  combine   once every CTA has counted its items done, all warps of the
+//            grid sum (token, 128-feature) blocks of y into out in a fixed
+//            order (j ascending, then shared groups), so the result does not
+//            depend on which CTA did what.
 //
 // The grid is one CTA per SM, launched cooperatively so that all CTAs are
 // resident: CTAs wait on each other only through counters in the caller's
@@ -56,7 +58,7 @@ constexpr int LS_COMPUTE_WARPS = 8;
 // CTAs per SM.  Two CTAs (two independent streams, four compute warps per
 // sub-partition, 112 registers, half the ring each) measured slower than one
 // CTA with 168 registers for every token tile, so all tiles run one.
-__host__ __device__ constexpr int ls_ctas_per_sm(int nt) { return nt > 0 ? 1 : 1; }
+__host__ __device__ constexpr int ls_ctas_per_sm(int /*nt*/) { return 1; }
 __host__ __device__ constexpr int ls_smem_limit(int ctas) { return ctas == 1 ? 232448 : 114688; }
 __host__ __device__ constexpr int ls_stage_target(int ctas) { return ctas == 1 ? 52224 : 26624; }
 constexpr int LS_R_MAX = 8;
@@ -82,22 +84,43 @@ __host__ __device__ constexpr int ls_pick_ch(int nb, int rows, int hsb, int wchu
 }
 __host__ __device__ constexpr int ls_max(int a, int b) { return a > b ? a : b; }
 
+// Items hold up to 8 * NT tokens (NT = the kernel's token tiles).  An item of
+// c tokens runs the code and stage geometry of its own tile class NTI (the
+// smallest power of two with 8 * NTI >= c): a token operand of 8 * NTI rows
+// and as many weight chunks per stage as then fit the stage target.
 template <int WFMT, int NT>
 struct LsCfg {
     static constexpr bool F16 = WFMT == FMT_MXFP4;
     static constexpr int W_CHUNK = F16 ? CHUNK_MX_BYTES : CHUNK_BF16_BYTES;
-    static constexpr int ROWS = 8 * NT;
-    static constexpr int HSB_DN = F16 ? ROWS * LS_HS_ROW * 4 : 0;
+    static constexpr int ROWS = 8 * NT;  // token rows of the largest item
     static constexpr int CTAS = ls_ctas_per_sm(NT);
     static constexpr int SMEM_LIMIT = ls_smem_limit(CTAS);
-    static constexpr int CH_GU = ls_pick_ch(1, ROWS, 0, W_CHUNK, ls_stage_target(CTAS));
-    static constexpr int CH_DN = ls_pick_ch(2, ROWS, HSB_DN, W_CHUNK, ls_stage_target(CTAS));
-    static constexpr int STAGE = (ls_max(ls_stage_bytes(1, ROWS, 0, CH_GU, W_CHUNK),
-                                         ls_stage_bytes(2, ROWS, HSB_DN, CH_DN, W_CHUNK)) +
+    static constexpr int TARGET = ls_stage_target(CTAS);
+    __host__ __device__ static constexpr int hsb_dn(int nti) { return F16 ? 8 * nti * LS_HS_ROW * 4 : 0; }
+    __host__ __device__ static constexpr int ch_gu(int nti) { return ls_pick_ch(1, 8 * nti, 0, W_CHUNK, TARGET); }
+    __host__ __device__ static constexpr int ch_dn(int nti)
+    {
+        return ls_pick_ch(2, 8 * nti, hsb_dn(nti), W_CHUNK, TARGET);
+    }
+    __host__ __device__ static constexpr int stage_of(int nti)
+    {
+        return ls_max(ls_stage_bytes(1, 8 * nti, 0, ch_gu(nti), W_CHUNK),
+                      ls_stage_bytes(2, 8 * nti, hsb_dn(nti), ch_dn(nti), W_CHUNK));
+    }
+    static constexpr int STAGE = (ls_max(ls_max(stage_of(1), NT >= 2 ? stage_of(2) : 0),
+                                         ls_max(NT >= 4 ? stage_of(4) : 0, NT >= 8 ? stage_of(8) : 0)) +
                                   127) / 128 * 128;
     static constexpr int RED_BYTES = 0;
     static constexpr int HMAX_BYTES = 2 * 8 * ROWS * 4;    // block maxima of h, double-buffered
 };
+
+// tile class of an item of c tokens in a kernel of NT token tiles
+template <int NT>
+__device__ __forceinline__ int ls_nti(int c)
+{
+    const int t = (c + 7) >> 3;
+    return t <= 1 ? 1 : t <= 2 ? (NT < 2 ? NT : 2) : t <= 4 ? (NT < 4 ? NT : 4) : NT;
+}
 
 // Shared-memory carve-up (bytes from the 1024-aligned base).  The ring comes
 // first; phase 0 uses it as scratch before the first copy is issued.
@@ -171,7 +194,7 @@ struct LayerArgs {
 
 __device__ __forceinline__ void mma_bf16(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1)
 {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
@@ -180,7 +203,7 @@ __device__ __forceinline__ void mma_bf16(float c[4], const uint32_t a[4], uint32
 
 __device__ __forceinline__ void mma_f16(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1)
 {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
@@ -190,11 +213,24 @@ __device__ __forceinline__ void mma_f16(float c[4], const uint32_t a[4], uint32_
 // m16n8k16 FP16 MMA with a zero C operand: d = A * B
 __device__ __forceinline__ void mma_f16_z(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1)
 {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%10,%10,%10,%10};"
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// Two E8M0 block scales (bytes 2H and 2H+1 of w) -> the BF16 pair of 2^(e-127)
+// (e = 0 gives the subnormal 2^-127, exactly), low byte in the low half.
+template <int H>
+__device__ __forceinline__ uint32_t ue8m0x2_bf16x2(uint32_t w)
+{
+    uint32_t d;
+    if (H == 0)
+        asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n cvt.rn.bf16x2.ue8m0x2 %0, lo;\n}" : "=r"(d) : "r"(w));
+    else
+        asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n cvt.rn.bf16x2.ue8m0x2 %0, hi;\n}" : "=r"(d) : "r"(w));
+    return d;
 }
 
 // FRAG_F16 word -> A fragment: each byte (two OCP E2M1 codes) converts to an
@@ -211,13 +247,6 @@ __device__ __forceinline__ void decode_e2m1(uint32_t w, uint32_t out[4])
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-__device__ __forceinline__ int atom_add_release(int *p, int v)
-{
-    int old;
-    asm volatile("atom.add.release.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
 }
 
 // B fragment: token rows hold K in the x16 order, so a lane's two registers
@@ -293,12 +322,18 @@ __device__ __noinline__ bool wait_geq(const int *p, int target, volatile int *ab
 
 // ------------------------------------------------------------------ phase 0a
 //
-// Warps 0..3 route (LS_ROUTE_THREADS threads, named barrier 1) while warps
-// 4..8 prepare token rows (LS_PREP_THREADS threads, named barrier 2); both
-// walk the same tokens t = blockIdx.x + i * gridDim.x.
-constexpr int LS_ROUTE_THREADS = 128;
+// Warps 0..3 route (one warp per token, no barrier) while warps 4..8 prepare
+// token rows (LS_PREP_THREADS threads, named barrier 2).  Token t belongs to
+// CTA t mod gridDim.x, which writes its routing outputs and its x16 row.
+// With few tokens (T <= LS_LOCAL_ROUTE_T) every CTA routes every token itself
+// so that it can build the schedule without waiting for the other CTAs; only
+// the token rows are then awaited, by the loader, before its first token copy.
+constexpr int LS_ROUTE_WARPS = 4;
+constexpr int LS_ROUTE_THREADS = LS_ROUTE_WARPS * 32;
 constexpr int LS_PREP_THREADS = LS_THREADS - LS_ROUTE_THREADS;
-constexpr int LS_SCRATCH_PREP = 9216;  // byte offset of the prep scratch (after 1024 keys + selection)
+constexpr int LS_SCRATCH_PREP = 9216;  // byte offset of the prep scratch (after the schedule's slot ids)
+constexpr int LS_LOCAL_ROUTE_T = 8;
+constexpr int LS_KEYS_PER_LANE = LS_MAX_EXPERTS / 32;
 
 // Order key of a logit: larger float -> larger key; +0 and -0 equal; NaN
 // below every number.
@@ -312,51 +347,69 @@ __device__ __forceinline__ uint32_t ls_logit_key(float f)
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-// Route token t (threads 0..LS_ROUTE_THREADS-1).  Every expert gets the
-// 64-bit key (order key << 32 | ~e), so keys are distinct and "larger logit,
-// then lower index" is one unsigned compare; the rank of expert e is the
-// number of larger keys, and the experts of rank < k are the selection, in
-// order.  Weights: w_j = exp(l_j - l_0) / sum_{j' < k} exp(l_j' - l_0), l_0
-// the largest kept logit.
-__device__ void ls_route_token(const LayerArgs &a, int t, uint8_t *scratch)
+// the logit of an order key (a NaN key gives a NaN)
+__device__ __forceinline__ float ls_key_logit(uint32_t key)
 {
-    unsigned long long *keys = reinterpret_cast<unsigned long long *>(scratch);
-    int *sel_e = reinterpret_cast<int *>(scratch + 8192);
-    float *sel_v = reinterpret_cast<float *>(sel_e + 32);
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+// Route token t with one warp: softmax top-k, renormalised over the kept k.
+// Lane l holds experts e = l + 32 i as order key + 1 (0: absent or taken).
+// Round j takes the largest key of the warp (redux max) and, among the
+// experts holding it, the lowest index (redux min), so "larger logit, then
+// lower index" is the selection order.  Weights: w_j = exp(l_j - l_0) /
+// sum_{j' < k} exp(l_j' - l_0), l_0 the largest kept logit.  The expert ids
+// go to ids_s[t * k + j] when ids_s is given, and the owner CTA writes both
+// outputs to the caller's arrays.
+__device__ void ls_route_warp(const LayerArgs &a, int t, int lane, int *ids_s, bool owner)
+{
     const float *row = a.logits + (size_t)t * a.E;
-    const int tid = threadIdx.x;
-    for (int e = tid; e < a.E; e += LS_ROUTE_THREADS)
-        keys[e] = ((unsigned long long)ls_logit_key(row[e]) << 32) | (unsigned long long)(0xFFFFFFFFu - e);
-    named_bar_sync(1, LS_ROUTE_THREADS);
-    for (int e = tid; e < a.E; e += LS_ROUTE_THREADS) {
-        const unsigned long long my = keys[e];
-        int r = 0;
-        int i = 0;
-        for (; i + 4 <= a.E; i += 4)
-            r += (keys[i] > my) + (keys[i + 1] > my) + (keys[i + 2] > my) + (keys[i + 3] > my);
-        for (; i < a.E; ++i)
-            r += keys[i] > my;
-        if (r < a.k) {
-            sel_e[r] = e;
-            sel_v[r] = row[e];
+    uint32_t key[LS_KEYS_PER_LANE];
+#pragma unroll
+    for (int i = 0; i < LS_KEYS_PER_LANE; ++i) {
+        const int e = lane + 32 * i;
+        key[i] = e < a.E ? ls_logit_key(__ldg(row + e)) + 1u : 0u;
+    }
+    int my_e = 0;
+    uint32_t my_key = 0;
+    for (int j = 0; j < a.k; ++j) {
+        uint32_t best = 0;
+        int bi = 0;
+#pragma unroll
+        for (int i = 0; i < LS_KEYS_PER_LANE; ++i)
+            if (key[i] > best) {  // strict: the lowest i (lowest expert of the lane) among equals
+                best = key[i];
+                bi = i;
+            }
+        const uint32_t m = __reduce_max_sync(0xffffffffu, best);
+        const uint32_t mine = lane + 32 * bi;
+        const uint32_t ew = __reduce_min_sync(0xffffffffu, best == m ? mine : 0xFFFFFFFFu);
+        if (mine == ew) {
+#pragma unroll
+            for (int i = 0; i < LS_KEYS_PER_LANE; ++i)
+                if (i == bi)
+                    key[i] = 0;
+        }
+        if (lane == j) {
+            my_e = (int)ew;
+            my_key = m - 1u;
         }
     }
-    named_bar_sync(1, LS_ROUTE_THREADS);
-    if (tid < 32) {
-        const int lane = tid;
-        const float my_v = lane < a.k ? sel_v[lane] : 0.f;
-        const float l0 = __shfl_sync(0xffffffffu, my_v, 0);
-        const float ex = lane < a.k ? expf(my_v - l0) : 0.f;
-        float sum = ex;
+    const float my_v = lane < a.k ? ls_key_logit(my_key) : 0.f;
+    const float l0 = __shfl_sync(0xffffffffu, my_v, 0);
+    const float ex = lane < a.k ? expf(my_v - l0) : 0.f;
+    float sum = ex;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if (lane < a.k) {
-            a.topk_ids[(size_t)t * a.k + lane] = sel_e[lane];
+    for (int o = 16; o > 0; o >>= 1)
+        sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane < a.k) {
+        if (ids_s)
+            ids_s[t * a.k + lane] = my_e;
+        if (owner) {
+            a.topk_ids[(size_t)t * a.k + lane] = my_e;
             a.topk_w[(size_t)t * a.k + lane] = ex / sum;
         }
     }
-    named_bar_sync(1, LS_ROUTE_THREADS);
 }
 
 // Token row t for the GEMMs, in the x16 K order (physical element 4q + c of
@@ -428,20 +481,23 @@ __device__ void ls_prep_token(const LayerArgs &a, int t, uint8_t *scratch)
 // CTA 0 has published the permutation; xs_s[t]: the x16 scales.
 template <int ROWS, bool F16>
 __device__ void ls_schedule(const LayerArgs &a, uint8_t *scratch, int *gcnt, int *gstart, int *tpre, int *sorted,
-                            int *xs_s)
+                            int *xs_s, bool local)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n = a.n, E = a.E, G = a.G;
-    int *sid = reinterpret_cast<int *>(scratch);
+    int *sid = reinterpret_cast<int *>(scratch);  // slot ids (local routing: already here)
     int *wtot = sid + ((n + 3) & ~3);     // [LS_WARPS][2] warp totals of the group scan
     int *wc = wtot + 2 * LS_WARPS;        // [LS_WARPS][E] per-warp running positions
     for (int g = tid; g < G; g += LS_THREADS)
         gcnt[g] = g < E ? 0 : a.T;
-    for (int s = tid; s < n; s += LS_THREADS)
-        sid[s] = __ldcg(a.topk_ids + s);
-    if (F16)
-        for (int t = tid; t < a.T; t += LS_THREADS)
-            xs_s[t] = __ldcg(a.xs + t);
+    if (!local) {
+        for (int s = tid; s < n; s += LS_THREADS)
+            sid[s] = __ldcg(a.topk_ids + s);
+        // (local routing: the loader fills xs_s once the token rows are ready)
+        if (F16)
+            for (int t = tid; t < a.T; t += LS_THREADS)
+                xs_s[t] = __ldcg(a.xs + t);
+    }
     __syncthreads();
     for (int s = tid; s < n; s += LS_THREADS)
         atomicAdd(&gcnt[sid[s]], 1);
@@ -673,22 +729,23 @@ __device__ __forceinline__ void ls_combine(const LayerArgs &a, int tt, int f, in
 
 // ------------------------------------------------------------------ one item's stages
 //
-// The compute warps' work on one item: every stage of the item, from the
-// ring.  Compute warp wg owns weight rows 16*wg .. 16*wg+15 of the 128-row
-// tile over the whole K.  acc[nt]: [0],[1] = row g, token columns 8nt+2q, +1;
-// [2],[3] = row g+8, same columns.  Returns false when a wait gave up.
-template <int WFMT, int NT, bool GU>
+// The compute warps' work on one item of tile class NTI: every stage of the
+// item, from the ring.  Compute warp wg owns weight rows 16*wg .. 16*wg+15 of
+// the 128-row tile over the whole K.  acc[nt]: [0],[1] = row g, token columns
+// 8nt+2q, +1; [2],[3] = row g+8, same columns.  Returns false when a wait gave
+// up.
+template <int WFMT, int NT, int NTI, bool GU>
 __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem &it, uint8_t *smem,
-                                               uint64_t *full, uint64_t *empty, const int2 *hdr, uint32_t &rc,
-                                               volatile int *abort_flag, float (&acc)[NT][4])
+                                               uint64_t *full, uint64_t *empty, uint32_t &rc,
+                                               volatile int *abort_flag, float (&acc)[NTI][4])
 {
     using C = LsCfg<WFMT, NT>;
     constexpr bool F16 = C::F16;
-    constexpr int ROWS = C::ROWS;
-    constexpr int CH = GU ? C::CH_GU : C::CH_DN;
+    constexpr int ROWS = 8 * NTI;
+    constexpr int CH = GU ? C::ch_gu(NTI) : C::ch_dn(NTI);
     constexpr int ROWB = ls_rowb(CH);
     constexpr int HS_OFF = (GU ? 1 : 2) * ROWS * ROWB;
-    constexpr int W_OFF = HS_OFF + (GU ? 0 : C::HSB_DN);
+    constexpr int W_OFF = HS_OFF + (GU ? 0 : C::hsb_dn(NTI));
     const int R = a.R;
     const int lane = threadIdx.x & 31, cw = (threadIdx.x >> 5) - 1;
     const int wg = cw, g = lane >> 2, q = lane & 3;
@@ -697,7 +754,7 @@ __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem 
     const int K = GU ? a.H : a.I;
     const int nt_used = (it.nvalid + 7) >> 3;  // 8-token tiles holding the item's tokens
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+    for (int nt = 0; nt < NTI; ++nt)
         acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
     for (int s = 0; s < nst; ++s, ++rc) {
         const int slot = rc % R;
@@ -709,7 +766,6 @@ __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem 
         const int sl0 = (s * 2 * CH) & ~3;
         // 64-wide half kh of chunk c; FULL: the whole chunk lies inside K
         auto half_chunk = [&](const int c, const int kh, auto full_tag) {
-            const int sh = 16 * kh;  // scale bytes of the half's two 32-wide blocks: 2kh, 2kh+1
             constexpr bool FULL = decltype(full_tag)::value;
             const uint8_t *wch = st + W_OFF + c * C::W_CHUNK;
             const int ks = 2 * c + kh;                 // 64-wide K slice inside the stage
@@ -721,16 +777,14 @@ __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem 
             const uint8_t *bk = brow + ks * 128;
             if (F16) {
                 // weights decode unscaled; each 32-wide block's partial sum takes the
-                // row's block scale 2^(e-127) in FP32 (bits max(e << 23, 0x400000))
+                // row's block scale 2^(e-127) in FP32 (a BF16 scale widened exactly)
                 const uint2 sc = *reinterpret_cast<const uint2 *>(wch + CHUNK_MX_CODE_BYTES + (wg * 8 + g) * 8);
                 const uint4 wv = *reinterpret_cast<const uint4 *>(wch + ((wg * 2 + kh) * 32 + lane) * 16);
                 const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
-                float sg[2], sg8[2];
-#pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    sg[b] = __int_as_float(max((int)(((sc.x >> (sh + 8 * b)) & 0xFFu) << 23), 0x00400000));
-                    sg8[b] = __int_as_float(max((int)(((sc.y >> (sh + 8 * b)) & 0xFFu) << 23), 0x00400000));
-                }
+                const uint32_t bx = kh ? ue8m0x2_bf16x2<1>(sc.x) : ue8m0x2_bf16x2<0>(sc.x);
+                const uint32_t by = kh ? ue8m0x2_bf16x2<1>(sc.y) : ue8m0x2_bf16x2<0>(sc.y);
+                const float sg[2] = {__uint_as_float(bx << 16), __uint_as_float(bx & 0xFFFF0000u)};
+                const float sg8[2] = {__uint_as_float(by << 16), __uint_as_float(by & 0xFFFF0000u)};
                 // the four A fragments of this half-chunk, decoded once for every token tile
                 uint32_t af[4][4];
 #pragma unroll
@@ -739,8 +793,8 @@ __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem 
                         decode_e2m1(words[jj], af[jj]);
                 const int *hs_st = reinterpret_cast<const int *>(st + HS_OFF) + (slice - sl0);
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    if (NT == 1 || nt < nt_used) {
+                for (int nt = 0; nt < NTI; ++nt) {
+                    if (NTI == 1 || nt < nt_used) {
                         const uint8_t *pb = bk + nt * 8 * ROWB;
                         float part[4];  // down: this slice's sum before the h block scale
 #pragma unroll
@@ -797,8 +851,8 @@ __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem 
                     const uint4 av = *reinterpret_cast<const uint4 *>(wch + ((wg * 8 + 4 * kh + jj) * 32 + lane) * 16);
                     const uint32_t af[4] = {av.x, av.y, av.z, av.w};
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        if (NT == 1 || nt < nt_used) {
+                    for (int nt = 0; nt < NTI; ++nt) {
+                        if (NTI == 1 || nt < nt_used) {
                             const uint8_t *pb = bk + nt * 8 * ROWB + jj * 32;
                             uint32_t b0, b1;
                             load_b(pb, b0, b1);
@@ -829,14 +883,149 @@ __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem 
         if (lane == 0)
             mbar_arrive(&empty[slot]);
     }
-    (void)hdr;
     return true;
+}
+
+// One item of tile class NTI on a compute warp: its stages, then the epilogue
+// (gate|up: SwiGLU and h; down: y).  Returns false when a wait gave up.
+template <int WFMT, int NT, int NTI>
+__device__ __forceinline__ bool ls_compute_item(const LayerArgs &a, const LsItem &it, uint8_t *smem, uint64_t *full,
+                                                uint64_t *empty, uint32_t &rc, volatile int *abort_flag,
+                                                const int *sorted, const int *xs_s, float *hmaxb, uint64_t *hmax_bar,
+                                                int gu_idx, int *grp_done)
+{
+    using C = LsCfg<WFMT, NT>;
+    constexpr bool F16 = C::F16;
+    const int lane = threadIdx.x & 31, wg = (threadIdx.x >> 5) - 1;
+    const int g = lane >> 2, q = lane & 3;
+    const bool gu = it.gu;
+    float acc[NTI][4];
+    const bool ok = gu ? ls_item_stages<WFMT, NT, NTI, true>(a, it, smem, full, empty, rc, abort_flag, acc)
+                       : ls_item_stages<WFMT, NT, NTI, false>(a, it, smem, full, empty, rc, abort_flag, acc);
+    if (!ok)
+        return false;
+
+    // ------------------------------------------------------ epilogue
+    // acc[nt]: [0],[1] = row g, tokens 8nt+2q, +1; [2],[3] = row g+8, same tokens.
+    if (gu) {
+        const int n = gu_row_feature(it.rt, 16 * wg + g);  // row g: gate, row g+8: up of feature n
+        float hv[NTI][2];
+#pragma unroll
+        for (int nt = 0; nt < NTI; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int tok = 8 * nt + 2 * q + e;
+                float gv = acc[nt][e], uv = acc[nt][2 + e];
+                if (F16) {  // undo the per-token scaling of x16
+                    const float fx = tok < it.nvalid ? pow2i(xs_s[ls_row_token(a, sorted, it, tok)]) : 0.f;
+                    gv *= fx;
+                    uv *= fx;
+                }
+                hv[nt][e] = (tok < it.nvalid && n < a.I) ? __fdividef(gv, 1.0f + __expf(-gv)) * uv : 0.f;
+            }
+        if (F16) {
+            // h leaves as FP16 hi + lo scaled by 2^-hs, hs per (position, 64-feature block):
+            // block maximum over the 8 features of each warp, then over the 8 warps
+            float *hm = hmaxb + (gu_idx & 1) * 8 * C::ROWS;
+#pragma unroll
+            for (int nt = 0; nt < NTI; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    float m = fabsf(hv[nt][e]);
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                    if (g == 0)
+                        hm[wg * C::ROWS + 8 * nt + 2 * q + e] = m;
+                }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(hmax_bar);
+            if (!mbar_wait_warp(hmax_bar, gu_idx & 1, abort_flag, a.err, lane))
+                return false;
+#pragma unroll
+            for (int nt = 0; nt < NTI; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int tok = 8 * nt + 2 * q + e;
+                    float m = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        m = fmaxf(m, hm[i * C::ROWS + tok]);
+                    const int mb = (int)((__float_as_uint(m) >> 23) & 0xFFu);
+                    int hsc = m > 0.f ? mb - 127 - 14 : 0;
+                    hsc = hsc < -100 ? -100 : (hsc > 100 ? 100 : hsc);
+                    if (tok < it.nvalid) {
+                        const float v = hv[nt][e] * pow2i(-hsc);
+                        const __half hb = __float2half_rn(v);
+                        const __half lb = __float2half_rn(v - __half2float(hb));
+                        if (n < a.I) {
+                            const size_t o =
+                                (size_t)(it.pos0 + tok) * a.I + (n & ~15) + x16_phys_k(n & 15);
+                            a.h[o] = __half_as_ushort(hb);
+                            a.h[o + a.h_plane] = __half_as_ushort(lb);
+                        }
+                        if (wg == 0 && g == 0)
+                            a.hs[(size_t)(it.pos0 + tok) * a.hs_pitch + it.rt] = hsc;
+                    }
+                }
+        } else {
+#pragma unroll
+            for (int nt = 0; nt < NTI; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int tok = 8 * nt + 2 * q + e;
+                    if (tok < it.nvalid && n < a.I) {
+                        const float v = hv[nt][e];
+                        const __nv_bfloat16 hb = __float2bfloat16_rn(v);
+                        const __nv_bfloat16 lb = __float2bfloat16_rn(v - __bfloat162float(hb));
+                        const size_t o = (size_t)(it.pos0 + tok) * a.I + (n & ~15) + x16_phys_k(n & 15);
+                        a.h[o] = __bfloat16_as_ushort(hb);
+                        a.h[o + a.h_plane] = __bfloat16_as_ushort(lb);
+                    }
+                }
+        }
+        // publish: this warp's part of the group's h is written (the fence makes
+        // the count a release)
+        __threadfence();
+        __syncwarp();
+        if (lane == 0)
+            atomicAdd(&grp_done[it.g], 1);
+    } else {
+        const int m = it.rt * TILE_ROWS + 16 * wg + g;
+#pragma unroll
+        for (int nt = 0; nt < NTI; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int tok = 8 * nt + 2 * q + e;
+                if (tok < it.nvalid) {
+                    float *yrow = a.y + (size_t)(it.pos0 + tok) * a.H;
+                    if (m < a.H)
+                        yrow[m] = acc[nt][e];
+                    if (m + 8 < a.H)
+                        yrow[m + 8] = acc[nt][2 + e];
+                }
+            }
+    }
+    return true;
+}
+
+// the wide tile classes out of line: they hold many accumulators and run only
+// for the few groups with more than 8 tokens
+template <int WFMT, int NT, int NTI>
+__device__ __noinline__ bool ls_compute_item_wide(const LayerArgs &a, const LsItem &it, uint8_t *smem, uint64_t *full,
+                                                  uint64_t *empty, uint32_t &rc, volatile int *abort_flag,
+                                                  const int *sorted, const int *xs_s, float *hmaxb,
+                                                  uint64_t *hmax_bar, int gu_idx, int *grp_done)
+{
+    return ls_compute_item<WFMT, NT, NTI>(a, it, smem, full, empty, rc, abort_flag, sorted, xs_s, hmaxb, hmax_bar,
+                                          gu_idx, grp_done);
 }
 
 // ------------------------------------------------------------------ the kernel
 
 template <int WFMT, int NT>
-__global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_kernel(const LayerArgs a)
+__global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_kernel(const __grid_constant__ LayerArgs a)
 {
     using C = LsCfg<WFMT, NT>;
     constexpr bool F16 = C::F16;
@@ -871,14 +1060,23 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
     }
 
     // ---------------------------------------------------------- phase 0a
-    int mine = 0;
-    for (int t = blockIdx.x; t < a.T; t += gridDim.x, ++mine) {
-        if (tid < LS_ROUTE_THREADS) {
-            if (a.E > 0)
-                ls_route_token(a, t, smem);
-        } else {
-            ls_prep_token<F16>(a, t, smem + LS_SCRATCH_PREP);
+    // local: this CTA routes every token (slot ids straight into the
+    // schedule's scratch); otherwise only its own tokens
+    const bool local = a.T <= LS_LOCAL_ROUTE_T;
+    const int mine = (int)blockIdx.x < a.T ? (a.T - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    if (tid < LS_ROUTE_THREADS) {
+        if (a.E > 0) {
+            if (local) {
+                for (int t = warp; t < a.T; t += LS_ROUTE_WARPS)
+                    ls_route_warp(a, t, lane, reinterpret_cast<int *>(smem), t % (int)gridDim.x == (int)blockIdx.x);
+            } else {
+                for (int i = warp; i < mine; i += LS_ROUTE_WARPS)
+                    ls_route_warp(a, (int)blockIdx.x + i * (int)gridDim.x, lane, nullptr, true);
+            }
         }
+    } else {
+        for (int t = blockIdx.x; t < a.T; t += gridDim.x)
+            ls_prep_token<F16>(a, t, smem + LS_SCRATCH_PREP);
     }
     fence_proxy_async_global();  // x16 is read by other CTAs' bulk copies
     __syncthreads();
@@ -887,14 +1085,14 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
             __threadfence();
             atomicAdd(&a.sync[SY_ROUTED], mine);
         }
-        misc[1] = wait_geq(&a.sync[SY_ROUTED], a.T, nullptr, a.err) ? 1 : 0;
+        misc[1] = local || wait_geq(&a.sync[SY_ROUTED], a.T, nullptr, a.err) ? 1 : 0;
     }
     __syncthreads();
     if (!misc[1])
         return;
 
     // ---------------------------------------------------------- phase 0b
-    ls_schedule<ROWS, F16>(a, smem, gcnt, gstart, tpre, sorted, xs_s);
+    ls_schedule<ROWS, F16>(a, smem, gcnt, gstart, tpre, sorted, xs_s, local);
     __syncthreads();
 
     const int rt_gu = a.gu_row_tiles, rt_dn = a.dn_row_tiles;
@@ -912,19 +1110,23 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
         // lane 0: completion count of the next item's group, read half-way through the
         // current item so that a down item rarely waits for the round trip
         int probe_g = -1, probe_v = 0;
+        // local routing: every CTA's token rows must be written before the first token copy
+        bool x_ready = !local;
         while (ok && u < total) {
             int nxt = 0;
             if (lane == 0)
                 nxt = (int)gridDim.x + atomicAdd(&a.sync[SY_WORK], 1);
             const LsItem it = ls_item<ROWS>(u, total_gu, rt_gu, rt_dn, a.G, gcnt, gstart, tpre);
-            const int CH = it.gu ? C::CH_GU : C::CH_DN;
+            const int nti = ls_nti<NT>(it.nvalid);  // the item's tile class: its stage geometry
+            const int irows = 8 * nti;
+            const int CH = it.gu ? C::ch_gu(nti) : C::ch_dn(nti);
             const int kch = it.gu ? a.gu_kchunks : a.dn_kchunks;
             const int nst = (kch + CH - 1) / CH;
             const int K = it.gu ? a.H : a.I;
             const int nb = it.gu ? 1 : 2;
             const int rowb = ls_rowb(CH);
-            const int hsb = it.gu ? 0 : C::HSB_DN;
-            const int w_off = nb * ROWS * rowb + hsb;
+            const int hsb = it.gu ? 0 : C::hsb_dn(nti);
+            const int w_off = nb * irows * rowb + hsb;
             const uint8_t *wsrc = (it.gu ? a.wgu + (size_t)it.g * a.gu_group_bytes
                                          : a.wdn + (size_t)it.g * a.dn_group_bytes) +
                                   (size_t)it.rt * kch * (size_t)a.chunk_bytes;
@@ -958,9 +1160,10 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
                 }
                 const uint32_t tbytes = (uint32_t)it.nvalid * (nb * vb + (uint32_t)nh * 4);
                 const bool wait_h = !it.gu && s == 0;
+                const bool wait_x = it.gu && s == 0 && !x_ready;
                 if (lane == 0) {
                     hdr[slot] = make_int2(u, s);
-                    if (wait_h)
+                    if (wait_h || wait_x)
                         mbar_expect_tx(&full[slot], wbytes);
                     else
                         mbar_arrive_expect_tx(&full[slot], wbytes + tbytes);
@@ -991,6 +1194,26 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
                     if (!(ok = __shfl_sync(0xffffffffu, hok, 0) != 0))
                         break;
                 }
+                if (wait_x) {
+                    // the token rows and scales of all tokens (written by their owner CTAs)
+                    int xok = 1;
+                    if (lane == 0) {
+                        xok = wait_geq(&a.sync[SY_ROUTED], a.T, abort_flag, a.err) ? 1 : 0;
+                        if (xok)
+                            fence_proxy_async_global();
+                    }
+                    __syncwarp();
+                    xok = __shfl_sync(0xffffffffu, xok, 0);
+                    if (F16 && xok && lane < a.T)
+                        xs_s[lane] = __ldcg(a.xs + lane);
+                    __syncwarp();
+                    // arrive in any case so that the weight copy can still complete the phase
+                    if (lane == 0)
+                        mbar_arrive_expect_tx(&full[slot], xok ? tbytes : 0u);
+                    x_ready = true;
+                    if (!(ok = xok != 0))
+                        break;
+                }
                 __syncwarp();
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
@@ -999,9 +1222,9 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
                         uint8_t *drow = st + r * rowb;
                         bulk_g2s(drow, src[i] + k0, vb, &full[slot]);
                         if (!it.gu) {
-                            bulk_g2s(drow + ROWS * rowb, src[i] + a.h_plane + k0, vb, &full[slot]);
+                            bulk_g2s(drow + irows * rowb, src[i] + a.h_plane + k0, vb, &full[slot]);
                             if (F16)
-                                bulk_g2s(st + nb * ROWS * rowb + r * LS_HS_ROW * 4,
+                                bulk_g2s(st + nb * irows * rowb + r * LS_HS_ROW * 4,
                                          a.hs + (size_t)pos_r[i] * a.hs_pitch + sl0, (uint32_t)nh * 4, &full[slot]);
                         }
                     }
@@ -1040,9 +1263,6 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
         __syncwarp();
     } else {
         // ------------------------------------------------------ compute warps
-        const int cw = warp - 1;
-        const int wg = cw;  // 16-row group of the 128-row tile
-        const int g = lane >> 2, q = lane & 3;
         uint32_t rc = 0;
         int gu_i = 0;
         bool ok = true;
@@ -1054,116 +1274,21 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
             if (h0.x < 0)
                 break;
             const LsItem it = ls_item<ROWS>(h0.x, total_gu, rt_gu, rt_dn, a.G, gcnt, gstart, tpre);
-            const bool gu = it.gu;
-            float acc[NT][4];
-            ok = gu ? ls_item_stages<WFMT, NT, true>(a, it, smem, full, empty, hdr, rc, abort_flag, acc)
-                    : ls_item_stages<WFMT, NT, false>(a, it, smem, full, empty, hdr, rc, abort_flag, acc);
+            const int gu_idx = it.gu ? gu_i++ : 0;
+            const int nti = ls_nti<NT>(it.nvalid);
+#define LS_ITEM(F_, NTI_) F_<WFMT, NT, NTI_>(a, it, smem, full, empty, rc, abort_flag, sorted, xs_s, hmaxb, hmax_bar, \
+                                            gu_idx, grp_done)
+            if (NT == 1 || nti == 1)
+                ok = LS_ITEM(ls_compute_item, 1);
+            else if (NT == 2 || nti == 2)
+                ok = LS_ITEM(ls_compute_item_wide, NT < 2 ? NT : 2);
+            else if (NT == 4 || nti == 4)
+                ok = LS_ITEM(ls_compute_item_wide, NT < 4 ? NT : 4);
+            else
+                ok = LS_ITEM(ls_compute_item_wide, NT);
+#undef LS_ITEM
             if (!ok)
                 break;
-            const int gu_idx = gu ? gu_i++ : 0;
-
-            // ------------------------------------------------------ epilogue
-            // acc[nt]: [0],[1] = row g, tokens 8nt+2q, +1; [2],[3] = row g+8, same tokens.
-            if (gu) {
-                const int n = gu_row_feature(it.rt, 16 * wg + g);  // row g: gate, row g+8: up of feature n
-                float hv[NT][2];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int tok = 8 * nt + 2 * q + e;
-                        float gv = acc[nt][e], uv = acc[nt][2 + e];
-                        if (F16) {  // undo the per-token scaling of x16
-                            const float fx = tok < it.nvalid ? pow2i(xs_s[ls_row_token(a, sorted, it, tok)]) : 0.f;
-                            gv *= fx;
-                            uv *= fx;
-                        }
-                        hv[nt][e] = (tok < it.nvalid && n < a.I) ? __fdividef(gv, 1.0f + __expf(-gv)) * uv : 0.f;
-                    }
-                if (F16) {
-                    // h leaves as FP16 hi + lo scaled by 2^-hs, hs per (position, 64-feature block):
-                    // block maximum over the 8 features of each warp, then over the 8 warps
-                    float *hm = hmaxb + (gu_idx & 1) * 8 * ROWS;
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            float m = fabsf(hv[nt][e]);
-                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-                            if (g == 0)
-                                hm[wg * ROWS + 8 * nt + 2 * q + e] = m;
-                        }
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(hmax_bar);
-                    if (!(ok = mbar_wait_warp(hmax_bar, gu_idx & 1, abort_flag, a.err, lane)))
-                        break;
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int tok = 8 * nt + 2 * q + e;
-                            float m = 0.f;
-#pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                m = fmaxf(m, hm[i * ROWS + tok]);
-                            const int mb = (int)((__float_as_uint(m) >> 23) & 0xFFu);
-                            int hsc = m > 0.f ? mb - 127 - 14 : 0;
-                            hsc = hsc < -100 ? -100 : (hsc > 100 ? 100 : hsc);
-                            if (tok < it.nvalid) {
-                                const float v = hv[nt][e] * pow2i(-hsc);
-                                const __half hb = __float2half_rn(v);
-                                const __half lb = __float2half_rn(v - __half2float(hb));
-                                if (n < a.I) {
-                                    const size_t o =
-                                        (size_t)(it.pos0 + tok) * a.I + (n & ~15) + x16_phys_k(n & 15);
-                                    a.h[o] = __half_as_ushort(hb);
-                                    a.h[o + a.h_plane] = __half_as_ushort(lb);
-                                }
-                                if (wg == 0 && g == 0)
-                                    a.hs[(size_t)(it.pos0 + tok) * a.hs_pitch + it.rt] = hsc;
-                            }
-                        }
-                } else {
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int tok = 8 * nt + 2 * q + e;
-                            if (tok < it.nvalid && n < a.I) {
-                                const float v = hv[nt][e];
-                                const __nv_bfloat16 hb = __float2bfloat16_rn(v);
-                                const __nv_bfloat16 lb = __float2bfloat16_rn(v - __bfloat162float(hb));
-                                const size_t o = (size_t)(it.pos0 + tok) * a.I + (n & ~15) + x16_phys_k(n & 15);
-                                a.h[o] = __bfloat16_as_ushort(hb);
-                                a.h[o + a.h_plane] = __bfloat16_as_ushort(lb);
-                            }
-                        }
-                }
-                // publish: this warp's part of the group's h is written (the fence makes
-                // the count a release)
-                __threadfence();
-                __syncwarp();
-                if (lane == 0)
-                    atomicAdd(&grp_done[it.g], 1);
-            } else {
-                const int m = it.rt * TILE_ROWS + 16 * wg + g;
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int tok = 8 * nt + 2 * q + e;
-                        if (tok < it.nvalid) {
-                            float *yrow = a.y + (size_t)(it.pos0 + tok) * a.H;
-                            if (m < a.H)
-                                yrow[m] = acc[nt][e];
-                            if (m + 8 < a.H)
-                                yrow[m + 8] = acc[nt][2 + e];
-                        }
-                    }
-            }
         }
         __threadfence();  // y and h of this warp, before the CTA reports that it is done
     }
