@@ -52,9 +52,12 @@ namespace {
 
 using namespace gemm;
 
-constexpr int LS_WARPS = 9;  // warp 0 streams, warps 1..8 compute (one 16-row group each)
+// warp 0 streams, warps 1..8 compute (one 16-row group each), warp 9 publishes
+// finished gate|up items to the other CTAs
+constexpr int LS_WARPS = 10;
 constexpr int LS_THREADS = LS_WARPS * 32;
 constexpr int LS_COMPUTE_WARPS = 8;
+constexpr int LS_PUB_R = 4;  // hand-off slots between the compute warps and the publisher
 // CTAs per SM.  Two CTAs (two independent streams, four compute warps per
 // sub-partition, 112 registers, half the ring each) measured slower than one
 // CTA with 168 registers for every token tile, so all tiles run one.
@@ -892,7 +895,7 @@ template <int WFMT, int NT, int NTI>
 __device__ __forceinline__ bool ls_compute_item(const LayerArgs &a, const LsItem &it, uint8_t *smem, uint64_t *full,
                                                 uint64_t *empty, uint32_t &rc, volatile int *abort_flag,
                                                 const int *sorted, const int *xs_s, float *hmaxb, uint64_t *hmax_bar,
-                                                int gu_idx, int *grp_done)
+                                                int gu_idx, uint64_t *pub_full, uint64_t *pub_empty, int *pub_g)
 {
     using C = LsCfg<WFMT, NT>;
     constexpr bool F16 = C::F16;
@@ -985,12 +988,16 @@ __device__ __forceinline__ bool ls_compute_item(const LayerArgs &a, const LsItem
                     }
                 }
         }
-        // publish: this warp's part of the group's h is written (the fence makes
-        // the count a release)
-        __threadfence();
-        __syncwarp();
-        if (lane == 0)
-            atomicAdd(&grp_done[it.g], 1);
+        // hand the item to the publisher warp, whose release at GPU scope covers
+        // this warp's h (ordered before it through the hand-off barrier)
+        const int ps = gu_idx % LS_PUB_R;
+        if (!mbar_wait_warp(&pub_empty[ps], ((gu_idx / LS_PUB_R) & 1) ^ 1, abort_flag, a.err, lane))
+            return false;
+        if (lane == 0) {
+            if (wg == 0)
+                pub_g[ps] = it.g;
+            mbar_arrive(&pub_full[ps]);
+        }
     } else {
         const int m = it.rt * TILE_ROWS + 16 * wg + g;
 #pragma unroll
@@ -1016,10 +1023,11 @@ template <int WFMT, int NT, int NTI>
 __device__ __noinline__ bool ls_compute_item_wide(const LayerArgs &a, const LsItem &it, uint8_t *smem, uint64_t *full,
                                                   uint64_t *empty, uint32_t &rc, volatile int *abort_flag,
                                                   const int *sorted, const int *xs_s, float *hmaxb,
-                                                  uint64_t *hmax_bar, int gu_idx, int *grp_done)
+                                                  uint64_t *hmax_bar, int gu_idx, uint64_t *pub_full,
+                                                  uint64_t *pub_empty, int *pub_g)
 {
     return ls_compute_item<WFMT, NT, NTI>(a, it, smem, full, empty, rc, abort_flag, sorted, xs_s, hmaxb, hmax_bar,
-                                          gu_idx, grp_done);
+                                          gu_idx, pub_full, pub_empty, pub_g);
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -1036,6 +1044,8 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
     int2 *hdr = reinterpret_cast<int2 *>(smem + L.hdr);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars), *empty = full + LS_R_MAX;
     uint64_t *hmax_bar = reinterpret_cast<uint64_t *>(smem + L.pbars);
+    uint64_t *pub_full = hmax_bar + 1, *pub_empty = pub_full + LS_PUB_R;  // publisher hand-off
+    int *pub_g = reinterpret_cast<int *>(smem + L.misc) + 4;
     int *misc = reinterpret_cast<int *>(smem + L.misc);
     volatile int *abort_flag = misc;
     float *hmaxb = reinterpret_cast<float *>(smem + L.hmax);
@@ -1052,6 +1062,10 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
             mbar_init(&empty[i], LS_COMPUTE_WARPS);
         }
         mbar_init(hmax_bar, LS_COMPUTE_WARPS);
+        for (int i = 0; i < LS_PUB_R; ++i) {
+            mbar_init(&pub_full[i], LS_COMPUTE_WARPS);
+            mbar_init(&pub_empty[i], 1);
+        }
         misc[0] = 0;
         for (int i = 0; i < (a.G + 31) / 32; ++i)
             gdone[i] = 0;
@@ -1261,7 +1275,7 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
                 if (armed & (1u << s))
                     mbar_drain(&full[s], (armed_par >> s) & 1);
         __syncwarp();
-    } else {
+    } else if (warp <= LS_COMPUTE_WARPS) {
         // ------------------------------------------------------ compute warps
         uint32_t rc = 0;
         int gu_i = 0;
@@ -1277,7 +1291,7 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
             const int gu_idx = it.gu ? gu_i++ : 0;
             const int nti = ls_nti<NT>(it.nvalid);
 #define LS_ITEM(F_, NTI_) F_<WFMT, NT, NTI_>(a, it, smem, full, empty, rc, abort_flag, sorted, xs_s, hmaxb, hmax_bar, \
-                                            gu_idx, grp_done)
+                                            gu_idx, pub_full, pub_empty, pub_g)
             if (NT == 1 || nti == 1)
                 ok = LS_ITEM(ls_compute_item, 1);
             else if (NT == 2 || nti == 2)
@@ -1290,13 +1304,41 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
             if (!ok)
                 break;
         }
-        __threadfence();  // y and h of this warp, before the CTA reports that it is done
+        if (ok) {
+            // terminal hand-off: no further item follows
+            const int ps = gu_i % LS_PUB_R;
+            if (mbar_wait_warp(&pub_empty[ps], ((gu_i / LS_PUB_R) & 1) ^ 1, abort_flag, a.err, lane) && lane == 0) {
+                if (warp == 1)
+                    pub_g[ps] = -1;
+                mbar_arrive(&pub_full[ps]);
+            }
+        }
+        __threadfence();  // y of this warp, before the CTA reports that it is done
+    } else {
+        // ------------------------------------------------------ publisher
+        // For each finished gate|up item, in order: once all compute warps have
+        // written their h, one release at GPU scope adds the item's warps to the
+        // group's count, so a compute warp never waits for its own writes.
+        for (int i = 0;; ++i) {
+            const int ps = i % LS_PUB_R;
+            if (!mbar_wait_sleep_warp(&pub_full[ps], (i / LS_PUB_R) & 1, abort_flag, a.err, lane))
+                break;
+            const int g = pub_g[ps];
+            if (g < 0)
+                break;
+            if (lane == 0) {
+                fence_acq_rel_gpu();
+                atomicAdd(&grp_done[g], LS_COMPUTE_WARPS);
+                mbar_arrive(&pub_empty[ps]);
+            }
+            __syncwarp();
+        }
     }
     __syncthreads();
 
     // ---------------------------------------------------------- combine
     // once every CTA has finished its items: warp w of CTA b combines the
-    // (token, 128-feature block)s w * gridDim.x + b, w * gridDim.x + b + 17 * gridDim.x, ...
+    // (token, 128-feature block)s w * gridDim.x + b, then every LS_WARPS * gridDim.x
     if (tid == 0) {
         red_release_add(&a.sync[SY_DONE], 1);
         bool okc = wait_geq(&a.sync[SY_DONE], (int)gridDim.x, abort_flag, a.err);
