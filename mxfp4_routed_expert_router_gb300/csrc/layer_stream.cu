@@ -64,7 +64,10 @@ constexpr int LS_PUB_R = 4;  // hand-off slots between the compute warps and the
 __host__ __device__ constexpr int ls_ctas_per_sm(int /*nt*/) { return 1; }
 __host__ __device__ constexpr int ls_smem_limit(int ctas) { return ctas == 1 ? 232448 : 114688; }
 __host__ __device__ constexpr int ls_stage_target(int ctas) { return ctas == 1 ? 52224 : 26624; }
-constexpr int LS_R_MAX = 8;
+constexpr int LS_R_MAX = 16;
+// stage target of the kernel for batches of at most two tokens (NT = 0): its
+// stages reserve two token rows, which leaves room for one more ring slot
+constexpr int LS_TINY_TARGET = 40960;
 constexpr int LS_HS_ROW = 16;  // ints of h block scales kept per token row and stage
 
 // ------------------------------------------------------------------ stage geometry
@@ -87,28 +90,37 @@ __host__ __device__ constexpr int ls_pick_ch(int nb, int rows, int hsb, int wchu
 }
 __host__ __device__ constexpr int ls_max(int a, int b) { return a > b ? a : b; }
 
-// Items hold up to 8 * NT tokens (NT = the kernel's token tiles).  An item of
-// c tokens runs the code and stage geometry of its own tile class NTI (the
-// smallest power of two with 8 * NTI >= c): a token operand of 8 * NTI rows
-// and as many weight chunks per stage as then fit the stage target.
+// Items hold up to 8 * NT tokens (NT = the kernel's token tiles; NT = 0 is the
+// kernel for batches of at most two tokens, with one tile).  An item of c
+// tokens runs the code and stage geometry of its own tile class NTI (the
+// smallest power of two with 8 * NTI >= c): a token operand of res_rows(NTI)
+// reserved rows (8 * NTI; two in the NT = 0 kernel, whose MMAs read the other
+// six rows of their 8-token tile from the bytes that follow, in the same
+// stage, and discard those columns) and as many weight chunks per stage as
+// then fit the stage target.
 template <int WFMT, int NT>
 struct LsCfg {
     static constexpr bool F16 = WFMT == FMT_MXFP4;
     static constexpr int W_CHUNK = F16 ? CHUNK_MX_BYTES : CHUNK_BF16_BYTES;
-    static constexpr int ROWS = 8 * NT;  // token rows of the largest item
+    static constexpr int NTK = NT == 0 ? 1 : NT;  // token tiles of the largest item
+    static constexpr int ROWS = 8 * NTK;          // token rows of the largest item
     static constexpr int CTAS = ls_ctas_per_sm(NT);
     static constexpr int SMEM_LIMIT = ls_smem_limit(CTAS);
-    static constexpr int TARGET = ls_stage_target(CTAS);
-    __host__ __device__ static constexpr int hsb_dn(int nti) { return F16 ? 8 * nti * LS_HS_ROW * 4 : 0; }
-    __host__ __device__ static constexpr int ch_gu(int nti) { return ls_pick_ch(1, 8 * nti, 0, W_CHUNK, TARGET); }
+    static constexpr int TARGET = NT == 0 ? LS_TINY_TARGET : ls_stage_target(CTAS);
+    __host__ __device__ static constexpr int res_rows(int nti) { return NT == 0 ? 2 : 8 * nti; }
+    __host__ __device__ static constexpr int hsb_dn(int nti) { return F16 ? res_rows(nti) * LS_HS_ROW * 4 : 0; }
+    __host__ __device__ static constexpr int ch_gu(int nti)
+    {
+        return ls_pick_ch(1, res_rows(nti), 0, W_CHUNK, TARGET);
+    }
     __host__ __device__ static constexpr int ch_dn(int nti)
     {
-        return ls_pick_ch(2, 8 * nti, hsb_dn(nti), W_CHUNK, TARGET);
+        return ls_pick_ch(2, res_rows(nti), hsb_dn(nti), W_CHUNK, TARGET);
     }
     __host__ __device__ static constexpr int stage_of(int nti)
     {
-        return ls_max(ls_stage_bytes(1, 8 * nti, 0, ch_gu(nti), W_CHUNK),
-                      ls_stage_bytes(2, 8 * nti, hsb_dn(nti), ch_dn(nti), W_CHUNK));
+        return ls_max(ls_stage_bytes(1, res_rows(nti), 0, ch_gu(nti), W_CHUNK),
+                      ls_stage_bytes(2, res_rows(nti), hsb_dn(nti), ch_dn(nti), W_CHUNK));
     }
     static constexpr int STAGE = (ls_max(ls_max(stage_of(1), NT >= 2 ? stage_of(2) : 0),
                                          ls_max(NT >= 4 ? stage_of(4) : 0, NT >= 8 ? stage_of(8) : 0)) +
@@ -121,6 +133,8 @@ struct LsCfg {
 template <int NT>
 __device__ __forceinline__ int ls_nti(int c)
 {
+    if (NT <= 1)
+        return 1;
     const int t = (c + 7) >> 3;
     return t <= 1 ? 1 : t <= 2 ? (NT < 2 ? NT : 2) : t <= 4 ? (NT < 4 ? NT : 4) : NT;
 }
@@ -744,10 +758,10 @@ __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem 
 {
     using C = LsCfg<WFMT, NT>;
     constexpr bool F16 = C::F16;
-    constexpr int ROWS = 8 * NTI;
+    constexpr int RES = C::res_rows(NTI);  // token rows reserved in the stage (per plane)
     constexpr int CH = GU ? C::ch_gu(NTI) : C::ch_dn(NTI);
     constexpr int ROWB = ls_rowb(CH);
-    constexpr int HS_OFF = (GU ? 1 : 2) * ROWS * ROWB;
+    constexpr int HS_OFF = (GU ? 1 : 2) * RES * ROWB;
     constexpr int W_OFF = HS_OFF + (GU ? 0 : C::hsb_dn(NTI));
     const int R = a.R;
     const int lane = threadIdx.x & 31, cw = (threadIdx.x >> 5) - 1;
@@ -810,9 +824,9 @@ __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem 
                                 load_b(pb + (2 * b + 1) * 32, b0, b1);
                                 mma_f16(t, af[2 * b + 1], b0, b1);
                                 if (!GU) {
-                                    load_b(pb + ROWS * ROWB + (2 * b) * 32, b0, b1);
+                                    load_b(pb + RES * ROWB + (2 * b) * 32, b0, b1);
                                     mma_f16(t, af[2 * b], b0, b1);
-                                    load_b(pb + ROWS * ROWB + (2 * b + 1) * 32, b0, b1);
+                                    load_b(pb + RES * ROWB + (2 * b + 1) * 32, b0, b1);
                                     mma_f16(t, af[2 * b + 1], b0, b1);
                                 }
                                 if (GU) {
@@ -861,7 +875,7 @@ __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem 
                             load_b(pb, b0, b1);
                             mma_bf16(acc[nt], af, b0, b1);
                             if (!GU) {
-                                load_b(pb + ROWS * ROWB, b0, b1);
+                                load_b(pb + RES * ROWB, b0, b1);
                                 mma_bf16(acc[nt], af, b0, b1);
                             }
                         }
@@ -1132,7 +1146,7 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
                 nxt = (int)gridDim.x + atomicAdd(&a.sync[SY_WORK], 1);
             const LsItem it = ls_item<ROWS>(u, total_gu, rt_gu, rt_dn, a.G, gcnt, gstart, tpre);
             const int nti = ls_nti<NT>(it.nvalid);  // the item's tile class: its stage geometry
-            const int irows = 8 * nti;
+            const int irows = C::res_rows(nti);
             const int CH = it.gu ? C::ch_gu(nti) : C::ch_dn(nti);
             const int kch = it.gu ? a.gu_kchunks : a.dn_kchunks;
             const int nst = (kch + CH - 1) / CH;
@@ -1292,14 +1306,14 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
             const int nti = ls_nti<NT>(it.nvalid);
 #define LS_ITEM(F_, NTI_) F_<WFMT, NT, NTI_>(a, it, smem, full, empty, rc, abort_flag, sorted, xs_s, hmaxb, hmax_bar, \
                                             gu_idx, pub_full, pub_empty, pub_g)
-            if (NT == 1 || nti == 1)
+            if (NT <= 1 || nti == 1)
                 ok = LS_ITEM(ls_compute_item, 1);
             else if (NT == 2 || nti == 2)
-                ok = LS_ITEM(ls_compute_item_wide, NT < 2 ? NT : 2);
+                ok = LS_ITEM(ls_compute_item_wide, NT < 2 ? 1 : 2);
             else if (NT == 4 || nti == 4)
-                ok = LS_ITEM(ls_compute_item_wide, NT < 4 ? NT : 4);
+                ok = LS_ITEM(ls_compute_item_wide, NT < 4 ? 1 : 4);
             else
-                ok = LS_ITEM(ls_compute_item_wide, NT);
+                ok = LS_ITEM(ls_compute_item_wide, NT < 8 ? 1 : 8);
 #undef LS_ITEM
             if (!ok)
                 break;
@@ -1406,13 +1420,14 @@ cudaError_t ls_launch(LayerArgs a, cudaStream_t st)
 int ls_nt(int T)
 {
     const int t = T < STREAM_MAX_T ? T : STREAM_MAX_T;
-    return t <= 8 ? 1 : t <= 16 ? 2 : t <= 32 ? 4 : 8;
+    return t <= 2 ? 0 : t <= 8 ? 1 : t <= 16 ? 2 : t <= 32 ? 4 : 8;
 }
 
 template <int WFMT>
 int ls_depth_fmt(int nt, int G, int n, int E, int T)
 {
     switch (nt) {
+    case 0: return ls_ring_depth<WFMT, 0>(G, n, E, T);
     case 1: return ls_ring_depth<WFMT, 1>(G, n, E, T);
     case 2: return ls_ring_depth<WFMT, 2>(G, n, E, T);
     case 4: return ls_ring_depth<WFMT, 4>(G, n, E, T);
@@ -1424,6 +1439,7 @@ template <int WFMT>
 cudaError_t ls_launch_fmt(int nt, const LayerArgs &a, cudaStream_t st)
 {
     switch (nt) {
+    case 0: return ls_launch<WFMT, 0>(a, st);
     case 1: return ls_launch<WFMT, 1>(a, st);
     case 2: return ls_launch<WFMT, 2>(a, st);
     case 4: return ls_launch<WFMT, 4>(a, st);

@@ -68,6 +68,8 @@ SMALL = [
     wl.custom("stream_ragged_T3_H288_I160_E16_S1_k4", 3, 288, 160, 16, 1, 4, seed=31),
     # streaming path, largest token tile (64 tokens per group tile)
     wl.custom("stream_T60_H256_I128_E64_S1_k4", 60, 256, 128, 64, 1, 4, seed=32),
+    # streaming path, batch of two tokens (two reserved token rows per stage), ragged K
+    wl.custom("stream_T2_H416_I224_E8_S1_k3", 2, 416, 224, 8, 1, 3, seed=36),
     # streaming path, items of every tile class: groups of 9-16 and 17-32 tokens
     wl.custom("stream_classes_T40_H256_I192_E16_S1_k4", 40, 256, 192, 16, 1, 4, seed=33),
     wl.custom("stream_classes_T21_H320_I128_E4_S1_k3", 21, 320, 128, 4, 1, 3, seed=35),
