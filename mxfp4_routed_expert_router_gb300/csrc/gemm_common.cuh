@@ -26,6 +26,7 @@ struct GemmArgs {
     long long h_plane;
     float *y_out;
     int *err;
+    int brows;  // token rows per TMA box of the B operand (16, or 64 when every B tensor has that many rows)
 };
 
 // ------------------------------------------------------------------ PTX helpers

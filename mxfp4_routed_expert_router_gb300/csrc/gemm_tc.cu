@@ -49,8 +49,9 @@ constexpr int N_EPI_WARPS = 8;  // two per TMEM lane quadrant, splitting the col
 constexpr int NUM_THREADS = (2 + N_DEC_WARPS + N_EPI_WARPS) * 32;
 constexpr int WARP_BLOAD = 0, WARP_MMA = 1, WARP_DEC0 = 2, WARP_EPI0 = WARP_DEC0 + N_DEC_WARPS;
 constexpr int A_STAGE_BYTES = TILE_ROWS * HALF_K * 2;  // 16 KB: 128 rows x 64 BF16
-constexpr int B_BOX_ROWS = 16;
-constexpr int B_BOX_BYTES = B_BOX_ROWS * HALF_K * 2;   // 2 KB
+// B operand TMA boxes: 64 token rows (8 KB) each, so that a stage takes few
+// TMA issues; 16 rows when a B tensor has fewer than 64 rows
+constexpr int B_BOX_ROWS_BIG = 64, B_BOX_ROWS_SMALL = 16;
 
 using TcArgs = GemmArgs;
 
@@ -239,8 +240,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             } else {
                 row0 = a.grp_start[w.g] + w.tok0;
             }
-            const int nbox = w.n_mma / B_BOX_ROWS;
-            const uint32_t bytes = (uint32_t)(nbox * B_BOX_BYTES * NB);
+            // whole boxes of brows rows (past the tile's tokens: rows the MMAs do not
+            // read, or zero fill past the tensor's last row)
+            const int nbox = (w.n_mma + a.brows - 1) / a.brows;
+            const int box_bytes = a.brows * HALF_K * 2;
+            const uint32_t bytes = (uint32_t)(nbox * box_bytes * NB);
             for (int st = 0; st < nstages; ++st, ++sc) {
                 const int slot = sc % S;
                 const uint32_t ph = (sc / S) & 1;
@@ -250,10 +254,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     mbar_arrive_expect_tx(&ab_full[slot], bytes);
                     uint8_t *bdst = smem + slot * L::STAGE + L::A_STAGE;
                     for (int b = 0; b < nbox; ++b) {
-                        tma_2d(bdst + b * B_BOX_BYTES, m0, st * HALF_K, row0 + b * B_BOX_ROWS, &ab_full[slot]);
+                        tma_2d(bdst + b * box_bytes, m0, st * HALF_K, row0 + b * a.brows, &ab_full[slot]);
                         if (!GU)
-                            tma_2d(bdst + NMAX * HALF_K * 2 + b * B_BOX_BYTES, &map_b2, st * HALF_K,
-                                   row0 + b * B_BOX_ROWS, &ab_full[slot]);
+                            tma_2d(bdst + NMAX * HALF_K * 2 + b * box_bytes, &map_b2, st * HALF_K,
+                                   row0 + b * a.brows, &ab_full[slot]);
                     }
                 }
                 armed |= 1u << slot;
@@ -604,12 +608,14 @@ cudaError_t launch_gemm_gate_up_tc(const Plan &p, const WeightStore &w, int fmt,
 {
     TcArgs a{w.base, w.group_bytes, w.kchunks, w.chunk_bytes, w.row_tiles, p.grp_start, p.grp_count, p.E, p.G,
              p.I, p.H, p.h, (long long)p.P * p.I, nullptr, p.err};
+    a.brows = p.T >= B_BOX_ROWS_BIG && (p.T * p.k == 0 || p.T * p.k >= B_BOX_ROWS_BIG) ? B_BOX_ROWS_BIG
+                                                                                       : B_BOX_ROWS_SMALL;
     CUtensorMap m1, m2;
-    cudaError_t e = make_map(&m2, x, p.T, p.H, B_BOX_ROWS);
+    cudaError_t e = make_map(&m2, x, p.T, p.H, a.brows);
     if (e != cudaSuccess)
         return e;
     if (p.T * p.k > 0) {
-        if ((e = make_map(&m1, p.x_perm, (long long)p.T * p.k, p.H, B_BOX_ROWS)) != cudaSuccess)
+        if ((e = make_map(&m1, p.x_perm, (long long)p.T * p.k, p.H, a.brows)) != cudaSuccess)
             return e;
     } else {
         m1 = m2;
@@ -621,11 +627,12 @@ cudaError_t launch_gemm_down_tc(const Plan &p, const WeightStore &w, int fmt, cu
 {
     TcArgs a{w.base, w.group_bytes, w.kchunks, w.chunk_bytes, w.row_tiles, p.grp_start, p.grp_count, p.E, p.G,
              p.I, p.H, nullptr, 0, p.y, p.err};
+    a.brows = p.P >= B_BOX_ROWS_BIG ? B_BOX_ROWS_BIG : B_BOX_ROWS_SMALL;
     CUtensorMap m1, m2;
-    cudaError_t e = make_map(&m1, p.h, p.P, p.I, B_BOX_ROWS);
+    cudaError_t e = make_map(&m1, p.h, p.P, p.I, a.brows);
     if (e != cudaSuccess)
         return e;
-    if ((e = make_map(&m2, p.h + (size_t)p.P * p.I, p.P, p.I, B_BOX_ROWS)) != cudaSuccess)
+    if ((e = make_map(&m2, p.h + (size_t)p.P * p.I, p.P, p.I, a.brows)) != cudaSuccess)
         return e;
     return launch_any<false>(a, fmt, p.T, m1, m2, st);
 }
