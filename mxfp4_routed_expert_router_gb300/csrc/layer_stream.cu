@@ -293,13 +293,6 @@ __device__ __forceinline__ int ld_acquire(const int *p)
     return v;
 }
 
-__device__ __forceinline__ int ld_relaxed(const int *p)
-{
-    int v;
-    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 __device__ __forceinline__ void st_release(int *p, int v)
@@ -1135,9 +1128,6 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
         fence_proxy_async_global();  // x16 of other CTAs, acquired above, is read by bulk copies
         // first item: blockIdx.x; the shared counter hands out the rest from gridDim.x on
         int u = blockIdx.x;
-        // lane 0: completion count of the next item's group, read half-way through the
-        // current item so that a down item rarely waits for the round trip
-        int probe_g = -1, probe_v = 0;
         // local routing: every CTA's token rows must be written before the first token copy
         bool x_ready = !local;
         while (ok && u < total) {
@@ -1207,10 +1197,7 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
                         if (!(gdone[it.g >> 5] & bit)) {
                             const int ntl = tpre[it.g + 1] - tpre[it.g];
                             const int target = ntl * rt_gu * 8;
-                            if (probe_g == it.g && probe_v >= target)
-                                fence_acq_rel_gpu();
-                            else
-                                hok = wait_geq(&grp_done[it.g], target, abort_flag, a.err) ? 1 : 0;
+                            hok = wait_geq(&grp_done[it.g], target, abort_flag, a.err) ? 1 : 0;
                             if (hok)
                                 gdone[it.g >> 5] |= bit;
                         }
@@ -1254,16 +1241,6 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
                             if (F16)
                                 bulk_g2s(st + nb * irows * rowb + r * LS_HS_ROW * 4,
                                          a.hs + (size_t)pos_r[i] * a.hs_pitch + sl0, (uint32_t)nh * 4, &full[slot]);
-                        }
-                    }
-                }
-                if (s == nst / 2 && lane == 0) {
-                    probe_g = -1;
-                    if (nxt < total) {
-                        const LsItem nx = ls_item<ROWS>(nxt, total_gu, rt_gu, rt_dn, a.G, gcnt, gstart, tpre);
-                        if (!nx.gu && !(gdone[nx.g >> 5] & (1u << (nx.g & 31)))) {
-                            probe_g = nx.g;
-                            probe_v = ld_relaxed(&grp_done[nx.g]);
                         }
                     }
                 }
