@@ -108,6 +108,7 @@ struct LsCfg {
     static constexpr int SMEM_LIMIT = ls_smem_limit(CTAS);
     static constexpr int TARGET = NT == 0 ? LS_TINY_TARGET : ls_stage_target(CTAS);
     __host__ __device__ static constexpr int res_rows(int nti) { return NT == 0 ? 2 : 8 * nti; }
+    static constexpr bool PACK_H = NT == 0 && F16;  // down items: h hi/lo of a token in adjacent rows
     __host__ __device__ static constexpr int hsb_dn(int nti) { return F16 ? res_rows(nti) * LS_HS_ROW * 4 : 0; }
     __host__ __device__ static constexpr int ch_gu(int nti)
     {
@@ -752,6 +753,9 @@ __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem 
     using C = LsCfg<WFMT, NT>;
     constexpr bool F16 = C::F16;
     constexpr int RES = C::res_rows(NTI);  // token rows reserved in the stage (per plane)
+    // down GEMM of the smallest batches: the hi and lo planes of token r sit in rows
+    // 2r and 2r+1 of one 8-column MMA tile, so one MMA per K step yields both
+    constexpr bool PACK = C::PACK_H && !GU;
     constexpr int CH = GU ? C::ch_gu(NTI) : C::ch_dn(NTI);
     constexpr int ROWB = ls_rowb(CH);
     constexpr int HS_OFF = (GU ? 1 : 2) * RES * ROWB;
@@ -816,7 +820,7 @@ __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem 
                                 mma_f16_z(t, af[2 * b], b0, b1);
                                 load_b(pb + (2 * b + 1) * 32, b0, b1);
                                 mma_f16(t, af[2 * b + 1], b0, b1);
-                                if (!GU) {
+                                if (!GU && !PACK) {
                                     load_b(pb + RES * ROWB + (2 * b) * 32, b0, b1);
                                     mma_f16(t, af[2 * b], b0, b1);
                                     load_b(pb + RES * ROWB + (2 * b + 1) * 32, b0, b1);
@@ -842,10 +846,13 @@ __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem 
                         }
                         if (!GU) {
                             // fold in the scale of this 64-feature block of h for each token
-                            // column (columns past the item's tokens hold stale data, discarded)
+                            // column (columns past the item's tokens hold stale data, discarded);
+                            // packed: columns 2q and 2q+1 are token q's hi and lo planes
                             const int r0 = 8 * nt + 2 * q;
-                            const float f0 = r0 < it.nvalid ? pow2i(hs_st[r0 * LS_HS_ROW]) : 0.f;
-                            const float f1 = r0 + 1 < it.nvalid ? pow2i(hs_st[(r0 + 1) * LS_HS_ROW]) : 0.f;
+                            const float f0 = PACK ? (q < it.nvalid ? pow2i(hs_st[q * LS_HS_ROW]) : 0.f)
+                                                  : (r0 < it.nvalid ? pow2i(hs_st[r0 * LS_HS_ROW]) : 0.f);
+                            const float f1 = PACK ? f0
+                                                  : (r0 + 1 < it.nvalid ? pow2i(hs_st[(r0 + 1) * LS_HS_ROW]) : 0.f);
                             acc[nt][0] = fmaf(part[0], f0, acc[nt][0]);
                             acc[nt][1] = fmaf(part[1], f1, acc[nt][1]);
                             acc[nt][2] = fmaf(part[2], f0, acc[nt][2]);
@@ -1007,19 +1014,30 @@ __device__ __forceinline__ bool ls_compute_item(const LayerArgs &a, const LsItem
         }
     } else {
         const int m = it.rt * TILE_ROWS + 16 * wg + g;
-#pragma unroll
-        for (int nt = 0; nt < NTI; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int tok = 8 * nt + 2 * q + e;
-                if (tok < it.nvalid) {
-                    float *yrow = a.y + (size_t)(it.pos0 + tok) * a.H;
-                    if (m < a.H)
-                        yrow[m] = acc[nt][e];
-                    if (m + 8 < a.H)
-                        yrow[m + 8] = acc[nt][2 + e];
-                }
+        if (C::PACK_H) {
+            // token q: its hi column 2q plus its lo column 2q+1
+            if (q < it.nvalid) {
+                float *yrow = a.y + (size_t)(it.pos0 + q) * a.H;
+                if (m < a.H)
+                    yrow[m] = acc[0][0] + acc[0][1];
+                if (m + 8 < a.H)
+                    yrow[m + 8] = acc[0][2] + acc[0][3];
             }
+        } else {
+#pragma unroll
+            for (int nt = 0; nt < NTI; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int tok = 8 * nt + 2 * q + e;
+                    if (tok < it.nvalid) {
+                        float *yrow = a.y + (size_t)(it.pos0 + tok) * a.H;
+                        if (m < a.H)
+                            yrow[m] = acc[nt][e];
+                        if (m + 8 < a.H)
+                            yrow[m + 8] = acc[nt][2 + e];
+                    }
+                }
+        }
     }
     return true;
 }
@@ -1234,10 +1252,12 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
                 for (int i = 0; i < 2; ++i) {
                     const int r = lane + 32 * i;
                     if (r < it.nvalid) {
-                        uint8_t *drow = st + r * rowb;
+                        // down items of the smallest batches: hi and lo of row r in rows 2r, 2r+1
+                        const bool pack = C::PACK_H && !it.gu;
+                        uint8_t *drow = st + (pack ? 2 * r : r) * rowb;
                         bulk_g2s(drow, src[i] + k0, vb, &full[slot]);
                         if (!it.gu) {
-                            bulk_g2s(drow + irows * rowb, src[i] + a.h_plane + k0, vb, &full[slot]);
+                            bulk_g2s(pack ? drow + rowb : drow + irows * rowb, src[i] + a.h_plane + k0, vb, &full[slot]);
                             if (F16)
                                 bulk_g2s(st + nb * irows * rowb + r * LS_HS_ROW * 4,
                                          a.hs + (size_t)pos_r[i] * a.hs_pitch + sl0, (uint32_t)nh * 4, &full[slot]);
