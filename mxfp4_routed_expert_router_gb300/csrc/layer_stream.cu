@@ -108,7 +108,6 @@ struct LsCfg {
     static constexpr int SMEM_LIMIT = ls_smem_limit(CTAS);
     static constexpr int TARGET = NT == 0 ? LS_TINY_TARGET : ls_stage_target(CTAS);
     __host__ __device__ static constexpr int res_rows(int nti) { return NT == 0 ? 2 : 8 * nti; }
-    static constexpr bool PACK_H = NT == 0 && F16;  // down items: h hi/lo of a token in adjacent rows
     __host__ __device__ static constexpr int hsb_dn(int nti) { return F16 ? res_rows(nti) * LS_HS_ROW * 4 : 0; }
     __host__ __device__ static constexpr int ch_gu(int nti)
     {
@@ -674,6 +673,16 @@ __device__ __forceinline__ LsItem ls_item(int u, int total_gu, int rt_gu, int rt
     return it;
 }
 
+// in the kernels for up to 16 tokens, a down item of at most four tokens
+// (MXFP4) packs each token's h hi and lo planes into adjacent columns of its
+// 8-token MMA tile (the wider kernels keep one code path for class 1: the
+// second one cost them registers and measured slower)
+template <int WFMT, int NT>
+__device__ __forceinline__ bool ls_packed(const LsItem &it)
+{
+    return WFMT == FMT_MXFP4 && NT <= 2 && !it.gu && it.nvalid <= 4;
+}
+
 // token of row r of an item: routed positions look it up (tokp: token of each
 // routed position); a shared group or dense slice holds every token in order
 __device__ __forceinline__ int ls_row_token(const LayerArgs &a, const int *tokp, const LsItem &it, int r)
@@ -745,7 +754,7 @@ __device__ __forceinline__ void ls_combine(const LayerArgs &a, int tt, int f, in
 // the 128-row tile over the whole K.  acc[nt]: [0],[1] = row g, token columns
 // 8nt+2q, +1; [2],[3] = row g+8, same columns.  Returns false when a wait gave
 // up.
-template <int WFMT, int NT, int NTI, bool GU>
+template <int WFMT, int NT, int NTI, bool GU, bool PK>
 __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem &it, uint8_t *smem,
                                                uint64_t *full, uint64_t *empty, uint32_t &rc,
                                                volatile int *abort_flag, float (&acc)[NTI][4])
@@ -753,9 +762,9 @@ __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem 
     using C = LsCfg<WFMT, NT>;
     constexpr bool F16 = C::F16;
     constexpr int RES = C::res_rows(NTI);  // token rows reserved in the stage (per plane)
-    // down GEMM of the smallest batches: the hi and lo planes of token r sit in rows
-    // 2r and 2r+1 of one 8-column MMA tile, so one MMA per K step yields both
-    constexpr bool PACK = C::PACK_H && !GU;
+    // down items of at most four tokens (PK): the hi and lo planes of token r sit in
+    // rows 2r and 2r+1 of one 8-column MMA tile, so one MMA per K step yields both
+    constexpr bool PACK = PK && !GU && F16;
     constexpr int CH = GU ? C::ch_gu(NTI) : C::ch_dn(NTI);
     constexpr int ROWB = ls_rowb(CH);
     constexpr int HS_OFF = (GU ? 1 : 2) * RES * ROWB;
@@ -905,7 +914,7 @@ __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem 
 
 // One item of tile class NTI on a compute warp: its stages, then the epilogue
 // (gate|up: SwiGLU and h; down: y).  Returns false when a wait gave up.
-template <int WFMT, int NT, int NTI>
+template <int WFMT, int NT, int NTI, bool PK = false>
 __device__ __forceinline__ bool ls_compute_item(const LayerArgs &a, const LsItem &it, uint8_t *smem, uint64_t *full,
                                                 uint64_t *empty, uint32_t &rc, volatile int *abort_flag,
                                                 const int *sorted, const int *xs_s, float *hmaxb, uint64_t *hmax_bar,
@@ -917,8 +926,8 @@ __device__ __forceinline__ bool ls_compute_item(const LayerArgs &a, const LsItem
     const int g = lane >> 2, q = lane & 3;
     const bool gu = it.gu;
     float acc[NTI][4];
-    const bool ok = gu ? ls_item_stages<WFMT, NT, NTI, true>(a, it, smem, full, empty, rc, abort_flag, acc)
-                       : ls_item_stages<WFMT, NT, NTI, false>(a, it, smem, full, empty, rc, abort_flag, acc);
+    const bool ok = gu ? ls_item_stages<WFMT, NT, NTI, true, PK>(a, it, smem, full, empty, rc, abort_flag, acc)
+                       : ls_item_stages<WFMT, NT, NTI, false, PK>(a, it, smem, full, empty, rc, abort_flag, acc);
     if (!ok)
         return false;
 
@@ -1014,7 +1023,7 @@ __device__ __forceinline__ bool ls_compute_item(const LayerArgs &a, const LsItem
         }
     } else {
         const int m = it.rt * TILE_ROWS + 16 * wg + g;
-        if (C::PACK_H) {
+        if (PK && F16) {
             // token q: its hi column 2q plus its lo column 2q+1
             if (q < it.nvalid) {
                 float *yrow = a.y + (size_t)(it.pos0 + q) * a.H;
@@ -1253,7 +1262,7 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
                     const int r = lane + 32 * i;
                     if (r < it.nvalid) {
                         // down items of the smallest batches: hi and lo of row r in rows 2r, 2r+1
-                        const bool pack = C::PACK_H && !it.gu;
+                        const bool pack = ls_packed<WFMT, NT>(it);
                         uint8_t *drow = st + (pack ? 2 * r : r) * rowb;
                         bulk_g2s(drow, src[i] + k0, vb, &full[slot]);
                         if (!it.gu) {
@@ -1301,11 +1310,21 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
             const LsItem it = ls_item<ROWS>(h0.x, total_gu, rt_gu, rt_dn, a.G, gcnt, gstart, tpre);
             const int gu_idx = it.gu ? gu_i++ : 0;
             const int nti = ls_nti<NT>(it.nvalid);
-#define LS_ITEM(F_, NTI_) F_<WFMT, NT, NTI_>(a, it, smem, full, empty, rc, abort_flag, sorted, xs_s, hmaxb, hmax_bar, \
-                                            gu_idx, pub_full, pub_empty, pub_g)
-            if (NT <= 1 || nti == 1)
-                ok = LS_ITEM(ls_compute_item, 1);
-            else if (NT == 2 || nti == 2)
+#define LS_ITEM(F_, ...)                                                                                      \
+    F_<WFMT, NT, __VA_ARGS__>(a, it, smem, full, empty, rc, abort_flag, sorted, xs_s, hmaxb, hmax_bar, gu_idx,   \
+                              pub_full, pub_empty, pub_g)
+            if (NT <= 1 || nti == 1) {
+                // class 1: the packed-down variant also runs gate|up items (identical there)
+                constexpr bool PKV = WFMT == FMT_MXFP4 && NT <= 2;  // the packed-down variant exists
+                if constexpr (NT == 0) {
+                    ok = LS_ITEM(ls_compute_item, 1, PKV);
+                } else {
+                    if (PKV && (it.gu || ls_packed<WFMT, NT>(it)))
+                        ok = LS_ITEM(ls_compute_item, 1, PKV);
+                    else
+                        ok = LS_ITEM(ls_compute_item, 1, false);
+                }
+            } else if (NT == 2 || nti == 2)
                 ok = LS_ITEM(ls_compute_item_wide, NT < 2 ? 1 : 2);
             else if (NT == 4 || nti == 4)
                 ok = LS_ITEM(ls_compute_item_wide, NT < 4 ? 1 : 4);
