@@ -12,9 +12,9 @@ arrays into it with ctypes.  Each function cites the passage it follows:
 * MXFP4 decode and size -- "DeepSeek-V4-Flash on a four-GPU Ampere
   workstation", section "MXFP4 is not NVFP4, and the difference matters on
   Ampere".
-* SwiGLU experts, weighted reduction, shared experts, routing as IDs + weights
-  -- "Cascadia: Resident 975B MoE Inference on Eleven AI PCs" §3.1 and Eq. (1)
-  of §3.3.
+* SwiGLU experts, weighted reduction, shared experts, routing as IDs + weights,
+  and the sigmoid + bias routing variant -- "Cascadia: Resident 975B MoE
+  Inference on Eleven AI PCs" §3.1 and Eq. (1) of §3.3.
 * Dense FFN as all-active slices -- same paper, §3.4, Eq. (2).
 """
 from __future__ import annotations
@@ -74,12 +74,16 @@ def lib():
             L.oracle_bf16_decode.restype = None
             L.oracle_route.argtypes = [vp, i64, ci, ci, vp, vp]
             L.oracle_route.restype = None
+            L.oracle_route_sigmoid.argtypes = [vp, vp, i64, ci, ci, ctypes.c_double, vp, vp]
+            L.oracle_route_sigmoid.restype = None
             L.oracle_permute.argtypes = [vp, i64, ci, ci, vp, vp, vp]
             L.oracle_permute.restype = None
             L.oracle_swiglu_ffn.argtypes = [vp, vp, i64, vp, i64, ci, ci, vp, vp]
             L.oracle_swiglu_ffn.restype = None
             L.oracle_moe_layer.argtypes = [ctypes.POINTER(_Layer), vp, vp, i64, ci, ci, vp, vp, vp]
             L.oracle_moe_layer.restype = ci
+            L.oracle_moe_layer_routed.argtypes = [ctypes.POINTER(_Layer), vp, vp, vp, i64, ci, ci, vp]
+            L.oracle_moe_layer_routed.restype = ci
             L.oracle_dense_ffn.argtypes = [ci, vp, vp, vp, vp, vp, vp, ci, ci, ci, vp, i64, ci, vp]
             L.oracle_dense_ffn.restype = ci
             _lib = L
@@ -139,6 +143,21 @@ def route(logits: np.ndarray, k: int):
     ids = np.empty((T, k), np.int32)
     w = np.empty((T, k), np.float64)
     lib().oracle_route(_p(logits), T, E, k, _p(ids), _p(w))
+    return ids, w
+
+
+def route_sigmoid(logits: np.ndarray, bias: np.ndarray | None, k: int, scale: float = 1.0):
+    """Sigmoid scores, bias-adjusted top-k selection, weights normalised over the
+    selected experts times scale ("Cascadia: Resident 975B MoE Inference on
+    Eleven AI PCs" §3.1): returns ids int32 [T, k], w float64 [T, k]."""
+    logits = _c(logits, np.float32)
+    T, E = logits.shape
+    if bias is not None:
+        bias = _c(bias, np.float32)
+        assert bias.shape == (E,)
+    ids = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float64)
+    lib().oracle_route_sigmoid(_p(logits), _p(bias), T, E, k, float(scale), _p(ids), _p(w))
     return ids, w
 
 
@@ -206,6 +225,30 @@ def moe_layer(W: OracleWeights, x_bf16: np.ndarray, logits: np.ndarray, k: int, 
     if rc != 0:
         raise ValueError(f"oracle_moe_layer failed with {rc}")
     return out, ids, w
+
+
+def moe_layer_routed(W: OracleWeights, x_bf16: np.ndarray, ids: np.ndarray, w: np.ndarray, nthreads: int = 1):
+    """The MoE layer for given routing (ids [n, k] in [0, E), weights [n, k]):
+    every selected and shared expert on its tokens and the weighted reduction
+    ("Cascadia" §3.1, Eq. (1) of §3.3, routing entering as IDs and weights).
+    Returns out float64 [n, H]."""
+    x_bf16 = _c(x_bf16, np.uint16)
+    ids = _c(ids, np.int32)
+    w = _c(w, np.float64)
+    n, H = x_bf16.shape
+    k = ids.shape[1]
+    assert H == W.hidden and ids.shape == (n, k) and w.shape == (n, k)
+    ne = W.n_experts + W.n_shared
+    arr = lambda lst: (ctypes.c_void_p * ne)(*[(None if a is None else a.ctypes.data) for a in lst])
+    keep = [arr(W.gu_codes), arr(W.gu_scales), arr(W.d_codes), arr(W.d_scales)]
+    cast = lambda a: ctypes.cast(a, ctypes.POINTER(ctypes.c_void_p))
+    L = _Layer(W.hidden, W.inter, W.n_experts, W.n_shared, 1 if W.weight_format == "bf16" else 0,
+               cast(keep[0]), cast(keep[1]), cast(keep[2]), cast(keep[3]))
+    out = np.empty((n, H), np.float64)
+    rc = lib().oracle_moe_layer_routed(ctypes.byref(L), _p(x_bf16), _p(ids), _p(w), n, k, nthreads, _p(out))
+    if rc != 0:
+        raise ValueError(f"oracle_moe_layer_routed failed with {rc}")
+    return out
 
 
 def dense_ffn(weights, x_bf16: np.ndarray, n_slices: int = 0, weight_format: str = "mxfp4") -> np.ndarray:

@@ -142,6 +142,54 @@ void oracle_route(const float *logits, int64_t T, int E, int k, int32_t *ids, do
     free(s);
 }
 
+/* The routing of "Cascadia: Resident 975B MoE Inference on Eleven AI PCs"
+ * §3.1: sigmoid scores, a bias-adjusted top-k selection, and weights
+ * normalised over the selected experts, times a model scale factor.  For
+ * token t and expert e: s_e = 1 / (1 + exp(-l_e)) in double; the selection
+ * key is s_e + b_e (the bias decides only which experts are kept); the k
+ * largest keys are kept in the router order (larger first, equal keys by the
+ * lower index, a NaN key after every number); their weights are
+ * w_j = scale * s_{e_j} / sum_{j' < k} s_{e_j'}.  bias may be NULL (zeros). */
+typedef struct {
+    double v;
+    int idx;
+} KeyedExpert;
+
+static int keyed_order(const void *pa, const void *pb)
+{
+    const KeyedExpert *a = (const KeyedExpert *)pa, *b = (const KeyedExpert *)pb;
+    int na = isnan(a->v), nb = isnan(b->v);
+    if (na != nb)
+        return na ? 1 : -1;
+    if (!na && a->v != b->v)
+        return a->v > b->v ? -1 : 1;
+    return a->idx < b->idx ? -1 : (a->idx > b->idx ? 1 : 0);
+}
+
+void oracle_route_sigmoid(const float *logits, const float *bias, int64_t T, int E, int k, double scale, int32_t *ids,
+                          double *w)
+{
+    KeyedExpert *s = (KeyedExpert *)malloc(sizeof(KeyedExpert) * (size_t)E);
+    double *score = (double *)malloc(sizeof(double) * (size_t)E);
+    for (int64_t t = 0; t < T; ++t) {
+        for (int e = 0; e < E; ++e) {
+            score[e] = 1.0 / (1.0 + exp(-(double)logits[t * E + e]));
+            s[e].v = score[e] + (bias ? (double)bias[e] : 0.0);
+            s[e].idx = e;
+        }
+        qsort(s, (size_t)E, sizeof(KeyedExpert), keyed_order);
+        double denom = 0.0;
+        for (int j = 0; j < k; ++j)
+            denom += score[s[j].idx];
+        for (int j = 0; j < k; ++j) {
+            ids[t * k + j] = s[j].idx;
+            w[t * k + j] = scale * score[s[j].idx] / denom;
+        }
+    }
+    free(score);
+    free(s);
+}
+
 /* Group slots by expert: a stable counting sort of the flattened slots
  * s = t*k + j by their expert id.  off[e] is the first sorted position of
  * expert e (off[E] = T*k), sorted_slot[p] the slot at position p, and
@@ -280,23 +328,26 @@ static int decode_matrix(int fmt, const void *codes, const uint8_t *scales, int6
  * x_bf16 [n_tok, H] BF16 bits, logits [n_tok, E], out [n_tok, H] double.
  * ids / w (optional, [n_tok, k]) receive the routing.
  * Returns 0, -1 (E8M0 = 255), -2 (weights of a used expert missing), -3 (bad args). */
-int oracle_moe_layer(const OracleLayer *L, const uint16_t *x_bf16, const float *logits, int64_t n_tok, int k,
-                     int nthreads, double *out, int32_t *ids_out, double *w_out)
+/* The layer for given routing (ids [n_tok, k] in [0, E), weights w): every
+ * selected and every shared expert on its tokens, then the weighted reduction
+ * (Eq. 1).  Returns 0, -1 (E8M0 = 255), -3 (bad args or an id out of range). */
+int oracle_moe_layer_routed(const OracleLayer *L, const uint16_t *x_bf16, const int32_t *ids, const double *w,
+                            int64_t n_tok, int k, int nthreads, double *out)
 {
     const int H = L->hidden, I = L->inter, E = L->n_experts, S = L->n_shared;
     if (k < 1 || k > E || H % 32 || I % 32)
         return -3;
+    for (int64_t i = 0; i < n_tok * k; ++i)
+        if (ids[i] < 0 || ids[i] >= E)
+            return -3;
     const int nsel = k + S;
     int rc = 0;
-    int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n_tok * k + 1));
-    double *w = (double *)malloc(sizeof(double) * (size_t)(n_tok * k + 1));
     double *x = (double *)malloc(sizeof(double) * (size_t)(n_tok * H + 1));
     double *y = (double *)calloc((size_t)(n_tok * nsel * H + 1), sizeof(double));
     int64_t *work = (int64_t *)malloc(sizeof(int64_t) * (size_t)(2 * n_tok * nsel + 2));
     float *Wgu = (float *)malloc(sizeof(float) * (size_t)2 * I * H);
     float *Wd = (float *)malloc(sizeof(float) * (size_t)H * I);
 
-    oracle_route(logits, n_tok, E, k, ids, w);
     for (int64_t i = 0; i < n_tok * H; ++i) {
         uint32_t u = (uint32_t)x_bf16[i] << 16;
         float f;
@@ -341,6 +392,28 @@ int oracle_moe_layer(const OracleLayer *L, const uint16_t *x_bf16, const float *
                 out[t * H + m] = acc;
             }
         }
+    }
+    free(x);
+    free(y);
+    free(work);
+    free(Wgu);
+    free(Wd);
+    return rc;
+}
+
+/* The routed layer: softmax top-k routing of the logits, then the layer for
+ * that routing; the routing goes to ids_out / w_out when given. */
+int oracle_moe_layer(const OracleLayer *L, const uint16_t *x_bf16, const float *logits, int64_t n_tok, int k,
+                     int nthreads, double *out, int32_t *ids_out, double *w_out)
+{
+    const int E = L->n_experts;
+    if (k < 1 || k > E)
+        return -3;
+    int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n_tok * k + 1));
+    double *w = (double *)malloc(sizeof(double) * (size_t)(n_tok * k + 1));
+    oracle_route(logits, n_tok, E, k, ids, w);
+    int rc = oracle_moe_layer_routed(L, x_bf16, ids, w, n_tok, k, nthreads, out);
+    if (rc == 0) {
         if (ids_out)
             memcpy(ids_out, ids, sizeof(int32_t) * (size_t)(n_tok * k));
         if (w_out)
@@ -348,11 +421,6 @@ int oracle_moe_layer(const OracleLayer *L, const uint16_t *x_bf16, const float *
     }
     free(ids);
     free(w);
-    free(x);
-    free(y);
-    free(work);
-    free(Wgu);
-    free(Wd);
     return rc;
 }
 

@@ -34,6 +34,13 @@ MUTATIONS = {
                         "            acc += h[n] * (double)wd[n];",
                         "for (int n = 0; n < I; ++n)\n            acc += h[n] * (double)Wd[(int64_t)n * ld_d + m % ld_d];"),
     "weights_reversed": ("acc += w[t * k + j] * y", "acc += w[t * k + (k - 1 - j)] * y"),
+    "sigmoid_bias_in_weights": ("w[t * k + j] = scale * score[s[j].idx] / denom;",
+                                "w[t * k + j] = scale * s[j].v / denom;"),
+    "sigmoid_bias_ignored": ("s[e].v = score[e] + (bias ? (double)bias[e] : 0.0);", "s[e].v = score[e];"),
+    "sigmoid_sign": ("score[e] = 1.0 / (1.0 + exp(-(double)logits[t * E + e]));",
+                     "score[e] = 1.0 / (1.0 + exp((double)logits[t * E + e]));"),
+    "sigmoid_normalised_over_all": ("for (int j = 0; j < k; ++j)\n            denom += score[s[j].idx];",
+                                    "for (int e = 0; e < E; ++e)\n            denom += score[e];"),
 }
 
 

@@ -376,3 +376,128 @@ def test_dense_rejects_slice_cutting_a_block():
     x = wl.f32_to_bf16_bits(np.ones((1, H), np.float32))
     with pytest.raises(ValueError):
         oracle.dense_ffn(w, x, 2)   # 48-wide slices
+
+
+# ------------------------------------------------------------------ sigmoid + bias routing pins
+# "Cascadia: Resident 975B MoE Inference on Eleven AI PCs" §3.1: sigmoid scores,
+# bias-adjusted top-k selection, weights normalised over the selected experts.
+
+def brute_route_sigmoid(l, b, k, scale):
+    """Plain-Python: key = sigmoid(l) + b (double), larger first, equal by lower
+    index, NaN last; weights = scale * sigmoid(l_j) / sum of the kept sigmoids."""
+    E = len(l)
+    s = [1.0 / (1.0 + math.exp(-float(v))) if not math.isnan(v) else float("nan") for v in l]
+    key = [s[e] + float(b[e]) for e in range(E)]
+    order = sorted(range(E), key=lambda e: (math.isnan(key[e]), 0.0 if math.isnan(key[e]) else -key[e], e))
+    sel = order[:k]
+    tot = sum(s[e] for e in sel)
+    return sel, [scale * s[e] / tot for e in sel]
+
+
+def test_route_sigmoid_brute_force():
+    rng = np.random.default_rng(31)
+    for trial in range(100):
+        E = int(rng.integers(1, 48))
+        k = int(rng.integers(1, min(E, 8) + 1))
+        l = (rng.standard_normal((3, E)) * 2).astype(np.float32)
+        b = (rng.standard_normal(E) * 0.3).astype(np.float32)
+        scale = float(rng.uniform(0.5, 3.0))
+        ids, w = oracle.route_sigmoid(l, b, k, scale)
+        for t in range(3):
+            sel, ww = brute_route_sigmoid(l[t].tolist(), b.tolist(), k, scale)
+            assert ids[t].tolist() == sel
+            np.testing.assert_allclose(w[t], ww, rtol=1e-14, atol=0)
+
+
+def test_route_sigmoid_zero_bias_selects_like_softmax():
+    # sigmoid is increasing, so without a bias the selection is the softmax router's
+    rng = np.random.default_rng(32)
+    l = rng.standard_normal((64, 128)).astype(np.float32)
+    ids_s, w_s = oracle.route_sigmoid(l, None, 6)
+    ids_m, _ = oracle.route(l, 6)
+    np.testing.assert_array_equal(ids_s, ids_m)
+    assert np.all(np.abs(w_s.sum(1) - 1.0) <= 1e-12)
+    sig = 1.0 / (1.0 + np.exp(-l.astype(np.float64)))
+    for t in range(64):
+        ratio = sig[t, ids_s[t]] / sig[t, ids_s[t]].sum()
+        np.testing.assert_allclose(w_s[t], ratio, rtol=1e-13)
+
+
+def test_route_sigmoid_bias_decides_selection_not_weights():
+    rng = np.random.default_rng(33)
+    l = rng.standard_normal((16, 32)).astype(np.float32)
+    b = np.zeros(32, np.float32)
+    b[5] = 10.0    # always selected ...
+    b[9] = -10.0   # ... never selected
+    ids, w = oracle.route_sigmoid(l, b, 4, 2.0)
+    assert np.all(ids[:, 0] == 5) and not np.any(ids == 9)
+    sig = 1.0 / (1.0 + np.exp(-l.astype(np.float64)))
+    for t in range(16):
+        np.testing.assert_allclose(w[t], 2.0 * sig[t, ids[t]] / sig[t, ids[t]].sum(), rtol=1e-13)
+    assert np.all(np.abs(w.sum(1) - 2.0) <= 1e-12)
+
+
+def test_route_sigmoid_ties_and_nan():
+    l = np.array([[0.5, 0.5, np.nan, -1.0, 0.5]], np.float32)
+    ids, _ = oracle.route_sigmoid(l, np.zeros(5, np.float32), 5)
+    assert ids[0].tolist() == [0, 1, 4, 3, 2]
+    # equal keys from different logits and biases tie exactly only if equal; lower index first
+    ids2, _ = oracle.route_sigmoid(np.zeros((1, 4), np.float32), np.array([0.0, 0.25, 0.25, 0.0], np.float32), 2)
+    assert ids2[0].tolist() == [1, 2]
+
+
+# ------------------------------------------------------------------ layer for given routing
+
+def test_layer_routed_equals_layer_on_its_own_routing():
+    cfg = wl.custom("rt", 7, 64, 64, 6, 1, 2, seed=34)
+    x, l = wl.tokens(cfg), wl.router_logits(cfg)
+    W = oracle.OracleWeights(64, 64, 6, 1)
+    for e in range(7):
+        W.set_expert(e, *wl.expert_weights(cfg, e))
+    out, ids, w = oracle.moe_layer(W, x, l, 2)
+    np.testing.assert_array_equal(oracle.moe_layer_routed(W, x, ids, w), out)
+
+
+def test_layer_routed_single_selection_closed_form():
+    # one selected expert with weight alpha and no shared expert: alpha times the
+    # textbook SwiGLU FFN of that expert, whatever the other experts hold
+    cfg = wl.custom("rt1", 5, 96, 64, 3, 0, 1, seed=35)
+    x = wl.tokens(cfg)
+    ws = [wl.expert_weights(cfg, e) for e in range(3)]
+    W = oracle.OracleWeights(96, 64, 3, 0)
+    for e in range(3):
+        W.set_expert(e, *ws[e])
+    ids = np.array([[2], [0], [2], [1], [2]], np.int32)
+    alpha = np.array([[0.5], [1.75], [-2.0], [3.0], [0.0]])
+    out = oracle.moe_layer_routed(W, x, ids, alpha)
+    xf = wl.bf16_bits_to_f32(x).astype(np.float64)
+    for t in range(5):
+        gc, gs, dc, ds = ws[ids[t, 0]]
+        Wgu, Wd = np_decode_golden(gc, gs), np_decode_golden(dc, ds)
+        g, u = xf[t] @ Wgu[:64].T, xf[t] @ Wgu[64:].T
+        want = alpha[t, 0] * ((g / (1 + np.exp(-g)) * u) @ Wd.T)
+        assert np.max(np.abs(out[t] - want)) <= 1e-12 * max(1.0, np.max(np.abs(want)))
+
+
+def test_layer_routed_is_linear_in_the_weights():
+    cfg = wl.custom("rt2", 6, 64, 32, 4, 1, 2, seed=36)
+    x = wl.tokens(cfg)
+    W = oracle.OracleWeights(64, 32, 4, 1)
+    for e in range(5):
+        W.set_expert(e, *wl.expert_weights(cfg, e))
+    rng = np.random.default_rng(36)
+    ids = np.stack([rng.choice(4, 2, replace=False) for _ in range(6)]).astype(np.int32)
+    w = rng.uniform(0.1, 1.0, (6, 2))
+    shared = oracle.moe_layer_routed(W, x, ids, np.zeros_like(w))
+    o1 = oracle.moe_layer_routed(W, x, ids, w) - shared
+    o2 = oracle.moe_layer_routed(W, x, ids, 2 * w) - shared
+    np.testing.assert_allclose(o2, 2 * o1, rtol=1e-12, atol=1e-12 * np.abs(o1).max())
+
+
+def test_layer_routed_rejects_ids_out_of_range():
+    cfg = wl.custom("rt3", 2, 64, 32, 3, 0, 1, seed=37)
+    W = oracle.OracleWeights(64, 32, 3, 0)
+    for e in range(3):
+        W.set_expert(e, *wl.expert_weights(cfg, e))
+    with pytest.raises(ValueError):
+        oracle.moe_layer_routed(W, wl.tokens(cfg), np.array([[0], [3]], np.int32), np.ones((2, 1)))
