@@ -62,6 +62,7 @@
 #define MOE_GB300_H
 
 #include <stddef.h>
+#include <stdint.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -153,6 +154,43 @@ typedef struct {
 MoeStatus moe_forward(MoeHandle *h, const void *x_bf16, const float *router_logits, int T, int k, float *out_fp32,
                       int accumulate, void *workspace, size_t ws_bytes, const MoeRoutingOut *routing,
                       void *cuda_stream);
+
+/* One routed MoE layer on T tokens for routing given by the caller: the
+ * interface of "Cascadia: Resident 975B MoE Inference on Eleven AI PCs" §3.1,
+ * where the router's results enter the expert computation as expert IDs and
+ * routing weights (the shared experts are added with weight 1, as in
+ * moe_forward).
+ *  topk_ids [T][k] int32 in [0, E), 4-byte aligned (an expert may appear more
+ *           than once for a token; each occurrence is its own slot)
+ *  topk_w   [T][k] float, 4-byte aligned, used as given
+ *  other arguments as for moe_forward; `routing` receives the copy of the
+ *  ids and weights the layer ran with and the grouping.
+ * An id outside [0, E) cannot be checked on the host: the device records it,
+ * runs that slot as expert 0 with weight 0 so that every access stays in
+ * bounds, and moe_sync_status() then reports MOE_EDEVICE.
+ * Errors: MOE_EINVAL (NULL/misaligned pointers, T < 0, k outside [1, k_max],
+ * a dense handle), MOE_EWORKSPACE, MOE_EDEVICE, MOE_ECUDA. */
+MoeStatus moe_forward_routed(MoeHandle *h, const void *x_bf16, const int32_t *topk_ids, const float *topk_w, int T,
+                             int k, float *out_fp32, int accumulate, void *workspace, size_t ws_bytes,
+                             const MoeRoutingOut *routing, void *cuda_stream);
+
+/* Largest E moe_route_sigmoid takes (one warp per token, 32 experts a lane). */
+#define MOE_ROUTE_SIGMOID_MAX_EXPERTS 1024
+
+/* The routing variant of "Cascadia" §3.1: sigmoid scores, a bias-adjusted
+ * top-k selection, and weights normalised over the selected experts times a
+ * model scale factor.  For token t: s_e = 1 / (1 + exp(-l_te)); the k
+ * largest keys s_e + bias_e are kept (larger first, equal keys by the lower
+ * index, a NaN after every number); w_j = routed_scale * s_j / sum of the
+ * kept s.  The bias decides only the selection.  Scores and keys are FP64,
+ * weights are stored as float.  The outputs feed moe_forward_routed.
+ *  router_logits [T][E] float, bias [E] float or NULL (zeros), topk_ids and
+ *  topk_w [T][k]: device pointers, 4-byte aligned, enqueued on cuda_stream.
+ * No handle and no workspace.  T == 0 enqueues nothing.
+ * Errors: MOE_EINVAL (T < 0, E outside [1, MOE_ROUTE_SIGMOID_MAX_EXPERTS], k
+ * outside [1, min(E, 32)], NULL or misaligned pointers), MOE_ECUDA. */
+MoeStatus moe_route_sigmoid(const float *router_logits, const float *bias, int T, int E, int k, float routed_scale,
+                            int32_t *topk_ids, float *topk_w, void *cuda_stream);
 
 /* The dense FFN of a dense handle on T tokens, as the sum of its all-active
  * slices ("Cascadia" §3.4, Eq. 2).  Arguments as for moe_forward; the

@@ -21,9 +21,9 @@ STATUS_NAMES = ["MOE_OK", "MOE_EINVAL", "MOE_EDIMS", "MOE_ESCALE", "MOE_ENOMEM",
 MOE_W_MXFP4, MOE_W_BF16 = 0, 1
 
 # every symbol include/moe.h declares
-EXPORTED = ("moe_load_weights", "moe_workspace_bytes", "moe_forward", "moe_dense_sliced_forward",
-            "moe_sync_status", "moe_profile_enable", "moe_profile_read", "moe_route_static", "moe_last_error",
-            "moe_free")
+EXPORTED = ("moe_load_weights", "moe_workspace_bytes", "moe_forward", "moe_forward_routed",
+            "moe_route_sigmoid", "moe_dense_sliced_forward", "moe_sync_status", "moe_profile_enable",
+            "moe_profile_read", "moe_route_static", "moe_last_error", "moe_free")
 STAGES = ("routing", "grouping", "gate_up", "down", "combine", "layer")
 
 
@@ -61,6 +61,10 @@ def _load():
     L.moe_workspace_bytes.restype = sz
     L.moe_forward.argtypes = [vp, vp, vp, ci, ci, vp, ci, vp, sz, ctypes.POINTER(MoeRoutingOut), vp]
     L.moe_forward.restype = ci
+    L.moe_forward_routed.argtypes = [vp, vp, vp, vp, ci, ci, vp, ci, vp, sz, ctypes.POINTER(MoeRoutingOut), vp]
+    L.moe_forward_routed.restype = ci
+    L.moe_route_sigmoid.argtypes = [vp, vp, ci, ci, ci, ctypes.c_float, vp, vp, vp]
+    L.moe_route_sigmoid.restype = ci
     L.moe_dense_sliced_forward.argtypes = [vp, vp, ci, vp, ci, vp, sz, vp]
     L.moe_dense_sliced_forward.restype = ci
     L.moe_sync_status.argtypes = [vp, vp]
@@ -125,6 +129,19 @@ def moe_forward(handle: int, x_bf16, router_logits, T: int, k: int, out_fp32, ac
     _check(lib.moe_forward(handle, _ptr(x_bf16), _ptr(router_logits), T, k, _ptr(out_fp32), int(bool(accumulate)),
                            _ptr(workspace), ws_bytes, ctypes.byref(routing) if routing is not None else None,
                            _stream(stream)))
+
+
+def moe_forward_routed(handle: int, x_bf16, topk_ids, topk_w, T: int, k: int, out_fp32, accumulate: bool, workspace,
+                       ws_bytes: int, routing: Optional[MoeRoutingOut] = None, stream=None) -> None:
+    _check(lib.moe_forward_routed(handle, _ptr(x_bf16), _ptr(topk_ids), _ptr(topk_w), T, k, _ptr(out_fp32),
+                                  int(bool(accumulate)), _ptr(workspace), ws_bytes,
+                                  ctypes.byref(routing) if routing is not None else None, _stream(stream)))
+
+
+def moe_route_sigmoid(router_logits, bias, T: int, E: int, k: int, routed_scale: float, topk_ids, topk_w,
+                      stream=None) -> None:
+    _check(lib.moe_route_sigmoid(_ptr(router_logits), _ptr(bias), T, E, k, float(routed_scale), _ptr(topk_ids),
+                                 _ptr(topk_w), _stream(stream)))
 
 
 def moe_dense_sliced_forward(handle: int, x_bf16, T: int, out_fp32, accumulate: bool, workspace, ws_bytes: int,

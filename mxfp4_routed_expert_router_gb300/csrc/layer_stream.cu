@@ -191,6 +191,8 @@ struct LayerArgs {
     int T, k, E, S, G, H, I, n;
     const uint16_t *x;
     const float *logits;
+    const int *ids_in;   // routing given by the caller (ids, weights) instead of logits, or NULL
+    const float *w_in;
     int *topk_ids;
     float *topk_w;
     int *expert_offsets, *sorted_slot, *slot_pos;
@@ -418,6 +420,29 @@ __device__ void ls_route_warp(const LayerArgs &a, int t, int lane, int *ids_s, b
         if (owner) {
             a.topk_ids[(size_t)t * a.k + lane] = my_e;
             a.topk_w[(size_t)t * a.k + lane] = ex / sum;
+        }
+    }
+}
+
+// Routing given by the caller for token t (one warp): lane j < k takes its id
+// and weight; an id outside [0, E) records DEV_ERR_BOUNDS and becomes expert 0
+// with weight 0, so that the layer stays in bounds.  The ids go to ids_s when
+// given, and the owner CTA writes both to the call's routing arrays.
+__device__ void ls_copy_route_warp(const LayerArgs &a, int t, int lane, int *ids_s, bool owner)
+{
+    if (lane < a.k) {
+        int e = __ldg(a.ids_in + (size_t)t * a.k + lane);
+        float wv = __ldg(a.w_in + (size_t)t * a.k + lane);
+        if (e < 0 || e >= a.E) {
+            atomicCAS(a.err, 0, DEV_ERR_BOUNDS);
+            e = 0;
+            wv = 0.f;
+        }
+        if (ids_s)
+            ids_s[t * a.k + lane] = e;
+        if (owner) {
+            a.topk_ids[(size_t)t * a.k + lane] = e;
+            a.topk_w[(size_t)t * a.k + lane] = wv;
         }
     }
 }
@@ -1115,11 +1140,21 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
     if (tid < LS_ROUTE_THREADS) {
         if (a.E > 0) {
             if (local) {
-                for (int t = warp; t < a.T; t += LS_ROUTE_WARPS)
-                    ls_route_warp(a, t, lane, reinterpret_cast<int *>(smem), t % (int)gridDim.x == (int)blockIdx.x);
+                for (int t = warp; t < a.T; t += LS_ROUTE_WARPS) {
+                    const bool own = t % (int)gridDim.x == (int)blockIdx.x;
+                    if (a.ids_in)
+                        ls_copy_route_warp(a, t, lane, reinterpret_cast<int *>(smem), own);
+                    else
+                        ls_route_warp(a, t, lane, reinterpret_cast<int *>(smem), own);
+                }
             } else {
-                for (int i = warp; i < mine; i += LS_ROUTE_WARPS)
-                    ls_route_warp(a, (int)blockIdx.x + i * (int)gridDim.x, lane, nullptr, true);
+                for (int i = warp; i < mine; i += LS_ROUTE_WARPS) {
+                    const int t = (int)blockIdx.x + i * (int)gridDim.x;
+                    if (a.ids_in)
+                        ls_copy_route_warp(a, t, lane, nullptr, true);
+                    else
+                        ls_route_warp(a, t, lane, nullptr, true);
+                }
             }
         }
     } else {
@@ -1482,7 +1517,8 @@ bool layer_stream_fits(const Plan &p, int fmt)
 }
 
 cudaError_t launch_layer_stream(const Plan &p, const WeightStore &gu, const WeightStore &dn, int fmt,
-                                const uint16_t *x, const float *logits, float *out, int accumulate, cudaStream_t st)
+                                const uint16_t *x, const float *logits, const int *ids_in, const float *w_in,
+                                float *out, int accumulate, cudaStream_t st)
 {
     cudaError_t e = cudaMemsetAsync(p.sync, 0, layer_stream_sync_bytes(p.G), st);
     if (e != cudaSuccess)
@@ -1507,6 +1543,8 @@ cudaError_t launch_layer_stream(const Plan &p, const WeightStore &gu, const Weig
     a.n = p.E > 0 ? p.T * p.k : 0;
     a.x = x;
     a.logits = logits;
+    a.ids_in = ids_in;
+    a.w_in = w_in;
     a.topk_ids = p.topk_ids;
     a.topk_w = p.topk_w;
     a.expert_offsets = p.expert_offsets;

@@ -120,8 +120,11 @@ MoeStatus check_pending(const MoeHandle *h)
     return MOE_OK;
 }
 
-MoeStatus run_layer(MoeHandle *h, const void *x, const float *logits, int T, int k, float *out, int accumulate,
-                    void *ws, size_t ws_bytes, const MoeRoutingOut *routing, cudaStream_t st)
+// One forward call.  Routing comes from the logits (softmax top-k), or, when
+// ids_in is given, from the caller's ids and weights.
+MoeStatus run_layer(MoeHandle *h, const void *x, const float *logits, const int *ids_in, const float *w_in, int T,
+                    int k, float *out, int accumulate, void *ws, size_t ws_bytes, const MoeRoutingOut *routing,
+                    cudaStream_t st)
 {
     Plan p;
     size_t need = plan_layout(h, T, k, (char *)ws, &p);
@@ -146,8 +149,8 @@ MoeStatus run_layer(MoeHandle *h, const void *x, const float *logits, int T, int
     if (stream && layer_stream_fits(p, h->fmt)) {
         for (int i = 0; i <= 5; ++i)
             mark(i);
-        if ((e = launch_layer_stream(p, h->gu_f, h->dn_f, h->fmt, (const uint16_t *)x, logits, out, accumulate,
-                                     st)) != cudaSuccess)
+        if ((e = launch_layer_stream(p, h->gu_f, h->dn_f, h->fmt, (const uint16_t *)x, logits, ids_in, w_in, out,
+                                     accumulate, st)) != cudaSuccess)
             return cuda_fail(e, "layer launch");
         mark(6);
         if (h->profile)
@@ -156,8 +159,14 @@ MoeStatus run_layer(MoeHandle *h, const void *x, const float *logits, int T, int
     }
     mark(0);
     if (h->E > 0) {
-        if ((e = launch_router(logits, T, h->E, k, p.topk_ids, p.topk_w, p.counts, h->E, st)) != cudaSuccess)
+        if (ids_in) {
+            if ((e = launch_routing_copy(ids_in, w_in, T * k, h->E, p.topk_ids, p.topk_w, p.counts, h->E, p.err,
+                                         st)) != cudaSuccess)
+                return cuda_fail(e, "routing copy launch");
+        } else if ((e = launch_router(logits, T, h->E, k, p.topk_ids, p.topk_w, p.counts, h->E, st)) !=
+                   cudaSuccess) {
             return cuda_fail(e, "router launch");
+        }
         mark(1);
         if ((e = launch_permute(p, st)) != cudaSuccess)
             return cuda_fail(e, "permute launch");
@@ -381,8 +390,57 @@ MoeStatus moe_forward(MoeHandle *h, const void *x_bf16, const float *router_logi
     MoeStatus s = check_pending(h);
     if (s != MOE_OK)
         return s;
-    return run_layer(h, x_bf16, router_logits, T, k, out_fp32, accumulate, workspace, ws_bytes, routing,
+    return run_layer(h, x_bf16, router_logits, nullptr, nullptr, T, k, out_fp32, accumulate, workspace, ws_bytes,
+                     routing, (cudaStream_t)cuda_stream);
+}
+
+MoeStatus moe_forward_routed(MoeHandle *h, const void *x_bf16, const int32_t *topk_ids, const float *topk_w, int T,
+                             int k, float *out_fp32, int accumulate, void *workspace, size_t ws_bytes,
+                             const MoeRoutingOut *routing, void *cuda_stream)
+{
+    if (!h)
+        return fail(MOE_EINVAL, "moe_forward_routed: NULL handle");
+    if (h->E == 0)
+        return fail(MOE_EINVAL, "moe_forward_routed on a dense handle; use moe_dense_sliced_forward");
+    if (T < 0 || T > (1 << 24))
+        return fail(MOE_EINVAL, "T = %d out of range [0, 2^24]", T);
+    if (k < 1 || k > h->k_max)
+        return fail(MOE_EINVAL, "k = %d out of range [1, %d]", k, h->k_max);
+    if (T == 0)
+        return check_pending(h);
+    if (!x_bf16 || !topk_ids || !topk_w || !out_fp32 || !workspace)
+        return fail(MOE_EINVAL, "moe_forward_routed: NULL pointer");
+    if (!aligned(x_bf16, 16) || !aligned(out_fp32, 16) || !aligned(topk_ids, 4) || !aligned(topk_w, 4))
+        return fail(MOE_EINVAL, "x and out must be 16-byte aligned, ids and weights 4-byte aligned");
+    if (!aligned(workspace, 256))
+        return fail(MOE_EWORKSPACE, "workspace must be 256-byte aligned");
+    MoeStatus s = check_pending(h);
+    if (s != MOE_OK)
+        return s;
+    return run_layer(h, x_bf16, nullptr, topk_ids, topk_w, T, k, out_fp32, accumulate, workspace, ws_bytes, routing,
                      (cudaStream_t)cuda_stream);
+}
+
+MoeStatus moe_route_sigmoid(const float *router_logits, const float *bias, int T, int E, int k, float routed_scale,
+                            int32_t *topk_ids, float *topk_w, void *cuda_stream)
+{
+    if (T < 0 || T > (1 << 24))
+        return fail(MOE_EINVAL, "T = %d out of range [0, 2^24]", T);
+    if (E < 1 || E > MOE_ROUTE_SIGMOID_MAX_EXPERTS)
+        return fail(MOE_EINVAL, "E = %d out of range [1, %d]", E, MOE_ROUTE_SIGMOID_MAX_EXPERTS);
+    if (k < 1 || k > E || k > 32)
+        return fail(MOE_EINVAL, "k = %d out of range [1, min(E, 32)]", k);
+    if (T == 0)
+        return MOE_OK;
+    if (!router_logits || !topk_ids || !topk_w)
+        return fail(MOE_EINVAL, "moe_route_sigmoid: NULL pointer");
+    if (!aligned(router_logits, 4) || !aligned(bias, 4) || !aligned(topk_ids, 4) || !aligned(topk_w, 4))
+        return fail(MOE_EINVAL, "moe_route_sigmoid: arrays must be 4-byte aligned");
+    cudaError_t e = launch_router_sigmoid(router_logits, bias, T, E, k, routed_scale, topk_ids, topk_w,
+                                          (cudaStream_t)cuda_stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "sigmoid router launch");
+    return MOE_OK;
 }
 
 MoeStatus moe_dense_sliced_forward(MoeHandle *h, const void *x_bf16, int T, float *out_fp32, int accumulate,
@@ -405,7 +463,7 @@ MoeStatus moe_dense_sliced_forward(MoeHandle *h, const void *x_bf16, int T, floa
     MoeStatus s = check_pending(h);
     if (s != MOE_OK)
         return s;
-    return run_layer(h, x_bf16, nullptr, T, 0, out_fp32, accumulate, workspace, ws_bytes, nullptr,
+    return run_layer(h, x_bf16, nullptr, nullptr, nullptr, T, 0, out_fp32, accumulate, workspace, ws_bytes, nullptr,
                      (cudaStream_t)cuda_stream);
 }
 

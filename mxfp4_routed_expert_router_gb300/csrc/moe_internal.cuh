@@ -145,6 +145,17 @@ cudaError_t launch_repack(int fmt, int layout, bool gate_up, const SrcMat &gate,
 cudaError_t launch_router(const float *logits, int T, int E, int k, int *ids, float *w, int *counts, int n_counts,
                           cudaStream_t st);
 
+// caller-given routing (ids, weights) copied into the call's routing arrays;
+// an id outside [0, E) records DEV_ERR_BOUNDS and becomes expert 0, weight 0;
+// counts[0 .. n_counts) are cleared for the histogram
+cudaError_t launch_routing_copy(const int *ids_in, const float *w_in, int n, int E, int *ids, float *w, int *counts,
+                                int n_counts, int *err, cudaStream_t st);
+
+// sigmoid scores, bias-adjusted top-k, weights normalised over the selection
+// times scale (bias may be NULL)
+cudaError_t launch_router_sigmoid(const float *logits, const float *bias, int T, int E, int k, float scale, int *ids,
+                                  float *w, cudaStream_t st);
+
 cudaError_t launch_permute(const Plan &p, cudaStream_t st);
 
 cudaError_t launch_dense_plan(const Plan &p, cudaStream_t st);
@@ -173,7 +184,8 @@ bool layer_stream_fits(const Plan &p, int fmt);
 
 // zeroes p.sync, then launches the layer kernel cooperatively (one CTA per SM)
 cudaError_t launch_layer_stream(const Plan &p, const WeightStore &gu, const WeightStore &dn, int fmt,
-                                const uint16_t *x, const float *logits, float *out, int accumulate, cudaStream_t st);
+                                const uint16_t *x, const float *logits, const int *ids_in, const float *w_in,
+                                float *out, int accumulate, cudaStream_t st);
 
 // Record msg as the calling thread's moe_last_error() text; returns status.
 int set_last_error(int status, const char *msg);

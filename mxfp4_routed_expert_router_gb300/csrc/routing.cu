@@ -101,6 +101,146 @@ cudaError_t launch_router(const float *logits, int T, int E, int k, int *ids, fl
     return cudaErrorInvalidValue;
 }
 
+// ---------------------------------------------------------------- routing given by the caller
+//
+// "Cascadia: Resident 975B MoE Inference on Eleven AI PCs" §3.1: routing
+// enters the expert computation as expert IDs and weights.  The caller's
+// arrays are copied into the call's routing arrays; an ID outside [0, E)
+// records DEV_ERR_BOUNDS (reported by moe_sync_status) and is replaced by
+// expert 0 with weight 0, so that everything after it stays in bounds.
+__global__ void routing_copy_kernel(const int *__restrict__ ids_in, const float *__restrict__ w_in, int n, int E,
+                                    int *__restrict__ ids, float *__restrict__ w, int *__restrict__ counts,
+                                    int n_counts, int *err)
+{
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < n_counts; i += blockDim.x)
+            counts[i] = 0;
+    for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < n; s += gridDim.x * blockDim.x) {
+        int e = ids_in[s];
+        float wv = w_in[s];
+        if (e < 0 || e >= E) {
+            atomicCAS(err, 0, DEV_ERR_BOUNDS);
+            e = 0;
+            wv = 0.f;
+        }
+        ids[s] = e;
+        w[s] = wv;
+    }
+}
+
+cudaError_t launch_routing_copy(const int *ids_in, const float *w_in, int n, int E, int *ids, float *w, int *counts,
+                                int n_counts, int *err, cudaStream_t st)
+{
+    int blocks = (n + 255) / 256;
+    if (blocks < 1)
+        blocks = 1;
+    if (blocks > 1024)
+        blocks = 1024;
+    routing_copy_kernel<<<blocks, 256, 0, st>>>(ids_in, w_in, n, E, ids, w, counts, n_counts, err);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- sigmoid routing
+//
+// The routing of "Cascadia" §3.1: sigmoid scores s_e = 1 / (1 + exp(-l_e)),
+// selection of the k largest keys s_e + b_e (the bias decides only the
+// selection), weights w_j = scale * s_j / sum of the selected scores.  Scores
+// and keys are FP64, so that the selection matches an FP64 reference except
+// for keys less than an FP64 ulp apart.  One warp per token; lane l holds the
+// keys of experts l, l+32, ... as order keys + 1 (0: absent or taken).  Each
+// round takes the warp's largest key and, among the experts holding it, the
+// lowest index.
+
+// total order of doubles as unsigned integers: larger value, larger key; +0
+// and -0 equal; NaN below every number
+__device__ __forceinline__ unsigned long long double_order_key(double d)
+{
+    if (isnan(d))
+        return 0ull;
+    if (d == 0.0)
+        d = 0.0;
+    const unsigned long long b = (unsigned long long)__double_as_longlong(d);
+    return (b & 0x8000000000000000ull) ? ~b : (b | 0x8000000000000000ull);
+}
+
+template <int NV>
+__global__ void router_sigmoid_kernel(const float *__restrict__ logits, const float *__restrict__ bias, int T, int E,
+                                      int k, float scale, int *__restrict__ ids, float *__restrict__ w)
+{
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp >= T)
+        return;
+    const float *row = logits + (long long)warp * E;
+    unsigned long long key[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int e = lane + 32 * i;
+        key[i] = 0ull;
+        if (e < E) {
+            const double sc = 1.0 / (1.0 + exp(-(double)row[e]));
+            key[i] = double_order_key(sc + (bias ? (double)bias[e] : 0.0)) + 1ull;
+        }
+    }
+    int my_e = 0;
+    for (int j = 0; j < k; ++j) {
+        unsigned long long best = 0ull;
+        int bi = 0;
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+            if (key[i] > best) {  // strict: the lowest expert of the lane among equals
+                best = key[i];
+                bi = i;
+            }
+        unsigned long long m = best;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const unsigned long long other = __shfl_xor_sync(0xffffffffu, m, o);
+            m = other > m ? other : m;
+        }
+        const unsigned mine = (unsigned)(lane + 32 * bi);
+        const unsigned ew = __reduce_min_sync(0xffffffffu, best == m ? mine : 0xFFFFFFFFu);
+        if (mine == ew) {
+#pragma unroll
+            for (int i = 0; i < NV; ++i)
+                if (i == bi)
+                    key[i] = 0ull;
+        }
+        if (lane == j)
+            my_e = (int)ew;
+    }
+    const double my_s = lane < k ? 1.0 / (1.0 + exp(-(double)row[my_e])) : 0.0;
+    double sum = my_s;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane < k) {
+        ids[(long long)warp * k + lane] = my_e;
+        w[(long long)warp * k + lane] = (float)((double)scale * my_s / sum);
+    }
+}
+
+cudaError_t launch_router_sigmoid(const float *logits, const float *bias, int T, int E, int k, float scale, int *ids,
+                                  float *w, cudaStream_t st)
+{
+    const int threads = 256;
+    const int blocks = (T * 32 + threads - 1) / threads;
+    const int nv = (E + 31) / 32;
+#define MOE_SIGMOID_CASE(N)                                                                                      \
+    if (nv <= N) {                                                                                               \
+        router_sigmoid_kernel<N><<<blocks, threads, 0, st>>>(logits, bias, T, E, k, scale, ids, w);              \
+        return cudaGetLastError();                                                                               \
+    }
+    MOE_SIGMOID_CASE(1)
+    MOE_SIGMOID_CASE(2)
+    MOE_SIGMOID_CASE(4)
+    MOE_SIGMOID_CASE(8)
+    MOE_SIGMOID_CASE(16)
+    MOE_SIGMOID_CASE(32)
+#undef MOE_SIGMOID_CASE
+    return cudaErrorInvalidValue;
+}
+
 // ---------------------------------------------------------------- histogram
 
 // counts[e] = number of slots routed to expert e (integer atomics: the result

@@ -81,6 +81,16 @@ class MoeLayer:
             B.moe_forward(self.handle, x, logits, T, k, out, accumulate, ws, n, routing, stream)
         return out
 
+    def forward_routed(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor,
+                       out: Optional[torch.Tensor] = None, accumulate: bool = False, routing=None, stream=None):
+        """The layer for routing given as expert ids (int32 [T, k]) and weights (float32 [T, k])."""
+        T, k = topk_ids.shape
+        if out is None:
+            out = torch.empty((T, self.cfg.hidden), dtype=torch.float32, device=self.device)
+        ws, n = self.workspace(T, k)
+        B.moe_forward_routed(self.handle, x, topk_ids, topk_w, T, k, out, accumulate, ws, n, routing, stream)
+        return out
+
     def sync(self, stream=None):
         B.moe_sync_status(self.handle, stream)
 

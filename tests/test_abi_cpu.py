@@ -80,6 +80,16 @@ def test_host_side_argument_checks_without_gpu(built):
     assert L.moe_forward(None, None, None, 1, 1, None, 0, None, 0, None, None) == b.MOE_EINVAL
     assert L.moe_dense_sliced_forward(None, None, 1, None, 0, None, 0, None) == b.MOE_EINVAL
     assert L.moe_sync_status(None, None) == b.MOE_EINVAL
+    assert L.moe_forward_routed(None, None, None, None, 1, 1, None, 0, None, 0, None, None) == b.MOE_EINVAL
+    # sigmoid routing: sizes and pointers are checked before any CUDA call
+    assert L.moe_route_sigmoid(None, None, 4, 0, 1, 1.0, None, None, None) == b.MOE_EINVAL
+    assert L.moe_route_sigmoid(None, None, 4, 1025, 1, 1.0, None, None, None) == b.MOE_EINVAL
+    assert L.moe_route_sigmoid(None, None, 4, 8, 9, 1.0, None, None, None) == b.MOE_EINVAL
+    assert L.moe_route_sigmoid(None, None, 4, 64, 33, 1.0, None, None, None) == b.MOE_EINVAL
+    assert L.moe_route_sigmoid(None, None, -1, 8, 2, 1.0, None, None, None) == b.MOE_EINVAL
+    assert L.moe_route_sigmoid(None, None, 4, 8, 2, 1.0, None, None, None) == b.MOE_EINVAL
+    assert b"NULL" in L.moe_last_error()
+    assert L.moe_route_sigmoid(None, None, 0, 8, 2, 1.0, None, None, None) == b.MOE_OK
     L.moe_free(None)  # no-op
 
 
