@@ -9,8 +9,9 @@
  *     k largest and renormalise over them, so that w_tj = exp(l_tj - l_max) /
  *     sum_{j' < k} exp(l_tj' - l_max).  Larger logits come first; equal logits
  *     (+0 equals -0) go to the lower expert index; NaN ranks below every
- *     number.  Routing enters the expert computation as expert IDs plus
- *     weights ("Cascadia: Resident 975B MoE Inference on Eleven AI PCs" §3.1).
+ *     number.  The expert computation sees the routing only as one expert id
+ *     and one weight per selection ("Cascadia: Resident 975B MoE Inference on
+ *     Eleven AI PCs" §3.1).
  *  2. Grouping.  Slots s = t*k + j are grouped by expert with a stable counting
  *     sort (ascending slot order within an expert) -- the expert-major
  *     arrangement of the same paper's §3.1.
@@ -157,9 +158,9 @@ MoeStatus moe_forward(MoeHandle *h, const void *x_bf16, const float *router_logi
 
 /* One routed MoE layer on T tokens for routing given by the caller: the
  * interface of "Cascadia: Resident 975B MoE Inference on Eleven AI PCs" §3.1,
- * where the router's results enter the expert computation as expert IDs and
- * routing weights (the shared experts are added with weight 1, as in
- * moe_forward).
+ * whose expert computation receives one expert id and one weight per
+ * selection from a router that runs elsewhere (the shared experts are added
+ * with weight 1, as in moe_forward).
  *  topk_ids [T][k] int32 in [0, E), 4-byte aligned (an expert may appear more
  *           than once for a token; each occurrence is its own slot)
  *  topk_w   [T][k] float, 4-byte aligned, used as given

@@ -2,8 +2,8 @@
 // the stable token permutation.
 //
 // Routing follows "Cascadia: Resident 975B MoE Inference on Eleven AI PCs"
-// §3.1: routing results enter the expert computation as expert IDs plus
-// weights, and the expert work is arranged expert-major.  The selection is a
+// §3.1: the expert computation sees the routing only as one expert id and one
+// weight per selection, and the expert work is arranged expert-major.  The selection is a
 // softmax top-k with renormalisation over the k kept experts.
 #include "moe_internal.cuh"
 
@@ -103,8 +103,8 @@ cudaError_t launch_router(const float *logits, int T, int E, int k, int *ids, fl
 
 // ---------------------------------------------------------------- routing given by the caller
 //
-// "Cascadia: Resident 975B MoE Inference on Eleven AI PCs" §3.1: routing
-// enters the expert computation as expert IDs and weights.  The caller's
+// "Cascadia: Resident 975B MoE Inference on Eleven AI PCs" §3.1: the router
+// hands the expert computation expert ids and their weights.  The caller's
 // arrays are copied into the call's routing arrays; an ID outside [0, E)
 // records DEV_ERR_BOUNDS (reported by moe_sync_status) and is replaced by
 // expert 0 with weight 0, so that everything after it stays in bounds.

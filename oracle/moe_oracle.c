@@ -19,7 +19,7 @@
  *  [C31] "Cascadia: Resident 975B MoE Inference on Eleven AI PCs" §3.1: each
  *        expert is a SwiGLU FFN (gate/up projections, SwiGLU, down projection),
  *        expert outputs are combined by a weighted reduction with the routing
- *        weights, routing enters as expert IDs plus weights, and shared experts
+ *        weights, the experts see the routing only as ids and weights, and shared experts
  *        are always included.
  *  [C33] same paper §3.3, Eq. (1): y_i = sum_e w_ie E_e(x_i).
  *  [C34] same paper §3.4, Eq. (2): the dense FFN equals the sum of its
