@@ -193,6 +193,41 @@ MoeStatus moe_forward_routed(MoeHandle *h, const void *x_bf16, const int32_t *to
 MoeStatus moe_route_sigmoid(const float *router_logits, const float *bias, int T, int E, int k, float routed_scale,
                             int32_t *topk_ids, float *topk_w, void *cuda_stream);
 
+/* ---- CUDA graphs: one forward call captured with fixed buffers ----
+ *
+ * A captured call replays with one launch: the counter clear, the layer's
+ * kernels and their dependencies become one graph.  For a routed handle give
+ * either router_logits (moe_forward) or topk_ids + topk_w (moe_forward_routed);
+ * for a dense handle neither (moe_dense_sliced_forward).  The other arguments
+ * are those of the captured call.  The graph keeps every pointer it was
+ * created with: write each step's inputs into the same x / logits / ids /
+ * weights buffers before moe_graph_launch, read out afterwards, and keep the
+ * buffers and the workspace alive and unused by other calls while a launch is
+ * in flight.  T is fixed per graph.  To serve a varying number of tokens,
+ * create one graph per bucket of T and pad: with ids + weights, give padded
+ * rows an id some real row uses and weight 0, so that they add no expert
+ * (their own out rows are to be ignored; real rows agree with an unpadded call
+ * within the layer's error bound, as the grouping, and with it the order of
+ * some sums, can differ).
+ * Capture runs on a private stream in this thread's capture mode; nothing is
+ * enqueued by moe_graph_create.  Argument errors are those of the captured
+ * call.
+ * Errors: MOE_EINVAL (NULL graph pointer or handle, T < 1, both or neither of
+ * logits and ids for a routed handle, or any error of the captured call),
+ * MOE_EWORKSPACE, MOE_EDEVICE, MOE_ENOMEM, MOE_ECUDA.  *graph is set only on
+ * MOE_OK. */
+typedef struct MoeGraph MoeGraph;
+MoeStatus moe_graph_create(MoeHandle *h, const void *x_bf16, const float *router_logits, const int32_t *topk_ids,
+                           const float *topk_w, int T, int k, float *out_fp32, int accumulate, void *workspace,
+                           size_t ws_bytes, MoeGraph **graph);
+
+/* Replays a captured call on cuda_stream.  Errors: MOE_EINVAL (NULL graph),
+ * MOE_EDEVICE (an earlier call reported a device error), MOE_ECUDA. */
+MoeStatus moe_graph_launch(MoeGraph *graph, void *cuda_stream);
+
+/* Frees a graph (NULL is a no-op).  No launch of it may be in flight. */
+void moe_graph_free(MoeGraph *graph);
+
 /* The dense FFN of a dense handle on T tokens, as the sum of its all-active
  * slices ("Cascadia" §3.4, Eq. 2).  Arguments as for moe_forward; the
  * workspace size is moe_workspace_bytes(h, T, 0).

@@ -23,7 +23,8 @@ MOE_W_MXFP4, MOE_W_BF16 = 0, 1
 # every symbol include/moe.h declares
 EXPORTED = ("moe_load_weights", "moe_workspace_bytes", "moe_forward", "moe_forward_routed",
             "moe_route_sigmoid", "moe_dense_sliced_forward", "moe_sync_status", "moe_profile_enable",
-            "moe_profile_read", "moe_route_static", "moe_last_error", "moe_free")
+            "moe_profile_read", "moe_route_static", "moe_graph_create", "moe_graph_launch", "moe_graph_free",
+            "moe_last_error", "moe_free")
 STAGES = ("routing", "grouping", "gate_up", "down", "combine", "layer")
 
 
@@ -65,6 +66,12 @@ def _load():
     L.moe_forward_routed.restype = ci
     L.moe_route_sigmoid.argtypes = [vp, vp, ci, ci, ci, ctypes.c_float, vp, vp, vp]
     L.moe_route_sigmoid.restype = ci
+    L.moe_graph_create.argtypes = [vp, vp, vp, vp, vp, ci, ci, vp, ci, vp, sz, ctypes.POINTER(vp)]
+    L.moe_graph_create.restype = ci
+    L.moe_graph_launch.argtypes = [vp, vp]
+    L.moe_graph_launch.restype = ci
+    L.moe_graph_free.argtypes = [vp]
+    L.moe_graph_free.restype = None
     L.moe_dense_sliced_forward.argtypes = [vp, vp, ci, vp, ci, vp, sz, vp]
     L.moe_dense_sliced_forward.restype = ci
     L.moe_sync_status.argtypes = [vp, vp]
@@ -142,6 +149,22 @@ def moe_route_sigmoid(router_logits, bias, T: int, E: int, k: int, routed_scale:
                       stream=None) -> None:
     _check(lib.moe_route_sigmoid(_ptr(router_logits), _ptr(bias), T, E, k, float(routed_scale), _ptr(topk_ids),
                                  _ptr(topk_w), _stream(stream)))
+
+
+def moe_graph_create(handle: int, x_bf16, router_logits, topk_ids, topk_w, T: int, k: int, out_fp32,
+                     accumulate: bool, workspace, ws_bytes: int) -> int:
+    g = ctypes.c_void_p()
+    _check(lib.moe_graph_create(handle, _ptr(x_bf16), _ptr(router_logits), _ptr(topk_ids), _ptr(topk_w), T, k,
+                                _ptr(out_fp32), int(bool(accumulate)), _ptr(workspace), ws_bytes, ctypes.byref(g)))
+    return g.value
+
+
+def moe_graph_launch(graph: int, stream=None) -> None:
+    _check(lib.moe_graph_launch(graph, _stream(stream)))
+
+
+def moe_graph_free(graph: int) -> None:
+    lib.moe_graph_free(graph)
 
 
 def moe_dense_sliced_forward(handle: int, x_bf16, T: int, out_fp32, accumulate: bool, workspace, ws_bytes: int,

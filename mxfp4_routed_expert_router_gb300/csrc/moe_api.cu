@@ -483,6 +483,99 @@ MoeStatus moe_sync_status(MoeHandle *h, void *cuda_stream)
     return MOE_OK;
 }
 
+// ---------------------------------------------------------------- CUDA graphs
+
+struct MoeGraph {
+    MoeHandle *h = nullptr;
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+};
+
+MoeStatus moe_graph_create(MoeHandle *h, const void *x_bf16, const float *router_logits, const int32_t *topk_ids,
+                           const float *topk_w, int T, int k, float *out_fp32, int accumulate, void *workspace,
+                           size_t ws_bytes, MoeGraph **graph)
+{
+    if (!graph)
+        return fail(MOE_EINVAL, "moe_graph_create: NULL graph pointer");
+    *graph = nullptr;
+    if (!h)
+        return fail(MOE_EINVAL, "moe_graph_create: NULL handle");
+    if (T < 1)
+        return fail(MOE_EINVAL, "moe_graph_create: T = %d, a graph needs at least one token", T);
+    if (h->E > 0 && !router_logits == !topk_ids)
+        return fail(MOE_EINVAL, "moe_graph_create: give either router logits or ids + weights");
+    // capture the call on a private stream, in this thread's capture mode only
+    cudaStream_t cs;
+    cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaStreamCreateWithFlags");
+    if ((e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal)) != cudaSuccess) {
+        cudaStreamDestroy(cs);
+        return cuda_fail(e, "cudaStreamBeginCapture");
+    }
+    MoeStatus st;
+    if (h->E == 0)
+        st = moe_dense_sliced_forward(h, x_bf16, T, out_fp32, accumulate, workspace, ws_bytes, cs);
+    else if (router_logits)
+        st = moe_forward(h, x_bf16, router_logits, T, k, out_fp32, accumulate, workspace, ws_bytes, nullptr, cs);
+    else
+        st = moe_forward_routed(h, x_bf16, topk_ids, topk_w, T, k, out_fp32, accumulate, workspace, ws_bytes,
+                                nullptr, cs);
+    cudaGraph_t g = nullptr;
+    e = cudaStreamEndCapture(cs, &g);
+    cudaStreamDestroy(cs);
+    if (st != MOE_OK) {
+        if (g)
+            cudaGraphDestroy(g);
+        return st;  // the failing call has set the message
+    }
+    if (e != cudaSuccess || !g) {
+        if (g)
+            cudaGraphDestroy(g);
+        return cuda_fail(e != cudaSuccess ? e : cudaErrorStreamCaptureInvalidated, "cudaStreamEndCapture");
+    }
+    cudaGraphExec_t ex = nullptr;
+    if ((e = cudaGraphInstantiate(&ex, g, 0)) != cudaSuccess) {
+        cudaGraphDestroy(g);
+        return cuda_fail(e, "cudaGraphInstantiate");
+    }
+    MoeGraph *mg = new (std::nothrow) MoeGraph;
+    if (!mg) {
+        cudaGraphExecDestroy(ex);
+        cudaGraphDestroy(g);
+        return fail(MOE_ENOMEM, "moe_graph_create: out of host memory");
+    }
+    mg->h = h;
+    mg->graph = g;
+    mg->exec = ex;
+    *graph = mg;
+    return MOE_OK;
+}
+
+MoeStatus moe_graph_launch(MoeGraph *g, void *cuda_stream)
+{
+    if (!g)
+        return fail(MOE_EINVAL, "moe_graph_launch: NULL graph");
+    MoeStatus s = check_pending(g->h);
+    if (s != MOE_OK)
+        return s;
+    cudaError_t e = cudaGraphLaunch(g->exec, (cudaStream_t)cuda_stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGraphLaunch");
+    return MOE_OK;
+}
+
+void moe_graph_free(MoeGraph *g)
+{
+    if (!g)
+        return;
+    if (g->exec)
+        cudaGraphExecDestroy(g->exec);
+    if (g->graph)
+        cudaGraphDestroy(g->graph);
+    delete g;
+}
+
 MoeStatus moe_profile_enable(MoeHandle *h, int enable)
 {
     if (!h)

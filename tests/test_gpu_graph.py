@@ -1,0 +1,124 @@
+"""GPU: forward calls captured into CUDA graphs (moe_graph_create / launch).
+
+A replay equals the eager call bit for bit on the same inputs, picks up new
+inputs written into the captured buffers, and a padded row bucket (padded rows
+routed to an expert a real row uses, with weight 0) gives the real rows of the
+unpadded call within the layer's bound.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from parity_util import TOL, rel_err
+
+from mxfp4_routed_expert_router_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def _mods():
+    from mxfp4_routed_expert_router_gb300 import binding, layer
+    return binding, layer
+
+
+CASES = [
+    wl.custom("graph_T1_H320_I192_E16_S1_k4", 1, 320, 192, 16, 1, 4, seed=51),     # single kernel, two-token class
+    wl.custom("graph_T6_H320_I192_E16_S1_k4", 6, 320, 192, 16, 1, 4, seed=52),     # single kernel, local routing
+    wl.custom("graph_T100_H288_I160_E16_S1_k4", 100, 288, 160, 16, 1, 4, seed=53),  # tensor-core path
+]
+
+
+@pytest.mark.parametrize("cfg", CASES, ids=lambda c: c.name)
+def test_graph_replay_equals_eager_and_takes_new_inputs(cfg):
+    B, layer = _mods()
+    L = layer.MoeLayer(cfg)
+    T, k = cfg.T, cfg.k
+    x = layer.bf16_tensor(wl.tokens(cfg))
+    lg = torch.from_numpy(wl.router_logits(cfg)).cuda()
+    ref = L.forward(x, lg, k).clone()
+    out = torch.full((T, cfg.hidden), float("nan"), dtype=torch.float32, device="cuda")
+    ws, n = L.workspace(T, k)
+    g = B.moe_graph_create(L.handle, x, lg, None, None, T, k, out, False, ws, n)
+    try:
+        for _ in range(3):
+            B.moe_graph_launch(g)
+        L.sync()
+        assert torch.equal(out, ref)
+        # new inputs in the same buffers
+        cfg2 = dataclasses.replace(cfg, seed=cfg.seed + 100)  # other tokens and logits, same layer
+        x.copy_(layer.bf16_tensor(wl.tokens(cfg2)))
+        lg.copy_(torch.from_numpy(wl.router_logits(cfg2)))
+        B.moe_graph_launch(g)
+        L.sync()
+        got = out.clone()
+        ref2 = L.forward(x, lg, k).clone()
+        L.sync()
+        assert torch.equal(got, ref2)
+    finally:
+        B.moe_graph_free(g)
+    L.free()
+
+
+def test_graph_padded_bucket_with_caller_routing():
+    B, layer = _mods()
+    cfg = wl.custom("graph_bucket_T3_H320_I192_E16_S1_k4", 3, 320, 192, 16, 1, 4, seed=54)
+    L = layer.MoeLayer(cfg)
+    rng = np.random.default_rng(54)
+    ids = np.stack([rng.choice(16, 4, replace=False) for _ in range(3)]).astype(np.int32)
+    w = rng.uniform(0.1, 1.0, (3, 4)).astype(np.float32)
+    x = wl.tokens(cfg)
+    ref = L.forward_routed(layer.bf16_tensor(x), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda()).clone()
+    L.sync()
+    # bucket of 4 rows: the padded row repeats row 0's experts with weight 0
+    Tb = 4
+    xb = torch.zeros((Tb, cfg.hidden), dtype=torch.bfloat16, device="cuda")
+    xb[:3] = layer.bf16_tensor(x)
+    idb = torch.from_numpy(np.concatenate([ids, ids[:1]])).cuda()
+    wb = torch.from_numpy(np.concatenate([w, np.zeros((1, 4), np.float32)])).cuda()
+    out = torch.empty((Tb, cfg.hidden), dtype=torch.float32, device="cuda")
+    ws, n = L.workspace(Tb, 4)
+    g = B.moe_graph_create(L.handle, xb, None, idb, wb, Tb, 4, out, False, ws, n)
+    try:
+        B.moe_graph_launch(g)
+        L.sync()
+        assert rel_err(out[:3].cpu().numpy(), ref.cpu().numpy()) <= TOL
+    finally:
+        B.moe_graph_free(g)
+    L.free()
+
+
+def test_graph_dense_slices():
+    B, layer = _mods()
+    cfg = wl.dense(1, "mxfp4")
+    L = layer.MoeLayer(cfg)
+    x = layer.bf16_tensor(wl.tokens(cfg))
+    ref = L.forward(x, None).clone()
+    out = torch.empty_like(ref)
+    ws, n = L.workspace(1, 0)
+    g = B.moe_graph_create(L.handle, x, None, None, None, 1, 0, out, False, ws, n)
+    try:
+        B.moe_graph_launch(g)
+        L.sync()
+        assert torch.equal(out, ref)
+    finally:
+        B.moe_graph_free(g)
+    L.free()
+
+
+def test_graph_rejects_both_routings():
+    B, layer = _mods()
+    cfg = CASES[0]
+    L = layer.MoeLayer(cfg)
+    x = layer.bf16_tensor(wl.tokens(cfg))
+    lg = torch.from_numpy(wl.router_logits(cfg)).cuda()
+    ids = torch.zeros((1, 4), dtype=torch.int32, device="cuda")
+    w = torch.zeros((1, 4), dtype=torch.float32, device="cuda")
+    out = torch.empty((1, cfg.hidden), dtype=torch.float32, device="cuda")
+    ws, n = L.workspace(1, 4)
+    with pytest.raises(B.MoeError):
+        B.moe_graph_create(L.handle, x, lg, ids, w, 1, 4, out, False, ws, n)
+    with pytest.raises(B.MoeError):
+        B.moe_graph_create(L.handle, x, None, None, None, 1, 4, out, False, ws, n)
+    L.free()
