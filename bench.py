@@ -271,6 +271,26 @@ def run_ours(args, cfg, rank, world):
         e.synchronize()
         e2e_times.append(s.elapsed_time(e))
     e2e_ms = sum(e2e_times) / len(e2e_times)
+
+    # the same step replayed from a CUDA graph of the call (moe_graph_create):
+    # device time per replay, L2 flushed between replays like the timed steps
+    ws, nws = L.workspace(cfg.T, 0 if cfg.dense else cfg.k)
+    graph = B.moe_graph_create(L.handle, x, logits, None, None, cfg.T, 0 if cfg.dense else cfg.k, out, False, ws,
+                               nws)
+    g_times = []
+    try:
+        for i in range(args.warmup + max(3, min(args.steps, 20))):
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            B.moe_graph_launch(graph, stream)
+            e.record(stream)
+            e.synchronize()
+            if i >= args.warmup:
+                g_times.append(s.elapsed_time(e))
+    finally:
+        B.moe_graph_free(graph)
+    graph_ms = sum(g_times) / len(g_times)
     h2d = x_bits.nbytes + (0 if cfg.dense else cfg.T * cfg.n_experts * 4)
     d2h = cfg.T * cfg.hidden * 4
 
@@ -330,6 +350,8 @@ def run_ours(args, cfg, rank, world):
         "roofline": roof,
         "e2e": {"value": world * cfg.T / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "graph": {"value": world * cfg.T / (graph_ms * 1e-3), "unit": "tokens/s", "ms_per_step": graph_ms,
+                  "note": "the same call replayed from a CUDA graph (moe_graph_create / moe_graph_launch)"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
