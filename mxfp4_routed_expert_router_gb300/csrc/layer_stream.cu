@@ -11,24 +11,29 @@
 // workstation", section "MXFP4 is not NVFP4, and the difference matters on
 // Ampere"):
 //
-//  phase 0a  each CTA routes its tokens (softmax top-k, renormalised) and
-//            writes their FP16 rows x16 (per-token power-of-two scale);
-//            a grid-wide counter tells every CTA when all tokens are done.
+//  phase 0a  tokens are routed (softmax top-k, renormalised; or the caller's
+//            ids and weights are copied and checked) and their FP16 rows x16
+//            written (per-token power-of-two scale).  With at most 8 tokens
+//            every CTA routes every token itself; otherwise each CTA routes
+//            its own and a grid-wide counter tells every CTA when all are done.
 //  phase 0b  every CTA builds the expert histogram, positions and the stable
 //            permutation in shared memory (CTA 0 also publishes them), then
 //            the work list: (gate|up, group, 128-row tile, token tile) items
 //            followed by (down, ...) items.
 //  stream    warp 0 takes items from a grid-wide counter and streams each
 //            item's weight chunks (one bulk copy per stage) plus its token
-//            rows (one bulk copy per row) into a ring of shared-memory stages;
-//            8 compute warps (16 weight rows each, the full K) decode MXFP4
-//            in registers straight into warp-level MMA fragments (FP16
-//            operands, FP32 accumulation, the E8M0 block scales applied in
-//            FP32 to each 32-wide block's partial sum).  gate|up epilogues
-//            write h (FP16 hi + lo, scaled per 64-feature block) and count
-//            finished warps per group; a down item's token rows are copied
-//            only once its group's h is complete, while its weights are
-//            already streaming.
+//            rows (one bulk copy per row and plane) into a ring of
+//            shared-memory stages sized by the item's tile class; 8 compute
+//            warps (16 weight rows each, the full K) decode MXFP4 in registers
+//            straight into warp-level MMA fragments (FP16 operands, FP32
+//            accumulation, the E8M0 block scales applied in FP32 to each
+//            32-wide block's partial sum).  gate|up epilogues write h (FP16
+//            hi + lo, scaled per 64-feature block) and hand the item to warp
+//            9, which publishes it to the other CTAs with one release; a
+//            down item's token rows are copied only once its group's h is
+//            complete, while its weights are already streaming.  Down items
+//            of at most four tokens (in the kernels for up to 16 tokens)
+//            carry each token's hi and lo planes in adjacent MMA columns.
 //  combine   once every CTA has counted its items done, all warps of the
 //            grid sum (token, 128-feature) blocks of y into out in a fixed
 //            order (j ascending, then shared groups), so the result does not
