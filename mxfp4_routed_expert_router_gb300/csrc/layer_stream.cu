@@ -703,14 +703,25 @@ __device__ __forceinline__ LsItem ls_item(int u, int total_gu, int rt_gu, int rt
     return it;
 }
 
-// in the kernels for up to 16 tokens, a down item of at most four tokens
-// (MXFP4) packs each token's h hi and lo planes into adjacent columns of its
-// 8-token MMA tile (the wider kernels keep one code path for class 1: the
-// second one cost them registers and measured slower)
+// a down item of at most four tokens (MXFP4) packs each token's h hi and lo
+// planes into adjacent columns of its 8-token MMA tile, except in the kernel
+// for up to 64 tokens (NT = 8), whose batches hold many down items of five to
+// eight tokens: there both class-1 variants cost registers, and moving those
+// items to class 2 measured slower
 template <int WFMT, int NT>
 __device__ __forceinline__ bool ls_packed(const LsItem &it)
 {
-    return WFMT == FMT_MXFP4 && NT <= 2 && !it.gu && it.nvalid <= 4;
+    return WFMT == FMT_MXFP4 && NT != 8 && !it.gu && it.nvalid <= 4;
+}
+
+// tile class of an item: in the kernel for up to 32 tokens (NT = 4) down items
+// of five to eight tokens take class 2, so that class 1 has one code path (the
+// packed one, which runs gate|up items unchanged)
+template <int WFMT, int NT>
+__device__ __forceinline__ int ls_nti_item(const LsItem &it)
+{
+    const int c = ls_nti<NT>(it.nvalid);
+    return WFMT == FMT_MXFP4 && NT == 4 && !it.gu && it.nvalid > 4 && c == 1 ? 2 : c;
 }
 
 // token of row r of an item: routed positions look it up (tokp: token of each
@@ -1202,7 +1213,7 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
             if (lane == 0)
                 nxt = (int)gridDim.x + atomicAdd(&a.sync[SY_WORK], 1);
             const LsItem it = ls_item<ROWS>(u, total_gu, rt_gu, rt_dn, a.G, gcnt, gstart, tpre);
-            const int nti = ls_nti<NT>(it.nvalid);  // the item's tile class: its stage geometry
+            const int nti = ls_nti_item<WFMT, NT>(it);  // the item's tile class: its stage geometry
             const int irows = C::res_rows(nti);
             const int CH = it.gu ? C::ch_gu(nti) : C::ch_dn(nti);
             const int kch = it.gu ? a.gu_kchunks : a.dn_kchunks;
@@ -1349,20 +1360,22 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
                 break;
             const LsItem it = ls_item<ROWS>(h0.x, total_gu, rt_gu, rt_dn, a.G, gcnt, gstart, tpre);
             const int gu_idx = it.gu ? gu_i++ : 0;
-            const int nti = ls_nti<NT>(it.nvalid);
+            const int nti = ls_nti_item<WFMT, NT>(it);
 #define LS_ITEM(F_, ...)                                                                                      \
     F_<WFMT, NT, __VA_ARGS__>(a, it, smem, full, empty, rc, abort_flag, sorted, xs_s, hmaxb, hmax_bar, gu_idx,   \
                               pub_full, pub_empty, pub_g)
             if (NT <= 1 || nti == 1) {
                 // class 1: the packed-down variant also runs gate|up items (identical there)
-                constexpr bool PKV = WFMT == FMT_MXFP4 && NT <= 2;  // the packed-down variant exists
-                if constexpr (NT == 0) {
-                    ok = LS_ITEM(ls_compute_item, 1, PKV);
-                } else {
+                if constexpr (NT == 0 || NT == 4) {
+                    ok = LS_ITEM(ls_compute_item, 1, WFMT == FMT_MXFP4);
+                } else if constexpr (NT <= 2) {
+                    constexpr bool PKV = WFMT == FMT_MXFP4;
                     if (PKV && (it.gu || ls_packed<WFMT, NT>(it)))
                         ok = LS_ITEM(ls_compute_item, 1, PKV);
                     else
                         ok = LS_ITEM(ls_compute_item, 1, false);
+                } else {
+                    ok = LS_ITEM(ls_compute_item, 1, false);
                 }
             } else if (NT == 2 || nti == 2)
                 ok = LS_ITEM(ls_compute_item_wide, NT < 2 ? 1 : 2);

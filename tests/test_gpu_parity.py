@@ -73,6 +73,8 @@ SMALL = [
     # streaming path, items of every tile class: groups of 9-16 and 17-32 tokens
     wl.custom("stream_classes_T40_H256_I192_E16_S1_k4", 40, 256, 192, 16, 1, 4, seed=33),
     wl.custom("stream_classes_T21_H320_I128_E4_S1_k3", 21, 320, 128, 4, 1, 3, seed=35),
+    # 32-token kernel: down items of 1-4 tokens (packed) and of 5-8 and 11 tokens (class 2)
+    wl.custom("stream_T30_H256_I128_E24_S1_k4", 30, 256, 128, 24, 1, 4, seed=39),
 ]
 
 
