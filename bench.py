@@ -291,6 +291,7 @@ def run_ours(args, cfg, rank, world):
     finally:
         B.moe_graph_free(graph)
     graph_ms = sum(g_times) / len(g_times)
+
     h2d = x_bits.nbytes + (0 if cfg.dense else cfg.T * cfg.n_experts * 4)
     d2h = cfg.T * cfg.hidden * 4
 

@@ -209,6 +209,10 @@ MoeStatus moe_route_sigmoid(const float *router_logits, const float *bias, int T
  * (their own out rows are to be ignored; real rows agree with an unpadded call
  * within the layer's error bound, as the grouping, and with it the order of
  * some sums, can differ).
+ * host (may be NULL; each member may be NULL) adds copies to the graph: the
+ * step's x, logits or ids and weights from PINNED host memory into the
+ * captured device buffers before the call, and out back to pinned host
+ * memory after it, so that one launch runs a whole serving step.
  * Capture runs on a private stream in this thread's capture mode; nothing is
  * enqueued by moe_graph_create.  Argument errors are those of the captured
  * call.
@@ -217,9 +221,16 @@ MoeStatus moe_route_sigmoid(const float *router_logits, const float *bias, int T
  * MOE_EWORKSPACE, MOE_EDEVICE, MOE_ENOMEM, MOE_ECUDA.  *graph is set only on
  * MOE_OK. */
 typedef struct MoeGraph MoeGraph;
+typedef struct {
+    const void *x_host;         /* [T][H] BF16, copied into x_bf16 */
+    const float *logits_host;   /* [T][E], copied into router_logits */
+    const int32_t *ids_host;    /* [T][k], copied into topk_ids */
+    const float *w_host;        /* [T][k], copied into topk_w */
+    float *out_host;            /* [T][H], receives out_fp32 */
+} MoeHostIO;
 MoeStatus moe_graph_create(MoeHandle *h, const void *x_bf16, const float *router_logits, const int32_t *topk_ids,
                            const float *topk_w, int T, int k, float *out_fp32, int accumulate, void *workspace,
-                           size_t ws_bytes, MoeGraph **graph);
+                           size_t ws_bytes, const MoeHostIO *host, MoeGraph **graph);
 
 /* Replays a captured call on cuda_stream.  Errors: MOE_EINVAL (NULL graph),
  * MOE_EDEVICE (an earlier call reported a device error), MOE_ECUDA. */

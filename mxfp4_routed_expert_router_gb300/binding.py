@@ -44,6 +44,11 @@ class MoeMx(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
 
 
+class MoeHostIO(ctypes.Structure):
+    _fields_ = [("x_host", ctypes.c_void_p), ("logits_host", ctypes.c_void_p), ("ids_host", ctypes.c_void_p),
+                ("w_host", ctypes.c_void_p), ("out_host", ctypes.c_void_p)]
+
+
 class MoeRoutingOut(ctypes.Structure):
     _fields_ = [("topk_ids", ctypes.c_void_p), ("topk_w", ctypes.c_void_p), ("expert_offsets", ctypes.c_void_p),
                 ("sorted_slot", ctypes.c_void_p), ("slot_pos", ctypes.c_void_p)]
@@ -66,7 +71,8 @@ def _load():
     L.moe_forward_routed.restype = ci
     L.moe_route_sigmoid.argtypes = [vp, vp, ci, ci, ci, ctypes.c_float, vp, vp, vp]
     L.moe_route_sigmoid.restype = ci
-    L.moe_graph_create.argtypes = [vp, vp, vp, vp, vp, ci, ci, vp, ci, vp, sz, ctypes.POINTER(vp)]
+    L.moe_graph_create.argtypes = [vp, vp, vp, vp, vp, ci, ci, vp, ci, vp, sz, ctypes.POINTER(MoeHostIO),
+                                   ctypes.POINTER(vp)]
     L.moe_graph_create.restype = ci
     L.moe_graph_launch.argtypes = [vp, vp]
     L.moe_graph_launch.restype = ci
@@ -152,10 +158,16 @@ def moe_route_sigmoid(router_logits, bias, T: int, E: int, k: int, routed_scale:
 
 
 def moe_graph_create(handle: int, x_bf16, router_logits, topk_ids, topk_w, T: int, k: int, out_fp32,
-                     accumulate: bool, workspace, ws_bytes: int) -> int:
+                     accumulate: bool, workspace, ws_bytes: int, x_host=None, logits_host=None, ids_host=None,
+                     w_host=None, out_host=None) -> int:
+    """Capture one forward call into a CUDA graph; the *_host buffers (pinned host memory, optional) add the
+    step's input and output copies to the graph."""
+    io = MoeHostIO(_ptr(x_host), _ptr(logits_host), _ptr(ids_host), _ptr(w_host), _ptr(out_host))
+    any_io = any(v is not None for v in (x_host, logits_host, ids_host, w_host, out_host))
     g = ctypes.c_void_p()
     _check(lib.moe_graph_create(handle, _ptr(x_bf16), _ptr(router_logits), _ptr(topk_ids), _ptr(topk_w), T, k,
-                                _ptr(out_fp32), int(bool(accumulate)), _ptr(workspace), ws_bytes, ctypes.byref(g)))
+                                _ptr(out_fp32), int(bool(accumulate)), _ptr(workspace), ws_bytes,
+                                ctypes.byref(io) if any_io else None, ctypes.byref(g)))
     return g.value
 
 

@@ -493,7 +493,7 @@ struct MoeGraph {
 
 MoeStatus moe_graph_create(MoeHandle *h, const void *x_bf16, const float *router_logits, const int32_t *topk_ids,
                            const float *topk_w, int T, int k, float *out_fp32, int accumulate, void *workspace,
-                           size_t ws_bytes, MoeGraph **graph)
+                           size_t ws_bytes, const MoeHostIO *host, MoeGraph **graph)
 {
     if (!graph)
         return fail(MOE_EINVAL, "moe_graph_create: NULL graph pointer");
@@ -513,6 +513,23 @@ MoeStatus moe_graph_create(MoeHandle *h, const void *x_bf16, const float *router
         cudaStreamDestroy(cs);
         return cuda_fail(e, "cudaStreamBeginCapture");
     }
+    // optional copies of the step's inputs from pinned host memory, before the call
+    auto h2d = [&](void *dst, const void *src, size_t bytes) {
+        return dst && src ? cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, cs) : cudaSuccess;
+    };
+    const size_t tk = (size_t)T * (size_t)(k > 0 ? k : 0);
+    if (host && (e = h2d((void *)x_bf16, host->x_host, (size_t)T * h->H * 2)) == cudaSuccess &&
+        (e = h2d((void *)router_logits, host->logits_host, (size_t)T * h->E * sizeof(float))) == cudaSuccess &&
+        (e = h2d((void *)topk_ids, host->ids_host, tk * sizeof(int32_t))) == cudaSuccess)
+        e = h2d((void *)topk_w, host->w_host, tk * sizeof(float));
+    if (e != cudaSuccess) {
+        cudaGraph_t g0 = nullptr;
+        cudaStreamEndCapture(cs, &g0);
+        if (g0)
+            cudaGraphDestroy(g0);
+        cudaStreamDestroy(cs);
+        return cuda_fail(e, "moe_graph_create: input copy");
+    }
     MoeStatus st;
     if (h->E == 0)
         st = moe_dense_sliced_forward(h, x_bf16, T, out_fp32, accumulate, workspace, ws_bytes, cs);
@@ -521,6 +538,11 @@ MoeStatus moe_graph_create(MoeHandle *h, const void *x_bf16, const float *router
     else
         st = moe_forward_routed(h, x_bf16, topk_ids, topk_w, T, k, out_fp32, accumulate, workspace, ws_bytes,
                                 nullptr, cs);
+    // optional copy of the result to pinned host memory, after the call
+    if (st == MOE_OK && host && host->out_host &&
+        (e = cudaMemcpyAsync(host->out_host, out_fp32, (size_t)T * h->H * sizeof(float), cudaMemcpyDeviceToHost,
+                             cs)) != cudaSuccess)
+        st = cuda_fail(e, "moe_graph_create: output copy");
     cudaGraph_t g = nullptr;
     e = cudaStreamEndCapture(cs, &g);
     cudaStreamDestroy(cs);

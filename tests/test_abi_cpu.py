@@ -91,8 +91,9 @@ def test_host_side_argument_checks_without_gpu(built):
     assert b"NULL" in L.moe_last_error()
     assert L.moe_route_sigmoid(None, None, 0, 8, 2, 1.0, None, None, None) == b.MOE_OK
     g = ctypes.c_void_p()
-    assert L.moe_graph_create(None, None, None, None, None, 1, 1, None, 0, None, 0, ctypes.byref(g)) == b.MOE_EINVAL
-    assert L.moe_graph_create(None, None, None, None, None, 1, 1, None, 0, None, 0, None) == b.MOE_EINVAL
+    assert L.moe_graph_create(None, None, None, None, None, 1, 1, None, 0, None, 0, None, ctypes.byref(g)) == \
+        b.MOE_EINVAL
+    assert L.moe_graph_create(None, None, None, None, None, 1, 1, None, 0, None, 0, None, None) == b.MOE_EINVAL
     assert L.moe_graph_launch(None, None) == b.MOE_EINVAL
     L.moe_graph_free(None)  # no-op
     L.moe_free(None)  # no-op

@@ -89,6 +89,43 @@ def test_graph_padded_bucket_with_caller_routing():
     L.free()
 
 
+def test_graph_with_host_copies():
+    # one launch runs the whole step: x and logits in from pinned host memory, out back
+    B, layer = _mods()
+    cfg = CASES[0]
+    L = layer.MoeLayer(cfg)
+    T, k = cfg.T, cfg.k
+    x_bits = wl.tokens(cfg)
+    lg_np = wl.router_logits(cfg)
+    ref = L.forward(layer.bf16_tensor(x_bits), torch.from_numpy(lg_np).cuda(), k).clone()
+    L.sync()
+    hx = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hl = torch.from_numpy(lg_np).pin_memory()
+    hout = torch.full((T, cfg.hidden), float("nan"), dtype=torch.float32).pin_memory()
+    x = torch.empty((T, cfg.hidden), dtype=torch.bfloat16, device="cuda")
+    lg = torch.empty((T, cfg.n_experts), dtype=torch.float32, device="cuda")
+    out = torch.empty((T, cfg.hidden), dtype=torch.float32, device="cuda")
+    ws, n = L.workspace(T, k)
+    g = B.moe_graph_create(L.handle, x, lg, None, None, T, k, out, False, ws, n, x_host=hx, logits_host=hl,
+                           out_host=hout)
+    try:
+        B.moe_graph_launch(g)
+        L.sync()
+        assert torch.equal(hout, ref.cpu())
+        # the next step's inputs are written into the pinned buffers only
+        cfg2 = dataclasses.replace(cfg, seed=cfg.seed + 100)
+        hx.copy_(torch.from_numpy(wl.tokens(cfg2).view(np.int16)).view(torch.bfloat16))
+        hl.copy_(torch.from_numpy(wl.router_logits(cfg2)))
+        B.moe_graph_launch(g)
+        L.sync()
+        ref2 = L.forward(hx.cuda(), hl.cuda(), k).clone()
+        L.sync()
+        assert torch.equal(hout, ref2.cpu())
+    finally:
+        B.moe_graph_free(g)
+    L.free()
+
+
 def test_graph_dense_slices():
     B, layer = _mods()
     cfg = wl.dense(1, "mxfp4")
