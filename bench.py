@@ -181,6 +181,22 @@ def ncu_traffic(kernel_key: str):
     return float(ent["bytes_per_launch"]) * float(ent.get("scale_to_workload", 1.0))
 
 
+# ------------------------------------------------------------------ ranks
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """The largest value over all ranks: a job's step time is its slowest rank's."""
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_rank: int, ms: float) -> float:
+    """Whole-job throughput of N independent replicas (weak scaling): every
+    rank's tokens over the slowest rank's step time."""
+    return world * tokens_per_rank / (ms * 1e-3)
+
+
 # ------------------------------------------------------------------ our arm
 
 def run_ours(args, cfg, rank, world):
@@ -236,9 +252,7 @@ def run_ours(args, cfg, rank, world):
     times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = sum(times) / len(times)
     if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(ms, dist, dev)
 
     # per-stage device time, from the library's own events on the same stream,
     # in separate (untimed) steps so that the events do not perturb the above
@@ -335,7 +349,7 @@ def run_ours(args, cfg, rank, world):
     # (FP32 accumulate); the tcgen05 path and BF16 weights run in BF16
     dtype = "f16" if streaming and cfg.weight_format == "mxfp4" else "bf16"
     weight_bytes = gate_up["weight_bytes"] + down["weight_bytes"]
-    value = world * cfg.T / (ms * 1e-3)
+    value = job_tokens_per_s(world, cfg.T, ms)
     res = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",

@@ -1,0 +1,91 @@
+"""CPU tests of bench.py's host logic: the algorithmic-byte model behind the
+roofline, the max-over-ranks step time of an N-rank run (world size 2 over
+gloo), the reference arm's JSON line, and the ranks that stay silent."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_algorithmic_bytes_of_decode():
+    # MXFP4 costs 17/32 byte per weight (4-bit codes + one E8M0 byte per 32):
+    # an expert (gate|up [4096, 7168] and down [7168, 2048]) is 23,396,352 bytes
+    cfg = bench.workload("decode_T1")
+    gu, dn, layer = bench.work_model(cfg, 9)
+    assert gu["per_unit"] + dn["per_unit"] == 23_396_352
+    assert layer["weight_bytes"] == 9 * 23_396_352
+    # plus x (BF16), the logits (FP32 [1][256]) and out (FP32)
+    assert layer["bytes"] == 9 * 23_396_352 + 7168 * 2 + 256 * 4 + 7168 * 4
+    # two flops per multiply-add over every (position, weight) pair: 9 positions
+    assert layer["flops"] == 2 * 9 * 3 * 2048 * 7168
+
+
+def test_job_throughput_is_weak_scaling():
+    assert bench.job_tokens_per_s(1, 1, 0.1) == pytest.approx(10_000.0)
+    assert bench.job_tokens_per_s(4, 8, 2.0) == pytest.approx(16_000.0)
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, values, q):
+    import torch.distributed as dist
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    try:
+        q.put((rank, bench.max_over_ranks(values[rank], dist)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_step_time_is_the_slowest_rank_over_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    values = [0.0712, 0.0901]
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, values, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert got == {0: max(values), 1: max(values)}
+
+
+def _bench(args, env_extra=None):
+    env = dict(os.environ, **(env_extra or {}))
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], capture_output=True, text=True,
+                          timeout=600, env=env, cwd=ROOT)
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = _bench(["--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "3"])
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["unit"] == "tokens/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+    assert d["config"]["workload"].startswith("tiny")
+
+
+def test_reference_arm_is_silent_on_other_ranks():
+    r = _bench(["--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "3"],
+               {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip() == ""
