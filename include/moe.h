@@ -35,6 +35,13 @@
  *  A dense SwiGLU FFN is run as n_slices all-active slices of its intermediate
  *  dimension, each with unit weight ("Cascadia" §3.4, Eq. 2).
  *
+ *  Other entry points: moe_forward_routed runs steps 2-4 on expert ids and
+ *  weights the caller computed (the interface of "Cascadia" §3.1, whose router
+ *  runs elsewhere); moe_route_sigmoid is that paper's routing variant (sigmoid
+ *  scores, bias-adjusted selection); moe_graph_create / moe_graph_launch
+ *  replay a captured forward call as one CUDA graph; moe_route_static routes
+ *  and groups without a workspace.
+ *
  * Layouts (all row-major, C order):
  *  - pack4 (MXFP4 codes): byte j of a row holds element 2j in its low nibble
  *    and element 2j+1 in its high nibble.  Code bit 3 is the sign; bits 0..2
@@ -47,9 +54,10 @@
  *    says otherwise.  The library owns only the handle and its own repacked
  *    copy of the weights (made at load; the caller's weight buffers can be
  *    freed as soon as moe_load_weights returns).
- *  - moe_forward and moe_dense_sliced_forward enqueue work on `cuda_stream`
- *    (a cudaStream_t, NULL = legacy default stream) and return without waiting
- *    for it.  They allocate nothing and never synchronise.
+ *  - The forward calls (moe_forward, moe_forward_routed,
+ *    moe_dense_sliced_forward) enqueue work on `cuda_stream` (a cudaStream_t,
+ *    NULL = legacy default stream) and return without waiting for it.  They
+ *    allocate nothing and never synchronise.
  *  - Every argument is checked on the host before anything is enqueued; a bad
  *    argument returns a status, never aborts, and leaves the outputs untouched.
  *    moe_last_error() then describes the problem.
