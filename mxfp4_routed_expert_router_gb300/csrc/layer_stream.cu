@@ -1447,8 +1447,8 @@ int ls_ring_depth(int G, int n, int E, int T)
     int R = (C::SMEM_LIMIT - base.total) / C::STAGE;
     if (R > LS_R_MAX)
         R = LS_R_MAX;
-    // phase-0 scratch lives in the ring: routing keys and selection, prep
-    // reduction; then the slot ids, group-scan totals and permutation counters
+    // phase-0 scratch lives in the ring: the slot ids of local routing and the
+    // prep reduction; then the slot ids, group-scan totals and permutation counters
     const long long scratch0 = LS_SCRATCH_PREP + 128;
     const long long scratch1 = ((long long)((n + 3) & ~3) + 2 * LS_WARPS + (long long)LS_WARPS * E) * 4;
     const long long ring = (long long)R * C::STAGE;
