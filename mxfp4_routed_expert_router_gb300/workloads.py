@@ -183,6 +183,24 @@ def mx_matrix(rng: np.random.Generator, rows: int, cols: int, e_lo: int, e_hi: i
     return codes, scales
 
 
+def i4_matrix(rng: np.random.Generator, rows: int, cols: int, scale_lo: float, scale_hi: float, zero_lo: int = 8,
+              zero_hi: int = 8, signed_scales: bool = False):
+    """Random group-32 INT4 matrix [rows, cols]: uniform 4-bit codes, FP16 group
+    scales with magnitude log-uniform in [scale_lo, scale_hi] (each with a random
+    sign when signed_scales), and zero points uniform in [zero_lo, zero_hi].
+
+    Returns (codes uint8 [rows, cols/2], scales uint16 FP16 bits [rows, cols/32],
+    zeros uint8 [rows, cols/32]).
+    """
+    assert cols % 32 == 0 and 0 <= zero_lo <= zero_hi <= 15
+    codes = np.frombuffer(rng.bytes(rows * cols // 2), dtype=np.uint8).reshape(rows, cols // 2).copy()
+    mag = np.exp(rng.uniform(np.log(scale_lo), np.log(scale_hi), size=(rows, cols // 32)))
+    sign = np.where(rng.integers(0, 2, size=mag.shape) == 1, -1.0, 1.0) if signed_scales else 1.0
+    scales = (sign * mag).astype(np.float16).view(np.uint16)
+    zeros = rng.integers(zero_lo, zero_hi + 1, size=(rows, cols // 32), dtype=np.uint8)
+    return codes, scales, zeros
+
+
 def expert_weights(cfg: LayerConfig, e: int):
     """MXFP4 weights of expert e (0..E-1 routed, E..E+S-1 shared).
 

@@ -16,6 +16,9 @@ arrays into it with ctypes.  Each function cites the passage it follows:
   and the sigmoid + bias routing variant -- "Cascadia: Resident 975B MoE
   Inference on Eleven AI PCs" §3.1 and Eq. (1) of §3.3.
 * Dense FFN as all-active slices -- same paper, §3.4, Eq. (2).
+* Group-32 INT4 weights with FP16 group scales and zero points -- same paper,
+  §3.1 (the exporter's packed nibbles and FP16 group scales) and §3.5 (scale
+  and zero-point overhead in the expert bytes).
 """
 from __future__ import annotations
 
@@ -52,7 +55,10 @@ class _Layer(ctypes.Structure):
         ("n_shared", ctypes.c_int), ("weight_format", ctypes.c_int),
         ("gu_codes", ctypes.POINTER(ctypes.c_void_p)), ("gu_scales", ctypes.POINTER(ctypes.c_void_p)),
         ("d_codes", ctypes.POINTER(ctypes.c_void_p)), ("d_scales", ctypes.POINTER(ctypes.c_void_p)),
+        ("gu_zeros", ctypes.POINTER(ctypes.c_void_p)), ("d_zeros", ctypes.POINTER(ctypes.c_void_p)),
     ]
+
+_FORMATS = {"mxfp4": 0, "bf16": 1, "int4g32": 2}
 
 
 def lib():
@@ -72,6 +78,14 @@ def lib():
             L.oracle_mx_decode.restype = ci
             L.oracle_bf16_decode.argtypes = [vp, i64, vp]
             L.oracle_bf16_decode.restype = None
+            L.oracle_fp16_value.argtypes = [ci]
+            L.oracle_fp16_value.restype = ctypes.c_double
+            L.oracle_i4_value.argtypes = [ci, ci, ci]
+            L.oracle_i4_value.restype = ctypes.c_float
+            L.oracle_i4_bytes.argtypes = [i64, i64, ci]
+            L.oracle_i4_bytes.restype = i64
+            L.oracle_i4_decode.argtypes = [vp, vp, vp, i64, i64, vp]
+            L.oracle_i4_decode.restype = ci
             L.oracle_route.argtypes = [vp, i64, ci, ci, vp, vp]
             L.oracle_route.restype = None
             L.oracle_route_sigmoid.argtypes = [vp, vp, i64, ci, ci, ctypes.c_double, vp, vp]
@@ -84,7 +98,7 @@ def lib():
             L.oracle_moe_layer.restype = ci
             L.oracle_moe_layer_routed.argtypes = [ctypes.POINTER(_Layer), vp, vp, vp, i64, ci, ci, vp]
             L.oracle_moe_layer_routed.restype = ci
-            L.oracle_dense_ffn.argtypes = [ci, vp, vp, vp, vp, vp, vp, ci, ci, ci, vp, i64, ci, vp]
+            L.oracle_dense_ffn.argtypes = [ci, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, vp, i64, ci, vp]
             L.oracle_dense_ffn.restype = ci
             _lib = L
     return _lib
@@ -124,6 +138,36 @@ def mx_decode(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     rc = lib().oracle_mx_decode(_p(codes), _p(scales), rows, cols, _p(out))
     if rc != 0:
         raise ValueError("E8M0 scale 255 (NaN) in MXFP4 matrix")
+    return out
+
+
+def fp16_value(bits: int) -> float:
+    """IEEE binary16 bit pattern to its value (double)."""
+    return lib().oracle_fp16_value(int(bits))
+
+
+def i4_value(q: int, z: int, scale_bits: int) -> float:
+    """Group-32 INT4 weight s * (q - z) rounded to float32 (exact)."""
+    return lib().oracle_i4_value(int(q), int(z), int(scale_bits))
+
+
+def i4_bytes(rows: int, cols: int, zero_points: bool = True) -> int:
+    """Bytes of a group-32 INT4 matrix [rows, cols]: codes, FP16 scales, zero points."""
+    return int(lib().oracle_i4_bytes(rows, cols, 1 if zero_points else 0))
+
+
+def i4_decode(codes: np.ndarray, scales: np.ndarray, zeros: np.ndarray | None = None) -> np.ndarray:
+    """Decode group-32 INT4 codes [rows, cols/2] + FP16 scale bits [rows, cols/32]
+    + zero points [rows, cols/32] (None: all 8) to float32 [rows, cols]."""
+    codes, scales = _c(codes, np.uint8), _c(scales, np.uint16)
+    rows, cols = codes.shape[0], codes.shape[1] * 2
+    assert scales.shape == (rows, cols // 32)
+    if zeros is not None:
+        zeros = _c(zeros, np.uint8)
+        assert zeros.shape == scales.shape
+    out = np.empty((rows, cols), np.float32)
+    if lib().oracle_i4_decode(_p(codes), _p(scales), _p(zeros), rows, cols, _p(out)) != 0:
+        raise ValueError("non-finite FP16 scale or zero point above 15 in INT4 matrix")
     return out
 
 
@@ -187,9 +231,13 @@ def swiglu_ffn(Wg: np.ndarray, Wu: np.ndarray, Wd: np.ndarray, x: np.ndarray) ->
 
 
 class OracleWeights:
-    """Host weights of an MoE layer, any subset of experts may be None."""
+    """Host weights of an MoE layer, any subset of experts may be None.
+
+    weight_format: "mxfp4" (codes + E8M0 scales), "bf16" (bits) or "int4g32"
+    (codes + FP16 scale bits + optional zero points)."""
 
     def __init__(self, hidden: int, inter: int, n_experts: int, n_shared: int, weight_format: str = "mxfp4"):
+        assert weight_format in _FORMATS
         self.hidden, self.inter, self.n_experts, self.n_shared = hidden, inter, n_experts, n_shared
         self.weight_format = weight_format
         n = n_experts + n_shared
@@ -197,13 +245,30 @@ class OracleWeights:
         self.gu_scales = [None] * n
         self.d_codes = [None] * n
         self.d_scales = [None] * n
+        self.gu_zeros = [None] * n
+        self.d_zeros = [None] * n
 
-    def set_expert(self, e: int, gu_codes, gu_scales, d_codes, d_scales):
+    def set_expert(self, e: int, gu_codes, gu_scales, d_codes, d_scales, gu_zeros=None, d_zeros=None):
         if self.weight_format == "bf16":
             self.gu_codes[e], self.d_codes[e] = _c(gu_codes, np.uint16), _c(d_codes, np.uint16)
-        else:
-            self.gu_codes[e], self.gu_scales[e] = _c(gu_codes, np.uint8), _c(gu_scales, np.uint8)
-            self.d_codes[e], self.d_scales[e] = _c(d_codes, np.uint8), _c(d_scales, np.uint8)
+            return
+        sdt = np.uint16 if self.weight_format == "int4g32" else np.uint8
+        self.gu_codes[e], self.gu_scales[e] = _c(gu_codes, np.uint8), _c(gu_scales, sdt)
+        self.d_codes[e], self.d_scales[e] = _c(d_codes, np.uint8), _c(d_scales, sdt)
+        if self.weight_format == "int4g32":
+            self.gu_zeros[e] = None if gu_zeros is None else _c(gu_zeros, np.uint8)
+            self.d_zeros[e] = None if d_zeros is None else _c(d_zeros, np.uint8)
+
+    def _layer(self):
+        """The C layer descriptor and the pointer arrays it refers to (keep both alive)."""
+        ne = self.n_experts + self.n_shared
+        arr = lambda lst: (ctypes.c_void_p * ne)(*[(None if a is None else a.ctypes.data) for a in lst])
+        keep = [arr(self.gu_codes), arr(self.gu_scales), arr(self.d_codes), arr(self.d_scales), arr(self.gu_zeros),
+                arr(self.d_zeros)]
+        cast = lambda a: ctypes.cast(a, ctypes.POINTER(ctypes.c_void_p))
+        L = _Layer(self.hidden, self.inter, self.n_experts, self.n_shared, _FORMATS[self.weight_format],
+                   *(cast(a) for a in keep))
+        return L, keep
 
 
 def moe_layer(W: OracleWeights, x_bf16: np.ndarray, logits: np.ndarray, k: int, nthreads: int = 1):
@@ -212,12 +277,7 @@ def moe_layer(W: OracleWeights, x_bf16: np.ndarray, logits: np.ndarray, k: int, 
     logits = _c(logits, np.float32)
     n, H = x_bf16.shape
     assert H == W.hidden and logits.shape == (n, W.n_experts)
-    ne = W.n_experts + W.n_shared
-    arr = lambda lst: (ctypes.c_void_p * ne)(*[(None if a is None else a.ctypes.data) for a in lst])
-    keep = [arr(W.gu_codes), arr(W.gu_scales), arr(W.d_codes), arr(W.d_scales)]
-    cast = lambda a: ctypes.cast(a, ctypes.POINTER(ctypes.c_void_p))
-    L = _Layer(W.hidden, W.inter, W.n_experts, W.n_shared, 1 if W.weight_format == "bf16" else 0,
-               cast(keep[0]), cast(keep[1]), cast(keep[2]), cast(keep[3]))
+    L, _keep = W._layer()
     out = np.empty((n, H), np.float64)
     ids = np.empty((n, k), np.int32)
     w = np.empty((n, k), np.float64)
@@ -238,12 +298,7 @@ def moe_layer_routed(W: OracleWeights, x_bf16: np.ndarray, ids: np.ndarray, w: n
     n, H = x_bf16.shape
     k = ids.shape[1]
     assert H == W.hidden and ids.shape == (n, k) and w.shape == (n, k)
-    ne = W.n_experts + W.n_shared
-    arr = lambda lst: (ctypes.c_void_p * ne)(*[(None if a is None else a.ctypes.data) for a in lst])
-    keep = [arr(W.gu_codes), arr(W.gu_scales), arr(W.d_codes), arr(W.d_scales)]
-    cast = lambda a: ctypes.cast(a, ctypes.POINTER(ctypes.c_void_p))
-    L = _Layer(W.hidden, W.inter, W.n_experts, W.n_shared, 1 if W.weight_format == "bf16" else 0,
-               cast(keep[0]), cast(keep[1]), cast(keep[2]), cast(keep[3]))
+    L, _keep = W._layer()
     out = np.empty((n, H), np.float64)
     rc = lib().oracle_moe_layer_routed(ctypes.byref(L), _p(x_bf16), _p(ids), _p(w), n, k, nthreads, _p(out))
     if rc != 0:
@@ -254,23 +309,26 @@ def moe_layer_routed(W: OracleWeights, x_bf16: np.ndarray, ids: np.ndarray, w: n
 def dense_ffn(weights, x_bf16: np.ndarray, n_slices: int = 0, weight_format: str = "mxfp4") -> np.ndarray:
     """Dense SwiGLU FFN on the given tokens, unsliced (n_slices=0) or as a sum of slices.
 
-    weights: MXFP4 ((g_codes, g_scales), (u_codes, u_scales), (d_codes, d_scales)) or
-    BF16 bits (W_g [I, H], W_u [I, H], W_d [H, I]).
+    weights: MXFP4 ((g_codes, g_scales), (u_codes, u_scales), (d_codes, d_scales)),
+    BF16 bits (W_g [I, H], W_u [I, H], W_d [H, I]), or group-32 INT4
+    ((g_codes, g_scales, g_zeros), (u_...), (d_...)) with FP16 scale bits and
+    zero points (None: all 8).
     """
     x_bf16 = _c(x_bf16, np.uint16)
     n, H = x_bf16.shape
+    gz = uz = dz = None
     if weight_format == "bf16":
         g, u, d = (_c(a, np.uint16) for a in weights)
         gs = us = ds = None
-        I = g.shape[0]
-        fmt = 1
+    elif weight_format == "int4g32":
+        (g, gs, gz), (u, us, uz), (d, ds, dz) = (
+            (_c(a, np.uint8), _c(b, np.uint16), None if z is None else _c(z, np.uint8)) for a, b, z in weights)
     else:
         (g, gs), (u, us), (d, ds) = ((_c(a, np.uint8), _c(b, np.uint8)) for a, b in weights)
-        I = g.shape[0]
-        fmt = 0
+    I = g.shape[0]
     out = np.empty((n, H), np.float64)
-    rc = lib().oracle_dense_ffn(fmt, _p(g), _p(gs), _p(u), _p(us), _p(d), _p(ds), H, I, n_slices, _p(x_bf16), n, 1,
-                                _p(out))
+    rc = lib().oracle_dense_ffn(_FORMATS[weight_format], _p(g), _p(gs), _p(gz), _p(u), _p(us), _p(uz), _p(d), _p(ds),
+                                _p(dz), H, I, n_slices, _p(x_bf16), n, 1, _p(out))
     if rc != 0:
         raise ValueError(f"oracle_dense_ffn failed with {rc}")
     return out

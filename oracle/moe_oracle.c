@@ -24,6 +24,9 @@
  *  [C33] same paper §3.3, Eq. (1): y_i = sum_e w_ie E_e(x_i).
  *  [C34] same paper §3.4, Eq. (2): the dense FFN equals the sum of its
  *        intermediate-dimension slices, every slice active with unit weight.
+ *  [I4]  same paper §3.1 (the exporter keeps the experts' group-32 INT4
+ *        packed nibbles and stores each group's scale as FP16) and §3.5 (the
+ *        expert bytes it counts include scale and zero-point overhead).
  *
  * Readings where the pages are silent (each also listed in the design notes):
  *  - Router: softmax over all experts, keep the k largest, renormalise over
@@ -36,6 +39,12 @@
  *  - E8M0 = 255 is NaN in the OCP format and is rejected.
  *  - Shared experts have weight 1.0 and are added outside the renormalisation.
  *  - Slots of one expert are kept in ascending slot order s = t*k + j.
+ *  - Group-32 INT4 [I4]: a weight is s * (q - z) for its unsigned 4-bit code q,
+ *    and the FP16 scale s and zero point z (0..15, one byte) of its group of
+ *    32 consecutive values along a row.  Element 2j is the low nibble of byte
+ *    j, as for MXFP4.  Without stored zero points every z is 8, which is the
+ *    symmetric signed grid -8..7.  A scale that is Inf or NaN, or a zero point
+ *    above 15, is rejected.
  */
 #include <math.h>
 #include <pthread.h>
@@ -96,6 +105,61 @@ void oracle_bf16_decode(const uint16_t *bits, int64_t n, float *out)
         uint32_t u = (uint32_t)bits[i] << 16;
         memcpy(&out[i], &u, 4);
     }
+}
+
+/* IEEE binary16 bits to double: sign bit 15, exponent bits 10..14 (bias 15),
+ * fraction bits 0..9.  Exponent 0 is zero or subnormal (fraction * 2^-24);
+ * exponent 31 is Inf (fraction 0) or NaN. */
+double oracle_fp16_value(int bits)
+{
+    int sign = (bits >> 15) & 1, ex = (bits >> 10) & 31, fr = bits & 1023;
+    double v;
+    if (ex == 31)
+        v = fr ? NAN : INFINITY;
+    else if (ex == 0)
+        v = ldexp((double)fr, -24);
+    else
+        v = ldexp((double)(1024 + fr), ex - 25);
+    return sign ? -v : v;
+}
+
+/* Decoded group-32 INT4 weight s * (q - z) [I4], computed in double and
+ * rounded to float.  The rounding is exact: |q - z| <= 15 has 4 significant
+ * bits and s has at most 11. */
+float oracle_i4_value(int q, int z, int scale_bits)
+{
+    return (float)((double)(q - z) * oracle_fp16_value(scale_bits));
+}
+
+/* Storage of a group-32 INT4 matrix [rows, cols]: cols/2 code bytes, then
+ * per 32 values a 2-byte FP16 scale and (when stored) a 1-byte zero point:
+ * 4 + 16/32 (+ 8/32) bits per weight. */
+int64_t oracle_i4_bytes(int64_t rows, int64_t cols, int with_zeros)
+{
+    return rows * (cols / 2) + rows * (cols / 32) * (with_zeros ? 3 : 2);
+}
+
+/* Decode a group-32 INT4 matrix [rows, cols] to float: codes [rows, cols/2],
+ * FP16 scale bits [rows, cols/32], zero points [rows, cols/32] or NULL (all
+ * 8).  Element i of a row takes group floor(i/32) [I4].  Returns 0, or -1 if a
+ * scale is Inf / NaN or a zero point is above 15. */
+int oracle_i4_decode(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, int64_t rows, int64_t cols,
+                     float *out)
+{
+    const int64_t ng = cols / 32;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t i = 0; i < cols; ++i) {
+            const int64_t grp = r * ng + i / 32;
+            const int sb = scales[grp];
+            const int z = zeros ? zeros[grp] : 8;
+            if (((sb >> 10) & 31) == 31 || z > 15)
+                return -1;
+            const uint8_t byte = codes[r * (cols / 2) + i / 2];
+            const int q = (i & 1) ? (byte >> 4) : (byte & 0xF);
+            out[r * cols + i] = oracle_i4_value(q, z, sb);
+        }
+    }
+    return 0;
 }
 
 /* ---------------------------------------------------------------- router */
@@ -250,16 +314,23 @@ void oracle_swiglu_ffn(const float *Wg, const float *Wu, int64_t ld_gu, const fl
 /* ---------------------------------------------------------------- layer */
 
 /* Weights of one layer.  Expert e in [0, E) is routed, [E, E+S) shared.
- * MXFP4: gu_codes[e] [2I, H/2], gu_scales[e] [2I, H/32] (gate rows 0..I-1,
- * up rows I..2I-1), d_codes[e] [H, I/2], d_scales[e] [H, I/32].
+ * MXFP4 (weight_format 0): gu_codes[e] [2I, H/2], gu_scales[e] uint8
+ * [2I, H/32] (gate rows 0..I-1, up rows I..2I-1), d_codes[e] [H, I/2],
+ * d_scales[e] uint8 [H, I/32].
  * BF16 (weight_format 1): gu_codes[e] is uint16 [2I, H], d_codes[e] uint16
- * [H, I], scales unused.  An entry may be NULL when no token uses it. */
+ * [H, I], scales unused.
+ * Group-32 INT4 (weight_format 2): codes as for MXFP4, scales uint16 FP16
+ * bits of the same shape, zero points uint8 of the same shape (the arrays, or
+ * an entry, may be NULL: all 8).
+ * An entry may be NULL when no token uses it. */
 typedef struct {
     int hidden, inter, n_experts, n_shared, weight_format;
     const void *const *gu_codes;
-    const uint8_t *const *gu_scales;
+    const void *const *gu_scales;
     const void *const *d_codes;
-    const uint8_t *const *d_scales;
+    const void *const *d_scales;
+    const uint8_t *const *gu_zeros;
+    const uint8_t *const *d_zeros;
 } OracleLayer;
 
 typedef struct {
@@ -307,7 +378,8 @@ static void run_ffn_jobs(const float *Wgu, const float *Wd, int H, int I, const 
         pthread_join(th[i], NULL);
 }
 
-static int decode_matrix(int fmt, const void *codes, const uint8_t *scales, int64_t rows, int64_t cols, float *out)
+static int decode_matrix(int fmt, const void *codes, const void *scales, const uint8_t *zeros, int64_t rows,
+                         int64_t cols, float *out)
 {
     if (codes == NULL)
         return -2;
@@ -317,20 +389,18 @@ static int decode_matrix(int fmt, const void *codes, const uint8_t *scales, int6
     }
     if (scales == NULL)
         return -2;
-    return oracle_mx_decode((const uint8_t *)codes, scales, rows, cols, out);
+    if (fmt == 2)
+        return oracle_i4_decode((const uint8_t *)codes, (const uint16_t *)scales, zeros, rows, cols, out);
+    return oracle_mx_decode((const uint8_t *)codes, (const uint8_t *)scales, rows, cols, out);
 }
 
-/* The MoE layer for n_tok tokens (any subset of a batch: a token's result
- * depends only on its own x row and logits row):
- *   route (softmax top-k, renormalised), run every selected expert and every
- *   shared expert on the token, and combine
- *   out_t = sum_{j<k} w_tj * y_{e_tj}(x_t) + sum_{shared s} y_s(x_t)   [C33, C31].
- * x_bf16 [n_tok, H] BF16 bits, logits [n_tok, E], out [n_tok, H] double.
- * ids / w (optional, [n_tok, k]) receive the routing.
- * Returns 0, -1 (E8M0 = 255), -2 (weights of a used expert missing), -3 (bad args). */
 /* The layer for given routing (ids [n_tok, k] in [0, E), weights w): every
  * selected and every shared expert on its tokens, then the weighted reduction
- * (Eq. 1).  Returns 0, -1 (E8M0 = 255), -3 (bad args or an id out of range). */
+ *   out_t = sum_{j<k} w_tj * y_{e_tj}(x_t) + sum_{shared s} y_s(x_t)   [C33, C31].
+ * A token's result depends only on its own x row and routing row.
+ * x_bf16 [n_tok, H] BF16 bits, out [n_tok, H] double.  Returns 0, -1 (a scale
+ * the format rejects), -2 (weights of a used expert missing), -3 (bad args or
+ * an id out of range). */
 int oracle_moe_layer_routed(const OracleLayer *L, const uint16_t *x_bf16, const int32_t *ids, const double *w,
                             int64_t n_tok, int k, int nthreads, double *out)
 {
@@ -373,10 +443,11 @@ int oracle_moe_layer_routed(const OracleLayer *L, const uint16_t *x_bf16, const 
         }
         if (nwork == 0)
             continue;
-        rc = decode_matrix(L->weight_format, L->gu_codes[e], L->gu_scales ? L->gu_scales[e] : NULL, 2 * (int64_t)I,
-                           H, Wgu);
+        rc = decode_matrix(L->weight_format, L->gu_codes[e], L->gu_scales ? L->gu_scales[e] : NULL,
+                           L->gu_zeros ? L->gu_zeros[e] : NULL, 2 * (int64_t)I, H, Wgu);
         if (rc == 0)
-            rc = decode_matrix(L->weight_format, L->d_codes[e], L->d_scales ? L->d_scales[e] : NULL, H, I, Wd);
+            rc = decode_matrix(L->weight_format, L->d_codes[e], L->d_scales ? L->d_scales[e] : NULL,
+                               L->d_zeros ? L->d_zeros[e] : NULL, H, I, Wd);
         if (rc == 0)
             run_ffn_jobs(Wgu, Wd, H, I, x, y, nsel, work, nwork, nthreads);
     }
@@ -401,8 +472,9 @@ int oracle_moe_layer_routed(const OracleLayer *L, const uint16_t *x_bf16, const 
     return rc;
 }
 
-/* The routed layer: softmax top-k routing of the logits, then the layer for
- * that routing; the routing goes to ids_out / w_out when given. */
+/* The routed MoE layer for n_tok tokens: softmax top-k routing of the logits
+ * (renormalised over the k kept), then the layer for that routing.  logits
+ * [n_tok, E]; the routing goes to ids_out / w_out ([n_tok, k]) when given. */
 int oracle_moe_layer(const OracleLayer *L, const uint16_t *x_bf16, const float *logits, int64_t n_tok, int k,
                      int nthreads, double *out, int32_t *ids_out, double *w_out)
 {
@@ -425,14 +497,16 @@ int oracle_moe_layer(const OracleLayer *L, const uint16_t *x_bf16, const float *
 }
 
 /* The dense SwiGLU FFN [C34] for n_tok tokens.  Weights are given unsliced:
- * gate [I, H], up [I, H], down [H, I] (MXFP4 with scales, or BF16 bits when
- * weight_format is 1).  With n_slices == 0 the FFN is evaluated as one block;
+ * gate [I, H], up [I, H], down [H, I] in weight_format 0 (MXFP4 codes and
+ * E8M0 scales), 1 (BF16 bits) or 2 (group-32 INT4 codes, FP16 scales, zero
+ * points or NULL).  With n_slices == 0 the FFN is evaluated as one block;
  * with n_slices > 0 it is evaluated as the sum over n_slices all-active slices
  * of width I / n_slices, each with unit weight (Eq. 2).  out [n_tok, H] double.
- * Returns 0, -1 (E8M0 = 255), -3 (bad args). */
-int oracle_dense_ffn(int weight_format, const void *g_codes, const uint8_t *g_scales, const void *u_codes,
-                     const uint8_t *u_scales, const void *d_codes, const uint8_t *d_scales, int H, int I,
-                     int n_slices, const uint16_t *x_bf16, int64_t n_tok, int nthreads, double *out)
+ * Returns 0, -1 (a scale the format rejects), -3 (bad args). */
+int oracle_dense_ffn(int weight_format, const void *g_codes, const void *g_scales, const uint8_t *g_zeros,
+                     const void *u_codes, const void *u_scales, const uint8_t *u_zeros, const void *d_codes,
+                     const void *d_scales, const uint8_t *d_zeros, int H, int I, int n_slices,
+                     const uint16_t *x_bf16, int64_t n_tok, int nthreads, double *out)
 {
     if (H % 32 || I % 32)
         return -3;
@@ -447,11 +521,11 @@ int oracle_dense_ffn(int weight_format, const void *g_codes, const uint8_t *g_sc
     float *Wd = (float *)malloc(sizeof(float) * (size_t)H * I);
     double *x = (double *)malloc(sizeof(double) * (size_t)(n_tok * H + 1));
     double *y = (double *)malloc(sizeof(double) * (size_t)(n_tok * H + 1));
-    rc = decode_matrix(weight_format, g_codes, g_scales, I, H, Wgu);
+    rc = decode_matrix(weight_format, g_codes, g_scales, g_zeros, I, H, Wgu);
     if (rc == 0)
-        rc = decode_matrix(weight_format, u_codes, u_scales, I, H, Wgu + (int64_t)I * H);
+        rc = decode_matrix(weight_format, u_codes, u_scales, u_zeros, I, H, Wgu + (int64_t)I * H);
     if (rc == 0)
-        rc = decode_matrix(weight_format, d_codes, d_scales, H, I, Wd);
+        rc = decode_matrix(weight_format, d_codes, d_scales, d_zeros, H, I, Wd);
     if (rc == 0) {
         for (int64_t i = 0; i < n_tok * H; ++i) {
             uint32_t u = (uint32_t)x_bf16[i] << 16;

@@ -39,6 +39,15 @@ MUTATIONS = {
     "sigmoid_bias_ignored": ("s[e].v = score[e] + (bias ? (double)bias[e] : 0.0);", "s[e].v = score[e];"),
     "sigmoid_sign": ("score[e] = 1.0 / (1.0 + exp(-(double)logits[t * E + e]));",
                      "score[e] = 1.0 / (1.0 + exp((double)logits[t * E + e]));"),
+    "i4_nibble_order": ("(i & 1) ? (byte >> 4) : (byte & 0xF)", "(i & 1) ? (byte & 0xF) : (byte >> 4)"),
+    "i4_zero_sign": ("(double)(q - z)", "(double)(z - q)"),
+    "i4_zero_ignored": ("(double)(q - z)", "(double)(q - 8)"),
+    "i4_group_of_16": ("r * ng + i / 32", "r * ng + (i / 16) % ng"),
+    "i4_default_zero_0": ("zeros ? zeros[grp] : 8", "zeros ? zeros[grp] : 0"),
+    "i4_zero_16_accepted": ("|| z > 15)", "|| z > 16)"),
+    "fp16_exponent_bias_16": ("ex - 25", "ex - 26"),
+    "fp16_subnormal_flushed": ("v = ldexp((double)fr, -24);", "v = 0.0;"),
+    "fp16_implicit_bit_dropped": ("ldexp((double)(1024 + fr), ex - 25)", "ldexp((double)fr, ex - 25)"),
     "sigmoid_normalised_over_all": ("for (int j = 0; j < k; ++j)\n            denom += score[s[j].idx];",
                                     "for (int e = 0; e < E; ++e)\n            denom += score[e];"),
 }

@@ -7,7 +7,9 @@ on tiny inputs written independently in numpy / plain Python, or special cases
 that reduce to a textbook SwiGLU FFN.  They are chosen so that a plausible slip
 in the oracle (nibble order, sign bit, magnitude order, exponent bias, block
 index, tie-break, renormalisation, permutation stability, gate/up swap, a
-dropped shared expert, a dropped slice) fails at least one of them.
+dropped shared expert, a dropped slice; for group-32 INT4 the zero point's
+sign or default, the group index and the FP16 scale decode) fails at least one
+of them.
 """
 import math
 import os
@@ -501,3 +503,183 @@ def test_layer_routed_rejects_ids_out_of_range():
         W.set_expert(e, *wl.expert_weights(cfg, e))
     with pytest.raises(ValueError):
         oracle.moe_layer_routed(W, wl.tokens(cfg), np.array([[0], [3]], np.int32), np.ones((2, 1)))
+
+
+# ------------------------------------------------------------------ group-32 INT4 pins
+# "Cascadia: Resident 975B MoE Inference on Eleven AI PCs" §3.1 (packed 4-bit
+# nibbles, one FP16 scale per 32-value group) and §3.5 (zero points).  Reading:
+# w = s * (q - z), q the unsigned nibble, z the group's zero point (8 when none
+# are stored), element 2j in the low nibble of byte j.
+
+FP16_ONE = 0x3C00
+
+
+def test_fp16_value_every_bit_pattern_matches_numpy():
+    bits = np.arange(65536, dtype=np.uint32)
+    want = bits.astype(np.uint16).view(np.float16).astype(np.float64)
+    got = np.array([oracle.fp16_value(int(b)) for b in bits])
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    np.testing.assert_array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+
+
+def test_i4_unit_scale_is_code_minus_zero():
+    for q in range(16):
+        for z in range(16):
+            assert oracle.i4_value(q, z, FP16_ONE) == q - z
+
+
+def test_i4_value_is_exact_product():
+    rng = np.random.default_rng(21)
+    # normal, subnormal, negative and extreme FP16 scales
+    sbits = np.concatenate([rng.integers(0, 0x7C00, 200), rng.integers(0x8000, 0xFC00, 200),
+                            [0x0001, 0x03FF, 0x0400, 0x7BFF, 0xFBFF, 0x8001]]).astype(np.uint16)
+    for b in sbits:
+        s = Fraction(float(np.uint16(b).view(np.float16)))
+        q, z = int(rng.integers(0, 16)), int(rng.integers(0, 16))
+        assert Fraction(oracle.i4_value(q, z, int(b))) == (q - z) * s, (q, z, hex(b))
+
+
+def test_i4_nibble_order_low_is_even():
+    codes = np.full((1, 16), 0x88, np.uint8)  # every element q = 8 -> 0 with z = 8
+    codes[0, 0] = 0x9A          # element 0: q = 10 -> 2, element 1: q = 9 -> 1
+    codes[0, 7] = 0x08          # element 14: q = 8 -> 0, element 15: q = 0 -> -8
+    out = oracle.i4_decode(codes, np.full((1, 1), FP16_ONE, np.uint16))
+    assert out[0, 0] == 2.0 and out[0, 1] == 1.0
+    assert out[0, 14] == 0.0 and out[0, 15] == -8.0
+    assert np.count_nonzero(out) == 3
+
+
+def test_i4_group_index_is_floor_k_over_32():
+    codes = np.full((1, 48), 0x99, np.uint8)  # every q = 9
+    scales = np.array([[0x3C00, 0x4000, 0x3400]], np.uint16)  # 1, 2, 0.25
+    zeros = np.array([[8, 7, 13]], np.uint8)
+    out = oracle.i4_decode(codes, scales, zeros)
+    assert np.all(out[0, :32] == 1.0)
+    assert np.all(out[0, 32:64] == 4.0)
+    assert np.all(out[0, 64:] == -1.0)
+
+
+def np_i4_decode(codes, scales, zeros):
+    """Independent numpy decode of a group-32 INT4 matrix."""
+    q = np.stack([codes & 0xF, codes >> 4], axis=-1).reshape(codes.shape[0], -1).astype(np.int64)
+    z = np.repeat(zeros.astype(np.int64), 32, axis=1)
+    s = np.repeat(scales.view(np.float16).astype(np.float64), 32, axis=1)
+    return (q - z) * s
+
+
+def test_i4_decode_matches_independent_numpy_random():
+    rng = np.random.default_rng(22)
+    codes, scales, zeros = wl.i4_matrix(rng, 9, 96, 2.0 ** -20, 2.0 ** 10, 0, 15, signed_scales=True)
+    got = oracle.i4_decode(codes, scales, zeros).astype(np.float64)
+    np.testing.assert_array_equal(got, np_i4_decode(codes, scales, zeros))
+    # without stored zero points every zero point is 8
+    np.testing.assert_array_equal(oracle.i4_decode(codes, scales), oracle.i4_decode(codes, scales, np.full_like(zeros, 8)))
+
+
+@pytest.mark.parametrize("sbits,zero", [(0x7C00, 8), (0xFC00, 8), (0x7E00, 8), (0x7C01, 8), (FP16_ONE, 16),
+                                        (FP16_ONE, 255)])
+def test_i4_rejects_nonfinite_scale_and_zero_above_15(sbits, zero):
+    scales = np.array([[FP16_ONE, sbits]], np.uint16)
+    zeros = np.array([[8, zero]], np.uint8)
+    with pytest.raises(ValueError):
+        oracle.i4_decode(np.zeros((1, 32), np.uint8), scales, zeros)
+
+
+def test_i4_accepts_zero_15_and_largest_scale():
+    out = oracle.i4_decode(np.zeros((1, 16), np.uint8), np.array([[0xFBFF]], np.uint16), np.array([[15]], np.uint8))
+    assert np.all(out == 15 * 65504.0)
+
+
+def test_i4_size_identity():
+    with open(os.path.join(GOLDEN, "int4g32_sizes.txt")) as f:
+        rows = [l.split() for l in f if l.strip() and not l.startswith("#")]
+    for r, c, z, b in rows:
+        r, c, z, b = int(r), int(c), int(z), int(b)
+        assert oracle.i4_bytes(r, c, bool(z)) == b
+        assert Fraction(8 * b, r * c) == (Fraction(19, 4) if z else Fraction(9, 2))
+
+
+def mx_as_i4(codes, scales):
+    """An MXFP4 matrix with E8M0 = 126 (scale 1/2) and magnitudes up to 3 (codes
+    0..5 and 8..13), written as group-32 INT4 with scale 1/4: q - z = 4 v."""
+    assert np.all(scales == 126)
+    v = np_decode_golden(codes, scales)            # multiples of 1/4 in [-1.5, 1.5]
+    rng = np.random.default_rng(int(codes.sum()) % 1000)
+    zeros = rng.integers(6, 10, size=scales.shape, dtype=np.uint8)
+    q = (4 * v).astype(np.int64) + np.repeat(zeros.astype(np.int64), 32, axis=1)
+    assert q.min() >= 0 and q.max() <= 15
+    q = q.reshape(q.shape[0], -1, 2)
+    i4 = (q[..., 0] | (q[..., 1] << 4)).astype(np.uint8)
+    return i4, np.full(scales.shape, 0x3400, np.uint16), zeros
+
+
+def small_mx(rng, rows, cols):
+    # codes whose magnitude index is at most 5 (|v| <= 3), every E8M0 = 126
+    lo = rng.integers(0, 6, (rows, cols // 2)) | (rng.integers(0, 2, (rows, cols // 2)) << 3)
+    hi = rng.integers(0, 6, (rows, cols // 2)) | (rng.integers(0, 2, (rows, cols // 2)) << 3)
+    return (lo | (hi << 4)).astype(np.uint8), np.full((rows, cols // 32), 126, np.uint8)
+
+
+def test_i4_layer_equals_mxfp4_layer_on_equal_weights():
+    # the same decoded weights in both formats give the same layer, bit for bit
+    cfg = wl.custom("i4eq", 7, 96, 64, 6, 1, 2, seed=23)
+    rng = np.random.default_rng(23)
+    Wm = oracle.OracleWeights(96, 64, 6, 1)
+    Wi = oracle.OracleWeights(96, 64, 6, 1, "int4g32")
+    for e in range(7):
+        gc, gs = small_mx(rng, 128, 96)
+        dc, ds = small_mx(rng, 96, 64)
+        Wm.set_expert(e, gc, gs, dc, ds)
+        gi, gsi, gz = mx_as_i4(gc, gs)
+        di, dsi, dz = mx_as_i4(dc, ds)
+        np.testing.assert_array_equal(oracle.i4_decode(gi, gsi, gz), oracle.mx_decode(gc, gs))
+        Wi.set_expert(e, gi, gsi, di, dsi, gz, dz)
+    x, l = wl.tokens(cfg), wl.router_logits(cfg)
+    a, ia, wa = oracle.moe_layer(Wm, x, l, 2)
+    b, ib, wb = oracle.moe_layer(Wi, x, l, 2)
+    np.testing.assert_array_equal(ia, ib)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_i4_layer_brute_force_tiny():
+    cfg = wl.custom("i4bf", 10, 64, 96, 5, 1, 3, seed=24)
+    rng = np.random.default_rng(24)
+    W = oracle.OracleWeights(64, 96, 5, 1, "int4g32")
+    dec = []
+    for e in range(6):
+        gu = wl.i4_matrix(rng, 192, 64, 2.0 ** -7, 2.0 ** -3, 4, 12, signed_scales=True)
+        dn = wl.i4_matrix(rng, 64, 96, 2.0 ** -7, 2.0 ** -3, 4, 12)
+        W.set_expert(e, gu[0], gu[1], dn[0], dn[1], gu[2], dn[2])
+        dec.append((np_i4_decode(*gu), np_i4_decode(*dn)))
+    x, l = wl.tokens(cfg), wl.router_logits(cfg)
+    out, ids, w = oracle.moe_layer(W, x, l, 3)
+    xf = wl.bf16_bits_to_f32(x).astype(np.float64)
+    want = np.zeros_like(out)
+    for t in range(cfg.T):
+        sel = brute_route(l[t].tolist(), 3)
+        lv = np.array([float(l[t, e]) for e in sel])
+        p = np.exp(lv - lv.max())
+        p /= p.sum()
+        for j, e in enumerate(list(sel) + [5]):
+            Wgu, Wd = dec[e]
+            g, u = xf[t] @ Wgu[:96].T, xf[t] @ Wgu[96:].T
+            want[t] += (p[j] if j < 3 else 1.0) * ((g / (1 + np.exp(-g)) * u) @ Wd.T)
+    assert np.max(np.abs(out - want)) / np.sqrt(np.mean(want ** 2)) <= 1e-12
+
+
+def test_i4_dense_slices_equal_unsliced_and_textbook():
+    H, I = 64, 128
+    rng = np.random.default_rng(25)
+    w = tuple(wl.i4_matrix(rng, r, c, 2.0 ** -7, 2.0 ** -4, 5, 11) for r, c in ((I, H), (I, H), (H, I)))
+    x = wl.f32_to_bf16_bits(rng.standard_normal((3, H)).astype(np.float32))
+    full = oracle.dense_ffn(w, x, 0, "int4g32")
+    sliced = oracle.dense_ffn(w, x, 4, "int4g32")
+    Wg, Wu, Wd = (np_i4_decode(*m) for m in w)
+    xf = wl.bf16_bits_to_f32(x).astype(np.float64)
+    g, u = xf @ Wg.T, xf @ Wu.T
+    want = (g / (1 + np.exp(-g)) * u) @ Wd.T
+    scale = np.sqrt(np.mean(want ** 2))
+    assert np.max(np.abs(full - want)) / scale <= 1e-12
+    assert np.max(np.abs(full - sliced)) / scale <= 1e-12
