@@ -83,14 +83,25 @@ typedef enum {
     MOE_OK = 0,
     MOE_EINVAL = 1,     /* a NULL or misaligned pointer, a negative size, k out of range, wrong handle kind */
     MOE_EDIMS = 2,      /* hidden / inter / slice width not a multiple of 32, or too large */
-    MOE_ESCALE = 3,     /* an E8M0 scale byte is 255 (NaN in the OCP format) */
+    MOE_ESCALE = 3,     /* a scale the format rejects: an E8M0 byte of 255 (NaN in the OCP format); for
+                           group-32 INT4 an FP16 scale that is Inf or NaN, or a zero point above 15 */
     MOE_ENOMEM = 4,     /* the library could not allocate its weight copy */
     MOE_ECUDA = 5,      /* a CUDA runtime call failed (message in moe_last_error) */
     MOE_EWORKSPACE = 6, /* workspace smaller than moe_workspace_bytes() or not 256-byte aligned */
     MOE_EDEVICE = 7     /* a kernel of an earlier call reported a device-side error */
 } MoeStatus;
 
-typedef enum { MOE_W_MXFP4 = 0, MOE_W_BF16 = 1 } MoeWeightFormat;
+/* Weight formats.  MXFP4 and BF16 as in "DeepSeek-V4-Flash on a four-GPU
+ * Ampere workstation" (section "MXFP4 is not NVFP4, and the difference matters
+ * on Ampere").  MOE_W_INT4G32 is the group-32 INT4 format of "Cascadia:
+ * Resident 975B MoE Inference on Eleven AI PCs" (§3.1: packed 4-bit nibbles
+ * with one FP16 scale per 32-value group; §3.5: zero points): the weight is
+ * s * (q - z) for the unsigned code q and its group's FP16 scale s and zero
+ * point z in 0..15.  INT4 layers run on the single-kernel path only: a forward
+ * call outside its range (more than 16*E or 4096 routed slots T*k, more than
+ * 512 routed experts, a dense layer with more than 64 tokens) returns
+ * MOE_EINVAL. */
+typedef enum { MOE_W_MXFP4 = 0, MOE_W_BF16 = 1, MOE_W_INT4G32 = 2 } MoeWeightFormat;
 
 typedef struct {
     int hidden;            /* H, multiple of 32, 32 .. 65536 */
@@ -99,15 +110,20 @@ typedef struct {
     int n_shared;          /* S always-on shared experts (0 .. 64); 0 for a dense layer */
     int k_max;             /* largest k a forward call may ask for, 1 .. min(E, 32); ignored when dense */
     int n_slices;          /* 0: routed MoE layer.  > 0: dense FFN cut into this many slices */
-    MoeWeightFormat fmt;   /* MXFP4 or BF16 weights */
+    MoeWeightFormat fmt;   /* MXFP4, BF16 or group-32 INT4 weights */
 } MoeConfig;
 
-/* One weight matrix.  MXFP4: codes = pack4 bytes [rows][cols/2], scales =
- * E8M0 bytes [rows][cols/32].  BF16: codes = BF16 [rows][cols], scales NULL.
- * Device pointers, any alignment. */
+/* One weight matrix.  MXFP4: codes = pack4 bytes [rows][cols/2] (element 2j
+ * in the low nibble of byte j), scales = E8M0 bytes [rows][cols/32].
+ * BF16: codes = BF16 [rows][cols], scales NULL.  INT4G32: codes as for MXFP4
+ * (unsigned 4-bit codes), scales = FP16 bits [rows][cols/32] (2-byte
+ * aligned), zeros = zero point bytes [rows][cols/32] or NULL (every zero
+ * point 8: the symmetric grid -8..7).  zeros is ignored by the other formats.
+ * Device pointers; any alignment except the INT4 scales'. */
 typedef struct {
     const void *codes;
     const void *scales;
+    const void *zeros;
 } MoeMx;
 
 /* Copy the weights into the library's own storage and return a handle.

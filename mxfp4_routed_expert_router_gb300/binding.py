@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libmoe_gb300.so")
 MOE_OK, MOE_EINVAL, MOE_EDIMS, MOE_ESCALE, MOE_ENOMEM, MOE_ECUDA, MOE_EWORKSPACE, MOE_EDEVICE = range(8)
 STATUS_NAMES = ["MOE_OK", "MOE_EINVAL", "MOE_EDIMS", "MOE_ESCALE", "MOE_ENOMEM", "MOE_ECUDA", "MOE_EWORKSPACE",
                 "MOE_EDEVICE"]
-MOE_W_MXFP4, MOE_W_BF16 = 0, 1
+MOE_W_MXFP4, MOE_W_BF16, MOE_W_INT4G32 = 0, 1, 2
 
 # every symbol include/moe.h declares
 EXPORTED = ("moe_load_weights", "moe_workspace_bytes", "moe_forward", "moe_forward_routed",
@@ -41,7 +41,7 @@ class MoeConfig(ctypes.Structure):
 
 
 class MoeMx(ctypes.Structure):
-    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("zeros", ctypes.c_void_p)]
 
 
 class MoeHostIO(ctypes.Structure):
@@ -125,9 +125,13 @@ def moe_last_error() -> str:
 
 
 def moe_load_weights(cfg: MoeConfig, gate_up: Sequence[Tuple], down: Sequence[Tuple], stream=None) -> int:
-    """Copy weights into the library; gate_up / down are sequences of (codes, scales_or_None)."""
-    gu = (MoeMx * max(1, len(gate_up)))(*[MoeMx(_ptr(c), _ptr(s)) for c, s in gate_up])
-    dn = (MoeMx * max(1, len(down)))(*[MoeMx(_ptr(c), _ptr(s)) for c, s in down])
+    """Copy weights into the library; gate_up / down are sequences of
+    (codes, scales_or_None) or, for INT4G32, (codes, scales, zeros_or_None)."""
+    def mx(m):
+        return MoeMx(_ptr(m[0]), _ptr(m[1]), _ptr(m[2]) if len(m) > 2 else None)
+
+    gu = (MoeMx * max(1, len(gate_up)))(*[mx(m) for m in gate_up])
+    dn = (MoeMx * max(1, len(down)))(*[mx(m) for m in down])
     h = ctypes.c_void_p()
     _check(lib.moe_load_weights(ctypes.byref(cfg), gu, dn, _stream(stream), ctypes.byref(h)))
     return h.value

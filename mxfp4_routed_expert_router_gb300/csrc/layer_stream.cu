@@ -9,7 +9,8 @@
 // and §3.3 Eq. 1; dense FFN as all-active slices, §3.4 Eq. 2; MXFP4 decoded
 // inside the reduction as in "DeepSeek-V4-Flash on a four-GPU Ampere
 // workstation", section "MXFP4 is not NVFP4, and the difference matters on
-// Ampere"):
+// Ampere"; group-32 INT4 with FP16 group scales and zero points, the format of
+// the same Cascadia paper's §3.1, decoded the same way):
 //
 //  phase 0a  tokens are routed (softmax top-k, renormalised; or the caller's
 //            ids and weights are copied and checked) and their FP16 rows x16
@@ -24,10 +25,10 @@
 //            item's weight chunks (one bulk copy per stage) plus its token
 //            rows (one bulk copy per row and plane) into a ring of
 //            shared-memory stages sized by the item's tile class; 8 compute
-//            warps (16 weight rows each, the full K) decode MXFP4 in registers
-//            straight into warp-level MMA fragments (FP16 operands, FP32
-//            accumulation, the E8M0 block scales applied in FP32 to each
-//            32-wide block's partial sum).  gate|up epilogues write h (FP16
+//            warps (16 weight rows each, the full K) decode MXFP4 or INT4 in
+//            registers straight into warp-level MMA fragments (FP16 operands,
+//            FP32 accumulation, the E8M0 or FP16 block scales applied in FP32
+//            to each 32-wide block's partial sum).  gate|up epilogues write h (FP16
 //            hi + lo, scaled per 64-feature block) and hand the item to warp
 //            9, which publishes it to the other CTAs with one release; a
 //            down item's token rows are copied only once its group's h is
@@ -105,8 +106,10 @@ __host__ __device__ constexpr int ls_max(int a, int b) { return a > b ? a : b; }
 // then fit the stage target.
 template <int WFMT, int NT>
 struct LsCfg {
-    static constexpr bool F16 = WFMT == FMT_MXFP4;
-    static constexpr int W_CHUNK = F16 ? CHUNK_MX_BYTES : CHUNK_BF16_BYTES;
+    static constexpr bool F16 = WFMT != FMT_BF16;  // MXFP4 and INT4 codes run FP16 MMAs
+    static constexpr int W_CHUNK = WFMT == FMT_MXFP4  ? CHUNK_MX_BYTES
+                                   : WFMT == FMT_INT4 ? CHUNK_I4_BYTES
+                                                      : CHUNK_BF16_BYTES;
     static constexpr int NTK = NT == 0 ? 1 : NT;  // token tiles of the largest item
     static constexpr int ROWS = 8 * NTK;          // token rows of the largest item
     static constexpr int CTAS = ls_ctas_per_sm(NT);
@@ -266,6 +269,32 @@ __device__ __forceinline__ void decode_e2m1(uint32_t w, uint32_t out[4])
         " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
         : "=r"(out[0]), "=r"(out[1]), "=r"(out[2]), "=r"(out[3])
         : "r"(w));
+}
+
+// FRAG_F16 word of group-32 INT4 codes -> A fragment.  Pair p holds its first
+// code in nibble p and its second in nibble p + 4; 0x6400 | q is the FP16
+// value 1024 + q (ulp 1 there), so subtracting 1024 + z leaves q - z exactly.
+// Pairs 0 and 2 belong to row g (zero point za), pairs 1 and 3 to row g + 8 (zb).
+__device__ __forceinline__ void decode_i4(uint32_t w, uint32_t za, uint32_t zb, uint32_t out[4])
+{
+    const uint32_t ma = (0x6400u + za) * 0x10001u, mb = (0x6400u + zb) * 0x10001u;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const uint32_t v = ((w >> (4 * p)) & 0x000F000Fu) | 0x64006400u;
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(out[p]) : "r"(v), "r"((p & 1) ? mb : ma));
+    }
+}
+
+// FP16 half H of w (H = 0: low) widened to FP32, exactly.
+template <int H>
+__device__ __forceinline__ float f16_half_to_f32(uint32_t w)
+{
+    float f;
+    if (H == 0)
+        asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n cvt.f32.f16 %0, lo;\n}" : "=f"(f) : "r"(w));
+    else
+        asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n cvt.f32.f16 %0, hi;\n}" : "=f"(f) : "r"(w));
+    return f;
 }
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n)
@@ -703,7 +732,7 @@ __device__ __forceinline__ LsItem ls_item(int u, int total_gu, int rt_gu, int rt
     return it;
 }
 
-// a down item of at most four tokens (MXFP4) packs each token's h hi and lo
+// a down item of at most four tokens (FP16 path: MXFP4 or INT4) packs each token's h hi and lo
 // planes into adjacent columns of its 8-token MMA tile, except in the kernel
 // for up to 64 tokens (NT = 8), whose batches hold many down items of five to
 // eight tokens: there both class-1 variants cost registers, and moving those
@@ -711,7 +740,7 @@ __device__ __forceinline__ LsItem ls_item(int u, int total_gu, int rt_gu, int rt
 template <int WFMT, int NT>
 __device__ __forceinline__ bool ls_packed(const LsItem &it)
 {
-    return WFMT == FMT_MXFP4 && NT != 8 && !it.gu && it.nvalid <= 4;
+    return LsCfg<WFMT, NT>::F16 && NT != 8 && !it.gu && it.nvalid <= 4;
 }
 
 // tile class of an item: in the kernel for up to 32 tokens (NT = 4) down items
@@ -721,7 +750,7 @@ template <int WFMT, int NT>
 __device__ __forceinline__ int ls_nti_item(const LsItem &it)
 {
     const int c = ls_nti<NT>(it.nvalid);
-    return WFMT == FMT_MXFP4 && NT == 4 && !it.gu && it.nvalid > 4 && c == 1 ? 2 : c;
+    return LsCfg<WFMT, NT>::F16 && NT == 4 && !it.gu && it.nvalid > 4 && c == 1 ? 2 : c;
 }
 
 // token of row r of an item: routed positions look it up (tokp: token of each
@@ -841,20 +870,42 @@ __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem 
             const uint8_t *bk = brow + ks * 128;
             if (F16) {
                 // weights decode unscaled; each 32-wide block's partial sum takes the
-                // row's block scale 2^(e-127) in FP32 (a BF16 scale widened exactly)
-                const uint2 sc = *reinterpret_cast<const uint2 *>(wch + CHUNK_MX_CODE_BYTES + (wg * 8 + g) * 8);
+                // row's block scale in FP32: MXFP4 2^(e-127) (a BF16 scale widened
+                // exactly), INT4 the group's FP16 scale (widened exactly)
                 const uint4 wv = *reinterpret_cast<const uint4 *>(wch + ((wg * 2 + kh) * 32 + lane) * 16);
                 const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
-                const uint32_t bx = kh ? ue8m0x2_bf16x2<1>(sc.x) : ue8m0x2_bf16x2<0>(sc.x);
-                const uint32_t by = kh ? ue8m0x2_bf16x2<1>(sc.y) : ue8m0x2_bf16x2<0>(sc.y);
-                const float sg[2] = {__uint_as_float(bx << 16), __uint_as_float(bx & 0xFFFF0000u)};
-                const float sg8[2] = {__uint_as_float(by << 16), __uint_as_float(by & 0xFFFF0000u)};
+                float sg[2], sg8[2];
                 // the four A fragments of this half-chunk, decoded once for every token tile
                 uint32_t af[4][4];
+                if constexpr (WFMT == FMT_MXFP4) {
+                    const uint2 sc = *reinterpret_cast<const uint2 *>(wch + CHUNK_MX_CODE_BYTES + (wg * 8 + g) * 8);
+                    const uint32_t bx = kh ? ue8m0x2_bf16x2<1>(sc.x) : ue8m0x2_bf16x2<0>(sc.x);
+                    const uint32_t by = kh ? ue8m0x2_bf16x2<1>(sc.y) : ue8m0x2_bf16x2<0>(sc.y);
+                    sg[0] = __uint_as_float(bx << 16);
+                    sg[1] = __uint_as_float(bx & 0xFFFF0000u);
+                    sg8[0] = __uint_as_float(by << 16);
+                    sg8[1] = __uint_as_float(by & 0xFFFF0000u);
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj)
-                    if (jj < 2 * nblk)
-                        decode_e2m1(words[jj], af[jj]);
+                    for (int jj = 0; jj < 4; ++jj)
+                        if (jj < 2 * nblk)
+                            decode_e2m1(words[jj], af[jj]);
+                } else {
+                    // rows g and g+8: FP16 scales of blocks 0..3 each, then their zero points
+                    const uint4 s4 = *reinterpret_cast<const uint4 *>(wch + CHUNK_MX_CODE_BYTES + (wg * 8 + g) * 16);
+                    const uint2 z2 = *reinterpret_cast<const uint2 *>(wch + CHUNK_MX_CODE_BYTES + CHUNK_I4_SCALE_BYTES +
+                                                                      (wg * 8 + g) * 8);
+                    const uint32_t sa = kh ? s4.y : s4.x, sb = kh ? s4.w : s4.z;  // blocks 2kh, 2kh+1
+                    sg[0] = f16_half_to_f32<0>(sa);
+                    sg[1] = f16_half_to_f32<1>(sa);
+                    sg8[0] = f16_half_to_f32<0>(sb);
+                    sg8[1] = f16_half_to_f32<1>(sb);
+                    const uint32_t za = kh ? z2.x >> 16 : z2.x, zb = kh ? z2.y >> 16 : z2.y;
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+                        if (jj < 2 * nblk)
+                            decode_i4(words[jj], (za >> (8 * (jj >> 1))) & 0xFFu, (zb >> (8 * (jj >> 1))) & 0xFFu,
+                                      af[jj]);
+                }
                 const int *hs_st = reinterpret_cast<const int *>(st + HS_OFF) + (slice - sl0);
 #pragma unroll
                 for (int nt = 0; nt < NTI; ++nt) {
@@ -1367,9 +1418,9 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
             if (NT <= 1 || nti == 1) {
                 // class 1: the packed-down variant also runs gate|up items (identical there)
                 if constexpr (NT == 0 || NT == 4) {
-                    ok = LS_ITEM(ls_compute_item, 1, WFMT == FMT_MXFP4);
+                    ok = LS_ITEM(ls_compute_item, 1, LsCfg<WFMT, NT>::F16);
                 } else if constexpr (NT <= 2) {
-                    constexpr bool PKV = WFMT == FMT_MXFP4;
+                    constexpr bool PKV = LsCfg<WFMT, NT>::F16;
                     if (PKV && (it.gu || ls_packed<WFMT, NT>(it)))
                         ok = LS_ITEM(ls_compute_item, 1, PKV);
                     else
@@ -1461,6 +1512,9 @@ template <int WFMT, int NT>
 cudaError_t ls_launch(LayerArgs a, cudaStream_t st)
 {
     using C = LsCfg<WFMT, NT>;
+    // the stages hold whole chunks of this format's size
+    if (a.chunk_bytes != C::W_CHUNK)
+        return cudaErrorInvalidValue;
     a.R = ls_ring_depth<WFMT, NT>(a.G, a.n, a.E, a.T);
     if (a.R < 2)
         return cudaErrorNotSupported;
@@ -1529,8 +1583,9 @@ bool layer_stream_fits(const Plan &p, int fmt)
         return false;
     const int nt = ls_nt(p.T);
     const int n = p.T * p.k;
-    const int R = fmt == FMT_MXFP4 ? ls_depth_fmt<FMT_MXFP4>(nt, p.G, n, p.E, p.T)
-                                   : ls_depth_fmt<FMT_BF16>(nt, p.G, n, p.E, p.T);
+    const int R = fmt == FMT_MXFP4  ? ls_depth_fmt<FMT_MXFP4>(nt, p.G, n, p.E, p.T)
+                  : fmt == FMT_INT4 ? ls_depth_fmt<FMT_INT4>(nt, p.G, n, p.E, p.T)
+                                    : ls_depth_fmt<FMT_BF16>(nt, p.G, n, p.E, p.T);
     return R >= 2;
 }
 
@@ -1580,7 +1635,9 @@ cudaError_t launch_layer_stream(const Plan &p, const WeightStore &gu, const Weig
     a.sync = p.sync;
     a.err = p.err;
     const int nt = ls_nt(p.T);
-    return fmt == FMT_MXFP4 ? ls_launch_fmt<FMT_MXFP4>(nt, a, st) : ls_launch_fmt<FMT_BF16>(nt, a, st);
+    return fmt == FMT_MXFP4  ? ls_launch_fmt<FMT_MXFP4>(nt, a, st)
+           : fmt == FMT_INT4 ? ls_launch_fmt<FMT_INT4>(nt, a, st)
+                             : ls_launch_fmt<FMT_BF16>(nt, a, st);
 }
 
 }  // namespace moe

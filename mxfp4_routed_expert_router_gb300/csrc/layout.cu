@@ -30,6 +30,29 @@ __device__ __forceinline__ uint8_t src_scale(const SrcMat *src, int srow, int k,
     return e;
 }
 
+// Group-32 INT4: the FP16 scale bits and the zero point of element k's group.
+// Past the logical end the scale is 0 and the zero point 8 (weight 0).  A scale
+// with exponent bits 31 (Inf or NaN) or a zero point above 15 sets *bad_scale.
+__device__ __forceinline__ uint16_t src_i4_scale(const SrcMat *src, int srow, int k, int K, int *bad_scale)
+{
+    if (srow < 0 || k >= K)
+        return 0;
+    const uint16_t s = reinterpret_cast<const uint16_t *>(src->scales)[srow * src->scale_stride + k / 32];
+    if ((s & 0x7C00u) == 0x7C00u)
+        atomicOr(bad_scale, 1);
+    return s;
+}
+
+__device__ __forceinline__ uint8_t src_i4_zero(const SrcMat *src, int srow, int k, int K, int *bad_scale)
+{
+    if (srow < 0 || k >= K || !src->zeros)
+        return 8;
+    const uint8_t z = src->zeros[srow * src->scale_stride + k / 32];
+    if (z > 15)
+        atomicOr(bad_scale, 1);
+    return z;
+}
+
 __device__ __forceinline__ uint16_t src_bf16(const SrcMat *src, int srow, int k, int K)
 {
     if (srow < 0 || k >= K)
@@ -145,9 +168,9 @@ __global__ void repack_frag_kernel(int fmt, int gate_up, SrcMat gate, SrcMat up,
     }
 }
 
-// FRAG_F16 layout (see moe_internal.cuh).
-__global__ void repack_frag_f16_kernel(int gate_up, SrcMat gate, SrcMat up, uint8_t *dst, int row_tiles, int kchunks,
-                                       int chunk_bytes, int logical_rows, int K, int *bad_scale)
+// FRAG_F16 layout (see moe_internal.cuh), MXFP4 or group-32 INT4 codes.
+__global__ void repack_frag_f16_kernel(int fmt, int gate_up, SrcMat gate, SrcMat up, uint8_t *dst, int row_tiles,
+                                       int kchunks, int chunk_bytes, int logical_rows, int K, int *bad_scale)
 {
     long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (long long)row_tiles * kchunks * 256)
@@ -163,13 +186,35 @@ __global__ void repack_frag_f16_kernel(int gate_up, SrcMat gate, SrcMat up, uint
     const int k0 = kc * CHUNK_K;
     for (int j = 0; j < 8; ++j) {
         const int ka = k0 + 16 * j + 2 * q, kb = ka + 8;
-        const uint32_t b0 = src_code(src0, srow0, ka, K) | src_code(src0, srow0, ka + 1, K) << 4;
-        const uint32_t b1 = src_code(src1, srow1, ka, K) | src_code(src1, srow1, ka + 1, K) << 4;
-        const uint32_t b2 = src_code(src0, srow0, kb, K) | src_code(src0, srow0, kb + 1, K) << 4;
-        const uint32_t b3 = src_code(src1, srow1, kb, K) | src_code(src1, srow1, kb + 1, K) << 4;
-        reinterpret_cast<uint32_t *>(chunk)[((w * 2 + j / 4) * 32 + t) * 4 + j % 4] = b0 | b1 << 8 | b2 << 16 | b3 << 24;
+        uint32_t word;
+        if (fmt == FMT_INT4) {
+            // pair p: first element in nibble p, second in nibble p + 4
+            const uint32_t first[4] = {src_code(src0, srow0, ka, K), src_code(src1, srow1, ka, K),
+                                       src_code(src0, srow0, kb, K), src_code(src1, srow1, kb, K)};
+            const uint32_t second[4] = {src_code(src0, srow0, ka + 1, K), src_code(src1, srow1, ka + 1, K),
+                                        src_code(src0, srow0, kb + 1, K), src_code(src1, srow1, kb + 1, K)};
+            word = 0;
+            for (int p = 0; p < 4; ++p)
+                word |= first[p] << (4 * p) | second[p] << (4 * p + 16);
+        } else {
+            const uint32_t b0 = src_code(src0, srow0, ka, K) | src_code(src0, srow0, ka + 1, K) << 4;
+            const uint32_t b1 = src_code(src1, srow1, ka, K) | src_code(src1, srow1, ka + 1, K) << 4;
+            const uint32_t b2 = src_code(src0, srow0, kb, K) | src_code(src0, srow0, kb + 1, K) << 4;
+            const uint32_t b3 = src_code(src1, srow1, kb, K) | src_code(src1, srow1, kb + 1, K) << 4;
+            word = b0 | b1 << 8 | b2 << 16 | b3 << 24;
+        }
+        reinterpret_cast<uint32_t *>(chunk)[((w * 2 + j / 4) * 32 + t) * 4 + j % 4] = word;
     }
-    if (q == 0) {
+    if (fmt == FMT_INT4 && q == 0) {
+        uint16_t *sc = reinterpret_cast<uint16_t *>(chunk + CHUNK_MX_CODE_BYTES + (w * 8 + g) * 16);
+        uint8_t *zp = chunk + CHUNK_MX_CODE_BYTES + CHUNK_I4_SCALE_BYTES + (w * 8 + g) * 8;
+        for (int b = 0; b < 4; ++b) {
+            sc[b] = src_i4_scale(src0, srow0, k0 + 32 * b, K, bad_scale);
+            sc[4 + b] = src_i4_scale(src1, srow1, k0 + 32 * b, K, bad_scale);
+            zp[b] = src_i4_zero(src0, srow0, k0 + 32 * b, K, bad_scale);
+            zp[4 + b] = src_i4_zero(src1, srow1, k0 + 32 * b, K, bad_scale);
+        }
+    } else if (q == 0) {
         uint8_t *sc = chunk + CHUNK_MX_CODE_BYTES + (w * 8 + g) * 8;
         for (int b = 0; b < 4; ++b) {
             sc[b] = src_scale(src0, srow0, k0 + 32 * b, K, bad_scale);
@@ -185,7 +230,7 @@ cudaError_t launch_repack(int fmt, int layout, bool gate_up, const SrcMat &gate,
         const int logical_rows = gate_up ? I : H;
         const long long total = (long long)ws.row_tiles * ws.kchunks * 256;
         repack_frag_f16_kernel<<<(unsigned)((total + 127) / 128), 128, 0, st>>>(
-            gate_up ? 1 : 0, gate, up, ws.base + (size_t)group * ws.group_bytes, ws.row_tiles, ws.kchunks,
+            fmt, gate_up ? 1 : 0, gate, up, ws.base + (size_t)group * ws.group_bytes, ws.row_tiles, ws.kchunks,
             ws.chunk_bytes, logical_rows, ws.cols, bad_scale);
         return cudaGetLastError();
     }

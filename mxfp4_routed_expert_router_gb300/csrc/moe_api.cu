@@ -64,7 +64,7 @@ void init_store(WeightStore &w, int rows_per_group_tiles_basis, bool gate_up, in
     w.row_tiles = gate_up ? (rows_per_group_tiles_basis + GU_FEATURES_PER_TILE - 1) / GU_FEATURES_PER_TILE
                           : (rows_per_group_tiles_basis + TILE_ROWS - 1) / TILE_ROWS;
     w.kchunks = (K + CHUNK_K - 1) / CHUNK_K;
-    w.chunk_bytes = fmt == FMT_MXFP4 ? CHUNK_MX_BYTES : CHUNK_BF16_BYTES;
+    w.chunk_bytes = fmt == FMT_MXFP4 ? CHUNK_MX_BYTES : fmt == FMT_INT4 ? CHUNK_I4_BYTES : CHUNK_BF16_BYTES;
     w.group_bytes = (size_t)w.row_tiles * w.kchunks * w.chunk_bytes;
 }
 
@@ -157,6 +157,9 @@ MoeStatus run_layer(MoeHandle *h, const void *x, const float *logits, const int 
             h->profiled = true;
         return MOE_OK;
     }
+    if (h->fmt == FMT_INT4)
+        return fail(MOE_EINVAL, "INT4 weights run on the single-kernel path only; this batch (T=%d, k=%d) is "
+                                "outside its range", T, k);
     mark(0);
     if (h->E > 0) {
         if (ids_in) {
@@ -229,7 +232,7 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
     if (!cfg || !gate_up || !down || !out)
         return fail(MOE_EINVAL, "moe_load_weights: NULL argument");
     const MoeConfig c = *cfg;
-    if (c.fmt != MOE_W_MXFP4 && c.fmt != MOE_W_BF16)
+    if (c.fmt != MOE_W_MXFP4 && c.fmt != MOE_W_BF16 && c.fmt != MOE_W_INT4G32)
         return fail(MOE_EINVAL, "unknown weight format %d", (int)c.fmt);
     if (c.hidden <= 0 || c.inter <= 0 || c.hidden % 32 || c.inter % 32 || c.hidden > 65536 || c.inter > 262144)
         return fail(MOE_EDIMS, "hidden (%d) and inter (%d) must be positive multiples of 32 (hidden <= 65536)",
@@ -259,14 +262,24 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
         k_max = c.k_max;
     }
     G = E + S;
-    const int fmt = c.fmt == MOE_W_MXFP4 ? FMT_MXFP4 : FMT_BF16;
+    const int fmt = c.fmt == MOE_W_MXFP4 ? FMT_MXFP4 : c.fmt == MOE_W_INT4G32 ? FMT_INT4 : FMT_BF16;
+    const bool nib = fmt != FMT_BF16;               // 4-bit codes
+    const long long ssz = fmt == FMT_INT4 ? 2 : 1;  // bytes per scale
     const int n_gu = dense ? 2 : G, n_dn = dense ? 1 : G;
     for (int i = 0; i < n_gu; ++i)
-        if (!gate_up[i].codes || (fmt == FMT_MXFP4 && !gate_up[i].scales))
+        if (!gate_up[i].codes || (nib && !gate_up[i].scales))
             return fail(MOE_EINVAL, "gate_up[%d] has a NULL pointer", i);
     for (int i = 0; i < n_dn; ++i)
-        if (!down[i].codes || (fmt == FMT_MXFP4 && !down[i].scales))
+        if (!down[i].codes || (nib && !down[i].scales))
             return fail(MOE_EINVAL, "down[%d] has a NULL pointer", i);
+    if (fmt == FMT_INT4) {
+        for (int i = 0; i < n_gu; ++i)
+            if (!aligned(gate_up[i].scales, 2))
+                return fail(MOE_EINVAL, "gate_up[%d].scales (FP16) is not 2-byte aligned", i);
+        for (int i = 0; i < n_dn; ++i)
+            if (!aligned(down[i].scales, 2))
+                return fail(MOE_EINVAL, "down[%d].scales (FP16) is not 2-byte aligned", i);
+    }
 
     MoeHandle *h = new (std::nothrow) MoeHandle();
     if (!h)
@@ -289,7 +302,9 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
     init_store(h->dn, c.hidden, false, I, fmt);
     h->gu_f = h->gu;
     h->dn_f = h->dn;
-    const int f_layout = fmt == FMT_MXFP4 ? LAYOUT_FRAG_F16 : LAYOUT_FRAG;
+    const int f_layout = nib ? LAYOUT_FRAG_F16 : LAYOUT_FRAG;
+    // INT4 runs on the single kernel only, which reads the FRAG copy
+    const bool tile = fmt != FMT_INT4;
     if ((e = cudaHostAlloc((void **)&h->err_host, 2 * sizeof(int), cudaHostAllocMapped)) != cudaSuccess) {
         destroy(h);
         return cuda_fail(e, "cudaHostAlloc");
@@ -300,46 +315,53 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
         destroy(h);
         return cuda_fail(e, "cudaHostGetDevicePointer");
     }
-    if (cudaMalloc(&h->gu.base, h->gu.group_bytes * G) != cudaSuccess ||
-        cudaMalloc(&h->dn.base, h->dn.group_bytes * G) != cudaSuccess ||
+    if ((tile && cudaMalloc(&h->gu.base, h->gu.group_bytes * G) != cudaSuccess) ||
+        (tile && cudaMalloc(&h->dn.base, h->dn.group_bytes * G) != cudaSuccess) ||
         cudaMalloc(&h->gu_f.base, h->gu_f.group_bytes * G) != cudaSuccess ||
         cudaMalloc(&h->dn_f.base, h->dn_f.group_bytes * G) != cudaSuccess) {
         cudaGetLastError();
         destroy(h);
         return fail(MOE_ENOMEM, "device allocation of %zu bytes of weights failed",
-                    2 * (h->gu.group_bytes + h->dn.group_bytes) * (size_t)G);
+                    (tile ? 2 : 1) * (h->gu.group_bytes + h->dn.group_bytes) * (size_t)G);
     }
     int *bad_scale = &h->err_dev[1];
-    const long long esz = fmt == FMT_MXFP4 ? 1 : 2;  // bytes per code unit of a row (MXFP4: per 2 elements)
+    // scale (and INT4 zero point) arrays advanced by a number of elements; NULL
+    // (BF16 scales, absent zero points) stays NULL
+    auto sc_at = [&](const void *p, long long elems) -> const uint8_t * {
+        return nib && p ? (const uint8_t *)p + elems * ssz : nullptr;
+    };
+    auto zp_at = [&](const void *p, long long elems) -> const uint8_t * {
+        return fmt == FMT_INT4 && p ? (const uint8_t *)p + elems : nullptr;
+    };
     for (int g = 0; g < G; ++g) {
         SrcMat gate{}, up{}, dn{};
+        const long long gs = nib ? c.hidden / 2 : (long long)c.hidden * 2;  // code bytes of a gate|up row
+        const long long ss = c.hidden / 32;                                  // scales of a gate|up row
         if (dense) {
             // slice g: gate/up rows [g*I, (g+1)*I) of the unsliced W_g / W_u; down columns likewise
-            const long long gs = fmt == FMT_MXFP4 ? c.hidden / 2 : (long long)c.hidden * 2;
-            const long long ss = c.hidden / 32;
-            gate = {(const uint8_t *)gate_up[0].codes + (long long)g * I * gs,
-                    fmt == FMT_MXFP4 ? (const uint8_t *)gate_up[0].scales + (long long)g * I * ss : nullptr, gs, ss};
-            up = {(const uint8_t *)gate_up[1].codes + (long long)g * I * gs,
-                  fmt == FMT_MXFP4 ? (const uint8_t *)gate_up[1].scales + (long long)g * I * ss : nullptr, gs, ss};
-            const long long dstride = fmt == FMT_MXFP4 ? c.inter / 2 : (long long)c.inter * 2;
+            const long long r0 = (long long)g * I;
+            gate = {(const uint8_t *)gate_up[0].codes + r0 * gs, sc_at(gate_up[0].scales, r0 * ss), gs, ss,
+                    zp_at(gate_up[0].zeros, r0 * ss)};
+            up = {(const uint8_t *)gate_up[1].codes + r0 * gs, sc_at(gate_up[1].scales, r0 * ss), gs, ss,
+                  zp_at(gate_up[1].zeros, r0 * ss)};
+            const long long dstride = nib ? c.inter / 2 : (long long)c.inter * 2;
             const long long dss = c.inter / 32;
-            const long long col_off = fmt == FMT_MXFP4 ? (long long)g * I / 2 : (long long)g * I * 2;
-            dn = {(const uint8_t *)down[0].codes + col_off,
-                  fmt == FMT_MXFP4 ? (const uint8_t *)down[0].scales + (long long)g * I / 32 : nullptr, dstride, dss};
+            const long long col_off = nib ? (long long)g * I / 2 : (long long)g * I * 2;
+            dn = {(const uint8_t *)down[0].codes + col_off, sc_at(down[0].scales, (long long)g * I / 32), dstride,
+                  dss, zp_at(down[0].zeros, (long long)g * I / 32)};
         } else {
-            const long long gs = fmt == FMT_MXFP4 ? c.hidden / 2 : (long long)c.hidden * 2;
-            const long long ss = c.hidden / 32;
-            gate = {(const uint8_t *)gate_up[g].codes, (const uint8_t *)gate_up[g].scales, gs, ss};
-            up = {(const uint8_t *)gate_up[g].codes + (long long)I * gs,
-                  fmt == FMT_MXFP4 ? (const uint8_t *)gate_up[g].scales + (long long)I * ss : nullptr, gs, ss};
-            const long long dstride = fmt == FMT_MXFP4 ? I / 2 : (long long)I * 2;
-            dn = {(const uint8_t *)down[g].codes, (const uint8_t *)down[g].scales, dstride, I / 32};
+            gate = {(const uint8_t *)gate_up[g].codes, sc_at(gate_up[g].scales, 0), gs, ss,
+                    zp_at(gate_up[g].zeros, 0)};
+            up = {(const uint8_t *)gate_up[g].codes + (long long)I * gs, sc_at(gate_up[g].scales, (long long)I * ss),
+                  gs, ss, zp_at(gate_up[g].zeros, (long long)I * ss)};
+            const long long dstride = nib ? I / 2 : (long long)I * 2;
+            dn = {(const uint8_t *)down[g].codes, sc_at(down[g].scales, 0), dstride, I / 32,
+                  zp_at(down[g].zeros, 0)};
         }
-        (void)esz;
-        if ((e = launch_repack(fmt, LAYOUT_TILE, true, gate, up, h->gu, g, I, c.hidden, bad_scale, st)) !=
-                cudaSuccess ||
-            (e = launch_repack(fmt, LAYOUT_TILE, false, dn, dn, h->dn, g, I, c.hidden, bad_scale, st)) !=
-                cudaSuccess ||
+        if ((tile && (e = launch_repack(fmt, LAYOUT_TILE, true, gate, up, h->gu, g, I, c.hidden, bad_scale, st)) !=
+                         cudaSuccess) ||
+            (tile && (e = launch_repack(fmt, LAYOUT_TILE, false, dn, dn, h->dn, g, I, c.hidden, bad_scale, st)) !=
+                         cudaSuccess) ||
             (e = launch_repack(fmt, f_layout, true, gate, up, h->gu_f, g, I, c.hidden, bad_scale, st)) !=
                 cudaSuccess ||
             (e = launch_repack(fmt, f_layout, false, dn, dn, h->dn_f, g, I, c.hidden, bad_scale, st)) !=
@@ -354,7 +376,8 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
     }
     if (*(volatile int *)bad_scale) {
         destroy(h);
-        return fail(MOE_ESCALE, "an E8M0 scale byte is 255 (NaN)");
+        return fail(MOE_ESCALE, fmt == FMT_INT4 ? "an INT4 FP16 scale is Inf or NaN, or a zero point is above 15"
+                                                : "an E8M0 scale byte is 255 (NaN)");
     }
     *out = h;
     return MOE_OK;

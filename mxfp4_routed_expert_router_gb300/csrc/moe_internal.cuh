@@ -35,6 +35,7 @@ namespace moe {
 //          [8192 + (w*8 + g)*8, +8)  scales: row 16w+g blocks 0..3, then row
 //                                    16w+g+8 blocks 0..3
 //   BF16:  [((w*8 + j)*32 + t)*16, +16)  the 8 BF16 values in that order
+//   INT4 (group-32 INT4, FRAG_F16 only): see FRAG_F16 below
 //
 // Row order inside a row tile (both layouts): r = 16*w + i.
 //   gate|up matrices: feature n = 64*tile + 8*w + (i % 8), of W_g when i < 8
@@ -49,6 +50,9 @@ constexpr int CHUNK_MX_CODE_BYTES = TILE_ROWS * CHUNK_K / 2;        // 8192
 constexpr int CHUNK_MX_SCALE_BYTES = TILE_ROWS * CHUNK_K / 32;      // 512
 constexpr int CHUNK_MX_BYTES = CHUNK_MX_CODE_BYTES + CHUNK_MX_SCALE_BYTES;  // 8704
 constexpr int CHUNK_BF16_BYTES = TILE_ROWS * CHUNK_K * 2;           // 32768
+constexpr int CHUNK_I4_SCALE_BYTES = TILE_ROWS * CHUNK_K / 32 * 2;  // 1024: FP16 group scales
+constexpr int CHUNK_I4_ZERO_BYTES = TILE_ROWS * CHUNK_K / 32;       // 512: zero points
+constexpr int CHUNK_I4_BYTES = CHUNK_MX_CODE_BYTES + CHUNK_I4_SCALE_BYTES + CHUNK_I4_ZERO_BYTES;  // 9728
 constexpr int HALF_K = CHUNK_K / 2;                                 // K of one pipeline stage
 
 enum ChunkLayout { LAYOUT_TILE = 0, LAYOUT_FRAG = 1, LAYOUT_FRAG_F16 = 2 };
@@ -62,6 +66,14 @@ enum ChunkLayout { LAYOUT_TILE = 0, LAYOUT_FRAG = 1, LAYOUT_FRAG_F16 = 2 };
 // The codes decode to FP16 unscaled (exactly: |v| <= 6); the raw E8M0 bytes
 // (same positions as in FRAG) scale each 32-wide block's MMA partial sum in
 // FP32, where every power of two 2^(e-127), e in [0, 254], is exact.
+// Group-32 INT4 weights use the same word positions, with the fragment's
+// element pair p (byte p above) in nibbles p (first element) and p + 4
+// (second), so that one shift and one mask put a pair in the two halves of a
+// word; the codes decode exactly to FP16 q - z, and each block's MMA partial
+// sum takes the group's FP16 scale in FP32.  After the codes:
+//   [8192 + (w*8 + g)*16, +16)         FP16 scales: row 16w+g blocks 0..3, then
+//                                      row 16w+g+8 blocks 0..3
+//   [9216 + (w*8 + g)*8, +8)           zero points (bytes), same order
 // FP16 token rows (x16 and its gathered copies) store K in a permuted order
 // inside every 16-element group so that a lane's two MMA B registers are
 // adjacent: physical element 4q + c (q, c in 0..3) holds logical element
@@ -73,7 +85,7 @@ __host__ __device__ constexpr int x16_phys_k(int k) { return 4 * ((k & 7) >> 1) 
 __host__ __device__ constexpr int gu_row_feature(int tile, int r) { return tile * 64 + 8 * (r >> 4) + (r & 7); }
 __host__ __device__ constexpr bool gu_row_is_up(int r) { return (r & 8) != 0; }
 
-enum WeightFormat { FMT_MXFP4 = 0, FMT_BF16 = 1 };
+enum WeightFormat { FMT_MXFP4 = 0, FMT_BF16 = 1, FMT_INT4 = 2 };
 
 struct WeightStore {
     uint8_t *base = nullptr;  // device
@@ -86,12 +98,15 @@ struct WeightStore {
 };
 
 // A caller-side source matrix for the repack: row r starts at
-// codes + r * code_stride (bytes), its scales at scales + r * scale_stride.
+// codes + r * code_stride (bytes); its scales are elements
+// r * scale_stride .. of `scales` (bytes for MXFP4, FP16 for INT4) and its
+// INT4 zero points bytes r * scale_stride .. of `zeros` (NULL: all 8).
 struct SrcMat {
     const uint8_t *codes;
     const uint8_t *scales;
     long long code_stride;
     long long scale_stride;
+    const uint8_t *zeros;
 };
 
 // ---------------------------------------------------------------- forward plan

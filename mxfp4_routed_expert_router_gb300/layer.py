@@ -26,6 +26,11 @@ def u8_tensor(a: np.ndarray, device="cuda") -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a)).to(device)
 
 
+def u16_tensor(a: np.ndarray, device="cuda") -> torch.Tensor:
+    """16-bit patterns (e.g. FP16 scale bits) as an int16 tensor, bits unchanged."""
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint16).view(np.int16)).to(device)
+
+
 class MoeLayer:
     """Owns a library handle for one synthetic layer configuration."""
 
@@ -35,13 +40,16 @@ class MoeLayer:
         self.dense = cfg.dense
         self._ws = None
         self.handle = None
-        fmt = B.MOE_W_BF16 if cfg.weight_format == "bf16" else B.MOE_W_MXFP4
+        fmt = {"bf16": B.MOE_W_BF16, "mxfp4": B.MOE_W_MXFP4, "int4g32": B.MOE_W_INT4G32}[cfg.weight_format]
         if cfg.dense:
             c = B.MoeConfig(hidden=cfg.hidden, inter=cfg.inter, n_experts=cfg.n_slices, n_shared=0, k_max=0,
                             n_slices=cfg.n_slices, fmt=fmt)
             g, u, d = wl.dense_weights(cfg)
             if fmt == B.MOE_W_BF16:
                 staged = [(bf16_tensor(a, device), None) for a in (g, u, d)]
+            elif fmt == B.MOE_W_INT4G32:
+                staged = [(u8_tensor(a[0], device), u16_tensor(a[1], device), u8_tensor(a[2], device))
+                          for a in (g, u, d)]
             else:
                 staged = [(u8_tensor(a[0], device), u8_tensor(a[1], device)) for a in (g, u, d)]
             gate_up, down = staged[:2], staged[2:]
@@ -54,9 +62,15 @@ class MoeLayer:
                 return wl.expert_weights(cfg, e)
 
             with cf.ThreadPoolExecutor(max_workers=8) as ex:
-                for gc, gs, dc, ds in ex.map(gen, range(cfg.n_groups)):
-                    gate_up.append((u8_tensor(gc, device), u8_tensor(gs, device)))
-                    down.append((u8_tensor(dc, device), u8_tensor(ds, device)))
+                for w in ex.map(gen, range(cfg.n_groups)):
+                    if fmt == B.MOE_W_INT4G32:
+                        gc, gs, dc, ds, gz, dz = w
+                        gate_up.append((u8_tensor(gc, device), u16_tensor(gs, device), u8_tensor(gz, device)))
+                        down.append((u8_tensor(dc, device), u16_tensor(ds, device), u8_tensor(dz, device)))
+                    else:
+                        gc, gs, dc, ds = w
+                        gate_up.append((u8_tensor(gc, device), u8_tensor(gs, device)))
+                        down.append((u8_tensor(dc, device), u8_tensor(ds, device)))
         self.config = c
         self.handle = B.moe_load_weights(c, gate_up, down, stream)
         del gate_up, down

@@ -72,7 +72,7 @@ class LayerConfig:
     # dense layer only
     dense: bool = False
     n_slices: int = 0
-    weight_format: str = "mxfp4"    # "mxfp4" | "bf16"
+    weight_format: str = "mxfp4"    # "mxfp4" | "bf16" | "int4g32"
 
     @property
     def n_groups(self) -> int:
@@ -201,13 +201,28 @@ def i4_matrix(rng: np.random.Generator, rows: int, cols: int, scale_lo: float, s
     return codes, scales, zeros
 
 
-def expert_weights(cfg: LayerConfig, e: int):
-    """MXFP4 weights of expert e (0..E-1 routed, E..E+S-1 shared).
+def _i4_scale_range(cfg: LayerConfig):
+    # group-32 INT4 scales log-uniform over the same powers of two as the MXFP4
+    # block scales, halved (|q - z| reaches 15 where |v(c)| reaches 6); zero
+    # points uniform in [6, 10]
+    return 2.0 ** (cfg.e8m0_lo - 128), 2.0 ** (cfg.e8m0_hi - 128), 6, 10
 
-    Returns (gate_up_codes [2I, H/2], gate_up_scales [2I, H/32],
-             down_codes [H, I/2], down_scales [H, I/32]), all uint8.
+
+def expert_weights(cfg: LayerConfig, e: int):
+    """Weights of expert e (0..E-1 routed, E..E+S-1 shared).
+
+    MXFP4: (gate_up_codes [2I, H/2], gate_up_scales [2I, H/32],
+            down_codes [H, I/2], down_scales [H, I/32]), all uint8.
+    INT4G32: (gate_up_codes, gate_up_scales, down_codes, down_scales,
+              gate_up_zeros, down_zeros): scales are FP16 bits (uint16), the
+              rest uint8, shapes as for MXFP4.
     """
     H, I = cfg.hidden, cfg.inter
+    if cfg.weight_format == "int4g32":
+        lo, hi, zlo, zhi = _i4_scale_range(cfg)
+        gc, gs, gz = i4_matrix(_rng(cfg.wseed, _TAG_GATE_UP, e), 2 * I, H, lo, hi, zlo, zhi)
+        dc, ds, dz = i4_matrix(_rng(cfg.wseed, _TAG_DOWN, e), H, I, lo, hi, zlo, zhi)
+        return gc, gs, dc, ds, gz, dz
     gc, gs = mx_matrix(_rng(cfg.wseed, _TAG_GATE_UP, e), 2 * I, H, cfg.e8m0_lo, cfg.e8m0_hi)
     dc, ds = mx_matrix(_rng(cfg.wseed, _TAG_DOWN, e), H, I, cfg.e8m0_lo, cfg.e8m0_hi)
     return gc, gs, dc, ds
@@ -218,6 +233,7 @@ def dense_weights(cfg: LayerConfig):
 
     BF16: (W_g [I, H], W_u [I, H], W_d [H, I]) as uint16 bits, N(0, 0.02).
     MXFP4: ((g_codes, g_scales), (u_codes, u_scales), (d_codes, d_scales)).
+    INT4G32: ((g_codes, g_scales, g_zeros), (u_...), (d_...)).
     """
     H, I = cfg.hidden, cfg.inter
     if cfg.weight_format == "bf16":
@@ -226,6 +242,10 @@ def dense_weights(cfg: LayerConfig):
             w = _rng(cfg.wseed, tag).standard_normal(shape, dtype=np.float32) * np.float32(0.02)
             out.append(f32_to_bf16_bits(w))
         return tuple(out)
+    if cfg.weight_format == "int4g32":
+        lo, hi, zlo, zhi = _i4_scale_range(cfg)
+        return tuple(i4_matrix(_rng(cfg.wseed, tag), r, c, lo, hi, zlo, zhi)
+                     for tag, r, c in ((_TAG_DENSE_G, I, H), (_TAG_DENSE_U, I, H), (_TAG_DENSE_D, H, I)))
     g = mx_matrix(_rng(cfg.wseed, _TAG_DENSE_G), I, H, cfg.e8m0_lo, cfg.e8m0_hi)
     u = mx_matrix(_rng(cfg.wseed, _TAG_DENSE_U), I, H, cfg.e8m0_lo, cfg.e8m0_hi)
     d = mx_matrix(_rng(cfg.wseed, _TAG_DENSE_D), H, I, cfg.e8m0_lo, cfg.e8m0_hi)

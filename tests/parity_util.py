@@ -28,7 +28,7 @@ def oracle_moe(cfg: wl.LayerConfig, x_bits: np.ndarray, logits: np.ndarray, toke
     xs, ls = x_bits[tokens], logits[tokens]
     ids, _ = oracle.route(ls, k)
     needed = sorted(set(ids.ravel().tolist()) | set(range(cfg.n_experts, cfg.n_groups)))
-    W = oracle.OracleWeights(cfg.hidden, cfg.inter, cfg.n_experts, cfg.n_shared)
+    W = oracle.OracleWeights(cfg.hidden, cfg.inter, cfg.n_experts, cfg.n_shared, cfg.weight_format)
     for e in needed:
         W.set_expert(e, *wl.expert_weights(cfg, e))
     out, ids, w = oracle.moe_layer(W, xs, ls, k, nthreads=NTHREADS)

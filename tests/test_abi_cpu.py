@@ -76,6 +76,13 @@ def test_host_side_argument_checks_without_gpu(built):
     # unknown format
     cfg = b.MoeConfig(hidden=64, inter=64, n_experts=2, n_shared=0, k_max=1, n_slices=0, fmt=7)
     assert L.moe_load_weights(ctypes.byref(cfg), fake, fake, None, ctypes.byref(h)) == b.MOE_EINVAL
+    # group-32 INT4: scales are FP16, so their pointer must be 2-byte aligned; zero points may be NULL
+    cfg = b.MoeConfig(hidden=64, inter=64, n_experts=2, n_shared=0, k_max=1, n_slices=0, fmt=b.MOE_W_INT4G32)
+    odd = (b.MoeMx * 2)(b.MoeMx(16, 16, None), b.MoeMx(16, 17, 16))
+    assert L.moe_load_weights(ctypes.byref(cfg), fake, odd, None, ctypes.byref(h)) == b.MOE_EINVAL
+    assert b"2-byte aligned" in L.moe_last_error()
+    assert L.moe_load_weights(ctypes.byref(cfg), nul, fake, None, ctypes.byref(h)) == b.MOE_EINVAL
+    assert b"NULL" in L.moe_last_error()
     # forward / dense forward / sync on a NULL handle
     assert L.moe_forward(None, None, None, 1, 1, None, 0, None, 0, None, None) == b.MOE_EINVAL
     assert L.moe_dense_sliced_forward(None, None, 1, None, 0, None, 0, None) == b.MOE_EINVAL
