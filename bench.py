@@ -40,6 +40,9 @@ METRIC = "MoE-layer tokens/s; decode weight-stream HBM GB/s; prefill tensor TFLO
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 512 << 20
 MX_BYTES_PER_WEIGHT = 17 / 32   # 4 bits of code + 8 bits of scale per 32 weights
+# stored bytes per weight of each format: group-32 INT4 carries a 16-bit scale
+# and an 8-bit zero point per 32 weights
+BYTES_PER_WEIGHT = {"mxfp4": MX_BYTES_PER_WEIGHT, "int4g32": 19 / 32, "bf16": 2.0}
 
 
 def workload(name: str) -> wl.LayerConfig:
@@ -53,7 +56,7 @@ def workload(name: str) -> wl.LayerConfig:
         return wl.sweep(T)
     if kind == "prefill":
         return wl.prefill(T)
-    if kind in ("dense_bf16", "dense_mxfp4"):
+    if kind in ("dense_bf16", "dense_mxfp4", "dense_int4g32"):
         return wl.dense(T, kind.split("_")[1])
     raise SystemExit(f"unknown workload {name}")
 
@@ -62,8 +65,9 @@ def describe(cfg: wl.LayerConfig) -> str:
     if cfg.dense:
         return (f"{cfg.name}: dense SwiGLU FFN T={cfg.T}, H={cfg.hidden}, I={cfg.inter} as {cfg.n_slices} "
                 f"all-active slices of {cfg.inter // cfg.n_slices}, {cfg.weight_format.upper()} weights")
+    fmt = {"mxfp4": "MXFP4", "int4g32": "group-32 INT4", "bf16": "BF16"}[cfg.weight_format]
     return (f"{cfg.name}: MoE layer T={cfg.T}, H={cfg.hidden}, I={cfg.inter}, E={cfg.n_experts} routed + "
-            f"{cfg.n_shared} shared MXFP4 experts, top-{cfg.k}, logits {cfg.logits}")
+            f"{cfg.n_shared} shared {fmt} experts, top-{cfg.k}, logits {cfg.logits}")
 
 
 def read_peaks():
@@ -82,18 +86,18 @@ def work_model(cfg: wl.LayerConfig, groups_active: int):
 
     groups_active: expert groups with at least one token (routed experts hit by
     the batch, plus shared experts / dense slices).  Weight bytes are counted
-    once per active group in their stored format (MXFP4: 17/32 byte per weight);
+    once per active group in their stored format (MXFP4: 17/32 byte per weight,
+    group-32 INT4 with zero points: 19/32);
     flops are 2 per multiply-add over every (position, weight) pair.
     """
     H, T = cfg.hidden, cfg.T
     if cfg.dense:
         I = cfg.inter // cfg.n_slices
         P = T * cfg.n_slices
-        wb = 2.0 if cfg.weight_format == "bf16" else MX_BYTES_PER_WEIGHT
     else:
         I = cfg.inter
         P = T * cfg.k + T * cfg.n_shared
-        wb = MX_BYTES_PER_WEIGHT
+    wb = BYTES_PER_WEIGHT[cfg.weight_format]
     gu_w = groups_active * 2 * I * H * wb
     dn_w = groups_active * H * I * wb
     gate_up = {"bytes": gu_w + T * H * 2 + P * I * 4, "flops": 2.0 * P * 2 * I * H,
@@ -347,14 +351,15 @@ def run_ours(args, cfg, rank, world):
     launches_per_step = 1 if streaming else (5 if cfg.dense else 7)
     # operand type of the GEMMs: the streaming layer decodes MXFP4 to FP16
     # (FP32 accumulate); the tcgen05 path and BF16 weights run in BF16
-    dtype = "f16" if streaming and cfg.weight_format == "mxfp4" else "bf16"
+    dtype = "f16" if streaming and cfg.weight_format in ("mxfp4", "int4g32") else "bf16"
     weight_bytes = gate_up["weight_bytes"] + down["weight_bytes"]
     value = job_tokens_per_s(world, cfg.T, ms)
     res = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": dtype, "data": "synthetic (seeded; random MXFP4 codes and E8M0 scales)",
-        "config": {"workload": describe(cfg), "T": cfg.T, "hidden": cfg.hidden, "inter": cfg.inter,
+        "config": {"workload": describe(cfg), "weights": cfg.weight_format, "T": cfg.T, "hidden": cfg.hidden,
+                   "inter": cfg.inter,
                    "experts": cfg.n_experts, "shared": cfg.n_shared, "top_k": cfg.k,
                    "active_groups": groups, "tokens_per_routed_expert": tokens_per_expert,
                    "l2": "flushed between steps (512 MB write outside the timed events)",
@@ -404,7 +409,7 @@ def oracle_sample(cfg: wl.LayerConfig, budget_s: float, max_tokens: int = None):
         else:
             ids, _ = oracle.route(lg[sample], cfg.k)
             needed = sorted(set(ids.ravel().tolist()) | set(range(cfg.n_experts, cfg.n_groups)))
-            W = oracle.OracleWeights(cfg.hidden, cfg.inter, cfg.n_experts, cfg.n_shared)
+            W = oracle.OracleWeights(cfg.hidden, cfg.inter, cfg.n_experts, cfg.n_shared, cfg.weight_format)
             for e in needed:
                 W.set_expert(e, *wl.expert_weights(cfg, e))
             t0 = time.perf_counter()  # weight generation is input synthesis, not oracle work
@@ -459,13 +464,17 @@ def main():
     ap.add_argument("--workload", default="decode_T1")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--weights", default="mxfp4", choices=["mxfp4", "int4g32"],
+                    help="weight format of a routed workload (group-32 INT4 runs the single-kernel sizes)")
     ap.add_argument("--experts", type=int, default=0,
                     help="profiling aid: routed experts of a smaller layer with the same shapes per expert")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     cfg = workload(args.workload)
+    import dataclasses
+    if args.weights != "mxfp4" and not cfg.dense:
+        cfg = dataclasses.replace(cfg, name=f"{cfg.name}_{args.weights}", weight_format=args.weights)
     if args.experts:
-        import dataclasses
         cfg = dataclasses.replace(cfg, name=f"{cfg.name}_E{args.experts}", n_experts=args.experts)
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))

@@ -72,8 +72,11 @@ __host__ __device__ constexpr int ls_smem_limit(int ctas) { return ctas == 1 ? 2
 __host__ __device__ constexpr int ls_stage_target(int ctas) { return ctas == 1 ? 52224 : 26624; }
 constexpr int LS_R_MAX = 16;
 // stage target of the kernel for batches of at most two tokens (NT = 0): its
-// stages reserve two token rows, which leaves room for one more ring slot
+// stages reserve two token rows, which leaves room for one more ring slot.
+// Group-32 INT4 chunks are larger (9,728 B against 8,704); its target still
+// takes four of them per gate|up stage.
 constexpr int LS_TINY_TARGET = 40960;
+constexpr int LS_TINY_TARGET_I4 = 41088;
 constexpr int LS_HS_ROW = 16;  // ints of h block scales kept per token row and stage
 
 // ------------------------------------------------------------------ stage geometry
@@ -114,7 +117,8 @@ struct LsCfg {
     static constexpr int ROWS = 8 * NTK;          // token rows of the largest item
     static constexpr int CTAS = ls_ctas_per_sm(NT);
     static constexpr int SMEM_LIMIT = ls_smem_limit(CTAS);
-    static constexpr int TARGET = NT == 0 ? LS_TINY_TARGET : ls_stage_target(CTAS);
+    static constexpr int TARGET = NT == 0 ? (WFMT == FMT_INT4 ? LS_TINY_TARGET_I4 : LS_TINY_TARGET)
+                                          : ls_stage_target(CTAS);
     __host__ __device__ static constexpr int res_rows(int nti) { return NT == 0 ? 2 : 8 * nti; }
     __host__ __device__ static constexpr int hsb_dn(int nti) { return F16 ? res_rows(nti) * LS_HS_ROW * 4 : 0; }
     __host__ __device__ static constexpr int ch_gu(int nti)

@@ -28,6 +28,18 @@ def test_algorithmic_bytes_of_decode():
     assert layer["flops"] == 2 * 9 * 3 * 2048 * 7168
 
 
+def test_algorithmic_bytes_of_int4_decode():
+    # group-32 INT4 with FP16 scales and zero points costs 19/32 byte per weight:
+    # an expert is 3 * 8,716,288 = 26,148,864 bytes
+    import dataclasses
+    cfg = dataclasses.replace(bench.workload("decode_T1"), weight_format="int4g32")
+    gu, dn, layer = bench.work_model(cfg, 9)
+    assert gu["per_unit"] + dn["per_unit"] == 26_148_864
+    assert layer["weight_bytes"] == 9 * 26_148_864
+    dense = bench.work_model(bench.workload("dense_int4g32_T1"), 9)[2]
+    assert dense["weight_bytes"] == 3 * 7168 * 18432 * 19 / 32
+
+
 def test_job_throughput_is_weak_scaling():
     assert bench.job_tokens_per_s(1, 1, 0.1) == pytest.approx(10_000.0)
     assert bench.job_tokens_per_s(4, 8, 2.0) == pytest.approx(16_000.0)
