@@ -28,6 +28,8 @@
  *     FP32; h is kept between the two projections as a hi + lo pair, about
  *     16 significant bits or more: BF16 pairs on the tensor-core path, FP16
  *     pairs with a power-of-two scale per 64 features on the decode path.
+ *     Weights may also be BF16, or group-32 INT4 with an FP16 scale and a zero
+ *     point per 32 values (the format of "Cascadia" §3.1; MoeWeightFormat).
  *  4. Combine.  out_t = sum_{j<k} w_tj y_{e_tj}(x_t) + sum_shared y_s(x_t) in
  *     FP32 ("Cascadia" §3.3, Eq. 1), written to (or, with accumulate, added
  *     to) the caller's FP32 buffer.
@@ -46,7 +48,8 @@
  *  - pack4 (MXFP4 codes): byte j of a row holds element 2j in its low nibble
  *    and element 2j+1 in its high nibble.  Code bit 3 is the sign; bits 0..2
  *    index the magnitude list above in the printed order.
- *  - scales: one E8M0 byte per 32 consecutive elements of a row.
+ *  - scales: one E8M0 byte per 32 consecutive elements of a row (INT4: one
+ *    FP16 bit pattern, and one zero-point byte, per 32 elements).
  *  - BF16 tensors are 16-bit BF16 bit patterns.
  *
  * Conventions:

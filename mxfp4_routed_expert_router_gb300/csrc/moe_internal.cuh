@@ -131,7 +131,7 @@ struct Plan {
     uint16_t *x_perm;         // [T*k][H] rows of x gathered in routed position order (BF16, or FP16 for
                               // the FP16 streaming path)
     uint16_t *x16;            // [T][H] token rows of the streaming path in x16 K order: FP16
-                              // x_t * 2^-xs[t] for MXFP4 weights, BF16 x_t for BF16 weights
+                              // x_t * 2^-xs[t] for MXFP4 and INT4 weights, BF16 x_t for BF16 weights
     int *xs;                  // [T] per-token power-of-two scale exponent of x16
     uint16_t *h;              // [2][P][I] h = hi plane + lo plane: BF16 (lo = bf16(h - hi)); on the FP16
                               // streaming path FP16 (h * 2^-hs = hi + lo); x16 K order on the streaming path
