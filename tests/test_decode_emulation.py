@@ -1,4 +1,5 @@
-"""CPU emulation of the GPU's in-register MXFP4 -> BF16 decode.
+"""CPU emulation of the GPU's in-register MXFP4 -> BF16 decode, and of the
+single kernel's group-32 INT4 -> FP16 decode.
 
 The CUDA kernels decode repacked 32-bit words with byte permutes (PRMT) and a
 BF16 multiply (mx_decode.cuh).  This test emulates those exact bit operations
@@ -156,3 +157,46 @@ def test_fragment_word_maps_to_mma_a_registers():
             lo, hi = bf16_bits_value(reg), bf16_bits_value(reg >> 16)
             assert lo == expect(int(tile[row, col]), e, tab)
             assert hi == expect(int(tile[row, col + 1]), e, tab)
+
+
+# ------------------------------------------------------------------ group-32 INT4 (single kernel)
+# The FRAG_F16 INT4 word holds the A fragment's element pair p in nibbles p
+# (first element) and p + 4 (second); the kernel turns a pair into FP16 q - z
+# with a shift, a mask, an OR with 0x6400 (FP16 1024) in both halves and one
+# FP16x2 subtraction of 1024 + z.  Emulated here with numpy's float16, which
+# rounds like the hardware's round-to-nearest subtraction.
+
+def i4_repack_word(first, second):
+    w = 0
+    for p in range(4):
+        w |= first[p] << (4 * p) | second[p] << (4 * p + 16)
+    return w
+
+
+def decode_i4_pair(w, p, z):
+    v = ((w >> (4 * p)) & 0x000F000F) | 0x64006400
+    halves = np.array([v & 0xFFFF, v >> 16], np.uint16).view(np.float16)
+    m = np.array([0x6400 + z, 0x6400 + z], np.uint16).view(np.float16)
+    return (halves - m).astype(np.float64)
+
+
+def test_i4_pair_decode_is_exact_for_every_code_and_zero_point():
+    for z in range(16):
+        for q0 in range(16):
+            for q1 in range(16):
+                w = i4_repack_word([q0, 0, 0, 0], [q1, 0, 0, 0])
+                got = decode_i4_pair(w, 0, z)
+                assert got[0] == q0 - z and got[1] == q1 - z, (q0, q1, z)
+
+
+def test_i4_fragment_word_maps_pairs_to_registers():
+    rng = np.random.default_rng(3)
+    for _ in range(200):
+        first = rng.integers(0, 16, 4).tolist()
+        second = rng.integers(0, 16, 4).tolist()
+        za, zb = int(rng.integers(0, 16)), int(rng.integers(0, 16))
+        w = i4_repack_word(first, second)
+        for p in range(4):
+            z = zb if p & 1 else za       # pairs 1 and 3 belong to row g + 8
+            got = decode_i4_pair(w, p, z)
+            assert got[0] == first[p] - z and got[1] == second[p] - z
