@@ -40,6 +40,22 @@ def test_algorithmic_bytes_of_int4_decode():
     assert dense["weight_bytes"] == 3 * 7168 * 18432 * 19 / 32
 
 
+def test_roofline_bound_and_fractions():
+    peaks = {"hbm_gbs": 6714.6, "bf16_tflops": 1937.1, "bf16_tflops_sustained": 1741.4}
+    _, _, layer = bench.work_model(bench.workload("decode_T1"), 9)
+    r = bench.roofline_entry(layer, 0.0705, peaks, "measured")
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert r["achieved"] == pytest.approx(layer["bytes"] / 70.5e-6 / 1e9)
+    assert r["frac"] == pytest.approx(r["achieved"] / 6714.6)
+    assert r["frac_nominal"] == pytest.approx(r["achieved"] / 7900.0)
+    # prefill gate|up: 73,728 token positions over 257 groups is a dense contraction
+    gu, _, _ = bench.work_model(bench.workload("prefill_T8192"), 257)
+    r = bench.roofline_entry(gu, 5.5, peaks, "measured")
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert r["frac"] == pytest.approx(gu["flops"] / 5.5e-3 / 1e12 / 1937.1)
+    assert r["frac_nominal"] == pytest.approx(gu["flops"] / 5.5e-3 / 1e12 / 2250.0)
+
+
 def test_job_throughput_is_weak_scaling():
     assert bench.job_tokens_per_s(1, 1, 0.1) == pytest.approx(10_000.0)
     assert bench.job_tokens_per_s(4, 8, 2.0) == pytest.approx(16_000.0)
