@@ -683,3 +683,34 @@ def test_i4_dense_slices_equal_unsliced_and_textbook():
     scale = np.sqrt(np.mean(want ** 2))
     assert np.max(np.abs(full - want)) / scale <= 1e-12
     assert np.max(np.abs(full - sliced)) / scale <= 1e-12
+
+
+def onehot_i4(rows, cols, positions, q, scale, z):
+    """INT4 matrix with one nonzero weight per row (code q at positions[r], code z
+    elsewhere, so that every other weight is 0), FP16 scale `scale`, zero point z."""
+    codes = np.full((rows, cols), z, np.uint8)
+    for r, c in enumerate(positions):
+        codes[r, c] = q
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    sbits = np.float16(scale).view(np.uint16)
+    return packed, np.full((rows, cols // 32), sbits, np.uint16), np.full((rows, cols // 32), z, np.uint8)
+
+
+def test_i4_onehot_expert_closed_form():
+    # non-power-of-two FP16 scales: the weights are exactly (q - z) * float(fp16(scale))
+    H, I = 64, 32
+    rng = np.random.default_rng(26)
+    a, b, dn = rng.integers(0, H, I), rng.integers(0, H, I), rng.integers(0, I, H)
+    sg, su, sd = (float(np.float16(v)) for v in (0.3, -1.7, 0.0123))
+    gc, gs, gz = onehot_i4(I, H, a, 11, 0.3, 9)     # gate row n = 2 * sg * e_{a_n}
+    uc, us, uz = onehot_i4(I, H, b, 0, -1.7, 5)     # up row n = -5 * su * e_{b_n}
+    dc, ds, dz = onehot_i4(H, I, dn, 15, 0.0123, 2)  # down row m = 13 * sd * e_{dn_m}
+    W = oracle.OracleWeights(H, I, 1, 0, "int4g32")
+    W.set_expert(0, np.concatenate([gc, uc]), np.concatenate([gs, us]), dc, ds, np.concatenate([gz, uz]), dz)
+    x = wl.f32_to_bf16_bits(rng.standard_normal((3, H)).astype(np.float32))
+    xf = wl.bf16_bits_to_f32(x).astype(np.float64)
+    out, ids, w = oracle.moe_layer(W, x, np.zeros((3, 1), np.float32), 1)
+    for t in range(3):
+        h = [silu(2 * sg * xf[t, a[n]]) * (-5 * su) * xf[t, b[n]] for n in range(I)]
+        want = [13 * sd * h[dn[m]] for m in range(H)]
+        np.testing.assert_allclose(out[t], want, rtol=1e-14, atol=0)
