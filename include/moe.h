@@ -146,8 +146,9 @@ typedef struct {
  * The library repacks into its own buffers (a copy, never a view of the
  * caller's memory, per the same section's note on narrow() views).  The call
  * is synchronous: it waits for `cuda_stream` before returning.
- * Errors: MOE_EINVAL (NULL pointers, bad counts), MOE_EDIMS, MOE_ESCALE,
- * MOE_ENOMEM, MOE_ECUDA.  *out is set only on MOE_OK. */
+ * Errors: MOE_EINVAL (NULL pointers, bad counts, INT4 scales not 2-byte
+ * aligned), MOE_EDIMS, MOE_ESCALE, MOE_ENOMEM, MOE_ECUDA.  *out is set only
+ * on MOE_OK. */
 MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const MoeMx *down, void *cuda_stream,
                            MoeHandle **out);
 
@@ -178,7 +179,8 @@ typedef struct {
  *  routing       NULL or device pointers that receive the routing
  * T == 0 enqueues nothing and returns MOE_OK.
  * Errors: MOE_EINVAL (NULL/misaligned pointers, T < 0, k outside
- * [1, k_max], a dense handle), MOE_EWORKSPACE, MOE_EDEVICE, MOE_ECUDA. */
+ * [1, k_max], a dense handle, an INT4 batch outside the single-kernel range),
+ * MOE_EWORKSPACE, MOE_EDEVICE, MOE_ECUDA. */
 MoeStatus moe_forward(MoeHandle *h, const void *x_bf16, const float *router_logits, int T, int k, float *out_fp32,
                       int accumulate, void *workspace, size_t ws_bytes, const MoeRoutingOut *routing,
                       void *cuda_stream);
@@ -197,7 +199,8 @@ MoeStatus moe_forward(MoeHandle *h, const void *x_bf16, const float *router_logi
  * runs that slot as expert 0 with weight 0 so that every access stays in
  * bounds, and moe_sync_status() then reports MOE_EDEVICE.
  * Errors: MOE_EINVAL (NULL/misaligned pointers, T < 0, k outside [1, k_max],
- * a dense handle), MOE_EWORKSPACE, MOE_EDEVICE, MOE_ECUDA. */
+ * a dense handle, an INT4 batch outside the single-kernel range),
+ * MOE_EWORKSPACE, MOE_EDEVICE, MOE_ECUDA. */
 MoeStatus moe_forward_routed(MoeHandle *h, const void *x_bf16, const int32_t *topk_ids, const float *topk_w, int T,
                              int k, float *out_fp32, int accumulate, void *workspace, size_t ws_bytes,
                              const MoeRoutingOut *routing, void *cuda_stream);
@@ -269,8 +272,8 @@ void moe_graph_free(MoeGraph *graph);
 /* The dense FFN of a dense handle on T tokens, as the sum of its all-active
  * slices ("Cascadia" §3.4, Eq. 2).  Arguments as for moe_forward; the
  * workspace size is moe_workspace_bytes(h, T, 0).
- * Errors: MOE_EINVAL (also for a routed handle), MOE_EWORKSPACE, MOE_EDEVICE,
- * MOE_ECUDA. */
+ * Errors: MOE_EINVAL (also for a routed handle, and for more than 64 tokens
+ * with INT4 weights), MOE_EWORKSPACE, MOE_EDEVICE, MOE_ECUDA. */
 MoeStatus moe_dense_sliced_forward(MoeHandle *h, const void *x_bf16, int T, float *out_fp32, int accumulate,
                                    void *workspace, size_t ws_bytes, void *cuda_stream);
 
