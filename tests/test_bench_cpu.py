@@ -112,6 +112,14 @@ def test_reference_arm_prints_one_contract_line():
     assert d["config"]["workload"].startswith("tiny")
 
 
+def test_reference_arm_with_int4_weights():
+    r = _bench(["--impl", "reference", "--workload", "tiny", "--weights", "int4g32", "--steps", "1", "--warmup", "3"])
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    assert d["impl"] == "reference" and d["value"] > 0
+    assert d["config"]["workload"].startswith("tiny_int4g32") and "group-32 INT4" in d["config"]["workload"]
+
+
 def test_reference_arm_is_silent_on_other_ranks():
     r = _bench(["--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "3"],
                {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
