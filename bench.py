@@ -222,77 +222,172 @@ def job_tokens_per_s(world: int, tokens_per_rank: int, ms: float) -> float:
 
 # ------------------------------------------------------------------ our arm
 
+# Workloads measured beside the headline one, on the same loaded layer (the
+# decode, sweep and prefill workloads share their expert weights): the metric
+# also asks for the sweep's weight-stream GB/s and prefill's tensor TFLOP/s.
+EXTRA_WORKLOADS = ("sweep_T15", "sweep_T88", "sweep_T176", "prefill_T8192")
+
+
+def same_layer(a: wl.LayerConfig, b: wl.LayerConfig) -> bool:
+    keys = ("hidden", "inter", "n_experts", "n_shared", "k", "wseed", "e8m0_lo", "e8m0_hi", "dense", "n_slices",
+            "weight_format")
+    return all(getattr(a, k) == getattr(b, k) for k in keys)
+
+
+def dominant_kernel(cfg, stage_ms, groups):
+    """The dominant kernel of a workload and its roofline inputs: the
+    single-kernel layer when the batch ran through it (profile stage 5), else
+    the longer of the two GEMM stages."""
+    gate_up, down, layer_w = work_model(cfg, groups)
+    if stage_ms.get("layer", 0.0) > stage_ms["gate_up"] + stage_ms["down"]:
+        return "layer", layer_w
+    name = "gate_up" if stage_ms["gate_up"] >= stage_ms["down"] else "down"
+    return name, gate_up if name == "gate_up" else down
+
+
+class Workload:
+    """Device-resident inputs of one workload on a loaded layer, and its timed steps."""
+
+    def __init__(self, L, cfg, dev):
+        import torch
+
+        from mxfp4_routed_expert_router_gb300 import binding as B
+        from mxfp4_routed_expert_router_gb300.layer import bf16_tensor
+
+        self.L, self.cfg, self.dev, self.B = L, cfg, dev, B
+        self.x_bits = wl.tokens(cfg)
+        self.x = bf16_tensor(self.x_bits, str(dev))
+        self.logits_np = None if cfg.dense else wl.router_logits(cfg)
+        self.logits = None if cfg.dense else torch.from_numpy(self.logits_np).to(dev)
+        self.out = torch.empty((cfg.T, cfg.hidden), dtype=torch.float32, device=dev)
+
+    def step(self, routing=None):
+        self.L.forward(self.x, self.logits, self.cfg.k, out=self.out, routing=routing)
+
+    def active_groups(self):
+        """Distinct active expert groups of this batch (the unit of the weight stream)."""
+        import torch
+        cfg = self.cfg
+        if cfg.dense:
+            return cfg.n_slices
+        ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=self.dev)
+        self.step(self.B.routing_out(topk_ids=ids))
+        self.L.sync()
+        return int(torch.unique(ids).numel()) + cfg.n_shared
+
+    def timed(self, steps, warmup, flush, stream, dist=None):
+        """Mean device ms per step over `steps` steps (CUDA events on the launching
+        stream, L2 flushed before each step outside the events) and the SM clocks
+        sampled meanwhile."""
+        import torch
+        for _ in range(warmup):
+            self.step()
+        self.L.sync()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize(self.dev)
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        with ClockSampler(self.dev.index) as clk:
+            for i in range(steps):
+                flush.zero_()
+                starts[i].record(stream)
+                self.step()
+                ends[i].record(stream)
+            torch.cuda.synchronize(self.dev)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize(self.dev)
+        times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        ms = sum(times) / len(times)
+        if dist:
+            ms = max_over_ranks(ms, dist, self.dev)
+        self.L.sync()
+        return ms, clk.summary()
+
+    def stages(self, n, flush):
+        """Per-stage device time from the library's own events on the same stream,
+        in separate (untimed) steps so that the events do not perturb the timed ones."""
+        B = self.B
+        B.moe_profile_enable(self.L.handle, True)
+        st = []
+        for _ in range(n):
+            flush.zero_()
+            self.step()
+            st.append(B.moe_profile_read(self.L.handle))
+        B.moe_profile_enable(self.L.handle, False)
+        self.L.sync()
+        return {k: sum(s[k] for s in st) / len(st) for k in st[0]}
+
+
+def summarize_extra(cfg, ms, clocks, stage_ms, groups, peaks, peak_src):
+    """Per-workload numbers of a workload measured beside the headline one."""
+    gate_up, down, layer_w = work_model(cfg, groups)
+    weight_bytes = gate_up["weight_bytes"] + down["weight_bytes"]
+    flops = gate_up["flops"] + down["flops"]
+    dom_name, dom = dominant_kernel(cfg, stage_ms, groups)
+    r = {"workload": describe(cfg), "T": cfg.T, "ms_per_step": ms, "tokens_per_s": cfg.T / (ms * 1e-3),
+         "active_groups": groups, "weight_GBps": weight_bytes / (ms * 1e-3) / 1e9,
+         "layer_TFLOPs": flops / (ms * 1e-3) / 1e12, "clocks": clocks,
+         "stages_ms": {"layer": stage_ms["layer"]} if dom_name == "layer" else stage_ms}
+    roof = roofline_entry(dom, stage_ms[dom_name], peaks, peak_src)
+    roof["kernel"] = "single-kernel MoE layer" if dom_name == "layer" else f"{dom_name} GEMM"
+    roof["kernel_ms"] = stage_ms[dom_name]
+    r["roofline"] = roof
+    if dom_name == "layer":
+        # HBM-bound: the weight stream over the step, as a fraction of the copy peak
+        r["weight_stream_frac"] = r["weight_GBps"] / peaks["hbm_gbs"]
+    else:
+        # tensor-bound: each GEMM, and the whole step, against the bf16 tensor peak
+        tp = peaks["bf16_tflops"]
+        r["gate_up"] = {"ms": stage_ms["gate_up"], "TFLOPs": gate_up["flops"] / (stage_ms["gate_up"] * 1e-3) / 1e12}
+        r["down"] = {"ms": stage_ms["down"], "TFLOPs": down["flops"] / (stage_ms["down"] * 1e-3) / 1e12}
+        for kk in ("gate_up", "down"):
+            r[kk]["tensor_frac"] = r[kk]["TFLOPs"] / tp
+        r["layer_tensor_frac"] = r["layer_TFLOPs"] / tp
+    r["peak_source"] = f"copy bandwidth / bf16 burst, of {peak_src}"
+    return r
+
+
+def bench_config(cfg: wl.LayerConfig, groups: int, world: int) -> dict:
+    """The `config` object of the JSON line (the same for both arms)."""
+    tokens_per_expert = (cfg.T * cfg.k) / max(1, groups - cfg.n_shared) if not cfg.dense else cfg.T
+    return {"workload": describe(cfg), "weights": cfg.weight_format, "T": cfg.T, "hidden": cfg.hidden,
+            "inter": cfg.inter, "experts": cfg.n_experts, "shared": cfg.n_shared, "top_k": cfg.k,
+            "active_groups": groups, "tokens_per_routed_expert": tokens_per_expert,
+            "l2": "flushed between steps (512 MB write outside the timed events)",
+            "parallelism": f"replicas x{world}"}
+
+
 def run_ours(args, cfg, rank, world):
     import torch
 
     from mxfp4_routed_expert_router_gb300 import binding as B
-    from mxfp4_routed_expert_router_gb300.layer import MoeLayer, bf16_tensor
+    from mxfp4_routed_expert_router_gb300.layer import MoeLayer
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     L = MoeLayer(cfg, device=str(dev))
-    x_bits = wl.tokens(cfg)
-    x = bf16_tensor(x_bits, str(dev))
-    logits = None if cfg.dense else torch.from_numpy(wl.router_logits(cfg)).to(dev)
-    out = torch.empty((cfg.T, cfg.hidden), dtype=torch.float32, device=dev)
+    W = Workload(L, cfg, dev)
+    x, logits, out, x_bits = W.x, W.logits, W.out, W.x_bits
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    ids = None
-    if not cfg.dense:
-        ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
-
-    def step(routing=None):
-        L.forward(x, logits, cfg.k, out=out, routing=routing)
 
     for _ in range(args.warmup):
-        step()
+        W.step()
     L.sync()
-    # distinct active expert groups of this batch (the unit of the weight stream)
-    if cfg.dense:
-        groups = cfg.n_slices
-    else:
-        step(B.routing_out(topk_ids=ids))
-        L.sync()
-        groups = int(torch.unique(ids).numel()) + cfg.n_shared
+    groups = W.active_groups()
 
     dist = None
     if world > 1:
         import torch.distributed as dist
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    with ClockSampler(dev.index) as clk:
-        for i in range(args.steps):
-            flush.zero_()
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
-        torch.cuda.synchronize(dev)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms = sum(times) / len(times)
-    if dist:
-        ms = max_over_ranks(ms, dist, dev)
-
-    # per-stage device time, from the library's own events on the same stream,
-    # in separate (untimed) steps so that the events do not perturb the above
-    B.moe_profile_enable(L.handle, True)
-    stages = []
-    for i in range(max(3, min(args.steps, 10))):
-        flush.zero_()
-        step()
-        stages.append(B.moe_profile_read(L.handle))
-    B.moe_profile_enable(L.handle, False)
-    L.sync()
-    stage_ms = {k: sum(s[k] for s in stages) / len(stages) for k in stages[0]}
+    ms, clocks = W.timed(args.steps, 0, flush, stream, dist)
+    stage_ms = W.stages(max(3, min(args.steps, 10)), flush)
 
     # end to end through the public API with host buffers: pinned x/logits in,
     # out back to pinned host memory, copies inside the timed region
     hx = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
-    hl = None if cfg.dense else torch.from_numpy(wl.router_logits(cfg)).pin_memory()
+    hl = None if cfg.dense else torch.from_numpy(W.logits_np).pin_memory()
     hout = torch.empty((cfg.T, cfg.hidden), dtype=torch.float32).pin_memory()
     e2e_times = []
     for i in range(max(3, min(args.steps, 20))):
@@ -334,20 +429,11 @@ def run_ours(args, cfg, rank, world):
 
     gate_up, down, layer_w = work_model(cfg, groups)
     peaks, peak_src = read_peaks()
-    # the dominant kernel of this workload: the single-kernel layer when the
-    # batch ran through it, else the longer GEMM stage
-    # (the stages a call does not run read as the few microseconds between two
-    # back-to-back events)
-    if stage_ms.get("layer", 0.0) > stage_ms["gate_up"] + stage_ms["down"]:
-        dom_name, dom = "layer", layer_w
-    else:
-        dom_name = "gate_up" if stage_ms["gate_up"] >= stage_ms["down"] else "down"
-        dom = gate_up if dom_name == "gate_up" else down
+    dom_name, dom = dominant_kernel(cfg, stage_ms, groups)
     dom_ms = stage_ms[dom_name]
     if dom_name == "layer":
         # the single kernel runs every stage; the other marks are empty
         stage_ms = {"layer": stage_ms["layer"]}
-    tokens_per_expert = (cfg.T * cfg.k) / max(1, groups - cfg.n_shared) if not cfg.dense else cfg.T
     roof = roofline_entry(dom, dom_ms, peaks, peak_src)
     roof["kernel"] = "single-kernel MoE layer" if dom_name == "layer" else f"{dom_name} GEMM"
     roof["traffic"] = ncu_traffic(f"{dom_name}:{cfg.name}")
@@ -368,12 +454,7 @@ def run_ours(args, cfg, rank, world):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": dtype, "data": "synthetic (seeded; random MXFP4 codes and E8M0 scales)",
-        "config": {"workload": describe(cfg), "weights": cfg.weight_format, "T": cfg.T, "hidden": cfg.hidden,
-                   "inter": cfg.inter,
-                   "experts": cfg.n_experts, "shared": cfg.n_shared, "top_k": cfg.k,
-                   "active_groups": groups, "tokens_per_routed_expert": tokens_per_expert,
-                   "l2": "flushed between steps (512 MB write outside the timed events)",
-                   "parallelism": f"replicas x{world}"},
+        "config": bench_config(cfg, groups, world),
         "weight_stream_GBps": weight_bytes / (ms * 1e-3) / 1e9,
         "layer_TFLOPs": (gate_up["flops"] + down["flops"]) / (ms * 1e-3) / 1e12,
         "stages_ms": stage_ms,
@@ -383,8 +464,32 @@ def run_ours(args, cfg, rank, world):
         "graph": {"value": world * cfg.T / (graph_ms * 1e-3), "unit": "tokens/s", "ms_per_step": graph_ms,
                   "note": "the same call replayed from a CUDA graph (moe_graph_create / moe_graph_launch)"},
         "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk.summary(),
+        "clocks": clocks,
     }
+    del W
+
+    # the other workloads of the metric on the same layer, each with its own
+    # timed steps, L2 flush, stage events and clock record
+    extras = {}
+    names = [] if args.extra == "none" else [n for n in args.extra.split(",") if n]
+    for name in names:
+        ecfg = workload(name)
+        if ecfg.name == cfg.name or not same_layer(ecfg, cfg):
+            continue
+        EW = Workload(L, ecfg, dev)
+        EW.step()
+        egroups = EW.active_groups()
+        esteps = max(3, min(args.steps, 10))
+        ems, eclk = EW.timed(esteps, args.warmup, flush, stream, dist)
+        est = EW.stages(3, flush)
+        e_ent = summarize_extra(ecfg, ems, eclk, est, egroups, peaks, peak_src)
+        e_ent["tokens_per_s"] = job_tokens_per_s(world, ecfg.T, ems)
+        e_ent["steps"] = esteps
+        e_ent["gpu_launches"] = esteps * (1 if e_ent["roofline"]["kernel"] == "single-kernel MoE layer" else 7)
+        extras[name] = e_ent
+        del EW
+    if extras:
+        res["workloads"] = extras
     L.free()
     return res
 
@@ -394,15 +499,22 @@ def run_ours(args, cfg, rank, world):
 _DENSE_CACHE = {}
 
 
-def oracle_sample(cfg: wl.LayerConfig, budget_s: float, max_tokens: int = None):
+def oracle_sample(cfg: wl.LayerConfig, budget_s: float, max_tokens: int = None, cores=None):
     """Time the CPU oracle, as it stands, on a bounded token sample of the workload.
 
-    Returns (tokens processed, seconds, threads used, description)."""
+    cores: the host CPUs the oracle may run on (its threads inherit the calling
+    thread's affinity; default: every CPU this process may use); it is given
+    one thread per core.  Returns (tokens processed, seconds, threads used,
+    description).  The oracle runs the (token, expert) jobs of one expert in
+    parallel, one expert after another, so the threads it actually uses are
+    bounded by the largest number of jobs of one expert in the sample."""
     import oracle
 
     oracle.build()
     x_bits = wl.tokens(cfg)
-    nthreads = os.cpu_count() or 1
+    all_cores = sorted(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else None
+    cores = sorted(cores) if cores is not None else all_cores
+    nthreads = len(cores) if cores else (os.cpu_count() or 1)
     sample = wl.sample_tokens(cfg.T, max_tokens or cfg.T)
     done, secs, rounds = 0, 0.0, 0
     if cfg.dense:
@@ -412,26 +524,53 @@ def oracle_sample(cfg: wl.LayerConfig, budget_s: float, max_tokens: int = None):
         weights = _DENSE_CACHE[cfg.name]
     else:
         lg = wl.router_logits(cfg)
-    while secs < budget_s or rounds == 0:
-        t0 = time.perf_counter()
-        if cfg.dense:
-            oracle.dense_ffn(weights, x_bits[sample], cfg.n_slices, cfg.weight_format)
-        else:
-            ids, _ = oracle.route(lg[sample], cfg.k)
-            needed = sorted(set(ids.ravel().tolist()) | set(range(cfg.n_experts, cfg.n_groups)))
-            W = oracle.OracleWeights(cfg.hidden, cfg.inter, cfg.n_experts, cfg.n_shared, cfg.weight_format)
-            for e in needed:
-                W.set_expert(e, *wl.expert_weights(cfg, e))
-            t0 = time.perf_counter()  # weight generation is input synthesis, not oracle work
-            oracle.moe_layer(W, x_bits[sample], lg[sample], cfg.k, nthreads=nthreads)
-        secs += time.perf_counter() - t0
-        done += len(sample)
-        rounds += 1
-    used = 1 if cfg.dense else min(nthreads, len(sample) * (cfg.k + cfg.n_shared))
+    if cores and all_cores and cores != all_cores:
+        os.sched_setaffinity(0, cores)
+    try:
+        while secs < budget_s or rounds == 0:
+            t0 = time.perf_counter()
+            if cfg.dense:
+                oracle.dense_ffn(weights, x_bits[sample], cfg.n_slices, cfg.weight_format)
+            else:
+                ids, _ = oracle.route(lg[sample], cfg.k)
+                needed = sorted(set(ids.ravel().tolist()) | set(range(cfg.n_experts, cfg.n_groups)))
+                W = oracle.OracleWeights(cfg.hidden, cfg.inter, cfg.n_experts, cfg.n_shared, cfg.weight_format)
+                for e in needed:
+                    W.set_expert(e, *wl.expert_weights(cfg, e))
+                t0 = time.perf_counter()  # weight generation is input synthesis, not oracle work
+                oracle.moe_layer(W, x_bits[sample], lg[sample], cfg.k, nthreads=nthreads)
+            secs += time.perf_counter() - t0
+            done += len(sample)
+            rounds += 1
+    finally:
+        if cores and all_cores and cores != all_cores:
+            os.sched_setaffinity(0, all_cores)
+    if cfg.dense:
+        used = 1
+    else:
+        ids, _ = oracle.route(lg[sample], cfg.k)
+        jobs = np.bincount(ids.ravel(), minlength=cfg.n_experts).tolist() + [len(sample)] * cfg.n_shared
+        used = max(min(nthreads, int(c)) for c in jobs if c > 0)
     desc = (f"{len(sample)} of {cfg.T} tokens per round x {rounds} rounds "
             f"({'dense FFN' if cfg.dense else 'full routing + every selected and shared expert'}, "
             f"weights decoded per round)")
     return done, secs, used, desc
+
+
+def cpu_baseline_entry(cfg, budget_s: float) -> dict:
+    """The oracle on the host's cores and, beside it, on one core."""
+    avail = sorted(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else list(range(os.cpu_count() or 1))
+    ntok = oracle_budget_tokens(cfg)
+    done, secs, used, desc = oracle_sample(cfg, budget_s, ntok, avail)
+    d1, s1, _, desc1 = oracle_sample(cfg, budget_s / 2, ntok, avail[:1])
+    return {"value": done / secs, "unit": "tokens/s", "cores": used, "kind": "oracle",
+            "sample": desc + f"; {secs:.1f} s of CPU work",
+            "host_cores": os.cpu_count(), "cores_available": len(avail),
+            "threads_given": len(avail),
+            "pinning": "the oracle's threads inherit this process's CPU affinity (all available cores); "
+                       "threads are not bound one to a core",
+            "single_core": {"value": d1 / s1, "unit": "tokens/s", "cores": 1,
+                            "pinning": f"bound to CPU {avail[0]}", "sample": desc1 + f"; {s1:.1f} s of CPU work"}}
 
 
 def oracle_budget_tokens(cfg):
@@ -443,6 +582,8 @@ def oracle_budget_tokens(cfg):
 def run_reference(args, cfg, rank, world):
     if rank != 0:
         return None
+    import oracle
+
     times = []
     sample_desc = ""
     used = 1
@@ -454,13 +595,18 @@ def run_reference(args, cfg, rank, world):
         times.append(secs / done)   # seconds per token
     per_tok = sum(times) / len(times)
     value = 1.0 / per_tok
+    if cfg.dense:
+        groups = cfg.n_slices
+    else:
+        ids, _ = oracle.route(wl.router_logits(cfg), cfg.k)
+        groups = len(np.unique(ids)) + cfg.n_shared
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_tok * 1e3 * cfg.T,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded)", "config": {"workload": describe(cfg), "T": cfg.T},
+        "data": "synthetic (seeded)", "config": bench_config(cfg, groups, 1),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
-                         "sample": sample_desc},
+                         "sample": sample_desc, "host_cores": os.cpu_count()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -476,6 +622,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--weights", default="mxfp4", choices=["mxfp4", "int4g32"],
                     help="weight format of a routed workload (group-32 INT4 runs the single-kernel sizes)")
+    ap.add_argument("--extra", default=",".join(EXTRA_WORKLOADS),
+                    help="comma-separated workloads measured beside the main one on the same layer ('none': skip)")
     ap.add_argument("--experts", type=int, default=0,
                     help="profiling aid: routed experts of a smaller layer with the same shapes per expert")
     args = ap.parse_args()
@@ -503,9 +651,7 @@ def main():
     res = run_ours(args, cfg, rank, world)
     if rank == 0:
         if not args.no_cpu_baseline:
-            done, secs, used, desc = oracle_sample(cfg, args.cpu_baseline_seconds, oracle_budget_tokens(cfg))
-            res["cpu_baseline"] = {"value": done / secs, "unit": "tokens/s", "cores": used, "kind": "oracle",
-                                   "sample": desc + f"; {secs:.1f} s of CPU work"}
+            res["cpu_baseline"] = cpu_baseline_entry(cfg, args.cpu_baseline_seconds)
         print(json.dumps(res))
     if world > 1:
         import torch.distributed as dist

@@ -333,12 +333,40 @@ int moe_profile_read(MoeHandle *h, float *ms, int n);
  * ordering between their streams) race on the array and give wrong results:
  * order them on one stream, or with events.
  *
+ * Device-side checks: the kernels record a failure in a flag of the same
+ * scratch, which this call clears on its stream before its kernels run; read
+ * it with moe_route_static_status().
+ *
  * Errors: MOE_EINVAL (E outside [1, MOE_ROUTE_STATIC_MAX_EXPERTS], k outside
  * [1, min(E, 32)], T < 0, T * k > MOE_ROUTE_STATIC_MAX_SLOTS, NULL pointer),
  * MOE_EDEVICE (device ordinal >= 64), MOE_ECUDA (symbol lookup or launch
  * failed).  The message is available from moe_last_error(). */
 MoeStatus moe_route_static(const float *router_logits, int T, int E, int k, int *topk_ids, float *topk_w,
                            int *expert_offsets, int *sorted_slot, int *slot_pos, void *cuda_stream);
+
+/* Device-side status of moe_route_static on the current device.  Waits for
+ * cuda_stream, then reads the error flag that the routing and grouping kernels
+ * set in the fixed scratch (a permutation whose counts disagree with the
+ * histogram).  Each moe_route_static call clears the flag on its stream before
+ * its kernels run, so the status covers the most recent call on this device
+ * (and any call that overlapped it).  Allocates nothing; a 4-byte synchronous
+ * device-to-host copy reads the flag.
+ * Returns MOE_OK (also when no call has run on this device), MOE_EDEVICE (the
+ * flag is set, or the device ordinal is >= 64) or MOE_ECUDA. */
+MoeStatus moe_route_static_status(void *cuda_stream);
+
+/* Test hook for the device-side wait limit.  No counterpart in the paper.
+ * Every wait in the kernels is bounded in time; this arms the next forward
+ * call on this handle that runs the single-kernel path (a decode-sized batch)
+ * so that its grid-wide completion wait before the combine has a target no
+ * launch reaches and a limit of limit_us microseconds.  The wait then expires
+ * in every CTA, which records a timeout and leaves without combining (out is
+ * not written).  That wait runs after all of the kernel's copies and MMAs
+ * have finished.  The handle's sticky device error is then reported as
+ * MOE_EDEVICE by moe_sync_status and later calls; use a fresh handle
+ * afterwards.  Not for production use.
+ * Errors: MOE_EINVAL (NULL handle, limit_us outside [1, 1000000]). */
+MoeStatus moe_debug_expire_next_wait(MoeHandle *h, int limit_us);
 
 /* Human-readable description of the last non-OK status returned on the
  * calling thread (thread-local, never NULL). */

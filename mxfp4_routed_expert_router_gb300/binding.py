@@ -23,8 +23,8 @@ MOE_W_MXFP4, MOE_W_BF16, MOE_W_INT4G32 = 0, 1, 2
 # every symbol include/moe.h declares
 EXPORTED = ("moe_load_weights", "moe_workspace_bytes", "moe_forward", "moe_forward_routed",
             "moe_route_sigmoid", "moe_dense_sliced_forward", "moe_sync_status", "moe_profile_enable",
-            "moe_profile_read", "moe_route_static", "moe_graph_create", "moe_graph_launch", "moe_graph_free",
-            "moe_last_error", "moe_free")
+            "moe_profile_read", "moe_route_static", "moe_route_static_status", "moe_graph_create",
+            "moe_graph_launch", "moe_graph_free", "moe_debug_expire_next_wait", "moe_last_error", "moe_free")
 STAGES = ("routing", "grouping", "gate_up", "down", "combine", "layer")
 
 
@@ -88,6 +88,10 @@ def _load():
     L.moe_profile_read.restype = ci
     L.moe_route_static.argtypes = [vp, ci, ci, ci, vp, vp, vp, vp, vp, vp]
     L.moe_route_static.restype = ci
+    L.moe_route_static_status.argtypes = [vp]
+    L.moe_route_static_status.restype = ci
+    L.moe_debug_expire_next_wait.argtypes = [vp, ci]
+    L.moe_debug_expire_next_wait.restype = ci
     L.moe_last_error.argtypes = []
     L.moe_last_error.restype = ctypes.c_char_p
     L.moe_free.argtypes = [vp]
@@ -211,6 +215,16 @@ def moe_route_static(router_logits, T: int, E: int, k: int, topk_ids, topk_w, ex
     """Routing and grouping with the library's fixed scratch; allocates nothing (see include/moe.h)."""
     _check(lib.moe_route_static(_ptr(router_logits), T, E, k, _ptr(topk_ids), _ptr(topk_w), _ptr(expert_offsets),
                                 _ptr(sorted_slot), _ptr(slot_pos), _stream(stream)))
+
+
+def moe_route_static_status(stream=None) -> None:
+    """Raise MoeError(MOE_EDEVICE) if the most recent moe_route_static call on this device flagged a device error."""
+    _check(lib.moe_route_static_status(_stream(stream)))
+
+
+def moe_debug_expire_next_wait(handle: int, limit_us: int) -> None:
+    """Test hook: the next single-kernel launch on this handle lets its completion wait expire (include/moe.h)."""
+    _check(lib.moe_debug_expire_next_wait(handle, int(limit_us)))
 
 
 def moe_free(handle: int) -> None:

@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -307,17 +309,45 @@ inline cudaError_t make_map_3d(CUtensorMap *m, const void *base, long long rows,
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+constexpr int MAX_DEVICES = 64;
+
+inline int current_device()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        dev = 0;
+    return dev;
+}
+
+// SM count of the current device, looked up once per device.
 inline int sm_count()
 {
-    static int n = 0;
-    if (!n) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0)
-            n = 1;
-    }
+    static std::atomic<int> cached[MAX_DEVICES];
+    const int dev = current_device();
+    int n = dev >= 0 && dev < MAX_DEVICES ? cached[dev].load(std::memory_order_relaxed) : 0;
+    if (n > 0)
+        return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        n = 1;
+    if (dev >= 0 && dev < MAX_DEVICES)
+        cached[dev].store(n, std::memory_order_relaxed);
     return n;
+}
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per device: `done` is the kernel's own flag array, indexed by
+// device ordinal.  Setting the attribute twice (two threads racing on a first
+// launch) is harmless.
+inline cudaError_t smem_limit_once(std::atomic<int> *done, const void *kern, int bytes)
+{
+    const int dev = current_device();
+    const bool cacheable = dev >= 0 && dev < MAX_DEVICES;
+    if (cacheable && done[dev].load(std::memory_order_acquire))
+        return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && cacheable)
+        done[dev].store(1, std::memory_order_release);
+    return e;
 }
 
 

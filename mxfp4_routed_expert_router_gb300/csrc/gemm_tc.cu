@@ -540,13 +540,10 @@ cudaError_t launch_cfg(const TcArgs &a, const CUtensorMap &m1, const CUtensorMap
     constexpr int NB = GU ? 1 : 2;
     constexpr int SMEM = Smem<NMAX, NB, S>::TOTAL;
     auto kern = gemm_tc_kernel<GU, WFMT, NMAX, S>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-        if (e != cudaSuccess)
-            return e;
-        attr = true;
-    }
+    static std::atomic<int> attr_set[MAX_DEVICES];
+    cudaError_t e = smem_limit_once(attr_set, (const void *)kern, SMEM);
+    if (e != cudaSuccess)
+        return e;
     kern<<<sm_count(), NUM_THREADS, SMEM, st>>>(a, m1, m2);
     return cudaGetLastError();
 }

@@ -219,6 +219,11 @@ struct LayerArgs {
     int *sync;
     int *err;
     int R;
+    // the grid-wide completion wait before the combine: extra count on its
+    // target and its time limit (0 and WAIT_LIMIT_NS in every normal launch;
+    // a test of the expiry path raises the target past reach)
+    int done_extra;
+    unsigned long long done_wait_ns;
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -346,9 +351,10 @@ __device__ __forceinline__ void red_release_add(int *p, int v)
 }
 
 // Bounded wait (one thread) until *p >= target, with acquire semantics.
-// Gives up after WAIT_LIMIT_NS (recording DEV_ERR_WAIT_TIMEOUT) or when the
-// CTA's abort flag is raised.
-__device__ __noinline__ bool wait_geq(const int *p, int target, volatile int *abort_flag, int *err)
+// Gives up after limit_ns (recording DEV_ERR_WAIT_TIMEOUT) or when the CTA's
+// abort flag is raised.
+__device__ __noinline__ bool wait_geq(const int *p, int target, volatile int *abort_flag, int *err,
+                                      uint64_t limit_ns = WAIT_LIMIT_NS)
 {
     if (ld_acquire(p) >= target)
         return true;
@@ -360,7 +366,7 @@ __device__ __noinline__ bool wait_geq(const int *p, int target, volatile int *ab
         if ((i & 15u) == 0) {
             if (abort_flag && *abort_flag)
                 return false;
-            if (global_ns() - t0 > WAIT_LIMIT_NS) {
+            if (global_ns() - t0 > limit_ns) {
                 atomicCAS(err, 0, DEV_ERR_WAIT_TIMEOUT);
                 if (abort_flag)
                     *abort_flag = 1;
@@ -1479,7 +1485,7 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
     // (token, 128-feature block)s w * gridDim.x + b, then every LS_WARPS * gridDim.x
     if (tid == 0) {
         red_release_add(&a.sync[SY_DONE], 1);
-        bool okc = wait_geq(&a.sync[SY_DONE], (int)gridDim.x, abort_flag, a.err);
+        bool okc = wait_geq(&a.sync[SY_DONE], (int)gridDim.x + a.done_extra, abort_flag, a.err, a.done_wait_ns);
         if (okc && a.E > 0 && a.n > 0)
             okc = wait_geq(&a.sync[SY_PERM], 1, abort_flag, a.err);
         misc[2] = okc ? 1 : 0;
@@ -1524,13 +1530,10 @@ cudaError_t ls_launch(LayerArgs a, cudaStream_t st)
         return cudaErrorNotSupported;
     const LsSmem L = ls_smem(a.R, a.G, a.n, a.T, C::STAGE, C::RED_BYTES, C::HMAX_BYTES);
     auto kern = layer_stream_kernel<WFMT, NT>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_LIMIT);
-        if (e != cudaSuccess)
-            return e;
-        attr = true;
-    }
+    static std::atomic<int> attr_set[MAX_DEVICES];
+    cudaError_t e = smem_limit_once(attr_set, (const void *)kern, C::SMEM_LIMIT);
+    if (e != cudaSuccess)
+        return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(sm_count() * C::CTAS));
     cfg.blockDim = dim3(LS_THREADS);
@@ -1595,7 +1598,7 @@ bool layer_stream_fits(const Plan &p, int fmt)
 
 cudaError_t launch_layer_stream(const Plan &p, const WeightStore &gu, const WeightStore &dn, int fmt,
                                 const uint16_t *x, const float *logits, const int *ids_in, const float *w_in,
-                                float *out, int accumulate, cudaStream_t st)
+                                float *out, int accumulate, cudaStream_t st, int expire_wait_us)
 {
     cudaError_t e = cudaMemsetAsync(p.sync, 0, layer_stream_sync_bytes(p.G), st);
     if (e != cudaSuccess)
@@ -1638,6 +1641,8 @@ cudaError_t launch_layer_stream(const Plan &p, const WeightStore &gu, const Weig
     a.accumulate = accumulate;
     a.sync = p.sync;
     a.err = p.err;
+    a.done_extra = expire_wait_us > 0 ? 1 : 0;
+    a.done_wait_ns = expire_wait_us > 0 ? (unsigned long long)expire_wait_us * 1000ull : WAIT_LIMIT_NS;
     const int nt = ls_nt(p.T);
     return fmt == FMT_MXFP4  ? ls_launch_fmt<FMT_MXFP4>(nt, a, st)
            : fmt == FMT_INT4 ? ls_launch_fmt<FMT_INT4>(nt, a, st)

@@ -27,6 +27,7 @@ struct MoeHandle {
     WeightStore gu_f, dn_f;    // FRAG layout (register-streaming GEMMs, decode-sized batches)
     int *err_host = nullptr;   // mapped pinned host memory, written by kernels on device-side errors
     int *err_dev = nullptr;    // device alias of err_host
+    int expire_wait_us = 0;    // moe_debug_expire_next_wait: armed for the next single-kernel launch
     bool profile = false;      // record stage events (moe_profile_enable)
     bool profiled = false;     // a call has recorded its events
     cudaEvent_t ev[7] = {};
@@ -149,8 +150,10 @@ MoeStatus run_layer(MoeHandle *h, const void *x, const float *logits, const int 
     if (stream && layer_stream_fits(p, h->fmt)) {
         for (int i = 0; i <= 5; ++i)
             mark(i);
+        const int expire = h->expire_wait_us;
+        h->expire_wait_us = 0;
         if ((e = launch_layer_stream(p, h->gu_f, h->dn_f, h->fmt, (const uint16_t *)x, logits, ids_in, w_in, out,
-                                     accumulate, st)) != cudaSuccess)
+                                     accumulate, st, expire)) != cudaSuccess)
             return cuda_fail(e, "layer launch");
         mark(6);
         if (h->profile)
@@ -650,6 +653,16 @@ int moe_profile_read(MoeHandle *h, float *ms, int n)
         ms[i] = t;
     }
     return m;
+}
+
+MoeStatus moe_debug_expire_next_wait(MoeHandle *h, int limit_us)
+{
+    if (!h)
+        return fail(MOE_EINVAL, "moe_debug_expire_next_wait: NULL handle");
+    if (limit_us < 1 || limit_us > 1000000)
+        return fail(MOE_EINVAL, "moe_debug_expire_next_wait: limit %d us outside [1, 1000000]", limit_us);
+    h->expire_wait_us = limit_us;
+    return MOE_OK;
 }
 
 const char *moe_last_error(void) { return g_msg; }

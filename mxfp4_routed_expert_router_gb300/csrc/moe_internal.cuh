@@ -197,10 +197,14 @@ size_t layer_stream_sync_bytes(int G);
 // shared-memory and scheduling limits)
 bool layer_stream_fits(const Plan &p, int fmt);
 
-// zeroes p.sync, then launches the layer kernel cooperatively (one CTA per SM)
+// zeroes p.sync, then launches the layer kernel cooperatively (one CTA per SM).
+// expire_wait_us > 0 (tests of the device-side wait limit only): the kernel's
+// grid-wide completion wait before the combine gets a target no launch reaches
+// and a limit of that many microseconds, so it expires, records
+// DEV_ERR_WAIT_TIMEOUT and the kernel leaves without combining.
 cudaError_t launch_layer_stream(const Plan &p, const WeightStore &gu, const WeightStore &dn, int fmt,
                                 const uint16_t *x, const float *logits, const int *ids_in, const float *w_in,
-                                float *out, int accumulate, cudaStream_t st);
+                                float *out, int accumulate, cudaStream_t st, int expire_wait_us = 0);
 
 // Record msg as the calling thread's moe_last_error() text; returns status.
 int set_last_error(int status, const char *msg);

@@ -22,7 +22,8 @@ constexpr int STATIC_MAX_SLOTS = MOE_ROUTE_STATIC_MAX_SLOTS;
 // of this call.  counts must read zero before the histogram adds to it: the
 // router kernel zeroes it at the start of every call.  The other members are
 // written before they are read within a call.  err is the kernels' first-error
-// flag (starts at zero when the module loads; not read back by this call).
+// flag: every call clears it on its stream before its kernels run, and
+// moe_route_static_status() reads it back.
 struct RouteScratch {
     int counts[STATIC_MAX_EXPERTS];
     int grp_start[STATIC_MAX_EXPERTS];
@@ -106,10 +107,39 @@ extern "C" MoeStatus moe_route_static(const float *router_logits, int T, int E, 
     p.grp_count = sc->grp_count;
     p.row_token = sc->row_token;
     p.err = &sc->err;
-    e = moe::launch_router(router_logits, T, E, k, topk_ids, topk_w, sc->counts, E, st);
+    // this call's device-side checks start from a clear flag
+    e = cudaMemsetAsync(&sc->err, 0, sizeof(int), st);
+    if (e == cudaSuccess)
+        e = moe::launch_router(router_logits, T, E, k, topk_ids, topk_w, sc->counts, E, st);
     if (e == cudaSuccess)
         e = moe::launch_permute(p, st);
     if (e != cudaSuccess)
         return report(MOE_ECUDA, "moe_route_static: kernel launch failed (error %lld)", (long long)e);
+    return MOE_OK;
+}
+
+extern "C" MoeStatus moe_route_static_status(void *cuda_stream)
+{
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return report(MOE_ECUDA, "moe_route_static_status: cudaGetDevice failed (error %lld)", (long long)e);
+    if (dev < 0 || dev >= MAX_DEVICES)
+        return report(MOE_EDEVICE, "moe_route_static_status: device ordinal %lld not supported", dev);
+    void *base;
+    {
+        std::lock_guard<std::mutex> lock(g_setup_mu);
+        base = g_scratch_addr[dev];
+    }
+    if (!base)
+        return MOE_OK;  // no call has run on this device
+    if ((e = cudaStreamSynchronize((cudaStream_t)cuda_stream)) != cudaSuccess)
+        return report(MOE_ECUDA, "moe_route_static_status: cudaStreamSynchronize failed (error %lld)", (long long)e);
+    int flag = 0;
+    e = cudaMemcpy(&flag, &static_cast<RouteScratch *>(base)->err, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess)
+        return report(MOE_ECUDA, "moe_route_static_status: reading the error flag failed (error %lld)", (long long)e);
+    if (flag != 0)
+        return report(MOE_EDEVICE, "moe_route_static: a kernel reported device error %lld", flag);
     return MOE_OK;
 }

@@ -38,3 +38,26 @@ def oracle_moe(cfg: wl.LayerConfig, x_bits: np.ndarray, logits: np.ndarray, toke
 def oracle_dense(cfg: wl.LayerConfig, x_bits: np.ndarray, tokens: np.ndarray, weights=None):
     weights = weights if weights is not None else wl.dense_weights(cfg)
     return oracle.dense_ffn(weights, x_bits[tokens], 0, cfg.weight_format)
+
+
+def oracle_weights(cfg: wl.LayerConfig, experts) -> "oracle.OracleWeights":
+    """Oracle weights holding the given experts (and every shared expert) of cfg."""
+    W = oracle.OracleWeights(cfg.hidden, cfg.inter, cfg.n_experts, cfg.n_shared, cfg.weight_format)
+    for e in sorted(set(int(v) for v in experts) | set(range(cfg.n_experts, cfg.n_groups))):
+        W.set_expert(e, *wl.expert_weights(cfg, e))
+    return W
+
+
+def oracle_moe_routed(cfg: wl.LayerConfig, x_bits: np.ndarray, ids: np.ndarray, w: np.ndarray):
+    """Oracle output of the layer for routing given as ids and weights (rows of x_bits)."""
+    W = oracle_weights(cfg, np.unique(ids))
+    return oracle.moe_layer_routed(W, x_bits, ids, w, nthreads=NTHREADS)
+
+
+def skewed_logits(cfg: wl.LayerConfig, hot: int, n_hot: int, boost: float = 8.0) -> np.ndarray:
+    """The config's logits with expert `hot` pushed to the top for the first
+    n_hot tokens, so that one group holds many token tiles (a seeded test
+    input; nothing of the layer's arithmetic)."""
+    lg = wl.router_logits(cfg).copy()
+    lg[:n_hot, hot] += np.float32(boost)
+    return lg

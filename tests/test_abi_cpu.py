@@ -103,6 +103,9 @@ def test_host_side_argument_checks_without_gpu(built):
     assert L.moe_graph_create(None, None, None, None, None, 1, 1, None, 0, None, 0, None, None) == b.MOE_EINVAL
     assert L.moe_graph_launch(None, None) == b.MOE_EINVAL
     L.moe_graph_free(None)  # no-op
+    # the wait-limit test hook checks its handle before anything else
+    assert L.moe_debug_expire_next_wait(None, 1000) == b.MOE_EINVAL
+    assert b"NULL handle" in L.moe_last_error()
     L.moe_free(None)  # no-op
 
 

@@ -15,7 +15,7 @@ import pytest
 import torch
 
 import oracle
-from parity_util import TOL, TOL_W, oracle_dense, oracle_moe, rel_err
+from parity_util import TOL, TOL_W, oracle_dense, oracle_moe, rel_err, skewed_logits
 
 from mxfp4_routed_expert_router_gb300 import workloads as wl
 
@@ -221,6 +221,36 @@ def test_bad_forward_arguments():
     L.free()
 
 
+def test_wait_expiry_reports_device_error_and_a_fresh_handle_works():
+    """A bounded wait that runs out: the single kernel's grid-wide completion wait
+    is armed with a target no launch reaches and a 1 ms limit.  The kernel must
+    leave cleanly, the handle must report MOE_EDEVICE (a timeout), the context
+    must stay usable, and a fresh handle must still match the oracle."""
+    B, layer = _binding()
+    cfg = wl.custom("expire_T4_H256_I128_E16_S1_k4", 4, 256, 128, 16, 1, 4, seed=63)
+    x, lg = wl.tokens(cfg), wl.router_logits(cfg)
+    L = layer.MoeLayer(cfg)
+    with pytest.raises(B.MoeError) as e:
+        B.moe_debug_expire_next_wait(L.handle, 0)
+    assert e.value.status == B.MOE_EINVAL
+    B.moe_debug_expire_next_wait(L.handle, 1000)
+    L.forward(layer.bf16_tensor(x), torch.from_numpy(lg).cuda())
+    with pytest.raises(B.MoeError) as e:
+        L.sync()
+    assert e.value.status == B.MOE_EDEVICE and "device error 3" in str(e.value)
+    # the error is sticky on this handle: the next call is refused before any launch
+    with pytest.raises(B.MoeError) as e:
+        L.forward(layer.bf16_tensor(x), torch.from_numpy(lg).cuda())
+    assert e.value.status == B.MOE_EDEVICE
+    L.free()
+    torch.cuda.synchronize()
+    L2 = layer.MoeLayer(cfg)
+    out, ids, w, off, ss, sp = run_routed(L2, cfg, x, lg)
+    check_routing(cfg, lg, ids, w, off, ss, sp)
+    assert rel_err(out, oracle_moe(cfg, x, lg, np.arange(cfg.T))) <= TOL
+    L2.free()
+
+
 # ------------------------------------------------------------------ the full-size layer (bench shapes)
 
 @pytest.fixture(scope="module")
@@ -246,6 +276,30 @@ def test_full_size_layer(big_layer, cfg, n_sample):
     ref = oracle_moe(cfg, x, lg, tok)
     assert rel_err(out[tok], ref) <= TOL
     assert np.all(np.isfinite(out))
+
+
+@pytest.mark.parametrize("cfg,hot_tokens", [
+    # one routed group of ~950 tokens: 4 gate|up token tiles of up to 256 and 8 down
+    # tiles of up to 128, both with a ragged last tile; the shared group spans all
+    # 1000 tokens; the other routed groups are small (one partial tile each)
+    (wl.custom("multi_tile_T1000_H7168_I2048_E6_S1_k2", 1000, 7168, 2048, 6, 1, 2, seed=61), 950),
+    # a group just past one tile boundary next to near-empty groups
+    (wl.custom("multi_tile_T300_H7168_I2048_E5_S1_k1", 300, 7168, 2048, 5, 1, 1, seed=62), 257),
+], ids=lambda v: v.name if hasattr(v, "name") else str(v))
+def test_full_hidden_multi_tile_every_element(cfg, hot_tokens):
+    """Full H and I on the tensor-core path, with groups that span several token
+    tiles of both GEMMs: every output element against the oracle."""
+    _, layer = _binding()
+    L = layer.MoeLayer(cfg)
+    x, lg = wl.tokens(cfg), skewed_logits(cfg, 0, hot_tokens)
+    out, ids, w, off, ss, sp = run_routed(L, cfg, x, lg)
+    L.free()
+    check_routing(cfg, lg, ids, w, off, ss, sp)
+    counts = np.diff(off)
+    assert counts[0] >= hot_tokens
+    ref = oracle_moe(cfg, x, lg, np.arange(cfg.T))
+    assert np.all(np.isfinite(out))
+    assert rel_err(out, ref) <= TOL
 
 
 # ------------------------------------------------------------------ dense FFN as all-active slices

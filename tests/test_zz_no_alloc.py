@@ -1,6 +1,8 @@
 """moe_route_static: routing and grouping with the library's fixed device
 scratch and no allocation.  Its results must equal those moe_forward writes
-through MoeRoutingOut on the same logits.
+through MoeRoutingOut on the same logits, and match the oracle's routing and
+stable permutation bit for bit (weights within 1e-6); its device-side error
+flag, read by moe_route_static_status, stays clear.
 
 Named to be collected last, so the GPU test runs both after every other test
 in the session and (run on its own) in a fresh process.
@@ -12,6 +14,7 @@ import re
 import numpy as np
 import pytest
 
+import oracle
 from parity_util import TOL_W
 from mxfp4_routed_expert_router_gb300 import workloads as wl
 
@@ -73,6 +76,17 @@ def _forward_routing(torch, B, L, cfg, x_bits, logits, k):
     return [b.cpu().numpy() for b in bufs]
 
 
+def _assert_oracle(static, logits, E, k):
+    ids, w, off, ss, sp = static
+    rid, rw = oracle.route(logits, k)
+    np.testing.assert_array_equal(ids, rid)
+    assert np.max(np.abs(w - rw)) <= TOL_W
+    roff, rss, rsp = oracle.permute(rid, E)
+    np.testing.assert_array_equal(off, roff)
+    np.testing.assert_array_equal(ss, rss)
+    np.testing.assert_array_equal(sp, rsp)
+
+
 def _assert_same(static, ref):
     ids, w, off, ss, sp = static
     rids, rw, roff, rss, rsp = ref
@@ -101,9 +115,11 @@ def test_route_static_matches_forward_routing_two_calls_in_a_row():
         bufs = _routing_buffers(torch, c.T, E, k)
         B.moe_route_static(torch.from_numpy(lg).cuda(), c.T, E, k, *bufs)
         outs.append(bufs)
-    torch.cuda.synchronize()
-    for bufs, ref in zip(outs, refs):
-        _assert_same([b.cpu().numpy() for b in bufs], ref)
+    B.moe_route_static_status()
+    for bufs, ref, (x, lg) in zip(outs, refs, inputs):
+        got = [b.cpu().numpy() for b in bufs]
+        _assert_same(got, ref)
+        _assert_oracle(got, lg, E, k)
     L.free()
 
 
@@ -123,8 +139,10 @@ def test_route_static_at_the_slot_limit():
     for _ in range(2):
         bufs = _routing_buffers(torch, T, E, k)
         B.moe_route_static(lg_d, T, E, k, *bufs)
-        torch.cuda.synchronize()
-        _assert_same([b.cpu().numpy() for b in bufs], ref)
+        B.moe_route_static_status()
+        got = [b.cpu().numpy() for b in bufs]
+        _assert_same(got, ref)
+        _assert_oracle(got, lg, E, k)
     with pytest.raises(B.MoeError) as e:
         B.moe_route_static(lg_d, T + 1, E, k, *_routing_buffers(torch, 1, E, k))
     assert e.value.status == B.MOE_EINVAL and "fixed scratch limit" in str(e.value)
