@@ -18,19 +18,6 @@ namespace {
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 constexpr int MAX_GROUPS = 1088;
 
-struct GemmArgs {
-    const uint8_t *wbase;
-    size_t group_bytes;
-    int kchunks, chunk_bytes, row_tiles;
-    const int *grp_start, *grp_count;
-    int E, G, I, H;
-    uint16_t *h_out;
-    long long h_plane;
-    float *y_out;
-    int *err;
-    int brows;  // token rows per TMA box of the B operand (16, or 64 when every B tensor has that many rows)
-};
-
 // ------------------------------------------------------------------ PTX helpers
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }

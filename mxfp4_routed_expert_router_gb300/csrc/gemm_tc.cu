@@ -7,33 +7,57 @@
 // with the SwiGLU expert of "Cascadia: Resident 975B MoE Inference on Eleven
 // AI PCs" §3.1 and MXFP4 weights decoded inside the reduction as in
 // "DeepSeek-V4-Flash on a four-GPU Ampere workstation", section "MXFP4 is not
-// NVFP4, and the difference matters on Ampere" (scale loaded once per 32-value
-// block, FP32 accumulation, no decoded copy of an expert in device memory).
+// NVFP4, and the difference matters on Ampere" (the block scale applied once
+// per 32-value block, FP32 accumulation, no decoded copy of an expert in
+// device memory).
 //
 // Mapping to the hardware ("swap-AB": weights are the M side):
-//   D[128 weight rows, N tokens] (FP32, TMEM)  +=  A[128 rows, K] . B[N tokens, K]^T
-//   A = 128 weight rows decoded to BF16 in shared memory by CUDA-core warps,
-//       straight from the MXFP4 chunks in global memory (each decoder thread
-//       keeps its next stages' raw bytes in flight in registers);
-//   B = token rows (BF16; for down the hi and lo BF16 planes of h, two MMAs per
-//       K step), loaded by TMA into the 128-byte-swizzled K-major layout;
-//   MMA = tcgen05.mma kind::f16, M=128, N = 16..NMAX, K=16, issued by one thread.
-// A work item is (group, pair of 128-row tiles, token tile): both row tiles
-// share every staged token tile, so a 64 KB stage feeds 2 x 128 x N x 64
-// multiply-adds -- twice as many per staged byte as one row tile.
+//   D[128 weight rows, N tokens] (FP32, tensor memory) += A[128 rows, K] . B[N tokens, K]^T
+//   A = weight rows, decoded by CUDA-core warps straight from the weight chunks
+//       in global memory and written into TENSOR MEMORY (tcgen05.st); the MMA
+//       reads A from there, so shared memory carries only the token operand;
+//   B = token rows, loaded by TMA into 128-byte-swizzled K-major tiles;
+//   MMA = tcgen05.mma kind::f16, M = 128, N = 16..256, K = 16, one thread.
+// A work item is (group, 128-row tile, token tile of up to 256), and a pipeline
+// stage is 128 values of K: eight MMAs of up to 128 cycles per hand-off between
+// the producers and the MMA thread.  (Measured: the tensor pipe idles when a
+// stage's hand-off guards few or short MMAs -- two 128 x 128 tiles per 64-wide
+// stage ran at about half rate; one 128 x 256 tile per 128-wide stage at full
+// rate.)  Tensor memory holds the 256-column accumulator and three stages of A
+// (64 columns each); shared memory three 64 KB stages of B.
+//
+// Two operand types (chosen per handle at load):
+//   FP16: MXFP4 weights whose E8M0 exponents span at most 23 within every row.
+//     A weight decodes to v(c) * 2^(e - b), b the row's largest exponent: one
+//     hardware e2m1x2 -> f16x2 conversion per pair and one multiply by a power
+//     of two, both exact (every value is a multiple of 2^-24 with at most two
+//     significant bits).  The epilogue multiplies each row's accumulator by
+//     2^(b - 127).  Token rows are FP16 x * 2^-xs (a power of two per token,
+//     chosen so that the conversion of the BF16 values is exact); h leaves
+//     gate|up in FP32 with a per-position maximum, is turned into one FP16
+//     plane with a power of two per position, and down runs one MMA per K step.
+//   BF16: BF16 weights, or MXFP4 whose exponents spread wider.  Weights decode
+//     exactly to BF16 v(c) * 2^(e - 127); tokens are the caller's BF16 rows; h
+//     is kept as BF16 hi + lo planes (lo = bf16(h - hi)), so down runs two MMAs
+//     per K step (and its stages hold 64 values of K, to keep 64 KB of B).
 // One CTA per SM walks a static schedule of work items.  Warp roles:
-//   warp 0      TMA-loads token tiles (B) into the stage ring
-//   warp 1      allocates TMEM, issues the MMAs, commits to mbarriers
-//   warps 2-17  decode MXFP4 (or copy BF16) into the swizzled A stages
-//   warps 18-25 epilogue, two warps per TMEM lane quadrant splitting the
-//               columns: TMEM -> registers, SwiGLU (gate|up) or FP32 y (down)
-// Two TMEM accumulator sets (when N allows) let the epilogue of one work item
-// overlap the MMAs of the next.  Every mbarrier wait is bounded: on a timeout
-// the kernel records DEV_ERR_WAIT_TIMEOUT, stops issuing work, waits (bounded)
-// for the copies and MMAs it has in flight, frees its TMEM and exits.
+//   warp 0      TMA-loads token tiles (B) into the shared-memory stage ring and
+//               prefetches the weight chunks ahead of the decoders into L2
+//   warp 1      allocates tensor memory, issues the MMAs, commits to mbarriers
+//   warps 2-13  decode weights into the tensor-memory A ring: three groups of
+//               four warps, group g decoding every third stage (ring slot g) in
+//               full; its warp w covers lane quadrant w % 4 (the lanes a warp
+//               may access)
+//   warps 14-21 epilogue, two warps per lane quadrant splitting the columns:
+//               tensor memory -> registers, SwiGLU (gate|up) or FP32 y (down);
+//               the accumulator is released once per work item.
+// Every mbarrier wait is bounded: on a timeout the kernel records
+// DEV_ERR_WAIT_TIMEOUT, stops issuing work, waits (bounded) for the copies and
+// MMAs it has in flight, frees its tensor memory and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "gemm_common.cuh"
 #include "mx_decode.cuh"
@@ -44,19 +68,62 @@ namespace {
 
 using namespace gemm;
 
-constexpr int N_DEC_WARPS = 16;
-constexpr int N_EPI_WARPS = 8;  // two per TMEM lane quadrant, splitting the columns
+constexpr int N_DEC_WARPS = 12;
+constexpr int N_DEC_GROUPS = N_DEC_WARPS / 4;  // groups of four warps, one per tensor-memory lane quadrant
+constexpr int N_EPI_WARPS = 8;                 // two per tensor-memory lane quadrant, splitting the columns
 constexpr int NUM_THREADS = (2 + N_DEC_WARPS + N_EPI_WARPS) * 32;
 constexpr int WARP_BLOAD = 0, WARP_MMA = 1, WARP_DEC0 = 2, WARP_EPI0 = WARP_DEC0 + N_DEC_WARPS;
-constexpr int A_STAGE_BYTES = TILE_ROWS * HALF_K * 2;  // 16 KB: 128 rows x 64 BF16
+constexpr int NMAX = 256;                      // token columns of a work item
+constexpr int TC_STAGES = 3;                   // pipeline stages in flight
+constexpr int TMEM_COLS = 512;                 // the whole tensor memory of the SM
+constexpr int A_SLOT_COLS = 64;                // tensor-memory columns of a stage of A: 128 16-bit values per lane
+constexpr int TMEM_A0 = NMAX;                  // first column of the A ring, after the accumulator
+static_assert(TMEM_A0 + TC_STAGES * A_SLOT_COLS <= TMEM_COLS, "tensor memory");
+// Decoder group g fills ring slot g only (stages g, g + TC_STAGES, ...): it then
+// waits on that slot's empty barrier for its own previous stage alone, never
+// for a phase two behind (where the parity it waits for would already read as
+// complete from an older phase).
+static_assert(N_DEC_GROUPS == TC_STAGES, "one decoder group per ring slot");
+constexpr int B_SLICE_BYTES = NMAX * HALF_K * 2;  // 32 KB: 256 token rows x 64 16-bit values (one swizzled tile)
+constexpr int B_STAGE_BYTES = 2 * B_SLICE_BYTES;  // two slices: 128 K values of one plane, or 64 of two planes
 // B operand TMA boxes: 64 token rows (8 KB) each, so that a stage takes few
 // TMA issues; 16 rows when a B tensor has fewer than 64 rows
 constexpr int B_BOX_ROWS_BIG = 64, B_BOX_ROWS_SMALL = 16;
+// the token loader also prefetches the weight chunks this many chunks ahead of
+// the stage it loads into L2, where the decoders' own loads (issued one of
+// their stages ahead) then find them
+constexpr int PF_CHUNKS = 8;
 
-using TcArgs = GemmArgs;
+struct TcArgs {
+    const uint8_t *wbase;
+    size_t group_bytes;
+    int kchunks, chunk_bytes, row_tiles;
+    const uint8_t *row_base;  // FP16 operands: largest E8M0 exponent of every row, [G][row_tiles * 128]
+    const int *grp_start, *grp_count;
+    int E, G, I, H;
+    // gate|up output: BF16 operands h hi + lo planes; FP16 operands FP32 h and per-position maxima
+    uint16_t *h_out;
+    long long h_plane;
+    float *h32;
+    int *hmax;
+    const int *row_token;  // token of each position
+    const int *xsp;        // FP16 operands: power of two of each position's FP16 token row
+    // down output
+    float *y_out;
+    const int *hsp;        // FP16 operands: per-position power of two of the FP16 h rows
+    int *err;
+    int brows;  // token rows per TMA box of the B operand (16, or 64 when every B tensor has that many rows)
+};
+
+enum { OP_F16 = 0, OP_BF16 = 1 };
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 __device__ __forceinline__ void tc_commit(uint64_t *bar)
 {
@@ -64,24 +131,36 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar)
                  : "memory");
 }
 
-// The four K=16 MMAs of one 64-wide stage: descriptors advance by 32 bytes
-// (2 in the address field) per K step; the first MMA accumulates only when
-// acc0 != 0, the other three always.
-__device__ __forceinline__ void tc_mma4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+// The four K=16 MMAs of one 64-wide stage with A in tensor memory: A advances
+// by 8 columns (16 values per lane) and the B descriptor by 32 bytes (2 in the
+// address field) per K step; the first MMA accumulates only when acc0 != 0,
+// the other three always.
+__device__ __forceinline__ void tc_mma4(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                         uint32_t acc0)
 {
     asm volatile(
         "{\n .reg .pred p0, p1;\n setp.ne.b32 p0, %4, 0;\n setp.eq.b32 p1, %4, %4;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %3, p1;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %3, p1;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %10, %3, p1;\n}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc0), "l"(a_desc + 2), "l"(b_desc + 2), "l"(a_desc + 4),
-        "l"(b_desc + 4), "l"(a_desc + 6), "l"(b_desc + 6)
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %3, p1;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %3, p1;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %10, %3, p1;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc0), "r"(a_tmem + 8), "l"(b_desc + 2), "r"(a_tmem + 16),
+        "l"(b_desc + 4), "r"(a_tmem + 24), "l"(b_desc + 6)
         : "memory");
 }
 
-// 32 consecutive TMEM columns of this warp's 32 lanes, one wait
+// 16 consecutive tensor-memory columns of this warp's 32 lanes from registers
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t v[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
+// 32 consecutive tensor-memory columns of this warp's 32 lanes, one wait
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32])
 {
     uint32_t r[32];
@@ -123,83 +202,85 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
            (2ull << 61);
 }
 
-// Instruction descriptor of kind::f16: BF16 A and B, FP32 D, both K-major,
-// M = 128, N given.
-__device__ __forceinline__ uint32_t idesc_bf16(int n)
+// Instruction descriptor of kind::f16: FP16 (OP_F16) or BF16 A and B, FP32 D,
+// both K-major, M = 128, N given.
+template <int OP>
+__device__ __forceinline__ uint32_t make_idesc(int n)
 {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(TILE_ROWS >> 4) << 24);
+    const uint32_t ab = OP == OP_BF16 ? (1u << 7) | (1u << 10) : 0u;
+    return (1u << 4) | ab | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(TILE_ROWS >> 4) << 24);
 }
 
-// Byte offset of 16-byte chunk c (0..7) of row r inside a 128-byte-swizzled
-// K-major tile whose rows are 128 bytes: 8-row groups are 1024 bytes apart
-// and the chunk index is XORed with the row's position in its group.
-__device__ __forceinline__ uint32_t sw128_offset(int r, int c)
+// {2^d, 2^d} in FP16 for d in [-24, 0] (below -14 a subnormal, exactly)
+__device__ __forceinline__ uint32_t f16x2_pow2(int d)
 {
-    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+    const uint32_t b = d >= -14 ? (uint32_t)(d + 15) << 10 : 1u << (d + 24);
+    return b * 0x10001u;
 }
 
-// Work item: (expert group, pair of 128-row weight tiles, token tile).  The two
-// row tiles share every token (B) stage, which halves the token bytes staged
-// per multiply-add against one row tile per item.
-__device__ __forceinline__ int tile_pairs(int row_tiles) { return (row_tiles + 1) / 2; }
+// 8 E2M1 codes (4 bytes; element 2j in the low nibble of byte j) -> 4 FP16
+// pairs times the power of two s2 (low element in the low half)
+__device__ __forceinline__ void e2m1x8_f16(uint32_t w, uint32_t s2, uint32_t *out)
+{
+    uint32_t c[4];
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+        : "=r"(c[0]), "=r"(c[1]), "=r"(c[2]), "=r"(c[3])
+        : "r"(w));
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(out[i]) : "r"(c[i]), "r"(s2));
+}
 
-template <int NMAX, int NB, int S>
+// 2^k as a float for |k| <= 126
+__device__ __forceinline__ float pow2i(int k) { return __int_as_float((127 + k) << 23); }
+
 struct Smem {
-    static constexpr int A_STAGE = 2 * A_STAGE_BYTES;        // two row tiles x 128 rows x 64 BF16
-    static constexpr int B_STAGE = NMAX * HALF_K * 2 * NB;   // NB token planes
-    static constexpr int STAGE = A_STAGE + B_STAGE;
-    static constexpr int BAR_OFF = S * STAGE;
-    static constexpr int N_BARS = 2 * S + 4;
+    static constexpr int BAR_OFF = TC_STAGES * B_STAGE_BYTES;
+    static constexpr int N_BARS = 2 * TC_STAGES + 2;
     static constexpr int SCHED_OFF = BAR_OFF + N_BARS * 8;
     static constexpr int MISC_OFF = SCHED_OFF + (MAX_GROUPS + 1) * 4;
-    static constexpr int TOTAL = MISC_OFF + 32 + 1024;  // + alignment slack
-};
-
-// Stages of raw weights a decoder thread keeps in flight in registers (its own
-// global loads, so no shared-memory staging of the raw chunks is needed).
-template <int WFMT>
-struct DecPipe {
-    static constexpr int PD = WFMT == FMT_MXFP4 ? 4 : 2;
-    static constexpr int V = WFMT == FMT_MXFP4 ? 1 : 2;  // vectors per thread, tile and stage (MXFP4: 8 bytes)
+    static constexpr int COLSC_OFF = MISC_OFF + 32;    // epilogue: column scales of an item, one row per warp
+    static constexpr int TOTAL = COLSC_OFF + N_EPI_WARPS * NMAX * 4 + 1024;  // + alignment slack
 };
 
 // ------------------------------------------------------------------ kernel
 
-template <bool GU, int WFMT, int NMAX, int S>
+template <bool GU, int OP, int WFMT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_b2)
 {
-    constexpr int NB = GU ? 1 : 2;
-    using L = Smem<NMAX, NB, S>;
-    constexpr int NBUF = 4 * NMAX <= 512 ? 2 : 1;      // accumulator sets (two row tiles each)
-    constexpr int TMEM_COLS_RAW = 2 * NMAX * NBUF;
-    constexpr int TMEM_COLS = TMEM_COLS_RAW < 32 ? 32 : TMEM_COLS_RAW;
-    static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM columns");
+    static_assert(OP == OP_BF16 || WFMT == FMT_MXFP4, "FP16 operands decode MXFP4 weights only");
+    constexpr int NB = (!GU && OP == OP_BF16) ? 2 : 1;  // token planes: down with BF16 operands reads h hi + lo
+    constexpr int KST = NB == 2 ? HALF_K : CHUNK_K;     // K values per stage
+    constexpr int NSL = KST / HALF_K;                   // 64-wide K slices per stage
+    constexpr int NBLK = KST / 32;                      // 32-value blocks per stage
+    constexpr int S = TC_STAGES;
+    using L = Smem;
     static_assert(L::TOTAL <= 232448, "shared memory");
-    using DP = DecPipe<WFMT>;
-    constexpr int PD = DP::PD, V = DP::V;
+    static_assert(NSL * NB == 2, "a stage holds two swizzled B tiles");
 
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);
     uint64_t *ab_full = bars, *ab_empty = bars + S;
-    uint64_t *acc_full = bars + 2 * S, *acc_empty = acc_full + 2;
+    uint64_t *acc_full = bars + 2 * S, *acc_empty = acc_full + 1;
     int *prefix = reinterpret_cast<int *>(smem + L::SCHED_OFF);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::MISC_OFF + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int pairs = tile_pairs(a.row_tiles);
+    const int rt_n = a.row_tiles;
+    const int rb_stride = a.row_tiles * TILE_ROWS;
 
     if (tid == 0) {
         for (int i = 0; i < S; ++i) {
-            mbar_init(&ab_full[i], 1 + N_DEC_WARPS);
+            mbar_init(&ab_full[i], 1 + 4);  // the token copy and the four warps of the stage's decoder group
             mbar_init(&ab_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&acc_full[i], 1);
-            mbar_init(&acc_empty[i], N_EPI_WARPS);
-        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, N_EPI_WARPS);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async();
@@ -211,7 +292,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (warp == WARP_BLOAD)
-        schedule_prefix(a.grp_count, a.G, pairs, NMAX, prefix, lane);
+        schedule_prefix(a.grp_count, a.G, rt_n, NMAX, prefix, lane);
     if (warp == WARP_BLOAD && lane == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b2)) : "memory");
@@ -221,20 +302,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int total = prefix[a.G];
-    const int nstages = 2 * a.kchunks;
+    const int nstages = a.kchunks * (CHUNK_K / KST);
+    // first weight chunk of row tile w.rt of group w.g
+    auto tile_src = [&](const WorkItem &w) {
+        return a.wbase + (size_t)w.g * a.group_bytes + (size_t)w.rt * a.kchunks * (size_t)a.chunk_bytes;
+    };
 
     // Every role walks the same static schedule t = blockIdx.x, +gridDim.x, ...
-    // (decompose() over row-tile pairs: w.rt is the pair index).  Single-thread
-    // roles keep the whole warp in the loop (lane 0 issues).
+    // (decompose() over row tiles: w.rt is the tile).  Single-thread roles keep
+    // the whole warp in the loop (lane 0 issues).
     if (warp == WARP_BLOAD) {
         // ---------------------------------------------------------- token tiles (B) -> stage ring
         uint32_t sc = 0, armed = 0, armed_par = 0;
         bool ok = true;
+        // L2 prefetch cursor over this CTA's (item, chunk) sequence, PF_CHUNKS chunks
+        // ahead of the loads
+        int pf_t = blockIdx.x, pf_c = 0;
+        const uint8_t *pf_src = nullptr;
+        auto pf_next = [&]() {  // prefetch one chunk and advance
+            if (pf_t >= total)
+                return;
+            if (pf_c == 0)
+                pf_src = tile_src(decompose(pf_t, prefix, a.grp_count, a.G, rt_n, NMAX));
+            if (lane == 0)
+                prefetch_l2(pf_src + (size_t)pf_c * a.chunk_bytes, (uint32_t)a.chunk_bytes);
+            if (++pf_c == a.kchunks) {
+                pf_c = 0;
+                pf_t += gridDim.x;
+            }
+        };
+        for (int i = 0; i < PF_CHUNKS; ++i)
+            pf_next();
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const WorkItem w = decompose(t, prefix, a.grp_count, a.G, pairs, NMAX);
+            const WorkItem w = decompose(t, prefix, a.grp_count, a.G, rt_n, NMAX);
             int row0;
             const CUtensorMap *m0 = &map_b;
-            if (GU && w.g >= a.E) {  // shared groups read x by token, routed groups gathered rows
+            if (GU && w.g >= a.E) {  // shared groups read the token rows by token, routed groups gathered rows
                 row0 = w.tok0;
                 m0 = &map_b2;
             } else {
@@ -244,20 +347,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // read, or zero fill past the tensor's last row)
             const int nbox = (w.n_mma + a.brows - 1) / a.brows;
             const int box_bytes = a.brows * HALF_K * 2;
-            const uint32_t bytes = (uint32_t)(nbox * box_bytes * NB);
+            const uint32_t bytes = (uint32_t)(nbox * box_bytes * 2);
             for (int st = 0; st < nstages; ++st, ++sc) {
                 const int slot = sc % S;
                 const uint32_t ph = (sc / S) & 1;
                 if (!(ok = mbar_wait_sleep_warp(&ab_empty[slot], ph ^ 1, abort_flag, a.err, lane)))
                     break;
+                if (KST == CHUNK_K || (st & 1) == 0)
+                    pf_next();
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&ab_full[slot], bytes);
-                    uint8_t *bdst = smem + slot * L::STAGE + L::A_STAGE;
+                    uint8_t *bdst = smem + slot * B_STAGE_BYTES;
+                    // the stage's two swizzled tiles: two 64-wide K slices of one plane,
+                    // or one slice of the h hi and lo planes
                     for (int b = 0; b < nbox; ++b) {
-                        tma_2d(bdst + b * box_bytes, m0, st * HALF_K, row0 + b * a.brows, &ab_full[slot]);
-                        if (!GU)
-                            tma_2d(bdst + NMAX * HALF_K * 2 + b * box_bytes, &map_b2, st * HALF_K,
-                                   row0 + b * a.brows, &ab_full[slot]);
+                        if (NB == 1) {
+                            tma_2d(bdst + b * box_bytes, m0, st * KST, row0 + b * a.brows, &ab_full[slot]);
+                            tma_2d(bdst + B_SLICE_BYTES + b * box_bytes, m0, st * KST + HALF_K, row0 + b * a.brows,
+                                   &ab_full[slot]);
+                        } else {
+                            tma_2d(bdst + b * box_bytes, m0, st * KST, row0 + b * a.brows, &ab_full[slot]);
+                            tma_2d(bdst + B_SLICE_BYTES + b * box_bytes, &map_b2, st * KST, row0 + b * a.brows,
+                                   &ab_full[slot]);
+                        }
                     }
                 }
                 armed |= 1u << slot;
@@ -273,36 +385,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
     } else if (warp == WARP_MMA) {
         // ---------------------------------------------------------- MMA issue (lane 0)
-        uint32_t sc = 0, tc = 0, last_acc = 0, last_par = 0;
-        const uint64_t desc0 = sw128_desc(smem_addr(smem));  // K-major SW128 descriptor of stage 0
+        uint32_t sc = 0, tc = 0;
+        const uint64_t desc0 = sw128_desc(smem_addr(smem));  // K-major SW128 descriptor of B stage 0
         bool issued = false, ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
-            const WorkItem w = decompose(t, prefix, a.grp_count, a.G, pairs, NMAX);
-            const bool two = 2 * w.rt + 1 < a.row_tiles;
-            const int buf = NBUF == 2 ? (tc & 1) : 0;
-            const uint32_t aph = (NBUF == 2 ? (tc >> 1) : tc) & 1;
-            if (!(ok = mbar_wait_sleep_warp(&acc_empty[buf], aph ^ 1, abort_flag, a.err, lane)))
+            const WorkItem w = decompose(t, prefix, a.grp_count, a.G, rt_n, NMAX);
+            if (!(ok = mbar_wait_warp(acc_empty, (tc & 1) ^ 1, abort_flag, a.err, lane)))
                 break;
             tc_fence_after();
-            const uint32_t d_tmem = tmem_base + (uint32_t)(buf * 2 * NMAX);
-            const uint32_t idesc = idesc_bf16(w.n_mma);
+            const uint32_t idesc = make_idesc<OP>(w.n_mma);
             for (int st = 0; st < nstages; ++st, ++sc) {
                 const int slot = sc % S;
-                if (!(ok = mbar_wait_sleep_warp(&ab_full[slot], (sc / S) & 1, abort_flag, a.err, lane)))
+                if (!(ok = mbar_wait_warp(&ab_full[slot], (sc / S) & 1, abort_flag, a.err, lane)))
                     break;
                 tc_fence_after();
                 if (lane == 0) {
                     // descriptors of this slot: base plus the slot's offset (address field = bytes >> 4)
-                    const uint64_t ad0 = desc0 + (uint64_t)((slot * L::STAGE) >> 4);
-                    const uint64_t bd0 = ad0 + (uint64_t)(L::A_STAGE >> 4);
-                    tc_mma4(d_tmem, ad0, bd0, idesc, st);
-                    if (!GU)
-                        tc_mma4(d_tmem, ad0, bd0 + (uint64_t)((NMAX * HALF_K * 2) >> 4), idesc, 1u);
-                    if (two) {
-                        const uint64_t ad1 = ad0 + (uint64_t)(A_STAGE_BYTES >> 4);
-                        tc_mma4(d_tmem + NMAX, ad1, bd0, idesc, st);
-                        if (!GU)
-                            tc_mma4(d_tmem + NMAX, ad1, bd0 + (uint64_t)((NMAX * HALF_K * 2) >> 4), idesc, 1u);
+                    const uint64_t bd = desc0 + (uint64_t)((slot * B_STAGE_BYTES) >> 4);
+                    const uint32_t at = tmem_base + (uint32_t)(TMEM_A0 + slot * A_SLOT_COLS);
+                    if (NB == 1) {
+#pragma unroll
+                        for (int sl = 0; sl < NSL; ++sl)
+                            tc_mma4(tmem_base, at + 32 * sl, bd + (uint64_t)((sl * B_SLICE_BYTES) >> 4), idesc,
+                                    st > 0 || sl > 0);
+                    } else {
+                        tc_mma4(tmem_base, at, bd, idesc, st);
+                        tc_mma4(tmem_base, at, bd + (uint64_t)(B_SLICE_BYTES >> 4), idesc, 1u);
                     }
                     tc_commit(&ab_empty[slot]);
                 }
@@ -312,190 +420,202 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!ok)
                 break;
             if (lane == 0)
-                tc_commit(&acc_full[buf]);
+                tc_commit(acc_full);
             __syncwarp();
-            last_acc = buf;
-            last_par = aph;
         }
         // drain: the MMAs of the last committed item have completed
-        if (lane == 0 && issued)
-            mbar_drain(&acc_full[last_acc], last_par);
+        if (lane == 0 && issued && tc > 0)
+            mbar_drain(acc_full, (tc - 1) & 1);
         __syncwarp();
     } else if (warp < WARP_EPI0) {
         // ---------------------------------------------------------- decoders
-        // Thread (r, blk, hf) owns row r of both row tiles and the 16 elements
-        // hf of the 32-wide block blk of every 64-wide stage.  It loads its raw
-        // codes and scale straight from global memory PD stages ahead (into
-        // registers), decodes the current stage into the swizzled A stage and
-        // arrives on ab_full once per warp.
-        const int dt = tid - WARP_DEC0 * 32;                     // 0..511
-        const int r = dt >> 2, blk = (dt >> 1) & 1, hf = dt & 1;  // tile row, block, half of the block
-        uint32_t soff[2];                                         // swizzled offsets of this thread's 2 x 16 bytes
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-            soff[c] = sw128_offset(r, blk * 4 + hf * 2 + c);
-        uint2 qc[PD][2][V];                    // raw codes (MXFP4: 8 bytes; BF16: 2 x 8... see V) per tile
-        uint4 qb[PD][2][V];                    // BF16 weights: 2 x 16 bytes per tile
-        uint32_t qs[PD][2];                    // E8M0 scale bytes (MXFP4)
-        (void)qc;
-        (void)qb;
-        // raw source of the stage PD ahead of the one being decoded; walked with
-        // counters (item, stage in item, chunk pointers) so that no division or
-        // schedule search runs per stage
-        int f_ii = 0, f_st = 0;                // next stage to fetch: item index, stage in item
-        const uint8_t *f_src[2] = {nullptr, nullptr};
+        // Group gi decodes every N_DEC_GROUPS-th stage (gs = gi, gi + 3, ...: ring
+        // slot gi) in full; its warp of lane quadrant q = warp % 4 decodes rows
+        // 32q..32q+31 (lane = row) of the item's row tile over the stage's KST
+        // values of K into the slot's columns of the tensor-memory A ring, so each
+        // warp pays the stage hand-off (wait, fences, arrive) once per three stages.  A lane
+        // loads its next stage's raw codes and scales straight from global
+        // memory (into registers) as soon as it has handed over the current one;
+        // the token loader has prefetched them into L2.
+        const int q = warp & 3;
+        const int gi = (warp - WARP_DEC0) >> 2;
+        const int r = 32 * q + lane;  // row inside the tile
+        const uint32_t tlane = (uint32_t)(32 * q) << 16;
         const int n_items = total > (int)blockIdx.x ? (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
-        auto set_item = [&](int ii) {
-            const WorkItem w = decompose(blockIdx.x + ii * gridDim.x, prefix, a.grp_count, a.G, pairs, NMAX);
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int rt = 2 * w.rt + j;
-                f_src[j] = rt < a.row_tiles
-                               ? a.wbase + (size_t)w.g * a.group_bytes + (size_t)rt * a.kchunks * (size_t)a.chunk_bytes
-                               : nullptr;
-            }
-        };
-        if (n_items > 0)
-            set_item(0);
-        auto fetch = [&](int k) {
-            if (f_ii >= n_items)
-                return;
-            const int h = f_st & 1;
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                if (!f_src[j])
-                    continue;
-                const uint8_t *ch = f_src[j];
-                if (WFMT == FMT_MXFP4) {
-                    qc[k][j][0] = __ldg(reinterpret_cast<const uint2 *>(ch + h * (CHUNK_MX_CODE_BYTES / 2) + r * 32 +
-                                                                        blk * 16 + hf * 8));
-                    qs[k][j] = __ldg(ch + CHUNK_MX_CODE_BYTES + r * 4 + h * 2 + blk);
-                } else {
-                    const uint4 *src =
-                        reinterpret_cast<const uint4 *>(ch + h * (CHUNK_BF16_BYTES / 2) + r * 128 + blk * 64 + hf * 32);
-#pragma unroll
-                    for (int v = 0; v < V; ++v)
-                        qb[k][j][v] = __ldg(src + v);
-                }
-            }
-            // advance: next half of the chunk, next chunk, or the next item
-            if (h == 1) {
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-                    if (f_src[j])
-                        f_src[j] += a.chunk_bytes;
-            }
-            if (++f_st == nstages) {
-                f_st = 0;
-                if (++f_ii < n_items)
-                    set_item(f_ii);
-            }
-        };
         const int total_st = n_items * nstages;
+        uint4 rc[NBLK];   // MXFP4: 16 code bytes per 32-value block
+        uint32_t re[NBLK], rb = 127;
+        const uint8_t *src = nullptr;  // the stage's chunk
+        int kh = 0;                    // 64-wide half of the chunk (stages of 64 values)
+        int cached_ii = -1;
+        const uint8_t *tile0 = nullptr;
+        uint32_t base_c = 127;
+        auto locate = [&](int gs) {
+            const int ii = gs / nstages, st = gs - ii * nstages;
+            if (ii != cached_ii) {
+                cached_ii = ii;
+                const WorkItem w = decompose(blockIdx.x + ii * gridDim.x, prefix, a.grp_count, a.G, rt_n, NMAX);
+                tile0 = tile_src(w);
+                if (OP == OP_F16)
+                    base_c = __ldg(a.row_base + (size_t)w.g * rb_stride + w.rt * TILE_ROWS + r);
+            }
+            src = tile0 + (size_t)(st * KST / CHUNK_K) * a.chunk_bytes;
+            kh = KST == CHUNK_K ? 0 : (st & 1);
+        };
+        auto fetch = [&](int gs) {  // MXFP4: the stage's codes and scales into registers
+            if (WFMT == FMT_BF16)
+                return;
+            locate(gs);
+            rb = base_c;
 #pragma unroll
-        for (int k = 0; k < PD; ++k)
-            fetch(k);
-        bool ok = true;
-        int c_st = 0, c_ii = 0;   // stage being decoded: stage in item, item
-        bool two = false;
-        if (n_items > 0) {
-            const WorkItem w = decompose(blockIdx.x, prefix, a.grp_count, a.G, pairs, NMAX);
-            two = 2 * w.rt + 1 < a.row_tiles;
-        }
-        for (int gs0 = 0; gs0 < total_st && ok; gs0 += PD) {
-#pragma unroll
-            for (int k = 0; k < PD; ++k) {
-                const int gs = gs0 + k;
-                if (gs >= total_st)
-                    break;
-                const int slot = gs % S;
-                if (!(ok = mbar_wait_sleep_warp(&ab_empty[slot], ((gs / S) & 1) ^ 1, abort_flag, a.err, lane)))
-                    break;
-                uint8_t *adst = smem + slot * L::STAGE;
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    if (j == 1 && !two)
-                        break;
-                    uint8_t *aj = adst + j * A_STAGE_BYTES;
-                    if (WFMT == FMT_MXFP4) {
-                        const uint32_t s2 = e8m0_to_bf16x2(qs[k][j]);
-                        const uint32_t words[2] = {qc[k][j][0].x, qc[k][j][0].y};
-#pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            uint32_t o[4];
-                            decode_word(words[c], s2, o);
-                            *reinterpret_cast<uint4 *>(aj + soff[c]) = make_uint4(o[0], o[1], o[2], o[3]);
-                        }
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 2; ++c)
-                            *reinterpret_cast<uint4 *>(aj + soff[c]) = qb[k][j][c];
-                    }
-                }
-                fence_proxy_async();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&ab_full[slot]);
-                fetch(k);
-                if (++c_st == nstages) {
-                    c_st = 0;
-                    if (++c_ii < n_items) {
-                        const WorkItem w =
-                            decompose(blockIdx.x + c_ii * gridDim.x, prefix, a.grp_count, a.G, pairs, NMAX);
-                        two = 2 * w.rt + 1 < a.row_tiles;
-                    }
+            for (int b = 0; b < NBLK; ++b) {
+                const int blk = NBLK == 4 ? b : 2 * kh + b;  // 32-value block of the chunk
+                if (OP == OP_F16) {
+                    // TILE_F16: 16 code bytes of (block, row r), then the E8M0 bytes
+                    rc[b] = __ldg(reinterpret_cast<const uint4 *>(src + (blk * TILE_ROWS + r) * 16));
+                    re[b] = __ldg(src + CHUNK_MX_CODE_BYTES + blk * TILE_ROWS + r);
+                } else {
+                    // TILE: repacked words of (half blk / 2, block blk % 2) of row r, then the scales
+                    rc[b] = __ldg(reinterpret_cast<const uint4 *>(src + (blk >> 1) * (CHUNK_MX_CODE_BYTES / 2) +
+                                                                  r * 32 + (blk & 1) * 16));
+                    re[b] = __ldg(src + CHUNK_MX_CODE_BYTES + r * 4 + blk);
                 }
             }
+        };
+        bool ok = true;
+        int gs = gi;
+        if (gs < total_st)
+            fetch(gs);
+        for (; gs < total_st && ok; gs += N_DEC_GROUPS) {
+            const int slot = gs % S;
+            if (!(ok = mbar_wait_warp(&ab_empty[slot], ((gs / S) & 1) ^ 1, abort_flag, a.err, lane)))
+                break;
+            tc_fence_after();
+            if (WFMT == FMT_BF16)
+                locate(gs);
+#pragma unroll
+            for (int b = 0; b < NBLK; ++b) {
+                uint32_t o[16];
+                if (WFMT == FMT_BF16) {
+                    // BF16 TILE: 64 values of half (k / 64) of row r
+                    const int k0 = (NBLK == 4 ? 0 : kh * HALF_K) + 32 * b;
+                    const uint4 *p = reinterpret_cast<const uint4 *>(src + (k0 >> 6) * (CHUNK_BF16_BYTES / 2) + r * 128 +
+                                                                     (k0 & 63) * 2);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const uint4 x4 = __ldg(p + v);
+                        o[4 * v] = x4.x;
+                        o[4 * v + 1] = x4.y;
+                        o[4 * v + 2] = x4.z;
+                        o[4 * v + 3] = x4.w;
+                    }
+                } else if (OP == OP_F16) {
+                    int d = (int)re[b] - (int)rb;
+                    d = d < -24 ? -24 : (d > 0 ? 0 : d);  // only blocks past K (code 0) fall outside [-23, 0]
+                    const uint32_t s2 = f16x2_pow2(d);
+                    e2m1x8_f16(rc[b].x, s2, o);
+                    e2m1x8_f16(rc[b].y, s2, o + 4);
+                    e2m1x8_f16(rc[b].z, s2, o + 8);
+                    e2m1x8_f16(rc[b].w, s2, o + 12);
+                } else {
+                    const uint32_t s2 = e8m0_to_bf16x2(re[b]);
+                    decode_word(rc[b].x, s2, o);
+                    decode_word(rc[b].y, s2, o + 4);
+                    decode_word(rc[b].z, s2, o + 8);
+                    decode_word(rc[b].w, s2, o + 12);
+                }
+                tmem_st16(tmem_base + tlane + (uint32_t)(TMEM_A0 + slot * A_SLOT_COLS + b * 16), o);
+            }
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&ab_full[slot]);
+            if (gs + N_DEC_GROUPS < total_st)
+                fetch(gs + N_DEC_GROUPS);
         }
     } else {
         // ---------------------------------------------------------- epilogue
-        const int q = warp & 3;                        // TMEM lane quadrant of this warp
-        const int eh = (warp - WARP_EPI0) >> 2;         // which column chunks of the quadrant it takes
-        // columns per TMEM wait: gate|up (whose epilogue the MMAs wait for) 32, down 16
+        const int q = warp & 3;                   // tensor-memory lane quadrant of this warp
+        const int eh = (warp - WARP_EPI0) >> 2;   // which column chunks of the quadrant it takes
+        // this warp's column scales (FP16 operands), indexed by column
+        float *csc = reinterpret_cast<float *>(smem + L::COLSC_OFF) + (warp - WARP_EPI0) * NMAX;
+        // columns per tensor-memory wait: gate|up 32, down 16
         constexpr int EC = GU ? 32 : 16;
         uint32_t tc = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
-            const WorkItem w = decompose(t, prefix, a.grp_count, a.G, pairs, NMAX);
-            const int buf = NBUF == 2 ? (tc & 1) : 0;
-            const uint32_t aph = (NBUF == 2 ? (tc >> 1) : tc) & 1;
-            if (!mbar_wait_sleep_warp(&acc_full[buf], aph, abort_flag, a.err, lane))
+            const WorkItem w = decompose(t, prefix, a.grp_count, a.G, rt_n, NMAX);
+            const int pos0 = a.grp_start[w.g] + w.tok0;
+            // FP16 operands: the power of two of each of this warp's columns' token row
+            // (gate|up) or h row (down), staged in shared memory while the item's MMAs
+            // still run
+            if (OP == OP_F16) {
+#pragma unroll 1
+                for (int i = 0; i < NMAX / (2 * EC); ++i)
+                    for (int c = EC * eh + 2 * EC * i + lane; c < EC * eh + 2 * EC * i + EC && c < w.nvalid; c += 32)
+                        csc[c] = pow2i(__ldg((GU ? a.xsp : a.hsp) + pos0 + c));
+                __syncwarp();
+            }
+            if (!mbar_wait_sleep_warp(acc_full, tc & 1, abort_flag, a.err, lane))
                 break;
             tc_fence_after();
-            const int pos0 = a.grp_start[w.g] + w.tok0;
+            const int rt = w.rt;
+            const int row = 32 * q + lane;
+            const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16);
+            // FP16 operands: this row's weight scale 2^(b - 127) (exact; a subnormal for b = 0)
+            const float wsc = OP == OP_F16
+                                  ? ldexpf(1.0f, (int)__ldg(a.row_base + (size_t)w.g * rb_stride + rt * TILE_ROWS + row) - 127)
+                                  : 1.0f;
+            // column groups of this warp: EC columns at c0 = EC * eh + 2 * EC * i
+            constexpr int NG = NMAX / (2 * EC);
 #pragma unroll 1
-            for (int j = 0; j < 2; ++j) {
-                const int rt = 2 * w.rt + j;
-                if (rt >= a.row_tiles)
+            for (int i = 0; i < NG; ++i) {
+                const int c0 = EC * eh + 2 * EC * i;
+                if (c0 >= w.n_mma)
                     break;
-                const uint32_t taddr =
-                    tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 2 * NMAX + j * NMAX);
-                for (int c0 = EC * eh; c0 < w.n_mma; c0 += 2 * EC) {
-                    // EC columns per wait (a second load may lie past n_mma, inside the
-                    // accumulator, and is then ignored)
-                    float v2[EC];
-                    if constexpr (EC == 32)
-                        tmem_ld32(taddr + c0, v2);
-                    else
-                        tmem_ld16(taddr + c0, v2);
+                // EC columns per wait (a second load may lie past n_mma, inside the
+                // accumulator, and is then ignored)
+                float v2[EC];
+                if constexpr (EC == 32)
+                    tmem_ld32(taddr + c0, v2);
+                else
+                    tmem_ld16(taddr + c0, v2);
 #pragma unroll
-                    for (int half = 0; half < EC / 16; ++half) {
+                for (int half = 0; half < EC / 16; ++half) {
                     const int c1 = c0 + 16 * half;
                     if (c1 >= w.n_mma)
                         break;
                     const float *v = v2 + 16 * half;
                     if (GU) {
                         // rows 16*gr + i: gate of feature 8*gr + i%8 when i < 8, up when i >= 8;
-                        // the gate lane finishes tokens c0..c0+7, its up partner (lane ^ 8) c0+8..c0+15
-                        const int n = gu_row_feature(rt, 32 * q + lane);
+                        // the gate lane finishes tokens c1..c1+7, its up partner (lane ^ 8) c1+8..c1+15
+                        const int n = gu_row_feature(rt, row);
                         const bool up_lane = gu_row_is_up(lane);
 #pragma unroll
                         for (int jj = 0; jj < 8; ++jj) {
-                            const float send = up_lane ? v[jj] : v[8 + jj];
+                            const float send = (up_lane ? v[jj] : v[8 + jj]) * wsc;
                             const float recv = __shfl_xor_sync(0xffffffffu, send, 8);
-                            const float gv = up_lane ? recv : v[jj];
-                            const float uv = up_lane ? v[8 + jj] : recv;
+                            float gv = up_lane ? recv : v[jj] * wsc;
+                            float uv = up_lane ? v[8 + jj] * wsc : recv;
                             const int tok = c1 + (up_lane ? 8 : 0) + jj;
-                            if (tok < w.nvalid && n < a.I) {
+                            const bool valid = tok < w.nvalid && n < a.I;
+                            if (OP == OP_F16) {
+                                // undo the token row's power of two, then FP32 h and the
+                                // position's running maximum of |h|
+                                const float fx = tok < w.nvalid ? csc[tok] : 0.f;
+                                gv *= fx;
+                                uv *= fx;
+                                const float hv = valid ? __fdividef(gv, 1.0f + __expf(-gv)) * uv : 0.f;
+                                if (valid)
+                                    a.h32[(size_t)(pos0 + tok) * a.I + n] = hv;
+                                float m = fabsf(hv);
+                                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                                if ((lane & 23) == 0 && tok < w.nvalid && m > 0.f)
+                                    atomicMax(a.hmax + pos0 + tok, __float_as_int(m));
+                            } else if (valid) {
                                 const float hv = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
                                 const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
                                 const __nv_bfloat16 lb = __float2bfloat16_rn(hv - __bfloat162float(hb));
@@ -505,21 +625,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             }
                         }
                     } else {
-                        const int m = rt * TILE_ROWS + 32 * q + lane;
-                        if (m < a.H) {
+                        const int m = rt * TILE_ROWS + row;
 #pragma unroll
-                            for (int jj = 0; jj < 16; ++jj)
-                                if (c1 + jj < w.nvalid)
-                                    a.y_out[(size_t)(pos0 + c1 + jj) * a.H + m] = v[jj];
+                        for (int jj = 0; jj < 16; ++jj) {
+                            if (m < a.H && c1 + jj < w.nvalid)
+                                a.y_out[(size_t)(pos0 + c1 + jj) * a.H + m] =
+                                    OP == OP_F16 ? v[jj] * wsc * csc[c1 + jj] : v[jj];
                         }
-                    }
                     }
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(&acc_empty[buf]);
+                mbar_arrive(acc_empty);
         }
     }
 
@@ -534,12 +653,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // ------------------------------------------------------------------ host side
 
-template <bool GU, int WFMT, int NMAX, int S>
+template <bool GU, int OP, int WFMT>
 cudaError_t launch_cfg(const TcArgs &a, const CUtensorMap &m1, const CUtensorMap &m2, cudaStream_t st)
 {
-    constexpr int NB = GU ? 1 : 2;
-    constexpr int SMEM = Smem<NMAX, NB, S>::TOTAL;
-    auto kern = gemm_tc_kernel<GU, WFMT, NMAX, S>;
+    constexpr int SMEM = Smem::TOTAL;
+    auto kern = gemm_tc_kernel<GU, OP, WFMT>;
     static std::atomic<int> attr_set[MAX_DEVICES];
     cudaError_t e = smem_limit_once(attr_set, (const void *)kern, SMEM);
     if (e != cudaSuccess)
@@ -548,37 +666,48 @@ cudaError_t launch_cfg(const TcArgs &a, const CUtensorMap &m1, const CUtensorMap
     return cudaGetLastError();
 }
 
-// token tile sizes: small batches use a small tile (more stages in flight),
-// larger batches the full tile.
-constexpr int SMALL_T = 64;
-
 template <bool GU>
-cudaError_t launch_any(const TcArgs &a, int fmt, int T, const CUtensorMap &m1, const CUtensorMap &m2,
+cudaError_t launch_any(const TcArgs &a, int fmt, bool f16, const CUtensorMap &m1, const CUtensorMap &m2,
                        cudaStream_t st)
 {
-    const bool small = T <= SMALL_T;
-    if constexpr (GU) {
-        if (fmt == FMT_MXFP4)
-            return small ? launch_cfg<true, FMT_MXFP4, 64, 4>(a, m1, m2, st)
-                         : launch_cfg<true, FMT_MXFP4, 256, 3>(a, m1, m2, st);
-        return small ? launch_cfg<true, FMT_BF16, 64, 4>(a, m1, m2, st)
-                     : launch_cfg<true, FMT_BF16, 256, 3>(a, m1, m2, st);
-    } else {
-        if (fmt == FMT_MXFP4)
-            return small ? launch_cfg<false, FMT_MXFP4, 64, 4>(a, m1, m2, st)
-                         : launch_cfg<false, FMT_MXFP4, 128, 3>(a, m1, m2, st);
-        return small ? launch_cfg<false, FMT_BF16, 64, 4>(a, m1, m2, st)
-                     : launch_cfg<false, FMT_BF16, 128, 3>(a, m1, m2, st);
-    }
+    if (f16)
+        return fmt == FMT_MXFP4 ? launch_cfg<GU, OP_F16, FMT_MXFP4>(a, m1, m2, st) : cudaErrorInvalidValue;
+    return fmt == FMT_MXFP4 ? launch_cfg<GU, OP_BF16, FMT_MXFP4>(a, m1, m2, st)
+                            : launch_cfg<GU, OP_BF16, FMT_BF16>(a, m1, m2, st);
+}
+
+TcArgs base_args(const Plan &p, const WeightStore &w)
+{
+    TcArgs a{};
+    a.wbase = w.base;
+    a.group_bytes = w.group_bytes;
+    a.kchunks = w.kchunks;
+    a.chunk_bytes = w.chunk_bytes;
+    a.row_tiles = w.row_tiles;
+    a.row_base = w.row_base;
+    a.grp_start = p.grp_start;
+    a.grp_count = p.grp_count;
+    a.E = p.E;
+    a.G = p.G;
+    a.I = p.I;
+    a.H = p.H;
+    a.row_token = p.row_token;
+    a.err = p.err;
+    return a;
 }
 
 }  // namespace
 
-// x_perm[p] = x[row_token[p]] for the routed positions p < T*k (16-byte copies).
+// x_perm[p] = x[row_token[p]] for the routed positions p < T*k (16-byte copies);
+// with token scales xs given, also xsp[p] = xs[row_token[p]].
 __global__ void gather_rows_kernel(const uint4 *__restrict__ x, const int *__restrict__ row_token, int n_rows,
-                                   int row_vecs, uint4 *__restrict__ out)
+                                   int row_vecs, uint4 *__restrict__ out, const int *__restrict__ xs,
+                                   int *__restrict__ xsp)
 {
     long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (xs)
+        for (long long p = i; p < n_rows; p += (long long)gridDim.x * blockDim.x)
+            xsp[p] = xs[row_token[p]];
     long long total = (long long)n_rows * row_vecs;
     for (; i < total; i += (long long)gridDim.x * blockDim.x) {
         const long long p = i / row_vecs, c = i % row_vecs;
@@ -586,7 +715,7 @@ __global__ void gather_rows_kernel(const uint4 *__restrict__ x, const int *__res
     }
 }
 
-cudaError_t launch_gather_rows(const Plan &p, const uint16_t *x, cudaStream_t st)
+cudaError_t launch_gather_rows(const Plan &p, const uint16_t *x, bool xs_rows, cudaStream_t st)
 {
     const int n = p.T * p.k;
     if (n == 0)
@@ -597,18 +726,117 @@ cudaError_t launch_gather_rows(const Plan &p, const uint16_t *x, cudaStream_t st
     if (blocks > 4 * 152 * 8)
         blocks = 4 * 152 * 8;
     gather_rows_kernel<<<(unsigned)blocks, 256, 0, st>>>(reinterpret_cast<const uint4 *>(x), p.row_token, n, row_vecs,
-                                                         reinterpret_cast<uint4 *>(p.x_perm));
+                                                         reinterpret_cast<uint4 *>(p.x_perm), xs_rows ? p.xs : nullptr,
+                                                         p.xsp);
     return cudaGetLastError();
 }
 
-cudaError_t launch_gemm_gate_up_tc(const Plan &p, const WeightStore &w, int fmt, const uint16_t *x, cudaStream_t st)
+// FP16 token rows: xs[t] = floor(log2 max|x_t|) - 14 (0 for an all-zero row,
+// clamped to [-100, 100]) and x16[t] = x_t * 2^-xs[t] in FP16, natural K
+// order.  The largest |x| of a token lands in [2^14, 2^15); a BF16 value has 8
+// significant bits, so the conversion is exact for every element within 2^31
+// of the token's largest.  One CTA per token.
+__global__ void token_prep_f16_kernel(const uint16_t *__restrict__ x, int H, uint16_t *__restrict__ x16,
+                                      int *__restrict__ xs, int *__restrict__ xsp, int n_routed, int T, int S)
 {
-    TcArgs a{w.base, w.group_bytes, w.kchunks, w.chunk_bytes, w.row_tiles, p.grp_start, p.grp_count, p.E, p.G,
-             p.I, p.H, p.h, (long long)p.P * p.I, nullptr, p.err};
+    __shared__ uint32_t red[32];
+    const int t = blockIdx.x;
+    const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
+    const int nv = H / 8;
+    uint32_t mx = 0;  // max |x| as BF16 bits without sign (monotonic for finite values)
+    for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+        const uint4 v = row[i];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            mx = max(mx, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
+    }
+    for (int o = 16; o > 0; o >>= 1)
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    mx = 0;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i)
+        mx = max(mx, red[i]);
+    int sc = mx == 0 ? 0 : (int)(mx >> 7) - 127 - 14;
+    sc = sc < -100 ? -100 : (sc > 100 ? 100 : sc);
+    if (threadIdx.x == 0)
+        xs[t] = sc;
+    for (int s = threadIdx.x; s < S; s += blockDim.x)  // shared groups / dense slices: position n + s*T + t
+        xsp[(size_t)n_routed + (size_t)s * T + t] = sc;
+    const float mul = __int_as_float((127 - sc) << 23);
+    uint4 *dst = reinterpret_cast<uint4 *>(x16 + (size_t)t * H);
+    for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+        const uint4 v = row[i];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __half lo = __float2half_rn(__uint_as_float(w[j] << 16) * mul);
+            const __half hi = __float2half_rn(__uint_as_float(w[j] & 0xFFFF0000u) * mul);
+            o[j] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+        }
+        dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// One FP16 plane of h with a power of two per position: hsp[p] =
+// floor(log2 max_n |h_pn|) - 14 (0 when the row is zero), h16[p][n] =
+// h32[p][n] * 2^-hsp[p].  One warp per position.
+__global__ void h_convert_kernel(const float *__restrict__ h32, const int *__restrict__ hmax, int P, int I,
+                                 uint16_t *__restrict__ h16, int *__restrict__ hsp)
+{
+    const int p = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (p >= P)
+        return;
+    const float m = __int_as_float(hmax[p]);
+    int sc = m > 0.f ? (int)((__float_as_uint(m) >> 23) & 0xFFu) - 127 - 14 : 0;
+    sc = sc < -100 ? -100 : (sc > 100 ? 100 : sc);
+    if (lane == 0)
+        hsp[p] = sc;
+    const float mul = __int_as_float((127 - sc) << 23);
+    const float4 *src = reinterpret_cast<const float4 *>(h32 + (size_t)p * I);
+    uint2 *dst = reinterpret_cast<uint2 *>(h16 + (size_t)p * I);
+    for (int i = lane; i < I / 4; i += 32) {
+        const float4 v = src[i];
+        const __half2 a = __floats2half2_rn(v.x * mul, v.y * mul);
+        const __half2 b = __floats2half2_rn(v.z * mul, v.w * mul);
+        dst[i] = make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&b));
+    }
+}
+
+cudaError_t launch_token_prep_f16(const Plan &p, const uint16_t *x, cudaStream_t st)
+{
+    if (p.T == 0)
+        return cudaSuccess;
+    token_prep_f16_kernel<<<p.T, 256, 0, st>>>(x, p.H, p.x16, p.xs, p.xsp, p.T * p.k, p.T, p.S);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_h_convert(const Plan &p, cudaStream_t st)
+{
+    if (p.P == 0)
+        return cudaSuccess;
+    h_convert_kernel<<<(unsigned)((p.P + 7) / 8), 256, 0, st>>>(reinterpret_cast<const float *>(p.h), p.hmax, p.P,
+                                                               p.I, p.h16, p.hsp);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_gate_up_tc(const Plan &p, const WeightStore &w, int fmt, bool f16, const uint16_t *x_rows,
+                                   cudaStream_t st)
+{
+    TcArgs a = base_args(p, w);
+    a.h_out = p.h;
+    a.h_plane = (long long)p.P * p.I;
+    a.h32 = reinterpret_cast<float *>(p.h);
+    a.hmax = p.hmax;
+    a.xsp = p.xsp;
     a.brows = p.T >= B_BOX_ROWS_BIG && (p.T * p.k == 0 || p.T * p.k >= B_BOX_ROWS_BIG) ? B_BOX_ROWS_BIG
                                                                                        : B_BOX_ROWS_SMALL;
     CUtensorMap m1, m2;
-    cudaError_t e = make_map(&m2, x, p.T, p.H, a.brows);
+    cudaError_t e = make_map(&m2, x_rows, p.T, p.H, a.brows);
     if (e != cudaSuccess)
         return e;
     if (p.T * p.k > 0) {
@@ -617,21 +845,28 @@ cudaError_t launch_gemm_gate_up_tc(const Plan &p, const WeightStore &w, int fmt,
     } else {
         m1 = m2;
     }
-    return launch_any<true>(a, fmt, p.T, m1, m2, st);
+    return launch_any<true>(a, fmt, f16, m1, m2, st);
 }
 
-cudaError_t launch_gemm_down_tc(const Plan &p, const WeightStore &w, int fmt, cudaStream_t st)
+cudaError_t launch_gemm_down_tc(const Plan &p, const WeightStore &w, int fmt, bool f16, cudaStream_t st)
 {
-    TcArgs a{w.base, w.group_bytes, w.kchunks, w.chunk_bytes, w.row_tiles, p.grp_start, p.grp_count, p.E, p.G,
-             p.I, p.H, nullptr, 0, p.y, p.err};
+    TcArgs a = base_args(p, w);
+    a.y_out = p.y;
+    a.hsp = p.hsp;
     a.brows = p.P >= B_BOX_ROWS_BIG ? B_BOX_ROWS_BIG : B_BOX_ROWS_SMALL;
     CUtensorMap m1, m2;
-    cudaError_t e = make_map(&m1, p.h, p.P, p.I, a.brows);
-    if (e != cudaSuccess)
-        return e;
-    if ((e = make_map(&m2, p.h + (size_t)p.P * p.I, p.P, p.I, a.brows)) != cudaSuccess)
-        return e;
-    return launch_any<false>(a, fmt, p.T, m1, m2, st);
+    cudaError_t e;
+    if (f16) {
+        if ((e = make_map(&m1, p.h16, p.P, p.I, a.brows)) != cudaSuccess)
+            return e;
+        m2 = m1;
+    } else {
+        if ((e = make_map(&m1, p.h, p.P, p.I, a.brows)) != cudaSuccess)
+            return e;
+        if ((e = make_map(&m2, p.h + (size_t)p.P * p.I, p.P, p.I, a.brows)) != cudaSuccess)
+            return e;
+    }
+    return launch_any<false>(a, fmt, f16, m1, m2, st);
 }
 
 }  // namespace moe

@@ -223,6 +223,72 @@ __global__ void repack_frag_f16_kernel(int fmt, int gate_up, SrcMat gate, SrcMat
     }
 }
 
+// TILE_F16 layout (MXFP4 only; see moe_internal.cuh): one thread builds one
+// row of one chunk -- plain pack4 code bytes per 32-value block and the raw
+// E8M0 bytes (127 past K, whose codes are 0).
+__global__ void repack_tile_f16_kernel(int gate_up, SrcMat gate, SrcMat up, uint8_t *dst, int row_tiles, int kchunks,
+                                       int chunk_bytes, int logical_rows, int K, int *bad_scale)
+{
+    long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long long)row_tiles * kchunks * TILE_ROWS)
+        return;
+    const int r = (int)(idx % TILE_ROWS);
+    const long long tk = idx / TILE_ROWS;
+    const int kc = (int)(tk % kchunks), tile = (int)(tk / kchunks);
+    int srow;
+    const SrcMat *src = tile_row_source(gate_up, &gate, &up, tile, r, logical_rows, &srow);
+    uint8_t *chunk = dst + ((long long)tile * kchunks + kc) * chunk_bytes;
+    const int k0 = kc * CHUNK_K;
+    for (int b = 0; b < CHUNK_K / 32; ++b) {
+        uint32_t words[4];
+        for (int c = 0; c < 4; ++c) {
+            uint32_t wv = 0;
+            for (int i = 0; i < 8; ++i)
+                wv |= src_code(src, srow, k0 + 32 * b + 8 * c + i, K) << (4 * i);
+            words[c] = wv;
+        }
+        *reinterpret_cast<uint4 *>(chunk + (b * TILE_ROWS + r) * 16) = make_uint4(words[0], words[1], words[2], words[3]);
+        chunk[CHUNK_MX_CODE_BYTES + b * TILE_ROWS + r] = src_scale(src, srow, k0 + 32 * b, K, bad_scale);
+    }
+}
+
+// Row bases of a TILE_F16 store: one thread per tile row; rows past the
+// logical end get 127 (their codes are 0).
+__global__ void row_base_kernel(int gate_up, SrcMat gate, SrcMat up, uint8_t *dst, int row_tiles, int logical_rows,
+                                int K, int *wide)
+{
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long long)row_tiles * TILE_ROWS)
+        return;
+    const int r = (int)(idx % TILE_ROWS), tile = (int)(idx / TILE_ROWS);
+    int srow;
+    const SrcMat *src = tile_row_source(gate_up, &gate, &up, tile, r, logical_rows, &srow);
+    if (srow < 0) {
+        dst[idx] = 127;
+        return;
+    }
+    const uint8_t *sc = src->scales + srow * src->scale_stride;
+    int mx = 0, mn = 255;
+    for (int b = 0; b < K / 32; ++b) {
+        const int e = sc[b];
+        mx = e > mx ? e : mx;
+        mn = e < mn ? e : mn;
+    }
+    dst[idx] = (uint8_t)mx;
+    if (mx - mn > TILE_F16_MAX_SPREAD)
+        atomicOr(wide, 1);
+}
+
+cudaError_t launch_row_base(bool gate_up, const SrcMat &gate, const SrcMat &up, const WeightStore &ws, int group,
+                            int I, int H, int *wide, cudaStream_t st)
+{
+    const int logical_rows = gate_up ? I : H;
+    const long long total = (long long)ws.row_tiles * TILE_ROWS;
+    row_base_kernel<<<(unsigned)((total + 127) / 128), 128, 0, st>>>(
+        gate_up ? 1 : 0, gate, up, ws.row_base + (size_t)group * total, ws.row_tiles, logical_rows, ws.cols, wide);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_repack(int fmt, int layout, bool gate_up, const SrcMat &gate, const SrcMat &up,
                           const WeightStore &ws, int group, int I, int H, int *bad_scale, cudaStream_t st)
 {
@@ -231,6 +297,14 @@ cudaError_t launch_repack(int fmt, int layout, bool gate_up, const SrcMat &gate,
         const long long total = (long long)ws.row_tiles * ws.kchunks * 256;
         repack_frag_f16_kernel<<<(unsigned)((total + 127) / 128), 128, 0, st>>>(
             fmt, gate_up ? 1 : 0, gate, up, ws.base + (size_t)group * ws.group_bytes, ws.row_tiles, ws.kchunks,
+            ws.chunk_bytes, logical_rows, ws.cols, bad_scale);
+        return cudaGetLastError();
+    }
+    if (layout == LAYOUT_TILE_F16) {
+        const int logical_rows = gate_up ? I : H;
+        const long long total = (long long)ws.row_tiles * ws.kchunks * TILE_ROWS;
+        repack_tile_f16_kernel<<<(unsigned)((total + 127) / 128), 128, 0, st>>>(
+            gate_up ? 1 : 0, gate, up, ws.base + (size_t)group * ws.group_bytes, ws.row_tiles, ws.kchunks,
             ws.chunk_bytes, logical_rows, ws.cols, bad_scale);
         return cudaGetLastError();
     }

@@ -23,7 +23,8 @@ struct MoeHandle {
     int fmt = 0;
     int k_max = 0;
     int device = 0;
-    WeightStore gu, dn;        // TILE layout (tensor-memory GEMMs, large batches)
+    WeightStore gu, dn;        // TILE or TILE_F16 layout (tensor-memory GEMMs, large batches)
+    bool tc_f16 = false;       // the tensor-memory GEMMs run FP16 operands (TILE_F16 store with row bases)
     WeightStore gu_f, dn_f;    // FRAG layout (register-streaming GEMMs, decode-sized batches)
     int *err_host = nullptr;   // mapped pinned host memory, written by kernels on device-side errors
     int *err_dev = nullptr;    // device alias of err_host
@@ -105,6 +106,10 @@ size_t plan_layout(const MoeHandle *h, int T, int k, char *base, Plan *p)
     q.hs_pitch = ((I + 63) / 64 + 3) & ~3;
     q.hs = (int *)take(sizeof(int) * (size_t)P * q.hs_pitch);
     q.h = (uint16_t *)take(2 * sizeof(uint16_t) * (size_t)P * I);
+    q.h16 = (uint16_t *)take(sizeof(uint16_t) * (size_t)P * I);
+    q.hmax = (int *)take(sizeof(int) * (size_t)P);
+    q.hsp = (int *)take(sizeof(int) * (size_t)P);
+    q.xsp = (int *)take(sizeof(int) * (size_t)P);
     q.y = (float *)take(sizeof(float) * (size_t)P * H);
     q.sync = (int *)take(layer_stream_sync_bytes(G));
     q.err = h->err_dev;
@@ -181,14 +186,35 @@ MoeStatus run_layer(MoeHandle *h, const void *x, const float *logits, const int 
         if ((e = launch_dense_plan(p, st)) != cudaSuccess)
             return cuda_fail(e, "dense plan launch");
     }
-    mark(2);
-    if ((e = launch_gather_rows(p, (const uint16_t *)x, st)) != cudaSuccess)
-        return cuda_fail(e, "gather launch");
-    if ((e = launch_gemm_gate_up_tc(p, h->gu, h->fmt, (const uint16_t *)x, st)) != cudaSuccess)
-        return cuda_fail(e, "gate/up launch");
-    mark(3);
-    if ((e = launch_gemm_down_tc(p, h->dn, h->fmt, st)) != cudaSuccess)
-        return cuda_fail(e, "down launch");
+    const uint16_t *xb = (const uint16_t *)x;
+    if (h->tc_f16) {
+        // FP16 operands: FP16 token rows with a power of two per token, gathered
+        // into position order; h as FP32 with per-position maxima, then one FP16
+        // plane with a power of two per position
+        if ((e = launch_token_prep_f16(p, xb, st)) != cudaSuccess)
+            return cuda_fail(e, "token prep launch");
+        if ((e = launch_gather_rows(p, p.x16, true, st)) != cudaSuccess)
+            return cuda_fail(e, "gather launch");
+        mark(2);
+        if ((e = cudaMemsetAsync(p.hmax, 0, sizeof(int) * (size_t)p.P, st)) != cudaSuccess)
+            return cuda_fail(e, "h maxima clear");
+        if ((e = launch_gemm_gate_up_tc(p, h->gu, h->fmt, true, p.x16, st)) != cudaSuccess)
+            return cuda_fail(e, "gate/up launch");
+        if ((e = launch_h_convert(p, st)) != cudaSuccess)
+            return cuda_fail(e, "h conversion launch");
+        mark(3);
+        if ((e = launch_gemm_down_tc(p, h->dn, h->fmt, true, st)) != cudaSuccess)
+            return cuda_fail(e, "down launch");
+    } else {
+        if ((e = launch_gather_rows(p, xb, false, st)) != cudaSuccess)
+            return cuda_fail(e, "gather launch");
+        mark(2);
+        if ((e = launch_gemm_gate_up_tc(p, h->gu, h->fmt, false, xb, st)) != cudaSuccess)
+            return cuda_fail(e, "gate/up launch");
+        mark(3);
+        if ((e = launch_gemm_down_tc(p, h->dn, h->fmt, false, st)) != cudaSuccess)
+            return cuda_fail(e, "down launch");
+    }
     mark(4);
     if ((e = launch_combine(p, out, accumulate, st)) != cudaSuccess)
         return cuda_fail(e, "combine launch");
@@ -207,6 +233,10 @@ void destroy(MoeHandle *h)
         cudaFree(h->gu.base);
     if (h->dn.base)
         cudaFree(h->dn.base);
+    if (h->gu.row_base)
+        cudaFree(h->gu.row_base);
+    if (h->dn.row_base)
+        cudaFree(h->dn.row_base);
     if (h->gu_f.base)
         cudaFree(h->gu_f.base);
     if (h->dn_f.base)
@@ -308,12 +338,14 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
     const int f_layout = nib ? LAYOUT_FRAG_F16 : LAYOUT_FRAG;
     // INT4 runs on the single kernel only, which reads the FRAG copy
     const bool tile = fmt != FMT_INT4;
-    if ((e = cudaHostAlloc((void **)&h->err_host, 2 * sizeof(int), cudaHostAllocMapped)) != cudaSuccess) {
+    // [0] device error flag, [1] a rejected scale at load, [2] an MXFP4 row whose
+    // exponents span too widely for FP16 operands
+    if ((e = cudaHostAlloc((void **)&h->err_host, 4 * sizeof(int), cudaHostAllocMapped)) != cudaSuccess) {
         destroy(h);
         return cuda_fail(e, "cudaHostAlloc");
     }
-    h->err_host[0] = 0;
-    h->err_host[1] = 0;
+    for (int i = 0; i < 4; ++i)
+        h->err_host[i] = 0;
     if ((e = cudaHostGetDevicePointer((void **)&h->err_dev, h->err_host, 0)) != cudaSuccess) {
         destroy(h);
         return cuda_fail(e, "cudaHostGetDevicePointer");
@@ -336,8 +368,8 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
     auto zp_at = [&](const void *p, long long elems) -> const uint8_t * {
         return fmt == FMT_INT4 && p ? (const uint8_t *)p + elems : nullptr;
     };
-    for (int g = 0; g < G; ++g) {
-        SrcMat gate{}, up{}, dn{};
+    // source matrices of group g: gate and up rows of gate|up, and down
+    auto sources = [&](int g, SrcMat &gate, SrcMat &up, SrcMat &dn) {
         const long long gs = nib ? c.hidden / 2 : (long long)c.hidden * 2;  // code bytes of a gate|up row
         const long long ss = c.hidden / 32;                                  // scales of a gate|up row
         if (dense) {
@@ -361,9 +393,47 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
             dn = {(const uint8_t *)down[g].codes, sc_at(down[g].scales, 0), dstride, I / 32,
                   zp_at(down[g].zeros, 0)};
         }
-        if ((tile && (e = launch_repack(fmt, LAYOUT_TILE, true, gate, up, h->gu, g, I, c.hidden, bad_scale, st)) !=
+    };
+    // MXFP4 on the tensor-memory GEMMs: FP16 operands when every row's block
+    // exponents span at most TILE_F16_MAX_SPREAD (checked on the device, one
+    // pass over the scales), else BF16 operands
+    int tile_layout = LAYOUT_TILE;
+    if (tile && fmt == FMT_MXFP4) {
+        const size_t gu_rb = (size_t)h->gu.row_tiles * TILE_ROWS * G, dn_rb = (size_t)h->dn.row_tiles * TILE_ROWS * G;
+        if (cudaMalloc(&h->gu.row_base, gu_rb) != cudaSuccess || cudaMalloc(&h->dn.row_base, dn_rb) != cudaSuccess) {
+            cudaGetLastError();
+            destroy(h);
+            return fail(MOE_ENOMEM, "device allocation of %zu bytes of row bases failed", gu_rb + dn_rb);
+        }
+        int *wide = &h->err_dev[2];
+        for (int g = 0; g < G; ++g) {
+            SrcMat gate{}, up{}, dn{};
+            sources(g, gate, up, dn);
+            if ((e = launch_row_base(true, gate, up, h->gu, g, I, c.hidden, wide, st)) != cudaSuccess ||
+                (e = launch_row_base(false, dn, dn, h->dn, g, I, c.hidden, wide, st)) != cudaSuccess) {
+                destroy(h);
+                return cuda_fail(e, "row base launch");
+            }
+        }
+        if ((e = cudaStreamSynchronize(st)) != cudaSuccess) {
+            destroy(h);
+            return cuda_fail(e, "row bases");
+        }
+        if (*(volatile int *)wide == 0) {
+            tile_layout = LAYOUT_TILE_F16;
+            h->tc_f16 = true;
+        } else {
+            cudaFree(h->gu.row_base);
+            cudaFree(h->dn.row_base);
+            h->gu.row_base = h->dn.row_base = nullptr;
+        }
+    }
+    for (int g = 0; g < G; ++g) {
+        SrcMat gate{}, up{}, dn{};
+        sources(g, gate, up, dn);
+        if ((tile && (e = launch_repack(fmt, tile_layout, true, gate, up, h->gu, g, I, c.hidden, bad_scale, st)) !=
                          cudaSuccess) ||
-            (tile && (e = launch_repack(fmt, LAYOUT_TILE, false, dn, dn, h->dn, g, I, c.hidden, bad_scale, st)) !=
+            (tile && (e = launch_repack(fmt, tile_layout, false, dn, dn, h->dn, g, I, c.hidden, bad_scale, st)) !=
                          cudaSuccess) ||
             (e = launch_repack(fmt, f_layout, true, gate, up, h->gu_f, g, I, c.hidden, bad_scale, st)) !=
                 cudaSuccess ||

@@ -55,7 +55,18 @@ constexpr int CHUNK_I4_ZERO_BYTES = TILE_ROWS * CHUNK_K / 32;       // 512: zero
 constexpr int CHUNK_I4_BYTES = CHUNK_MX_CODE_BYTES + CHUNK_I4_SCALE_BYTES + CHUNK_I4_ZERO_BYTES;  // 9728
 constexpr int HALF_K = CHUNK_K / 2;                                 // K of one pipeline stage
 
-enum ChunkLayout { LAYOUT_TILE = 0, LAYOUT_FRAG = 1, LAYOUT_FRAG_F16 = 2 };
+enum ChunkLayout { LAYOUT_TILE = 0, LAYOUT_FRAG = 1, LAYOUT_FRAG_F16 = 2, LAYOUT_TILE_F16 = 3 };
+
+// TILE_F16 layout (tcgen05 kernel with FP16 operands, MXFP4 only): the 128-K
+// chunk is four 32-value blocks b; row r's codes of block b are 16 plain pack4
+// bytes (element 2j in the low nibble of byte j) at [(b*128 + r)*16, +16), so
+// that 32 lanes holding 32 consecutive rows read 512 contiguous bytes; the
+// E8M0 byte of (block b, row r) is at [8192 + b*128 + r].  The largest
+// exponent of every row over its whole K (the row base b_row) is kept beside
+// the chunks (WeightStore::row_base); a weight decodes to FP16
+// v(c) * 2^(e - b_row), exact when the row's exponents span at most
+// TILE_F16_MAX_SPREAD.
+constexpr int TILE_F16_MAX_SPREAD = 23;
 
 // FRAG_F16 layout (streaming layer with FP16 operands): the same fragment
 // order as FRAG, but each word holds the 8 codes as 4 plain OCP E2M1 byte
@@ -95,6 +106,7 @@ struct WeightStore {
     int kchunks = 0;
     int chunk_bytes = 0;
     size_t group_bytes = 0;   // bytes of one expert group's matrix
+    uint8_t *row_base = nullptr;  // TILE_F16: largest E8M0 exponent of each row, [G][row_tiles * 128] (device)
 };
 
 // A caller-side source matrix for the repack: row r starts at
@@ -131,10 +143,16 @@ struct Plan {
     uint16_t *x_perm;         // [T*k][H] rows of x gathered in routed position order (BF16, or FP16 for
                               // the FP16 streaming path)
     uint16_t *x16;            // [T][H] token rows of the streaming path in x16 K order: FP16
-                              // x_t * 2^-xs[t] for MXFP4 and INT4 weights, BF16 x_t for BF16 weights
+                              // x_t * 2^-xs[t] for MXFP4 and INT4 weights, BF16 x_t for BF16 weights;
+                              // on the tcgen05 FP16 path FP16 x_t * 2^-xs[t] in natural K order
     int *xs;                  // [T] per-token power-of-two scale exponent of x16
+    int *xsp;                 // [P] tcgen05 FP16 path: xs of each position's token
     uint16_t *h;              // [2][P][I] h = hi plane + lo plane: BF16 (lo = bf16(h - hi)); on the FP16
-                              // streaming path FP16 (h * 2^-hs = hi + lo); x16 K order on the streaming path
+                              // streaming path FP16 (h * 2^-hs = hi + lo); x16 K order on the streaming path.
+                              // The tcgen05 path with FP16 operands keeps FP32 h [P][I] here instead.
+    uint16_t *h16;            // [P][I] tcgen05 FP16 path: FP16 h * 2^-hsp[p]
+    int *hmax;                // [P] tcgen05 FP16 path: largest |h| of each position (float bits), zeroed per call
+    int *hsp;                 // [P] tcgen05 FP16 path: power of two of each position's h16 row
     int *hs;                  // [P][hs_pitch] FP16 streaming path: power-of-two scale of each position's
                               // 64-feature block of h
     int hs_pitch;             // ceil(I/64) rounded up to a multiple of 4 (16-byte rows)
@@ -177,11 +195,28 @@ cudaError_t launch_dense_plan(const Plan &p, cudaStream_t st);
 
 cudaError_t launch_combine(const Plan &p, float *out, int accumulate, cudaStream_t st);
 
-cudaError_t launch_gather_rows(const Plan &p, const uint16_t *x, cudaStream_t st);
+// x_perm[p] = x[row_token[p]] for the routed positions; with xs_rows (x is the
+// FP16 token rows x16) also p.xsp[p] = p.xs[row_token[p]]
+cudaError_t launch_gather_rows(const Plan &p, const uint16_t *x, bool xs_rows, cudaStream_t st);
 
-cudaError_t launch_gemm_gate_up_tc(const Plan &p, const WeightStore &w, int fmt, const uint16_t *x, cudaStream_t st);
+// row bases of a TILE_F16 store for one group: for every tile row, the
+// largest E8M0 exponent over the row's K; a row whose exponents span more than
+// TILE_F16_MAX_SPREAD sets *wide
+cudaError_t launch_row_base(bool gate_up, const SrcMat &gate, const SrcMat &up, const WeightStore &ws, int group,
+                            int I, int H, int *wide, cudaStream_t st);
 
-cudaError_t launch_gemm_down_tc(const Plan &p, const WeightStore &w, int fmt, cudaStream_t st);
+// tcgen05 path with FP16 operands: FP16 token rows x16 and their powers of two xs
+cudaError_t launch_token_prep_f16(const Plan &p, const uint16_t *x, cudaStream_t st);
+
+// tcgen05 path with FP16 operands: FP32 h (in p.h) -> FP16 h16 with per-position powers of two
+cudaError_t launch_h_convert(const Plan &p, cudaStream_t st);
+
+// f16: FP16 operands (TILE_F16 MXFP4 store, token rows x_rows = x16 and the
+// gathered FP16 rows in x_perm); otherwise BF16 operands (x_rows = the caller's x)
+cudaError_t launch_gemm_gate_up_tc(const Plan &p, const WeightStore &w, int fmt, bool f16, const uint16_t *x_rows,
+                                   cudaStream_t st);
+
+cudaError_t launch_gemm_down_tc(const Plan &p, const WeightStore &w, int fmt, bool f16, cudaStream_t st);
 
 // The whole layer in one persistent kernel for decode-sized batches
 // (layer_stream.cu): token tiles of at most STREAM_MAX_T tokens; larger

@@ -75,6 +75,11 @@ SMALL = [
     wl.custom("stream_classes_T21_H320_I128_E4_S1_k3", 21, 320, 128, 4, 1, 3, seed=35),
     # 32-token kernel: down items of 1-4 tokens (packed) and of 5-8 and 11 tokens (class 2)
     wl.custom("stream_T30_H256_I128_E24_S1_k4", 30, 256, 128, 24, 1, 4, seed=39),
+    # tensor-core path, FP16 operands at the widest exponent span they take (23 within a row):
+    # weights down to 0.5 * 2^-23 relative to the row's largest scale are FP16 subnormals
+    wl.custom("tc_span23_T100_H288_I160_E16_S1_k4", 100, 288, 160, 16, 1, 4, seed=64, e8m0_lo=107, e8m0_hi=130),
+    # tensor-core path, exponents spanning more than 23 within rows: BF16 operands
+    wl.custom("tc_span34_T100_H288_I160_E16_S1_k4", 100, 288, 160, 16, 1, 4, seed=65, e8m0_lo=96, e8m0_hi=130),
 ]
 
 
