@@ -18,13 +18,15 @@
 //       reads A from there, so shared memory carries only the token operand;
 //   B = token rows, loaded by TMA into 128-byte-swizzled K-major tiles;
 //   MMA = tcgen05.mma kind::f16, M = 128, N = 16..256, K = 16, one thread.
-// A work item is (group, 128-row tile, token tile of up to 256), and a pipeline
-// stage is 128 values of K: eight MMAs of up to 128 cycles per hand-off between
-// the producers and the MMA thread.  (Measured: the tensor pipe idles when a
-// stage's hand-off guards few or short MMAs -- two 128 x 128 tiles per 64-wide
-// stage ran at about half rate; one 128 x 256 tile per 128-wide stage at full
-// rate.)  Tensor memory holds the 256-column accumulator and three stages of A
-// (64 columns each); shared memory three 64 KB stages of B.
+// A work item is (group, 128-row tile, token tile of up to 192), and a pipeline
+// stage is 128 values of K: eight long MMAs (up to 96 cycles each) per hand-off
+// between the producers and the MMA thread.  (Measured: the tensor pipe idles
+// when a stage's hand-off guards few or short MMAs -- two 128 x 128 tiles per
+// 64-wide stage ran at about half rate; one 128 x 256 tile per 128-wide stage at
+// full rate.)  Tensor memory holds two 192-column accumulators, so that the
+// epilogue of one item overlaps the MMAs of the next, and two stages of A (64
+// columns each); shared memory holds four 48 KB stages of B, a deeper ring
+// with its own barriers, so that token tiles arrive ahead despite L2 latency.
 //
 // Two operand types (chosen per handle at load):
 //   FP16: MXFP4 weights whose E8M0 exponents span at most 23 within every row.
@@ -44,13 +46,12 @@
 //   warp 0      TMA-loads token tiles (B) into the shared-memory stage ring and
 //               prefetches the weight chunks ahead of the decoders into L2
 //   warp 1      allocates tensor memory, issues the MMAs, commits to mbarriers
-//   warps 2-13  decode weights into the tensor-memory A ring: three groups of
-//               four warps, group g decoding every third stage (ring slot g) in
+//   warps 2-9   decode weights into the tensor-memory A ring: two groups of
+//               four warps, group g decoding every other stage (A slot g) in
 //               full; its warp w covers lane quadrant w % 4 (the lanes a warp
 //               may access)
-//   warps 14-21 epilogue, two warps per lane quadrant splitting the columns:
-//               tensor memory -> registers, SwiGLU (gate|up) or FP32 y (down);
-//               the accumulator is released once per work item.
+//   warps 10-17 epilogue, two warps per lane quadrant splitting the columns:
+//               tensor memory -> registers, SwiGLU (gate|up) or FP32 y (down).
 // Every mbarrier wait is bounded: on a timeout the kernel records
 // DEV_ERR_WAIT_TIMEOUT, stops issuing work, waits (bounded) for the copies and
 // MMAs it has in flight, frees its tensor memory and exits.
@@ -68,24 +69,27 @@ namespace {
 
 using namespace gemm;
 
-constexpr int N_DEC_WARPS = 12;
+constexpr int N_DEC_WARPS = 8;
 constexpr int N_DEC_GROUPS = N_DEC_WARPS / 4;  // groups of four warps, one per tensor-memory lane quadrant
 constexpr int N_EPI_WARPS = 8;                 // two per tensor-memory lane quadrant, splitting the columns
 constexpr int NUM_THREADS = (2 + N_DEC_WARPS + N_EPI_WARPS) * 32;
 constexpr int WARP_BLOAD = 0, WARP_MMA = 1, WARP_DEC0 = 2, WARP_EPI0 = WARP_DEC0 + N_DEC_WARPS;
-constexpr int NMAX = 256;                      // token columns of a work item
-constexpr int TC_STAGES = 3;                   // pipeline stages in flight
+constexpr int NMAX = 192;                      // token columns of a work item
+constexpr int NBUF = 2;                        // accumulators: one item's epilogue overlaps the next item's MMAs
+constexpr int A_STAGES = 2;                    // A ring (tensor memory)
+constexpr int B_STAGES = 4;                    // B ring (shared memory)
 constexpr int TMEM_COLS = 512;                 // the whole tensor memory of the SM
 constexpr int A_SLOT_COLS = 64;                // tensor-memory columns of a stage of A: 128 16-bit values per lane
-constexpr int TMEM_A0 = NMAX;                  // first column of the A ring, after the accumulator
-static_assert(TMEM_A0 + TC_STAGES * A_SLOT_COLS <= TMEM_COLS, "tensor memory");
-// Decoder group g fills ring slot g only (stages g, g + TC_STAGES, ...): it then
+constexpr int TMEM_A0 = NBUF * NMAX;           // first column of the A ring, after the accumulators
+static_assert(TMEM_A0 + A_STAGES * A_SLOT_COLS <= TMEM_COLS, "tensor memory");
+// Decoder group g fills A slot g only (stages g, g + A_STAGES, ...): it then
 // waits on that slot's empty barrier for its own previous stage alone, never
 // for a phase two behind (where the parity it waits for would already read as
 // complete from an older phase).
-static_assert(N_DEC_GROUPS == TC_STAGES, "one decoder group per ring slot");
-constexpr int B_SLICE_BYTES = NMAX * HALF_K * 2;  // 32 KB: 256 token rows x 64 16-bit values (one swizzled tile)
+static_assert(N_DEC_GROUPS == A_STAGES, "one decoder group per A slot");
+constexpr int B_SLICE_BYTES = NMAX * HALF_K * 2;  // 24 KB: 192 token rows x 64 16-bit values (one swizzled tile)
 constexpr int B_STAGE_BYTES = 2 * B_SLICE_BYTES;  // two slices: 128 K values of one plane, or 64 of two planes
+static_assert(B_SLICE_BYTES % 1024 == 0, "swizzled tiles start on 1024-byte boundaries");
 // B operand TMA boxes: 64 token rows (8 KB) each, so that a stage takes few
 // TMA issues; 16 rows when a B tensor has fewer than 64 rows
 constexpr int B_BOX_ROWS_BIG = 64, B_BOX_ROWS_SMALL = 16;
@@ -237,8 +241,8 @@ __device__ __forceinline__ void e2m1x8_f16(uint32_t w, uint32_t s2, uint32_t *ou
 __device__ __forceinline__ float pow2i(int k) { return __int_as_float((127 + k) << 23); }
 
 struct Smem {
-    static constexpr int BAR_OFF = TC_STAGES * B_STAGE_BYTES;
-    static constexpr int N_BARS = 2 * TC_STAGES + 2;
+    static constexpr int BAR_OFF = B_STAGES * B_STAGE_BYTES;
+    static constexpr int N_BARS = 2 * B_STAGES + 2 * A_STAGES + 2 * NBUF;
     static constexpr int SCHED_OFF = BAR_OFF + N_BARS * 8;
     static constexpr int MISC_OFF = SCHED_OFF + (MAX_GROUPS + 1) * 4;
     static constexpr int COLSC_OFF = MISC_OFF + 32;    // epilogue: column scales of an item, one row per warp
@@ -256,7 +260,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     constexpr int KST = NB == 2 ? HALF_K : CHUNK_K;     // K values per stage
     constexpr int NSL = KST / HALF_K;                   // 64-wide K slices per stage
     constexpr int NBLK = KST / 32;                      // 32-value blocks per stage
-    constexpr int S = TC_STAGES;
     using L = Smem;
     static_assert(L::TOTAL <= 232448, "shared memory");
     static_assert(NSL * NB == 2, "a stage holds two swizzled B tiles");
@@ -264,8 +267,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);
-    uint64_t *ab_full = bars, *ab_empty = bars + S;
-    uint64_t *acc_full = bars + 2 * S, *acc_empty = acc_full + 1;
+    uint64_t *b_full = bars, *b_empty = b_full + B_STAGES;
+    uint64_t *a_full = b_empty + B_STAGES, *a_empty = a_full + A_STAGES;
+    uint64_t *acc_full = a_empty + A_STAGES, *acc_empty = acc_full + NBUF;
     int *prefix = reinterpret_cast<int *>(smem + L::SCHED_OFF);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::MISC_OFF + 4);
@@ -275,12 +279,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int rb_stride = a.row_tiles * TILE_ROWS;
 
     if (tid == 0) {
-        for (int i = 0; i < S; ++i) {
-            mbar_init(&ab_full[i], 1 + 4);  // the token copy and the four warps of the stage's decoder group
-            mbar_init(&ab_empty[i], 1);
+        for (int i = 0; i < B_STAGES; ++i) {
+            mbar_init(&b_full[i], 1);  // the token copies (expect-tx)
+            mbar_init(&b_empty[i], 1);
         }
-        mbar_init(acc_full, 1);
-        mbar_init(acc_empty, N_EPI_WARPS);
+        for (int i = 0; i < A_STAGES; ++i) {
+            mbar_init(&a_full[i], 4);  // the four warps of the slot's decoder group
+            mbar_init(&a_empty[i], 1);
+        }
+        for (int i = 0; i < NBUF; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], N_EPI_WARPS);
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async();
@@ -349,26 +359,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int box_bytes = a.brows * HALF_K * 2;
             const uint32_t bytes = (uint32_t)(nbox * box_bytes * 2);
             for (int st = 0; st < nstages; ++st, ++sc) {
-                const int slot = sc % S;
-                const uint32_t ph = (sc / S) & 1;
-                if (!(ok = mbar_wait_sleep_warp(&ab_empty[slot], ph ^ 1, abort_flag, a.err, lane)))
+                const int slot = sc % B_STAGES;
+                const uint32_t ph = (sc / B_STAGES) & 1;
+                if (!(ok = mbar_wait_sleep_warp(&b_empty[slot], ph ^ 1, abort_flag, a.err, lane)))
                     break;
                 if (KST == CHUNK_K || (st & 1) == 0)
                     pf_next();
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&ab_full[slot], bytes);
+                    mbar_arrive_expect_tx(&b_full[slot], bytes);
                     uint8_t *bdst = smem + slot * B_STAGE_BYTES;
                     // the stage's two swizzled tiles: two 64-wide K slices of one plane,
                     // or one slice of the h hi and lo planes
                     for (int b = 0; b < nbox; ++b) {
                         if (NB == 1) {
-                            tma_2d(bdst + b * box_bytes, m0, st * KST, row0 + b * a.brows, &ab_full[slot]);
+                            tma_2d(bdst + b * box_bytes, m0, st * KST, row0 + b * a.brows, &b_full[slot]);
                             tma_2d(bdst + B_SLICE_BYTES + b * box_bytes, m0, st * KST + HALF_K, row0 + b * a.brows,
-                                   &ab_full[slot]);
+                                   &b_full[slot]);
                         } else {
-                            tma_2d(bdst + b * box_bytes, m0, st * KST, row0 + b * a.brows, &ab_full[slot]);
+                            tma_2d(bdst + b * box_bytes, m0, st * KST, row0 + b * a.brows, &b_full[slot]);
                             tma_2d(bdst + B_SLICE_BYTES + b * box_bytes, &map_b2, st * KST, row0 + b * a.brows,
-                                   &ab_full[slot]);
+                                   &b_full[slot]);
                         }
                     }
                 }
@@ -379,9 +389,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // drain: every armed stage's B tiles have landed (returns at once on the
         // normal path, where the MMA has consumed them; bounded after an abort)
         if (lane == 0)
-            for (int s = 0; s < S; ++s)
+            for (int s = 0; s < B_STAGES; ++s)
                 if (armed & (1u << s))
-                    mbar_drain(&ab_full[s], (armed_par >> s) & 1);
+                    mbar_drain(&b_full[s], (armed_par >> s) & 1);
         __syncwarp();
     } else if (warp == WARP_MMA) {
         // ---------------------------------------------------------- MMA issue (lane 0)
@@ -390,29 +400,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool issued = false, ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
             const WorkItem w = decompose(t, prefix, a.grp_count, a.G, rt_n, NMAX);
-            if (!(ok = mbar_wait_warp(acc_empty, (tc & 1) ^ 1, abort_flag, a.err, lane)))
+            const int buf = tc % NBUF;
+            if (!(ok = mbar_wait_warp(&acc_empty[buf], ((tc / NBUF) & 1) ^ 1, abort_flag, a.err, lane)))
                 break;
             tc_fence_after();
             const uint32_t idesc = make_idesc<OP>(w.n_mma);
+            const uint32_t d_tmem = tmem_base + (uint32_t)(buf * NMAX);
             for (int st = 0; st < nstages; ++st, ++sc) {
-                const int slot = sc % S;
-                if (!(ok = mbar_wait_warp(&ab_full[slot], (sc / S) & 1, abort_flag, a.err, lane)))
+                // a_full completes once the stage's A is in tensor memory and its B tiles
+                // have landed (the decoder group waits for the token copy before it
+                // arrives), so each stage costs the MMA thread one wait
+                const int bs = sc % B_STAGES, as = sc % A_STAGES;
+                if (!(ok = mbar_wait_warp(&a_full[as], (sc / A_STAGES) & 1, abort_flag, a.err, lane)))
                     break;
                 tc_fence_after();
                 if (lane == 0) {
                     // descriptors of this slot: base plus the slot's offset (address field = bytes >> 4)
-                    const uint64_t bd = desc0 + (uint64_t)((slot * B_STAGE_BYTES) >> 4);
-                    const uint32_t at = tmem_base + (uint32_t)(TMEM_A0 + slot * A_SLOT_COLS);
+                    const uint64_t bd = desc0 + (uint64_t)((bs * B_STAGE_BYTES) >> 4);
+                    const uint32_t at = tmem_base + (uint32_t)(TMEM_A0 + as * A_SLOT_COLS);
                     if (NB == 1) {
 #pragma unroll
                         for (int sl = 0; sl < NSL; ++sl)
-                            tc_mma4(tmem_base, at + 32 * sl, bd + (uint64_t)((sl * B_SLICE_BYTES) >> 4), idesc,
+                            tc_mma4(d_tmem, at + 32 * sl, bd + (uint64_t)((sl * B_SLICE_BYTES) >> 4), idesc,
                                     st > 0 || sl > 0);
                     } else {
-                        tc_mma4(tmem_base, at, bd, idesc, st);
-                        tc_mma4(tmem_base, at, bd + (uint64_t)(B_SLICE_BYTES >> 4), idesc, 1u);
+                        tc_mma4(d_tmem, at, bd, idesc, st);
+                        tc_mma4(d_tmem, at, bd + (uint64_t)(B_SLICE_BYTES >> 4), idesc, 1u);
                     }
-                    tc_commit(&ab_empty[slot]);
+                    tc_commit(&b_empty[bs]);
+                    tc_commit(&a_empty[as]);
                 }
                 __syncwarp();
                 issued = true;
@@ -420,20 +436,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!ok)
                 break;
             if (lane == 0)
-                tc_commit(acc_full);
+                tc_commit(&acc_full[buf]);
             __syncwarp();
         }
         // drain: the MMAs of the last committed item have completed
         if (lane == 0 && issued && tc > 0)
-            mbar_drain(acc_full, (tc - 1) & 1);
+            mbar_drain(&acc_full[(tc - 1) % NBUF], ((tc - 1) / NBUF) & 1);
         __syncwarp();
     } else if (warp < WARP_EPI0) {
         // ---------------------------------------------------------- decoders
-        // Group gi decodes every N_DEC_GROUPS-th stage (gs = gi, gi + 3, ...: ring
+        // Group gi decodes every N_DEC_GROUPS-th stage (gs = gi, gi + 2, ...: A
         // slot gi) in full; its warp of lane quadrant q = warp % 4 decodes rows
         // 32q..32q+31 (lane = row) of the item's row tile over the stage's KST
         // values of K into the slot's columns of the tensor-memory A ring, so each
-        // warp pays the stage hand-off (wait, fences, arrive) once per three stages.  A lane
+        // warp pays the stage hand-off (wait, fences, arrive) once per two stages.  A lane
         // loads its next stage's raw codes and scales straight from global
         // memory (into registers) as soon as it has handed over the current one;
         // the token loader has prefetched them into L2.
@@ -487,8 +503,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (gs < total_st)
             fetch(gs);
         for (; gs < total_st && ok; gs += N_DEC_GROUPS) {
-            const int slot = gs % S;
-            if (!(ok = mbar_wait_warp(&ab_empty[slot], ((gs / S) & 1) ^ 1, abort_flag, a.err, lane)))
+            const int slot = gi;  // = gs % A_STAGES
+            if (!(ok = mbar_wait_warp(&a_empty[slot], ((gs / A_STAGES) & 1) ^ 1, abort_flag, a.err, lane)))
                 break;
             tc_fence_after();
             if (WFMT == FMT_BF16)
@@ -528,9 +544,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tc_fence_before();
-            __syncwarp();
+            // the stage's token tiles must have landed too: the MMA thread waits on
+            // a_full alone (this group waited on this B slot four stages ago, so the
+            // parity below is never two phases ahead)
+            if (!(ok = mbar_wait_warp(&b_full[gs % B_STAGES], (gs / B_STAGES) & 1, abort_flag, a.err, lane)))
+                break;
             if (lane == 0)
-                mbar_arrive(&ab_full[slot]);
+                mbar_arrive(&a_full[slot]);
             if (gs + N_DEC_GROUPS < total_st)
                 fetch(gs + N_DEC_GROUPS);
         }
@@ -556,12 +576,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         csc[c] = pow2i(__ldg((GU ? a.xsp : a.hsp) + pos0 + c));
                 __syncwarp();
             }
-            if (!mbar_wait_sleep_warp(acc_full, tc & 1, abort_flag, a.err, lane))
+            const int buf = tc % NBUF;
+            if (!mbar_wait_sleep_warp(&acc_full[buf], (tc / NBUF) & 1, abort_flag, a.err, lane))
                 break;
             tc_fence_after();
             const int rt = w.rt;
             const int row = 32 * q + lane;
-            const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16);
+            const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * NMAX);
             // FP16 operands: this row's weight scale 2^(b - 127) (exact; a subnormal for b = 0)
             const float wsc = OP == OP_F16
                                   ? ldexpf(1.0f, (int)__ldg(a.row_base + (size_t)w.g * rb_stride + rt * TILE_ROWS + row) - 127)
@@ -638,7 +659,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(acc_empty);
+                mbar_arrive(&acc_empty[buf]);
         }
     }
 
