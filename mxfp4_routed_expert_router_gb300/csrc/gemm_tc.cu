@@ -394,27 +394,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     mbar_drain(&b_full[s], (armed_par >> s) & 1);
         __syncwarp();
     } else if (warp == WARP_MMA) {
-        // ---------------------------------------------------------- MMA issue (lane 0)
-        uint32_t sc = 0, tc = 0;
-        const uint64_t desc0 = sw128_desc(smem_addr(smem));  // K-major SW128 descriptor of B stage 0
-        bool issued = false, ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
-            const WorkItem w = decompose(t, prefix, a.grp_count, a.G, rt_n, NMAX);
-            const int buf = tc % NBUF;
-            if (!(ok = mbar_wait_warp(&acc_empty[buf], ((tc / NBUF) & 1) ^ 1, abort_flag, a.err, lane)))
-                break;
-            tc_fence_after();
-            const uint32_t idesc = make_idesc<OP>(w.n_mma);
-            const uint32_t d_tmem = tmem_base + (uint32_t)(buf * NMAX);
-            for (int st = 0; st < nstages; ++st, ++sc) {
-                // a_full completes once the stage's A is in tensor memory and its B tiles
-                // have landed (the decoder group waits for the token copy before it
-                // arrives), so each stage costs the MMA thread one wait
-                const int bs = sc % B_STAGES, as = sc % A_STAGES;
-                if (!(ok = mbar_wait_warp(&a_full[as], (sc / A_STAGES) & 1, abort_flag, a.err, lane)))
+        // ---------------------------------------------------------- MMA issue
+        // Lane 0 alone runs this role: its waits, fences and MMAs need no
+        // warp-wide step between stages.
+        if (lane == 0) {
+            uint32_t sc = 0, tc = 0;
+            const uint64_t desc0 = sw128_desc(smem_addr(smem));  // K-major SW128 descriptor of B stage 0
+            bool ok = true, partial = false;  // partial: an aborted item has MMAs in flight
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
+                const WorkItem w = decompose(t, prefix, a.grp_count, a.G, rt_n, NMAX);
+                const int buf = tc % NBUF;
+                if (!(ok = mbar_wait(&acc_empty[buf], ((tc / NBUF) & 1) ^ 1, abort_flag, a.err)))
                     break;
                 tc_fence_after();
-                if (lane == 0) {
+                const uint32_t idesc = make_idesc<OP>(w.n_mma);
+                const uint32_t d_tmem = tmem_base + (uint32_t)(buf * NMAX);
+                for (int st = 0; st < nstages; ++st, ++sc) {
+                    // a_full completes once the stage's A is in tensor memory and its B
+                    // tiles have landed (the decoder group waits for the token copy
+                    // before it arrives), so each stage costs the MMA thread one wait
+                    const int bs = sc % B_STAGES, as = sc % A_STAGES;
+                    if (!(ok = mbar_wait(&a_full[as], (sc / A_STAGES) & 1, abort_flag, a.err)))
+                        break;
+                    tc_fence_after();
                     // descriptors of this slot: base plus the slot's offset (address field = bytes >> 4)
                     const uint64_t bd = desc0 + (uint64_t)((bs * B_STAGE_BYTES) >> 4);
                     const uint32_t at = tmem_base + (uint32_t)(TMEM_A0 + as * A_SLOT_COLS);
@@ -429,19 +431,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     tc_commit(&b_empty[bs]);
                     tc_commit(&a_empty[as]);
+                    partial = true;
                 }
-                __syncwarp();
-                issued = true;
-            }
-            if (!ok)
-                break;
-            if (lane == 0)
+                if (!ok)
+                    break;
                 tc_commit(&acc_full[buf]);
-            __syncwarp();
+                partial = false;
+            }
+            // drain: every MMA issued has completed.  After an abort in the middle of
+            // item tc, its MMAs are committed to its accumulator barrier first.
+            if (partial) {
+                tc_commit(&acc_full[tc % NBUF]);
+                mbar_drain(&acc_full[tc % NBUF], (tc / NBUF) & 1);
+            } else if (tc > 0) {
+                mbar_drain(&acc_full[(tc - 1) % NBUF], ((tc - 1) / NBUF) & 1);
+            }
         }
-        // drain: the MMAs of the last committed item have completed
-        if (lane == 0 && issued && tc > 0)
-            mbar_drain(&acc_full[(tc - 1) % NBUF], ((tc - 1) / NBUF) & 1);
         __syncwarp();
     } else if (warp < WARP_EPI0) {
         // ---------------------------------------------------------- decoders
