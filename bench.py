@@ -169,15 +169,50 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def roofline_entry(dom: dict, dom_ms: float, peaks: dict, peak_src: str) -> dict:
+def tc_fp16_operands(cfg) -> bool:
+    """Whether the tensor-memory GEMMs take FP16 operands for this layer: the
+    library decodes MXFP4 weights exactly to FP16 against a per-row exponent
+    base when no row's E8M0 exponents span more than 23; the seeded exponents
+    are uniform in [e8m0_lo, e8m0_hi], so a range of at most 23 guarantees it.
+    BF16 weights, and MXFP4 rows of a wider span, run with BF16 operands."""
+    return cfg.weight_format == "mxfp4" and cfg.e8m0_hi - cfg.e8m0_lo <= 23
+
+
+def kernels_per_step(cfg, streaming: bool) -> int:
+    """Kernels of this library launched by one forward call.
+
+    The single-kernel layer launches one kernel.  Otherwise: router, histogram
+    and permutation (routed) or the dense plan (dense); with FP16 operands the
+    token preparation, the row gather, gate|up, the h conversion and down (the
+    h maxima are cleared by a memset, not a kernel); with BF16 operands the row
+    gather, gate|up and down; then the combine."""
+    if streaming:
+        return 1
+    return (1 if cfg.dense else 3) + (5 if tc_fp16_operands(cfg) else 3) + 1
+
+
+def operand_dtype(cfg, streaming: bool) -> str:
+    """Operand type of the layer's products (FP32 accumulation throughout): the
+    single-kernel layer decodes MXFP4 and INT4 weights to FP16; the tensor-memory
+    GEMMs take FP16 or BF16 operands as tc_fp16_operands says."""
+    if streaming:
+        return "f16" if cfg.weight_format in ("mxfp4", "int4g32") else "bf16"
+    return "f16" if tc_fp16_operands(cfg) else "bf16"
+
+
+def roofline_entry(dom: dict, dom_ms: float, peaks: dict, peak_src: str, dtype: str = "bf16") -> dict:
     """Roofline of a kernel from its algorithmic bytes and flops and its time:
     the bound is whichever minimum time is longer at the measured peaks; the
-    fraction is also given against the datasheet peak (frac_nominal)."""
+    fraction is also given against the datasheet peak (frac_nominal).  FP16
+    and BF16 products have the same dense tensor rate (2.25 PFLOP/s nominal
+    each), so an FP16 contraction takes the measured BF16 peak times 1."""
     tensor_bound = dom["flops"] / (peaks["bf16_tflops"] * 1e12) > dom["bytes"] / (peaks["hbm_gbs"] * 1e9)
     if tensor_bound:
         achieved = dom["flops"] / (dom_ms * 1e-3) / 1e12
         return {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"], "peak_source": f"bf16 burst, of {peak_src}",
+                "frac": achieved / peaks["bf16_tflops"],
+                "peak_source": (f"bf16 burst, of {peak_src}" if dtype == "bf16" else
+                                f"{dtype}: bf16 burst x 1 (equal nominal rates), of {peak_src}"),
                 "frac_nominal": achieved / NOMINAL_PEAKS["bf16_tflops"]}
     achieved = dom["bytes"] / (dom_ms * 1e-3) / 1e9
     return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -330,7 +365,7 @@ def summarize_extra(cfg, ms, clocks, stage_ms, groups, peaks, peak_src):
          "active_groups": groups, "weight_GBps": weight_bytes / (ms * 1e-3) / 1e9,
          "layer_TFLOPs": flops / (ms * 1e-3) / 1e12, "clocks": clocks,
          "stages_ms": {"layer": stage_ms["layer"]} if dom_name == "layer" else stage_ms}
-    roof = roofline_entry(dom, stage_ms[dom_name], peaks, peak_src)
+    roof = roofline_entry(dom, stage_ms[dom_name], peaks, peak_src, operand_dtype(cfg, dom_name == "layer"))
     roof["kernel"] = "single-kernel MoE layer" if dom_name == "layer" else f"{dom_name} GEMM"
     roof["kernel_ms"] = stage_ms[dom_name]
     r["roofline"] = roof
@@ -434,20 +469,15 @@ def run_ours(args, cfg, rank, world):
     if dom_name == "layer":
         # the single kernel runs every stage; the other marks are empty
         stage_ms = {"layer": stage_ms["layer"]}
-    roof = roofline_entry(dom, dom_ms, peaks, peak_src)
+    roof = roofline_entry(dom, dom_ms, peaks, peak_src, operand_dtype(cfg, dom_name == "layer"))
     roof["kernel"] = "single-kernel MoE layer" if dom_name == "layer" else f"{dom_name} GEMM"
     roof["traffic"] = ncu_traffic(f"{dom_name}:{cfg.name}")
     roof["algorithmic_bytes"] = dom["bytes"]
     roof["algorithmic_flops"] = dom["flops"]
     roof["kernel_ms"] = dom_ms
-    # the single-kernel layer launches one kernel (after clearing its counters);
-    # otherwise router, histogram, permutation (or the dense plan), token
-    # gather, gate|up GEMM, down GEMM, combine
     streaming = dom_name == "layer"
-    launches_per_step = 1 if streaming else (5 if cfg.dense else 7)
-    # operand type of the GEMMs: the streaming layer decodes MXFP4 to FP16
-    # (FP32 accumulate); the tcgen05 path and BF16 weights run in BF16
-    dtype = "f16" if streaming and cfg.weight_format in ("mxfp4", "int4g32") else "bf16"
+    launches_per_step = kernels_per_step(cfg, streaming)
+    dtype = operand_dtype(cfg, streaming)
     weight_bytes = gate_up["weight_bytes"] + down["weight_bytes"]
     value = job_tokens_per_s(world, cfg.T, ms)
     res = {
@@ -485,7 +515,8 @@ def run_ours(args, cfg, rank, world):
         e_ent = summarize_extra(ecfg, ems, eclk, est, egroups, peaks, peak_src)
         e_ent["tokens_per_s"] = job_tokens_per_s(world, ecfg.T, ems)
         e_ent["steps"] = esteps
-        e_ent["gpu_launches"] = esteps * (1 if e_ent["roofline"]["kernel"] == "single-kernel MoE layer" else 7)
+        e_ent["gpu_launches"] = esteps * kernels_per_step(ecfg, e_ent["roofline"]["kernel"] == "single-kernel MoE layer")
+        e_ent["dtype"] = operand_dtype(ecfg, e_ent["roofline"]["kernel"] == "single-kernel MoE layer")
         extras[name] = e_ent
         del EW
     if extras:

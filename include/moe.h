@@ -284,10 +284,13 @@ MoeStatus moe_sync_status(MoeHandle *h, void *cuda_stream);
 
 /* Per-stage timing for benchmarking.  While enabled, every forward call on
  * this handle records CUDA events on its stream around its stages.  Stages:
- * [0] routing (router kernel), [1] grouping (histogram + permutation, or the
- * dense plan), [2] gate|up GEMM with SwiGLU, [3] down GEMM, [4] combine,
- * [5] the single-kernel layer that decode-sized batches run instead of
- * [0]..[4].  A stage a call does not run reads 0.
+ * [0] routing (router kernel, or the copy of caller routing), [1] grouping and
+ * token rows (histogram + permutation, or the dense plan; then, with FP16
+ * operands, the per-token FP16 conversion, and the gather of token rows into
+ * position order), [2] gate|up GEMM with SwiGLU (with FP16 operands also the
+ * clear of the per-position maxima and the conversion of h to one FP16 plane),
+ * [3] down GEMM, [4] combine, [5] the single-kernel layer that decode-sized
+ * batches run instead of [0]..[4].  A stage a call does not run reads 0.
  * Errors: MOE_EINVAL (NULL handle), MOE_ECUDA (event creation failed). */
 MoeStatus moe_profile_enable(MoeHandle *h, int enable);
 
