@@ -28,13 +28,12 @@
 //            warps (16 weight rows each, the full K) decode MXFP4 or INT4 in
 //            registers straight into warp-level MMA fragments (FP16 operands,
 //            FP32 accumulation, the E8M0 or FP16 block scales applied in FP32
-//            to each 32-wide block's partial sum).  gate|up epilogues write h (FP16
-//            hi + lo, scaled per 64-feature block) and hand the item to warp
+//            to each 32-wide block's partial sum).  gate|up epilogues write h
+//            (one FP16 plane, scaled by a power of two per 64-feature block;
+//            BF16 hi + lo planes for BF16 weights) and hand the item to warp
 //            9, which publishes it to the other CTAs with one release; a
 //            down item's token rows are copied only once its group's h is
-//            complete, while its weights are already streaming.  Down items
-//            of at most four tokens (in the kernels for up to 16 tokens)
-//            carry each token's hi and lo planes in adjacent MMA columns.
+//            complete, while its weights are already streaming.
 //  combine   once every CTA has counted its items done, all warps of the
 //            grid sum (token, 128-feature) blocks of y into out in a fixed
 //            order (j ascending, then shared groups), so the result does not
@@ -78,6 +77,10 @@ constexpr int LS_R_MAX = 16;
 constexpr int LS_TINY_TARGET = 40960;
 constexpr int LS_TINY_TARGET_I4 = 41088;
 constexpr int LS_HS_ROW = 16;  // ints of h block scales kept per token row and stage
+// L2 prefetch at kernel entry of the leading shared groups' gate|up weights:
+// at most this many bytes over the grid, in pieces of LS_PF_PIECE
+constexpr size_t LS_PF_BYTES = 24u << 20;
+constexpr uint32_t LS_PF_PIECE = 32768;
 
 // ------------------------------------------------------------------ stage geometry
 //
@@ -119,6 +122,9 @@ struct LsCfg {
     static constexpr int SMEM_LIMIT = ls_smem_limit(CTAS);
     static constexpr int TARGET = NT == 0 ? (WFMT == FMT_INT4 ? LS_TINY_TARGET_I4 : LS_TINY_TARGET)
                                           : ls_stage_target(CTAS);
+    // token operands of a down stage: one FP16 plane of h (MXFP4, INT4), or the
+    // BF16 hi and lo planes (BF16 weights)
+    static constexpr int NB_DN = F16 ? 1 : 2;
     __host__ __device__ static constexpr int res_rows(int nti) { return NT == 0 ? 2 : 8 * nti; }
     __host__ __device__ static constexpr int hsb_dn(int nti) { return F16 ? res_rows(nti) * LS_HS_ROW * 4 : 0; }
     __host__ __device__ static constexpr int ch_gu(int nti)
@@ -127,12 +133,12 @@ struct LsCfg {
     }
     __host__ __device__ static constexpr int ch_dn(int nti)
     {
-        return ls_pick_ch(2, res_rows(nti), hsb_dn(nti), W_CHUNK, TARGET);
+        return ls_pick_ch(NB_DN, res_rows(nti), hsb_dn(nti), W_CHUNK, TARGET);
     }
     __host__ __device__ static constexpr int stage_of(int nti)
     {
         return ls_max(ls_stage_bytes(1, res_rows(nti), 0, ch_gu(nti), W_CHUNK),
-                      ls_stage_bytes(2, res_rows(nti), hsb_dn(nti), ch_dn(nti), W_CHUNK));
+                      ls_stage_bytes(NB_DN, res_rows(nti), hsb_dn(nti), ch_dn(nti), W_CHUNK));
     }
     static constexpr int STAGE = (ls_max(ls_max(stage_of(1), NT >= 2 ? stage_of(2) : 0),
                                          ls_max(NT >= 4 ? stage_of(4) : 0, NT >= 8 ? stage_of(8) : 0)) +
@@ -339,6 +345,12 @@ __device__ __forceinline__ int ld_acquire(const int *p)
 }
 
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// bring [p, p + bytes) into L2 (16-byte aligned address, size a multiple of 16)
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 __device__ __forceinline__ void st_release(int *p, int v)
 {
@@ -551,13 +563,19 @@ __device__ void ls_prep_token(const LayerArgs &a, int t, uint8_t *scratch)
 
 // ------------------------------------------------------------------ phase 0b
 
+// Work-list order of the groups: the shared groups (or dense slices) first, then
+// the routed experts in index order.  The shared groups' items do not depend on
+// the routing, so their weights can start moving before it is done.
+__device__ __forceinline__ int ls_group_of(int j, int E, int G) { return j < G - E ? E + j : j - (G - E); }
+
 // Groups, positions, token tiles and (routed) the stable permutation, in
 // shared memory.  Positions: routed slots 0..n-1 in expert-major order (slots
 // of one expert in ascending slot order s = t*k + j), then shared group s at
 // n + s*T + t.  gcnt[g] / gstart[g]: tokens and first position of group g;
-// tpre[g]: first token tile of group g (a group of c tokens has ceil(c/ROWS)
-// tiles); sorted[p]: slot at routed position p, replaced by its token once
-// CTA 0 has published the permutation; xs_s[t]: the x16 scales.
+// tpre[j]: first token tile of the j-th group in work-list order (ls_group_of;
+// a group of c tokens has ceil(c/ROWS) tiles); sorted[p]: slot at routed
+// position p, replaced by its token once CTA 0 has published the permutation;
+// xs_s[t]: the x16 scales.
 template <int ROWS, bool F16>
 __device__ void ls_schedule(const LayerArgs &a, uint8_t *scratch, int *gcnt, int *gstart, int *tpre, int *sorted,
                             int *xs_s, bool local)
@@ -581,12 +599,14 @@ __device__ void ls_schedule(const LayerArgs &a, uint8_t *scratch, int *gcnt, int
     for (int s = tid; s < n; s += LS_THREADS)
         atomicAdd(&gcnt[sid[s]], 1);
     __syncthreads();
-    // group scan: positions (routed groups only) and token tiles, 32 groups per
-    // warp, LS_WARPS * 32 groups per round
+    // group scan in work-list order: positions (routed groups only, which keeps
+    // them in expert order) and token tiles, 32 groups per warp, LS_WARPS * 32
+    // groups per round
     int base_pos = 0, base_tiles = 0;
     for (int g0 = 0; g0 < G; g0 += LS_WARPS * 32) {
-        const int g = g0 + warp * 32 + lane;
-        const int c = g < G ? gcnt[g] : 0;
+        const int j = g0 + warp * 32 + lane;
+        const int g = j < G ? ls_group_of(j, E, G) : G;
+        const int c = j < G ? gcnt[g] : 0;
         const int cp = g < E ? c : 0;
         const int tl = (c + ROWS - 1) / ROWS;
         int ip = cp, it = tl;
@@ -612,9 +632,9 @@ __device__ void ls_schedule(const LayerArgs &a, uint8_t *scratch, int *gcnt, int
             tp += wtot[2 * w];
             tt += wtot[2 * w + 1];
         }
-        if (g < G) {
+        if (j < G) {
             gstart[g] = g < E ? op + ip - cp : n + (g - E) * a.T;
-            tpre[g] = ot + it - tl;
+            tpre[j] = ot + it - tl;
         }
         base_pos += tp;
         base_tiles += tt;
@@ -706,13 +726,15 @@ __device__ void ls_schedule(const LayerArgs &a, uint8_t *scratch, int *gcnt, int
 struct LsItem {
     bool gu;
     int g, rt, tok0, nvalid, pos0;
+    int ntl;  // token tiles of the group
 };
 
-// Item u: gate|up items u < total_gu, then down items.  Items of one group are
-// ordered row tile major, token tile minor; a group of c tokens in ntiles
-// tiles gives each tile ceil(c / ntiles) tokens rounded up to 8.
+// Item u: gate|up items u < total_gu, then down items, groups in work-list
+// order.  Items of one group are ordered row tile major, token tile minor; a
+// group of c tokens in ntiles tiles gives each tile ceil(c / ntiles) tokens
+// rounded up to 8.
 template <int ROWS>
-__device__ __forceinline__ LsItem ls_item(int u, int total_gu, int rt_gu, int rt_dn, int G, const int *gcnt,
+__device__ __forceinline__ LsItem ls_item(int u, int total_gu, int rt_gu, int rt_dn, int E, int G, const int *gcnt,
                                           const int *gstart, const int *tpre)
 {
     LsItem it;
@@ -729,38 +751,25 @@ __device__ __forceinline__ LsItem ls_item(int u, int total_gu, int rt_gu, int rt
         else
             hi = mid;
     }
-    it.g = lo;
+    it.g = ls_group_of(lo, E, G);
     const int ntiles = tpre[lo + 1] - tpre[lo];
+    it.ntl = ntiles;
     const int local = u - tpre[lo] * rtn;
     it.rt = local / ntiles;
     const int tt = local % ntiles;
-    const int cnt = gcnt[lo];
+    const int cnt = gcnt[it.g];
     const int per = ((cnt + ntiles - 1) / ntiles + 7) & ~7;
     it.tok0 = tt * per;
     it.nvalid = min(per, cnt - it.tok0);
-    it.pos0 = gstart[lo] + it.tok0;
+    it.pos0 = gstart[it.g] + it.tok0;
     return it;
 }
 
-// a down item of at most four tokens (FP16 path: MXFP4 or INT4) packs each token's h hi and lo
-// planes into adjacent columns of its 8-token MMA tile, except in the kernel
-// for up to 64 tokens (NT = 8), whose batches hold many down items of five to
-// eight tokens: there both class-1 variants cost registers, and moving those
-// items to class 2 measured slower
-template <int WFMT, int NT>
-__device__ __forceinline__ bool ls_packed(const LsItem &it)
-{
-    return LsCfg<WFMT, NT>::F16 && NT != 8 && !it.gu && it.nvalid <= 4;
-}
-
-// tile class of an item: in the kernel for up to 32 tokens (NT = 4) down items
-// of five to eight tokens take class 2, so that class 1 has one code path (the
-// packed one, which runs gate|up items unchanged)
+// tile class of an item
 template <int WFMT, int NT>
 __device__ __forceinline__ int ls_nti_item(const LsItem &it)
 {
-    const int c = ls_nti<NT>(it.nvalid);
-    return LsCfg<WFMT, NT>::F16 && NT == 4 && !it.gu && it.nvalid > 4 && c == 1 ? 2 : c;
+    return ls_nti<NT>(it.nvalid);
 }
 
 // token of row r of an item: routed positions look it up (tokp: token of each
@@ -834,7 +843,7 @@ __device__ __forceinline__ void ls_combine(const LayerArgs &a, int tt, int f, in
 // the 128-row tile over the whole K.  acc[nt]: [0],[1] = row g, token columns
 // 8nt+2q, +1; [2],[3] = row g+8, same columns.  Returns false when a wait gave
 // up.
-template <int WFMT, int NT, int NTI, bool GU, bool PK>
+template <int WFMT, int NT, int NTI, bool GU>
 __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem &it, uint8_t *smem,
                                                uint64_t *full, uint64_t *empty, uint32_t &rc,
                                                volatile int *abort_flag, float (&acc)[NTI][4])
@@ -842,12 +851,9 @@ __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem 
     using C = LsCfg<WFMT, NT>;
     constexpr bool F16 = C::F16;
     constexpr int RES = C::res_rows(NTI);  // token rows reserved in the stage (per plane)
-    // down items of at most four tokens (PK): the hi and lo planes of token r sit in
-    // rows 2r and 2r+1 of one 8-column MMA tile, so one MMA per K step yields both
-    constexpr bool PACK = PK && !GU && F16;
     constexpr int CH = GU ? C::ch_gu(NTI) : C::ch_dn(NTI);
     constexpr int ROWB = ls_rowb(CH);
-    constexpr int HS_OFF = (GU ? 1 : 2) * RES * ROWB;
+    constexpr int HS_OFF = (GU ? 1 : C::NB_DN) * RES * ROWB;
     constexpr int W_OFF = HS_OFF + (GU ? 0 : C::hsb_dn(NTI));
     const int R = a.R;
     const int lane = threadIdx.x & 31, cw = (threadIdx.x >> 5) - 1;
@@ -931,12 +937,6 @@ __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem 
                                 mma_f16_z(t, af[2 * b], b0, b1);
                                 load_b(pb + (2 * b + 1) * 32, b0, b1);
                                 mma_f16(t, af[2 * b + 1], b0, b1);
-                                if (!GU && !PACK) {
-                                    load_b(pb + RES * ROWB + (2 * b) * 32, b0, b1);
-                                    mma_f16(t, af[2 * b], b0, b1);
-                                    load_b(pb + RES * ROWB + (2 * b + 1) * 32, b0, b1);
-                                    mma_f16(t, af[2 * b + 1], b0, b1);
-                                }
                                 if (GU) {
                                     acc[nt][0] = fmaf(t[0], sg[b], acc[nt][0]);
                                     acc[nt][1] = fmaf(t[1], sg[b], acc[nt][1]);
@@ -957,13 +957,10 @@ __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem 
                         }
                         if (!GU) {
                             // fold in the scale of this 64-feature block of h for each token
-                            // column (columns past the item's tokens hold stale data, discarded);
-                            // packed: columns 2q and 2q+1 are token q's hi and lo planes
+                            // column (columns past the item's tokens hold stale data, discarded)
                             const int r0 = 8 * nt + 2 * q;
-                            const float f0 = PACK ? (q < it.nvalid ? pow2i(hs_st[q * LS_HS_ROW]) : 0.f)
-                                                  : (r0 < it.nvalid ? pow2i(hs_st[r0 * LS_HS_ROW]) : 0.f);
-                            const float f1 = PACK ? f0
-                                                  : (r0 + 1 < it.nvalid ? pow2i(hs_st[(r0 + 1) * LS_HS_ROW]) : 0.f);
+                            const float f0 = r0 < it.nvalid ? pow2i(hs_st[r0 * LS_HS_ROW]) : 0.f;
+                            const float f1 = r0 + 1 < it.nvalid ? pow2i(hs_st[(r0 + 1) * LS_HS_ROW]) : 0.f;
                             acc[nt][0] = fmaf(part[0], f0, acc[nt][0]);
                             acc[nt][1] = fmaf(part[1], f1, acc[nt][1]);
                             acc[nt][2] = fmaf(part[2], f0, acc[nt][2]);
@@ -1016,7 +1013,7 @@ __device__ __forceinline__ bool ls_item_stages(const LayerArgs &a, const LsItem 
 
 // One item of tile class NTI on a compute warp: its stages, then the epilogue
 // (gate|up: SwiGLU and h; down: y).  Returns false when a wait gave up.
-template <int WFMT, int NT, int NTI, bool PK = false>
+template <int WFMT, int NT, int NTI>
 __device__ __forceinline__ bool ls_compute_item(const LayerArgs &a, const LsItem &it, uint8_t *smem, uint64_t *full,
                                                 uint64_t *empty, uint32_t &rc, volatile int *abort_flag,
                                                 const int *sorted, const int *xs_s, float *hmaxb, uint64_t *hmax_bar,
@@ -1028,8 +1025,8 @@ __device__ __forceinline__ bool ls_compute_item(const LayerArgs &a, const LsItem
     const int g = lane >> 2, q = lane & 3;
     const bool gu = it.gu;
     float acc[NTI][4];
-    const bool ok = gu ? ls_item_stages<WFMT, NT, NTI, true, PK>(a, it, smem, full, empty, rc, abort_flag, acc)
-                       : ls_item_stages<WFMT, NT, NTI, false, PK>(a, it, smem, full, empty, rc, abort_flag, acc);
+    const bool ok = gu ? ls_item_stages<WFMT, NT, NTI, true>(a, it, smem, full, empty, rc, abort_flag, acc)
+                       : ls_item_stages<WFMT, NT, NTI, false>(a, it, smem, full, empty, rc, abort_flag, acc);
     if (!ok)
         return false;
 
@@ -1052,8 +1049,9 @@ __device__ __forceinline__ bool ls_compute_item(const LayerArgs &a, const LsItem
                 hv[nt][e] = (tok < it.nvalid && n < a.I) ? __fdividef(gv, 1.0f + __expf(-gv)) * uv : 0.f;
             }
         if (F16) {
-            // h leaves as FP16 hi + lo scaled by 2^-hs, hs per (position, 64-feature block):
-            // block maximum over the 8 features of each warp, then over the 8 warps
+            // h leaves as one FP16 plane scaled by 2^-hs, hs per (position, 64-feature
+            // block): block maximum over the 8 features of each warp, then over the 8
+            // warps; the block's largest value lands in [2^14, 2^15)
             float *hm = hmaxb + (gu_idx & 1) * 8 * C::ROWS;
 #pragma unroll
             for (int nt = 0; nt < NTI; ++nt)
@@ -1084,14 +1082,10 @@ __device__ __forceinline__ bool ls_compute_item(const LayerArgs &a, const LsItem
                     int hsc = m > 0.f ? mb - 127 - 14 : 0;
                     hsc = hsc < -100 ? -100 : (hsc > 100 ? 100 : hsc);
                     if (tok < it.nvalid) {
-                        const float v = hv[nt][e] * pow2i(-hsc);
-                        const __half hb = __float2half_rn(v);
-                        const __half lb = __float2half_rn(v - __half2float(hb));
                         if (n < a.I) {
                             const size_t o =
                                 (size_t)(it.pos0 + tok) * a.I + (n & ~15) + x16_phys_k(n & 15);
-                            a.h[o] = __half_as_ushort(hb);
-                            a.h[o + a.h_plane] = __half_as_ushort(lb);
+                            a.h[o] = __half_as_ushort(__float2half_rn(hv[nt][e] * pow2i(-hsc)));
                         }
                         if (wg == 0 && g == 0)
                             a.hs[(size_t)(it.pos0 + tok) * a.hs_pitch + it.rt] = hsc;
@@ -1125,30 +1119,19 @@ __device__ __forceinline__ bool ls_compute_item(const LayerArgs &a, const LsItem
         }
     } else {
         const int m = it.rt * TILE_ROWS + 16 * wg + g;
-        if (PK && F16) {
-            // token q: its hi column 2q plus its lo column 2q+1
-            if (q < it.nvalid) {
-                float *yrow = a.y + (size_t)(it.pos0 + q) * a.H;
-                if (m < a.H)
-                    yrow[m] = acc[0][0] + acc[0][1];
-                if (m + 8 < a.H)
-                    yrow[m + 8] = acc[0][2] + acc[0][3];
-            }
-        } else {
 #pragma unroll
-            for (int nt = 0; nt < NTI; ++nt)
+        for (int nt = 0; nt < NTI; ++nt)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int tok = 8 * nt + 2 * q + e;
-                    if (tok < it.nvalid) {
-                        float *yrow = a.y + (size_t)(it.pos0 + tok) * a.H;
-                        if (m < a.H)
-                            yrow[m] = acc[nt][e];
-                        if (m + 8 < a.H)
-                            yrow[m + 8] = acc[nt][2 + e];
-                    }
+            for (int e = 0; e < 2; ++e) {
+                const int tok = 8 * nt + 2 * q + e;
+                if (tok < it.nvalid) {
+                    float *yrow = a.y + (size_t)(it.pos0 + tok) * a.H;
+                    if (m < a.H)
+                        yrow[m] = acc[nt][e];
+                    if (m + 8 < a.H)
+                        yrow[m + 8] = acc[nt][2 + e];
                 }
-        }
+            }
     }
     return true;
 }
@@ -1207,6 +1190,18 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
             gdone[i] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async();
+    }
+    // The shared groups (or dense slices) lead the work list and need no
+    // routing, so their gate|up weights start moving into L2 now, while the
+    // tokens are routed: CTA b prefetches the b-th share of the first
+    // LS_PF_BYTES (group bytes and shares are multiples of 16).
+    if (tid == LS_THREADS - 32 && a.E < a.G) {
+        const size_t total = min((size_t)(a.G - a.E) * a.gu_group_bytes, LS_PF_BYTES);
+        const size_t per = (total / gridDim.x + 15) & ~(size_t)15;
+        const size_t lo = per * blockIdx.x, hi = min(lo + per, total);
+        const uint8_t *base = a.wgu + (size_t)a.E * a.gu_group_bytes;
+        for (size_t o = lo; o < hi; o += LS_PF_PIECE)
+            prefetch_l2(base + o, (uint32_t)min((size_t)LS_PF_PIECE, hi - o));
     }
 
     // ---------------------------------------------------------- phase 0a
@@ -1273,14 +1268,14 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
             int nxt = 0;
             if (lane == 0)
                 nxt = (int)gridDim.x + atomicAdd(&a.sync[SY_WORK], 1);
-            const LsItem it = ls_item<ROWS>(u, total_gu, rt_gu, rt_dn, a.G, gcnt, gstart, tpre);
+            const LsItem it = ls_item<ROWS>(u, total_gu, rt_gu, rt_dn, a.E, a.G, gcnt, gstart, tpre);
             const int nti = ls_nti_item<WFMT, NT>(it);  // the item's tile class: its stage geometry
             const int irows = C::res_rows(nti);
             const int CH = it.gu ? C::ch_gu(nti) : C::ch_dn(nti);
             const int kch = it.gu ? a.gu_kchunks : a.dn_kchunks;
             const int nst = (kch + CH - 1) / CH;
             const int K = it.gu ? a.H : a.I;
-            const int nb = it.gu ? 1 : 2;
+            const int nb = it.gu ? 1 : C::NB_DN;
             const int rowb = ls_rowb(CH);
             const int hsb = it.gu ? 0 : C::hsb_dn(nti);
             const int w_off = nb * irows * rowb + hsb;
@@ -1302,7 +1297,8 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
             for (int s = 0; s < nst; ++s, ++rc) {
                 const int slot = rc % R;
                 const uint32_t ph = (rc / R) & 1;
-                if (!(ok = mbar_wait_warp(&empty[slot], ph ^ 1, abort_flag, a.err, lane)))
+                // (a sleeping wait: the loader shares its sub-partition with compute warps)
+                if (!(ok = mbar_wait_sleep_warp(&empty[slot], ph ^ 1, abort_flag, a.err, lane)))
                     break;
                 uint8_t *st = smem + (size_t)slot * C::STAGE;
                 const int ch_n = min(CH, kch - s * CH);
@@ -1334,8 +1330,7 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
                     if (lane == 0) {
                         const uint32_t bit = 1u << (it.g & 31);
                         if (!(gdone[it.g >> 5] & bit)) {
-                            const int ntl = tpre[it.g + 1] - tpre[it.g];
-                            const int target = ntl * rt_gu * 8;
+                            const int target = it.ntl * rt_gu * 8;
                             hok = wait_geq(&grp_done[it.g], target, abort_flag, a.err) ? 1 : 0;
                             if (hok)
                                 gdone[it.g >> 5] |= bit;
@@ -1373,13 +1368,12 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
                 for (int i = 0; i < 2; ++i) {
                     const int r = lane + 32 * i;
                     if (r < it.nvalid) {
-                        // down items of the smallest batches: hi and lo of row r in rows 2r, 2r+1
-                        const bool pack = ls_packed<WFMT, NT>(it);
-                        uint8_t *drow = st + (pack ? 2 * r : r) * rowb;
+                        uint8_t *drow = st + r * rowb;
                         bulk_g2s(drow, src[i] + k0, vb, &full[slot]);
                         if (!it.gu) {
-                            bulk_g2s(pack ? drow + rowb : drow + irows * rowb, src[i] + a.h_plane + k0, vb, &full[slot]);
-                            if (F16)
+                            if (!F16)  // BF16: the lo plane of h
+                                bulk_g2s(drow + irows * rowb, src[i] + a.h_plane + k0, vb, &full[slot]);
+                            else
                                 bulk_g2s(st + nb * irows * rowb + r * LS_HS_ROW * 4,
                                          a.hs + (size_t)pos_r[i] * a.hs_pitch + sl0, (uint32_t)nh * 4, &full[slot]);
                         }
@@ -1419,26 +1413,15 @@ __global__ void __launch_bounds__(LS_THREADS, ls_ctas_per_sm(NT)) layer_stream_k
             const int2 h0 = hdr[slot];
             if (h0.x < 0)
                 break;
-            const LsItem it = ls_item<ROWS>(h0.x, total_gu, rt_gu, rt_dn, a.G, gcnt, gstart, tpre);
+            const LsItem it = ls_item<ROWS>(h0.x, total_gu, rt_gu, rt_dn, a.E, a.G, gcnt, gstart, tpre);
             const int gu_idx = it.gu ? gu_i++ : 0;
             const int nti = ls_nti_item<WFMT, NT>(it);
 #define LS_ITEM(F_, ...)                                                                                      \
     F_<WFMT, NT, __VA_ARGS__>(a, it, smem, full, empty, rc, abort_flag, sorted, xs_s, hmaxb, hmax_bar, gu_idx,   \
                               pub_full, pub_empty, pub_g)
-            if (NT <= 1 || nti == 1) {
-                // class 1: the packed-down variant also runs gate|up items (identical there)
-                if constexpr (NT == 0 || NT == 4) {
-                    ok = LS_ITEM(ls_compute_item, 1, LsCfg<WFMT, NT>::F16);
-                } else if constexpr (NT <= 2) {
-                    constexpr bool PKV = LsCfg<WFMT, NT>::F16;
-                    if (PKV && (it.gu || ls_packed<WFMT, NT>(it)))
-                        ok = LS_ITEM(ls_compute_item, 1, PKV);
-                    else
-                        ok = LS_ITEM(ls_compute_item, 1, false);
-                } else {
-                    ok = LS_ITEM(ls_compute_item, 1, false);
-                }
-            } else if (NT == 2 || nti == 2)
+            if (NT <= 1 || nti == 1)
+                ok = LS_ITEM(ls_compute_item, 1);
+            else if (NT == 2 || nti == 2)
                 ok = LS_ITEM(ls_compute_item_wide, NT < 2 ? 1 : 2);
             else if (NT == 4 || nti == 4)
                 ok = LS_ITEM(ls_compute_item_wide, NT < 4 ? 1 : 4);
