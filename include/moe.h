@@ -25,9 +25,9 @@
  *     workstation", section "MXFP4 is not NVFP4, and the difference matters on
  *     Ampere".  Weights are decoded on chip inside the reduction; no BF16 copy
  *     of an expert is ever written to device memory.  Products accumulate in
- *     FP32; h is kept between the two projections as a hi + lo pair, about
- *     16 significant bits or more: BF16 pairs on the tensor-core path, FP16
- *     pairs with a power-of-two scale per 64 features on the decode path.
+ *     FP32; h is kept between the two projections in FP16 with a power-of-two
+ *     scale (per token on the tensor-core path, per token and 64 features on
+ *     the decode path), or as a BF16 hi + lo pair when the weights are BF16.
  *     Weights may also be BF16, or group-32 INT4 with an FP16 scale and a zero
  *     point per 32 values (the format of "Cascadia" §3.1; MoeWeightFormat).
  *  4. Combine.  out_t = sum_{j<k} w_tj y_{e_tj}(x_t) + sum_shared y_s(x_t) in

@@ -36,8 +36,9 @@
 //     significant bits).  The epilogue multiplies each row's accumulator by
 //     2^(b - 127).  Token rows are FP16 x * 2^-xs (a power of two per token,
 //     chosen so that the conversion of the BF16 values is exact); h leaves
-//     gate|up in FP32 with a per-position maximum, is turned into one FP16
-//     plane with a power of two per position, and down runs one MMA per K step.
+//     gate|up as one FP16 plane h * 2^-hs with a power of two per position
+//     fixed before the GEMM from a bound on |h| (token_prep_f16_kernel), and
+//     down runs one MMA per K step.
 //   BF16: BF16 weights, or MXFP4 whose exponents spread wider.  Weights decode
 //     exactly to BF16 v(c) * 2^(e - 127); tokens are the caller's BF16 rows; h
 //     is kept as BF16 hi + lo planes (lo = bf16(h - hi)), so down runs two MMAs
@@ -105,16 +106,16 @@ struct TcArgs {
     const uint8_t *row_base;  // FP16 operands: largest E8M0 exponent of every row, [G][row_tiles * 128]
     const int *grp_start, *grp_count;
     int E, G, I, H;
-    // gate|up output: BF16 operands h hi + lo planes; FP16 operands FP32 h and per-position maxima
+    // gate|up output: BF16 operands h hi + lo planes; FP16 operands one FP16 plane h16
     uint16_t *h_out;
     long long h_plane;
-    float *h32;
-    int *hmax;
+    uint16_t *h16;
     const int *row_token;  // token of each position
     const int *xsp;        // FP16 operands: power of two of each position's FP16 token row
     // down output
     float *y_out;
-    const int *hsp;        // FP16 operands: per-position power of two of the FP16 h rows
+    const int *hsp;        // FP16 operands: per-position power of two of the FP16 h rows (written by
+                           // gate|up with it, read by down)
     int *err;
     int brows;  // token rows per TMA box of the B operand (16, or 64 when every B tensor has that many rows)
 };
@@ -246,7 +247,8 @@ struct Smem {
     static constexpr int SCHED_OFF = BAR_OFF + N_BARS * 8;
     static constexpr int MISC_OFF = SCHED_OFF + (MAX_GROUPS + 1) * 4;
     static constexpr int COLSC_OFF = MISC_OFF + 32;    // epilogue: column scales of an item, one row per warp
-    static constexpr int TOTAL = COLSC_OFF + N_EPI_WARPS * NMAX * 4 + 1024;  // + alignment slack
+    static constexpr int HSC_OFF = COLSC_OFF + N_EPI_WARPS * NMAX * 4;  // gate|up: h scales, one row per warp
+    static constexpr int TOTAL = HSC_OFF + N_EPI_WARPS * NMAX * 4 + 1024;  // + alignment slack
 };
 
 // ------------------------------------------------------------------ kernel
@@ -565,6 +567,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int eh = (warp - WARP_EPI0) >> 2;   // which column chunks of the quadrant it takes
         // this warp's column scales (FP16 operands), indexed by column
         float *csc = reinterpret_cast<float *>(smem + L::COLSC_OFF) + (warp - WARP_EPI0) * NMAX;
+        float *hsc = reinterpret_cast<float *>(smem + L::HSC_OFF) + (warp - WARP_EPI0) * NMAX;  // gate|up, FP16
         // columns per tensor-memory wait: gate|up 32, down 16
         constexpr int EC = GU ? 32 : 16;
         uint32_t tc = 0;
@@ -577,8 +580,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (OP == OP_F16) {
 #pragma unroll 1
                 for (int i = 0; i < NMAX / (2 * EC); ++i)
-                    for (int c = EC * eh + 2 * EC * i + lane; c < EC * eh + 2 * EC * i + EC && c < w.nvalid; c += 32)
+                    for (int c = EC * eh + 2 * EC * i + lane; c < EC * eh + 2 * EC * i + EC && c < w.nvalid; c += 32) {
                         csc[c] = pow2i(__ldg((GU ? a.xsp : a.hsp) + pos0 + c));
+                        if (GU)
+                            hsc[c] = pow2i(-__ldg(a.hsp + pos0 + c));
+                    }
                 __syncwarp();
             }
             const int buf = tc % NBUF;
@@ -626,21 +632,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             const int tok = c1 + (up_lane ? 8 : 0) + jj;
                             const bool valid = tok < w.nvalid && n < a.I;
                             if (OP == OP_F16) {
-                                // undo the token row's power of two, then FP32 h and the
-                                // position's running maximum of |h|
-                                const float fx = tok < w.nvalid ? csc[tok] : 0.f;
-                                gv *= fx;
-                                uv *= fx;
-                                const float hv = valid ? __fdividef(gv, 1.0f + __expf(-gv)) * uv : 0.f;
-                                if (valid)
-                                    a.h32[(size_t)(pos0 + tok) * a.I + n] = hv;
-                                float m = fabsf(hv);
-                                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-                                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-                                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-                                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-                                if ((lane & 23) == 0 && tok < w.nvalid && m > 0.f)
-                                    atomicMax(a.hmax + pos0 + tok, __float_as_int(m));
+                                // undo the token row's power of two; h leaves in FP16 times
+                                // the position's power of two
+                                if (valid) {
+                                    gv *= csc[tok];
+                                    uv *= csc[tok];
+                                    const float hv = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+                                    a.h16[(size_t)(pos0 + tok) * a.I + n] = __half_as_ushort(__float2half_rn(hv * hsc[tok]));
+                                }
                             } else if (valid) {
                                 const float hv = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
                                 const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
@@ -724,16 +723,11 @@ TcArgs base_args(const Plan &p, const WeightStore &w)
 
 }  // namespace
 
-// x_perm[p] = x[row_token[p]] for the routed positions p < T*k (16-byte copies);
-// with token scales xs given, also xsp[p] = xs[row_token[p]].
+// x_perm[p] = x[row_token[p]] for the routed positions p < T*k (16-byte copies)
 __global__ void gather_rows_kernel(const uint4 *__restrict__ x, const int *__restrict__ row_token, int n_rows,
-                                   int row_vecs, uint4 *__restrict__ out, const int *__restrict__ xs,
-                                   int *__restrict__ xsp)
+                                   int row_vecs, uint4 *__restrict__ out)
 {
     long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (xs)
-        for (long long p = i; p < n_rows; p += (long long)gridDim.x * blockDim.x)
-            xsp[p] = xs[row_token[p]];
     long long total = (long long)n_rows * row_vecs;
     for (; i < total; i += (long long)gridDim.x * blockDim.x) {
         const long long p = i / row_vecs, c = i % row_vecs;
@@ -741,7 +735,7 @@ __global__ void gather_rows_kernel(const uint4 *__restrict__ x, const int *__res
     }
 }
 
-cudaError_t launch_gather_rows(const Plan &p, const uint16_t *x, bool xs_rows, cudaStream_t st)
+cudaError_t launch_gather_rows(const Plan &p, const uint16_t *x, cudaStream_t st)
 {
     const int n = p.T * p.k;
     if (n == 0)
@@ -752,23 +746,55 @@ cudaError_t launch_gather_rows(const Plan &p, const uint16_t *x, bool xs_rows, c
     if (blocks > 4 * 152 * 8)
         blocks = 4 * 152 * 8;
     gather_rows_kernel<<<(unsigned)blocks, 256, 0, st>>>(reinterpret_cast<const uint4 *>(x), p.row_token, n, row_vecs,
-                                                         reinterpret_cast<uint4 *>(p.x_perm), xs_rows ? p.xs : nullptr,
-                                                         p.xsp);
+                                                         reinterpret_cast<uint4 *>(p.x_perm));
     return cudaGetLastError();
 }
 
-// FP16 token rows: xs[t] = floor(log2 max|x_t|) - 14 (0 for an all-zero row,
-// clamped to [-100, 100]) and x16[t] = x_t * 2^-xs[t] in FP16, natural K
-// order.  The largest |x| of a token lands in [2^14, 2^15); a BF16 value has 8
-// significant bits, so the conversion is exact for every element within 2^31
-// of the token's largest.  One CTA per token.
+// FP16 token rows, and the power of two of each position's h.  One CTA per
+// token t.
+//  - xs[t] = floor(log2 max|x_t|) - 14 (0 for an all-zero row, clamped to
+//    [-100, 100]) and x16 = x_t * 2^-xs[t] in FP16, natural K order: the
+//    largest |x| of a token lands in [2^14, 2^15); a BF16 value has 8
+//    significant bits, so the conversion is exact for every element within
+//    2^31 of the token's largest.  The row goes to x16[t] (read by the shared
+//    groups and dense slices) and to x_perm[p] for each routed position p of
+//    the token (slot_pos), so that no separate gather pass reads it back.
+//  - hsp[p]: h = SiLU(g) * u obeys |h| <= |g| |u| (|SiLU(z)| <= |z|) and, by
+//    Cauchy-Schwarz, |g_n| |u_n| <= |x|^2 |w_g,n| |w_u,n|.  With
+//    L_e = max_n log2(|w_g,n| |w_u,n|) over the features of the position's
+//    group (computed at load, see gu_norm_kernel) and log2 |x_t|^2 from the
+//    FP16 row, hsp[p] = ceil(log2 bound + 0.01) - 15 keeps |h| * 2^-hsp below
+//    2^15, inside FP16, before h exists; FP16 keeps 11 significant bits of
+//    every value above 2^-14 in those units.
+//  - xsp[p] = xs[t] for every position of the token.
+__device__ __forceinline__ float ordered_key_to_float(int key)
+{
+    const uint32_t k = (uint32_t)key;
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+__device__ __forceinline__ int h_scale_of(float lx, float lw)
+{
+    const float l = lx + lw;
+    int hs = l > -1000.f ? (int)ceilf(l + 0.01f) - 15 : -100;
+    return hs < -100 ? -100 : (hs > 100 ? 100 : hs);
+}
+
 __global__ void token_prep_f16_kernel(const uint16_t *__restrict__ x, int H, uint16_t *__restrict__ x16,
-                                      int *__restrict__ xs, int *__restrict__ xsp, int n_routed, int T, int S)
+                                      uint16_t *__restrict__ x_perm, int *__restrict__ xs, int *__restrict__ xsp,
+                                      int *__restrict__ hsp, const int *__restrict__ slot_pos,
+                                      const int *__restrict__ topk_ids, const int *__restrict__ gkey, int k, int E,
+                                      int T, int S)
 {
     __shared__ uint32_t red[32];
+    __shared__ float fred[32];
+    __shared__ int pos[32];  // routed positions of this token (k <= 32)
     const int t = blockIdx.x;
+    const int n_routed = T * k;
     const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
     const int nv = H / 8;
+    if ((int)threadIdx.x < k)
+        pos[threadIdx.x] = slot_pos[(size_t)t * k + threadIdx.x];
     uint32_t mx = 0;  // max |x| as BF16 bits without sign (monotonic for finite values)
     for (int i = threadIdx.x; i < nv; i += blockDim.x) {
         const uint4 v = row[i];
@@ -787,12 +813,9 @@ __global__ void token_prep_f16_kernel(const uint16_t *__restrict__ x, int H, uin
         mx = max(mx, red[i]);
     int sc = mx == 0 ? 0 : (int)(mx >> 7) - 127 - 14;
     sc = sc < -100 ? -100 : (sc > 100 ? 100 : sc);
-    if (threadIdx.x == 0)
-        xs[t] = sc;
-    for (int s = threadIdx.x; s < S; s += blockDim.x)  // shared groups / dense slices: position n + s*T + t
-        xsp[(size_t)n_routed + (size_t)s * T + t] = sc;
     const float mul = __int_as_float((127 - sc) << 23);
     uint4 *dst = reinterpret_cast<uint4 *>(x16 + (size_t)t * H);
+    float ss = 0.f;  // sum of squares of the FP16 row (each below 2^30: no overflow at any H here)
     for (int i = threadIdx.x; i < nv; i += blockDim.x) {
         const uint4 v = row[i];
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -801,52 +824,48 @@ __global__ void token_prep_f16_kernel(const uint16_t *__restrict__ x, int H, uin
         for (int j = 0; j < 4; ++j) {
             const __half lo = __float2half_rn(__uint_as_float(w[j] << 16) * mul);
             const __half hi = __float2half_rn(__uint_as_float(w[j] & 0xFFFF0000u) * mul);
+            const float fl = __half2float(lo), fh = __half2float(hi);
+            ss = fmaf(fl, fl, fmaf(fh, fh, ss));
             o[j] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
         }
-        dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+        const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[i] = ov;
+        for (int j = 0; j < k; ++j)
+            reinterpret_cast<uint4 *>(x_perm + (size_t)pos[j] * H)[i] = ov;
+    }
+    for (int o = 16; o > 0; o >>= 1)
+        ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0)
+        fred[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    ss = 0.f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i)
+        ss += fred[i];
+    // log2 |x_t|^2 (the row's FP16 values times 2^xs), rounded up a little for the
+    // FP32 sum's own rounding
+    const float lx = ss > 0.f ? 2.f * (float)sc + __log2f(ss) + 0.01f : -2000.f;
+    if (threadIdx.x == 0)
+        xs[t] = sc;
+    if ((int)threadIdx.x < k) {
+        const int p = pos[threadIdx.x];
+        xsp[p] = sc;
+        hsp[p] = h_scale_of(lx, ordered_key_to_float(gkey[topk_ids[(size_t)t * k + threadIdx.x]]));
+    }
+    for (int s = threadIdx.x; s < S; s += blockDim.x) {  // shared groups / dense slices: position n + s*T + t
+        const size_t p = (size_t)n_routed + (size_t)s * T + t;
+        xsp[p] = sc;
+        hsp[p] = h_scale_of(lx, ordered_key_to_float(gkey[E + s]));
     }
 }
 
-// One FP16 plane of h with a power of two per position: hsp[p] =
-// floor(log2 max_n |h_pn|) - 14 (0 when the row is zero), h16[p][n] =
-// h32[p][n] * 2^-hsp[p].  One warp per position.
-__global__ void h_convert_kernel(const float *__restrict__ h32, const int *__restrict__ hmax, int P, int I,
-                                 uint16_t *__restrict__ h16, int *__restrict__ hsp)
-{
-    const int p = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (p >= P)
-        return;
-    const float m = __int_as_float(hmax[p]);
-    int sc = m > 0.f ? (int)((__float_as_uint(m) >> 23) & 0xFFu) - 127 - 14 : 0;
-    sc = sc < -100 ? -100 : (sc > 100 ? 100 : sc);
-    if (lane == 0)
-        hsp[p] = sc;
-    const float mul = __int_as_float((127 - sc) << 23);
-    const float4 *src = reinterpret_cast<const float4 *>(h32 + (size_t)p * I);
-    uint2 *dst = reinterpret_cast<uint2 *>(h16 + (size_t)p * I);
-    for (int i = lane; i < I / 4; i += 32) {
-        const float4 v = src[i];
-        const __half2 a = __floats2half2_rn(v.x * mul, v.y * mul);
-        const __half2 b = __floats2half2_rn(v.z * mul, v.w * mul);
-        dst[i] = make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&b));
-    }
-}
-
-cudaError_t launch_token_prep_f16(const Plan &p, const uint16_t *x, cudaStream_t st)
+cudaError_t launch_token_prep_f16(const Plan &p, const uint16_t *x, const int *gu_norm_key, cudaStream_t st)
 {
     if (p.T == 0)
         return cudaSuccess;
-    token_prep_f16_kernel<<<p.T, 256, 0, st>>>(x, p.H, p.x16, p.xs, p.xsp, p.T * p.k, p.T, p.S);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_h_convert(const Plan &p, cudaStream_t st)
-{
-    if (p.P == 0)
-        return cudaSuccess;
-    h_convert_kernel<<<(unsigned)((p.P + 7) / 8), 256, 0, st>>>(reinterpret_cast<const float *>(p.h), p.hmax, p.P,
-                                                               p.I, p.h16, p.hsp);
+    if (p.k > 32)
+        return cudaErrorInvalidValue;
+    token_prep_f16_kernel<<<p.T, 256, 0, st>>>(x, p.H, p.x16, p.x_perm, p.xs, p.xsp, p.hsp, p.slot_pos, p.topk_ids,
+                                               gu_norm_key, p.k, p.E, p.T, p.S);
     return cudaGetLastError();
 }
 
@@ -856,8 +875,8 @@ cudaError_t launch_gemm_gate_up_tc(const Plan &p, const WeightStore &w, int fmt,
     TcArgs a = base_args(p, w);
     a.h_out = p.h;
     a.h_plane = (long long)p.P * p.I;
-    a.h32 = reinterpret_cast<float *>(p.h);
-    a.hmax = p.hmax;
+    a.h16 = p.h16;
+    a.hsp = p.hsp;
     a.xsp = p.xsp;
     a.brows = p.T >= B_BOX_ROWS_BIG && (p.T * p.k == 0 || p.T * p.k >= B_BOX_ROWS_BIG) ? B_BOX_ROWS_BIG
                                                                                        : B_BOX_ROWS_SMALL;

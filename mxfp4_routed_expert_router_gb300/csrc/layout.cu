@@ -60,6 +60,57 @@ __device__ __forceinline__ uint16_t src_bf16(const SrcMat *src, int srow, int k,
     return reinterpret_cast<const uint16_t *>(src->codes + srow * src->code_stride)[k];
 }
 
+// One warp per feature n of a gate|up matrix: log2 |w_g,n|^2 and log2 |w_u,n|^2
+// of the decoded MXFP4 rows, each sum taken in double against the row's largest
+// exponent (no underflow of small blocks, no overflow of large ones); their
+// mean, rounded up by 2^-10, goes into out as an order-preserving integer key
+// with atomicMax.  An all-zero row counts as log2 = -2000.
+__global__ void gu_norm_kernel(SrcMat gate, SrcMat up, int I, int K, unsigned *out)
+{
+    const int n = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (n >= I)
+        return;
+    float l2[2];
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+        const SrcMat &src = m == 0 ? gate : up;
+        const uint8_t *sc = src.scales + (long long)n * src.scale_stride;
+        const uint8_t *cd = src.codes + (long long)n * src.code_stride;
+        int emax = 0;
+        for (int b = lane; b < K / 32; b += 32)
+            emax = max(emax, (int)sc[b]);
+        for (int o = 16; o > 0; o >>= 1)
+            emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
+        // sum over blocks of 4^(e_b - emax) * sum_i v(c_i)^2, v^2 in units of 1/4
+        double acc = 0.0;
+        for (int b = lane; b < K / 32; b += 32) {
+            int q = 0;  // sum of (2 v)^2 over the block: v in {0, .5, 1, 1.5, 2, 3, 4, 6}
+            for (int i = 0; i < 16; ++i) {
+                // (2v)^2 of the magnitude indices 0..7, one byte each: 0, 1, 4, 9, 16, 36, 64, 144
+                constexpr unsigned long long SQ = 0x9040241009040100ull;
+                const uint8_t byte = cd[b * 16 + i];
+                q += (int)((SQ >> (8 * (byte & 7))) & 0xFFu) + (int)((SQ >> (8 * ((byte >> 4) & 7))) & 0xFFu);
+            }
+            acc += ldexp((double)q * 0.25, 2 * ((int)sc[b] - emax));
+        }
+        for (int o = 16; o > 0; o >>= 1)
+            acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        l2[m] = acc > 0.0 ? (float)(log2(acc) + 2.0 * (emax - 127)) : -2000.f;
+    }
+    if (lane == 0) {
+        const float v = 0.5f * (l2[0] + l2[1]) + 0.001f;
+        const uint32_t b = __float_as_uint(v);
+        atomicMax(out, (b & 0x80000000u) ? ~b : (b | 0x80000000u));
+    }
+}
+
+cudaError_t launch_gu_norm(const SrcMat &gate, const SrcMat &up, int group, int I, int H, int *out, cudaStream_t st)
+{
+    gu_norm_kernel<<<(unsigned)((I + 7) / 8), 256, 0, st>>>(gate, up, I, H, reinterpret_cast<unsigned *>(out) + group);
+    return cudaGetLastError();
+}
+
 // Source matrix and row of tile row r of row tile `tile` (row order in moe_internal.cuh).
 __device__ __forceinline__ const SrcMat *tile_row_source(int gate_up, const SrcMat *gate, const SrcMat *up,
                                                          int tile, int r, int logical_rows, int *srow)

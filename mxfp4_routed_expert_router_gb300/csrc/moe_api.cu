@@ -25,6 +25,7 @@ struct MoeHandle {
     int device = 0;
     WeightStore gu, dn;        // TILE or TILE_F16 layout (tensor-memory GEMMs, large batches)
     bool tc_f16 = false;       // the tensor-memory GEMMs run FP16 operands (TILE_F16 store with row bases)
+    int *gu_norm_key = nullptr;  // FP16 operands: per group, key of max_n log2(|w_g,n| |w_u,n|) (device)
     WeightStore gu_f, dn_f;    // FRAG layout (register-streaming GEMMs, decode-sized batches)
     int *err_host = nullptr;   // mapped pinned host memory, written by kernels on device-side errors
     int *err_dev = nullptr;    // device alias of err_host
@@ -94,6 +95,7 @@ size_t plan_layout(const MoeHandle *h, int T, int k, char *base, Plan *p)
     q.topk_ids = (int *)take(sizeof(int) * (n > 0 ? n : 1));
     q.topk_w = (float *)take(sizeof(float) * (n > 0 ? n : 1));
     q.counts = (int *)take(sizeof(int) * (E > 0 ? E : 1));
+    q.chunk_cnt = (int *)take(sizeof(int) * (size_t)((n + 1023) / 1024 + 1) * (E > 0 ? E : 1));
     q.expert_offsets = (int *)take(sizeof(int) * (E + 1));
     q.sorted_slot = (int *)take(sizeof(int) * (n > 0 ? n : 1));
     q.slot_pos = (int *)take(sizeof(int) * (n > 0 ? n : 1));
@@ -107,7 +109,6 @@ size_t plan_layout(const MoeHandle *h, int T, int k, char *base, Plan *p)
     q.hs = (int *)take(sizeof(int) * (size_t)P * q.hs_pitch);
     q.h = (uint16_t *)take(2 * sizeof(uint16_t) * (size_t)P * I);
     q.h16 = (uint16_t *)take(sizeof(uint16_t) * (size_t)P * I);
-    q.hmax = (int *)take(sizeof(int) * (size_t)P);
     q.hsp = (int *)take(sizeof(int) * (size_t)P);
     q.xsp = (int *)take(sizeof(int) * (size_t)P);
     q.y = (float *)take(sizeof(float) * (size_t)P * H);
@@ -188,25 +189,20 @@ MoeStatus run_layer(MoeHandle *h, const void *x, const float *logits, const int 
     }
     const uint16_t *xb = (const uint16_t *)x;
     if (h->tc_f16) {
-        // FP16 operands: FP16 token rows with a power of two per token, gathered
-        // into position order; h as FP32 with per-position maxima, then one FP16
-        // plane with a power of two per position
-        if ((e = launch_token_prep_f16(p, xb, st)) != cudaSuccess)
+        // FP16 operands: FP16 token rows with a power of two per token, written
+        // in token and in position order by one pass, with the power of two of
+        // each position's h (from a bound on |h|); gate|up writes one FP16 plane
+        // of h, which down reads
+        if ((e = launch_token_prep_f16(p, xb, h->gu_norm_key, st)) != cudaSuccess)
             return cuda_fail(e, "token prep launch");
-        if ((e = launch_gather_rows(p, p.x16, true, st)) != cudaSuccess)
-            return cuda_fail(e, "gather launch");
         mark(2);
-        if ((e = cudaMemsetAsync(p.hmax, 0, sizeof(int) * (size_t)p.P, st)) != cudaSuccess)
-            return cuda_fail(e, "h maxima clear");
         if ((e = launch_gemm_gate_up_tc(p, h->gu, h->fmt, true, p.x16, st)) != cudaSuccess)
             return cuda_fail(e, "gate/up launch");
-        if ((e = launch_h_convert(p, st)) != cudaSuccess)
-            return cuda_fail(e, "h conversion launch");
         mark(3);
         if ((e = launch_gemm_down_tc(p, h->dn, h->fmt, true, st)) != cudaSuccess)
             return cuda_fail(e, "down launch");
     } else {
-        if ((e = launch_gather_rows(p, xb, false, st)) != cudaSuccess)
+        if ((e = launch_gather_rows(p, xb, st)) != cudaSuccess)
             return cuda_fail(e, "gather launch");
         mark(2);
         if ((e = launch_gemm_gate_up_tc(p, h->gu, h->fmt, false, xb, st)) != cudaSuccess)
@@ -233,6 +229,8 @@ void destroy(MoeHandle *h)
         cudaFree(h->gu.base);
     if (h->dn.base)
         cudaFree(h->dn.base);
+    if (h->gu_norm_key)
+        cudaFree(h->gu_norm_key);
     if (h->gu.row_base)
         cudaFree(h->gu.row_base);
     if (h->dn.row_base)
@@ -400,17 +398,23 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
     int tile_layout = LAYOUT_TILE;
     if (tile && fmt == FMT_MXFP4) {
         const size_t gu_rb = (size_t)h->gu.row_tiles * TILE_ROWS * G, dn_rb = (size_t)h->dn.row_tiles * TILE_ROWS * G;
-        if (cudaMalloc(&h->gu.row_base, gu_rb) != cudaSuccess || cudaMalloc(&h->dn.row_base, dn_rb) != cudaSuccess) {
+        if (cudaMalloc(&h->gu.row_base, gu_rb) != cudaSuccess || cudaMalloc(&h->dn.row_base, dn_rb) != cudaSuccess ||
+            cudaMalloc(&h->gu_norm_key, sizeof(int) * (size_t)G) != cudaSuccess) {
             cudaGetLastError();
             destroy(h);
             return fail(MOE_ENOMEM, "device allocation of %zu bytes of row bases failed", gu_rb + dn_rb);
+        }
+        if ((e = cudaMemsetAsync(h->gu_norm_key, 0, sizeof(int) * (size_t)G, st)) != cudaSuccess) {
+            destroy(h);
+            return cuda_fail(e, "norm key clear");
         }
         int *wide = &h->err_dev[2];
         for (int g = 0; g < G; ++g) {
             SrcMat gate{}, up{}, dn{};
             sources(g, gate, up, dn);
             if ((e = launch_row_base(true, gate, up, h->gu, g, I, c.hidden, wide, st)) != cudaSuccess ||
-                (e = launch_row_base(false, dn, dn, h->dn, g, I, c.hidden, wide, st)) != cudaSuccess) {
+                (e = launch_row_base(false, dn, dn, h->dn, g, I, c.hidden, wide, st)) != cudaSuccess ||
+                (e = launch_gu_norm(gate, up, g, I, c.hidden, h->gu_norm_key, st)) != cudaSuccess) {
                 destroy(h);
                 return cuda_fail(e, "row base launch");
             }
@@ -425,7 +429,9 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
         } else {
             cudaFree(h->gu.row_base);
             cudaFree(h->dn.row_base);
+            cudaFree(h->gu_norm_key);
             h->gu.row_base = h->dn.row_base = nullptr;
+            h->gu_norm_key = nullptr;
         }
     }
     for (int g = 0; g < G; ++g) {

@@ -134,6 +134,8 @@ struct Plan {
     int *topk_ids;            // [T*k]
     float *topk_w;            // [T*k]
     int *counts;              // [max(E,1)]
+    int *chunk_cnt;           // [ceil(T*k/1024)][E] per-chunk expert counts of the permutation (NULL: the
+                              // one-CTA-per-expert permutation kernel, which needs no such scratch)
     int *expert_offsets;      // [E+1]
     int *sorted_slot;         // [T*k]
     int *slot_pos;            // [T*k]
@@ -148,10 +150,9 @@ struct Plan {
     int *xs;                  // [T] per-token power-of-two scale exponent of x16
     int *xsp;                 // [P] tcgen05 FP16 path: xs of each position's token
     uint16_t *h;              // [2][P][I] h = hi plane + lo plane: BF16 (lo = bf16(h - hi)); on the FP16
-                              // streaming path FP16 (h * 2^-hs = hi + lo); x16 K order on the streaming path.
-                              // The tcgen05 path with FP16 operands keeps FP32 h [P][I] here instead.
+                              // streaming path the first plane only, FP16 h * 2^-hs; x16 K order on the
+                              // streaming path.
     uint16_t *h16;            // [P][I] tcgen05 FP16 path: FP16 h * 2^-hsp[p]
-    int *hmax;                // [P] tcgen05 FP16 path: largest |h| of each position (float bits), zeroed per call
     int *hsp;                 // [P] tcgen05 FP16 path: power of two of each position's h16 row
     int *hs;                  // [P][hs_pitch] FP16 streaming path: power-of-two scale of each position's
                               // 64-feature block of h
@@ -195,9 +196,8 @@ cudaError_t launch_dense_plan(const Plan &p, cudaStream_t st);
 
 cudaError_t launch_combine(const Plan &p, float *out, int accumulate, cudaStream_t st);
 
-// x_perm[p] = x[row_token[p]] for the routed positions; with xs_rows (x is the
-// FP16 token rows x16) also p.xsp[p] = p.xs[row_token[p]]
-cudaError_t launch_gather_rows(const Plan &p, const uint16_t *x, bool xs_rows, cudaStream_t st);
+// x_perm[p] = x[row_token[p]] for the routed positions (BF16 operands)
+cudaError_t launch_gather_rows(const Plan &p, const uint16_t *x, cudaStream_t st);
 
 // row bases of a TILE_F16 store for one group: for every tile row, the
 // largest E8M0 exponent over the row's K; a row whose exponents span more than
@@ -205,11 +205,18 @@ cudaError_t launch_gather_rows(const Plan &p, const uint16_t *x, bool xs_rows, c
 cudaError_t launch_row_base(bool gate_up, const SrcMat &gate, const SrcMat &up, const WeightStore &ws, int group,
                             int I, int H, int *wide, cudaStream_t st);
 
-// tcgen05 path with FP16 operands: FP16 token rows x16 and their powers of two xs
-cudaError_t launch_token_prep_f16(const Plan &p, const uint16_t *x, cudaStream_t st);
+// For the h scales of the tcgen05 path with FP16 operands: out[group] = an
+// order-preserving integer key of max_n log2(|w_g,n| |w_u,n|) over the
+// features n of one group (Euclidean norms of the decoded gate and up rows of
+// an MXFP4 matrix, rounded up; unsigned order of the key bits); out[group]
+// must start at 0
+cudaError_t launch_gu_norm(const SrcMat &gate, const SrcMat &up, int group, int I, int H, int *out,
+                           cudaStream_t st);
 
-// tcgen05 path with FP16 operands: FP32 h (in p.h) -> FP16 h16 with per-position powers of two
-cudaError_t launch_h_convert(const Plan &p, cudaStream_t st);
+// tcgen05 path with FP16 operands (after the permutation): FP16 token rows x16,
+// their copies in routed position order (x_perm), the powers of two xs / xsp,
+// and the per-position h scales hsp from gu_norm_key (one key per group)
+cudaError_t launch_token_prep_f16(const Plan &p, const uint16_t *x, const int *gu_norm_key, cudaStream_t st);
 
 // f16: FP16 operands (TILE_F16 MXFP4 store, token rows x_rows = x16 and the
 // gathered FP16 rows in x_perm); otherwise BF16 operands (x_rows = the caller's x)

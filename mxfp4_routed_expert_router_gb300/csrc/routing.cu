@@ -351,9 +351,159 @@ __global__ void permute_kernel(const int *__restrict__ ids, int T, int k, int E,
         atomicCAS(err, 0, DEV_ERR_PERMUTE_COUNT);
 }
 
+// Chunked stable counting sort (moe_forward's path): the slots are cut into
+// chunks of PERM_CHUNK; one kernel counts each chunk's slots per expert, a
+// second gives every chunk its starting position per expert (slots of the
+// experts below, then of the same expert in earlier chunks) and places the
+// chunk's slots in slot order.  Integer counts only: the result equals the
+// one-CTA-per-expert kernel above, bit for bit.
+constexpr int PERM_CHUNK = 1024;
+constexpr int PERM_CT = 256;                    // threads of the chunked kernels
+constexpr int PERM_CW = PERM_CT / 32;           // warps
+constexpr int PERM_WSLOTS = PERM_CHUNK / PERM_CW;  // consecutive slots per warp
+
+__global__ void chunk_hist_kernel(const int *__restrict__ ids, int n, int E, int *__restrict__ chunk_cnt)
+{
+    extern __shared__ int h[];
+    for (int i = threadIdx.x; i < E; i += blockDim.x)
+        h[i] = 0;
+    __syncthreads();
+    const int s0 = blockIdx.x * PERM_CHUNK, s1 = min(n, s0 + PERM_CHUNK);
+    for (int s = s0 + threadIdx.x; s < s1; s += blockDim.x) {
+        const int e = ids[s];
+        if ((unsigned)e < (unsigned)E)
+            atomicAdd(&h[e], 1);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < E; i += blockDim.x)
+        chunk_cnt[(size_t)blockIdx.x * E + i] = h[i];
+}
+
+__global__ void chunk_scatter_kernel(const int *__restrict__ ids, int T, int k, int E, int S, int nchunks,
+                                     const int *__restrict__ chunk_cnt, int *__restrict__ counts,
+                                     int *__restrict__ expert_offsets, int *__restrict__ sorted_slot,
+                                     int *__restrict__ slot_pos, int *__restrict__ grp_start,
+                                     int *__restrict__ grp_count, int *__restrict__ row_token, int *err)
+{
+    extern __shared__ int sm[];
+    int *base = sm;            // [E]  first position of this chunk's slots of expert e
+    int *wc = sm + E;          // [PERM_CW][E]  per-warp counts, then per-warp running positions
+    __shared__ int wsum[PERM_CW];
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int n = T * k, c = blockIdx.x;
+    // per expert: all slots (tot) and those of earlier chunks (pre); this thread
+    // takes experts [e0, e1) for the scan
+    const int per = (E + PERM_CT - 1) / PERM_CT;
+    const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+    int mytot = 0;
+    for (int e = e0; e < e1; ++e) {
+        int tot = 0, pre = 0;
+        for (int cc = 0; cc < nchunks; ++cc) {
+            const int v = chunk_cnt[(size_t)cc * E + e];
+            tot += v;
+            pre += cc < c ? v : 0;
+        }
+        base[e] = tot;
+        wc[e] = pre;
+        mytot += tot;
+    }
+    // exclusive scan of the totals over experts
+    int incl = mytot;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += v;
+    }
+    if (lane == 31)
+        wsum[wid] = incl;
+    __syncthreads();
+    int run = incl - mytot;
+    for (int w = 0; w < wid; ++w)
+        run += wsum[w];
+    int grand = 0;
+    for (int w = 0; w < PERM_CW; ++w)
+        grand += wsum[w];
+    for (int e = e0; e < e1; ++e) {
+        const int tot = base[e];
+        if (c == 0) {
+            counts[e] = tot;
+            expert_offsets[e] = run;
+            grp_start[e] = run;
+            grp_count[e] = tot;
+        }
+        base[e] = run + wc[e];
+        run += tot;
+    }
+    if (c == 0 && tid == 0) {
+        expert_offsets[E] = grand;
+        if (grand != n)
+            atomicCAS(err, 0, DEV_ERR_PERMUTE_COUNT);
+    }
+    if (c == 0)
+        for (int s = tid; s < S; s += blockDim.x) {
+            grp_start[E + s] = n + s * T;
+            grp_count[E + s] = T;
+        }
+    for (long long i = (long long)c * blockDim.x + tid; i < (long long)S * T; i += (long long)nchunks * blockDim.x)
+        row_token[n + i] = (int)(i % T);
+    __syncthreads();
+    // per-warp counts of the chunk, then each warp's first position per expert
+    const int ws0 = c * PERM_CHUNK + wid * PERM_WSLOTS, ws1 = min(n, ws0 + PERM_WSLOTS);
+    int *my = wc + wid * E;
+    for (int e = lane; e < E; e += 32)
+        my[e] = 0;
+    __syncwarp();
+    for (int s = ws0 + lane; s < ws1; s += 32) {
+        const int e = ids[s];
+        if ((unsigned)e < (unsigned)E)
+            atomicAdd(&my[e], 1);
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += blockDim.x) {
+        int r = base[e];
+        for (int w = 0; w < PERM_CW; ++w) {
+            const int v = wc[w * E + e];
+            wc[w * E + e] = r;
+            r += v;
+        }
+    }
+    __syncthreads();
+    // each warp places its slots in order, 32 at a time
+    for (int b = ws0; b < ws1; b += 32) {
+        const int s = b + lane;
+        const bool act = s < ws1;
+        const int e = act ? ids[s] : -1;
+        const bool ok = act && (unsigned)e < (unsigned)E;
+        const unsigned m = __match_any_sync(0xffffffffu, ok ? e : -1);
+        if (ok) {
+            const int pos = my[e] + __popc(m & ((1u << lane) - 1u));
+            sorted_slot[pos] = s;
+            slot_pos[s] = pos;
+            row_token[pos] = s / k;
+        } else if (act) {
+            atomicCAS(err, 0, DEV_ERR_PERMUTE_COUNT);
+        }
+        __syncwarp();
+        if (ok && lane == 31 - __clz(m))
+            my[e] += __popc(m);
+        __syncwarp();
+    }
+}
+
 cudaError_t launch_permute(const Plan &p, cudaStream_t st)
 {
     const int n = p.T * p.k;
+    if (p.chunk_cnt && p.E > 0 && n > 0) {
+        const int nchunks = (n + PERM_CHUNK - 1) / PERM_CHUNK;
+        chunk_hist_kernel<<<nchunks, PERM_CT, p.E * sizeof(int), st>>>(p.topk_ids, n, p.E, p.chunk_cnt);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return e;
+        chunk_scatter_kernel<<<nchunks, PERM_CT, (1 + PERM_CW) * p.E * sizeof(int), st>>>(
+            p.topk_ids, p.T, p.k, p.E, p.S, nchunks, p.chunk_cnt, p.counts, p.expert_offsets, p.sorted_slot,
+            p.slot_pos, p.grp_start, p.grp_count, p.row_token, p.err);
+        return cudaGetLastError();
+    }
     if (p.E > 0 && n > 0) {
         int blocks = (n + 1023) / 1024;
         if (blocks > 296)
