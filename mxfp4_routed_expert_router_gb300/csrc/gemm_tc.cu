@@ -38,7 +38,9 @@
 //     chosen so that the conversion of the BF16 values is exact); h leaves
 //     gate|up as one FP16 plane h * 2^-hs with a power of two per position
 //     fixed before the GEMM from a bound on |h| (token_prep_f16_kernel), and
-//     down runs one MMA per K step.
+//     down runs one MMA per K step and writes y as FP16 with a power of two
+//     per position from a bound on |y| (half the bytes of FP32 y for the
+//     combine to read).
 //   BF16: BF16 weights, or MXFP4 whose exponents spread wider.  Weights decode
 //     exactly to BF16 v(c) * 2^(e - 127); tokens are the caller's BF16 rows; h
 //     is kept as BF16 hi + lo planes (lo = bf16(h - hi)), so down runs two MMAs
@@ -112,8 +114,10 @@ struct TcArgs {
     uint16_t *h16;
     const int *row_token;  // token of each position
     const int *xsp;        // FP16 operands: power of two of each position's FP16 token row
-    // down output
+    // down output: BF16 operands FP32 y; FP16 operands FP16 y16 with a power of two per position
     float *y_out;
+    uint16_t *y16;
+    const int *ys;
     const int *hsp;        // FP16 operands: per-position power of two of the FP16 h rows (written by
                            // gate|up with it, read by down)
     int *err;
@@ -581,9 +585,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll 1
                 for (int i = 0; i < NMAX / (2 * EC); ++i)
                     for (int c = EC * eh + 2 * EC * i + lane; c < EC * eh + 2 * EC * i + EC && c < w.nvalid; c += 32) {
-                        csc[c] = pow2i(__ldg((GU ? a.xsp : a.hsp) + pos0 + c));
-                        if (GU)
+                        if (GU) {
+                            csc[c] = pow2i(__ldg(a.xsp + pos0 + c));
                             hsc[c] = pow2i(-__ldg(a.hsp + pos0 + c));
+                        } else {
+                            // the h row's power of two over the y row's
+                            csc[c] = pow2i(__ldg(a.hsp + pos0 + c) - __ldg(a.ys + pos0 + c));
+                        }
                     }
                 __syncwarp();
             }
@@ -653,9 +661,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const int m = rt * TILE_ROWS + row;
 #pragma unroll
                         for (int jj = 0; jj < 16; ++jj) {
-                            if (m < a.H && c1 + jj < w.nvalid)
-                                a.y_out[(size_t)(pos0 + c1 + jj) * a.H + m] =
-                                    OP == OP_F16 ? v[jj] * wsc * csc[c1 + jj] : v[jj];
+                            if (m < a.H && c1 + jj < w.nvalid) {
+                                const size_t o = (size_t)(pos0 + c1 + jj) * a.H + m;
+                                if (OP == OP_F16)
+                                    a.y16[o] = __half_as_ushort(__float2half_rn(v[jj] * wsc * csc[c1 + jj]));
+                                else
+                                    a.y_out[o] = v[jj];
+                            }
                         }
                     }
                 }
@@ -766,6 +778,8 @@ cudaError_t launch_gather_rows(const Plan &p, const uint16_t *x, cudaStream_t st
 //    FP16 row, hsp[p] = ceil(log2 bound + 0.01) - 15 keeps |h| * 2^-hsp below
 //    2^15, inside FP16, before h exists; FP16 keeps 11 significant bits of
 //    every value above 2^-14 in those units.
+//  - ys[p]: the power of two of the position's FP16 y row (y_scale_of), from
+//    the same h bound and the load-time row norms of the down matrix.
 //  - xsp[p] = xs[t] for every position of the token.
 __device__ __forceinline__ float ordered_key_to_float(int key)
 {
@@ -780,11 +794,24 @@ __device__ __forceinline__ int h_scale_of(float lx, float lw)
     return hs < -100 ? -100 : (hs > 100 ? 100 : hs);
 }
 
+// Power of two of a position's FP16 y row: |y_m| <= |h| |w_d,m| <= sqrt(I) *
+// max|h| * max_m |w_d,m|, and max|h| <= 2^(hs + 15), so ys = hs + ceil(log2
+// sqrt(I) + ld + 0.01) keeps |y| * 2^-ys below 2^15 (ld = max_m log2 |w_d,m| of
+// the group), clamped so that 2^ys and 2^(hs - ys) stay normal FP32 numbers.
+__device__ __forceinline__ int y_scale_of(int hs, int I, float ld)
+{
+    const float l = 0.5f * __log2f((float)I) + ld;
+    int ys = l > -1000.f ? hs + (int)ceilf(l + 0.01f) : hs - 126;
+    ys = ys < hs - 126 ? hs - 126 : (ys > hs + 126 ? hs + 126 : ys);
+    return ys < -126 ? -126 : (ys > 126 ? 126 : ys);
+}
+
 __global__ void token_prep_f16_kernel(const uint16_t *__restrict__ x, int H, uint16_t *__restrict__ x16,
                                       uint16_t *__restrict__ x_perm, int *__restrict__ xs, int *__restrict__ xsp,
                                       int *__restrict__ hsp, const int *__restrict__ slot_pos,
-                                      const int *__restrict__ topk_ids, const int *__restrict__ gkey, int k, int E,
-                                      int T, int S)
+                                      const int *__restrict__ topk_ids, const int *__restrict__ gkey,
+                                      const int *__restrict__ dkey, int *__restrict__ ys, int I, int k, int E, int T,
+                                      int S)
 {
     __shared__ uint32_t red[32];
     __shared__ float fred[32];
@@ -848,24 +875,30 @@ __global__ void token_prep_f16_kernel(const uint16_t *__restrict__ x, int H, uin
         xs[t] = sc;
     if ((int)threadIdx.x < k) {
         const int p = pos[threadIdx.x];
+        const int e = topk_ids[(size_t)t * k + threadIdx.x];
+        const int hs = h_scale_of(lx, ordered_key_to_float(gkey[e]));
         xsp[p] = sc;
-        hsp[p] = h_scale_of(lx, ordered_key_to_float(gkey[topk_ids[(size_t)t * k + threadIdx.x]]));
+        hsp[p] = hs;
+        ys[p] = y_scale_of(hs, I, ordered_key_to_float(dkey[e]));
     }
     for (int s = threadIdx.x; s < S; s += blockDim.x) {  // shared groups / dense slices: position n + s*T + t
         const size_t p = (size_t)n_routed + (size_t)s * T + t;
+        const int hs = h_scale_of(lx, ordered_key_to_float(gkey[E + s]));
         xsp[p] = sc;
-        hsp[p] = h_scale_of(lx, ordered_key_to_float(gkey[E + s]));
+        hsp[p] = hs;
+        ys[p] = y_scale_of(hs, I, ordered_key_to_float(dkey[E + s]));
     }
 }
 
-cudaError_t launch_token_prep_f16(const Plan &p, const uint16_t *x, const int *gu_norm_key, cudaStream_t st)
+cudaError_t launch_token_prep_f16(const Plan &p, const uint16_t *x, const int *gu_norm_key, const int *dn_norm_key,
+                                  cudaStream_t st)
 {
     if (p.T == 0)
         return cudaSuccess;
     if (p.k > 32)
         return cudaErrorInvalidValue;
     token_prep_f16_kernel<<<p.T, 256, 0, st>>>(x, p.H, p.x16, p.x_perm, p.xs, p.xsp, p.hsp, p.slot_pos, p.topk_ids,
-                                               gu_norm_key, p.k, p.E, p.T, p.S);
+                                               gu_norm_key, dn_norm_key, p.ys, p.I, p.k, p.E, p.T, p.S);
     return cudaGetLastError();
 }
 
@@ -897,6 +930,8 @@ cudaError_t launch_gemm_down_tc(const Plan &p, const WeightStore &w, int fmt, bo
 {
     TcArgs a = base_args(p, w);
     a.y_out = p.y;
+    a.y16 = reinterpret_cast<uint16_t *>(p.y);
+    a.ys = p.ys;
     a.hsp = p.hsp;
     a.brows = p.P >= B_BOX_ROWS_BIG ? B_BOX_ROWS_BIG : B_BOX_ROWS_SMALL;
     CUtensorMap m1, m2;

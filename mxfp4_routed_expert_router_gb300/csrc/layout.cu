@@ -60,12 +60,14 @@ __device__ __forceinline__ uint16_t src_bf16(const SrcMat *src, int srow, int k,
     return reinterpret_cast<const uint16_t *>(src->codes + srow * src->code_stride)[k];
 }
 
-// One warp per feature n of a gate|up matrix: log2 |w_g,n|^2 and log2 |w_u,n|^2
-// of the decoded MXFP4 rows, each sum taken in double against the row's largest
-// exponent (no underflow of small blocks, no overflow of large ones); their
-// mean, rounded up by 2^-10, goes into out as an order-preserving integer key
-// with atomicMax.  An all-zero row counts as log2 = -2000.
-__global__ void gu_norm_kernel(SrcMat gate, SrcMat up, int I, int K, unsigned *out)
+// One warp per row n of a pair of MXFP4 matrices (gate and up rows of one
+// feature; or a down row twice): log2 |a_n|^2 and log2 |b_n|^2 of the decoded
+// rows, each sum taken in double against the row's largest exponent (no
+// underflow of small blocks, no overflow of large ones); `scale` times their
+// sum, rounded up by 2^-10, goes into out as an order-preserving key with
+// atomicMax (scale 1/2: log2 |a_n| |b_n|; 1/4 with a = b: log2 |a_n|).  An
+// all-zero row counts as log2 = -2000.
+__global__ void gu_norm_kernel(SrcMat gate, SrcMat up, int I, int K, float scale, unsigned *out)
 {
     const int n = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -99,7 +101,7 @@ __global__ void gu_norm_kernel(SrcMat gate, SrcMat up, int I, int K, unsigned *o
         l2[m] = acc > 0.0 ? (float)(log2(acc) + 2.0 * (emax - 127)) : -2000.f;
     }
     if (lane == 0) {
-        const float v = 0.5f * (l2[0] + l2[1]) + 0.001f;
+        const float v = scale * (l2[0] + l2[1]) + 0.001f;
         const uint32_t b = __float_as_uint(v);
         atomicMax(out, (b & 0x80000000u) ? ~b : (b | 0x80000000u));
     }
@@ -107,7 +109,15 @@ __global__ void gu_norm_kernel(SrcMat gate, SrcMat up, int I, int K, unsigned *o
 
 cudaError_t launch_gu_norm(const SrcMat &gate, const SrcMat &up, int group, int I, int H, int *out, cudaStream_t st)
 {
-    gu_norm_kernel<<<(unsigned)((I + 7) / 8), 256, 0, st>>>(gate, up, I, H, reinterpret_cast<unsigned *>(out) + group);
+    gu_norm_kernel<<<(unsigned)((I + 7) / 8), 256, 0, st>>>(gate, up, I, H, 0.5f,
+                                                            reinterpret_cast<unsigned *>(out) + group);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dn_norm(const SrcMat &dn, int group, int I, int H, int *out, cudaStream_t st)
+{
+    gu_norm_kernel<<<(unsigned)((H + 7) / 8), 256, 0, st>>>(dn, dn, H, I, 0.25f,
+                                                            reinterpret_cast<unsigned *>(out) + group);
     return cudaGetLastError();
 }
 
@@ -439,6 +449,46 @@ __global__ void combine_kernel(const float *__restrict__ y, const float *__restr
         acc.w += v.w;
     }
     reinterpret_cast<float4 *>(out)[(long long)t * h4 + c] = acc;
+}
+
+// The same over FP16 rows: y[p] = y16[p] * 2^ys[p], in the same fixed order.
+__global__ void combine_f16_kernel(const uint16_t *__restrict__ y16, const int *__restrict__ ys,
+                                   const float *__restrict__ w, const int *__restrict__ slot_pos, int T, int k, int S,
+                                   int H, float *__restrict__ out, int accumulate)
+{
+    const int h4 = H / 4;
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (long long)T * h4)
+        return;
+    const int t = (int)(i / h4);
+    const int c = (int)(i % h4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (accumulate)
+        acc = reinterpret_cast<const float4 *>(out)[(long long)t * h4 + c];
+    auto row = [&](long long p, float f) {
+        const uint2 v = reinterpret_cast<const uint2 *>(y16)[p * h4 + c];
+        const float sc = f * __int_as_float((127 + ys[p]) << 23);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
+        acc.x = fmaf(sc, a.x, acc.x);
+        acc.y = fmaf(sc, a.y, acc.y);
+        acc.z = fmaf(sc, b.x, acc.z);
+        acc.w = fmaf(sc, b.y, acc.w);
+    };
+    for (int j = 0; j < k; ++j)
+        row(slot_pos[t * k + j], w[t * k + j]);
+    for (int s = 0; s < S; ++s)
+        row((long long)T * k + (long long)s * T + t, 1.0f);
+    reinterpret_cast<float4 *>(out)[(long long)t * h4 + c] = acc;
+}
+
+cudaError_t launch_combine_f16(const Plan &p, float *out, int accumulate, cudaStream_t st)
+{
+    long long n = (long long)p.T * (p.H / 4);
+    combine_f16_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(reinterpret_cast<const uint16_t *>(p.y), p.ys,
+                                                                   p.topk_w, p.slot_pos, p.T, p.k, p.S, p.H, out,
+                                                                   accumulate);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const Plan &p, float *out, int accumulate, cudaStream_t st)

@@ -26,6 +26,7 @@ struct MoeHandle {
     WeightStore gu, dn;        // TILE or TILE_F16 layout (tensor-memory GEMMs, large batches)
     bool tc_f16 = false;       // the tensor-memory GEMMs run FP16 operands (TILE_F16 store with row bases)
     int *gu_norm_key = nullptr;  // FP16 operands: per group, key of max_n log2(|w_g,n| |w_u,n|) (device)
+    int *dn_norm_key = nullptr;  // FP16 operands: per group, key of max_m log2 |w_d,m| (device)
     WeightStore gu_f, dn_f;    // FRAG layout (register-streaming GEMMs, decode-sized batches)
     int *err_host = nullptr;   // mapped pinned host memory, written by kernels on device-side errors
     int *err_dev = nullptr;    // device alias of err_host
@@ -112,6 +113,7 @@ size_t plan_layout(const MoeHandle *h, int T, int k, char *base, Plan *p)
     q.hsp = (int *)take(sizeof(int) * (size_t)P);
     q.xsp = (int *)take(sizeof(int) * (size_t)P);
     q.y = (float *)take(sizeof(float) * (size_t)P * H);
+    q.ys = (int *)take(sizeof(int) * (size_t)P);
     q.sync = (int *)take(layer_stream_sync_bytes(G));
     q.err = h->err_dev;
     if (p)
@@ -193,7 +195,7 @@ MoeStatus run_layer(MoeHandle *h, const void *x, const float *logits, const int 
         // in token and in position order by one pass, with the power of two of
         // each position's h (from a bound on |h|); gate|up writes one FP16 plane
         // of h, which down reads
-        if ((e = launch_token_prep_f16(p, xb, h->gu_norm_key, st)) != cudaSuccess)
+        if ((e = launch_token_prep_f16(p, xb, h->gu_norm_key, h->dn_norm_key, st)) != cudaSuccess)
             return cuda_fail(e, "token prep launch");
         mark(2);
         if ((e = launch_gemm_gate_up_tc(p, h->gu, h->fmt, true, p.x16, st)) != cudaSuccess)
@@ -212,7 +214,8 @@ MoeStatus run_layer(MoeHandle *h, const void *x, const float *logits, const int 
             return cuda_fail(e, "down launch");
     }
     mark(4);
-    if ((e = launch_combine(p, out, accumulate, st)) != cudaSuccess)
+    if ((e = h->tc_f16 ? launch_combine_f16(p, out, accumulate, st) : launch_combine(p, out, accumulate, st)) !=
+        cudaSuccess)
         return cuda_fail(e, "combine launch");
     mark(5);
     mark(6);
@@ -231,6 +234,8 @@ void destroy(MoeHandle *h)
         cudaFree(h->dn.base);
     if (h->gu_norm_key)
         cudaFree(h->gu_norm_key);
+    if (h->dn_norm_key)
+        cudaFree(h->dn_norm_key);
     if (h->gu.row_base)
         cudaFree(h->gu.row_base);
     if (h->dn.row_base)
@@ -399,12 +404,14 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
     if (tile && fmt == FMT_MXFP4) {
         const size_t gu_rb = (size_t)h->gu.row_tiles * TILE_ROWS * G, dn_rb = (size_t)h->dn.row_tiles * TILE_ROWS * G;
         if (cudaMalloc(&h->gu.row_base, gu_rb) != cudaSuccess || cudaMalloc(&h->dn.row_base, dn_rb) != cudaSuccess ||
-            cudaMalloc(&h->gu_norm_key, sizeof(int) * (size_t)G) != cudaSuccess) {
+            cudaMalloc(&h->gu_norm_key, sizeof(int) * (size_t)G) != cudaSuccess ||
+            cudaMalloc(&h->dn_norm_key, sizeof(int) * (size_t)G) != cudaSuccess) {
             cudaGetLastError();
             destroy(h);
             return fail(MOE_ENOMEM, "device allocation of %zu bytes of row bases failed", gu_rb + dn_rb);
         }
-        if ((e = cudaMemsetAsync(h->gu_norm_key, 0, sizeof(int) * (size_t)G, st)) != cudaSuccess) {
+        if ((e = cudaMemsetAsync(h->gu_norm_key, 0, sizeof(int) * (size_t)G, st)) != cudaSuccess ||
+            (e = cudaMemsetAsync(h->dn_norm_key, 0, sizeof(int) * (size_t)G, st)) != cudaSuccess) {
             destroy(h);
             return cuda_fail(e, "norm key clear");
         }
@@ -414,7 +421,8 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
             sources(g, gate, up, dn);
             if ((e = launch_row_base(true, gate, up, h->gu, g, I, c.hidden, wide, st)) != cudaSuccess ||
                 (e = launch_row_base(false, dn, dn, h->dn, g, I, c.hidden, wide, st)) != cudaSuccess ||
-                (e = launch_gu_norm(gate, up, g, I, c.hidden, h->gu_norm_key, st)) != cudaSuccess) {
+                (e = launch_gu_norm(gate, up, g, I, c.hidden, h->gu_norm_key, st)) != cudaSuccess ||
+                (e = launch_dn_norm(dn, g, I, c.hidden, h->dn_norm_key, st)) != cudaSuccess) {
                 destroy(h);
                 return cuda_fail(e, "row base launch");
             }
@@ -430,8 +438,9 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
             cudaFree(h->gu.row_base);
             cudaFree(h->dn.row_base);
             cudaFree(h->gu_norm_key);
+            cudaFree(h->dn_norm_key);
             h->gu.row_base = h->dn.row_base = nullptr;
-            h->gu_norm_key = nullptr;
+            h->gu_norm_key = h->dn_norm_key = nullptr;
         }
     }
     for (int g = 0; g < G; ++g) {

@@ -157,7 +157,8 @@ struct Plan {
     int *hs;                  // [P][hs_pitch] FP16 streaming path: power-of-two scale of each position's
                               // 64-feature block of h
     int hs_pitch;             // ceil(I/64) rounded up to a multiple of 4 (16-byte rows)
-    float *y;                 // [P][H] FP32
+    float *y;                 // [P][H] FP32; the tcgen05 FP16 path keeps FP16 y * 2^-ys[p] here instead
+    int *ys;                  // [P] tcgen05 FP16 path: power of two of each position's FP16 y row
     int *sync;                // streaming path: grid-wide counters, zeroed before each launch
     int *err;                 // device-visible error flag (mapped host memory)
 };
@@ -195,6 +196,8 @@ cudaError_t launch_permute(const Plan &p, cudaStream_t st);
 cudaError_t launch_dense_plan(const Plan &p, cudaStream_t st);
 
 cudaError_t launch_combine(const Plan &p, float *out, int accumulate, cudaStream_t st);
+// the same over the FP16 rows y16 * 2^ys[p] of the tcgen05 FP16 path (in p.y)
+cudaError_t launch_combine_f16(const Plan &p, float *out, int accumulate, cudaStream_t st);
 
 // x_perm[p] = x[row_token[p]] for the routed positions (BF16 operands)
 cudaError_t launch_gather_rows(const Plan &p, const uint16_t *x, cudaStream_t st);
@@ -212,11 +215,15 @@ cudaError_t launch_row_base(bool gate_up, const SrcMat &gate, const SrcMat &up, 
 // must start at 0
 cudaError_t launch_gu_norm(const SrcMat &gate, const SrcMat &up, int group, int I, int H, int *out,
                            cudaStream_t st);
+// the same for the rows of a down matrix (H rows of I values): a key of
+// max_m log2 |w_d,m|
+cudaError_t launch_dn_norm(const SrcMat &dn, int group, int I, int H, int *out, cudaStream_t st);
 
 // tcgen05 path with FP16 operands (after the permutation): FP16 token rows x16,
 // their copies in routed position order (x_perm), the powers of two xs / xsp,
 // and the per-position h scales hsp from gu_norm_key (one key per group)
-cudaError_t launch_token_prep_f16(const Plan &p, const uint16_t *x, const int *gu_norm_key, cudaStream_t st);
+cudaError_t launch_token_prep_f16(const Plan &p, const uint16_t *x, const int *gu_norm_key, const int *dn_norm_key,
+                                  cudaStream_t st);
 
 // f16: FP16 operands (TILE_F16 MXFP4 store, token rows x_rows = x16 and the
 // gathered FP16 rows in x_perm); otherwise BF16 operands (x_rows = the caller's x)
