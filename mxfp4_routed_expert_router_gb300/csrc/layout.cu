@@ -62,46 +62,54 @@ __device__ __forceinline__ uint16_t src_bf16(const SrcMat *src, int srow, int k,
 
 // One warp per row n of a pair of MXFP4 matrices (gate and up rows of one
 // feature; or a down row twice): log2 |a_n|^2 and log2 |b_n|^2 of the decoded
-// rows, each sum taken in double against the row's largest exponent (no
-// underflow of small blocks, no overflow of large ones); `scale` times their
-// sum, rounded up by 2^-10, goes into out as an order-preserving key with
+// rows, in FP32 against the row's largest exponent among blocks with a nonzero
+// code (that block alone contributes at least 1/4, so the blocks too small to
+// register below it change the sum by less than 2^-100 of it); `scale` times
+// their sum, rounded up by 2^-10, goes into out as an order-preserving key with
 // atomicMax (scale 1/2: log2 |a_n| |b_n|; 1/4 with a = b: log2 |a_n|).  An
 // all-zero row counts as log2 = -2000.
+__device__ __forceinline__ float row_log2_sq(const SrcMat &src, int n, int K, int lane)
+{
+    const uint8_t *sc = src.scales + (long long)n * src.scale_stride;
+    const uint8_t *cd = src.codes + (long long)n * src.code_stride;
+    // (2v)^2 of the magnitude indices 0..7, one byte each: 0, 1, 4, 9, 16, 36, 64, 144
+    constexpr unsigned long long SQ = 0x9040241009040100ull;
+    float acc = 0.f;  // sum of the lane's blocks of q * 4^(e - lmax), q = sum (2v)^2
+    int lmax = -1;    // largest exponent of the lane's blocks with a nonzero code
+    for (int b = lane; b < K / 32; b += 32) {
+        int q = 0;
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t byte = cd[b * 16 + i];
+            q += (int)((SQ >> (8 * (byte & 7u))) & 0xFFu) + (int)((SQ >> (8 * ((byte >> 4) & 7u))) & 0xFFu);
+        }
+        if (q == 0)
+            continue;
+        const int e = sc[b];
+        if (e > lmax) {
+            acc = lmax < 0 ? 0.f : ldexpf(acc, 2 * (lmax - e));
+            lmax = e;
+        }
+        acc += ldexpf((float)q, 2 * (e - lmax));
+    }
+    int wmax = lmax;
+    for (int o = 16; o > 0; o >>= 1)
+        wmax = max(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+    float v = lmax < 0 ? 0.f : ldexpf(acc, 2 * (lmax - wmax));
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    // sum v(c)^2 = q / 4 at 4^(wmax - 127)
+    return wmax < 0 ? -2000.f : log2f(v) - 2.f + 2.f * (float)(wmax - 127);
+}
+
 __global__ void gu_norm_kernel(SrcMat gate, SrcMat up, int I, int K, float scale, unsigned *out)
 {
     const int n = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (n >= I)
         return;
-    float l2[2];
-#pragma unroll
-    for (int m = 0; m < 2; ++m) {
-        const SrcMat &src = m == 0 ? gate : up;
-        const uint8_t *sc = src.scales + (long long)n * src.scale_stride;
-        const uint8_t *cd = src.codes + (long long)n * src.code_stride;
-        int emax = 0;
-        for (int b = lane; b < K / 32; b += 32)
-            emax = max(emax, (int)sc[b]);
-        for (int o = 16; o > 0; o >>= 1)
-            emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
-        // sum over blocks of 4^(e_b - emax) * sum_i v(c_i)^2, v^2 in units of 1/4
-        double acc = 0.0;
-        for (int b = lane; b < K / 32; b += 32) {
-            int q = 0;  // sum of (2 v)^2 over the block: v in {0, .5, 1, 1.5, 2, 3, 4, 6}
-            for (int i = 0; i < 16; ++i) {
-                // (2v)^2 of the magnitude indices 0..7, one byte each: 0, 1, 4, 9, 16, 36, 64, 144
-                constexpr unsigned long long SQ = 0x9040241009040100ull;
-                const uint8_t byte = cd[b * 16 + i];
-                q += (int)((SQ >> (8 * (byte & 7))) & 0xFFu) + (int)((SQ >> (8 * ((byte >> 4) & 7))) & 0xFFu);
-            }
-            acc += ldexp((double)q * 0.25, 2 * ((int)sc[b] - emax));
-        }
-        for (int o = 16; o > 0; o >>= 1)
-            acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        l2[m] = acc > 0.0 ? (float)(log2(acc) + 2.0 * (emax - 127)) : -2000.f;
-    }
+    const float l0 = row_log2_sq(gate, n, K, lane), l1 = row_log2_sq(up, n, K, lane);
     if (lane == 0) {
-        const float v = scale * (l2[0] + l2[1]) + 0.001f;
+        const float v = scale * (l0 + l1) + 0.001f;
         const uint32_t b = __float_as_uint(v);
         atomicMax(out, (b & 0x80000000u) ? ~b : (b | 0x80000000u));
     }
@@ -318,26 +326,35 @@ __global__ void repack_tile_f16_kernel(int gate_up, SrcMat gate, SrcMat up, uint
 __global__ void row_base_kernel(int gate_up, SrcMat gate, SrcMat up, uint8_t *dst, int row_tiles, int logical_rows,
                                 int K, int *wide)
 {
-    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    // one warp per tile row; lanes read the row's scale bytes side by side
+    const long long idx = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
     if (idx >= (long long)row_tiles * TILE_ROWS)
         return;
     const int r = (int)(idx % TILE_ROWS), tile = (int)(idx / TILE_ROWS);
     int srow;
     const SrcMat *src = tile_row_source(gate_up, &gate, &up, tile, r, logical_rows, &srow);
     if (srow < 0) {
-        dst[idx] = 127;
+        if (lane == 0)
+            dst[idx] = 127;
         return;
     }
     const uint8_t *sc = src->scales + srow * src->scale_stride;
     int mx = 0, mn = 255;
-    for (int b = 0; b < K / 32; ++b) {
+    for (int b = lane; b < K / 32; b += 32) {
         const int e = sc[b];
         mx = e > mx ? e : mx;
         mn = e < mn ? e : mn;
     }
-    dst[idx] = (uint8_t)mx;
-    if (mx - mn > TILE_F16_MAX_SPREAD)
-        atomicOr(wide, 1);
+    for (int o = 16; o > 0; o >>= 1) {
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    }
+    if (lane == 0) {
+        dst[idx] = (uint8_t)mx;
+        if (mx - mn > TILE_F16_MAX_SPREAD)
+            atomicOr(wide, 1);
+    }
 }
 
 cudaError_t launch_row_base(bool gate_up, const SrcMat &gate, const SrcMat &up, const WeightStore &ws, int group,
@@ -345,7 +362,7 @@ cudaError_t launch_row_base(bool gate_up, const SrcMat &gate, const SrcMat &up, 
 {
     const int logical_rows = gate_up ? I : H;
     const long long total = (long long)ws.row_tiles * TILE_ROWS;
-    row_base_kernel<<<(unsigned)((total + 127) / 128), 128, 0, st>>>(
+    row_base_kernel<<<(unsigned)((total + 7) / 8), 256, 0, st>>>(
         gate_up ? 1 : 0, gate, up, ws.row_base + (size_t)group * total, ws.row_tiles, logical_rows, ws.cols, wide);
     return cudaGetLastError();
 }
