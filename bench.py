@@ -172,23 +172,25 @@ class ClockSampler:
 def tc_fp16_operands(cfg) -> bool:
     """Whether the tensor-memory GEMMs take FP16 operands for this layer: the
     library decodes MXFP4 weights exactly to FP16 against a per-row exponent
-    base when no row's E8M0 exponents span more than 23; the seeded exponents
-    are uniform in [e8m0_lo, e8m0_hi], so a range of at most 23 guarantees it.
-    BF16 weights, and MXFP4 rows of a wider span, run with BF16 operands."""
+    base when no row's E8M0 exponents span more than 23 (the seeded exponents
+    are uniform in [e8m0_lo, e8m0_hi], so a range of at most 23 guarantees it),
+    and group-32 INT4 weights always to FP16 hi + lo pairs.  BF16 weights, and
+    MXFP4 rows of a wider span, run with BF16 operands."""
+    if cfg.weight_format == "int4g32":
+        return True
     return cfg.weight_format == "mxfp4" and cfg.e8m0_hi - cfg.e8m0_lo <= 23
 
 
 def kernels_per_step(cfg, streaming: bool) -> int:
     """Kernels of this library launched by one forward call.
 
-    The single-kernel layer launches one kernel.  Otherwise: router, histogram
-    and permutation (routed) or the dense plan (dense); with FP16 operands the
-    token preparation, the row gather, gate|up, the h conversion and down (the
-    h maxima are cleared by a memset, not a kernel); with BF16 operands the row
-    gather, gate|up and down; then the combine."""
+    The single-kernel layer launches one kernel.  Otherwise: the router and the
+    two kernels of the chunked permutation (routed) or the dense plan (dense);
+    the token preparation (FP16 operands) or the row gather (BF16 operands);
+    gate|up and down; then the combine."""
     if streaming:
         return 1
-    return (1 if cfg.dense else 3) + (5 if tc_fp16_operands(cfg) else 3) + 1
+    return (1 if cfg.dense else 3) + 3 + 1
 
 
 def operand_dtype(cfg, streaming: bool) -> str:
@@ -652,7 +654,7 @@ def main():
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--weights", default="mxfp4", choices=["mxfp4", "int4g32"],
-                    help="weight format of a routed workload (group-32 INT4 runs the single-kernel sizes)")
+                    help="weight format of a routed workload")
     ap.add_argument("--extra", default=",".join(EXTRA_WORKLOADS),
                     help="comma-separated workloads measured beside the main one on the same layer ('none': skip)")
     ap.add_argument("--experts", type=int, default=0,

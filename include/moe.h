@@ -100,10 +100,12 @@ typedef enum {
  * Resident 975B MoE Inference on Eleven AI PCs" (§3.1: packed 4-bit nibbles
  * with one FP16 scale per 32-value group; §3.5: zero points): the weight is
  * s * (q - z) for the unsigned code q and its group's FP16 scale s and zero
- * point z in 0..15.  INT4 layers run on the single-kernel path only: a forward
- * call outside its range (more than 16*E or 4096 routed slots T*k, more than
- * 512 routed experts, a dense layer with more than 64 tokens) returns
- * MOE_EINVAL. */
+ * point z in 0..15.  INT4 layers run both paths: the single kernel decodes
+ * s * (q - z) exactly (FP16 q - z, the scale applied in FP32 to each 32-value
+ * block); the tensor-core GEMMs of larger batches split each weight, relative
+ * to a power of two per row, into an FP16 pair hi + lo and run two MMAs per K
+ * step (exact for every group whose scale is within 2^-24 of its row's
+ * largest; smaller groups round at about 2^-35 of the row's largest weight). */
 typedef enum { MOE_W_MXFP4 = 0, MOE_W_BF16 = 1, MOE_W_INT4G32 = 2 } MoeWeightFormat;
 
 typedef struct {
@@ -179,8 +181,7 @@ typedef struct {
  *  routing       NULL or device pointers that receive the routing
  * T == 0 enqueues nothing and returns MOE_OK.
  * Errors: MOE_EINVAL (NULL/misaligned pointers, T < 0, k outside
- * [1, k_max], a dense handle, an INT4 batch outside the single-kernel range),
- * MOE_EWORKSPACE, MOE_EDEVICE, MOE_ECUDA. */
+ * [1, k_max], a dense handle), MOE_EWORKSPACE, MOE_EDEVICE, MOE_ECUDA. */
 MoeStatus moe_forward(MoeHandle *h, const void *x_bf16, const float *router_logits, int T, int k, float *out_fp32,
                       int accumulate, void *workspace, size_t ws_bytes, const MoeRoutingOut *routing,
                       void *cuda_stream);
@@ -199,8 +200,7 @@ MoeStatus moe_forward(MoeHandle *h, const void *x_bf16, const float *router_logi
  * runs that slot as expert 0 with weight 0 so that every access stays in
  * bounds, and moe_sync_status() then reports MOE_EDEVICE.
  * Errors: MOE_EINVAL (NULL/misaligned pointers, T < 0, k outside [1, k_max],
- * a dense handle, an INT4 batch outside the single-kernel range),
- * MOE_EWORKSPACE, MOE_EDEVICE, MOE_ECUDA. */
+ * a dense handle), MOE_EWORKSPACE, MOE_EDEVICE, MOE_ECUDA. */
 MoeStatus moe_forward_routed(MoeHandle *h, const void *x_bf16, const int32_t *topk_ids, const float *topk_w, int T,
                              int k, float *out_fp32, int accumulate, void *workspace, size_t ws_bytes,
                              const MoeRoutingOut *routing, void *cuda_stream);
@@ -272,8 +272,8 @@ void moe_graph_free(MoeGraph *graph);
 /* The dense FFN of a dense handle on T tokens, as the sum of its all-active
  * slices ("Cascadia" §3.4, Eq. 2).  Arguments as for moe_forward; the
  * workspace size is moe_workspace_bytes(h, T, 0).
- * Errors: MOE_EINVAL (also for a routed handle, and for more than 64 tokens
- * with INT4 weights), MOE_EWORKSPACE, MOE_EDEVICE, MOE_ECUDA. */
+ * Errors: MOE_EINVAL (also for a routed handle), MOE_EWORKSPACE, MOE_EDEVICE,
+ * MOE_ECUDA. */
 MoeStatus moe_dense_sliced_forward(MoeHandle *h, const void *x_bf16, int T, float *out_fp32, int accumulate,
                                    void *workspace, size_t ws_bytes, void *cuda_stream);
 

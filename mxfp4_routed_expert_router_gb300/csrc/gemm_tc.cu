@@ -124,7 +124,9 @@ struct TcArgs {
     int brows;  // token rows per TMA box of the B operand (16, or 64 when every B tensor has that many rows)
 };
 
-enum { OP_F16 = 0, OP_BF16 = 1 };
+// operand paths: FP16 (MXFP4 decoded exactly), BF16, and FP16 hi + lo pairs of
+// group-32 INT4 weights (two MMAs per K step on 64-value stages)
+enum { OP_F16 = 0, OP_BF16 = 1, OP_I4 = 2 };
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -220,6 +222,20 @@ __device__ __forceinline__ uint32_t make_idesc(int n)
     return (1u << 4) | ab | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(TILE_ROWS >> 4) << 24);
 }
 
+// One INT4 pair into FP16 hi and lo words: w holds the pair's codes in bits
+// 0..3 and 16..19; 0x6400 | q is the FP16 value 1024 + q (ulp 1), so
+// subtracting zz = {1024 + z, 1024 + z} leaves q - z exactly; hi = s2 (q - z)
+// rounded to FP16, lo = s2 (q - z) - hi from one fused multiply-add (exact: the
+// product has at most 15 significant bits, hi takes 11).
+__device__ __forceinline__ void i4_pair_hilo(uint32_t w, uint32_t zz, uint32_t s2, uint32_t &hi, uint32_t &lo)
+{
+    const uint32_t v = (w & 0x000F000Fu) | 0x64006400u;
+    uint32_t qz;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(qz) : "r"(v), "r"(zz));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(qz), "r"(s2));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(lo) : "r"(qz), "r"(s2), "r"(hi ^ 0x80008000u));
+}
+
 // {2^d, 2^d} in FP16 for d in [-24, 0] (below -14 a subnormal, exactly)
 __device__ __forceinline__ uint32_t f16x2_pow2(int d)
 {
@@ -261,14 +277,17 @@ template <bool GU, int OP, int WFMT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_b2)
 {
-    static_assert(OP == OP_BF16 || WFMT == FMT_MXFP4, "FP16 operands decode MXFP4 weights only");
+    static_assert(OP == OP_BF16 || (OP == OP_F16 && WFMT == FMT_MXFP4) || (OP == OP_I4 && WFMT == FMT_INT4),
+                  "FP16 operands decode MXFP4 weights, FP16 pairs INT4 weights");
+    constexpr bool FT = OP != OP_BF16;                  // FP16 token operands (x16, h16) and scaled epilogues
     constexpr int NB = (!GU && OP == OP_BF16) ? 2 : 1;  // token planes: down with BF16 operands reads h hi + lo
-    constexpr int KST = NB == 2 ? HALF_K : CHUNK_K;     // K values per stage
+    constexpr int KST = (NB == 2 || OP == OP_I4) ? HALF_K : CHUNK_K;  // K values per stage
     constexpr int NSL = KST / HALF_K;                   // 64-wide K slices per stage
+    constexpr int NSLB = NSL * NB;                      // swizzled B tiles per stage
     constexpr int NBLK = KST / 32;                      // 32-value blocks per stage
     using L = Smem;
     static_assert(L::TOTAL <= 232448, "shared memory");
-    static_assert(NSL * NB == 2, "a stage holds two swizzled B tiles");
+    static_assert(NSLB == 2 || (OP == OP_I4 && NSLB == 1), "a stage holds two swizzled B tiles (INT4: one)");
 
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
@@ -363,7 +382,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // read, or zero fill past the tensor's last row)
             const int nbox = (w.n_mma + a.brows - 1) / a.brows;
             const int box_bytes = a.brows * HALF_K * 2;
-            const uint32_t bytes = (uint32_t)(nbox * box_bytes * 2);
+            const uint32_t bytes = (uint32_t)(nbox * box_bytes * NSLB);
             for (int st = 0; st < nstages; ++st, ++sc) {
                 const int slot = sc % B_STAGES;
                 const uint32_t ph = (sc / B_STAGES) & 1;
@@ -377,7 +396,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     // the stage's two swizzled tiles: two 64-wide K slices of one plane,
                     // or one slice of the h hi and lo planes
                     for (int b = 0; b < nbox; ++b) {
-                        if (NB == 1) {
+                        if (NSLB == 1) {
+                            tma_2d(bdst + b * box_bytes, m0, st * KST, row0 + b * a.brows, &b_full[slot]);
+                        } else if (NB == 1) {
                             tma_2d(bdst + b * box_bytes, m0, st * KST, row0 + b * a.brows, &b_full[slot]);
                             tma_2d(bdst + B_SLICE_BYTES + b * box_bytes, m0, st * KST + HALF_K, row0 + b * a.brows,
                                    &b_full[slot]);
@@ -413,7 +434,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!(ok = mbar_wait(&acc_empty[buf], ((tc / NBUF) & 1) ^ 1, abort_flag, a.err)))
                     break;
                 tc_fence_after();
-                const uint32_t idesc = make_idesc<OP>(w.n_mma);
+                const uint32_t idesc = make_idesc<OP == OP_BF16 ? OP_BF16 : OP_F16>(w.n_mma);
                 const uint32_t d_tmem = tmem_base + (uint32_t)(buf * NMAX);
                 for (int st = 0; st < nstages; ++st, ++sc) {
                     // a_full completes once the stage's A is in tensor memory and its B
@@ -426,7 +447,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     // descriptors of this slot: base plus the slot's offset (address field = bytes >> 4)
                     const uint64_t bd = desc0 + (uint64_t)((bs * B_STAGE_BYTES) >> 4);
                     const uint32_t at = tmem_base + (uint32_t)(TMEM_A0 + as * A_SLOT_COLS);
-                    if (NB == 1) {
+                    if (OP == OP_I4) {
+                        // the stage's 64 values of K: the hi tile (columns 0..31), then the lo tile
+                        tc_mma4(d_tmem, at, bd, idesc, st);
+                        tc_mma4(d_tmem, at + 32, bd, idesc, 1u);
+                    } else if (NB == 1) {
 #pragma unroll
                         for (int sl = 0; sl < NSL; ++sl)
                             tc_mma4(d_tmem, at + 32 * sl, bd + (uint64_t)((sl * B_SLICE_BYTES) >> 4), idesc,
@@ -483,7 +508,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 cached_ii = ii;
                 const WorkItem w = decompose(blockIdx.x + ii * gridDim.x, prefix, a.grp_count, a.G, rt_n, NMAX);
                 tile0 = tile_src(w);
-                if (OP == OP_F16)
+                if (FT)
                     base_c = __ldg(a.row_base + (size_t)w.g * rb_stride + w.rt * TILE_ROWS + r);
             }
             src = tile0 + (size_t)(st * KST / CHUNK_K) * a.chunk_bytes;
@@ -497,7 +522,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int b = 0; b < NBLK; ++b) {
                 const int blk = NBLK == 4 ? b : 2 * kh + b;  // 32-value block of the chunk
-                if (OP == OP_F16) {
+                if (OP == OP_I4) {
+                    // TILE_I4: 16 code bytes of (block, row r); the FP16 scale and the zero point
+                    rc[b] = __ldg(reinterpret_cast<const uint4 *>(src + (blk * TILE_ROWS + r) * 16));
+                    re[b] = (uint32_t)__ldg(reinterpret_cast<const uint16_t *>(src + CHUNK_MX_CODE_BYTES) +
+                                            blk * TILE_ROWS + r) |
+                            ((uint32_t)__ldg(src + CHUNK_MX_CODE_BYTES + CHUNK_I4_SCALE_BYTES + blk * TILE_ROWS + r)
+                             << 16);
+                } else if (OP == OP_F16) {
                     // TILE_F16: 16 code bytes of (block, row r), then the E8M0 bytes
                     rc[b] = __ldg(reinterpret_cast<const uint4 *>(src + (blk * TILE_ROWS + r) * 16));
                     re[b] = __ldg(src + CHUNK_MX_CODE_BYTES + blk * TILE_ROWS + r);
@@ -536,6 +568,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         o[4 * v + 2] = x4.z;
                         o[4 * v + 3] = x4.w;
                     }
+                } else if (OP == OP_I4) {
+                    // w = s (q - z) relative to the row base: s' = s * 2^-b_row (below 2^12),
+                    // hi = fp16(s' (q - z)), lo = s' (q - z) - hi (exact in FP16: at most
+                    // four significant bits left), into two tensor-memory tiles
+                    const float sf = __half2float(__ushort_as_half((unsigned short)(re[b] & 0xFFFFu))) *
+                                     __int_as_float((254 - (int)rb) << 23);
+                    const uint32_t sh = (uint32_t)__half_as_ushort(__float2half_rn(sf));
+                    const uint32_t s2 = sh | (sh << 16);
+                    const uint32_t zz = (0x6400u + (re[b] >> 16)) * 0x10001u;
+                    uint32_t lo[16];
+                    const uint32_t words[4] = {rc[b].x, rc[b].y, rc[b].z, rc[b].w};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int p = 0; p < 4; ++p)
+                            i4_pair_hilo(words[c] >> (4 * p), zz, s2, o[4 * c + p], lo[4 * c + p]);
+                    tmem_st16(tmem_base + tlane + (uint32_t)(TMEM_A0 + slot * A_SLOT_COLS + 32 + b * 16), lo);
                 } else if (OP == OP_F16) {
                     int d = (int)re[b] - (int)rb;
                     d = d < -24 ? -24 : (d > 0 ? 0 : d);  // only blocks past K (code 0) fall outside [-23, 0]
@@ -569,7 +618,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;                   // tensor-memory lane quadrant of this warp
         const int eh = (warp - WARP_EPI0) >> 2;   // which column chunks of the quadrant it takes
-        // this warp's column scales (FP16 operands), indexed by column
+        // this warp's column scales (FP16 token operands), indexed by column
         float *csc = reinterpret_cast<float *>(smem + L::COLSC_OFF) + (warp - WARP_EPI0) * NMAX;
         float *hsc = reinterpret_cast<float *>(smem + L::HSC_OFF) + (warp - WARP_EPI0) * NMAX;  // gate|up, FP16
         // columns per tensor-memory wait: gate|up 32, down 16
@@ -581,7 +630,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // FP16 operands: the power of two of each of this warp's columns' token row
             // (gate|up) or h row (down), staged in shared memory while the item's MMAs
             // still run
-            if (OP == OP_F16) {
+            if (FT) {
 #pragma unroll 1
                 for (int i = 0; i < NMAX / (2 * EC); ++i)
                     for (int c = EC * eh + 2 * EC * i + lane; c < EC * eh + 2 * EC * i + EC && c < w.nvalid; c += 32) {
@@ -603,7 +652,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int row = 32 * q + lane;
             const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * NMAX);
             // FP16 operands: this row's weight scale 2^(b - 127) (exact; a subnormal for b = 0)
-            const float wsc = OP == OP_F16
+            const float wsc = FT
                                   ? ldexpf(1.0f, (int)__ldg(a.row_base + (size_t)w.g * rb_stride + rt * TILE_ROWS + row) - 127)
                                   : 1.0f;
             // column groups of this warp: EC columns at c0 = EC * eh + 2 * EC * i
@@ -639,7 +688,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             float uv = up_lane ? v[8 + jj] * wsc : recv;
                             const int tok = c1 + (up_lane ? 8 : 0) + jj;
                             const bool valid = tok < w.nvalid && n < a.I;
-                            if (OP == OP_F16) {
+                            if (FT) {
                                 // undo the token row's power of two; h leaves in FP16 times
                                 // the position's power of two
                                 if (valid) {
@@ -663,7 +712,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         for (int jj = 0; jj < 16; ++jj) {
                             if (m < a.H && c1 + jj < w.nvalid) {
                                 const size_t o = (size_t)(pos0 + c1 + jj) * a.H + m;
-                                if (OP == OP_F16)
+                                if (FT)
                                     a.y16[o] = __half_as_ushort(__float2half_rn(v[jj] * wsc * csc[c1 + jj]));
                                 else
                                     a.y_out[o] = v[jj];
@@ -708,7 +757,9 @@ cudaError_t launch_any(const TcArgs &a, int fmt, bool f16, const CUtensorMap &m1
                        cudaStream_t st)
 {
     if (f16)
-        return fmt == FMT_MXFP4 ? launch_cfg<GU, OP_F16, FMT_MXFP4>(a, m1, m2, st) : cudaErrorInvalidValue;
+        return fmt == FMT_MXFP4  ? launch_cfg<GU, OP_F16, FMT_MXFP4>(a, m1, m2, st)
+               : fmt == FMT_INT4 ? launch_cfg<GU, OP_I4, FMT_INT4>(a, m1, m2, st)
+                                 : cudaErrorInvalidValue;
     return fmt == FMT_MXFP4 ? launch_cfg<GU, OP_BF16, FMT_MXFP4>(a, m1, m2, st)
                             : launch_cfg<GU, OP_BF16, FMT_BF16>(a, m1, m2, st);
 }

@@ -101,13 +101,38 @@ __device__ __forceinline__ float row_log2_sq(const SrcMat &src, int n, int K, in
     return wmax < 0 ? -2000.f : log2f(v) - 2.f + 2.f * (float)(wmax - 127);
 }
 
-__global__ void gu_norm_kernel(SrcMat gate, SrcMat up, int I, int K, float scale, unsigned *out)
+// log2 |w_n|^2 of a group-32 INT4 row: sum over blocks of s_b^2 * sum (q - z_b)^2
+// in FP32 (s^2 of an FP16 scale lies in [2^-48, 2^32]: no under- or overflow).
+__device__ __forceinline__ float i4_row_log2_sq(const SrcMat &src, int n, int K, int lane)
+{
+    const uint16_t *sc = reinterpret_cast<const uint16_t *>(src.scales) + (long long)n * src.scale_stride;
+    const uint8_t *zp = src.zeros ? src.zeros + (long long)n * src.scale_stride : nullptr;
+    const uint8_t *cd = src.codes + (long long)n * src.code_stride;
+    float acc = 0.f;
+    for (int b = lane; b < K / 32; b += 32) {
+        const int z = zp ? zp[b] : 8;
+        int q2 = 0;
+        for (int i = 0; i < 16; ++i) {
+            const int byte = cd[b * 16 + i];
+            const int d0 = (byte & 15) - z, d1 = (byte >> 4) - z;
+            q2 += d0 * d0 + d1 * d1;
+        }
+        const float s = __half2float(__ushort_as_half(sc[b]));
+        acc = fmaf(s * s, (float)q2, acc);
+    }
+    for (int o = 16; o > 0; o >>= 1)
+        acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    return acc > 0.f ? log2f(acc) : -2000.f;
+}
+
+__global__ void gu_norm_kernel(int fmt, SrcMat gate, SrcMat up, int I, int K, float scale, unsigned *out)
 {
     const int n = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (n >= I)
         return;
-    const float l0 = row_log2_sq(gate, n, K, lane), l1 = row_log2_sq(up, n, K, lane);
+    const float l0 = fmt == FMT_INT4 ? i4_row_log2_sq(gate, n, K, lane) : row_log2_sq(gate, n, K, lane);
+    const float l1 = fmt == FMT_INT4 ? i4_row_log2_sq(up, n, K, lane) : row_log2_sq(up, n, K, lane);
     if (lane == 0) {
         const float v = scale * (l0 + l1) + 0.001f;
         const uint32_t b = __float_as_uint(v);
@@ -115,16 +140,17 @@ __global__ void gu_norm_kernel(SrcMat gate, SrcMat up, int I, int K, float scale
     }
 }
 
-cudaError_t launch_gu_norm(const SrcMat &gate, const SrcMat &up, int group, int I, int H, int *out, cudaStream_t st)
+cudaError_t launch_gu_norm(int fmt, const SrcMat &gate, const SrcMat &up, int group, int I, int H, int *out,
+                           cudaStream_t st)
 {
-    gu_norm_kernel<<<(unsigned)((I + 7) / 8), 256, 0, st>>>(gate, up, I, H, 0.5f,
+    gu_norm_kernel<<<(unsigned)((I + 7) / 8), 256, 0, st>>>(fmt, gate, up, I, H, 0.5f,
                                                             reinterpret_cast<unsigned *>(out) + group);
     return cudaGetLastError();
 }
 
-cudaError_t launch_dn_norm(const SrcMat &dn, int group, int I, int H, int *out, cudaStream_t st)
+cudaError_t launch_dn_norm(int fmt, const SrcMat &dn, int group, int I, int H, int *out, cudaStream_t st)
 {
-    gu_norm_kernel<<<(unsigned)((H + 7) / 8), 256, 0, st>>>(dn, dn, H, I, 0.25f,
+    gu_norm_kernel<<<(unsigned)((H + 7) / 8), 256, 0, st>>>(fmt, dn, dn, H, I, 0.25f,
                                                             reinterpret_cast<unsigned *>(out) + group);
     return cudaGetLastError();
 }
@@ -321,6 +347,70 @@ __global__ void repack_tile_f16_kernel(int gate_up, SrcMat gate, SrcMat up, uint
     }
 }
 
+// TILE_I4 layout (group-32 INT4; see moe_internal.cuh): one thread builds one
+// row of one chunk -- per 32-value block, the codes with pair (2p, 2p + 1) of
+// each 8-value word in nibbles p and p + 4, the FP16 scale bits and the zero
+// point (scale 0 and zero point 8 past K, a weight of 0).
+__global__ void repack_tile_i4_kernel(int gate_up, SrcMat gate, SrcMat up, uint8_t *dst, int row_tiles, int kchunks,
+                                      int chunk_bytes, int logical_rows, int K, int *bad_scale)
+{
+    long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long long)row_tiles * kchunks * TILE_ROWS)
+        return;
+    const int r = (int)(idx % TILE_ROWS);
+    const long long tk = idx / TILE_ROWS;
+    const int kc = (int)(tk % kchunks), tile = (int)(tk / kchunks);
+    int srow;
+    const SrcMat *src = tile_row_source(gate_up, &gate, &up, tile, r, logical_rows, &srow);
+    uint8_t *chunk = dst + ((long long)tile * kchunks + kc) * chunk_bytes;
+    const int k0 = kc * CHUNK_K;
+    for (int b = 0; b < CHUNK_K / 32; ++b) {
+        uint32_t words[4];
+        for (int c = 0; c < 4; ++c) {
+            uint32_t wv = 0;
+            for (int p = 0; p < 4; ++p) {
+                const int k = k0 + 32 * b + 8 * c + 2 * p;
+                wv |= src_code(src, srow, k, K) << (4 * p);
+                wv |= src_code(src, srow, k + 1, K) << (4 * p + 16);
+            }
+            words[c] = wv;
+        }
+        *reinterpret_cast<uint4 *>(chunk + (b * TILE_ROWS + r) * 16) = make_uint4(words[0], words[1], words[2], words[3]);
+        reinterpret_cast<uint16_t *>(chunk + CHUNK_MX_CODE_BYTES)[b * TILE_ROWS + r] =
+            src_i4_scale(src, srow, k0 + 32 * b, K, bad_scale);
+        chunk[CHUNK_MX_CODE_BYTES + CHUNK_I4_SCALE_BYTES + b * TILE_ROWS + r] =
+            src_i4_zero(src, srow, k0 + 32 * b, K, bad_scale);
+    }
+}
+
+// Row bases of a TILE_I4 store: one warp per tile row, b_row + 127 with b_row =
+// floor(log2 max|s|) - TILE_I4_BASE_SHIFT over the row's nonzero FP16 scales
+// (127 for a row with none, or past the logical end).
+__global__ void row_base_i4_kernel(int gate_up, SrcMat gate, SrcMat up, uint8_t *dst, int row_tiles, int logical_rows,
+                                   int K)
+{
+    const long long idx = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (idx >= (long long)row_tiles * TILE_ROWS)
+        return;
+    const int r = (int)(idx % TILE_ROWS), tile = (int)(idx / TILE_ROWS);
+    int srow;
+    const SrcMat *src = tile_row_source(gate_up, &gate, &up, tile, r, logical_rows, &srow);
+    int mx = -1000;
+    if (srow >= 0) {
+        const uint16_t *sc = reinterpret_cast<const uint16_t *>(src->scales) + (long long)srow * src->scale_stride;
+        for (int b = lane; b < K / 32; b += 32) {
+            const float s = fabsf(__half2float(__ushort_as_half(sc[b])));
+            if (s > 0.f && s <= 65504.f)
+                mx = max(mx, ilogbf(s));
+        }
+    }
+    for (int o = 16; o > 0; o >>= 1)
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0)
+        dst[idx] = (uint8_t)(mx == -1000 ? 127 : mx - TILE_I4_BASE_SHIFT + 127);
+}
+
 // Row bases of a TILE_F16 store: one thread per tile row; rows past the
 // logical end get 127 (their codes are 0).
 __global__ void row_base_kernel(int gate_up, SrcMat gate, SrcMat up, uint8_t *dst, int row_tiles, int logical_rows,
@@ -357,13 +447,18 @@ __global__ void row_base_kernel(int gate_up, SrcMat gate, SrcMat up, uint8_t *ds
     }
 }
 
-cudaError_t launch_row_base(bool gate_up, const SrcMat &gate, const SrcMat &up, const WeightStore &ws, int group,
-                            int I, int H, int *wide, cudaStream_t st)
+cudaError_t launch_row_base(int fmt, bool gate_up, const SrcMat &gate, const SrcMat &up, const WeightStore &ws,
+                            int group, int I, int H, int *wide, cudaStream_t st)
 {
     const int logical_rows = gate_up ? I : H;
     const long long total = (long long)ws.row_tiles * TILE_ROWS;
-    row_base_kernel<<<(unsigned)((total + 7) / 8), 256, 0, st>>>(
-        gate_up ? 1 : 0, gate, up, ws.row_base + (size_t)group * total, ws.row_tiles, logical_rows, ws.cols, wide);
+    if (fmt == FMT_INT4)
+        row_base_i4_kernel<<<(unsigned)((total + 7) / 8), 256, 0, st>>>(
+            gate_up ? 1 : 0, gate, up, ws.row_base + (size_t)group * total, ws.row_tiles, logical_rows, ws.cols);
+    else
+        row_base_kernel<<<(unsigned)((total + 7) / 8), 256, 0, st>>>(
+            gate_up ? 1 : 0, gate, up, ws.row_base + (size_t)group * total, ws.row_tiles, logical_rows, ws.cols,
+            wide);
     return cudaGetLastError();
 }
 
@@ -375,6 +470,14 @@ cudaError_t launch_repack(int fmt, int layout, bool gate_up, const SrcMat &gate,
         const long long total = (long long)ws.row_tiles * ws.kchunks * 256;
         repack_frag_f16_kernel<<<(unsigned)((total + 127) / 128), 128, 0, st>>>(
             fmt, gate_up ? 1 : 0, gate, up, ws.base + (size_t)group * ws.group_bytes, ws.row_tiles, ws.kchunks,
+            ws.chunk_bytes, logical_rows, ws.cols, bad_scale);
+        return cudaGetLastError();
+    }
+    if (layout == LAYOUT_TILE_I4) {
+        const int logical_rows = gate_up ? I : H;
+        const long long total = (long long)ws.row_tiles * ws.kchunks * TILE_ROWS;
+        repack_tile_i4_kernel<<<(unsigned)((total + 127) / 128), 128, 0, st>>>(
+            gate_up ? 1 : 0, gate, up, ws.base + (size_t)group * ws.group_bytes, ws.row_tiles, ws.kchunks,
             ws.chunk_bytes, logical_rows, ws.cols, bad_scale);
         return cudaGetLastError();
     }

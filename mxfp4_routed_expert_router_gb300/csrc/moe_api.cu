@@ -168,9 +168,6 @@ MoeStatus run_layer(MoeHandle *h, const void *x, const float *logits, const int 
             h->profiled = true;
         return MOE_OK;
     }
-    if (h->fmt == FMT_INT4)
-        return fail(MOE_EINVAL, "INT4 weights run on the single-kernel path only; this batch (T=%d, k=%d) is "
-                                "outside its range", T, k);
     mark(0);
     if (h->E > 0) {
         if (ids_in) {
@@ -339,8 +336,8 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
     h->gu_f = h->gu;
     h->dn_f = h->dn;
     const int f_layout = nib ? LAYOUT_FRAG_F16 : LAYOUT_FRAG;
-    // INT4 runs on the single kernel only, which reads the FRAG copy
-    const bool tile = fmt != FMT_INT4;
+    // every format keeps a TILE-family copy for the tensor-memory GEMMs
+    const bool tile = true;
     // [0] device error flag, [1] a rejected scale at load, [2] an MXFP4 row whose
     // exponents span too widely for FP16 operands
     if ((e = cudaHostAlloc((void **)&h->err_host, 4 * sizeof(int), cudaHostAllocMapped)) != cudaSuccess) {
@@ -399,9 +396,10 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
     };
     // MXFP4 on the tensor-memory GEMMs: FP16 operands when every row's block
     // exponents span at most TILE_F16_MAX_SPREAD (checked on the device, one
-    // pass over the scales), else BF16 operands
+    // pass over the scales), else BF16 operands.  Group-32 INT4: FP16 hi + lo
+    // operands against a per-row base (TILE_I4), always.
     int tile_layout = LAYOUT_TILE;
-    if (tile && fmt == FMT_MXFP4) {
+    if (tile && (fmt == FMT_MXFP4 || fmt == FMT_INT4)) {
         const size_t gu_rb = (size_t)h->gu.row_tiles * TILE_ROWS * G, dn_rb = (size_t)h->dn.row_tiles * TILE_ROWS * G;
         if (cudaMalloc(&h->gu.row_base, gu_rb) != cudaSuccess || cudaMalloc(&h->dn.row_base, dn_rb) != cudaSuccess ||
             cudaMalloc(&h->gu_norm_key, sizeof(int) * (size_t)G) != cudaSuccess ||
@@ -419,10 +417,10 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
         for (int g = 0; g < G; ++g) {
             SrcMat gate{}, up{}, dn{};
             sources(g, gate, up, dn);
-            if ((e = launch_row_base(true, gate, up, h->gu, g, I, c.hidden, wide, st)) != cudaSuccess ||
-                (e = launch_row_base(false, dn, dn, h->dn, g, I, c.hidden, wide, st)) != cudaSuccess ||
-                (e = launch_gu_norm(gate, up, g, I, c.hidden, h->gu_norm_key, st)) != cudaSuccess ||
-                (e = launch_dn_norm(dn, g, I, c.hidden, h->dn_norm_key, st)) != cudaSuccess) {
+            if ((e = launch_row_base(fmt, true, gate, up, h->gu, g, I, c.hidden, wide, st)) != cudaSuccess ||
+                (e = launch_row_base(fmt, false, dn, dn, h->dn, g, I, c.hidden, wide, st)) != cudaSuccess ||
+                (e = launch_gu_norm(fmt, gate, up, g, I, c.hidden, h->gu_norm_key, st)) != cudaSuccess ||
+                (e = launch_dn_norm(fmt, dn, g, I, c.hidden, h->dn_norm_key, st)) != cudaSuccess) {
                 destroy(h);
                 return cuda_fail(e, "row base launch");
             }
@@ -431,7 +429,10 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
             destroy(h);
             return cuda_fail(e, "row bases");
         }
-        if (*(volatile int *)wide == 0) {
+        if (fmt == FMT_INT4) {
+            tile_layout = LAYOUT_TILE_I4;
+            h->tc_f16 = true;
+        } else if (*(volatile int *)wide == 0) {
             tile_layout = LAYOUT_TILE_F16;
             h->tc_f16 = true;
         } else {

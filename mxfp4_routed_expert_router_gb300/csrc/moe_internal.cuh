@@ -55,7 +55,18 @@ constexpr int CHUNK_I4_ZERO_BYTES = TILE_ROWS * CHUNK_K / 32;       // 512: zero
 constexpr int CHUNK_I4_BYTES = CHUNK_MX_CODE_BYTES + CHUNK_I4_SCALE_BYTES + CHUNK_I4_ZERO_BYTES;  // 9728
 constexpr int HALF_K = CHUNK_K / 2;                                 // K of one pipeline stage
 
-enum ChunkLayout { LAYOUT_TILE = 0, LAYOUT_FRAG = 1, LAYOUT_FRAG_F16 = 2, LAYOUT_TILE_F16 = 3 };
+enum ChunkLayout { LAYOUT_TILE = 0, LAYOUT_FRAG = 1, LAYOUT_FRAG_F16 = 2, LAYOUT_TILE_F16 = 3, LAYOUT_TILE_I4 = 4 };
+
+// TILE_I4 layout (tcgen05 kernel, group-32 INT4): the 128-K chunk is four
+// 32-value blocks b; row r's 32 codes of block b are 16 bytes at
+// [(b*128 + r)*16, +16): word c holds values 8c..8c+7 of the block, the pair
+// (8c + 2p, 8c + 2p + 1) in nibbles p and p + 4, so that one shift and one mask
+// put a pair into the two halves of a 32-bit word.  The FP16 scale of (block b,
+// row r) is at [8192 + (b*128 + r)*2], its zero point at [9216 + b*128 + r]
+// (9,728 bytes, as CHUNK_I4_BYTES).  The row base kept beside the chunks is
+// b_row + 127 with b_row = floor(log2 max|s|) - 11 over the row's scales, so
+// that s * 2^-b_row lies below 2^12 and every weight below 15 * 2^12 in FP16.
+constexpr int TILE_I4_BASE_SHIFT = 11;
 
 // TILE_F16 layout (tcgen05 kernel with FP16 operands, MXFP4 only): the 128-K
 // chunk is four 32-value blocks b; row r's codes of block b are 16 plain pack4
@@ -204,20 +215,21 @@ cudaError_t launch_gather_rows(const Plan &p, const uint16_t *x, cudaStream_t st
 
 // row bases of a TILE_F16 store for one group: for every tile row, the
 // largest E8M0 exponent over the row's K; a row whose exponents span more than
-// TILE_F16_MAX_SPREAD sets *wide
-cudaError_t launch_row_base(bool gate_up, const SrcMat &gate, const SrcMat &up, const WeightStore &ws, int group,
-                            int I, int H, int *wide, cudaStream_t st);
+// TILE_F16_MAX_SPREAD sets *wide.  With fmt FMT_INT4, the TILE_I4 row base
+// (see above; wide is not used)
+cudaError_t launch_row_base(int fmt, bool gate_up, const SrcMat &gate, const SrcMat &up, const WeightStore &ws,
+                            int group, int I, int H, int *wide, cudaStream_t st);
 
 // For the h scales of the tcgen05 path with FP16 operands: out[group] = an
 // order-preserving integer key of max_n log2(|w_g,n| |w_u,n|) over the
 // features n of one group (Euclidean norms of the decoded gate and up rows of
 // an MXFP4 matrix, rounded up; unsigned order of the key bits); out[group]
 // must start at 0
-cudaError_t launch_gu_norm(const SrcMat &gate, const SrcMat &up, int group, int I, int H, int *out,
+cudaError_t launch_gu_norm(int fmt, const SrcMat &gate, const SrcMat &up, int group, int I, int H, int *out,
                            cudaStream_t st);
 // the same for the rows of a down matrix (H rows of I values): a key of
-// max_m log2 |w_d,m|
-cudaError_t launch_dn_norm(const SrcMat &dn, int group, int I, int H, int *out, cudaStream_t st);
+// max_m log2 |w_d,m|.  fmt: FMT_MXFP4 or FMT_INT4 (group-32 INT4 sources)
+cudaError_t launch_dn_norm(int fmt, const SrcMat &dn, int group, int I, int H, int *out, cudaStream_t st);
 
 // tcgen05 path with FP16 operands (after the permutation): FP16 token rows x16,
 // their copies in routed position order (x_perm), the powers of two xs / xsp,

@@ -200,3 +200,50 @@ def test_i4_fragment_word_maps_pairs_to_registers():
             z = zb if p & 1 else za       # pairs 1 and 3 belong to row g + 8
             got = decode_i4_pair(w, p, z)
             assert got[0] == first[p] - z and got[1] == second[p] - z
+
+
+# ------------------------------------------------------------------ group-32 INT4 (tensor-core GEMMs)
+# The TILE_I4 decoder turns s (q - z) into two FP16 values: s' = s * 2^-b_row in
+# FP16 (b_row = floor(log2 max|s|) - 11 over the row, so s' < 2^12), qz = q - z
+# as above, hi = fp16(qz * s') and lo = fp16(qz * s' - hi) from a fused
+# multiply-add, which rounds once from the exact value.  Emulated with numpy:
+# the exact product and residual in float64, each rounded once to float16.
+
+def i4_hilo(qz, s_prime):
+    prod = float(qz) * float(s_prime)             # exact: 4 x 11 significant bits
+    hi = np.float16(prod)
+    lo = np.float16(prod - float(hi))             # one rounding of the exact residual
+    return hi, lo, prod
+
+
+def test_i4_hi_lo_split_is_exact_for_normal_scales():
+    rng = np.random.default_rng(5)
+    # FP16 scales s' across the normal range below 2^12, including the extremes
+    sp = [np.float16(2.0 ** -14), np.float16(4095.0), np.float16(1.0), np.float16(0.3)]
+    sp += [np.float16(v) for v in np.exp2(rng.uniform(-14, 12, 400)) * rng.choice([-1, 1], 400)]
+    for s in sp:
+        assert np.isfinite(s) and abs(float(s)) >= 2.0 ** -14
+        for qz in range(-15, 16):
+            hi, lo, prod = i4_hilo(qz, s)
+            assert float(hi) + float(lo) == prod, (qz, float(s))
+            assert abs(float(hi)) <= 15 * 4096
+
+
+def test_i4_row_base_keeps_scales_exact_and_weights_finite():
+    rng = np.random.default_rng(6)
+    for _ in range(300):
+        top = int(rng.integers(-24, 16))           # exponent of the row's largest FP16 scale
+        s_max = np.float16(np.exp2(top) * rng.uniform(1.0, 1.999))
+        if not np.isfinite(s_max) or s_max == 0:
+            continue
+        b = int(np.floor(np.log2(float(s_max)))) - 11
+        for d in range(0, 25):                      # groups up to 2^-24 below the row's largest
+            s = np.float16(float(s_max) * 2.0 ** -d * rng.uniform(0.5, 1.0))
+            if s == 0:
+                continue
+            sp = np.float16(float(s) * 2.0 ** -b)   # exact unless it falls below the FP16 normal range
+            if abs(float(sp)) >= 2.0 ** -14:
+                assert float(sp) == float(s) * 2.0 ** -b
+            assert abs(float(sp)) < 4096.0
+            hi, lo, prod = i4_hilo(15, sp)
+            assert np.isfinite(hi) and abs(float(hi)) <= 15 * 4096
