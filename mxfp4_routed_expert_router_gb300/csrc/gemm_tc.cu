@@ -93,6 +93,16 @@ static_assert(N_DEC_GROUPS == A_STAGES, "one decoder group per A slot");
 constexpr int B_SLICE_BYTES = NMAX * HALF_K * 2;  // 24 KB: 192 token rows x 64 16-bit values (one swizzled tile)
 constexpr int B_STAGE_BYTES = 2 * B_SLICE_BYTES;  // two slices: 128 K values of one plane, or 64 of two planes
 static_assert(B_SLICE_BYTES % 1024 == 0, "swizzled tiles start on 1024-byte boundaries");
+// BF16 weights need no decode: their A tiles (128 rows x 64 values, one
+// swizzled 16 KB tile per 64-wide half of a chunk of the TILE store) come by
+// TMA into the same shared-memory stage as the token tiles, and the MMA reads A
+// from there.  Stages are 64 values of K: a token slice (two for down, h hi and
+// lo) plus the A tile, five stages (40 KB) for gate|up and three (64 KB) for down.
+constexpr int A_SMEM_TILE = TILE_ROWS * HALF_K * 2;
+constexpr int RING_MAX = 5;
+constexpr int RING_BYTES_MAX = 5 * (B_SLICE_BYTES + A_SMEM_TILE);
+static_assert(RING_BYTES_MAX >= B_STAGES * B_STAGE_BYTES && RING_BYTES_MAX >= 3 * (2 * B_SLICE_BYTES + A_SMEM_TILE),
+              "ring room");
 // B operand TMA boxes: 64 token rows (8 KB) each, so that a stage takes few
 // TMA issues; 16 rows when a B tensor has fewer than 64 rows
 constexpr int B_BOX_ROWS_BIG = 64, B_BOX_ROWS_SMALL = 16;
@@ -222,6 +232,23 @@ __device__ __forceinline__ uint32_t make_idesc(int n)
     return (1u << 4) | ab | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(TILE_ROWS >> 4) << 24);
 }
 
+// The four K=16 MMAs of one 64-wide stage with both operands in shared memory
+// (128-byte-swizzled K-major tiles): both descriptors advance by 32 bytes (2 in
+// the address field) per K step.
+__device__ __forceinline__ void tc_mma4_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t acc0)
+{
+    asm volatile(
+        "{\n .reg .pred p0, p1;\n setp.ne.b32 p0, %4, 0;\n setp.eq.b32 p1, %4, %4;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %3, p1;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %3, p1;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %10, %3, p1;\n}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc0), "l"(a_desc + 2), "l"(b_desc + 2), "l"(a_desc + 4),
+        "l"(b_desc + 4), "l"(a_desc + 6), "l"(b_desc + 6)
+        : "memory");
+}
+
 // One INT4 pair into FP16 hi and lo words: w holds the pair's codes in bits
 // 0..3 and 16..19; 0x6400 | q is the FP16 value 1024 + q (ulp 1), so
 // subtracting zz = {1024 + z, 1024 + z} leaves q - z exactly; hi = s2 (q - z)
@@ -262,8 +289,8 @@ __device__ __forceinline__ void e2m1x8_f16(uint32_t w, uint32_t s2, uint32_t *ou
 __device__ __forceinline__ float pow2i(int k) { return __int_as_float((127 + k) << 23); }
 
 struct Smem {
-    static constexpr int BAR_OFF = B_STAGES * B_STAGE_BYTES;
-    static constexpr int N_BARS = 2 * B_STAGES + 2 * A_STAGES + 2 * NBUF;
+    static constexpr int BAR_OFF = RING_BYTES_MAX;
+    static constexpr int N_BARS = 2 * RING_MAX + 2 * A_STAGES + 2 * NBUF;
     static constexpr int SCHED_OFF = BAR_OFF + N_BARS * 8;
     static constexpr int MISC_OFF = SCHED_OFF + (MAX_GROUPS + 1) * 4;
     static constexpr int COLSC_OFF = MISC_OFF + 32;    // epilogue: column scales of an item, one row per warp
@@ -275,25 +302,31 @@ struct Smem {
 
 template <bool GU, int OP, int WFMT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_b2)
+    gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_b2,
+                   const __grid_constant__ CUtensorMap map_a)
 {
     static_assert(OP == OP_BF16 || (OP == OP_F16 && WFMT == FMT_MXFP4) || (OP == OP_I4 && WFMT == FMT_INT4),
                   "FP16 operands decode MXFP4 weights, FP16 pairs INT4 weights");
     constexpr bool FT = OP != OP_BF16;                  // FP16 token operands (x16, h16) and scaled epilogues
     constexpr int NB = (!GU && OP == OP_BF16) ? 2 : 1;  // token planes: down with BF16 operands reads h hi + lo
-    constexpr int KST = (NB == 2 || OP == OP_I4) ? HALF_K : CHUNK_K;  // K values per stage
+    constexpr bool AS = WFMT == FMT_BF16;               // A by TMA into shared memory (BF16 weights)
+    constexpr int KST = (AS || NB == 2 || OP == OP_I4) ? HALF_K : CHUNK_K;  // K values per stage
     constexpr int NSL = KST / HALF_K;                   // 64-wide K slices per stage
     constexpr int NSLB = NSL * NB;                      // swizzled B tiles per stage
     constexpr int NBLK = KST / 32;                      // 32-value blocks per stage
     using L = Smem;
     static_assert(L::TOTAL <= 232448, "shared memory");
-    static_assert(NSLB == 2 || (OP == OP_I4 && NSLB == 1), "a stage holds two swizzled B tiles (INT4: one)");
+    static_assert(NSLB == 2 || ((OP == OP_I4 || AS) && NSLB == 1), "a stage holds two swizzled B tiles (INT4: one)");
+    // the stage ring: token tiles, and with AS the A tile after them
+    constexpr int STAGE_BYTES = AS ? NSLB * B_SLICE_BYTES + A_SMEM_TILE : B_STAGE_BYTES;
+    constexpr int RING = AS ? (NSLB == 1 ? 5 : 3) : B_STAGES;
+    static_assert(RING <= RING_MAX && RING * STAGE_BYTES <= RING_BYTES_MAX && STAGE_BYTES % 1024 == 0, "ring");
 
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);
-    uint64_t *b_full = bars, *b_empty = b_full + B_STAGES;
-    uint64_t *a_full = b_empty + B_STAGES, *a_empty = a_full + A_STAGES;
+    uint64_t *b_full = bars, *b_empty = b_full + RING_MAX;
+    uint64_t *a_full = b_empty + RING_MAX, *a_empty = a_full + A_STAGES;
     uint64_t *acc_full = a_empty + A_STAGES, *acc_empty = acc_full + NBUF;
     int *prefix = reinterpret_cast<int *>(smem + L::SCHED_OFF);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);
@@ -304,7 +337,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int rb_stride = a.row_tiles * TILE_ROWS;
 
     if (tid == 0) {
-        for (int i = 0; i < B_STAGES; ++i) {
+        for (int i = 0; i < RING; ++i) {
             mbar_init(&b_full[i], 1);  // the token copies (expect-tx)
             mbar_init(&b_empty[i], 1);
         }
@@ -331,6 +364,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == WARP_BLOAD && lane == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b2)) : "memory");
+        if (AS)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a)) : "memory");
     }
     tc_fence_before();
     __syncthreads();
@@ -382,17 +417,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // read, or zero fill past the tensor's last row)
             const int nbox = (w.n_mma + a.brows - 1) / a.brows;
             const int box_bytes = a.brows * HALF_K * 2;
-            const uint32_t bytes = (uint32_t)(nbox * box_bytes * NSLB);
+            const uint32_t bytes = (uint32_t)(nbox * box_bytes * NSLB) + (AS ? (uint32_t)A_SMEM_TILE : 0u);
+            // AS: the item's A tiles, rows of the TILE store seen as [halves * 128][64]
+            const int a_row0 = ((w.g * rt_n + w.rt) * a.kchunks) * 2 * TILE_ROWS;
             for (int st = 0; st < nstages; ++st, ++sc) {
-                const int slot = sc % B_STAGES;
-                const uint32_t ph = (sc / B_STAGES) & 1;
+                const int slot = sc % RING;
+                const uint32_t ph = (sc / RING) & 1;
                 if (!(ok = mbar_wait_sleep_warp(&b_empty[slot], ph ^ 1, abort_flag, a.err, lane)))
                     break;
                 if (KST == CHUNK_K || (st & 1) == 0)
                     pf_next();
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&b_full[slot], bytes);
-                    uint8_t *bdst = smem + slot * B_STAGE_BYTES;
+                    uint8_t *bdst = smem + slot * STAGE_BYTES;
+                    if (AS)
+                        tma_2d(bdst + NSLB * B_SLICE_BYTES, &map_a, 0, a_row0 + st * TILE_ROWS, &b_full[slot]);
                     // the stage's two swizzled tiles: two 64-wide K slices of one plane,
                     // or one slice of the h hi and lo planes
                     for (int b = 0; b < nbox; ++b) {
@@ -416,7 +455,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // drain: every armed stage's B tiles have landed (returns at once on the
         // normal path, where the MMA has consumed them; bounded after an abort)
         if (lane == 0)
-            for (int s = 0; s < B_STAGES; ++s)
+            for (int s = 0; s < RING; ++s)
                 if (armed & (1u << s))
                     mbar_drain(&b_full[s], (armed_par >> s) & 1);
         __syncwarp();
@@ -440,14 +479,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     // a_full completes once the stage's A is in tensor memory and its B
                     // tiles have landed (the decoder group waits for the token copy
                     // before it arrives), so each stage costs the MMA thread one wait
-                    const int bs = sc % B_STAGES, as = sc % A_STAGES;
-                    if (!(ok = mbar_wait(&a_full[as], (sc / A_STAGES) & 1, abort_flag, a.err)))
+                    const int bs = sc % RING, as = sc % A_STAGES;
+                    // AS: the stage's A and B tiles come together on b_full
+                    if (!(ok = AS ? mbar_wait(&b_full[bs], (sc / RING) & 1, abort_flag, a.err)
+                                  : mbar_wait(&a_full[as], (sc / A_STAGES) & 1, abort_flag, a.err)))
                         break;
                     tc_fence_after();
                     // descriptors of this slot: base plus the slot's offset (address field = bytes >> 4)
-                    const uint64_t bd = desc0 + (uint64_t)((bs * B_STAGE_BYTES) >> 4);
+                    const uint64_t bd = desc0 + (uint64_t)((bs * STAGE_BYTES) >> 4);
                     const uint32_t at = tmem_base + (uint32_t)(TMEM_A0 + as * A_SLOT_COLS);
-                    if (OP == OP_I4) {
+                    if (AS) {
+                        const uint64_t ad = bd + (uint64_t)((NSLB * B_SLICE_BYTES) >> 4);
+                        tc_mma4_ss(d_tmem, ad, bd, idesc, st);
+                        if (NB == 2)
+                            tc_mma4_ss(d_tmem, ad, bd + (uint64_t)(B_SLICE_BYTES >> 4), idesc, 1u);
+                    } else if (OP == OP_I4) {
                         // the stage's 64 values of K: the hi tile (columns 0..31), then the lo tile
                         tc_mma4(d_tmem, at, bd, idesc, st);
                         tc_mma4(d_tmem, at + 32, bd, idesc, 1u);
@@ -461,7 +507,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         tc_mma4(d_tmem, at, bd + (uint64_t)(B_SLICE_BYTES >> 4), idesc, 1u);
                     }
                     tc_commit(&b_empty[bs]);
-                    tc_commit(&a_empty[as]);
+                    if (!AS)
+                        tc_commit(&a_empty[as]);
                     partial = true;
                 }
                 if (!ok)
@@ -494,7 +541,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int r = 32 * q + lane;  // row inside the tile
         const uint32_t tlane = (uint32_t)(32 * q) << 16;
         const int n_items = total > (int)blockIdx.x ? (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
-        const int total_st = n_items * nstages;
+        const int total_st = AS ? 0 : n_items * nstages;  // AS: the A tiles come by TMA, no decoding
         uint4 rc[NBLK];   // MXFP4: 16 code bytes per 32-value block
         uint32_t re[NBLK], rb = 127;
         const uint8_t *src = nullptr;  // the stage's chunk
@@ -607,7 +654,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // the stage's token tiles must have landed too: the MMA thread waits on
             // a_full alone (this group waited on this B slot four stages ago, so the
             // parity below is never two phases ahead)
-            if (!(ok = mbar_wait_warp(&b_full[gs % B_STAGES], (gs / B_STAGES) & 1, abort_flag, a.err, lane)))
+            if (!(ok = mbar_wait_warp(&b_full[gs % RING], (gs / RING) & 1, abort_flag, a.err, lane)))
                 break;
             if (lane == 0)
                 mbar_arrive(&a_full[slot]);
@@ -740,7 +787,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // ------------------------------------------------------------------ host side
 
 template <bool GU, int OP, int WFMT>
-cudaError_t launch_cfg(const TcArgs &a, const CUtensorMap &m1, const CUtensorMap &m2, cudaStream_t st)
+cudaError_t launch_cfg(const TcArgs &a, const CUtensorMap &m1, const CUtensorMap &m2, const CUtensorMap &ma,
+                       cudaStream_t st)
 {
     constexpr int SMEM = Smem::TOTAL;
     auto kern = gemm_tc_kernel<GU, OP, WFMT>;
@@ -748,20 +796,33 @@ cudaError_t launch_cfg(const TcArgs &a, const CUtensorMap &m1, const CUtensorMap
     cudaError_t e = smem_limit_once(attr_set, (const void *)kern, SMEM);
     if (e != cudaSuccess)
         return e;
-    kern<<<sm_count(), NUM_THREADS, SMEM, st>>>(a, m1, m2);
+    kern<<<sm_count(), NUM_THREADS, SMEM, st>>>(a, m1, m2, ma);
     return cudaGetLastError();
 }
 
+// The A tensor map of a BF16 TILE store: its 64-wide halves of 128 rows as a
+// [G * row_tiles * kchunks * 2 * 128][64] BF16 tensor, 128-row boxes.
+cudaError_t make_a_map(CUtensorMap *m, const WeightStore &w, int G)
+{
+    const long long rows = (long long)G * w.row_tiles * w.kchunks * 2 * TILE_ROWS;
+    return make_map(m, w.base, rows, HALF_K, TILE_ROWS);
+}
+
 template <bool GU>
-cudaError_t launch_any(const TcArgs &a, int fmt, bool f16, const CUtensorMap &m1, const CUtensorMap &m2,
-                       cudaStream_t st)
+cudaError_t launch_any(const TcArgs &a, const WeightStore &w, int fmt, bool f16, const CUtensorMap &m1,
+                       const CUtensorMap &m2, cudaStream_t st)
 {
     if (f16)
-        return fmt == FMT_MXFP4  ? launch_cfg<GU, OP_F16, FMT_MXFP4>(a, m1, m2, st)
-               : fmt == FMT_INT4 ? launch_cfg<GU, OP_I4, FMT_INT4>(a, m1, m2, st)
+        return fmt == FMT_MXFP4  ? launch_cfg<GU, OP_F16, FMT_MXFP4>(a, m1, m2, m1, st)
+               : fmt == FMT_INT4 ? launch_cfg<GU, OP_I4, FMT_INT4>(a, m1, m2, m1, st)
                                  : cudaErrorInvalidValue;
-    return fmt == FMT_MXFP4 ? launch_cfg<GU, OP_BF16, FMT_MXFP4>(a, m1, m2, st)
-                            : launch_cfg<GU, OP_BF16, FMT_BF16>(a, m1, m2, st);
+    if (fmt == FMT_MXFP4)
+        return launch_cfg<GU, OP_BF16, FMT_MXFP4>(a, m1, m2, m1, st);
+    CUtensorMap ma;
+    cudaError_t e = make_a_map(&ma, w, a.G);
+    if (e != cudaSuccess)
+        return e;
+    return launch_cfg<GU, OP_BF16, FMT_BF16>(a, m1, m2, ma, st);
 }
 
 TcArgs base_args(const Plan &p, const WeightStore &w)
@@ -974,7 +1035,7 @@ cudaError_t launch_gemm_gate_up_tc(const Plan &p, const WeightStore &w, int fmt,
     } else {
         m1 = m2;
     }
-    return launch_any<true>(a, fmt, f16, m1, m2, st);
+    return launch_any<true>(a, w, fmt, f16, m1, m2, st);
 }
 
 cudaError_t launch_gemm_down_tc(const Plan &p, const WeightStore &w, int fmt, bool f16, cudaStream_t st)
@@ -997,7 +1058,7 @@ cudaError_t launch_gemm_down_tc(const Plan &p, const WeightStore &w, int fmt, bo
         if ((e = make_map(&m2, p.h + (size_t)p.P * p.I, p.P, p.I, a.brows)) != cudaSuccess)
             return e;
     }
-    return launch_any<false>(a, fmt, f16, m1, m2, st);
+    return launch_any<false>(a, w, fmt, f16, m1, m2, st);
 }
 
 }  // namespace moe
