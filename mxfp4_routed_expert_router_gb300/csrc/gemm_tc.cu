@@ -41,20 +41,28 @@
 //     down runs one MMA per K step and writes y as FP16 with a power of two
 //     per position from a bound on |y| (half the bytes of FP32 y for the
 //     combine to read).
-//   BF16: BF16 weights, or MXFP4 whose exponents spread wider.  Weights decode
-//     exactly to BF16 v(c) * 2^(e - 127); tokens are the caller's BF16 rows; h
-//     is kept as BF16 hi + lo planes (lo = bf16(h - hi)), so down runs two MMAs
-//     per K step (and its stages hold 64 values of K, to keep 64 KB of B).
+//   FP16 hi + lo (group-32 INT4): w = s (q - z) relative to a power of two per
+//     row, split into an exact FP16 pair; the decoders write hi and lo into the
+//     two halves of an A slot, stages are 64 values of K, and the MMA thread
+//     runs four MMAs on each half.  Tokens, h and y as for FP16.
+//   BF16: BF16 weights, or MXFP4 whose exponents spread wider.  MXFP4 decodes
+//     exactly to BF16 v(c) * 2^(e - 127); BF16 weights need no decode, and
+//     their A tiles come by TMA into the token tiles' shared-memory stage,
+//     the MMAs reading both operands from shared memory (the decoder warps
+//     idle).  Tokens are the caller's BF16 rows; h is kept as BF16 hi + lo
+//     planes (lo = bf16(h - hi)), so down runs two MMAs per K step (and its
+//     stages hold 64 values of K, to keep 64 KB of B).
 // One CTA per SM walks a static schedule of work items.  Warp roles:
-//   warp 0      TMA-loads token tiles (B) into the shared-memory stage ring and
-//               prefetches the weight chunks ahead of the decoders into L2
+//   warp 0      TMA-loads token tiles (B; with BF16 weights also the A tiles)
+//               into the shared-memory stage ring and prefetches the weight
+//               chunks ahead into L2
 //   warp 1      allocates tensor memory, issues the MMAs, commits to mbarriers
 //   warps 2-9   decode weights into the tensor-memory A ring: two groups of
 //               four warps, group g decoding every other stage (A slot g) in
 //               full; its warp w covers lane quadrant w % 4 (the lanes a warp
 //               may access)
 //   warps 10-17 epilogue, two warps per lane quadrant splitting the columns:
-//               tensor memory -> registers, SwiGLU (gate|up) or FP32 y (down).
+//               tensor memory -> registers, SwiGLU (gate|up) or y (down).
 // Every mbarrier wait is bounded: on a timeout the kernel records
 // DEV_ERR_WAIT_TIMEOUT, stops issuing work, waits (bounded) for the copies and
 // MMAs it has in flight, frees its tensor memory and exits.
