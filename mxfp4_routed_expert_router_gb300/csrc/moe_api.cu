@@ -336,8 +336,6 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
     h->gu_f = h->gu;
     h->dn_f = h->dn;
     const int f_layout = nib ? LAYOUT_FRAG_F16 : LAYOUT_FRAG;
-    // every format keeps a TILE-family copy for the tensor-memory GEMMs
-    const bool tile = true;
     // [0] device error flag, [1] a rejected scale at load, [2] an MXFP4 row whose
     // exponents span too widely for FP16 operands
     if ((e = cudaHostAlloc((void **)&h->err_host, 4 * sizeof(int), cudaHostAllocMapped)) != cudaSuccess) {
@@ -350,14 +348,16 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
         destroy(h);
         return cuda_fail(e, "cudaHostGetDevicePointer");
     }
-    if ((tile && cudaMalloc(&h->gu.base, h->gu.group_bytes * G) != cudaSuccess) ||
-        (tile && cudaMalloc(&h->dn.base, h->dn.group_bytes * G) != cudaSuccess) ||
+    // two copies of every weight: a TILE-family one for the tensor-memory GEMMs and
+    // a FRAG one for the single-kernel layer
+    if (cudaMalloc(&h->gu.base, h->gu.group_bytes * G) != cudaSuccess ||
+        cudaMalloc(&h->dn.base, h->dn.group_bytes * G) != cudaSuccess ||
         cudaMalloc(&h->gu_f.base, h->gu_f.group_bytes * G) != cudaSuccess ||
         cudaMalloc(&h->dn_f.base, h->dn_f.group_bytes * G) != cudaSuccess) {
         cudaGetLastError();
         destroy(h);
         return fail(MOE_ENOMEM, "device allocation of %zu bytes of weights failed",
-                    (tile ? 2 : 1) * (h->gu.group_bytes + h->dn.group_bytes) * (size_t)G);
+                    2 * (h->gu.group_bytes + h->dn.group_bytes) * (size_t)G);
     }
     int *bad_scale = &h->err_dev[1];
     // scale (and INT4 zero point) arrays advanced by a number of elements; NULL
@@ -399,7 +399,7 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
     // pass over the scales), else BF16 operands.  Group-32 INT4: FP16 hi + lo
     // operands against a per-row base (TILE_I4), always.
     int tile_layout = LAYOUT_TILE;
-    if (tile && (fmt == FMT_MXFP4 || fmt == FMT_INT4)) {
+    if (fmt == FMT_MXFP4 || fmt == FMT_INT4) {
         const size_t gu_rb = (size_t)h->gu.row_tiles * TILE_ROWS * G, dn_rb = (size_t)h->dn.row_tiles * TILE_ROWS * G;
         if (cudaMalloc(&h->gu.row_base, gu_rb) != cudaSuccess || cudaMalloc(&h->dn.row_base, dn_rb) != cudaSuccess ||
             cudaMalloc(&h->gu_norm_key, sizeof(int) * (size_t)G) != cudaSuccess ||
@@ -447,10 +447,10 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
     for (int g = 0; g < G; ++g) {
         SrcMat gate{}, up{}, dn{};
         sources(g, gate, up, dn);
-        if ((tile && (e = launch_repack(fmt, tile_layout, true, gate, up, h->gu, g, I, c.hidden, bad_scale, st)) !=
-                         cudaSuccess) ||
-            (tile && (e = launch_repack(fmt, tile_layout, false, dn, dn, h->dn, g, I, c.hidden, bad_scale, st)) !=
-                         cudaSuccess) ||
+        if ((e = launch_repack(fmt, tile_layout, true, gate, up, h->gu, g, I, c.hidden, bad_scale, st)) !=
+                cudaSuccess ||
+            (e = launch_repack(fmt, tile_layout, false, dn, dn, h->dn, g, I, c.hidden, bad_scale, st)) !=
+                cudaSuccess ||
             (e = launch_repack(fmt, f_layout, true, gate, up, h->gu_f, g, I, c.hidden, bad_scale, st)) !=
                 cudaSuccess ||
             (e = launch_repack(fmt, f_layout, false, dn, dn, h->dn_f, g, I, c.hidden, bad_scale, st)) !=
