@@ -191,14 +191,21 @@ MoeStatus moe_forward(MoeHandle *h, const void *x_bf16, const float *router_logi
  * whose expert computation receives one expert id and one weight per
  * selection from a router that runs elsewhere (the shared experts are added
  * with weight 1, as in moe_forward).
- *  topk_ids [T][k] int32 in [0, E), 4-byte aligned (an expert may appear more
- *           than once for a token; each occurrence is its own slot)
+ *  topk_ids [T][k] int32 in [0, E) or -1, 4-byte aligned (an expert may
+ *           appear more than once for a token; each occurrence is its own
+ *           slot).  -1 is an empty slot: it adds nothing and its weight is
+ *           not read.  A holder of a subset of the experts passes the routing
+ *           with the other experts' slots set to -1 and gets its part of the
+ *           sum over experts (each holder adds the shared experts it holds).
  *  topk_w   [T][k] float, 4-byte aligned, used as given
  *  other arguments as for moe_forward; `routing` receives the copy of the
- *  ids and weights the layer ran with and the grouping.
- * An id outside [0, E) cannot be checked on the host: the device records it,
- * runs that slot as expert 0 with weight 0 so that every access stays in
- * bounds, and moe_sync_status() then reports MOE_EDEVICE.
+ *  ids and weights the layer ran with (an empty slot: id -1, weight 0) and
+ *  the grouping: expert_offsets[E] is then the number of non-empty slots,
+ *  slot_pos is -1 for an empty slot and sorted_slot is -1 at the positions
+ *  from expert_offsets[E] to T*k.
+ * Any other id outside [0, E) cannot be checked on the host: the device
+ * records it, runs that slot as expert 0 with weight 0 so that every access
+ * stays in bounds, and moe_sync_status() then reports MOE_EDEVICE.
  * Errors: MOE_EINVAL (NULL/misaligned pointers, T < 0, k outside [1, k_max],
  * a dense handle), MOE_EWORKSPACE, MOE_EDEVICE, MOE_ECUDA. */
 MoeStatus moe_forward_routed(MoeHandle *h, const void *x_bf16, const int32_t *topk_ids, const float *topk_w, int T,

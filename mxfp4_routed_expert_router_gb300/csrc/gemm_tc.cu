@@ -978,7 +978,8 @@ __global__ void token_prep_f16_kernel(const uint16_t *__restrict__ x, int H, uin
         const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
         dst[i] = ov;
         for (int j = 0; j < k; ++j)
-            reinterpret_cast<uint4 *>(x_perm + (size_t)pos[j] * H)[i] = ov;
+            if (pos[j] >= 0)  // (an empty slot of caller routing has no position)
+                reinterpret_cast<uint4 *>(x_perm + (size_t)pos[j] * H)[i] = ov;
     }
     for (int o = 16; o > 0; o >>= 1)
         ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -993,7 +994,7 @@ __global__ void token_prep_f16_kernel(const uint16_t *__restrict__ x, int H, uin
     const float lx = ss > 0.f ? 2.f * (float)sc + __log2f(ss) + 0.01f : -2000.f;
     if (threadIdx.x == 0)
         xs[t] = sc;
-    if ((int)threadIdx.x < k) {
+    if ((int)threadIdx.x < k && pos[threadIdx.x] >= 0) {
         const int p = pos[threadIdx.x];
         const int e = topk_ids[(size_t)t * k + threadIdx.x];
         const int hs = h_scale_of(lx, ordered_key_to_float(gkey[e]));

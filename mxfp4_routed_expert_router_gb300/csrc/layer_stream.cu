@@ -481,15 +481,18 @@ __device__ void ls_route_warp(const LayerArgs &a, int t, int lane, int *ids_s, b
 }
 
 // Routing given by the caller for token t (one warp): lane j < k takes its id
-// and weight; an id outside [0, E) records DEV_ERR_BOUNDS and becomes expert 0
-// with weight 0, so that the layer stays in bounds.  The ids go to ids_s when
+// and weight; id -1 is an empty slot (kept, weight 0); any other id outside
+// [0, E) records DEV_ERR_BOUNDS and becomes expert 0 with weight 0, so that
+// the layer stays in bounds.  The ids go to ids_s when
 // given, and the owner CTA writes both to the call's routing arrays.
 __device__ void ls_copy_route_warp(const LayerArgs &a, int t, int lane, int *ids_s, bool owner)
 {
     if (lane < a.k) {
         int e = __ldg(a.ids_in + (size_t)t * a.k + lane);
         float wv = __ldg(a.w_in + (size_t)t * a.k + lane);
-        if (e < 0 || e >= a.E) {
+        if (e == -1) {
+            wv = 0.f;
+        } else if (e < 0 || e >= a.E) {
             atomicCAS(a.err, 0, DEV_ERR_BOUNDS);
             e = 0;
             wv = 0.f;
@@ -571,7 +574,8 @@ __device__ __forceinline__ int ls_group_of(int j, int E, int G) { return j < G -
 // Groups, positions, token tiles and (routed) the stable permutation, in
 // shared memory.  Positions: routed slots 0..n-1 in expert-major order (slots
 // of one expert in ascending slot order s = t*k + j), then shared group s at
-// n + s*T + t.  gcnt[g] / gstart[g]: tokens and first position of group g;
+// n + s*T + t.  An empty slot (id -1, from caller routing) takes no position;
+// the routed positions from expert_offsets[E] to n are then left unused.  gcnt[g] / gstart[g]: tokens and first position of group g;
 // tpre[j]: first token tile of the j-th group in work-list order (ls_group_of;
 // a group of c tokens has ceil(c/ROWS) tiles); sorted[p]: slot at routed
 // position p, replaced by its token once CTA 0 has published the permutation;
@@ -597,7 +601,8 @@ __device__ void ls_schedule(const LayerArgs &a, uint8_t *scratch, int *gcnt, int
     }
     __syncthreads();
     for (int s = tid; s < n; s += LS_THREADS)
-        atomicAdd(&gcnt[sid[s]], 1);
+        if (sid[s] >= 0)
+            atomicAdd(&gcnt[sid[s]], 1);
     __syncthreads();
     // group scan in work-list order: positions (routed groups only, which keeps
     // them in expert order) and token tiles, 32 groups per warp, LS_WARPS * 32
@@ -655,8 +660,8 @@ __device__ void ls_schedule(const LayerArgs &a, uint8_t *scratch, int *gcnt, int
         if (warp == 0) {
             for (int base = 0; base < n; base += 32) {
                 const int s = base + lane;
-                const bool act = s < n;
-                const int e = act ? sid[s] : -1;
+                const int e = s < n ? sid[s] : -1;
+                const bool act = e >= 0;
                 const unsigned m = __match_any_sync(0xffffffffu, e);
                 if (act)
                     sorted[wc[e] + __popc(m & ((1u << lane) - 1u))] = s;
@@ -676,7 +681,8 @@ __device__ void ls_schedule(const LayerArgs &a, uint8_t *scratch, int *gcnt, int
             my[e] = 0;
         __syncwarp();
         for (int s = lo + lane; s < hi; s += 32)
-            atomicAdd(&my[sid[s]], 1);
+            if (sid[s] >= 0)
+                atomicAdd(&my[sid[s]], 1);
         __syncthreads();
         for (int e = tid; e < E; e += LS_THREADS) {
             int run = gstart[e];
@@ -689,8 +695,8 @@ __device__ void ls_schedule(const LayerArgs &a, uint8_t *scratch, int *gcnt, int
         __syncthreads();
         for (int base = lo; base < hi; base += 32) {
             const int s = base + lane;
-            const bool act = s < hi;
-            const int e = act ? sid[s] : -1;
+            const int e = s < hi ? sid[s] : -1;
+            const bool act = e >= 0;
             const unsigned m = __match_any_sync(0xffffffffu, e);
             if (act)
                 sorted[my[e] + __popc(m & ((1u << lane) - 1u))] = s;
@@ -700,15 +706,22 @@ __device__ void ls_schedule(const LayerArgs &a, uint8_t *scratch, int *gcnt, int
             __syncwarp();
         }
     }
+    // (base_pos: the routed positions taken, n less the empty slots)
+    for (int p = base_pos + tid; p < n; p += LS_THREADS)
+        sorted[p] = -1;
     __syncthreads();
     if (blockIdx.x == 0) {
         for (int e = tid; e <= E; e += LS_THREADS)
-            a.expert_offsets[e] = e < E ? gstart[e] : n;
+            a.expert_offsets[e] = e < E ? gstart[e] : base_pos;
         for (int p = tid; p < n; p += LS_THREADS) {
             const int s = sorted[p];
             a.sorted_slot[p] = s;
-            a.slot_pos[s] = p;
+            if (s >= 0)
+                a.slot_pos[s] = p;
         }
+        for (int s = tid; s < n; s += LS_THREADS)
+            if (sid[s] < 0)
+                a.slot_pos[s] = -1;
         __syncthreads();
         if (tid == 0) {
             __threadfence();
@@ -718,7 +731,7 @@ __device__ void ls_schedule(const LayerArgs &a, uint8_t *scratch, int *gcnt, int
     // from here on the GEMMs need only each routed position's token
     __syncthreads();
     for (int p = tid; p < n; p += LS_THREADS)
-        sorted[p] /= a.k;
+        sorted[p] = sorted[p] < 0 ? 0 : sorted[p] / a.k;
 }
 
 // ------------------------------------------------------------------ work items
@@ -780,7 +793,8 @@ __device__ __forceinline__ int ls_row_token(const LayerArgs &a, const int *tokp,
 }
 
 // out[t][f..f+3] (+)= sum_{j<k} w_tj y[slot_pos[t*k+j]][f..] + sum_s y[n+s*T+t][f..],
-// in that order; loads in batches of 8 so that their latencies overlap.
+// in that order (an empty slot, slot_pos -1, adds nothing); loads in batches
+// of 8 so that their latencies overlap.
 __device__ __forceinline__ void ls_combine(const LayerArgs &a, int tt, int f, int lane)
 {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -797,16 +811,17 @@ __device__ __forceinline__ void ls_combine(const LayerArgs &a, int tt, int f, in
             pl = __ldcg(a.slot_pos + (size_t)tt * a.k + j0 + lane);
         }
         float4 v[8];
+        int pv[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            const int p = __shfl_sync(0xffffffffu, pl, u);
-            if (u < jn && on)
-                v[u] = __ldcg(reinterpret_cast<const float4 *>(a.y + (size_t)p * a.H + f));
+            pv[u] = __shfl_sync(0xffffffffu, pl, u);
+            if (u < jn && on && pv[u] >= 0)
+                v[u] = __ldcg(reinterpret_cast<const float4 *>(a.y + (size_t)pv[u] * a.H + f));
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const float wj = __shfl_sync(0xffffffffu, wl, u);
-            if (u < jn && on) {
+            if (u < jn && on && pv[u] >= 0) {
                 acc.x = fmaf(wj, v[u].x, acc.x);
                 acc.y = fmaf(wj, v[u].y, acc.y);
                 acc.z = fmaf(wj, v[u].z, acc.z);

@@ -554,6 +554,8 @@ __global__ void combine_kernel(const float *__restrict__ y, const float *__restr
     for (int j = 0; j < k; ++j) {
         float wj = w[t * k + j];
         int p = slot_pos[t * k + j];
+        if (p < 0)  // an empty slot of caller routing
+            continue;
         float4 v = reinterpret_cast<const float4 *>(y)[(long long)p * h4 + c];
         acc.x = fmaf(wj, v.x, acc.x);
         acc.y = fmaf(wj, v.y, acc.y);
@@ -595,8 +597,11 @@ __global__ void combine_f16_kernel(const uint16_t *__restrict__ y16, const int *
         acc.z = fmaf(sc, b.x, acc.z);
         acc.w = fmaf(sc, b.y, acc.w);
     };
-    for (int j = 0; j < k; ++j)
-        row(slot_pos[t * k + j], w[t * k + j]);
+    for (int j = 0; j < k; ++j) {
+        const int p = slot_pos[t * k + j];
+        if (p >= 0)  // (-1: an empty slot of caller routing)
+            row(p, w[t * k + j]);
+    }
     for (int s = 0; s < S; ++s)
         row((long long)T * k + (long long)s * T + t, 1.0f);
     reinterpret_cast<float4 *>(out)[(long long)t * h4 + c] = acc;

@@ -96,7 +96,7 @@ size_t plan_layout(const MoeHandle *h, int T, int k, char *base, Plan *p)
     q.topk_ids = (int *)take(sizeof(int) * (n > 0 ? n : 1));
     q.topk_w = (float *)take(sizeof(float) * (n > 0 ? n : 1));
     q.counts = (int *)take(sizeof(int) * (E > 0 ? E : 1));
-    q.chunk_cnt = (int *)take(sizeof(int) * (size_t)((n + 1023) / 1024 + 1) * (E > 0 ? E : 1));
+    q.chunk_cnt = (int *)take(sizeof(int) * (size_t)((n + 1023) / 1024 + 1) * (E + 1));
     q.expert_offsets = (int *)take(sizeof(int) * (E + 1));
     q.sorted_slot = (int *)take(sizeof(int) * (n > 0 ? n : 1));
     q.slot_pos = (int *)take(sizeof(int) * (n > 0 ? n : 1));

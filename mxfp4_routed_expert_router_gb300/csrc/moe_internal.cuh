@@ -145,7 +145,7 @@ struct Plan {
     int *topk_ids;            // [T*k]
     float *topk_w;            // [T*k]
     int *counts;              // [max(E,1)]
-    int *chunk_cnt;           // [ceil(T*k/1024)][E] per-chunk expert counts of the permutation (NULL: the
+    int *chunk_cnt;           // [ceil(T*k/1024)][E+1] per-chunk expert (and empty-slot) counts of the permutation (NULL: the
                               // one-CTA-per-expert permutation kernel, which needs no such scratch)
     int *expert_offsets;      // [E+1]
     int *sorted_slot;         // [T*k]

@@ -105,9 +105,11 @@ cudaError_t launch_router(const float *logits, int T, int E, int k, int *ids, fl
 //
 // "Cascadia: Resident 975B MoE Inference on Eleven AI PCs" §3.1: the router
 // hands the expert computation expert ids and their weights.  The caller's
-// arrays are copied into the call's routing arrays; an ID outside [0, E)
-// records DEV_ERR_BOUNDS (reported by moe_sync_status) and is replaced by
-// expert 0 with weight 0, so that everything after it stays in bounds.
+// arrays are copied into the call's routing arrays.  An ID of -1 marks an empty
+// slot (no expert, weight 0: it is not grouped and adds nothing); any other ID
+// outside [0, E) records DEV_ERR_BOUNDS (reported by moe_sync_status) and is
+// replaced by expert 0 with weight 0, so that everything after it stays in
+// bounds.
 __global__ void routing_copy_kernel(const int *__restrict__ ids_in, const float *__restrict__ w_in, int n, int E,
                                     int *__restrict__ ids, float *__restrict__ w, int *__restrict__ counts,
                                     int n_counts, int *err)
@@ -118,7 +120,9 @@ __global__ void routing_copy_kernel(const int *__restrict__ ids_in, const float 
     for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < n; s += gridDim.x * blockDim.x) {
         int e = ids_in[s];
         float wv = w_in[s];
-        if (e < 0 || e >= E) {
+        if (e == -1) {
+            wv = 0.f;
+        } else if (e < 0 || e >= E) {
             atomicCAS(err, 0, DEV_ERR_BOUNDS);
             e = 0;
             wv = 0.f;
@@ -252,7 +256,8 @@ __global__ void histogram_kernel(const int *__restrict__ ids, int n, int E, int 
         sh_hist[i] = 0;
     __syncthreads();
     for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < n; s += gridDim.x * blockDim.x)
-        atomicAdd(&sh_hist[ids[s]], 1);
+        if ((unsigned)ids[s] < (unsigned)E)
+            atomicAdd(&sh_hist[ids[s]], 1);
     __syncthreads();
     for (int i = threadIdx.x; i < E; i += blockDim.x)
         if (sh_hist[i])
@@ -352,11 +357,14 @@ __global__ void permute_kernel(const int *__restrict__ ids, int T, int k, int E,
 }
 
 // Chunked stable counting sort (moe_forward's path): the slots are cut into
-// chunks of PERM_CHUNK; one kernel counts each chunk's slots per expert, a
-// second gives every chunk its starting position per expert (slots of the
-// experts below, then of the same expert in earlier chunks) and places the
-// chunk's slots in slot order.  Integer counts only: the result equals the
-// one-CTA-per-expert kernel above, bit for bit.
+// chunks of PERM_CHUNK; one kernel counts each chunk's slots per expert (and,
+// in column E, its empty slots: ID -1 from caller routing), a second gives
+// every chunk its starting position per expert (slots of the experts below,
+// then of the same expert in earlier chunks) and places the chunk's slots in
+// slot order.  Integer counts only: the result equals the one-CTA-per-expert
+// kernel above, bit for bit.  Empty slots get no position (slot_pos -1); the
+// positions from expert_offsets[E] to T*k are left unused (sorted_slot -1,
+// token 0).
 constexpr int PERM_CHUNK = 1024;
 constexpr int PERM_CT = 256;                    // threads of the chunked kernels
 constexpr int PERM_CW = PERM_CT / 32;           // warps
@@ -364,8 +372,8 @@ constexpr int PERM_WSLOTS = PERM_CHUNK / PERM_CW;  // consecutive slots per warp
 
 __global__ void chunk_hist_kernel(const int *__restrict__ ids, int n, int E, int *__restrict__ chunk_cnt)
 {
-    extern __shared__ int h[];
-    for (int i = threadIdx.x; i < E; i += blockDim.x)
+    extern __shared__ int h[];  // [E + 1]: per expert, then the empty slots
+    for (int i = threadIdx.x; i <= E; i += blockDim.x)
         h[i] = 0;
     __syncthreads();
     const int s0 = blockIdx.x * PERM_CHUNK, s1 = min(n, s0 + PERM_CHUNK);
@@ -373,10 +381,12 @@ __global__ void chunk_hist_kernel(const int *__restrict__ ids, int n, int E, int
         const int e = ids[s];
         if ((unsigned)e < (unsigned)E)
             atomicAdd(&h[e], 1);
+        else if (e == -1)
+            atomicAdd(&h[E], 1);
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < E; i += blockDim.x)
-        chunk_cnt[(size_t)blockIdx.x * E + i] = h[i];
+    for (int i = threadIdx.x; i <= E; i += blockDim.x)
+        chunk_cnt[(size_t)blockIdx.x * (E + 1) + i] = h[i];
 }
 
 __global__ void chunk_scatter_kernel(const int *__restrict__ ids, int T, int k, int E, int S, int nchunks,
@@ -399,7 +409,7 @@ __global__ void chunk_scatter_kernel(const int *__restrict__ ids, int T, int k, 
     for (int e = e0; e < e1; ++e) {
         int tot = 0, pre = 0;
         for (int cc = 0; cc < nchunks; ++cc) {
-            const int v = chunk_cnt[(size_t)cc * E + e];
+            const int v = chunk_cnt[(size_t)cc * (E + 1) + e];
             tot += v;
             pre += cc < c ? v : 0;
         }
@@ -436,9 +446,17 @@ __global__ void chunk_scatter_kernel(const int *__restrict__ ids, int T, int k, 
     }
     if (c == 0 && tid == 0) {
         expert_offsets[E] = grand;
-        if (grand != n)
+        int empty = 0;
+        for (int cc = 0; cc < nchunks; ++cc)
+            empty += chunk_cnt[(size_t)cc * (E + 1) + E];
+        if (grand + empty != n)
             atomicCAS(err, 0, DEV_ERR_PERMUTE_COUNT);
     }
+    if (c == 0)  // positions left unused by empty slots
+        for (int p = grand + tid; p < n; p += blockDim.x) {
+            sorted_slot[p] = -1;
+            row_token[p] = 0;
+        }
     if (c == 0)
         for (int s = tid; s < S; s += blockDim.x) {
             grp_start[E + s] = n + s * T;
@@ -480,6 +498,8 @@ __global__ void chunk_scatter_kernel(const int *__restrict__ ids, int T, int k, 
             sorted_slot[pos] = s;
             slot_pos[s] = pos;
             row_token[pos] = s / k;
+        } else if (act && e == -1) {
+            slot_pos[s] = -1;  // an empty slot
         } else if (act) {
             atomicCAS(err, 0, DEV_ERR_PERMUTE_COUNT);
         }
@@ -495,7 +515,7 @@ cudaError_t launch_permute(const Plan &p, cudaStream_t st)
     const int n = p.T * p.k;
     if (p.chunk_cnt && p.E > 0 && n > 0) {
         const int nchunks = (n + PERM_CHUNK - 1) / PERM_CHUNK;
-        chunk_hist_kernel<<<nchunks, PERM_CT, p.E * sizeof(int), st>>>(p.topk_ids, n, p.E, p.chunk_cnt);
+        chunk_hist_kernel<<<nchunks, PERM_CT, (p.E + 1) * sizeof(int), st>>>(p.topk_ids, n, p.E, p.chunk_cnt);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess)
             return e;

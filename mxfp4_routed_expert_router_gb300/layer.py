@@ -97,7 +97,8 @@ class MoeLayer:
 
     def forward_routed(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor,
                        out: Optional[torch.Tensor] = None, accumulate: bool = False, routing=None, stream=None):
-        """The layer for routing given as expert ids (int32 [T, k]) and weights (float32 [T, k])."""
+        """The layer for routing given as expert ids (int32 [T, k]) and weights (float32 [T, k]).
+        An id of -1 is an empty slot (it adds nothing; its weight is not read)."""
         T, k = topk_ids.shape
         if out is None:
             out = torch.empty((T, self.cfg.hidden), dtype=torch.float32, device=self.device)

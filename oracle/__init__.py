@@ -288,9 +288,11 @@ def moe_layer(W: OracleWeights, x_bf16: np.ndarray, logits: np.ndarray, k: int, 
 
 
 def moe_layer_routed(W: OracleWeights, x_bf16: np.ndarray, ids: np.ndarray, w: np.ndarray, nthreads: int = 1):
-    """The MoE layer for given routing (ids [n, k] in [0, E), weights [n, k]):
+    """The MoE layer for given routing (ids [n, k] in [0, E) or -1, weights [n, k]):
     every selected and shared expert on its tokens and the weighted reduction
     ("Cascadia" §3.1, Eq. (1) of §3.3; the routing reaches it as ids and weights).
+    An id of -1 is an empty slot: its term is left out of the sum, so that
+    holders of disjoint expert subsets each compute their part of Eq. (1).
     Returns out float64 [n, H]."""
     x_bf16 = _c(x_bf16, np.uint16)
     ids = _c(ids, np.int32)

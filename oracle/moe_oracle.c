@@ -256,8 +256,10 @@ void oracle_route_sigmoid(const float *logits, const float *bias, int64_t T, int
 
 /* Group slots by expert: a stable counting sort of the flattened slots
  * s = t*k + j by their expert id.  off[e] is the first sorted position of
- * expert e (off[E] = T*k), sorted_slot[p] the slot at position p, and
- * slot_pos[s] its inverse. */
+ * expert e (off[E] = the number of slots placed), sorted_slot[p] the slot at
+ * position p, and slot_pos[s] its inverse.  A slot with id -1 (empty) is not
+ * placed: its slot_pos is -1, and sorted_slot holds -1 at the positions from
+ * off[E] to T*k that no slot takes. */
 void oracle_permute(const int32_t *ids, int64_t T, int k, int E, int32_t *off, int32_t *sorted_slot,
                     int32_t *slot_pos)
 {
@@ -266,15 +268,19 @@ void oracle_permute(const int32_t *ids, int64_t T, int k, int E, int32_t *off, i
     for (int e = 0; e <= E; ++e)
         off[e] = 0;
     for (int64_t s = 0; s < n; ++s)
-        off[ids[s] + 1] += 1;
+        if (ids[s] != -1)
+            off[ids[s] + 1] += 1;
     for (int e = 0; e < E; ++e)
         off[e + 1] += off[e];
     for (int e = 0; e < E; ++e)
         next[e] = off[e];
+    for (int64_t p = off[E]; p < n; ++p)
+        sorted_slot[p] = -1;
     for (int64_t s = 0; s < n; ++s) {
-        int32_t p = next[ids[s]]++;
-        sorted_slot[p] = (int32_t)s;
+        int32_t p = ids[s] == -1 ? -1 : next[ids[s]]++;
         slot_pos[s] = p;
+        if (p >= 0)
+            sorted_slot[p] = (int32_t)s;
     }
     free(next);
 }
@@ -394,9 +400,13 @@ static int decode_matrix(int fmt, const void *codes, const void *scales, const u
     return oracle_mx_decode((const uint8_t *)codes, (const uint8_t *)scales, rows, cols, out);
 }
 
-/* The layer for given routing (ids [n_tok, k] in [0, E), weights w): every
- * selected and every shared expert on its tokens, then the weighted reduction
+/* The layer for given routing (ids [n_tok, k] in [0, E) or -1, weights w):
+ * every selected and every shared expert on its tokens, then the weighted
+ * reduction
  *   out_t = sum_{j<k} w_tj * y_{e_tj}(x_t) + sum_{shared s} y_s(x_t)   [C33, C31].
+ * An id of -1 is an empty slot whose term is left out of the sum (its weight
+ * is not read): Eq. (1)'s sum over experts split between holders of disjoint
+ * expert subsets, each summing the terms of its own experts.
  * A token's result depends only on its own x row and routing row.
  * x_bf16 [n_tok, H] BF16 bits, out [n_tok, H] double.  Returns 0, -1 (a scale
  * the format rejects), -2 (weights of a used expert missing), -3 (bad args or
@@ -408,7 +418,7 @@ int oracle_moe_layer_routed(const OracleLayer *L, const uint16_t *x_bf16, const 
     if (k < 1 || k > E || H % 32 || I % 32)
         return -3;
     for (int64_t i = 0; i < n_tok * k; ++i)
-        if (ids[i] < 0 || ids[i] >= E)
+        if (ids[i] != -1 && (ids[i] < 0 || ids[i] >= E))
             return -3;
     const int nsel = k + S;
     int rc = 0;
@@ -457,7 +467,8 @@ int oracle_moe_layer_routed(const OracleLayer *L, const uint16_t *x_bf16, const 
             for (int m = 0; m < H; ++m) {
                 double acc = 0.0;
                 for (int j = 0; j < k; ++j)
-                    acc += w[t * k + j] * y[(t * nsel + j) * H + m];
+                    if (ids[t * k + j] != -1)
+                        acc += w[t * k + j] * y[(t * nsel + j) * H + m];
                 for (int s = 0; s < S; ++s)
                     acc += y[(t * nsel + k + s) * H + m];
                 out[t * H + m] = acc;

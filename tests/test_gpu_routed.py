@@ -76,7 +76,7 @@ def _random_routing(T, E, k, seed):
 
 def _oracle_routed(cfg, x_bits, ids, w):
     W = oracle.OracleWeights(cfg.hidden, cfg.inter, cfg.n_experts, cfg.n_shared)
-    for e in sorted(set(ids.ravel().tolist()) | set(range(cfg.n_experts, cfg.n_groups))):
+    for e in sorted(set(ids.ravel().tolist()) - {-1} | set(range(cfg.n_experts, cfg.n_groups))):
         W.set_expert(e, *wl.expert_weights(cfg, e))
     return oracle.moe_layer_routed(W, x_bits, ids, w.astype(np.float64), nthreads=NTHREADS)
 
@@ -143,4 +143,56 @@ def test_forward_routed_id_out_of_range(cfg):
     ok_w[bad] = 0.0
     ref = _oracle_routed(cfg, x, ok_ids, ok_w)
     assert rel_err(out.cpu().numpy(), ref) <= TOL
+    L.free()
+
+
+# Empty slots (id -1): a holder of a subset of the experts runs the caller's
+# routing with the slots of the other experts emptied; each empty slot adds
+# nothing and its weight is never read (NaN here).  Cases for both paths: the
+# single weight-streaming kernel (T*k <= 16 E, one of them with more than 2048
+# slots) and the tensor-memory GEMMs with the chunked permutation (one of them
+# over three chunks of 1024 slots).
+EMPTY = [
+    ROUTED[0],
+    ROUTED[1],
+    ROUTED[3],
+    wl.custom("routed_T300_H288_I160_E160_S1_k8", 300, 288, 160, 160, 1, 8, seed=45),
+    wl.custom("routed_T600_H288_I160_E16_S1_k4", 600, 288, 160, 16, 1, 4, seed=46),
+]
+
+
+@pytest.mark.parametrize("cfg", EMPTY, ids=lambda c: c.name)
+def test_forward_routed_empty_slots(cfg):
+    B, layer = _mods()
+    L = layer.MoeLayer(cfg)
+    x = wl.tokens(cfg)
+    ids, w = _random_routing(cfg.T, cfg.n_experts, cfg.k, cfg.seed + 2)
+    rng = np.random.default_rng(cfg.seed + 3)
+    # the experts of the other holder (every third one) and a random eighth of
+    # the slots are empty; token 0 has no routed slot left
+    empty = (ids % 3 == 1) | (rng.random(ids.shape) < 0.125)
+    empty[0, :] = True
+    ids[empty] = -1
+    w[empty] = np.nan
+    T, k, E = cfg.T, cfg.k, cfg.n_experts
+    dev = dict(device="cuda")
+    rid = torch.full((T, k), -7, dtype=torch.int32, **dev)
+    rw = torch.full((T, k), -1.0, dtype=torch.float32, **dev)
+    off = torch.full((E + 1,), -7, dtype=torch.int32, **dev)
+    ss = torch.full((T * k,), -7, dtype=torch.int32, **dev)
+    sp = torch.full((T * k,), -7, dtype=torch.int32, **dev)
+    out = L.forward_routed(layer.bf16_tensor(x), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(),
+                           routing=B.routing_out(topk_ids=rid, topk_w=rw, expert_offsets=off, sorted_slot=ss,
+                                                 slot_pos=sp))
+    L.sync()
+    np.testing.assert_array_equal(rid.cpu().numpy(), ids)
+    np.testing.assert_array_equal(rw.cpu().numpy(), np.where(empty, np.float32(0), w))
+    roff, rss, rsp = oracle.permute(ids, E)
+    np.testing.assert_array_equal(off.cpu().numpy(), roff)
+    np.testing.assert_array_equal(ss.cpu().numpy(), rss)
+    np.testing.assert_array_equal(sp.cpu().numpy(), rsp)
+    got = out.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    ref = _oracle_routed(cfg, x, ids, w)
+    assert rel_err(got, ref) <= TOL
     L.free()

@@ -34,6 +34,9 @@ MUTATIONS = {
                         "            acc += h[n] * (double)wd[n];",
                         "for (int n = 0; n < I; ++n)\n            acc += h[n] * (double)Wd[(int64_t)n * ld_d + m % ld_d];"),
     "weights_reversed": ("acc += w[t * k + j] * y", "acc += w[t * k + (k - 1 - j)] * y"),
+    "empty_slot_weight_read": ("if (ids[t * k + j] != -1)\n                        acc +=", "if (1)\n                        acc +="),
+    "empty_slot_placed_last": ("int32_t p = ids[s] == -1 ? -1 : next[ids[s]]++;",
+                               "int32_t p = ids[s] == -1 ? (int32_t)(n - 1) : next[ids[s]]++;"),
     "sigmoid_bias_in_weights": ("w[t * k + j] = scale * score[s[j].idx] / denom;",
                                 "w[t * k + j] = scale * s[j].v / denom;"),
     "sigmoid_bias_ignored": ("s[e].v = score[e] + (bias ? (double)bias[e] : 0.0);", "s[e].v = score[e];"),

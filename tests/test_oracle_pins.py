@@ -200,6 +200,28 @@ def test_permute_against_python_stable_sort():
         assert np.all(sp[ss] == np.arange(T * k))
 
 
+def test_permute_empty_slots_take_no_position():
+    # id -1 marks an empty slot: the placed slots sort exactly as if the empty
+    # ones were not there, the empty ones get slot_pos -1 and the positions past
+    # the placed ones hold -1
+    rng = np.random.default_rng(15)
+    for trial in range(20):
+        T, E = int(rng.integers(1, 40)), int(rng.integers(1, 12))
+        k = int(rng.integers(1, 6))
+        ids = rng.integers(-1, E, (T, k)).astype(np.int32)
+        off, ss, sp = oracle.permute(ids, E)
+        flat = ids.ravel().tolist()
+        placed = [s for s in range(T * k) if flat[s] != -1]
+        want_ss = sorted(placed, key=lambda s: flat[s])
+        assert ss[:len(placed)].tolist() == want_ss
+        assert np.all(ss[len(placed):] == -1)
+        assert off[E] == len(placed)
+        counts = np.bincount(ids.ravel()[ids.ravel() >= 0], minlength=E)
+        assert off.tolist() == [0] + np.cumsum(counts).tolist()
+        assert [sp[s] for s in range(T * k) if flat[s] == -1] == [-1] * (T * k - len(placed))
+        assert np.all(sp[np.array(want_ss, np.int64)] == np.arange(len(placed)))
+
+
 # ------------------------------------------------------------------ expert / layer pins
 
 def silu(z):
@@ -494,6 +516,41 @@ def test_layer_routed_is_linear_in_the_weights():
     o1 = oracle.moe_layer_routed(W, x, ids, w) - shared
     o2 = oracle.moe_layer_routed(W, x, ids, 2 * w) - shared
     np.testing.assert_allclose(o2, 2 * o1, rtol=1e-12, atol=1e-12 * np.abs(o1).max())
+
+
+def test_layer_routed_empty_slot_drops_its_term():
+    # an id of -1 leaves the slot's term out of Eq. (1): column 1 empty on every
+    # token equals the layer with k = 1 on column 0 alone, and the empty slot's
+    # weight (NaN here) is never read
+    cfg = wl.custom("rte", 6, 64, 32, 4, 1, 2, seed=38)
+    x = wl.tokens(cfg)
+    W = oracle.OracleWeights(64, 32, 4, 1)
+    for e in range(5):
+        W.set_expert(e, *wl.expert_weights(cfg, e))
+    ids1 = np.array([[2], [0], [3], [3], [1], [0]], np.int32)
+    w1 = np.array([[0.5], [1.25], [0.75], [2.0], [1.0], [0.25]])
+    ids2 = np.concatenate([ids1, np.full((6, 1), -1, np.int32)], axis=1)
+    w2 = np.concatenate([w1, np.full((6, 1), np.nan)], axis=1)
+    np.testing.assert_array_equal(oracle.moe_layer_routed(W, x, ids2, w2), oracle.moe_layer_routed(W, x, ids1, w1))
+
+
+def test_layer_routed_expert_subsets_sum_to_the_layer():
+    # holders of disjoint expert subsets (the other subset's slots empty) each
+    # add the shared expert once; their sum less one shared-only pass (every
+    # slot empty) is the whole layer
+    cfg = wl.custom("rts", 8, 64, 32, 6, 1, 3, seed=39)
+    x = wl.tokens(cfg)
+    W = oracle.OracleWeights(64, 32, 6, 1)
+    for e in range(7):
+        W.set_expert(e, *wl.expert_weights(cfg, e))
+    rng = np.random.default_rng(39)
+    ids = np.stack([rng.choice(6, 3, replace=False) for _ in range(8)]).astype(np.int32)
+    w = rng.uniform(0.1, 1.0, (8, 3))
+    full = oracle.moe_layer_routed(W, x, ids, w)
+    lo = oracle.moe_layer_routed(W, x, np.where(ids < 3, ids, -1).astype(np.int32), w)
+    hi = oracle.moe_layer_routed(W, x, np.where(ids >= 3, ids, -1).astype(np.int32), w)
+    shared = oracle.moe_layer_routed(W, x, np.full_like(ids, -1), w)
+    np.testing.assert_allclose(lo + hi - shared, full, rtol=1e-12, atol=1e-12 * np.abs(full).max())
 
 
 def test_layer_routed_rejects_ids_out_of_range():
