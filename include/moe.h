@@ -113,7 +113,8 @@ typedef struct {
     int inter;             /* I per expert, or the dense FFN's total I; multiple of 32 */
     int n_experts;         /* E routed experts (1 .. 1024); for a dense layer: n_slices */
     int n_shared;          /* S always-on shared experts (0 .. 64); 0 for a dense layer */
-    int k_max;             /* largest k a forward call may ask for, 1 .. min(E, 32); ignored when dense */
+    int k_max;             /* largest k a forward call may ask for, 1 .. 32 (moe_forward also needs
+                              k <= E; moe_forward_routed does not); ignored when dense */
     int n_slices;          /* 0: routed MoE layer.  > 0: dense FFN cut into this many slices */
     MoeWeightFormat fmt;   /* MXFP4, BF16 or group-32 INT4 weights */
 } MoeConfig;
@@ -194,23 +195,39 @@ MoeStatus moe_forward(MoeHandle *h, const void *x_bf16, const float *router_logi
  *  topk_ids [T][k] int32 in [0, E) or -1, 4-byte aligned (an expert may
  *           appear more than once for a token; each occurrence is its own
  *           slot).  -1 is an empty slot: it adds nothing and its weight is
- *           not read.  A holder of a subset of the experts passes the routing
- *           with the other experts' slots set to -1 and gets its part of the
- *           sum over experts (each holder adds the shared experts it holds).
+ *           not read.  On a handle given an expert range (moe_set_expert_range)
+ *           the ids are global ids in [0, n_experts_total) or -1, and a slot
+ *           of an expert outside the handle's range is an empty slot too.
  *  topk_w   [T][k] float, 4-byte aligned, used as given
  *  other arguments as for moe_forward; `routing` receives the copy of the
- *  ids and weights the layer ran with (an empty slot: id -1, weight 0) and
- *  the grouping: expert_offsets[E] is then the number of non-empty slots,
- *  slot_pos is -1 for an empty slot and sorted_slot is -1 at the positions
- *  from expert_offsets[E] to T*k.
- * Any other id outside [0, E) cannot be checked on the host: the device
- * records it, runs that slot as expert 0 with weight 0 so that every access
- * stays in bounds, and moe_sync_status() then reports MOE_EDEVICE.
+ *  ids (the handle's own expert indices 0..E-1) and weights the layer ran
+ *  with (an empty slot: id -1, weight 0) and the grouping: expert_offsets[E]
+ *  is then the number of non-empty slots, slot_pos is -1 for an empty slot
+ *  and sorted_slot is -1 at the positions from expert_offsets[E] to T*k.
+ * Any other id cannot be checked on the host: the device records it, runs
+ * that slot as expert 0 with weight 0 so that every access stays in bounds,
+ * and moe_sync_status() then reports MOE_EDEVICE.
  * Errors: MOE_EINVAL (NULL/misaligned pointers, T < 0, k outside [1, k_max],
  * a dense handle), MOE_EWORKSPACE, MOE_EDEVICE, MOE_ECUDA. */
 MoeStatus moe_forward_routed(MoeHandle *h, const void *x_bf16, const int32_t *topk_ids, const float *topk_w, int T,
                              int k, float *out_fp32, int accumulate, void *workspace, size_t ws_bytes,
                              const MoeRoutingOut *routing, void *cuda_stream);
+
+/* Expert parallelism: the handle's E routed experts are experts
+ * [expert_base, expert_base + E) of a layer of n_experts_total, held in order
+ * (its expert i is the layer's expert expert_base + i).  moe_forward_routed
+ * then takes the layer's global expert ids and runs only the slots of the
+ * experts held, as empty slots otherwise, so that the outputs of holders of
+ * disjoint ranges (the shared experts loaded on one of them) add up to the
+ * whole layer: Eq. (1) of "Cascadia: Resident 975B MoE Inference on Eleven AI
+ * PCs" §3.3 is a sum over experts.  The token rows and routing are given to
+ * every holder whole, and the caller adds the FP32 outputs (an all-reduce or
+ * reduce-scatter across devices).  moe_forward, which routes over the
+ * handle's own experts, is refused on a handle with a range other than
+ * [0, E) of E.  Host-side only: no device work; applies to later calls.
+ * Errors: MOE_EINVAL (NULL or dense handle, expert_base < 0,
+ * expert_base + E > n_experts_total, n_experts_total > 2^20). */
+MoeStatus moe_set_expert_range(MoeHandle *h, int expert_base, int n_experts_total);
 
 /* Largest E moe_route_sigmoid takes (one warp per token, 32 experts a lane). */
 #define MOE_ROUTE_SIGMOID_MAX_EXPERTS 1024

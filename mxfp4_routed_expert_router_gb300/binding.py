@@ -21,7 +21,7 @@ STATUS_NAMES = ["MOE_OK", "MOE_EINVAL", "MOE_EDIMS", "MOE_ESCALE", "MOE_ENOMEM",
 MOE_W_MXFP4, MOE_W_BF16, MOE_W_INT4G32 = 0, 1, 2
 
 # every symbol include/moe.h declares
-EXPORTED = ("moe_load_weights", "moe_workspace_bytes", "moe_forward", "moe_forward_routed",
+EXPORTED = ("moe_load_weights", "moe_workspace_bytes", "moe_forward", "moe_forward_routed", "moe_set_expert_range",
             "moe_route_sigmoid", "moe_dense_sliced_forward", "moe_sync_status", "moe_profile_enable",
             "moe_profile_read", "moe_route_static", "moe_route_static_status", "moe_graph_create",
             "moe_graph_launch", "moe_graph_free", "moe_debug_expire_next_wait", "moe_last_error", "moe_free")
@@ -69,6 +69,8 @@ def _load():
     L.moe_forward.restype = ci
     L.moe_forward_routed.argtypes = [vp, vp, vp, vp, ci, ci, vp, ci, vp, sz, ctypes.POINTER(MoeRoutingOut), vp]
     L.moe_forward_routed.restype = ci
+    L.moe_set_expert_range.argtypes = [vp, ci, ci]
+    L.moe_set_expert_range.restype = ci
     L.moe_route_sigmoid.argtypes = [vp, vp, ci, ci, ci, ctypes.c_float, vp, vp, vp]
     L.moe_route_sigmoid.restype = ci
     L.moe_graph_create.argtypes = [vp, vp, vp, vp, vp, ci, ci, vp, ci, vp, sz, ctypes.POINTER(MoeHostIO),
@@ -157,6 +159,10 @@ def moe_forward_routed(handle: int, x_bf16, topk_ids, topk_w, T: int, k: int, ou
     _check(lib.moe_forward_routed(handle, _ptr(x_bf16), _ptr(topk_ids), _ptr(topk_w), T, k, _ptr(out_fp32),
                                   int(bool(accumulate)), _ptr(workspace), ws_bytes,
                                   ctypes.byref(routing) if routing is not None else None, _stream(stream)))
+
+
+def moe_set_expert_range(handle: int, expert_base: int, n_experts_total: int) -> None:
+    _check(lib.moe_set_expert_range(handle, int(expert_base), int(n_experts_total)))
 
 
 def moe_route_sigmoid(router_logits, bias, T: int, E: int, k: int, routed_scale: float, topk_ids, topk_w,

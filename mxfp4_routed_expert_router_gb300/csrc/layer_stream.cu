@@ -210,6 +210,7 @@ struct LayerArgs {
     const uint16_t *x;
     const float *logits;
     const int *ids_in;   // routing given by the caller (ids, weights) instead of logits, or NULL
+    int ebase, etotal;   // caller routing: the groups 0..E-1 are expert ids [ebase, ebase + E) of etotal
     const float *w_in;
     int *topk_ids;
     float *topk_w;
@@ -481,9 +482,11 @@ __device__ void ls_route_warp(const LayerArgs &a, int t, int lane, int *ids_s, b
 }
 
 // Routing given by the caller for token t (one warp): lane j < k takes its id
-// and weight; id -1 is an empty slot (kept, weight 0); any other id outside
-// [0, E) records DEV_ERR_BOUNDS and becomes expert 0 with weight 0, so that
-// the layer stays in bounds.  The ids go to ids_s when
+// and weight.  Ids are global: the layer holds experts [ebase, ebase + E) of
+// etotal as its groups 0..E-1.  Id -1, or an expert held elsewhere, is an
+// empty slot (id -1, weight 0); any other id outside [0, etotal) records
+// DEV_ERR_BOUNDS and becomes group 0 with weight 0, so that the layer stays in
+// bounds.  The ids go to ids_s when
 // given, and the owner CTA writes both to the call's routing arrays.
 __device__ void ls_copy_route_warp(const LayerArgs &a, int t, int lane, int *ids_s, bool owner)
 {
@@ -492,10 +495,15 @@ __device__ void ls_copy_route_warp(const LayerArgs &a, int t, int lane, int *ids
         float wv = __ldg(a.w_in + (size_t)t * a.k + lane);
         if (e == -1) {
             wv = 0.f;
-        } else if (e < 0 || e >= a.E) {
+        } else if (e < 0 || e >= a.etotal) {
             atomicCAS(a.err, 0, DEV_ERR_BOUNDS);
             e = 0;
             wv = 0.f;
+        } else if (e < a.ebase || e - a.ebase >= a.E) {
+            e = -1;
+            wv = 0.f;
+        } else {
+            e -= a.ebase;
         }
         if (ids_s)
             ids_s[t * a.k + lane] = e;
@@ -1622,6 +1630,8 @@ cudaError_t launch_layer_stream(const Plan &p, const WeightStore &gu, const Weig
     a.x = x;
     a.logits = logits;
     a.ids_in = ids_in;
+    a.ebase = p.ebase;
+    a.etotal = p.etotal;
     a.w_in = w_in;
     a.topk_ids = p.topk_ids;
     a.topk_w = p.topk_w;

@@ -22,6 +22,7 @@ struct MoeHandle {
     int H = 0, I = 0;          // hidden, per-group intermediate
     int fmt = 0;
     int k_max = 0;
+    int ebase = 0, etotal = 0;  // the experts held are ids [ebase, ebase + E) of etotal (moe_set_expert_range)
     int device = 0;
     WeightStore gu, dn;        // TILE or TILE_F16 layout (tensor-memory GEMMs, large batches)
     bool tc_f16 = false;       // the tensor-memory GEMMs run FP16 operands (TILE_F16 store with row bases)
@@ -93,6 +94,8 @@ size_t plan_layout(const MoeHandle *h, int T, int k, char *base, Plan *p)
     q.H = H;
     q.I = I;
     q.P = (int)P;
+    q.ebase = h->ebase;
+    q.etotal = h->etotal;
     q.topk_ids = (int *)take(sizeof(int) * (n > 0 ? n : 1));
     q.topk_w = (float *)take(sizeof(float) * (n > 0 ? n : 1));
     q.counts = (int *)take(sizeof(int) * (E > 0 ? E : 1));
@@ -171,8 +174,8 @@ MoeStatus run_layer(MoeHandle *h, const void *x, const float *logits, const int 
     mark(0);
     if (h->E > 0) {
         if (ids_in) {
-            if ((e = launch_routing_copy(ids_in, w_in, T * k, h->E, p.topk_ids, p.topk_w, p.counts, h->E, p.err,
-                                         st)) != cudaSuccess)
+            if ((e = launch_routing_copy(ids_in, w_in, T * k, h->E, h->ebase, h->etotal, p.topk_ids, p.topk_w,
+                                         p.counts, h->E, p.err, st)) != cudaSuccess)
                 return cuda_fail(e, "routing copy launch");
         } else if ((e = launch_router(logits, T, h->E, k, p.topk_ids, p.topk_w, p.counts, h->E, st)) !=
                    cudaSuccess) {
@@ -287,8 +290,8 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
             return fail(MOE_EINVAL, "n_slices must be >= 0");
         if (c.n_experts < 1 || c.n_experts > 1024 || c.n_shared < 0 || c.n_shared > 64)
             return fail(MOE_EINVAL, "n_experts must be in [1, 1024] and n_shared in [0, 64]");
-        if (c.k_max < 1 || c.k_max > 32 || c.k_max > c.n_experts)
-            return fail(MOE_EINVAL, "k_max must be in [1, min(n_experts, 32)]");
+        if (c.k_max < 1 || c.k_max > 32)
+            return fail(MOE_EINVAL, "k_max must be in [1, 32]");
         E = c.n_experts;
         S = c.n_shared;
         I = c.inter;
@@ -325,6 +328,8 @@ MoeStatus moe_load_weights(const MoeConfig *cfg, const MoeMx *gate_up, const Moe
     h->I = I;
     h->fmt = fmt;
     h->k_max = k_max;
+    h->ebase = 0;
+    h->etotal = E;
     cudaStream_t st = (cudaStream_t)cuda_stream;
     cudaError_t e = cudaGetDevice(&h->device);
     if (e != cudaSuccess) {
@@ -489,8 +494,12 @@ MoeStatus moe_forward(MoeHandle *h, const void *x_bf16, const float *router_logi
         return fail(MOE_EINVAL, "moe_forward on a dense handle; use moe_dense_sliced_forward");
     if (T < 0 || T > (1 << 24))
         return fail(MOE_EINVAL, "T = %d out of range [0, 2^24]", T);
-    if (k < 1 || k > h->k_max)
-        return fail(MOE_EINVAL, "k = %d out of range [1, %d]", k, h->k_max);
+    if (k < 1 || k > h->k_max || k > h->E)
+        return fail(MOE_EINVAL, "k = %d out of range [1, %d]", k, h->k_max < h->E ? h->k_max : h->E);
+    if (h->ebase != 0 || h->etotal != h->E)
+        return fail(MOE_EINVAL, "moe_forward on a handle holding experts [%d, %d) of %d: route first "
+                                "(moe_route_static, moe_route_sigmoid) and call moe_forward_routed",
+                    h->ebase, h->ebase + h->E, h->etotal);
     if (T == 0)
         return check_pending(h);
     if (!x_bf16 || !router_logits || !out_fp32 || !workspace)
@@ -531,6 +540,21 @@ MoeStatus moe_forward_routed(MoeHandle *h, const void *x_bf16, const int32_t *to
         return s;
     return run_layer(h, x_bf16, nullptr, topk_ids, topk_w, T, k, out_fp32, accumulate, workspace, ws_bytes, routing,
                      (cudaStream_t)cuda_stream);
+}
+
+MoeStatus moe_set_expert_range(MoeHandle *h, int expert_base, int n_experts_total)
+{
+    if (!h)
+        return fail(MOE_EINVAL, "moe_set_expert_range: NULL handle");
+    if (h->E == 0)
+        return fail(MOE_EINVAL, "moe_set_expert_range on a dense handle");
+    if (expert_base < 0 || n_experts_total < 1 || n_experts_total > (1 << 20) ||
+        (long long)expert_base + h->E > n_experts_total)
+        return fail(MOE_EINVAL, "experts [%d, %d) are not a part of [0, %d) (at most 2^20 experts)", expert_base,
+                    expert_base + h->E, n_experts_total);
+    h->ebase = expert_base;
+    h->etotal = n_experts_total;
+    return MOE_OK;
 }
 
 MoeStatus moe_route_sigmoid(const float *router_logits, const float *bias, int T, int E, int k, float routed_scale,

@@ -141,6 +141,7 @@ struct SrcMat {
 struct Plan {
     int T, k, E, S, G, H, I;
     int P;                    // T*k + S*T positions
+    int ebase, etotal;        // caller routing: the routed groups are expert ids [ebase, ebase + E) of etotal
     // workspace arrays
     int *topk_ids;            // [T*k]
     float *topk_w;            // [T*k]
@@ -194,7 +195,8 @@ cudaError_t launch_router(const float *logits, int T, int E, int k, int *ids, fl
 // caller-given routing (ids, weights) copied into the call's routing arrays;
 // an id outside [0, E) records DEV_ERR_BOUNDS and becomes expert 0, weight 0;
 // counts[0 .. n_counts) are cleared for the histogram
-cudaError_t launch_routing_copy(const int *ids_in, const float *w_in, int n, int E, int *ids, float *w, int *counts,
+cudaError_t launch_routing_copy(const int *ids_in, const float *w_in, int n, int E, int ebase, int etotal, int *ids,
+                                float *w, int *counts,
                                 int n_counts, int *err, cudaStream_t st);
 
 // sigmoid scores, bias-adjusted top-k, weights normalised over the selection

@@ -105,14 +105,32 @@ cudaError_t launch_router(const float *logits, int T, int E, int k, int *ids, fl
 //
 // "Cascadia: Resident 975B MoE Inference on Eleven AI PCs" §3.1: the router
 // hands the expert computation expert ids and their weights.  The caller's
-// arrays are copied into the call's routing arrays.  An ID of -1 marks an empty
-// slot (no expert, weight 0: it is not grouped and adds nothing); any other ID
-// outside [0, E) records DEV_ERR_BOUNDS (reported by moe_sync_status) and is
-// replaced by expert 0 with weight 0, so that everything after it stays in
+// arrays are copied into the call's routing arrays.  The ids are global: the
+// layer holds experts [ebase, ebase + E) of etotal, which become its groups
+// 0..E-1.  An ID of -1, or of an expert held elsewhere, marks an empty slot
+// (ID -1, weight 0: it is not grouped and adds nothing); any other ID outside
+// [0, etotal) records DEV_ERR_BOUNDS (reported by moe_sync_status) and is
+// replaced by group 0 with weight 0, so that everything after it stays in
 // bounds.
+__device__ __forceinline__ void route_in(int &e, float &wv, int E, int ebase, int etotal, int *err)
+{
+    if (e == -1) {
+        wv = 0.f;
+    } else if (e < 0 || e >= etotal) {
+        atomicCAS(err, 0, DEV_ERR_BOUNDS);
+        e = 0;
+        wv = 0.f;
+    } else if (e < ebase || e - ebase >= E) {
+        e = -1;
+        wv = 0.f;
+    } else {
+        e -= ebase;
+    }
+}
+
 __global__ void routing_copy_kernel(const int *__restrict__ ids_in, const float *__restrict__ w_in, int n, int E,
-                                    int *__restrict__ ids, float *__restrict__ w, int *__restrict__ counts,
-                                    int n_counts, int *err)
+                                    int ebase, int etotal, int *__restrict__ ids, float *__restrict__ w,
+                                    int *__restrict__ counts, int n_counts, int *err)
 {
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i < n_counts; i += blockDim.x)
@@ -120,27 +138,21 @@ __global__ void routing_copy_kernel(const int *__restrict__ ids_in, const float 
     for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < n; s += gridDim.x * blockDim.x) {
         int e = ids_in[s];
         float wv = w_in[s];
-        if (e == -1) {
-            wv = 0.f;
-        } else if (e < 0 || e >= E) {
-            atomicCAS(err, 0, DEV_ERR_BOUNDS);
-            e = 0;
-            wv = 0.f;
-        }
+        route_in(e, wv, E, ebase, etotal, err);
         ids[s] = e;
         w[s] = wv;
     }
 }
 
-cudaError_t launch_routing_copy(const int *ids_in, const float *w_in, int n, int E, int *ids, float *w, int *counts,
-                                int n_counts, int *err, cudaStream_t st)
+cudaError_t launch_routing_copy(const int *ids_in, const float *w_in, int n, int E, int ebase, int etotal, int *ids,
+                                float *w, int *counts, int n_counts, int *err, cudaStream_t st)
 {
     int blocks = (n + 255) / 256;
     if (blocks < 1)
         blocks = 1;
     if (blocks > 1024)
         blocks = 1024;
-    routing_copy_kernel<<<blocks, 256, 0, st>>>(ids_in, w_in, n, E, ids, w, counts, n_counts, err);
+    routing_copy_kernel<<<blocks, 256, 0, st>>>(ids_in, w_in, n, E, ebase, etotal, ids, w, counts, n_counts, err);
     return cudaGetLastError();
 }
 

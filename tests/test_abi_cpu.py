@@ -66,9 +66,11 @@ def test_host_side_argument_checks_without_gpu(built):
     # dense slice width cutting a 32-value block
     cfg = b.MoeConfig(hidden=64, inter=96, n_experts=2, n_shared=0, k_max=1, n_slices=2, fmt=b.MOE_W_MXFP4)
     assert L.moe_load_weights(ctypes.byref(cfg), fake, fake, None, ctypes.byref(h)) == b.MOE_EDIMS
-    # k_max > n_experts
-    cfg = b.MoeConfig(hidden=64, inter=64, n_experts=2, n_shared=0, k_max=3, n_slices=0, fmt=b.MOE_W_MXFP4)
-    assert L.moe_load_weights(ctypes.byref(cfg), fake, fake, None, ctypes.byref(h)) == b.MOE_EINVAL
+    # k_max outside [1, 32] (k_max above n_experts is allowed: caller routing may
+    # repeat an expert or leave slots empty)
+    for km in (0, 33):
+        cfg = b.MoeConfig(hidden=64, inter=64, n_experts=2, n_shared=0, k_max=km, n_slices=0, fmt=b.MOE_W_MXFP4)
+        assert L.moe_load_weights(ctypes.byref(cfg), fake, fake, None, ctypes.byref(h)) == b.MOE_EINVAL
     # NULL weight pointer
     cfg = b.MoeConfig(hidden=64, inter=64, n_experts=2, n_shared=0, k_max=1, n_slices=0, fmt=b.MOE_W_MXFP4)
     nul = (b.MoeMx * 2)(b.MoeMx(16, 16), b.MoeMx(16, None))
@@ -88,6 +90,7 @@ def test_host_side_argument_checks_without_gpu(built):
     assert L.moe_dense_sliced_forward(None, None, 1, None, 0, None, 0, None) == b.MOE_EINVAL
     assert L.moe_sync_status(None, None) == b.MOE_EINVAL
     assert L.moe_forward_routed(None, None, None, None, 1, 1, None, 0, None, 0, None, None) == b.MOE_EINVAL
+    assert L.moe_set_expert_range(None, 0, 8) == b.MOE_EINVAL
     # sigmoid routing: sizes and pointers are checked before any CUDA call
     assert L.moe_route_sigmoid(None, None, 4, 0, 1, 1.0, None, None, None) == b.MOE_EINVAL
     assert L.moe_route_sigmoid(None, None, 4, 1025, 1, 1.0, None, None, None) == b.MOE_EINVAL
