@@ -370,6 +370,7 @@ def summarize_extra(cfg, ms, clocks, stage_ms, groups, peaks, peak_src):
     roof = roofline_entry(dom, stage_ms[dom_name], peaks, peak_src, operand_dtype(cfg, dom_name == "layer"))
     roof["kernel"] = "single-kernel MoE layer" if dom_name == "layer" else f"{dom_name} GEMM"
     roof["kernel_ms"] = stage_ms[dom_name]
+    roof["traffic"] = ncu_traffic(f"{dom_name}:{cfg.name}")
     r["roofline"] = roof
     if dom_name == "layer":
         # HBM-bound: the weight stream over the step, as a fraction of the copy peak
