@@ -182,7 +182,8 @@ typedef struct {
  *  routing       NULL or device pointers that receive the routing
  * T == 0 enqueues nothing and returns MOE_OK.
  * Errors: MOE_EINVAL (NULL/misaligned pointers, T < 0, k outside
- * [1, k_max], a dense handle), MOE_EWORKSPACE, MOE_EDEVICE, MOE_ECUDA. */
+ * [1, min(k_max, E)], a dense handle, a handle given an expert range other
+ * than [0, E) of E), MOE_EWORKSPACE, MOE_EDEVICE, MOE_ECUDA. */
 MoeStatus moe_forward(MoeHandle *h, const void *x_bf16, const float *router_logits, int T, int k, float *out_fp32,
                       int accumulate, void *workspace, size_t ws_bytes, const MoeRoutingOut *routing,
                       void *cuda_stream);
