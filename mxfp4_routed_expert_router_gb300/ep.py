@@ -19,9 +19,8 @@ experts) moves fewer bytes when T is large and is not built here.
 This module is host logic only: it computes the ranges, picks the rank's
 weights, and wraps one rank's library handle; the id mapping, the grouping and
 every step of the layer run in libmoe_gb300.so, and the sum across ranks is
-torch.distributed's all-reduce (NCCL between GPUs).  Every run in this
-repository has one GPU, so the multi-GPU scaling of this split is not measured
-here.
+torch.distributed's all-reduce (NCCL between GPUs).  The tests run the ranks
+one after another on a single device and the all-reduce over gloo on the CPU.
 """
 from __future__ import annotations
 

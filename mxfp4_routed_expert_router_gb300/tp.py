@@ -19,8 +19,8 @@ is cut; the loader's rule for dense slices is the same.
 This module is host logic only: it computes the ranges, cuts the caller's
 weight arrays, and wraps one rank's library handle; every step of the layer
 runs in libmoe_gb300.so, and the sum across ranks is torch.distributed's
-all-reduce (NCCL between GPUs).  Every run in this repository has one GPU, so
-the multi-GPU scaling of this split is not measured here.
+all-reduce (NCCL between GPUs).  The tests run the ranks one after another on
+a single device and the all-reduce over gloo on the CPU.
 """
 from __future__ import annotations
 

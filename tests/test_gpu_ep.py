@@ -8,8 +8,7 @@ every rank's routing copy must be the host mapping (its own indices, -1
 elsewhere), its partial output the oracle's partial layer, and the sum of the
 partials the oracle's whole layer (Eq. (1) of "Cascadia: Resident 975B MoE
 Inference on Eleven AI PCs" §3.3 is a sum over experts).  Between GPUs that sum
-is one all-reduce; every run here has one GPU, so that step is covered by the
-gloo test on the CPU."""
+is one all-reduce, which the gloo test on the CPU covers."""
 import numpy as np
 import pytest
 import torch

@@ -6,8 +6,7 @@ layer on that slice.  On one GPU the ranks run one after the other; their
 partial outputs must each match the oracle's partial layer, and their sum the
 oracle's full layer (the sum-over-slices identity of "Cascadia: Resident 975B
 MoE Inference on Eleven AI PCs" §3.4, Eq. 2).  Between GPUs that sum is one
-all-reduce; every run here has one GPU, so that step is covered by the gloo
-test on the CPU."""
+all-reduce, which the gloo test on the CPU covers."""
 import numpy as np
 import pytest
 import torch
