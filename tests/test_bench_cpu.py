@@ -1,6 +1,7 @@
 """CPU tests of bench.py's host logic: the algorithmic-byte model behind the
-roofline, the max-over-ranks step time of an N-rank run (world size 2 over
-gloo), the reference arm's JSON line, and the ranks that stay silent."""
+roofline, the ncu traffic captures keyed by their kernel sources, the
+max-over-ranks step time of an N-rank run (world size 2 over gloo), the
+reference arm's JSON line, and the ranks that stay silent."""
 import json
 import os
 import socket
@@ -54,6 +55,42 @@ def test_roofline_bound_and_fractions():
     assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
     assert r["frac"] == pytest.approx(gu["flops"] / 5.5e-3 / 1e12 / 1937.1)
     assert r["frac_nominal"] == pytest.approx(gu["flops"] / 5.5e-3 / 1e12 / 2250.0)
+
+
+def test_traffic_entries_match_their_sources_and_go_stale_on_change(tmp_path, monkeypatch):
+    # every committed capture is keyed by the sha256 of the kernel source it was
+    # taken on; a changed source yields no traffic rather than a stale figure
+    import hashlib
+    import shutil
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        entries = json.load(f)
+    for key, ent in entries.items():
+        with open(os.path.join(ROOT, ent["source"]), "rb") as f:
+            assert hashlib.sha256(f.read()).hexdigest() == ent["source_sha256"], key
+        assert ent["bytes_per_launch"] == ent["dram_bytes_read"] + ent["dram_bytes_write"], key
+        assert bench.ncu_traffic(key) == pytest.approx(ent["bytes_per_launch"] * ent.get("scale_to_workload", 1.0))
+    assert bench.ncu_traffic("layer:no_such_workload") is None
+    fake = tmp_path / "repo"
+    shutil.copytree(os.path.join(ROOT, "profiles"), fake / "profiles")
+    src = entries["layer:decode_T1"]["source"]
+    (fake / os.path.dirname(src)).mkdir(parents=True)
+    shutil.copy(os.path.join(ROOT, src), fake / src)
+    monkeypatch.setattr(bench, "ROOT", str(fake))
+    assert bench.ncu_traffic("layer:decode_T1") is not None
+    with open(fake / src, "a") as f:
+        f.write("\n// edited\n")
+    assert bench.ncu_traffic("layer:decode_T1") is None
+
+
+def test_extra_workload_roofline_carries_traffic():
+    peaks = {"hbm_gbs": 6714.6, "bf16_tflops": 1937.1}
+    stage = {"routing": 0.01, "grouping": 0.02, "gate_up": 4.3, "down": 2.45, "combine": 0.3, "layer": 0.0}
+    r = bench.summarize_extra(bench.workload("prefill_T8192"), 7.3, {}, stage, 257, peaks, "measured")
+    assert r["roofline"]["kernel"] == "gate_up GEMM"
+    assert r["roofline"]["traffic"] == bench.ncu_traffic("gate_up:prefill_T8192")
+    stage = {"routing": 0.0, "grouping": 0.0, "gate_up": 0.0, "down": 0.0, "combine": 0.0, "layer": 1.48}
+    r = bench.summarize_extra(bench.workload("sweep_T88"), 1.48, {}, stage, 187, peaks, "measured")
+    assert r["roofline"]["kernel"] == "single-kernel MoE layer" and r["roofline"]["traffic"] is None
 
 
 def test_job_throughput_is_weak_scaling():
